@@ -1,0 +1,255 @@
+"""MoE expert path: segments, permutation, grouped GEMMs, SwiGLU, combine.
+
+Oracle: test infrastructure only.  All GEMMs run in fp64 on dequantised
+codes (x_hat = q * s_b * s_g is exact in fp64), so the only rounding in a
+GEMM result is the final rounding to the output dtype.
+
+Sources: "miniTE technical report" section 5.2 (quantised outputs in one
+contiguous buffer, expert boundaries given by offsets, zero-token experts and
+padding handled in the same grouped path), section 5.3 (row amax accumulated
+by the producer: the permute for FC1, the weighted SwiGLU for FC2), section
+5.4 (FC1 epilogue: ACC x alpha_a[m] (x alpha_b), C = gate | up,
+D = act(gate, up) x prob, amax of D); "Towards Blackwell-native 8-bit and
+4-bit RL", section "Recipe 1 / Training" (dgrad uses the column-wise weight
+copy, wgrad the column-wise activation and gradient copies).
+
+Readings the pages leave open (each one is fixed here):
+* Segment order: rows of expert e are the (token, slot) pairs routed to e in
+  ascending flat index t*k + j; each segment is padded to a multiple of 128
+  rows; padding rows are all zero and carry probability 0.
+* SwiGLU: D = silu(g) * u * p with g = FC1 output columns [0, I) and
+  u = columns [I, 2I); silu(g) = g / (1 + exp(-g)).
+* D is rounded to bf16 before its row amax and its re-quantisation.
+* The FC2 output Y_perm is rounded to bf16; the combine sums each token's k
+  rows in slot order and rounds once to bf16.
+* Backward: probabilities and routing are constants (no router gradient);
+  dY_perm[row] = dY[token of row].
+"""
+from __future__ import annotations
+
+import numpy as np
+
+from . import formats as F
+from . import quant as Q
+
+ROW_PAD = 128
+
+
+def silu(g):
+    return g / (1.0 + np.exp(-g))
+
+
+def dsilu(g):
+    s = 1.0 / (1.0 + np.exp(-g))
+    return s * (1.0 + g * (1.0 - s))
+
+
+# ------------------------------------------------------------ segments
+
+def build_segments(topk_ids: np.ndarray, topk_prob: np.ndarray, E: int, pad=ROW_PAD):
+    """Counting sort of the T*k routed (token, slot) pairs by expert.
+
+    Returns seg_offsets int32 [E+1], perm int32 [R_pad] (flat index t*k + j,
+    -1 for padding), inv_perm int32 [T*k] (flat index -> row), row_prob
+    float32 [R_pad] (0 for padding).
+    """
+    ids = np.asarray(topk_ids, dtype=np.int64).reshape(-1)
+    prob = np.asarray(topk_prob, dtype=np.float32).reshape(-1)
+    counts = np.bincount(ids, minlength=E)
+    padded = (counts + pad - 1) // pad * pad
+    seg = np.zeros(E + 1, dtype=np.int64)
+    seg[1:] = np.cumsum(padded)
+    R_pad = int(seg[-1])
+    perm = np.full(R_pad, -1, dtype=np.int64)
+    inv = np.empty(ids.size, dtype=np.int64)
+    fill = seg[:-1].copy()
+    for f in range(ids.size):               # ascending flat index
+        e = ids[f]
+        inv[f] = fill[e]
+        perm[fill[e]] = f
+        fill[e] += 1
+    row_prob = np.zeros(R_pad, dtype=np.float32)
+    real = perm >= 0
+    row_prob[real] = prob[perm[real]]
+    return (seg.astype(np.int32), perm.astype(np.int32), inv.astype(np.int32),
+            row_prob)
+
+
+def expert_of_rows(seg_offsets: np.ndarray) -> np.ndarray:
+    seg = np.asarray(seg_offsets, dtype=np.int64)
+    e = np.repeat(np.arange(len(seg) - 1), np.diff(seg))
+    return e
+
+
+# ------------------------------------------------------------ grouped GEMM
+
+def grouped_gemm(a: np.ndarray, b: np.ndarray, seg_offsets: np.ndarray) -> np.ndarray:
+    """C[r, n] = sum_k a[r, k] * b[e(r), n, k] for the rows of each segment.
+
+    a [R, K] fp64, b [E, N, K] fp64 -> C [R, N] fp64.  One library matmul per
+    expert (the definition of a grouped GEMM, nothing more).
+    """
+    seg = np.asarray(seg_offsets, dtype=np.int64)
+    R = a.shape[0]
+    C = np.zeros((R, b.shape[1]), dtype=np.float64)
+    for e in range(len(seg) - 1):
+        r0, r1 = seg[e], seg[e + 1]
+        if r1 > r0:
+            C[r0:r1] = a[r0:r1] @ b[e].T
+    return C
+
+
+def grouped_wgrad(at: np.ndarray, bt: np.ndarray, seg_offsets: np.ndarray) -> np.ndarray:
+    """dW[e] = at[:, seg e] @ bt[:, seg e].T : contraction over each expert's rows.
+
+    at [N, R] fp64, bt [K, R] fp64 -> [E, N, K] fp64 (zero for empty experts).
+    """
+    seg = np.asarray(seg_offsets, dtype=np.int64)
+    E = len(seg) - 1
+    out = np.zeros((E, at.shape[0], bt.shape[0]), dtype=np.float64)
+    for e in range(E):
+        r0, r1 = seg[e], seg[e + 1]
+        if r1 > r0:
+            out[e] = at[:, r0:r1] @ bt[:, r0:r1].T
+    return out
+
+
+def gather_rows(x: np.ndarray, perm: np.ndarray, k: int) -> np.ndarray:
+    """X_perm[row] = x[perm[row] // k]; zero rows for padding (perm = -1)."""
+    perm = np.asarray(perm, dtype=np.int64)
+    out = np.zeros((perm.size,) + x.shape[1:], dtype=x.dtype)
+    real = perm >= 0
+    out[real] = x[perm[real] // k]
+    return out
+
+
+def combine(y_perm: np.ndarray, inv_perm: np.ndarray, T: int, k: int) -> np.ndarray:
+    """out[t] = sum over slots j (in order) of y_perm[inv_perm[t*k + j]]."""
+    inv = np.asarray(inv_perm, dtype=np.int64).reshape(T, k)
+    out = np.zeros((T,) + y_perm.shape[1:], dtype=np.float64)
+    for j in range(k):
+        out += y_perm[inv[:, j]]
+    return out
+
+
+# ------------------------------------------------------------ NVFP4 forward
+
+def nvfp4_weights(w1: np.ndarray, w2: np.ndarray):
+    """Quantise W1 [E, 2I, H] (gate|up jointly) and W2 [E, H, I] per expert."""
+    E, I2, H = w1.shape
+    I = I2 // 2
+    w1q = Q.nvfp4_quantize_joint([w1[:, :I], w1[:, I:]], E)
+    w2q = Q.nvfp4_quantize_joint([w2], E)
+    return w1q, w2q
+
+
+def dequant_weights_nvfp4(wq):
+    packed, sb, sg = wq
+    E, R, _ = packed.shape
+    return np.stack([Q.nvfp4_dequantize(packed[e], sb[e], sg[e]) for e in range(E)])
+
+
+def fc1_epilogue(acc: np.ndarray, row_prob: np.ndarray, I: int) -> np.ndarray:
+    """D = bf16( silu(g) * u * p ); acc already carries alpha_a * alpha_b."""
+    g, u = acc[:, :I], acc[:, I:2 * I]
+    d = silu(g) * u * np.asarray(row_prob, dtype=np.float64)[:, None]
+    return F.bf16_round(d)
+
+
+def nvfp4_moe_forward(x: np.ndarray, topk_ids, topk_prob, w1, w2, E: int):
+    """The full NVFP4 expert-layer forward.
+
+    x [T, H] bf16 values; w1 [E, 2I, H]; w2 [E, H, I].  Returns a dict with
+    every intermediate the CUDA path materialises.
+    """
+    T, H = x.shape
+    k = np.asarray(topk_ids).shape[1]
+    I = w1.shape[1] // 2
+    # per-token activation quantisation of X (once per token)
+    qx, sx, tsx = Q.nvfp4_quantize_per_token(x)
+    seg, perm, inv, row_prob = build_segments(topk_ids, topk_prob, E)
+    xq_deq = Q.nvfp4_dequantize(qx, sx, tsx)                 # [T, H]
+    a1 = gather_rows(xq_deq, perm, k)                        # [R_pad, H]
+    (w1p, w1s, w1g), (w2p, w2s, w2g) = nvfp4_weights(w1, w2)
+    b1 = dequant_weights_nvfp4((w1p, w1s, w1g))
+    acc1 = grouped_gemm(a1, b1, seg)                         # fp64
+    d = fc1_epilogue(acc1, row_prob, I)
+    amax_d = np.max(np.abs(d), axis=1).astype(np.float32)
+    qd, sd, tsd = Q.nvfp4_quantize_per_token(d, amax_d)
+    b2 = dequant_weights_nvfp4((w2p, w2s, w2g))
+    y = grouped_gemm(Q.nvfp4_dequantize(qd, sd, tsd), b2, seg)
+    y_bf16 = F.bf16_round(y)
+    out = F.bf16_round(combine(y_bf16, inv, T, k))
+    return dict(qx=qx, sx=sx, tsx=tsx, seg=seg, perm=perm, inv=inv,
+                row_prob=row_prob, w1=(w1p, w1s, w1g), w2=(w2p, w2s, w2g),
+                acc1=acc1, d=d, amax_d=amax_d, qd=qd, sd=sd, tsd=tsd,
+                y=y_bf16, out=out)
+
+
+def nvfp4_gemm_single(x: np.ndarray, w_gate: np.ndarray, w_up: np.ndarray):
+    """One expert, no SwiGLU: per-token X quantisation, joint gate/up weight
+    quantisation, C = deq(X) deq(W)^T in fp64 ([M, 2N], fp32 output)."""
+    qx, sx, tsx = Q.nvfp4_quantize_per_token(x)
+    wp, ws, wg = Q.nvfp4_quantize_joint([w_gate[None], w_up[None]], 1)
+    a = Q.nvfp4_dequantize(qx, sx, tsx)
+    b = Q.nvfp4_dequantize(wp[0], ws[0], wg[0])
+    c = a @ b.T
+    return dict(qx=qx, sx=sx, tsx=tsx, wq=(wp, ws, wg), c=c)
+
+
+# ------------------------------------------------------------ MXFP8 fwd + bwd
+
+def mx_rows(x):
+    """Row-wise MXFP8 round trip: dequantised fp64 values [R, C]."""
+    c, s = Q.mxfp8_quantize_rowwise(x)
+    return Q.mxfp8_dequantize(c, s)
+
+
+def mx_cols_t(x):
+    """Column-wise MXFP8 copy, dequantised, in its stored transposed form [C, R]."""
+    c, s = Q.mxfp8_quantize_colwise(x)
+    return Q.mxfp8_dequantize(c, s)
+
+
+def swiglu_backward(dd: np.ndarray, c1: np.ndarray, row_prob: np.ndarray, I: int):
+    """dH = [dg | du] for D = silu(g) * u * p (p constant)."""
+    g, u = c1[:, :I], c1[:, I:2 * I]
+    p = np.asarray(row_prob, dtype=np.float64)[:, None]
+    dg = dd * p * u * dsilu(g)
+    du = dd * p * silu(g)
+    return np.concatenate([dg, du], axis=1)
+
+
+def mxfp8_moe_fwd_bwd(x, topk_ids, topk_prob, w1, w2, dy, E: int):
+    """End-to-end MXFP8 expert layer, forward and backward.
+
+    Every GEMM operand is quantised from bf16: fprop uses row-wise copies,
+    dgrad the row-wise gradient and the column-wise weight, wgrad the
+    column-wise gradient and activation copies.
+    """
+    T, H = x.shape
+    k = np.asarray(topk_ids).shape[1]
+    I = w1.shape[1] // 2
+    seg, perm, inv, row_prob = build_segments(topk_ids, topk_prob, E)
+    xp = gather_rows(np.asarray(x, dtype=np.float64), perm, k)     # bf16 values
+    # forward FC1
+    b1 = np.stack([mx_rows(w1[e]) for e in range(E)])              # [E, 2I, H]
+    acc1 = grouped_gemm(mx_rows(xp), b1, seg)
+    c1 = F.bf16_round(acc1)                                        # saved gate|up
+    d = fc1_epilogue(acc1, row_prob, I)
+    # forward FC2
+    b2 = np.stack([mx_rows(w2[e]) for e in range(E)])              # [E, H, I]
+    y = F.bf16_round(grouped_gemm(mx_rows(d), b2, seg))
+    out = F.bf16_round(combine(y, inv, T, k))
+    # backward
+    dyp = gather_rows(np.asarray(dy, dtype=np.float64), perm, k)   # [R_pad, H]
+    w2c = np.stack([mx_cols_t(w2[e]) for e in range(E)])           # [E, I, H]
+    dd = grouped_gemm(mx_rows(dyp), w2c, seg)                      # [R_pad, I] fp64
+    dw2 = grouped_wgrad(mx_cols_t(dyp), mx_cols_t(d), seg)         # [E, H, I]
+    dh = F.bf16_round(swiglu_backward(dd, c1, row_prob, I))        # [R_pad, 2I]
+    w1c = np.stack([mx_cols_t(w1[e]) for e in range(E)])           # [E, H, 2I]
+    dxp = F.bf16_round(grouped_gemm(mx_rows(dh), w1c, seg))        # [R_pad, H]
+    dx = F.bf16_round(combine(dxp, inv, T, k))
+    dw1 = grouped_wgrad(mx_cols_t(dh), mx_cols_t(xp), seg)         # [E, 2I, H]
+    return dict(seg=seg, perm=perm, inv=inv, row_prob=row_prob, c1=c1, d=d,
+                y=y, out=out, dd=dd, dh=dh, dxp=dxp, dx=dx, dw1=dw1, dw2=dw2)
