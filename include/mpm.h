@@ -1,0 +1,317 @@
+/*
+ * mpm.h -- C ABI of libmpm: microscaled-precision (MXFP8 / NVFP4) quantisers
+ * and block-scaled MoE grouped GEMMs for sm_103a (GB300).
+ *
+ * Every call is asynchronous on the caller's CUDA stream, allocates no device
+ * memory, and validates its arguments on the host before launching anything:
+ * a call that returns a status other than MPM_OK has launched nothing.  The
+ * caller owns every buffer.  Pointers named *_dev are device pointers; all
+ * other pointers are host pointers.  Identical inputs always give identical
+ * output bytes (no floating-point atomics, fixed reduction orders).
+ *
+ * Formats (source: "Towards Blackwell-native 8-bit and 4-bit RL", section
+ * "Format background"; "miniTE technical report", section 2.2):
+ *   MXFP8  32 consecutive E4M3 values share one E8M0 power-of-two scale,
+ *          rounded up so the block max never clips.
+ *   NVFP4  E2M1 codes, one E4M3 scale per 16 values (round to nearest), and an
+ *          FP32 outer scale; decode x_hat = q * s_b * s_g.
+ *
+ * Layouts shared by all calls:
+ *   - bf16 inputs are row-major with a leading dimension in elements.
+ *   - FP4 codes are packed two per byte, element 2j in the low nibble.
+ *   - Scale matrices [rows, cols] are stored in 128x4 tiles: rows padded to a
+ *     multiple of 128 and cols to a multiple of 4 with zero bytes; tile
+ *     (rt, ct) starts at byte (rt * pad4(cols) / 4 + ct) * 512 and holds entry
+ *     (r, c) at (r % 32) * 16 + (r / 32 % 4) * 4 + c % 4.  Size:
+ *     mpm_scale_bytes(rows, cols).  This is the operand layout the sm_100
+ *     family block-scaled tensor-core MMA reads its scale factors in.
+ *
+ * Errors: host-side validation failures return MPM_ERR_NULL / _SHAPE /
+ * _ALIGN / _UNSUPPORTED; a failed launch returns MPM_ERR_CUDA.  Problems only
+ * visible on the device (an expert offset table that is not monotone or that
+ * exceeds the row capacity, a pipeline wait that ran out of time) set a
+ * per-device status word and make the kernel skip the affected work (no trap,
+ * no hang); read it with mpm_get_device_status().
+ */
+#ifndef MPM_H
+#define MPM_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MPM_OK = 0,
+  MPM_ERR_NULL = 1,          /* a required pointer is NULL                     */
+  MPM_ERR_SHAPE = 2,         /* a size is zero/negative/inconsistent           */
+  MPM_ERR_ALIGN = 3,         /* a pointer or leading dimension is misaligned   */
+  MPM_ERR_UNSUPPORTED = 4,   /* valid request this build does not implement    */
+  MPM_ERR_CUDA = 5,          /* a CUDA runtime/driver call failed              */
+  MPM_ERR_DEVICE_TIMEOUT = 6,/* (device status) a bounded pipeline wait expired */
+  MPM_ERR_DEVICE_BOUNDS = 7  /* (device status) bad offsets / row indices       */
+} mpm_status;
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* mpm_status_string(int status);
+
+/* Library version, e.g. 100 for 1.0.0. */
+int mpm_version(void);
+
+/* Bytes of a 128x4-tiled scale matrix: pad128(rows) * pad4(cols). */
+size_t mpm_scale_bytes(int64_t rows, int64_t cols);
+
+/* ------------------------------------------------------------------------ */
+/* Quantisers                                                               */
+/* ------------------------------------------------------------------------ */
+
+#define MPM_ROWWISE 1u
+#define MPM_COLWISE 2u
+
+/*
+ * MXFP8 quantisation of x_dev (bf16 [M, K], leading dimension ldx elements)
+ * into a row-wise 1x32 copy and/or a column-wise 32x1 copy, each quantised
+ * independently from the bf16 input in one pass over it.
+ * Source: "Towards Blackwell-native 8-bit and 4-bit RL", sections "Format
+ * background / MXFP8" (E8M0 scale rounded up) and "Recipe 1 / Training"
+ * (row-wise and column-wise copies materialised by one quantisation).
+ *
+ * Per block of 32 values v: a = max|v|; e = smallest integer with
+ * a <= 448 * 2^e, clamped to [-127, 127] (a = 0 gives -127); scale byte
+ * e + 127; code = E4M3(v * 2^-e), round to nearest even, saturating.
+ *
+ * flags: MPM_ROWWISE and/or MPM_COLWISE.
+ * ROWWISE: row_q_dev  u8 [M, K] (leading dim K),
+ *          row_s_dev  scales [M, K/32] in 128x4 tiles (mpm_scale_bytes(M, K/32)).
+ * COLWISE: col_q_dev  u8 [K, ldc] -- the copy is stored TRANSPOSED, so each
+ *          column block is 32 contiguous bytes; ldc >= M, columns >= M of
+ *          each row are not written,
+ *          col_s_dev  scales [K, ceil(M/32)] in 128x4 tiles.
+ * The last column block of a partial 32-row group behaves as zero padded.
+ * m_valid_dev (nullable): device int32; if given, only rows < min(M, *m_valid)
+ * are quantised and rows at or beyond it read as zero (used for buffers whose
+ * used row count is known only on the device).
+ * Requirements: M >= 1, K >= 32, K % 32 == 0, ldx >= K, ldx % 8 == 0,
+ * x_dev 16-byte aligned, ldc % 16 == 0, all output pointers 16-byte aligned.
+ */
+mpm_status mpm_mxfp8_quantize(const void* x_dev, int64_t M, int64_t K, int64_t ldx,
+                              unsigned flags,
+                              uint8_t* row_q_dev, uint8_t* row_s_dev,
+                              uint8_t* col_q_dev, int64_t ldc, uint8_t* col_s_dev,
+                              const int32_t* m_valid_dev, cudaStream_t stream);
+
+/*
+ * Per-token NVFP4 quantisation: one call returns the packed FP4 codes, the
+ * E4M3 block scales and the per-token FP32 outer scales.
+ * Source: "Towards Blackwell-native 8-bit and 4-bit RL", section "Per-token
+ * activation scaling" (one online FP32 scale per token, returned by the same
+ * call that emits the codes and block scales); "miniTE technical report",
+ * section 5.6 (s_g = amax / 2688) and section 5.3 (reuse of an amax computed
+ * by the producer of the activation).
+ *
+ * Per row, every step IEEE binary32 round-to-nearest (no FMA contraction):
+ *   a   = max_j |x_j|  (or amax_in_dev[row] when given)
+ *   s_g = a / 2688, raised to 2^-116 if it is below that; a = 0 -> s_g = 0
+ *   per 16-block: s_b = E4M3_rn_satfinite(bmax / (6 * s_g))
+ *   s_b = 0 -> codes 0; else r = 1 / (s_b * s_g), q_j = E2M1_rn_satfinite(x_j * r)
+ *
+ * x_dev: bf16 [M, K], leading dimension ldx elements.
+ * amax_in_dev (nullable): fp32 [M] row amax computed by the producer.
+ * q_dev: u8 [M, K/2] (leading dim K/2).  s_dev: scales [M, K/16] in 128x4
+ * tiles.  token_scale_dev: fp32 [M] (the s_g above).
+ * m_valid_dev (nullable): as for mpm_mxfp8_quantize; rows at or beyond the
+ * device row count are left untouched (their scale tiles are not written).
+ * Requirements: M >= 1, K % 64 == 0, 64 <= K <= 16384, ldx % 8 == 0,
+ * all pointers 16-byte aligned (token_scale_dev and amax_in_dev 4-byte).
+ */
+mpm_status mpm_nvfp4_quantize_per_token(const void* x_dev, int64_t M, int64_t K,
+                                        int64_t ldx, const float* amax_in_dev,
+                                        uint8_t* q_dev, uint8_t* s_dev,
+                                        float* token_scale_dev,
+                                        const int32_t* m_valid_dev,
+                                        cudaStream_t stream);
+
+/*
+ * NVFP4 weight quantisation with one FP32 outer scale per expert shared by
+ * all given parts (gate and up quantised jointly so that the fused gate|up
+ * GEMM sees one weight scale).
+ * Source: "Towards Blackwell-native 8-bit and 4-bit RL", section "Per-token
+ * activation scaling" (gate/up paired quantisation with a shared FP32 scale);
+ * block and element rules as for mpm_nvfp4_quantize_per_token.
+ *
+ * parts_dev: host array of nparts device pointers; part p is bf16
+ * [E, part_rows[p], K] contiguous.  The quantised expert e holds the parts'
+ * rows concatenated in order: R = sum(part_rows) rows.
+ * q_dev: u8 [E, R, K/2].  s_dev: E consecutive scale matrices [R, K/16] in
+ * 128x4 tiles, expert e at byte e * mpm_scale_bytes(R, K/16).
+ * tensor_scale_dev: fp32 [E] (s_g of each expert).
+ * ws_dev: workspace of at least mpm_nvfp4_weight_workspace_bytes(E) bytes.
+ * Requirements: nparts in 1..4, E >= 1, K % 64 == 0, 64 <= K <= 16384,
+ * each part_rows[p] >= 1, R % 128 == 0.
+ */
+size_t mpm_nvfp4_weight_workspace_bytes(int64_t E);
+mpm_status mpm_nvfp4_quantize_weight(const void* const* parts_dev, const int64_t* part_rows,
+                                     int nparts, int64_t K, int64_t E,
+                                     uint8_t* q_dev, uint8_t* s_dev, float* tensor_scale_dev,
+                                     void* ws_dev, size_t ws_bytes, cudaStream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* Expert segments, permutation, combine                                    */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * Row capacity of the permuted buffers for T tokens, top-k and E experts with
+ * segments padded to 128 rows: pad128(T*k) + 128*E.
+ */
+int64_t mpm_moe_row_capacity(int64_t T, int k, int64_t E);
+size_t mpm_moe_segments_workspace_bytes(int64_t T, int k, int64_t E);
+
+/*
+ * Counting sort of the T*k routed (token, slot) pairs by expert into one
+ * contiguous buffer, each expert's segment padded to 128 rows.
+ * Source: "miniTE technical report", section 5.2 (contiguous buffer with
+ * expert boundaries given by offsets kept on the device; zero-token experts
+ * and padding handled in the same path).
+ *
+ * topk_ids_dev: int32 [T, k] expert ids in [0, E); topk_prob_dev: fp32 [T, k].
+ * Outputs (device): seg_offsets int32 [E+1] (seg_offsets[0] = 0, segment e is
+ * rows [seg_offsets[e], seg_offsets[e+1]), a multiple of 128 long); perm
+ * int32 [capacity] (row -> flat index t*k + j, -1 for padding rows and rows
+ * beyond seg_offsets[E]); inv_perm int32 [T*k] (flat index -> row); row_prob
+ * fp32 [capacity] (0 for padding).  Rows of one expert are in ascending flat
+ * index order (stable).  An id outside [0, E) sets MPM_ERR_DEVICE_BOUNDS and
+ * the pair is dropped.
+ */
+mpm_status mpm_moe_build_segments(const int32_t* topk_ids_dev, const float* topk_prob_dev,
+                                  int64_t T, int k, int64_t E,
+                                  int32_t* seg_offsets_dev, int32_t* perm_dev,
+                                  int32_t* inv_perm_dev, float* row_prob_dev,
+                                  void* ws_dev, size_t ws_bytes, cudaStream_t stream);
+
+/*
+ * Gather rows into the permuted layout: dst[row] = src[perm[row] / k] for
+ * rows < seg_offsets[E] with perm[row] >= 0, zero for padding rows.
+ * MPM_GATHER_BF16:  src bf16 [T, K] (ld K) -> dst bf16 [capacity, K].
+ * MPM_GATHER_NVFP4: src codes u8 [T, K/2], scales (128x4 tiles of [T, K/16])
+ *   and token scales fp32 [T] -> the same three for [capacity] rows
+ *   (src_s / dst_s / src_ts / dst_ts used only here).
+ * Source: "miniTE technical report", section 5.3 (dispatch/permute before the
+ * FC1 quantised GEMM).  Requirements: K % 64 == 0.
+ */
+#define MPM_GATHER_BF16 0
+#define MPM_GATHER_NVFP4 1
+mpm_status mpm_moe_gather(int what, const void* src_dev, const uint8_t* src_s_dev,
+                          const float* src_ts_dev, int64_t T, int64_t K, int k,
+                          const int32_t* perm_dev, const int32_t* seg_offsets_dev,
+                          int64_t E, int64_t capacity,
+                          void* dst_dev, uint8_t* dst_s_dev, float* dst_ts_dev,
+                          cudaStream_t stream);
+
+/*
+ * out[t] = sum over j = 0..k-1 (in that order, fp32) of y_perm[inv_perm[t*k+j]],
+ * rounded once to bf16.  y_perm bf16 [capacity, H]; out bf16 [T, H].
+ * Source: "miniTE technical report", section 5.3 (expert outputs, weighted by
+ * the router, summed back per token); the router weight is applied earlier in
+ * the FC1 epilogue.  Requirements: H % 8 == 0.
+ */
+mpm_status mpm_moe_combine(const void* y_perm_dev, const int32_t* inv_perm_dev,
+                           int64_t T, int k, int64_t H, void* out_dev,
+                           cudaStream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* Block-scaled grouped GEMM (tcgen05)                                      */
+/* ------------------------------------------------------------------------ */
+
+#define MPM_KIND_NVFP4 0   /* E2M1 x E2M1, E4M3 scales per 16, fp32 accumulate */
+#define MPM_KIND_MXFP8 1   /* E4M3 x E4M3, E8M0 scales per 32, fp32 accumulate */
+
+#define MPM_GROUP_M 0      /* rows of A split into expert segments (fprop, dgrad) */
+#define MPM_GROUP_K 1      /* reduction split into expert segments (wgrad)        */
+
+#define MPM_EPI_F32 0            /* out fp32 [rows, N]                             */
+#define MPM_EPI_BF16 1           /* out bf16 [rows, N]                             */
+#define MPM_EPI_SWIGLU 2         /* out2 = D bf16 [rows, N/2], amax atomically max'd */
+#define MPM_EPI_SWIGLU_SAVE 3    /* SWIGLU and out = C bf16 [rows, N] (gate|up)     */
+#define MPM_EPI_DSWIGLU 4        /* out = dH bf16 [rows, 2N] from aux = C bf16       */
+
+/*
+ * Descriptor of one grouped GEMM  C_e = A_e * B_e^T  (both operands K-major,
+ * i.e. row-major with the reduction dimension contiguous).
+ *
+ * GROUP_M: rows [seg[e], seg[e+1]) of A (a [capacity, K] matrix) multiply
+ *   expert e's B, rows e*b_rows_per_expert .. +N of the B matrix, reduction
+ *   columns e*b_k_per_expert .. +K.  Output rows = A rows.  seg_dev may be
+ *   NULL for one dense group of a_rows rows.
+ * GROUP_K: for expert e, A is the [M_out, .] matrix and B the [N, .] matrix
+ *   restricted to reduction columns [seg[e], seg[e+1]); output expert e is
+ *   [M_out, N] at out + e * M_out * ldo (fp32 only).  Empty experts give 0.
+ *
+ * a_dev / b_dev: codes (NVFP4: packed, K/2 bytes per row; MXFP8: K bytes),
+ * lda_bytes / ldb_bytes their row pitches (multiples of 16).
+ * sfa_dev / sfb_dev: their scale matrices in 128x4 tiles, sfa_cols / sfb_cols
+ * the UNPADDED scale column counts of the whole A / B matrices
+ * (row pitch/16 or /32 elements); B's per-expert rows are addressed
+ * directly inside one tiled matrix (b_rows_per_expert % 128 == 0).
+ * alpha_a_dev (NVFP4, GROUP_M): fp32 per-row outer scale of A; alpha_b_dev:
+ * fp32 [E] outer scale of each expert's B (either may be NULL = 1).
+ * Epilogue: acc * alpha_a[row] * alpha_b[e], then
+ *   F32/BF16: store;  SWIGLU: D[r, j] = silu(g) * u * row_prob[r] with
+ *   g = column j, u = column N/2 + j, rounded to bf16, and amax_dev[r] =
+ *   max(amax_dev[r], max_j |D[r, j]|) (fp32 bits, caller zeroes it first);
+ *   DSWIGLU: dD = acc, with (g, u) read from aux (bf16 C, [rows, 2N]):
+ *   dH[r, j] = dD*p*u*silu'(g), dH[r, N+j] = dD*p*silu(g), bf16.
+ * Source: "miniTE technical report", section 5.2 (grouped GEMM over a
+ * contiguous buffer with device offsets), section 5.4 (FC1 epilogue:
+ * ACC x alpha_a[m] (x alpha_b), C = gate|up, D = act(gate, up) x prob, amax
+ * of D); "Towards Blackwell-native 8-bit and 4-bit RL", section "Recipe 1 /
+ * Training" (dgrad with the column-wise weight copy, wgrad with column-wise
+ * activation and gradient copies).
+ * Requirements: K % 256 == 0 (NVFP4) or % 128 == 0 (MXFP8) in GROUP_M;
+ * N % 256 == 0 (SwiGLU: N/2 % 128 == 0); GROUP_K: M_out % 128 == 0,
+ * segments multiples of 128 rows.
+ */
+typedef struct {
+  int kind;                    /* MPM_KIND_*                                   */
+  int group;                   /* MPM_GROUP_*                                  */
+  int epilogue;                /* MPM_EPI_*                                    */
+  int64_t E;                   /* experts (groups)                             */
+  int64_t a_rows;              /* GROUP_M: row capacity of A (grid bound);
+                                  GROUP_K: M_out                               */
+  int64_t N;                   /* output columns per expert                    */
+  int64_t K;                   /* reduction length (GROUP_M); GROUP_K: unused  */
+  const int32_t* seg_dev;      /* [E+1] device offsets (rows of A, or the
+                                  reduction for GROUP_K)                        */
+  const uint8_t* a_dev; int64_t lda_bytes; int64_t a_total_rows;
+  const uint8_t* b_dev; int64_t ldb_bytes; int64_t b_total_rows;
+  int64_t b_rows_per_expert;   /* row offset of expert e's B is e * this       */
+  int64_t b_k_per_expert;      /* reduction-column offset of expert e's B      */
+  const uint8_t* sfa_dev; int64_t sfa_cols;
+  const uint8_t* sfb_dev; int64_t sfb_cols;
+  const float* alpha_a_dev;
+  const float* alpha_b_dev;
+  const float* row_prob_dev;   /* SWIGLU / DSWIGLU                             */
+  void* out_dev; int64_t ldo;  /* elements                                     */
+  void* out2_dev; int64_t ldo2;/* SWIGLU(_SAVE): D                             */
+  const void* aux_dev; int64_t ld_aux; /* DSWIGLU: C (gate|up)                 */
+  float* amax_dev;             /* SWIGLU: fp32 [rows]                          */
+} mpm_grouped_gemm_desc;
+
+mpm_status mpm_moe_grouped_gemm(const mpm_grouped_gemm_desc* desc, cudaStream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* Device status                                                            */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * Copies the current device's status word to *host_out (0 = MPM_OK, else an
+ * mpm_status from a kernel) and resets it to 0.  Synchronises the stream.
+ */
+mpm_status mpm_get_device_status(int32_t* host_out, cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MPM_H */

@@ -1,0 +1,301 @@
+// C ABI of libmpm: host-side validation and launch of the sm_103a kernels.
+// Nothing here allocates device memory; every entry point validates its
+// arguments before launching anything and returns an mpm_status.
+#include <cuda.h>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "quant.cuh"
+#include "moe.cuh"
+#include "gemm.cuh"
+
+namespace {
+
+__device__ int g_status_word;
+
+constexpr int kMaxDevices = 64;
+
+int* status_ptr() {
+  static int* ptrs[kMaxDevices] = {nullptr};
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!ptrs[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return nullptr;
+    ptrs[dev] = static_cast<int*>(p);
+  }
+  return ptrs[dev];
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+mpm_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MPM_OK : MPM_ERR_CUDA; }
+
+long long pad_to(long long v, long long m) { return (v + m - 1) / m * m; }
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// 2-D uint8 tensor map over [rows, pitch bytes] with a 128 x 128 box and the
+// 128-byte swizzle (the K-major operand layout of the MMA).
+bool make_tmap(CUtensorMap* m, const void* base, long long pitch, long long rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)pitch, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)pitch};
+  cuuint32_t box[2] = {128, 128};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box,
+                  estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* mpm_status_string(int s) {
+  switch (s) {
+    case MPM_OK: return "MPM_OK";
+    case MPM_ERR_NULL: return "MPM_ERR_NULL";
+    case MPM_ERR_SHAPE: return "MPM_ERR_SHAPE";
+    case MPM_ERR_ALIGN: return "MPM_ERR_ALIGN";
+    case MPM_ERR_UNSUPPORTED: return "MPM_ERR_UNSUPPORTED";
+    case MPM_ERR_CUDA: return "MPM_ERR_CUDA";
+    case MPM_ERR_DEVICE_TIMEOUT: return "MPM_ERR_DEVICE_TIMEOUT";
+    case MPM_ERR_DEVICE_BOUNDS: return "MPM_ERR_DEVICE_BOUNDS";
+    default: return "MPM_ERR_UNKNOWN";
+  }
+}
+
+int mpm_version(void) { return 100; }
+
+size_t mpm_scale_bytes(int64_t rows, int64_t cols) {
+  if (rows <= 0 || cols <= 0) return 0;
+  return (size_t)(pad_to(rows, 128) * pad_to(cols, 4));
+}
+
+mpm_status mpm_mxfp8_quantize(const void* x, int64_t M, int64_t K, int64_t ldx, unsigned flags,
+                              uint8_t* row_q, uint8_t* row_s, uint8_t* col_q, int64_t ldc,
+                              uint8_t* col_s, const int32_t* m_valid, cudaStream_t stream) {
+  if (!x) return MPM_ERR_NULL;
+  if ((flags & (MPM_ROWWISE | MPM_COLWISE)) == 0 || (flags & ~3u)) return MPM_ERR_SHAPE;
+  if (M < 1 || K < 32 || K % 32 != 0 || ldx < K) return MPM_ERR_SHAPE;
+  if (M > (1ll << 31) - 256 || K > (1ll << 31) - 256) return MPM_ERR_SHAPE;
+  if (!aligned(x, 16) || ldx % 8 != 0) return MPM_ERR_ALIGN;
+  if (flags & MPM_ROWWISE) {
+    if (!row_q || !row_s) return MPM_ERR_NULL;
+    if (!aligned(row_q, 16)) return MPM_ERR_ALIGN;
+  }
+  if (flags & MPM_COLWISE) {
+    if (!col_q || !col_s) return MPM_ERR_NULL;
+    if (ldc < M) return MPM_ERR_SHAPE;
+    if (!aligned(col_q, 16) || ldc % 16 != 0) return MPM_ERR_ALIGN;
+  }
+  return cuda_status(mpm::launch_mxfp8(x, M, K, ldx, flags, row_q, row_s, col_q, ldc, col_s,
+                                       m_valid, stream));
+}
+
+mpm_status mpm_nvfp4_quantize_per_token(const void* x, int64_t M, int64_t K, int64_t ldx,
+                                        const float* amax_in, uint8_t* q, uint8_t* s,
+                                        float* ts, const int32_t* m_valid,
+                                        cudaStream_t stream) {
+  if (!x || !q || !s || !ts) return MPM_ERR_NULL;
+  if (M < 1 || K < 64 || K % 64 != 0 || K > 8192 || ldx < K) return MPM_ERR_SHAPE;
+  if (M > (1ll << 31) - 256) return MPM_ERR_SHAPE;
+  if (!aligned(x, 16) || ldx % 8 != 0 || !aligned(q, 16) || !aligned(ts, 4)) return MPM_ERR_ALIGN;
+  if (amax_in && !aligned(amax_in, 4)) return MPM_ERR_ALIGN;
+  return cuda_status(mpm::launch_nvfp4_per_token(x, M, (int)K, ldx, amax_in, q, s, ts, m_valid,
+                                                 stream));
+}
+
+size_t mpm_nvfp4_weight_workspace_bytes(int64_t E) {
+  return E > 0 ? (size_t)pad_to(E * 4, 256) : 0;
+}
+
+mpm_status mpm_nvfp4_quantize_weight(const void* const* parts, const int64_t* part_rows,
+                                     int nparts, int64_t K, int64_t E, uint8_t* q, uint8_t* s,
+                                     float* ts, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  if (!parts || !part_rows || !q || !s || !ts || !ws) return MPM_ERR_NULL;
+  if (nparts < 1 || nparts > 4 || E < 1 || K < 64 || K % 64 != 0 || K > 8192) return MPM_ERR_SHAPE;
+  long long R = 0;
+  long long rows[4];
+  for (int i = 0; i < nparts; ++i) {
+    if (!parts[i]) return MPM_ERR_NULL;
+    if (part_rows[i] < 1) return MPM_ERR_SHAPE;
+    if (!aligned(parts[i], 16)) return MPM_ERR_ALIGN;
+    rows[i] = part_rows[i];
+    R += part_rows[i];
+  }
+  if (R % 128 != 0 || E * R > (1ll << 31) - 256) return MPM_ERR_SHAPE;
+  if (ws_bytes < mpm_nvfp4_weight_workspace_bytes(E)) return MPM_ERR_SHAPE;
+  if (!aligned(q, 16) || !aligned(ws, 4) || !aligned(ts, 4)) return MPM_ERR_ALIGN;
+  return cuda_status(mpm::launch_nvfp4_weight(parts, rows, nparts, (int)K, E, q, s, ts,
+                                              static_cast<unsigned*>(ws), stream));
+}
+
+int64_t mpm_moe_row_capacity(int64_t T, int k, int64_t E) {
+  if (T < 1 || k < 1 || E < 1) return 0;
+  return pad_to(T * k, 128) + 128 * E;
+}
+
+size_t mpm_moe_segments_workspace_bytes(int64_t T, int k, int64_t E) {
+  if (T < 1 || k < 1 || E < 1) return 0;
+  return mpm::segments_ws_bytes(T, k, E);
+}
+
+mpm_status mpm_moe_build_segments(const int32_t* ids, const float* prob, int64_t T, int k,
+                                  int64_t E, int32_t* seg, int32_t* perm, int32_t* inv,
+                                  float* row_prob, void* ws, size_t ws_bytes,
+                                  cudaStream_t stream) {
+  if (!ids || !prob || !seg || !perm || !inv || !row_prob || !ws) return MPM_ERR_NULL;
+  if (T < 1 || k < 1 || k > 64 || E < 1 || E > 1024) return MPM_ERR_SHAPE;
+  if (T * k > (1ll << 30)) return MPM_ERR_SHAPE;
+  if (ws_bytes < mpm::segments_ws_bytes(T, k, E)) return MPM_ERR_SHAPE;
+  if (!aligned(ws, 4)) return MPM_ERR_ALIGN;
+  return cuda_status(mpm::launch_build_segments(ids, prob, T, k, E, seg, perm, inv, row_prob,
+                                                mpm_moe_row_capacity(T, k, E), ws, status_ptr(),
+                                                stream));
+}
+
+mpm_status mpm_moe_gather(int what, const void* src, const uint8_t* src_s, const float* src_ts,
+                          int64_t T, int64_t K, int k, const int32_t* perm, const int32_t* seg,
+                          int64_t E, int64_t capacity, void* dst, uint8_t* dst_s,
+                          float* dst_ts, cudaStream_t stream) {
+  if (!src || !perm || !seg || !dst) return MPM_ERR_NULL;
+  if (what != MPM_GATHER_BF16 && what != MPM_GATHER_NVFP4) return MPM_ERR_UNSUPPORTED;
+  if (T < 1 || K < 64 || K % 64 != 0 || k < 1 || E < 1 || capacity < 1) return MPM_ERR_SHAPE;
+  if (what == MPM_GATHER_NVFP4) {
+    if (!src_s || !src_ts || !dst_s || !dst_ts) return MPM_ERR_NULL;
+    if (!aligned(src_s, 4) || !aligned(dst_s, 4)) return MPM_ERR_ALIGN;
+  }
+  if (!aligned(src, 16) || !aligned(dst, 16)) return MPM_ERR_ALIGN;
+  return cuda_status(mpm::launch_gather(what, src, src_s, src_ts, K, k, perm, seg + E, capacity,
+                                        dst, dst_s, dst_ts, stream));
+}
+
+mpm_status mpm_moe_combine(const void* y, const int32_t* inv, int64_t T, int k, int64_t H,
+                           void* out, cudaStream_t stream) {
+  if (!y || !inv || !out) return MPM_ERR_NULL;
+  if (T < 1 || k < 1 || H < 8 || H % 8 != 0) return MPM_ERR_SHAPE;
+  if (!aligned(y, 16) || !aligned(out, 16)) return MPM_ERR_ALIGN;
+  return cuda_status(mpm::launch_combine(y, inv, T, k, H, out, stream));
+}
+
+mpm_status mpm_moe_grouped_gemm(const mpm_grouped_gemm_desc* d, cudaStream_t stream) {
+  if (!d) return MPM_ERR_NULL;
+  if (d->kind != MPM_KIND_NVFP4 && d->kind != MPM_KIND_MXFP8) return MPM_ERR_UNSUPPORTED;
+  if (d->group != MPM_GROUP_M && d->group != MPM_GROUP_K) return MPM_ERR_UNSUPPORTED;
+  if (d->epilogue < MPM_EPI_F32 || d->epilogue > MPM_EPI_DSWIGLU) return MPM_ERR_UNSUPPORTED;
+  if (!d->a_dev || !d->b_dev || !d->sfa_dev || !d->sfb_dev || !d->out_dev) return MPM_ERR_NULL;
+  if (d->E < 1 || d->E > 65535 || d->N < 256 || d->N % 256 != 0 || d->a_rows < 1)
+    return MPM_ERR_SHAPE;
+  const bool swiglu = d->epilogue == MPM_EPI_SWIGLU || d->epilogue == MPM_EPI_SWIGLU_SAVE;
+  const int elems_per_kb = d->kind == MPM_KIND_NVFP4 ? 256 : 128;
+  const int vec = d->kind == MPM_KIND_NVFP4 ? 16 : 32;
+  if (d->group == MPM_GROUP_M) {
+    if (d->K < elems_per_kb || d->K % elems_per_kb != 0) return MPM_ERR_SHAPE;
+    if (!d->seg_dev && d->E != 1) return MPM_ERR_NULL;
+    if (d->b_k_per_expert < 0 || d->b_k_per_expert % (d->kind == MPM_KIND_NVFP4 ? 64 : 128))
+      return MPM_ERR_SHAPE;
+  } else {
+    if (d->kind != MPM_KIND_MXFP8 || d->epilogue != MPM_EPI_F32) return MPM_ERR_UNSUPPORTED;
+    if (!d->seg_dev) return MPM_ERR_NULL;
+    if (d->a_rows % 128 != 0) return MPM_ERR_SHAPE;
+  }
+  if (d->b_rows_per_expert < 0 || d->b_rows_per_expert % 128 != 0) return MPM_ERR_SHAPE;
+  if (d->a_total_rows < 1 || d->b_total_rows < 1) return MPM_ERR_SHAPE;
+  if (d->lda_bytes < 128 || d->lda_bytes % 16 || d->ldb_bytes < 128 || d->ldb_bytes % 16)
+    return MPM_ERR_ALIGN;
+  if (!aligned(d->a_dev, 16) || !aligned(d->b_dev, 16) || !aligned(d->sfa_dev, 16) ||
+      !aligned(d->sfb_dev, 16) || !aligned(d->out_dev, 16))
+    return MPM_ERR_ALIGN;
+  if (d->sfa_cols < 1 || d->sfb_cols < 1) return MPM_ERR_SHAPE;
+  if (d->group == MPM_GROUP_M) {
+    const int bytes_per_elem2 = d->kind == MPM_KIND_NVFP4 ? 1 : 2;   // bytes = elems * this / 2
+    if (d->K * bytes_per_elem2 / 2 > d->lda_bytes) return MPM_ERR_SHAPE;
+    if (d->sfa_cols < d->K / vec) return MPM_ERR_SHAPE;
+  }
+  if (swiglu) {
+    if (!d->out2_dev || !d->row_prob_dev) return MPM_ERR_NULL;
+    if ((d->N / 2) % 128 != 0) return MPM_ERR_SHAPE;
+    if (!aligned(d->out2_dev, 16) || d->ldo2 % 8 || d->ldo2 < d->N / 2) return MPM_ERR_ALIGN;
+    if (d->epilogue == MPM_EPI_SWIGLU_SAVE && (d->ldo % 8 || d->ldo < d->N)) return MPM_ERR_ALIGN;
+  } else if (d->epilogue == MPM_EPI_DSWIGLU) {
+    if (!d->aux_dev || !d->row_prob_dev) return MPM_ERR_NULL;
+    if (!aligned(d->aux_dev, 16) || d->ld_aux % 8 || d->ld_aux < 2 * d->N) return MPM_ERR_ALIGN;
+    if (d->ldo % 8 || d->ldo < 2 * d->N) return MPM_ERR_ALIGN;
+  } else {
+    const int q = d->epilogue == MPM_EPI_F32 ? 4 : 8;
+    if (d->ldo % q || d->ldo < d->N) return MPM_ERR_ALIGN;
+  }
+
+  CUtensorMap ta, tb;
+  if (!make_tmap(&ta, d->a_dev, d->lda_bytes, d->a_total_rows)) return MPM_ERR_CUDA;
+  if (!make_tmap(&tb, d->b_dev, d->ldb_bytes, d->b_total_rows)) return MPM_ERR_CUDA;
+
+  mpm::GemmArgs a{};
+  a.group = d->group;
+  a.E = (int)d->E;
+  a.a_rows = d->a_rows;
+  a.N = d->N;
+  a.K = d->K;
+  a.M_out = d->a_rows;
+  a.seg = d->seg_dev;
+  a.b_rows_per_e = d->b_rows_per_expert;
+  a.b_k_per_e = d->b_k_per_expert;
+  a.sfa = d->sfa_dev; a.sfa_cols_pad = pad_to(d->sfa_cols, 4);
+  a.sfb = d->sfb_dev; a.sfb_cols_pad = pad_to(d->sfb_cols, 4);
+  a.alpha_a = d->alpha_a_dev;
+  a.alpha_b = d->alpha_b_dev;
+  a.row_prob = d->row_prob_dev;
+  a.out = d->out_dev; a.ldo = d->ldo;
+  a.out2 = d->out2_dev; a.ldo2 = d->ldo2;
+  a.aux = d->aux_dev; a.ld_aux = d->ld_aux;
+  a.amax = d->amax_dev;
+  a.status = status_ptr();
+
+  dim3 grid;
+  if (d->group == MPM_GROUP_M) {
+    grid = dim3((unsigned)(swiglu ? (d->N / 2) / 128 : d->N / 256),
+                (unsigned)((d->a_rows + 127) / 128), 1);
+  } else {
+    grid = dim3((unsigned)(d->N / 256), (unsigned)(d->a_rows / 128), (unsigned)d->E);
+  }
+  if (grid.y > 65535 && d->group == MPM_GROUP_M) return MPM_ERR_SHAPE;
+  return cuda_status(mpm::launch_grouped_gemm(d->kind, d->epilogue, ta, tb, a, grid, stream));
+}
+
+mpm_status mpm_get_device_status(int32_t* host_out, cudaStream_t stream) {
+  if (!host_out) return MPM_ERR_NULL;
+  int* p = status_ptr();
+  if (!p) return MPM_ERR_CUDA;
+  int zero = 0;
+  if (cudaMemcpyAsync(host_out, p, sizeof(int), cudaMemcpyDeviceToHost, stream) != cudaSuccess)
+    return MPM_ERR_CUDA;
+  if (cudaMemcpyAsync(p, &zero, sizeof(int), cudaMemcpyHostToDevice, stream) != cudaSuccess)
+    return MPM_ERR_CUDA;
+  return cuda_status(cudaStreamSynchronize(stream));
+}
+
+}  // extern "C"

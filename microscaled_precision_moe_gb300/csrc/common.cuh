@@ -1,0 +1,237 @@
+// Shared device helpers for libmpm (sm_103a): status word, format conversions,
+// and thin inline-PTX wrappers for mbarrier, TMA, bulk copies and tcgen05.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cstdint>
+
+#include "../../include/mpm.h"
+
+#define MPM_DEV __device__ __forceinline__
+
+namespace mpm {
+
+// ---------------------------------------------------------------- status word
+// One int per device (set by kernels on device-side errors, read and reset by
+// mpm_get_device_status); kernels receive its address.  The first error wins.
+MPM_DEV void set_status(int* st, int code) {
+  if (st) atomicCAS(st, 0, code);
+}
+
+// Bounded waits: about 2^32 cycles (~2 s at 2 GHz) before giving up.
+constexpr long long kWaitLimitCycles = 1ll << 32;
+
+// ---------------------------------------------------------------- bf16 / fp32
+MPM_DEV float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
+MPM_DEV float bf16hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// max of |bf16| over the two halves of a word, as a 16-bit pattern pair:
+// non-negative bf16 patterns order like unsigned integers.
+MPM_DEV uint32_t absmax_bf16x2(uint32_t acc, uint32_t w) {
+  return __vmaxu2(acc, w & 0x7FFF7FFFu);
+}
+
+// two fp32 -> packed E2M1 byte (lo in the low nibble), RN, satfinite
+MPM_DEV uint32_t cvt_e2m1x2(float lo, float hi) {
+  uint32_t out;
+  asm volatile(
+      "{\n\t.reg .b8 b;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b, %2, %1;\n\t"
+      "cvt.u32.u8 %0, b;\n\t}"
+      : "=r"(out) : "f"(lo), "f"(hi));
+  return out;
+}
+
+// two fp32 -> packed E4M3 pair (lo in the low byte), RN, satfinite
+MPM_DEV uint32_t cvt_e4m3x2(float lo, float hi) {
+  uint16_t out;
+  asm volatile("cvt.rn.satfinite.e4m3x2.f32 %0, %2, %1;" : "=h"(out) : "f"(lo), "f"(hi));
+  return out;
+}
+
+// E4M3 byte -> fp32 (exact), through the exact e4m3 -> f16 conversion
+MPM_DEV float e4m3_to_f32(uint32_t code) {
+  uint32_t h2;
+  uint16_t in = (uint16_t)(code & 0xFF);
+  asm volatile("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(in));
+  __half lo = __ushort_as_half((unsigned short)(h2 & 0xFFFF));
+  return __half2float(lo);
+}
+
+MPM_DEV uint32_t float_bits(float f) { return __float_as_uint(f); }
+
+// ---------------------------------------------------------------- 128x4 scale tiles
+// byte offset of scale entry (r, c) in a tiled [rows, cols] scale matrix whose
+// padded column count is cols_pad (multiple of 4)
+MPM_DEV size_t sf_offset(long long r, long long c, long long cols_pad) {
+  long long rt = r >> 7, rr = r & 127, ct = c >> 2, cc = c & 3;
+  return (size_t)((rt * (cols_pad >> 2) + ct) * 512 + (rr & 31) * 16 + (rr >> 5) * 4 + cc);
+}
+
+// ---------------------------------------------------------------- shared memory
+MPM_DEV uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// ---------------------------------------------------------------- mbarrier
+MPM_DEV void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" :: "r"(bar), "r"(count) : "memory");
+}
+MPM_DEV void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+MPM_DEV void fence_proxy_async() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+MPM_DEV void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;"
+               :: "r"(bar), "r"(bytes) : "memory");
+}
+MPM_DEV uint32_t mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
+  return ok;
+}
+// Bounded wait; returns false (and records MPM_ERR_DEVICE_TIMEOUT) on timeout.
+MPM_DEV bool mbar_wait(uint32_t bar, uint32_t parity, int* st) {
+  if (mbar_try_wait(bar, parity)) return true;
+  long long t0 = clock64();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (clock64() - t0 > kWaitLimitCycles) {
+      set_status(st, MPM_ERR_DEVICE_TIMEOUT);
+      return false;
+    }
+  }
+}
+
+// ---------------------------------------------------------------- TMA / bulk copies
+MPM_DEV void tma_load_2d(uint32_t dst, const void* tmap, int x, int y, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];"
+      :: "r"(dst), "l"(tmap), "r"(x), "r"(y), "r"(bar) : "memory");
+}
+MPM_DEV void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+      :: "r"(dst), "l"(src), "r"(bytes), "r"(bar) : "memory");
+}
+MPM_DEV void prefetch_tmap(const void* tmap) {
+  asm volatile("prefetch.tensormap [%0];" :: "l"(tmap) : "memory");
+}
+
+// ---------------------------------------------------------------- tcgen05
+MPM_DEV void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+               :: "r"(dst_smem), "r"(ncols) : "memory");
+}
+MPM_DEV void tmem_relinquish() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+MPM_DEV void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;"
+               :: "r"(taddr), "r"(ncols) : "memory");
+}
+MPM_DEV void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+MPM_DEV void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+// arrive on an mbarrier once all prior tcgen05 async ops of this thread finish
+MPM_DEV void tc_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
+               :: "r"(bar) : "memory");
+}
+// copy a 32-row x 16-byte block from shared memory to TMEM, replicated into
+// the four 32-lane quarters (4 columns)
+MPM_DEV void tc_cp_32x128b_x4(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;"
+               :: "r"(taddr), "l"(sdesc) : "memory");
+}
+
+// D[tmem] (+)= A[smem] * B[smem]^T, E2M1 x E2M1 with E4M3 scales per 16
+MPM_DEV void mma_nvf4(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                      uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X"
+      " [%0], %1, %2, %3, [%5], [%6], p;\n\t}"
+      :: "r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate),
+         "r"(sfa_tmem), "r"(sfb_tmem) : "memory");
+}
+// D[tmem] (+)= A[smem] * B[smem]^T, E4M3 x E4M3 with E8M0 scales per 32
+MPM_DEV void mma_mxf8(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                      uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X"
+      " [%0], %1, %2, %3, [%5], [%6], p;\n\t}"
+      :: "r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate),
+         "r"(sfa_tmem), "r"(sfb_tmem) : "memory");
+}
+
+// 32 lanes x 32 columns of 32-bit accumulator -> 32 registers per thread
+MPM_DEV void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32"
+      " {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15,"
+      " %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31},"
+      " [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
+        "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]),
+        "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]),
+        "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]),
+        "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+}
+MPM_DEV void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// ---------------------------------------------------------------- descriptors
+// Shared-memory matrix descriptor (tcgen05 format): K-major operand stored as
+// rows of 128 bytes with the 128-byte swizzle, 8-row groups 1024 bytes apart.
+MPM_DEV uint64_t sdesc_sw128(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);          // start address
+  d |= (uint64_t)1 << 16;                            // leading byte offset (unused)
+  d |= (uint64_t)(1024 >> 4) << 32;                  // stride byte offset
+  d |= (uint64_t)1 << 46;                            // descriptor version
+  d |= (uint64_t)2 << 61;                            // 128-byte swizzle
+  return d;
+}
+// Descriptor of a 32-row x 16-byte block without swizzle (core matrices of
+// 8 rows x 16 bytes, 128 bytes apart): the source of a scale-factor copy.
+MPM_DEV uint64_t sdesc_sf(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)0 << 16;
+  d |= (uint64_t)(128 >> 4) << 32;
+  d |= (uint64_t)1 << 46;
+  return d;
+}
+
+// Instruction descriptor of a block-scaled MMA, M = 128, K-major A and B.
+//   fmt: operand format code (E2M1 = 1 for mxf4nvf4, E4M3 = 0 for mxf8f6f4)
+//   ue8m0: scale type (0 = UE4M3, 1 = UE8M0); sf_id: byte of the scale word
+__host__ __device__ constexpr uint32_t idesc_block_scaled(uint32_t fmt, uint32_t n,
+                                                          uint32_t ue8m0, uint32_t sf_id) {
+  return (sf_id << 4)            // B scale-factor id
+       | (fmt << 7)              // A format
+       | (fmt << 10)             // B format
+       | ((n >> 3) << 17)        // N / 8
+       | (ue8m0 << 23)           // scale type
+       | ((128u >> 4) << 24)     // M / 16
+       | (sf_id << 29);          // A scale-factor id
+}
+
+}  // namespace mpm

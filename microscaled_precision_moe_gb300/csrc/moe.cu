@@ -1,0 +1,241 @@
+// Expert segments, permutation gather and combine for sm_103a.
+//
+// "miniTE technical report", section 5.2: the routed rows of all experts sit
+// in one contiguous buffer whose expert boundaries are offsets kept on the
+// device; zero-token experts and the padding of each segment (to 128 rows, one
+// MMA tile) are handled in the same path.  Section 5.3: the permute gathers
+// each routed (token, slot) row; the combine sums a token's expert outputs.
+//
+// The counting sort is stable: rows of one expert appear in ascending flat
+// index t*k + j.  Every step is integer work, so results are bit-identical
+// run to run.
+#include "moe.cuh"
+
+namespace mpm {
+
+constexpr int kSegChunk = 4096;   // flat (token, slot) pairs per chunk
+
+// 1) per-chunk expert histogram: hist[chunk][e]
+__global__ void __launch_bounds__(256) seg_hist_kernel(const int* ids, long long n, int E,
+                                                      int* hist, int* st) {
+  extern __shared__ int h[];
+  for (int e = threadIdx.x; e < E; e += blockDim.x) h[e] = 0;
+  __syncthreads();
+  const long long base = (long long)blockIdx.x * kSegChunk;
+  for (int i = threadIdx.x; i < kSegChunk; i += blockDim.x) {
+    const long long f = base + i;
+    if (f >= n) break;
+    const int e = ids[f];
+    if (e >= 0 && e < E) atomicAdd(&h[e], 1);
+    else set_status(st, MPM_ERR_DEVICE_BOUNDS);
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) hist[(long long)blockIdx.x * E + e] = h[e];
+}
+
+// 2) one CTA: per-expert totals, padded segment offsets (exclusive scan), and
+//    each chunk's first row per expert: base[chunk][e]
+__global__ void __launch_bounds__(1024) seg_scan_kernel(const int* hist, int nchunks, int E,
+                                                       int* base, int* seg_offsets) {
+  __shared__ int padded[1024];
+  __shared__ int total_sh[1024];
+  const int e = threadIdx.x;
+  int tot = 0;
+  if (e < E) {
+    for (int c = 0; c < nchunks; ++c) {
+      const int v = hist[(long long)c * E + e];
+      base[(long long)c * E + e] = tot;        // exclusive within the expert
+      tot += v;
+    }
+  }
+  total_sh[e] = tot;
+  padded[e] = (e < E) ? (tot + 127) / 128 * 128 : 0;
+  __syncthreads();
+  // Hillis-Steele inclusive scan over padded sizes
+  for (int o = 1; o < 1024; o <<= 1) {
+    const int v = (e >= o) ? padded[e - o] : 0;
+    __syncthreads();
+    padded[e] += v;
+    __syncthreads();
+  }
+  const int excl = padded[e] - ((e < E) ? (total_sh[e] + 127) / 128 * 128 : 0);
+  if (e < E) {
+    seg_offsets[e] = excl;
+    for (int c = 0; c < nchunks; ++c) base[(long long)c * E + e] += excl;
+  }
+  if (e == E - 1) seg_offsets[E] = padded[e];
+}
+
+// 3) stable scatter: one warp walks its chunk in order, 32 pairs at a time
+__global__ void __launch_bounds__(32) seg_scatter_kernel(const int* ids, const float* prob,
+                                                        long long n, int E, const int* base,
+                                                        int* perm, int* inv_perm,
+                                                        float* row_prob) {
+  extern __shared__ int cnt[];
+  const int lane = threadIdx.x;
+  for (int e = lane; e < E; e += 32) cnt[e] = base[(long long)blockIdx.x * E + e];
+  __syncwarp();
+  const long long c0 = (long long)blockIdx.x * kSegChunk;
+  for (int s = 0; s < kSegChunk; s += 32) {
+    const long long f = c0 + s + lane;
+    int e = -1;
+    if (f < n) {
+      e = ids[f];
+      if (e < 0 || e >= E) e = -1;
+    }
+    const unsigned grp = __match_any_sync(0xFFFFFFFFu, e);
+    const unsigned lt = (1u << lane) - 1u;
+    const int rank = __popc(grp & lt);
+    int row = -1;
+    if (e >= 0) row = cnt[e] + rank;
+    __syncwarp();
+    if (e >= 0 && (grp >> lane) == 1u) cnt[e] += __popc(grp);   // highest lane of group
+    __syncwarp();
+    if (f < n) {
+      inv_perm[f] = row;
+      if (row >= 0) {
+        perm[row] = (int)f;
+        row_prob[row] = prob[f];
+      }
+    }
+    if (c0 + s + 32 >= n) break;
+  }
+}
+
+// ---------------------------------------------------------------- gather
+// dst[row] = src[perm[row] / k] (bf16 rows), zeros for padding rows
+__global__ void __launch_bounds__(256) gather_bf16_kernel(const uint4* src, long long K8,
+                                                         int k, const int* perm,
+                                                         const int* seg_end, long long cap,
+                                                         uint4* dst) {
+  const long long row = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  long long rend = *seg_end;
+  if (rend > cap) rend = cap;
+  if (row >= rend) return;
+  const int f = perm[row];
+  uint4* d = dst + row * K8;
+  if (f < 0) {
+    for (long long i = lane; i < K8; i += 32) d[i] = make_uint4(0, 0, 0, 0);
+    return;
+  }
+  const uint4* s = src + (long long)(f / k) * K8;
+  for (long long i = lane; i < K8; i += 32) d[i] = __ldg(s + i);
+}
+
+// NVFP4 rows: codes (K/2 bytes), 128x4-tiled scales (K/16 columns) and the
+// token scale move together
+__global__ void __launch_bounds__(256) gather_nvfp4_kernel(const uint4* src_q, const uint8_t* src_s,
+                                                          const float* src_ts, long long K,
+                                                          int k, const int* perm,
+                                                          const int* seg_end, long long cap,
+                                                          uint4* dst_q, uint8_t* dst_s,
+                                                          float* dst_ts) {
+  const long long row = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  long long rend = *seg_end;
+  if (rend > cap) rend = cap;
+  if (row >= rend) return;
+  const int f = perm[row];
+  const long long q16 = K / 32;          // uint4 chunks of packed codes per row
+  const long long cols = K / 16, cpad = cols;   // K % 64 == 0
+  uint4* dq = dst_q + row * q16;
+  if (f < 0) {
+    for (long long i = lane; i < q16; i += 32) dq[i] = make_uint4(0, 0, 0, 0);
+    for (long long g = lane; g < cols / 4; g += 32)
+      *reinterpret_cast<uint32_t*>(dst_s + sf_offset(row, g * 4, cpad)) = 0u;
+    if (lane == 0) dst_ts[row] = 0.0f;
+    return;
+  }
+  const long long t = f / k;
+  const uint4* sq = src_q + t * q16;
+  for (long long i = lane; i < q16; i += 32) dq[i] = __ldg(sq + i);
+  for (long long g = lane; g < cols / 4; g += 32)
+    *reinterpret_cast<uint32_t*>(dst_s + sf_offset(row, g * 4, cpad)) =
+        *reinterpret_cast<const uint32_t*>(src_s + sf_offset(t, g * 4, cpad));
+  if (lane == 0) dst_ts[row] = src_ts[t];
+}
+
+// ---------------------------------------------------------------- combine
+// out[t] = sum_j y[inv[t*k + j]] in fp32, slot order, one rounding to bf16
+__global__ void __launch_bounds__(128) combine_kernel(const uint4* y, const int* inv, long long T,
+                                                     int k, long long H8, uint4* out) {
+  const long long c = (long long)blockIdx.y * blockDim.x + threadIdx.x;
+  const long long t = blockIdx.x;
+  if (c >= H8) return;
+  float acc[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+  for (int j = 0; j < k; ++j) {
+    const int r = inv[t * k + j];
+    if (r < 0) continue;
+    const uint4 v = __ldg(y + (long long)r * H8 + c);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      acc[2 * i] = __fadd_rn(acc[2 * i], bf16lo(w[i]));
+      acc[2 * i + 1] = __fadd_rn(acc[2 * i + 1], bf16hi(w[i]));
+    }
+  }
+  uint32_t o[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    __nv_bfloat162 b = __floats2bfloat162_rn(acc[2 * i], acc[2 * i + 1]);
+    o[i] = *reinterpret_cast<uint32_t*>(&b);
+  }
+  out[t * H8 + c] = make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+// ---------------------------------------------------------------- launchers
+size_t segments_ws_bytes(long long T, int k, long long E) {
+  const long long n = T * k;
+  const long long nchunks = (n + kSegChunk - 1) / kSegChunk;
+  return (size_t)(2 * nchunks * E) * sizeof(int);
+}
+
+cudaError_t launch_build_segments(const int* ids, const float* prob, long long T, int k,
+                                  long long E, int* seg_offsets, int* perm, int* inv_perm,
+                                  float* row_prob, long long cap, void* ws, int* st,
+                                  cudaStream_t s) {
+  const long long n = T * k;
+  const int nchunks = (int)((n + kSegChunk - 1) / kSegChunk);
+  int* hist = static_cast<int*>(ws);
+  int* base = hist + (long long)nchunks * E;
+  cudaError_t err;
+  if ((err = cudaMemsetAsync(perm, 0xFF, (size_t)cap * sizeof(int), s)) != cudaSuccess) return err;
+  if ((err = cudaMemsetAsync(row_prob, 0, (size_t)cap * sizeof(float), s)) != cudaSuccess) return err;
+  seg_hist_kernel<<<nchunks, 256, (size_t)E * sizeof(int), s>>>(ids, n, (int)E, hist, st);
+  if ((err = cudaGetLastError()) != cudaSuccess) return err;
+  seg_scan_kernel<<<1, 1024, 0, s>>>(hist, nchunks, (int)E, base, seg_offsets);
+  if ((err = cudaGetLastError()) != cudaSuccess) return err;
+  seg_scatter_kernel<<<nchunks, 32, (size_t)E * sizeof(int), s>>>(ids, prob, n, (int)E, base,
+                                                                  perm, inv_perm, row_prob);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gather(int what, const void* src, const uint8_t* src_s, const float* src_ts,
+                          long long K, int k, const int* perm, const int* seg_end,
+                          long long cap, void* dst, uint8_t* dst_s, float* dst_ts,
+                          cudaStream_t s) {
+  const unsigned grid = (unsigned)((cap + 7) / 8);
+  if (what == MPM_GATHER_BF16) {
+    gather_bf16_kernel<<<grid, 256, 0, s>>>(static_cast<const uint4*>(src), K / 8, k, perm,
+                                            seg_end, cap, static_cast<uint4*>(dst));
+  } else {
+    gather_nvfp4_kernel<<<grid, 256, 0, s>>>(static_cast<const uint4*>(src), src_s, src_ts, K,
+                                             k, perm, seg_end, cap, static_cast<uint4*>(dst),
+                                             dst_s, dst_ts);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_combine(const void* y, const int* inv, long long T, int k, long long H,
+                           void* out, cudaStream_t s) {
+  const long long H8 = H / 8;
+  const dim3 grid((unsigned)T, (unsigned)((H8 + 127) / 128));
+  combine_kernel<<<grid, 128, 0, s>>>(static_cast<const uint4*>(y), inv, T, k, H8,
+                                      static_cast<uint4*>(out));
+  return cudaGetLastError();
+}
+
+}  // namespace mpm

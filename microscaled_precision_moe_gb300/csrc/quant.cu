@@ -1,0 +1,444 @@
+// MXFP8 and NVFP4 quantisers for sm_103a.
+//
+// NVFP4 (E2M1 codes, E4M3 scale per 16, FP32 outer scale; "Towards
+// Blackwell-native 8-bit and 4-bit RL", sections "Format background / NVFP4"
+// and "Per-token activation scaling"; "miniTE technical report", section 5.6
+// for s_g = amax / 2688).  One warp per row: the row is read once with 128-bit
+// loads and kept in registers, the row amax is reduced with warp shuffles, and
+// codes plus 128x4-tiled scales are written directly in the operand layout of
+// the block-scaled MMA.
+//
+// MXFP8 (E4M3 codes, E8M0 scale per 32 rounded up; same post, sections
+// "Format background / MXFP8" and "Recipe 1 / Training").  A CTA reads a
+// 128 x 64 bf16 tile once, writes the row-wise 1x32 copy from registers and the
+// column-wise 32x1 copy, transposed, from a shared-memory copy of the tile.
+#include "quant.cuh"
+
+namespace mpm {
+
+// ============================================================================
+// NVFP4
+// ============================================================================
+
+// Canonical per-row fp32 sequence, step 2: s_g = a / 2688 with the 2^-116 floor.
+MPM_DEV float nvfp4_outer(float a) {
+  if (!(a > 0.0f)) return 0.0f;
+  float sg = __fdiv_rn(a, 2688.0f);
+  const float floor_sg = 0x1p-116f;
+  return sg < floor_sg ? floor_sg : sg;
+}
+
+struct Nvfp4Rows {
+  const __nv_bfloat16* part[4];
+  long long part_rows[4];   // rows per group in each part
+  int nparts;
+  long long R;              // rows per group (sum of part_rows)
+  long long ldx;            // elements (single-part activation mode)
+  long long rows;           // total rows to quantise (= groups * R)
+  long long rows_pad;       // rows whose scale bytes are written (zeros past rows)
+  int K;
+  int amax_mode;            // 0 = own row max, 1 = amax_in[row], 2 = group amax bits
+  const float* amax_in;
+  const unsigned* group_amax;
+  uint8_t* q;
+  uint8_t* s;
+  float* ts;                // per row (modes 0/1) or per group (mode 2)
+  const int* m_valid;
+};
+
+MPM_DEV const __nv_bfloat16* nvfp4_row_ptr(const Nvfp4Rows& p, long long row) {
+  if (p.nparts == 1 && p.amax_mode != 2) return p.part[0] + row * p.ldx;
+  long long g = row / p.R, lr = row - g * p.R;
+  int k = 0;
+#pragma unroll
+  for (int i = 0; i < 3; ++i)
+    if (k < p.nparts - 1 && lr >= p.part_rows[k]) { lr -= p.part_rows[k]; ++k; }
+  return p.part[k] + (g * p.part_rows[k] + lr) * (long long)p.K;
+}
+
+template <int NB>
+__global__ void __launch_bounds__(128) nvfp4_quant_rows_kernel(const Nvfp4Rows p) {
+  const int lane = threadIdx.x & 31;
+  const long long row = (long long)blockIdx.x * 4 + (threadIdx.x >> 5);
+  long long rows_eff = p.rows;
+  if (p.m_valid) {
+    long long mv = *p.m_valid;
+    rows_eff = mv < rows_eff ? mv : rows_eff;
+    if (row >= rows_eff) return;
+  }
+  const int nblk = p.K >> 4;
+  const long long cols_pad = nblk;          // K % 64 == 0 -> nblk % 4 == 0
+  if (row >= rows_eff) {
+    if (row < p.rows_pad) {                 // padding rows of the last tile
+      for (int b = lane; b < nblk; b += 32) p.s[sf_offset(row, b, cols_pad)] = 0;
+    }
+    return;
+  }
+  const __nv_bfloat16* xr = nvfp4_row_ptr(p, row);
+
+  uint4 v[NB][2];
+#pragma unroll
+  for (int i = 0; i < NB; ++i) {
+    const int b = i * 32 + lane;
+    if (b < nblk) {
+      const uint4* src = reinterpret_cast<const uint4*>(xr + (long long)b * 16);
+      v[i][0] = __ldcs(src);
+      v[i][1] = __ldcs(src + 1);
+    } else {
+      v[i][0] = make_uint4(0, 0, 0, 0);
+      v[i][1] = make_uint4(0, 0, 0, 0);
+    }
+  }
+  // per-block |x| max (as bf16 bit patterns) and the lane max
+  uint32_t bmax16[NB];
+  uint32_t lmax = 0;
+#pragma unroll
+  for (int i = 0; i < NB; ++i) {
+    uint32_t m = 0;
+    m = absmax_bf16x2(m, v[i][0].x); m = absmax_bf16x2(m, v[i][0].y);
+    m = absmax_bf16x2(m, v[i][0].z); m = absmax_bf16x2(m, v[i][0].w);
+    m = absmax_bf16x2(m, v[i][1].x); m = absmax_bf16x2(m, v[i][1].y);
+    m = absmax_bf16x2(m, v[i][1].z); m = absmax_bf16x2(m, v[i][1].w);
+    m = max(m & 0xFFFFu, m >> 16);
+    bmax16[i] = m;
+    lmax = max(lmax, m);
+  }
+  float a;
+  if (p.amax_mode == 0) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) lmax = max(lmax, __shfl_xor_sync(0xFFFFFFFFu, lmax, o));
+    a = __uint_as_float(lmax << 16);
+  } else if (p.amax_mode == 1) {
+    a = p.amax_in[row];
+  } else {
+    a = __uint_as_float(p.group_amax[row / p.R]);
+  }
+  const float sg = nvfp4_outer(a);
+  if (lane == 0) {
+    if (p.amax_mode != 2) p.ts[row] = sg;
+    else if (row % p.R == 0) p.ts[row / p.R] = sg;
+  }
+  const float six_sg = __fmul_rn(6.0f, sg);
+  uint8_t* qr = p.q + row * (long long)(p.K >> 1);
+#pragma unroll
+  for (int i = 0; i < NB; ++i) {
+    const int b = i * 32 + lane;
+    if (b >= nblk) continue;
+    uint32_t sb = 0;
+    if (sg > 0.0f) {
+      const float sbf = __fdiv_rn(__uint_as_float(bmax16[i] << 16), six_sg);
+      sb = cvt_e4m3x2(sbf, 0.0f) & 0xFFu;
+    }
+    const float sbv = e4m3_to_f32(sb);
+    uint2 out = make_uint2(0, 0);
+    if (sbv > 0.0f) {
+      const float r = __frcp_rn(__fmul_rn(sbv, sg));
+      const uint32_t w[8] = {v[i][0].x, v[i][0].y, v[i][0].z, v[i][0].w,
+                             v[i][1].x, v[i][1].y, v[i][1].z, v[i][1].w};
+      uint32_t bytes[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        bytes[j] = cvt_e2m1x2(__fmul_rn(bf16lo(w[j]), r), __fmul_rn(bf16hi(w[j]), r));
+      out.x = bytes[0] | (bytes[1] << 8) | (bytes[2] << 16) | (bytes[3] << 24);
+      out.y = bytes[4] | (bytes[5] << 8) | (bytes[6] << 16) | (bytes[7] << 24);
+    }
+    *reinterpret_cast<uint2*>(qr + (long long)b * 8) = out;
+    p.s[sf_offset(row, b, cols_pad)] = (uint8_t)sb;
+  }
+}
+
+// Per-group amax for the joint weight scale: |x| max over a group's rows of
+// all parts, as fp32 bits, reduced with an integer atomicMax (order-free).
+struct GroupAmax {
+  const __nv_bfloat16* part[4];
+  long long part_elems[4];  // elements per group in each part
+  int nparts;
+  unsigned* out;            // [groups]
+};
+
+__global__ void __launch_bounds__(256) group_amax_kernel(const GroupAmax p, int chunks_per_group) {
+  const int g = blockIdx.y;
+  const int c = blockIdx.x;
+  uint32_t m = 0;
+  for (int k = 0; k < p.nparts; ++k) {
+    const long long n = p.part_elems[k];
+    const uint4* src = reinterpret_cast<const uint4*>(p.part[k] + g * n);
+    const long long nv = n >> 3;
+    const long long per = (nv + chunks_per_group - 1) / chunks_per_group;
+    const long long lo = c * per, hi = min(nv, lo + per);
+    for (long long i = lo + threadIdx.x; i < hi; i += blockDim.x) {
+      uint4 w = __ldcs(src + i);
+      m = absmax_bf16x2(m, w.x); m = absmax_bf16x2(m, w.y);
+      m = absmax_bf16x2(m, w.z); m = absmax_bf16x2(m, w.w);
+    }
+  }
+  m = max(m & 0xFFFFu, m >> 16);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+  __shared__ uint32_t wm[8];
+  if ((threadIdx.x & 31) == 0) wm[threadIdx.x >> 5] = m;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    uint32_t r = 0;
+    for (int i = 0; i < (int)(blockDim.x >> 5); ++i) r = max(r, wm[i]);
+    atomicMax(p.out + g, r << 16);
+  }
+}
+
+// ============================================================================
+// MXFP8
+// ============================================================================
+
+// Scale exponent e of a block whose |max| has the fp32 bit pattern `bits`:
+// the smallest e with a <= 448 * 2^e, clamped to [-127, 127].  For
+// a = 1.f * 2^p:  e = p - 8 + [1.f > 1.75].  Zero and subnormal a clamp to -127.
+MPM_DEV int mx_exponent(uint32_t bits) {
+  const int E = (int)(bits >> 23) & 0xFF;
+  if (E == 0) return -127;
+  const int e = (E - 127) - 8 + (((bits & 0x7FFFFFu) > 0x600000u) ? 1 : 0);
+  return e < -127 ? -127 : (e > 127 ? 127 : e);
+}
+
+// 32 bf16 values (16 words) -> 32 E4M3 codes (8 words) scaled by 2^-e
+MPM_DEV void mx_encode32(const uint32_t (&w)[16], float scale, uint32_t (&o)[8]) {
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const uint32_t p0 = cvt_e4m3x2(__fmul_rn(bf16lo(w[2 * j]), scale),
+                                   __fmul_rn(bf16hi(w[2 * j]), scale));
+    const uint32_t p1 = cvt_e4m3x2(__fmul_rn(bf16lo(w[2 * j + 1]), scale),
+                                   __fmul_rn(bf16hi(w[2 * j + 1]), scale));
+    o[j] = p0 | (p1 << 16);
+  }
+}
+
+MPM_DEV float pow2_neg(int e) { return __uint_as_float((uint32_t)(127 - e) << 23); }
+
+struct Mxfp8Args {
+  const __nv_bfloat16* x;
+  long long M, K, ldx;
+  unsigned flags;
+  uint8_t* row_q; uint8_t* row_s; long long row_s_cols_pad;
+  uint8_t* col_q; long long ldc; uint8_t* col_s; long long col_s_cols_pad;
+  const int* m_valid;
+};
+
+constexpr int MX_TM = 128, MX_TK = 64;
+
+__global__ void __launch_bounds__(256) mxfp8_quant_kernel(const Mxfp8Args p) {
+  __shared__ __align__(16) uint16_t tile[MX_TM][MX_TK];
+  const long long m0 = (long long)blockIdx.y * MX_TM;
+  const long long k0 = (long long)blockIdx.x * MX_TK;
+  long long M_eff = p.M;
+  if (p.m_valid) { long long mv = *p.m_valid; M_eff = mv < M_eff ? mv : M_eff; }
+  if (m0 >= M_eff) return;
+  const int t = threadIdx.x;
+
+  // ---- load: thread t owns row t/2, columns (t%2)*32 .. +32 (one row block)
+  {
+    const int r = t >> 1, half = t & 1;
+    const long long row = m0 + r;
+    const long long col = k0 + half * 32;
+    uint32_t w[16];
+    const bool in = (row < M_eff) && (col < p.K);
+    if (in) {
+      const uint4* src = reinterpret_cast<const uint4*>(p.x + row * p.ldx + col);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        uint4 u = __ldcs(src + j);
+        w[4 * j] = u.x; w[4 * j + 1] = u.y; w[4 * j + 2] = u.z; w[4 * j + 3] = u.w;
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < 16; ++j) w[j] = 0;
+    }
+    if (p.flags & MPM_ROWWISE) {
+      if (in) {
+        uint32_t m = 0;
+#pragma unroll
+        for (int j = 0; j < 16; ++j) m = absmax_bf16x2(m, w[j]);
+        m = max(m & 0xFFFFu, m >> 16);
+        const int e = mx_exponent(m << 16);
+        uint32_t o[8];
+        mx_encode32(w, pow2_neg(e), o);
+        uint4* dst = reinterpret_cast<uint4*>(p.row_q + row * p.K + col);
+        dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
+        dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+        p.row_s[sf_offset(row, col >> 5, p.row_s_cols_pad)] = (uint8_t)(e + 127);
+      }
+    }
+    if (p.flags & MPM_COLWISE) {
+      uint4* st = reinterpret_cast<uint4*>(&tile[r][half * 32]);
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        st[j] = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+    }
+  }
+  if (!(p.flags & MPM_COLWISE)) return;
+  __syncthreads();
+
+  // ---- column blocks: thread t owns column t%64, rows (t/64)*32 .. +32
+  {
+    const int c = t & 63, g = t >> 6;
+    const long long col = k0 + c;
+    const long long mb = m0 + g * 32;
+    if (col >= p.K || mb >= M_eff) return;
+    uint32_t w[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j)
+      w[j] = (uint32_t)tile[g * 32 + 2 * j][c] | ((uint32_t)tile[g * 32 + 2 * j + 1][c] << 16);
+    uint32_t m = 0;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) m = absmax_bf16x2(m, w[j]);
+    m = max(m & 0xFFFFu, m >> 16);
+    const int e = mx_exponent(m << 16);
+    uint32_t o[8];
+    mx_encode32(w, pow2_neg(e), o);
+    uint8_t* dst = p.col_q + col * p.ldc + mb;
+    const long long nvalid = M_eff - mb;
+    if (nvalid >= 32) {
+      uint4* d4 = reinterpret_cast<uint4*>(dst);
+      d4[0] = make_uint4(o[0], o[1], o[2], o[3]);
+      d4[1] = make_uint4(o[4], o[5], o[6], o[7]);
+    } else {
+      for (int j = 0; j < nvalid; ++j) dst[j] = (uint8_t)(o[j >> 2] >> (8 * (j & 3)));
+    }
+    p.col_s[sf_offset(col, mb >> 5, p.col_s_cols_pad)] = (uint8_t)(e + 127);
+  }
+}
+
+// Zero the padding entries of a 128x4-tiled scale matrix: columns [cols,
+// cols_pad) of rows [0, rows), and all columns of rows [rows, rows_pad).
+__global__ void zero_scale_padding_kernel(uint8_t* s, long long rows, long long cols) {
+  const long long rows_pad = (rows + 127) / 128 * 128, cols_pad = (cols + 3) / 4 * 4;
+  const long long ncp = cols_pad - cols;
+  const long long nA = rows * ncp;
+  const long long nB = (rows_pad - rows) * cols_pad;
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < nA + nB;
+       i += (long long)gridDim.x * blockDim.x) {
+    long long r, c;
+    if (i < nA) { r = i / ncp; c = cols + i % ncp; }
+    else { long long j = i - nA; r = rows + j / cols_pad; c = j % cols_pad; }
+    s[sf_offset(r, c, cols_pad)] = 0;
+  }
+}
+
+// ============================================================================
+// launchers
+// ============================================================================
+
+static int nb_for(int nblk) {
+  const int need = (nblk + 31) / 32;
+  const int opts[] = {1, 2, 4, 8, 14, 16};
+  for (int o : opts) if (o >= need) return o;
+  return -1;
+}
+
+static cudaError_t launch_nvfp4_rows(const Nvfp4Rows& p, cudaStream_t st) {
+  const int nb = nb_for(p.K >> 4);
+  const long long warps = p.rows_pad > p.rows ? p.rows_pad : p.rows;
+  const dim3 grid((unsigned)((warps + 3) / 4)), block(128);
+  switch (nb) {
+    case 1: nvfp4_quant_rows_kernel<1><<<grid, block, 0, st>>>(p); break;
+    case 2: nvfp4_quant_rows_kernel<2><<<grid, block, 0, st>>>(p); break;
+    case 4: nvfp4_quant_rows_kernel<4><<<grid, block, 0, st>>>(p); break;
+    case 8: nvfp4_quant_rows_kernel<8><<<grid, block, 0, st>>>(p); break;
+    case 14: nvfp4_quant_rows_kernel<14><<<grid, block, 0, st>>>(p); break;
+    case 16: nvfp4_quant_rows_kernel<16><<<grid, block, 0, st>>>(p); break;
+    default: return cudaErrorInvalidValue;
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_nvfp4_per_token(const void* x, long long M, int K, long long ldx,
+                                   const float* amax_in, uint8_t* q, uint8_t* s, float* ts,
+                                   const int* m_valid, cudaStream_t st) {
+  Nvfp4Rows p{};
+  p.part[0] = static_cast<const __nv_bfloat16*>(x);
+  p.part_rows[0] = M;
+  p.nparts = 1;
+  p.R = M;
+  p.ldx = ldx;
+  p.rows = M;
+  p.rows_pad = m_valid ? M : (M + 127) / 128 * 128;
+  p.K = K;
+  p.amax_mode = amax_in ? 1 : 0;
+  p.amax_in = amax_in;
+  p.q = q; p.s = s; p.ts = ts;
+  p.m_valid = m_valid;
+  return launch_nvfp4_rows(p, st);
+}
+
+cudaError_t launch_nvfp4_weight(const void* const* parts, const long long* part_rows, int nparts,
+                                int K, long long E, uint8_t* q, uint8_t* s, float* ts,
+                                unsigned* ws, cudaStream_t st) {
+  cudaError_t err = cudaMemsetAsync(ws, 0, (size_t)E * sizeof(unsigned), st);
+  if (err != cudaSuccess) return err;
+  GroupAmax ga{};
+  long long R = 0;
+  for (int i = 0; i < nparts; ++i) {
+    ga.part[i] = static_cast<const __nv_bfloat16*>(parts[i]);
+    ga.part_elems[i] = part_rows[i] * K;
+    R += part_rows[i];
+  }
+  ga.nparts = nparts;
+  ga.out = ws;
+  const long long per_group = R * K;
+  int chunks = (int)((per_group + (1 << 20) - 1) >> 20);   // ~1M elements per CTA
+  if (chunks < 1) chunks = 1;
+  if (chunks > 1024) chunks = 1024;
+  group_amax_kernel<<<dim3(chunks, (unsigned)E), 256, 0, st>>>(ga, chunks);
+  err = cudaGetLastError();
+  if (err != cudaSuccess) return err;
+  Nvfp4Rows p{};
+  for (int i = 0; i < nparts; ++i) {
+    p.part[i] = ga.part[i];
+    p.part_rows[i] = part_rows[i];
+  }
+  p.nparts = nparts;
+  p.R = R;
+  p.ldx = K;
+  p.rows = E * R;
+  p.rows_pad = E * R;
+  p.K = K;
+  p.amax_mode = 2;
+  p.group_amax = ws;
+  p.q = q; p.s = s; p.ts = ts;
+  p.m_valid = nullptr;
+  return launch_nvfp4_rows(p, st);
+}
+
+cudaError_t launch_mxfp8(const void* x, long long M, long long K, long long ldx, unsigned flags,
+                         uint8_t* row_q, uint8_t* row_s, uint8_t* col_q, long long ldc,
+                         uint8_t* col_s, const int* m_valid, cudaStream_t st) {
+  Mxfp8Args p{};
+  p.x = static_cast<const __nv_bfloat16*>(x);
+  p.M = M; p.K = K; p.ldx = ldx; p.flags = flags;
+  p.row_q = row_q; p.row_s = row_s; p.row_s_cols_pad = (K / 32 + 3) / 4 * 4;
+  p.col_q = col_q; p.ldc = ldc; p.col_s = col_s;
+  p.col_s_cols_pad = ((M + 31) / 32 + 3) / 4 * 4;
+  p.m_valid = m_valid;
+  const dim3 grid((unsigned)((K + MX_TK - 1) / MX_TK), (unsigned)((M + MX_TM - 1) / MX_TM));
+  mxfp8_quant_kernel<<<grid, 256, 0, st>>>(p);
+  cudaError_t err = cudaGetLastError();
+  if (err != cudaSuccess) return err;
+  if (m_valid) return cudaSuccess;      // device-sized buffers: padding never read
+  const int zb = 256;
+  if (flags & MPM_ROWWISE) {
+    long long n = ((M + 127) / 128 * 128) * ((K / 32 + 3) / 4 * 4) - M * (K / 32);
+    if (n > 0) {
+      zero_scale_padding_kernel<<<(unsigned)((n + zb - 1) / zb > 1024 ? 1024 : (n + zb - 1) / zb), zb, 0, st>>>(row_s, M, K / 32);
+      if ((err = cudaGetLastError()) != cudaSuccess) return err;
+    }
+  }
+  if (flags & MPM_COLWISE) {
+    const long long cc = (M + 31) / 32;
+    long long n = ((K + 127) / 128 * 128) * ((cc + 3) / 4 * 4) - K * cc;
+    if (n > 0) {
+      zero_scale_padding_kernel<<<(unsigned)((n + zb - 1) / zb > 1024 ? 1024 : (n + zb - 1) / zb), zb, 0, st>>>(col_s, K, cc);
+      if ((err = cudaGetLastError()) != cudaSuccess) return err;
+    }
+  }
+  return cudaSuccess;
+}
+
+}  // namespace mpm

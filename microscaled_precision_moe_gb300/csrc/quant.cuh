@@ -1,0 +1,15 @@
+// Launchers of the quantiser kernels (host side, called by the C ABI layer).
+#pragma once
+#include "common.cuh"
+
+namespace mpm {
+cudaError_t launch_nvfp4_per_token(const void* x, long long M, int K, long long ldx,
+                                   const float* amax_in, uint8_t* q, uint8_t* s, float* ts,
+                                   const int* m_valid, cudaStream_t st);
+cudaError_t launch_nvfp4_weight(const void* const* parts, const long long* part_rows, int nparts,
+                                int K, long long E, uint8_t* q, uint8_t* s, float* ts,
+                                unsigned* ws, cudaStream_t st);
+cudaError_t launch_mxfp8(const void* x, long long M, long long K, long long ldx, unsigned flags,
+                         uint8_t* row_q, uint8_t* row_s, uint8_t* col_q, long long ldc,
+                         uint8_t* col_s, const int* m_valid, cudaStream_t st);
+}  // namespace mpm

@@ -1,0 +1,221 @@
+"""Torch-facing wrappers of the libmpm C ABI (same names, minus the prefix).
+
+PyTorch provides device memory and the current stream only; each function
+allocates its outputs with torch and passes raw pointers to the library,
+where every step runs in CUDA kernels.  Tensors must live on a CUDA device.
+"""
+from __future__ import annotations
+
+import ctypes as C
+
+import torch
+
+from . import _lib as L
+
+
+def _ptr(t):
+    return None if t is None else C.c_void_p(t.data_ptr())
+
+
+def _stream(dev=None):
+    return C.c_void_p(torch.cuda.current_stream(dev).cuda_stream)
+
+
+def _need_cuda(*ts):
+    for t in ts:
+        if t is not None and not t.is_cuda:
+            raise ValueError("libmpm operates on CUDA tensors only")
+
+
+def scale_bytes(rows: int, cols: int) -> int:
+    return int(L.load().mpm_scale_bytes(rows, cols))
+
+
+def pad_to(n: int, m: int) -> int:
+    return (n + m - 1) // m * m
+
+
+# ------------------------------------------------------------------ quantisers
+
+def mxfp8_quantize(x, rowwise=True, colwise=True, ldc=None, m_valid=None, out=None):
+    """MXFP8 row-wise 1x32 and/or column-wise 32x1 copies of bf16 x [M, K].
+
+    Returns dict with row_q [M, K], row_s (tiled [M, K/32]), col_q [K, ldc]
+    (transposed), col_s (tiled [K, ceil(M/32)]).
+    """
+    lib = L.load()
+    _need_cuda(x)
+    assert x.dtype == torch.bfloat16 and x.dim() == 2 and x.stride(1) == 1
+    M, K = x.shape
+    ldc = ldc or pad_to(M, 16)
+    dev = x.device
+    o = out or {}
+    flags = (L.ROWWISE if rowwise else 0) | (L.COLWISE if colwise else 0)
+    if rowwise:
+        o.setdefault("row_q", torch.empty(M, K, dtype=torch.uint8, device=dev))
+        o.setdefault("row_s", torch.empty(scale_bytes(M, K // 32), dtype=torch.uint8, device=dev))
+    if colwise:
+        o.setdefault("col_q", torch.empty(K, ldc, dtype=torch.uint8, device=dev))
+        o.setdefault("col_s", torch.empty(scale_bytes(K, (M + 31) // 32), dtype=torch.uint8,
+                                          device=dev))
+    st = lib.mpm_mxfp8_quantize(_ptr(x), M, K, x.stride(0), flags, _ptr(o.get("row_q")),
+                                _ptr(o.get("row_s")), _ptr(o.get("col_q")), ldc,
+                                _ptr(o.get("col_s")), _ptr(m_valid), _stream(dev))
+    L.check(st, "mpm_mxfp8_quantize")
+    return o
+
+
+def nvfp4_quantize_per_token(x, amax_in=None, m_valid=None, out=None):
+    """Per-token NVFP4 of bf16 x [M, K]: (q [M, K/2] u8, s tiled [M, K/16] u8,
+    token_scale [M] fp32) from one call."""
+    lib = L.load()
+    _need_cuda(x)
+    assert x.dtype == torch.bfloat16 and x.dim() == 2 and x.stride(1) == 1
+    M, K = x.shape
+    dev = x.device
+    if out is None:
+        out = (torch.empty(M, K // 2, dtype=torch.uint8, device=dev),
+               torch.empty(scale_bytes(M, K // 16), dtype=torch.uint8, device=dev),
+               torch.empty(M, dtype=torch.float32, device=dev))
+    q, s, ts = out
+    st = lib.mpm_nvfp4_quantize_per_token(_ptr(x), M, K, x.stride(0), _ptr(amax_in), _ptr(q),
+                                          _ptr(s), _ptr(ts), _ptr(m_valid), _stream(dev))
+    L.check(st, "mpm_nvfp4_quantize_per_token")
+    return q, s, ts
+
+
+def nvfp4_quantize_weight(parts, out=None, ws=None):
+    """Joint NVFP4 quantisation of per-expert parts [E, rows_p, K] (bf16) with
+    one FP32 outer scale per expert: (q [E, R, K/2], s [E * tiled(R, K/16)],
+    tensor_scale [E])."""
+    lib = L.load()
+    _need_cuda(*parts)
+    E, _, K = parts[0].shape
+    for p in parts:
+        assert p.dtype == torch.bfloat16 and p.is_contiguous() and p.shape[0] == E and p.shape[2] == K
+    R = sum(p.shape[1] for p in parts)
+    dev = parts[0].device
+    if out is None:
+        out = (torch.empty(E, R, K // 2, dtype=torch.uint8, device=dev),
+               torch.empty(E * scale_bytes(R, K // 16), dtype=torch.uint8, device=dev),
+               torch.empty(E, dtype=torch.float32, device=dev))
+    q, s, ts = out
+    wsb = int(lib.mpm_nvfp4_weight_workspace_bytes(E))
+    if ws is None:
+        ws = torch.empty(wsb, dtype=torch.uint8, device=dev)
+    ptrs = (C.c_void_p * len(parts))(*[p.data_ptr() for p in parts])
+    rows = (C.c_int64 * len(parts))(*[p.shape[1] for p in parts])
+    st = lib.mpm_nvfp4_quantize_weight(ptrs, rows, len(parts), K, E, _ptr(q), _ptr(s), _ptr(ts),
+                                       _ptr(ws), ws.numel(), _stream(dev))
+    L.check(st, "mpm_nvfp4_quantize_weight")
+    return q, s, ts
+
+
+# ------------------------------------------------------------------ routing
+
+def moe_row_capacity(T: int, k: int, E: int) -> int:
+    return int(L.load().mpm_moe_row_capacity(T, k, E))
+
+
+def moe_build_segments(topk_ids, topk_prob, E: int, out=None, ws=None):
+    """(seg_offsets [E+1], perm [cap], inv_perm [T*k], row_prob [cap], cap)."""
+    lib = L.load()
+    _need_cuda(topk_ids, topk_prob)
+    assert topk_ids.dtype == torch.int32 and topk_prob.dtype == torch.float32
+    T, k = topk_ids.shape
+    dev = topk_ids.device
+    cap = moe_row_capacity(T, k, E)
+    if out is None:
+        out = (torch.empty(E + 1, dtype=torch.int32, device=dev),
+               torch.empty(cap, dtype=torch.int32, device=dev),
+               torch.empty(T * k, dtype=torch.int32, device=dev),
+               torch.empty(cap, dtype=torch.float32, device=dev))
+    seg, perm, inv, rp = out
+    wsb = int(lib.mpm_moe_segments_workspace_bytes(T, k, E))
+    if ws is None:
+        ws = torch.empty(wsb, dtype=torch.uint8, device=dev)
+    st = lib.mpm_moe_build_segments(_ptr(topk_ids.contiguous()), _ptr(topk_prob.contiguous()), T,
+                                    k, E, _ptr(seg), _ptr(perm), _ptr(inv), _ptr(rp), _ptr(ws),
+                                    ws.numel(), _stream(dev))
+    L.check(st, "mpm_moe_build_segments")
+    return seg, perm, inv, rp, cap
+
+
+def moe_gather_bf16(x, perm, seg, E: int, k: int, cap: int, out=None):
+    lib = L.load()
+    T, K = x.shape
+    if out is None:
+        out = torch.empty(cap, K, dtype=torch.bfloat16, device=x.device)
+    st = lib.mpm_moe_gather(L.GATHER_BF16, _ptr(x), None, None, T, K, k, _ptr(perm), _ptr(seg),
+                            E, cap, _ptr(out), None, None, _stream(x.device))
+    L.check(st, "mpm_moe_gather")
+    return out
+
+
+def moe_gather_nvfp4(q, s, ts, K: int, perm, seg, E: int, k: int, cap: int, out=None):
+    lib = L.load()
+    T = q.shape[0]
+    dev = q.device
+    if out is None:
+        out = (torch.empty(cap, K // 2, dtype=torch.uint8, device=dev),
+               torch.empty(scale_bytes(cap, K // 16), dtype=torch.uint8, device=dev),
+               torch.empty(cap, dtype=torch.float32, device=dev))
+    dq, ds, dts = out
+    st = lib.mpm_moe_gather(L.GATHER_NVFP4, _ptr(q), _ptr(s), _ptr(ts), T, K, k, _ptr(perm),
+                            _ptr(seg), E, cap, _ptr(dq), _ptr(ds), _ptr(dts), _stream(dev))
+    L.check(st, "mpm_moe_gather")
+    return dq, ds, dts
+
+
+def moe_combine(y_perm, inv_perm, T: int, k: int, out=None):
+    lib = L.load()
+    H = y_perm.shape[1]
+    if out is None:
+        out = torch.empty(T, H, dtype=torch.bfloat16, device=y_perm.device)
+    st = lib.mpm_moe_combine(_ptr(y_perm), _ptr(inv_perm), T, k, H, _ptr(out),
+                             _stream(y_perm.device))
+    L.check(st, "mpm_moe_combine")
+    return out
+
+
+# ------------------------------------------------------------------ GEMM
+
+def moe_grouped_gemm(kind, group, epilogue, E, a_rows, N, K, seg, a, b, sfa, sfa_cols, sfb,
+                     sfb_cols, out, b_rows_per_expert=0, b_k_per_expert=0, alpha_a=None,
+                     alpha_b=None, row_prob=None, out2=None, aux=None, amax=None):
+    """One grouped block-scaled GEMM launch (see mpm_grouped_gemm_desc).
+
+    a, b: uint8 code matrices [rows, pitch bytes]; out / out2 / aux: row-major
+    tensors whose row strides become ldo / ldo2 / ld_aux.
+    """
+    lib = L.load()
+    _need_cuda(a, b, sfa, sfb, out)
+    d = L.GroupedGemmDesc()
+    d.kind, d.group, d.epilogue = kind, group, epilogue
+    d.E, d.a_rows, d.N, d.K = E, a_rows, N, K
+    d.seg_dev = None if seg is None else seg.data_ptr()
+    d.a_dev, d.lda_bytes, d.a_total_rows = a.data_ptr(), a.stride(0), a.shape[0]
+    d.b_dev, d.ldb_bytes = b.data_ptr(), b.stride(-2)
+    d.b_total_rows = b.numel() // b.stride(-2)
+    d.b_rows_per_expert, d.b_k_per_expert = b_rows_per_expert, b_k_per_expert
+    d.sfa_dev, d.sfa_cols = sfa.data_ptr(), sfa_cols
+    d.sfb_dev, d.sfb_cols = sfb.data_ptr(), sfb_cols
+    d.alpha_a_dev = None if alpha_a is None else alpha_a.data_ptr()
+    d.alpha_b_dev = None if alpha_b is None else alpha_b.data_ptr()
+    d.row_prob_dev = None if row_prob is None else row_prob.data_ptr()
+    d.out_dev, d.ldo = out.data_ptr(), out.stride(-2)
+    if out2 is not None:
+        d.out2_dev, d.ldo2 = out2.data_ptr(), out2.stride(-2)
+    if aux is not None:
+        d.aux_dev, d.ld_aux = aux.data_ptr(), aux.stride(-2)
+    d.amax_dev = None if amax is None else amax.data_ptr()
+    st = lib.mpm_moe_grouped_gemm(C.byref(d), _stream(a.device))
+    L.check(st, "mpm_moe_grouped_gemm")
+    return out
+
+
+def get_device_status() -> int:
+    lib = L.load()
+    v = C.c_int32(0)
+    L.check(lib.mpm_get_device_status(C.byref(v), _stream()), "mpm_get_device_status")
+    return int(v.value)

@@ -1,0 +1,78 @@
+"""The C-ABI library builds for sm_103a, loads, exports every symbol that
+include/mpm.h declares, and rejects bad arguments on the host before any
+launch (CPU only: none of these calls reaches the GPU)."""
+import ctypes as C
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "mpm.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    names = re.findall(r"\b(mpm_[a-z0-9_]+)\s*\(", src)
+    return sorted(set(names))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from microscaled_precision_moe_gb300 import build, _lib
+    build.build()
+    return _lib.load()
+
+
+def test_every_declared_symbol_is_exported(lib):
+    from microscaled_precision_moe_gb300 import _lib
+    names = _declared()
+    assert len(names) >= 14
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(names) == set(_lib.EXPORTED)
+
+
+def test_pure_host_queries(lib):
+    assert lib.mpm_version() == 100
+    assert lib.mpm_scale_bytes(8288, 64) == 8320 * 64
+    assert lib.mpm_scale_bytes(2048, 259) == 2048 * 260
+    assert lib.mpm_moe_row_capacity(32768, 8, 256) == 262144 + 128 * 256
+    assert lib.mpm_status_string(7) == b"MPM_ERR_DEVICE_BOUNDS"
+
+
+def test_host_validation_rejects_before_launch(lib):
+    from microscaled_precision_moe_gb300 import _lib as L
+    fake = C.c_void_p(0x10000)          # never dereferenced: validation fails first
+    odd = C.c_void_p(0x10008)
+    # NULL input
+    assert lib.mpm_nvfp4_quantize_per_token(None, 4, 64, 64, None, fake, fake, fake, None, None) == 1
+    # K not a multiple of 64 / too large
+    assert lib.mpm_nvfp4_quantize_per_token(fake, 4, 48, 64, None, fake, fake, fake, None, None) == 2
+    assert lib.mpm_nvfp4_quantize_per_token(fake, 4, 16384, 16384, None, fake, fake, fake, None, None) == 2
+    # misaligned input / leading dimension
+    assert lib.mpm_nvfp4_quantize_per_token(odd, 4, 64, 64, None, fake, fake, fake, None, None) == 3
+    assert lib.mpm_nvfp4_quantize_per_token(fake, 4, 64, 68, None, fake, fake, fake, None, None) == 3
+    # MXFP8: no copy requested, K % 32, ldc < M
+    assert lib.mpm_mxfp8_quantize(fake, 4, 64, 64, 0, fake, fake, fake, 16, fake, None, None) == 2
+    assert lib.mpm_mxfp8_quantize(fake, 4, 40, 40, 1, fake, fake, None, 0, None, None, None) == 2
+    assert lib.mpm_mxfp8_quantize(fake, 64, 64, 64, 2, None, None, fake, 32, fake, None, None) == 2
+    # segments: E too large, workspace too small
+    assert lib.mpm_moe_build_segments(fake, fake, 4, 2, 2048, fake, fake, fake, fake, fake, 1 << 20, None) == 2
+    assert lib.mpm_moe_build_segments(fake, fake, 4, 2, 8, fake, fake, fake, fake, fake, 0, None) == 2
+    # GEMM descriptor: bad N, bad K, wgrad on NVFP4
+    d = L.GroupedGemmDesc()
+    d.kind, d.group, d.epilogue, d.E, d.a_rows, d.N, d.K = 0, 0, 0, 1, 128, 200, 256
+    for f in ("a_dev", "b_dev", "sfa_dev", "sfb_dev", "out_dev"):
+        setattr(d, f, 0x10000)
+    d.lda_bytes = d.ldb_bytes = 128
+    d.a_total_rows = d.b_total_rows = 128
+    d.sfa_cols = d.sfb_cols = 16
+    d.ldo = 256
+    assert lib.mpm_moe_grouped_gemm(C.byref(d), None) == 2
+    d.N, d.K = 256, 100
+    assert lib.mpm_moe_grouped_gemm(C.byref(d), None) == 2
+    d.K, d.group = 256, 1
+    d.seg_dev = 0x10000
+    assert lib.mpm_moe_grouped_gemm(C.byref(d), None) == 4
+    assert lib.mpm_moe_grouped_gemm(None, None) == 1

@@ -1,0 +1,185 @@
+"""GPU parity of the quantisers against the oracle: every code and scale byte
+must match (the quantisers are an encoding, so parity is bit-exact)."""
+import numpy as np
+import pytest
+import torch
+
+from oracle import quant as Q
+from oracle import formats as F
+from microscaled_precision_moe_gb300 import synth
+from tests.gpu_util import need_gpu, np_bf16, u8, assert_bytes_equal
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    need_gpu()
+
+
+def _ops():
+    from microscaled_precision_moe_gb300 import ops
+    return ops
+
+
+def _check_nvfp4(x_dev, amax=None, rows=None):
+    ops = _ops()
+    q, s, ts = ops.nvfp4_quantize_per_token(x_dev, amax_in=amax)
+    torch.cuda.synchronize()
+    x = np_bf16(x_dev)
+    M, K = x.shape
+    sel = np.arange(M) if rows is None else np.asarray(rows)
+    a_ref = None if amax is None else amax.cpu().numpy()[sel]
+    rq, rs, rts = Q.nvfp4_quantize_per_token(x[sel], a_ref)
+    assert_bytes_equal(u8(q)[sel], rq, "nvfp4 codes")
+    got_s = Q.unswizzle_scales(u8(s), M, K // 16)[sel]
+    assert_bytes_equal(got_s, rs, "nvfp4 block scales")
+    assert_bytes_equal(ts.cpu().numpy()[sel].view(np.uint32), rts.view(np.uint32), "token scales")
+    if rows is None:
+        # padding bytes of the last tile are zero
+        ref_full = Q.swizzle_scales(rs)
+        assert_bytes_equal(u8(s), ref_full, "nvfp4 tiled scale bytes")
+
+
+def test_nvfp4_single_expert_activation():
+    x, _, _ = synth.single_expert_inputs(device="cuda")
+    _check_nvfp4(x)
+
+
+@pytest.mark.parametrize("M,K", [(1, 64), (5, 128), (129, 768), (300, 2048), (77, 7168), (64, 8192)])
+def test_nvfp4_shapes(M, K):
+    x = synth.normal_bf16(3, 50 + K, (M, K), "cuda", std=2.0, outlier_p=0.01, outlier_mul=100.0)
+    _check_nvfp4(x)
+
+
+def test_nvfp4_strided_input_and_amax_reuse():
+    base = synth.normal_bf16(4, 60, (96, 1024 + 64), "cuda")
+    x = base[:, :1024]
+    amax = x.float().abs().amax(dim=1).contiguous()
+    ops = _ops()
+    q1, s1, t1 = ops.nvfp4_quantize_per_token(x)
+    q2, s2, t2 = ops.nvfp4_quantize_per_token(x, amax_in=amax)
+    torch.cuda.synchronize()
+    assert torch.equal(q1, q2) and torch.equal(s1, s2) and torch.equal(t1, t2)
+    _check_nvfp4(x)
+
+
+def test_nvfp4_extremes():
+    K = 256
+    rows = []
+    rows.append(np.zeros(K))
+    rows.append(np.full(K, F.bf16_bits_to_f32(np.array([0x7F7F], np.uint16))[0]))
+    rows.append(F.bf16_bits_to_f32(np.arange(1, K + 1, dtype=np.uint16) % 127 + 1))
+    neg_small = np.zeros(K)
+    neg_small[0] = 6.0
+    neg_small[1:] = -0.01
+    neg_small[100] = -0.0
+    rows.append(neg_small)
+    one = np.zeros(K)
+    one[40] = -3.0
+    rows.append(one)
+    ties = np.tile(np.array([6.0, 0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0, -0.25, -0.75, -1.25,
+                             -1.75, -2.5, -3.5, -5.0, 0.0]), K // 16)
+    rows.append(ties)
+    x = torch.from_numpy(np.stack(rows).astype(np.float32)).to(torch.bfloat16).cuda()
+    _check_nvfp4(x)
+
+
+def test_nvfp4_activation_large_sample():
+    """The 32768 x 7168 activation of the 671B-shaped layer, on sampled rows,
+    plus the 16384 x 2048 one in full."""
+    s = synth.MOE_671B
+    x = synth.moe_activations(s, device="cuda")
+    rows = np.random.default_rng(0).choice(s.T, 256, replace=False)
+    _check_nvfp4(x, rows=rows)
+    del x
+    x = synth.moe_activations(synth.MOE_30B, device="cuda")
+    _check_nvfp4(x)
+
+
+def test_nvfp4_weight_joint_scale():
+    _, wg, wu = synth.single_expert_inputs(device="cuda")
+    ops = _ops()
+    q, s, ts = ops.nvfp4_quantize_weight([wg[None].contiguous(), wu[None].contiguous()])
+    torch.cuda.synchronize()
+    rq, rs, rts = Q.nvfp4_quantize_joint([np_bf16(wg)[None], np_bf16(wu)[None]], 1)
+    assert_bytes_equal(u8(q), rq, "weight codes")
+    assert_bytes_equal(u8(s), Q.swizzle_scales(rs[0]), "weight scales")
+    assert_bytes_equal(ts.cpu().numpy().view(np.uint32), rts.view(np.uint32), "weight s_g")
+
+
+def test_nvfp4_weight_experts_with_outliers():
+    s = synth.scaled(synth.MOE_671B, H=1024, I=256, E=6)
+    w1, w2 = synth.moe_weights(s, device="cuda")
+    I = s.I
+    ops = _ops()
+    g, u = w1[:, :I].contiguous(), w1[:, I:].contiguous()
+    q, sc, ts = ops.nvfp4_quantize_weight([g, u])
+    q2, sc2, ts2 = ops.nvfp4_quantize_weight([w2])
+    torch.cuda.synchronize()
+    rq, rs, rts = Q.nvfp4_quantize_joint([np_bf16(g), np_bf16(u)], s.E)
+    assert_bytes_equal(u8(q), rq, "W1 codes")
+    per = Q.scale_bytes(2 * I, s.H // 16)
+    for e in range(s.E):
+        assert_bytes_equal(u8(sc)[e * per:(e + 1) * per], Q.swizzle_scales(rs[e]), f"W1 scales e{e}")
+    assert_bytes_equal(ts.cpu().numpy().view(np.uint32), rts.view(np.uint32), "W1 s_g")
+    rq2, rs2, rts2 = Q.nvfp4_quantize_joint([np_bf16(w2)], s.E)
+    assert_bytes_equal(u8(q2), rq2, "W2 codes")
+    assert_bytes_equal(ts2.cpu().numpy().view(np.uint32), rts2.view(np.uint32), "W2 s_g")
+
+
+def _check_mxfp8(x_dev, ldc=None):
+    ops = _ops()
+    o = ops.mxfp8_quantize(x_dev, ldc=ldc)
+    torch.cuda.synchronize()
+    x = np_bf16(x_dev)
+    M, K = x.shape
+    rq, rs = Q.mxfp8_quantize_rowwise(x)
+    assert_bytes_equal(u8(o["row_q"]), rq, "mxfp8 row codes")
+    assert_bytes_equal(u8(o["row_s"]), Q.swizzle_scales(rs), "mxfp8 row scales (tiled, padded)")
+    cq, cs = Q.mxfp8_quantize_colwise(x)
+    assert_bytes_equal(u8(o["col_q"])[:, :M], cq, "mxfp8 col codes")
+    assert_bytes_equal(u8(o["col_s"]), Q.swizzle_scales(cs), "mxfp8 col scales (tiled, padded)")
+
+
+def test_mxfp8_quantizer_workload():
+    """8192 x 2048 activations (1% rows x1e3) plus 32 zero rows, 32 rows of
+    +-448 and 32 rows of bf16 subnormals: both copies byte-exact."""
+    x = synth.mxfp8_quantizer_input(device="cuda")
+    assert x.shape == (8288, 2048)
+    _check_mxfp8(x)
+
+
+@pytest.mark.parametrize("M,K", [(1, 32), (33, 64), (40, 96), (200, 160), (257, 2048)])
+def test_mxfp8_shapes(M, K):
+    x = synth.normal_bf16(5, 70 + K, (M, K), "cuda", std=3.0, outlier_p=0.02, outlier_mul=1e4)
+    _check_mxfp8(x, ldc=((M + 15) // 16) * 16)
+
+
+def test_quantizers_deterministic():
+    x = synth.normal_bf16(6, 80, (512, 2048), "cuda")
+    ops = _ops()
+    a = ops.nvfp4_quantize_per_token(x)
+    b = ops.nvfp4_quantize_per_token(x)
+    m1 = ops.mxfp8_quantize(x)
+    m2 = ops.mxfp8_quantize(x)
+    torch.cuda.synchronize()
+    for u, v in zip(a, b):
+        assert torch.equal(u, v)
+    for k in m1:
+        assert torch.equal(m1[k], m2[k])
+
+
+def test_batch_independence_on_gpu():
+    x = synth.normal_bf16(7, 81, (256, 512), "cuda", std=1.0, outlier_p=0.01, outlier_mul=1e3)
+    perm = torch.randperm(256, generator=torch.Generator().manual_seed(0)).cuda()
+    ops = _ops()
+    q, s, ts = ops.nvfp4_quantize_per_token(x)
+    qp, sp, tsp = ops.nvfp4_quantize_per_token(x[perm].contiguous())
+    q1, s1, ts1 = ops.nvfp4_quantize_per_token(x[17:18].contiguous())
+    torch.cuda.synchronize()
+    assert torch.equal(q[perm], qp) and torch.equal(ts[perm], tsp)
+    assert torch.equal(q[17], q1[0]) and torch.equal(ts[17], ts1[0])
+    S = Q.unswizzle_scales(u8(s), 256, 32)
+    Sp = Q.unswizzle_scales(u8(sp), 256, 32)
+    assert np.array_equal(S[perm.cpu().numpy()], Sp)
