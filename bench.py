@@ -1,0 +1,466 @@
+#!/usr/bin/env python3
+"""Benchmark of the microscaled-precision MoE hot path on one GB300.
+
+Headline step: one NVFP4 expert-layer forward of the 671B-shaped layer
+(32768 tokens, hidden 7168, 256 experts, intermediate 2048, top-8 with
+Zipf(1.1) expert load): per-token activation quantisation, segment build,
+gather, FC1 grouped GEMM + SwiGLU x prob + row amax, re-quantisation reusing
+the amax, FC2 grouped GEMM, combine.  Weights are quantised once, outside the
+step (a weight update is a separate event), and timed separately.
+
+value = algorithmic GEMM FLOPs of the step (real rows, padding excluded) /
+step time, in TFLOP/s.  Inputs are resident in HBM and larger than L2
+(activations 470 MB, FP4 weights 5.6 GB), so no L2 flush is needed.
+Secondary lines (same JSON, key "also"): quantiser GB/s against HBM, the MXFP8
+layer forward+backward on the 30B-shaped layer, the NVFP4 30B-shaped forward.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "quantizer HBM GB/s; NVFP4/MXFP8 grouped-GEMM TFLOPS; % of GB300 roofline"
+NOMINAL_FP4_OVER_BF16 = 13.5 / 2.25      # dense nominal ratio (B300 row of the pages)
+NOMINAL_FP8_OVER_BF16 = 4.5 / 2.25
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return dict(hbm=d["hbm_gbs"], bf16=d["bf16_tflops"], bf16_sus=d["bf16_tflops_sustained"],
+                    src="measured")
+    return dict(hbm=6800.0, bf16=1900.0, bf16_sus=1700.0, src="fallback")
+
+
+# ---------------------------------------------------------------- distributed
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    if ws > 1:
+        import torch.distributed as dist
+        rank = int(os.environ["RANK"])
+        local = int(os.environ.get("LOCAL_RANK", rank))
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+        return dist, rank, ws
+    return None, 0, 1
+
+
+def _barrier(dist):
+    if dist is not None:
+        dist.barrier()
+
+
+def _max_over_ranks(dist, v: float) -> float:
+    if dist is None:
+        return v
+    t = torch.tensor([v], device="cuda", dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi samples (200 ms) during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self._t = threading.Thread(target=self._read, daemon=True)
+            self._t.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in self.lines:
+            f = [x.strip() for x in l.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": float(max(mx)),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- oracle CPU arm
+
+def _oracle_prepare(shape, ids, prob, n_experts=1, seed=0):
+    """Inputs of a bounded CPU sample of the workload: the whole routed row
+    set of n_experts experts of median load (their bf16 activations, their
+    bf16 W1 and W2, the router weights)."""
+    from microscaled_precision_moe_gb300 import synth
+    ids_n = ids.numpy()
+    counts = np.bincount(ids_n.ravel(), minlength=shape.E)
+    order = np.argsort(counts, kind="stable")
+    picks = [int(e) for e in order[len(order) // 2:len(order) // 2 + n_experts]]
+    items = []
+    for e in picks:
+        f = np.flatnonzero(ids_n.ravel() == e)
+        tok = torch.from_numpy(f // shape.k)
+        x = synth.moe_activations(shape, seed, rows=tok).float().numpy()
+        w1, w2 = synth.moe_weights(shape, seed, experts=[e])
+        items.append((e, x, w1.float().numpy()[0], w2.float().numpy()[0],
+                      prob.numpy().ravel()[f]))
+    return items
+
+
+def _oracle_run(shape, items):
+    """The oracle's NVFP4 expert path on the prepared sample: per-token
+    quantisation of the routed rows, joint gate/up and W2 quantisation, fp64
+    FC1, SwiGLU x prob, bf16, row amax, re-quantisation, fp64 FC2.
+    Returns (algorithmic GEMM flops, seconds, description)."""
+    from oracle import quant as Q
+    from oracle import moe as MO
+    from oracle import formats as F
+    I, H = shape.I, shape.H
+    flops, rows = 0, 0
+    t0 = time.perf_counter()
+    for e, x, w1, w2, p in items:
+        qx, sx, tsx = Q.nvfp4_quantize_per_token(x)
+        a = Q.nvfp4_dequantize(qx, sx, tsx)
+        b1 = MO.dequant_weights_nvfp4(Q.nvfp4_quantize_joint([w1[None, :I], w1[None, I:]], 1))[0]
+        b2 = MO.dequant_weights_nvfp4(Q.nvfp4_quantize_joint([w2[None]], 1))[0]
+        with np.errstate(over="ignore"):
+            d = MO.fc1_epilogue(a @ b1.T, p, I)
+        amax = np.max(np.abs(d), axis=1).astype(np.float32)
+        qd, sd, tsd = Q.nvfp4_quantize_per_token(d, amax)
+        F.bf16_round(Q.nvfp4_dequantize(qd, sd, tsd) @ b2.T)
+        n = x.shape[0]
+        rows += n
+        flops += 2 * n * H * 2 * I + 2 * n * I * H
+    secs = time.perf_counter() - t0
+    desc = (f"oracle NVFP4 expert path (numpy, fp64 GEMMs) over every routed row of "
+            f"{len(items)} median-load expert(s): {rows} of {shape.T * shape.k} rows, "
+            f"including their weight quantisation")
+    return flops, secs, desc
+
+
+def _cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count()
+
+
+# ---------------------------------------------------------------- GPU helpers
+
+def _events(n):
+    return [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+
+
+def _time_loop(fn, iters):
+    s, e = _events(2)
+    torch.cuda.synchronize()
+    s.record()
+    for _ in range(iters):
+        fn()
+    e.record()
+    torch.cuda.synchronize()
+    return s.elapsed_time(e) / iters
+
+
+def _quantizer_lines(peak_hbm):
+    """Quantiser throughput with rotating input buffers larger than L2."""
+    from microscaled_precision_moe_gb300 import ops, synth
+    out = {}
+    # MXFP8 quantiser workload: 8288 x 2048 (row + column copies); 8 rotating
+    # copies (8 x 34 MB) so each launch reads from HBM
+    base = synth.mxfp8_quantizer_input(device="cuda")
+    xs = [base.clone() for _ in range(8)]
+    outs = [ops.mxfp8_quantize(x) for x in xs]
+    M, K = base.shape
+    byts = M * K * 2 + 2 * M * K + ops.scale_bytes(M, K // 32) + ops.scale_bytes(K, (M + 31) // 32)
+    for i in range(3):
+        ops.mxfp8_quantize(xs[i], out=outs[i])
+    it = [0]
+
+    def f():
+        j = it[0] % 8
+        ops.mxfp8_quantize(xs[j], out=outs[j])
+        it[0] += 1
+    ms = _time_loop(f, 80)
+    gbs = byts / (ms * 1e-3) / 1e9
+    out["mxfp8_quantize_8288x2048_rowcol"] = {"GB/s": round(gbs, 1), "us": round(ms * 1e3, 2),
+                                              "bytes": byts, "frac_hbm": round(gbs / peak_hbm, 3)}
+    del xs, outs
+    # NVFP4 per-token activation quantiser, 32768 x 7168 (470 MB > L2)
+    x = synth.normal_bf16(0, synth.TID_X, (32768, 7168), "cuda")
+    o = ops.nvfp4_quantize_per_token(x)
+    for _ in range(3):
+        ops.nvfp4_quantize_per_token(x, out=o)
+    ms = _time_loop(lambda: ops.nvfp4_quantize_per_token(x, out=o), 30)
+    byts = x.numel() * 2 + x.numel() // 2 + ops.scale_bytes(32768, 7168 // 16) + 32768 * 4
+    gbs = byts / (ms * 1e-3) / 1e9
+    out["nvfp4_quantize_per_token_32768x7168"] = {"GB/s": round(gbs, 1), "us": round(ms * 1e3, 2),
+                                                  "bytes": byts, "frac_hbm": round(gbs / peak_hbm, 3)}
+    del x, o
+    torch.cuda.empty_cache()
+    return out
+
+
+def _mxfp8_layer_line(peak_fp8, steps=10):
+    from microscaled_precision_moe_gb300 import synth
+    from microscaled_precision_moe_gb300.moe import MXFP8MoE
+    s = synth.MOE_30B_BWD
+    ids, prob = synth.routing(s)
+    x = synth.moe_activations(s, device="cuda")
+    w1, w2 = synth.moe_weights(s, device="cuda")
+    dy = synth.moe_grad_out(s, device="cuda")
+    L = MXFP8MoE(s.T, s.H, s.I, s.E, s.k)
+    idc, prc = ids.cuda(), prob.cuda()
+
+    def step():
+        L.quantize_weights(w1, w2)
+        L.forward(x, idc, prc)
+        L.backward(dy)
+    for _ in range(3):
+        step()
+    ms = _time_loop(step, steps)
+    tf = L.gemm_flops() / (ms * 1e-3) / 1e12
+    r = {"workload": s.name, "ms_per_step": round(ms, 3), "TFLOP/s": round(tf, 1),
+         "frac_fp8_peak": round(tf / peak_fp8, 3),
+         "note": "whole fwd+bwd step (weight quantisation included) / GEMM algorithmic FLOPs"}
+    del L, x, w1, w2, dy
+    torch.cuda.empty_cache()
+    return r
+
+
+def _nvfp4_30b_line(peak_fp4, steps=10):
+    from microscaled_precision_moe_gb300 import synth
+    from microscaled_precision_moe_gb300.moe import NVFP4MoE, NVFP4Weights
+    s = synth.MOE_30B
+    ids, prob = synth.routing(s)
+    x = synth.moe_activations(s, device="cuda")
+    w1, w2 = synth.moe_weights(s, device="cuda")
+    W = NVFP4Weights.quantize(w1, w2)
+    L = NVFP4MoE(s.T, s.H, s.I, s.E, s.k)
+    idc, prc = ids.cuda(), prob.cuda()
+    for _ in range(3):
+        L.forward(x, idc, prc, W)
+    ms = _time_loop(lambda: L.forward(x, idc, prc, W), steps)
+    tf = sum(L.gemm_flops()) / (ms * 1e-3) / 1e12
+    r = {"workload": s.name, "ms_per_step": round(ms, 3), "TFLOP/s": round(tf, 1),
+         "frac_fp4_peak": round(tf / peak_fp4, 3)}
+    del L, W, x, w1, w2
+    torch.cuda.empty_cache()
+    return r
+
+
+# ---------------------------------------------------------------- main
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-also", action="store_true", help="skip the secondary lines")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    from microscaled_precision_moe_gb300 import synth
+    shape = synth.MOE_671B
+    peaks = _peaks()
+    peak_fp4_sus = peaks["bf16_sus"] * NOMINAL_FP4_OVER_BF16
+    peak_fp8_sus = peaks["bf16_sus"] * NOMINAL_FP8_OVER_BF16
+    cfg = {"workload": shape.name, "tokens": shape.T, "hidden": shape.H,
+           "intermediate": shape.I, "experts": shape.E, "top_k": shape.k,
+           "expert_load": "Zipf(1.1) via Gumbel-top-k", "weights": "N(0,0.01), 1e-4 outliers x100",
+           "l2": "no flush: activations 470 MB and FP4 weights 5.6 GB exceed L2"}
+
+    if args.impl == "reference":
+        rank = int(os.environ.get("RANK", "0"))
+        if rank != 0:
+            return 0
+        ids, prob = synth.routing(shape)
+        items = _oracle_prepare(shape, ids, prob, n_experts=1)
+        for _ in range(min(args.warmup, 1)):
+            _oracle_run(shape, items)
+        vals, descs = [], []
+        t_all = time.perf_counter()
+        for _ in range(args.steps):
+            fl, sec, desc = _oracle_run(shape, items)
+            vals.append(fl / sec / 1e12)
+            descs.append(desc)
+        wall = time.perf_counter() - t_all
+        v = float(np.median(vals))
+        line = {"impl": "reference", "metric": METRIC, "value": round(v, 6), "unit": "TFLOP/s",
+                "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+                "ms_per_step": round(wall / args.steps * 1e3, 1), "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+                "config": cfg,
+                "cpu_baseline": {"value": round(v, 6), "unit": "TFLOP/s", "cores": _cores(),
+                                 "kind": "oracle", "sample": descs[0]},
+                "e2e": {"value": round(v, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}}
+        print(json.dumps(line), flush=True)
+        return 0
+
+    dist, rank, world = _dist()
+    dev = torch.cuda.current_device()
+    from microscaled_precision_moe_gb300 import build
+    build.build()
+    from microscaled_precision_moe_gb300 import ops
+    from microscaled_precision_moe_gb300.moe import NVFP4MoE, NVFP4Weights
+
+    # ---- inputs (seeded, synthetic) and weights quantised once
+    ids, prob = synth.routing(shape)
+    x = synth.moe_activations(shape, device="cuda")
+    w1, w2 = synth.moe_weights(shape, device="cuda")
+    torch.cuda.synchronize()
+    W = NVFP4Weights.quantize(w1, w2)
+    for _ in range(2):
+        NVFP4Weights.quantize(w1, w2)
+    t_wq = _time_loop(lambda: NVFP4Weights.quantize(w1, w2), 3)
+    wbytes = (w1.numel() + w2.numel()) * 2.5 + (w1.numel() + w2.numel()) // 16
+    del w1, w2
+    torch.cuda.empty_cache()
+    idc, prc = ids.cuda(), prob.cuda()
+    layer = NVFP4MoE(shape.T, shape.H, shape.I, shape.E, shape.k)
+    fl1, fl2 = layer.gemm_flops()
+    flops = fl1 + fl2
+
+    for _ in range(args.warmup):
+        layer.forward(x, idc, prc, W)
+    torch.cuda.synchronize()
+    assert ops.get_device_status() == 0
+
+    # ---- timed region: K steps, per-stage events on the launching stream
+    nst = len(NVFP4MoE.STAGES) + 1
+    ev = [_events(nst) for _ in range(args.steps)]
+    stream = torch.cuda.current_stream()
+    start, end = _events(2)
+    _barrier(dist)
+    torch.cuda.synchronize()
+    with ClockSampler(dev) as clk:
+        start.record(stream)
+        for i in range(args.steps):
+            evi = ev[i]
+            layer.forward(x, idc, prc, W, mark=lambda j, evi=evi: evi[j].record(stream))
+        end.record(stream)
+        torch.cuda.synchronize()
+        _barrier(dist)
+    ms = start.elapsed_time(end) / args.steps
+    ms = _max_over_ranks(dist, ms)
+    stage_ms = {name: float(np.mean([ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(args.steps)]))
+                for j, name in enumerate(NVFP4MoE.STAGES)}
+    value = world * flops / (ms * 1e-3) / 1e12
+
+    # ---- e2e through the public API: pinned host inputs in, output back out
+    xh = x.cpu().pin_memory()
+    idh, prh = ids.pin_memory(), prob.pin_memory()
+    outh = torch.empty(shape.T, shape.H, dtype=torch.bfloat16).pin_memory()
+    xd = torch.empty_like(x)
+    idd, prd = torch.empty_like(idc), torch.empty_like(prc)
+
+    def e2e_step():
+        xd.copy_(xh, non_blocking=True)
+        idd.copy_(idh, non_blocking=True)
+        prd.copy_(prh, non_blocking=True)
+        out = layer.forward(xd, idd, prd, W)
+        outh.copy_(out, non_blocking=True)
+    for _ in range(2):
+        e2e_step()
+    e2e_ms = _time_loop(e2e_step, max(3, args.steps // 2))
+    h2d = xh.numel() * 2 + idh.numel() * 4 + prh.numel() * 4
+    d2h = outh.numel() * 2
+
+    # ---- roofline of the dominant kernel (FC1 grouped GEMM, tensor bound)
+    fc1_ms = stage_ms["fc1"]
+    ach = fl1 / (fc1_ms * 1e-3) / 1e12
+    roof = {"bound": "tensor", "kernel": "grouped_gemm_kernel<NVFP4, SWIGLU> (FC1)",
+            "achieved": round(ach, 1), "peak": round(peak_fp4_sus, 1), "unit": "TFLOP/s",
+            "frac": round(ach / peak_fp4_sus, 4), "traffic": None,
+            "peak_source": f"{peaks['src']} sustained bf16 x {NOMINAL_FP4_OVER_BF16:g} "
+                           f"(dense FP4/BF16 nominal ratio)",
+            "per_launch_flops": fl1}
+
+    line = {"metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "nvfp4", "data": "synthetic (seeded counter-based generator)",
+            "config": cfg, "parallelism": "replicas" if world > 1 else "single",
+            "clocks": clk.summary(), "roofline": roof,
+            "stage_ms": {k: round(v, 4) for k, v in stage_ms.items()},
+            "gpu_launches": NVFP4MoE.LAUNCHES_PER_FORWARD * args.steps,
+            "e2e": {"value": round(world * flops / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+                    "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+                    "ms_per_step": round(e2e_ms, 4)},
+            "weight_quantize": {"ms": round(t_wq, 3),
+                                "GB/s": round(wbytes / (t_wq * 1e-3) / 1e9, 1)}}
+    del xh, outh, xd, layer, W, x
+    torch.cuda.empty_cache()
+
+    if rank == 0:
+        fl_s, sec_s, desc = _oracle_run(shape, _oracle_prepare(shape, ids, prob, n_experts=3))
+        line["cpu_baseline"] = {"value": round(fl_s / sec_s / 1e12, 6), "unit": "TFLOP/s",
+                                "cores": _cores(), "kind": "oracle", "sample": desc}
+    if not args.no_also:
+        also = {"quantizers": _quantizer_lines(peaks["hbm"])}
+        also["mxfp8_layer_fwd_bwd"] = _mxfp8_layer_line(peak_fp8_sus)
+        also["nvfp4_layer_fwd_30b"] = _nvfp4_30b_line(peak_fp4_sus)
+        also["stage_GBps_or_TFLOPs"] = {
+            "quant_x_GB/s": round((shape.T * shape.H * 2.5625 + shape.T * 4) /
+                                  (stage_ms["quant_x"] * 1e-3) / 1e9, 1),
+            "fc1_TFLOP/s": round(ach, 1),
+            "fc2_TFLOP/s": round(fl2 / (stage_ms["fc2"] * 1e-3) / 1e12, 1)}
+        line["also"] = also
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -198,8 +198,11 @@ mpm_status mpm_moe_build_segments(const int32_t* topk_ids_dev, const float* topk
  * MPM_GATHER_NVFP4: src codes u8 [T, K/2], scales (128x4 tiles of [T, K/16])
  *   and token scales fp32 [T] -> the same three for [capacity] rows
  *   (src_s / dst_s / src_ts / dst_ts used only here).
+ * amax_zero_dev (nullable): fp32 [capacity]; entries of the gathered rows are
+ * set to 0, ready for the row-amax reduction of the FC1 epilogue.
  * Source: "miniTE technical report", section 5.3 (dispatch/permute before the
- * FC1 quantised GEMM).  Requirements: K % 64 == 0.
+ * FC1 quantised GEMM; the padding step handles the activation and its amax
+ * together).  Requirements: K % 64 == 0.
  */
 #define MPM_GATHER_BF16 0
 #define MPM_GATHER_NVFP4 1
@@ -208,7 +211,7 @@ mpm_status mpm_moe_gather(int what, const void* src_dev, const uint8_t* src_s_de
                           const int32_t* perm_dev, const int32_t* seg_offsets_dev,
                           int64_t E, int64_t capacity,
                           void* dst_dev, uint8_t* dst_s_dev, float* dst_ts_dev,
-                          cudaStream_t stream);
+                          float* amax_zero_dev, cudaStream_t stream);
 
 /*
  * out[t] = sum over j = 0..k-1 (in that order, fp32) of y_perm[inv_perm[t*k+j]],

@@ -58,7 +58,7 @@ _SIGS = {
     "mpm_moe_segments_workspace_bytes": (_sz, [_i64, _int, _i64]),
     "mpm_moe_build_segments": (_int, [_vp, _vp, _i64, _int, _i64, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
     "mpm_moe_gather": (_int, [_int, _vp, _vp, _vp, _i64, _i64, _int, _vp, _vp, _i64, _i64,
-                              _vp, _vp, _vp, _vp]),
+                              _vp, _vp, _vp, _vp, _vp]),
     "mpm_moe_combine": (_int, [_vp, _vp, _i64, _int, _i64, _vp, _vp]),
     "mpm_moe_grouped_gemm": (_int, [C.POINTER(GroupedGemmDesc), _vp]),
     "mpm_get_device_status": (_int, [C.POINTER(C.c_int32), _vp]),

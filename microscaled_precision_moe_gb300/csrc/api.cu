@@ -181,7 +181,7 @@ mpm_status mpm_moe_build_segments(const int32_t* ids, const float* prob, int64_t
 mpm_status mpm_moe_gather(int what, const void* src, const uint8_t* src_s, const float* src_ts,
                           int64_t T, int64_t K, int k, const int32_t* perm, const int32_t* seg,
                           int64_t E, int64_t capacity, void* dst, uint8_t* dst_s,
-                          float* dst_ts, cudaStream_t stream) {
+                          float* dst_ts, float* amax_zero, cudaStream_t stream) {
   if (!src || !perm || !seg || !dst) return MPM_ERR_NULL;
   if (what != MPM_GATHER_BF16 && what != MPM_GATHER_NVFP4) return MPM_ERR_UNSUPPORTED;
   if (T < 1 || K < 64 || K % 64 != 0 || k < 1 || E < 1 || capacity < 1) return MPM_ERR_SHAPE;
@@ -190,8 +190,9 @@ mpm_status mpm_moe_gather(int what, const void* src, const uint8_t* src_s, const
     if (!aligned(src_s, 4) || !aligned(dst_s, 4)) return MPM_ERR_ALIGN;
   }
   if (!aligned(src, 16) || !aligned(dst, 16)) return MPM_ERR_ALIGN;
+  if (amax_zero && !aligned(amax_zero, 4)) return MPM_ERR_ALIGN;
   return cuda_status(mpm::launch_gather(what, src, src_s, src_ts, K, k, perm, seg + E, capacity,
-                                        dst, dst_s, dst_ts, stream));
+                                        dst, dst_s, dst_ts, amax_zero, stream));
 }
 
 mpm_status mpm_moe_combine(const void* y, const int32_t* inv, int64_t T, int k, int64_t H,

@@ -107,12 +107,13 @@ __global__ void __launch_bounds__(32) seg_scatter_kernel(const int* ids, const f
 __global__ void __launch_bounds__(256) gather_bf16_kernel(const uint4* src, long long K8,
                                                          int k, const int* perm,
                                                          const int* seg_end, long long cap,
-                                                         uint4* dst) {
+                                                         uint4* dst, float* amax_zero) {
   const long long row = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   long long rend = *seg_end;
   if (rend > cap) rend = cap;
   if (row >= rend) return;
+  if (amax_zero && lane == 0) amax_zero[row] = 0.0f;
   const int f = perm[row];
   uint4* d = dst + row * K8;
   if (f < 0) {
@@ -130,12 +131,13 @@ __global__ void __launch_bounds__(256) gather_nvfp4_kernel(const uint4* src_q, c
                                                           int k, const int* perm,
                                                           const int* seg_end, long long cap,
                                                           uint4* dst_q, uint8_t* dst_s,
-                                                          float* dst_ts) {
+                                                          float* dst_ts, float* amax_zero) {
   const long long row = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   long long rend = *seg_end;
   if (rend > cap) rend = cap;
   if (row >= rend) return;
+  if (amax_zero && lane == 0) amax_zero[row] = 0.0f;
   const int f = perm[row];
   const long long q16 = K / 32;          // uint4 chunks of packed codes per row
   const long long cols = K / 16, cpad = cols;   // K % 64 == 0
@@ -216,15 +218,15 @@ cudaError_t launch_build_segments(const int* ids, const float* prob, long long T
 cudaError_t launch_gather(int what, const void* src, const uint8_t* src_s, const float* src_ts,
                           long long K, int k, const int* perm, const int* seg_end,
                           long long cap, void* dst, uint8_t* dst_s, float* dst_ts,
-                          cudaStream_t s) {
+                          float* amax_zero, cudaStream_t s) {
   const unsigned grid = (unsigned)((cap + 7) / 8);
   if (what == MPM_GATHER_BF16) {
     gather_bf16_kernel<<<grid, 256, 0, s>>>(static_cast<const uint4*>(src), K / 8, k, perm,
-                                            seg_end, cap, static_cast<uint4*>(dst));
+                                            seg_end, cap, static_cast<uint4*>(dst), amax_zero);
   } else {
     gather_nvfp4_kernel<<<grid, 256, 0, s>>>(static_cast<const uint4*>(src), src_s, src_ts, K,
                                              k, perm, seg_end, cap, static_cast<uint4*>(dst),
-                                             dst_s, dst_ts);
+                                             dst_s, dst_ts, amax_zero);
   }
   return cudaGetLastError();
 }

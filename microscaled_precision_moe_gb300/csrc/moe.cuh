@@ -11,7 +11,7 @@ cudaError_t launch_build_segments(const int* ids, const float* prob, long long T
 cudaError_t launch_gather(int what, const void* src, const uint8_t* src_s, const float* src_ts,
                           long long K, int k, const int* perm, const int* seg_end,
                           long long cap, void* dst, uint8_t* dst_s, float* dst_ts,
-                          cudaStream_t s);
+                          float* amax_zero, cudaStream_t s);
 cudaError_t launch_combine(const void* y, const int* inv, long long T, int k, long long H,
                            void* out, cudaStream_t s);
 }  // namespace mpm

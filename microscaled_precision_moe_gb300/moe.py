@@ -1,0 +1,228 @@
+"""MoE expert layer on the libmpm kernels: NVFP4 forward, MXFP8 forward+backward.
+
+Every step of both paths runs in the library's CUDA kernels; this module only
+owns the buffers (allocated once per shape, reused every step) and sequences
+the calls on the current stream.  No host synchronisation happens inside a
+step: expert offsets stay on the device.
+
+NVFP4 forward ("miniTE technical report", sections 5.2-5.4; "Towards
+Blackwell-native 8-bit and 4-bit RL", section "Per-token activation
+scaling"):
+  X --per-token NVFP4--> (q, s, ts) --gather by expert--> A
+  A x W1[e]^T  (gate|up)  --epilogue: alpha, SwiGLU x prob, row amax--> D (bf16)
+  D --per-token NVFP4 reusing the amax--> A2
+  A2 x W2[e]^T --epilogue: alpha--> Y_perm (bf16) --combine--> out (bf16)
+
+MXFP8 forward + backward ("Towards Blackwell-native 8-bit and 4-bit RL",
+section "Recipe 1 / Training"): every GEMM operand is quantised from bf16;
+fprop uses row-wise copies, dgrad the row-wise gradient and the column-wise
+weight copy, wgrad the column-wise gradient and activation copies.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+
+import torch
+
+from . import _lib as L
+from . import ops
+
+
+def _sb(rows, cols):
+    return ops.scale_bytes(rows, cols)
+
+
+# ============================================================================
+# NVFP4
+# ============================================================================
+
+@dataclass
+class NVFP4Weights:
+    """Quantised expert weights: W1 = gate|up [E, 2I, H/2] with one outer scale
+    per expert shared by gate and up, W2 [E, H, I/2]."""
+    w1_q: torch.Tensor
+    w1_s: torch.Tensor
+    w1_ts: torch.Tensor
+    w2_q: torch.Tensor
+    w2_s: torch.Tensor
+    w2_ts: torch.Tensor
+    E: int
+    H: int
+    I: int
+
+    @staticmethod
+    def quantize(w1: torch.Tensor, w2: torch.Tensor) -> "NVFP4Weights":
+        E, I2, H = w1.shape
+        I = I2 // 2
+        # W1 [E, 2I, H] already holds each expert's gate rows then up rows, so
+        # one part of 2I rows per expert gives the joint gate/up scale
+        q1, s1, t1 = ops.nvfp4_quantize_weight([w1.contiguous()])
+        q2, s2, t2 = ops.nvfp4_quantize_weight([w2.contiguous()])
+        return NVFP4Weights(q1, s1, t1, q2, s2, t2, E, H, I)
+
+
+class NVFP4MoE:
+    """Buffers and launch sequence of the NVFP4 expert-layer forward for a
+    fixed (T, H, I, E, k)."""
+
+    def __init__(self, T, H, I, E, k, device="cuda"):
+        self.T, self.H, self.I, self.E, self.k = T, H, I, E, k
+        dev = torch.device(device)
+        cap = ops.moe_row_capacity(T, k, E)
+        self.cap = cap
+        u8, f32, bf = torch.uint8, torch.float32, torch.bfloat16
+        e = lambda *s, dtype: torch.empty(*s, dtype=dtype, device=dev)
+        self.xq = (e(T, H // 2, dtype=u8), e(_sb(T, H // 16), dtype=u8), e(T, dtype=f32))
+        self.seg = (e(E + 1, dtype=torch.int32), e(cap, dtype=torch.int32),
+                    e(T * k, dtype=torch.int32), e(cap, dtype=f32))
+        self.seg_ws = e(int(L.load().mpm_moe_segments_workspace_bytes(T, k, E)), dtype=u8)
+        self.aq = (e(cap, H // 2, dtype=u8), e(_sb(cap, H // 16), dtype=u8), e(cap, dtype=f32))
+        self.d = e(cap, I, dtype=bf)
+        self.amax = e(cap, dtype=f32)
+        self.dq = (e(cap, I // 2, dtype=u8), e(_sb(cap, I // 16), dtype=u8), e(cap, dtype=f32))
+        self.y = e(cap, H, dtype=bf)
+        self.out = e(T, H, dtype=bf)
+
+    # each call below is one or more library launches on the current stream
+    STAGES = ("quant_x", "segments", "gather", "fc1", "quant_d", "fc2", "combine")
+
+    def forward(self, x, topk_ids, topk_prob, w: NVFP4Weights, mark=None):
+        """out [T, H] bf16.  ``mark(i)`` (optional) is called before stage i
+        of STAGES and once more at the end (used to record CUDA events)."""
+        T, H, I, E, k, cap = self.T, self.H, self.I, self.E, self.k, self.cap
+        mark = mark or (lambda i: None)
+        mark(0)
+        ops.nvfp4_quantize_per_token(x, out=self.xq)
+        seg, perm, inv, rp = self.seg
+        mark(1)
+        ops.moe_build_segments(topk_ids, topk_prob, E, out=self.seg, ws=self.seg_ws)
+        mark(2)
+        ops.moe_gather_nvfp4(*self.xq, H, perm, seg, E, k, cap, out=self.aq, amax_zero=self.amax)
+        aq, as_, ats = self.aq
+        mark(3)
+        ops.moe_grouped_gemm(L.KIND_NVFP4, L.GROUP_M, L.EPI_SWIGLU, E, cap, 2 * I, H, seg,
+                             aq, w.w1_q.view(E * 2 * I, H // 2), as_, H // 16, w.w1_s, H // 16,
+                             self.d, b_rows_per_expert=2 * I, alpha_a=ats, alpha_b=w.w1_ts,
+                             row_prob=rp, out2=self.d, amax=self.amax)
+        mark(4)
+        ops.nvfp4_quantize_per_token(self.d, amax_in=self.amax, m_valid=seg[E:], out=self.dq)
+        dq, ds, dts = self.dq
+        mark(5)
+        ops.moe_grouped_gemm(L.KIND_NVFP4, L.GROUP_M, L.EPI_BF16, E, cap, H, I, seg,
+                             dq, w.w2_q.view(E * H, I // 2), ds, I // 16, w.w2_s, I // 16,
+                             self.y, b_rows_per_expert=H, alpha_a=dts, alpha_b=w.w2_ts)
+        mark(6)
+        ops.moe_combine(self.y, inv, T, k, out=self.out)
+        mark(7)
+        return self.out
+
+    # kernels launched by one forward: quantiser, 3 segment kernels, gather,
+    # FC1, quantiser, FC2, combine
+    LAUNCHES_PER_FORWARD = 9
+
+    def gemm_flops(self):
+        """Algorithmic FLOPs of the two GEMMs over real (unpadded) rows:
+        (FC1, FC2)."""
+        R = self.T * self.k
+        return 2 * R * self.H * 2 * self.I, 2 * R * self.I * self.H
+
+
+# ============================================================================
+# MXFP8
+# ============================================================================
+
+class MXFP8MoE:
+    """Buffers and launch sequence of the MXFP8 expert layer, forward and
+    backward, for a fixed (T, H, I, E, k)."""
+
+    def __init__(self, T, H, I, E, k, device="cuda"):
+        self.T, self.H, self.I, self.E, self.k = T, H, I, E, k
+        dev = torch.device(device)
+        cap = ops.moe_row_capacity(T, k, E)
+        self.cap = cap
+        u8, f32, bf = torch.uint8, torch.float32, torch.bfloat16
+        e = lambda *s, dtype: torch.empty(*s, dtype=dtype, device=dev)
+
+        def mx(M, K, row=True, col=True):
+            o = {}
+            if row:
+                o["row_q"] = e(M, K, dtype=u8)
+                o["row_s"] = e(_sb(M, K // 32), dtype=u8)
+            if col:
+                o["col_q"] = e(K, M, dtype=u8)
+                o["col_s"] = e(_sb(K, (M + 31) // 32), dtype=u8)
+            return o
+
+        self.seg = (e(E + 1, dtype=torch.int32), e(cap, dtype=torch.int32),
+                    e(T * k, dtype=torch.int32), e(cap, dtype=f32))
+        self.seg_ws = e(int(L.load().mpm_moe_segments_workspace_bytes(T, k, E)), dtype=u8)
+        self.w1 = mx(E * 2 * I, H)
+        self.w2 = mx(E * H, I)
+        self.xp = e(cap, H, dtype=bf)
+        self.xq = mx(cap, H)
+        self.c1 = e(cap, 2 * I, dtype=bf)
+        self.d = e(cap, I, dtype=bf)
+        self.dq = mx(cap, I)
+        self.y = e(cap, H, dtype=bf)
+        self.out = e(T, H, dtype=bf)
+        self.dyp = e(cap, H, dtype=bf)
+        self.dyq = mx(cap, H)
+        self.dh = e(cap, 2 * I, dtype=bf)
+        self.dhq = mx(cap, 2 * I)
+        self.dxp = e(cap, H, dtype=bf)
+        self.dx = e(T, H, dtype=bf)
+        self.dw1 = e(E, 2 * I, H, dtype=f32)
+        self.dw2 = e(E, H, I, dtype=f32)
+
+    def quantize_weights(self, w1, w2):
+        E, H, I = self.E, self.H, self.I
+        ops.mxfp8_quantize(w1.reshape(E * 2 * I, H), ldc=E * 2 * I, out=self.w1)
+        ops.mxfp8_quantize(w2.reshape(E * H, I), ldc=E * H, out=self.w2)
+
+    def forward(self, x, topk_ids, topk_prob):
+        T, H, I, E, k, cap = self.T, self.H, self.I, self.E, self.k, self.cap
+        seg, perm, inv, rp = self.seg
+        ops.moe_build_segments(topk_ids, topk_prob, E, out=self.seg, ws=self.seg_ws)
+        ops.moe_gather_bf16(x, perm, seg, E, k, cap, out=self.xp)
+        ops.mxfp8_quantize(self.xp, ldc=cap, m_valid=seg[E:], out=self.xq)
+        ops.moe_grouped_gemm(L.KIND_MXFP8, L.GROUP_M, L.EPI_SWIGLU_SAVE, E, cap, 2 * I, H, seg,
+                             self.xq["row_q"], self.w1["row_q"], self.xq["row_s"], H // 32,
+                             self.w1["row_s"], H // 32, self.c1, b_rows_per_expert=2 * I,
+                             row_prob=rp, out2=self.d)
+        ops.mxfp8_quantize(self.d, ldc=cap, m_valid=seg[E:], out=self.dq)
+        ops.moe_grouped_gemm(L.KIND_MXFP8, L.GROUP_M, L.EPI_BF16, E, cap, H, I, seg,
+                             self.dq["row_q"], self.w2["row_q"], self.dq["row_s"], I // 32,
+                             self.w2["row_s"], I // 32, self.y, b_rows_per_expert=H)
+        ops.moe_combine(self.y, inv, T, k, out=self.out)
+        return self.out
+
+    def backward(self, dy):
+        T, H, I, E, k, cap = self.T, self.H, self.I, self.E, self.k, self.cap
+        seg, perm, inv, rp = self.seg
+        ops.moe_gather_bf16(dy, perm, seg, E, k, cap, out=self.dyp)
+        ops.mxfp8_quantize(self.dyp, ldc=cap, m_valid=seg[E:], out=self.dyq)
+        # FC2 dgrad with the SwiGLU backward fused: dH = [dg | du]
+        ops.moe_grouped_gemm(L.KIND_MXFP8, L.GROUP_M, L.EPI_DSWIGLU, E, cap, I, H, seg,
+                             self.dyq["row_q"], self.w2["col_q"], self.dyq["row_s"], H // 32,
+                             self.w2["col_s"], (E * H) // 32, self.dh, b_rows_per_expert=0,
+                             b_k_per_expert=H, row_prob=rp, aux=self.c1)
+        # FC2 wgrad: dW2[e] = dY_e^T . D_e
+        ops.moe_grouped_gemm(L.KIND_MXFP8, L.GROUP_K, L.EPI_F32, E, H, I, 0, seg,
+                             self.dyq["col_q"], self.dq["col_q"], self.dyq["col_s"], cap // 32,
+                             self.dq["col_s"], cap // 32, self.dw2)
+        ops.mxfp8_quantize(self.dh, ldc=cap, m_valid=seg[E:], out=self.dhq)
+        # FC1 dgrad: dX_perm = dH . W1_e (column-wise W1 copy)
+        ops.moe_grouped_gemm(L.KIND_MXFP8, L.GROUP_M, L.EPI_BF16, E, cap, H, 2 * I, seg,
+                             self.dhq["row_q"], self.w1["col_q"], self.dhq["row_s"], (2 * I) // 32,
+                             self.w1["col_s"], (E * 2 * I) // 32, self.dxp, b_rows_per_expert=0,
+                             b_k_per_expert=2 * I)
+        ops.moe_combine(self.dxp, inv, T, k, out=self.dx)
+        # FC1 wgrad: dW1[e] = dH_e^T . X_e
+        ops.moe_grouped_gemm(L.KIND_MXFP8, L.GROUP_K, L.EPI_F32, E, 2 * I, H, 0, seg,
+                             self.dhq["col_q"], self.xq["col_q"], self.dhq["col_s"], cap // 32,
+                             self.xq["col_s"], cap // 32, self.dw1)
+        return self.dx, self.dw1, self.dw2
+
+    def gemm_flops(self):
+        R = self.T * self.k
+        return 3 * (2 * R * self.H * 2 * self.I + 2 * R * self.I * self.H)

@@ -141,18 +141,19 @@ def moe_build_segments(topk_ids, topk_prob, E: int, out=None, ws=None):
     return seg, perm, inv, rp, cap
 
 
-def moe_gather_bf16(x, perm, seg, E: int, k: int, cap: int, out=None):
+def moe_gather_bf16(x, perm, seg, E: int, k: int, cap: int, out=None, amax_zero=None):
     lib = L.load()
     T, K = x.shape
     if out is None:
         out = torch.empty(cap, K, dtype=torch.bfloat16, device=x.device)
     st = lib.mpm_moe_gather(L.GATHER_BF16, _ptr(x), None, None, T, K, k, _ptr(perm), _ptr(seg),
-                            E, cap, _ptr(out), None, None, _stream(x.device))
+                            E, cap, _ptr(out), None, None, _ptr(amax_zero), _stream(x.device))
     L.check(st, "mpm_moe_gather")
     return out
 
 
-def moe_gather_nvfp4(q, s, ts, K: int, perm, seg, E: int, k: int, cap: int, out=None):
+def moe_gather_nvfp4(q, s, ts, K: int, perm, seg, E: int, k: int, cap: int, out=None,
+                     amax_zero=None):
     lib = L.load()
     T = q.shape[0]
     dev = q.device
@@ -162,7 +163,8 @@ def moe_gather_nvfp4(q, s, ts, K: int, perm, seg, E: int, k: int, cap: int, out=
                torch.empty(cap, dtype=torch.float32, device=dev))
     dq, ds, dts = out
     st = lib.mpm_moe_gather(L.GATHER_NVFP4, _ptr(q), _ptr(s), _ptr(ts), T, K, k, _ptr(perm),
-                            _ptr(seg), E, cap, _ptr(dq), _ptr(ds), _ptr(dts), _stream(dev))
+                            _ptr(seg), E, cap, _ptr(dq), _ptr(ds), _ptr(dts), _ptr(amax_zero),
+                            _stream(dev))
     L.check(st, "mpm_moe_gather")
     return dq, ds, dts
 

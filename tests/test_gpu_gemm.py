@@ -63,17 +63,54 @@ def _grouped_nvfp4_setup(shape, seed=0):
     return ids, prob, x, w1, w2, seg, perm, inv, rp, cap
 
 
+def _chained_compare(d_gpu, y_gpu, out_gpu, r, k, what):
+    """Compare a chained FC1 -> re-quantise -> FC2 -> combine result.
+
+    The FP4 re-quantisation of D is discontinuous: where the kernel's fp32
+    accumulation rounds an element of D to a neighbouring bf16 value (the
+    oracle accumulates exactly in fp64), the row's codes or its amax, and so
+    its outer scale, can change.  So: D itself meets the GEMM tolerance and
+    differs from the oracle's D by at most one bf16 step per element in a
+    small fraction of elements; rows of D that are bit-identical give
+    bit-identical FP4 operands (the quantiser is byte-exact), so their Y rows
+    and the outputs of tokens whose rows all match must meet the GEMM
+    tolerance; every row stays within the NVFP4 re-quantisation noise."""
+    R = int(r["seg"][-1])
+    d = d_gpu[:R]
+    _assert_close(d, r["d"], f"{what}: FC1 SwiGLU D")
+    diff = d != r["d"]
+    # one bf16 step of the reference, or an absolute floor for values that
+    # come out of cancellation in the K-long accumulation
+    ulp = np.abs(r["d"]) * 2.0 ** -7
+    floor = 1e-4 * np.max(np.abs(r["d"]))
+    assert np.all(np.abs(d - r["d"]) <= np.maximum(ulp, floor)), f"{what}: D beyond one step"
+    assert diff.mean() < 1e-3, f"{what}: {diff.mean():.2e} of D elements differ"
+    same = ~diff.any(axis=1)
+    assert same.mean() > 0.9, f"{what}: only {same.mean():.3f} of D rows bit-identical"
+    y = y_gpu[:R]
+    _assert_close(y[same], r["y"][same], f"{what}: FC2 rows with identical operands")
+    if (~same).any():
+        rel = np.linalg.norm(y[~same] - r["y"][~same]) / np.linalg.norm(r["y"][~same])
+        assert rel < 0.1, f"{what}: re-quantised rows differ by {rel:.3e}"
+    rows_ok = np.ones(R, dtype=bool)
+    rows_ok[~same] = False
+    inv = r["inv"].reshape(-1, k)
+    tok_ok = rows_ok[inv].all(axis=1)
+    _assert_close(out_gpu[tok_ok], r["out"][tok_ok], f"{what}: output of unaffected tokens")
+    assert Mx.rel_frobenius(out_gpu, r["out"]) < 1e-2, f"{what}: layer output"
+
+
 def test_nvfp4_grouped_fc1_swiglu_and_fc2():
     shape = synth.scaled(synth.MOE_30B, T=300, H=512, I=256, E=6, k=4)
     ops, L = _ops(), _L()
     ids, prob, x, w1, w2, seg, perm, inv, rp, cap = _grouped_nvfp4_setup(shape)
     E, H, I, k = shape.E, shape.H, shape.I, shape.k
     qx, sx, tsx = ops.nvfp4_quantize_per_token(x)
-    aq, as_, ats = ops.moe_gather_nvfp4(qx, sx, tsx, H, perm, seg, E, k, cap)
+    amax = torch.full((cap,), 7.0, dtype=torch.float32, device="cuda")    # gather zeroes it
+    aq, as_, ats = ops.moe_gather_nvfp4(qx, sx, tsx, H, perm, seg, E, k, cap, amax_zero=amax)
     q1, s1, t1 = ops.nvfp4_quantize_weight([w1[:, :I].contiguous(), w1[:, I:].contiguous()])
     q2, s2, t2 = ops.nvfp4_quantize_weight([w2])
     d = torch.empty(cap, I, dtype=torch.bfloat16, device="cuda")
-    amax = torch.zeros(cap, dtype=torch.float32, device="cuda")
     ops.moe_grouped_gemm(L.KIND_NVFP4, L.GROUP_M, L.EPI_SWIGLU, E, cap, 2 * I, H, seg,
                          aq, q1.view(E * 2 * I, H // 2), as_, H // 16, s1, H // 16, d,
                          b_rows_per_expert=2 * I, alpha_a=ats, alpha_b=t1, row_prob=rp,
@@ -90,11 +127,54 @@ def test_nvfp4_grouped_fc1_swiglu_and_fc2():
         r = MO.nvfp4_moe_forward(np_bf16(x), ids.numpy(), prob.numpy(), np_bf16(w1),
                                  np_bf16(w2), E)
     R = int(r["seg"][-1])
-    _assert_close(np_bf16(d)[:R], r["d"], "FC1 SwiGLU D")
     amax_ref = np.max(np.abs(np_bf16(d)[:R]), axis=1)
     assert np.array_equal(amax.cpu().numpy()[:R], amax_ref), "amax(D) equals the row max of D"
-    _assert_close(np_bf16(y)[:R], r["y"], "FC2 Y_perm")
-    _assert_close(np_bf16(out), r["out"], "layer output")
+    _chained_compare(np_bf16(d), np_bf16(y), np_bf16(out), r, k, "NVFP4 layer")
+
+
+def test_nvfp4_fc2_on_identical_operands():
+    """FC2 alone: the same seeded bf16 D quantised by both sides (byte-exact),
+    then the grouped GEMM against the fp64 GEMM: strict tolerance."""
+    shape = synth.scaled(synth.MOE_30B, T=400, H=768, I=512, E=5, k=3)
+    ops, L = _ops(), _L()
+    ids, prob, x, w1, w2, seg, perm, inv, rp, cap = _grouped_nvfp4_setup(shape, seed=2)
+    E, H, I = shape.E, shape.H, shape.I
+    dsrc = synth.normal_bf16(2, 77, (cap, I), "cuda", std=0.05, outlier_p=1e-3, outlier_mul=20.0)
+    qd, sd, tsd = ops.nvfp4_quantize_per_token(dsrc)
+    q2, s2, t2 = ops.nvfp4_quantize_weight([w2])
+    y = torch.empty(cap, H, dtype=torch.bfloat16, device="cuda")
+    ops.moe_grouped_gemm(L.KIND_NVFP4, L.GROUP_M, L.EPI_BF16, E, cap, H, I, seg,
+                         qd, q2.view(E * H, I // 2), sd, I // 16, s2, I // 16, y,
+                         b_rows_per_expert=H, alpha_a=tsd, alpha_b=t2)
+    torch.cuda.synchronize()
+    segn = seg.cpu().numpy()
+    R = int(segn[-1])
+    dn = np_bf16(dsrc)[:R]
+    rq, rs, rts = Q.nvfp4_quantize_per_token(dn)
+    a = Q.nvfp4_dequantize(rq, rs, rts)
+    w2q = Q.nvfp4_quantize_joint([np_bf16(w2)], E)
+    b = MO.dequant_weights_nvfp4(w2q)
+    ref = F.bf16_round(MO.grouped_gemm(a, b, segn))
+    _assert_close(np_bf16(y)[:R], ref, "NVFP4 FC2 (identical operands)")
+
+
+def test_nvfp4_layer_api():
+    """The public layer API (NVFP4MoE) on a reduced 30B-A3B-shaped layer."""
+    from microscaled_precision_moe_gb300.moe import NVFP4MoE, NVFP4Weights
+    shape = synth.scaled(synth.MOE_30B, T=512, H=1024, I=256, E=16)
+    ids, prob = synth.routing(shape)
+    x = synth.moe_activations(shape, device="cuda")
+    w1, w2 = synth.moe_weights(shape, device="cuda")
+    layer = NVFP4MoE(shape.T, shape.H, shape.I, shape.E, shape.k)
+    w = NVFP4Weights.quantize(w1, w2)
+    out = layer.forward(x, ids.cuda(), prob.cuda(), w).clone()
+    out2 = layer.forward(x, ids.cuda(), prob.cuda(), w)
+    torch.cuda.synchronize()
+    assert torch.equal(out, out2), "deterministic"
+    with np.errstate(over="ignore"):
+        r = MO.nvfp4_moe_forward(np_bf16(x), ids.numpy(), prob.numpy(), np_bf16(w1),
+                                 np_bf16(w2), shape.E)
+    _chained_compare(np_bf16(layer.d), np_bf16(layer.y), np_bf16(out), r, shape.k, "NVFP4MoE")
 
 
 def test_mxfp8_grouped_fprop_dgrad_wgrad():
@@ -142,3 +222,38 @@ def test_mxfp8_grouped_fprop_dgrad_wgrad():
                   "MXFP8 dgrad")
     ref_dw = MO.grouped_wgrad(MO.mx_cols_t(gyn), MO.mx_cols_t(xpn), segn)
     _assert_close(dw.cpu().numpy(), ref_dw, "MXFP8 wgrad")
+
+
+def test_mxfp8_layer_fwd_bwd_api():
+    """The MXFP8 layer (forward and backward) through MXFP8MoE against the
+    oracle.  FC1's outputs (C = gate|up, D) come from identical operands and
+    meet the GEMM tolerance; later stages consume re-quantised tensors, so a
+    one-step bf16 difference upstream can move an E4M3 code: their bound is
+    the same GEMM tolerance (measured errors are near 1e-5)."""
+    from microscaled_precision_moe_gb300.moe import MXFP8MoE
+    shape = synth.scaled(synth.MOE_30B_BWD, T=384, H=512, I=256, E=8, k=4)
+    ids, prob = synth.routing(shape)
+    x = synth.moe_activations(shape, device="cuda")
+    w1, w2 = synth.moe_weights(shape, device="cuda")
+    dy = synth.moe_grad_out(shape, device="cuda")
+    layer = MXFP8MoE(shape.T, shape.H, shape.I, shape.E, shape.k)
+    layer.quantize_weights(w1, w2)
+    out = layer.forward(x, ids.cuda(), prob.cuda())
+    dx, dw1, dw2 = layer.backward(dy)
+    torch.cuda.synchronize()
+    from microscaled_precision_moe_gb300 import ops
+    assert ops.get_device_status() == 0
+    with np.errstate(over="ignore"):
+        r = MO.mxfp8_moe_fwd_bwd(np_bf16(x), ids.numpy(), prob.numpy(), np_bf16(w1),
+                                 np_bf16(w2), np_bf16(dy), shape.E)
+    R = int(r["seg"][-1])
+    _assert_close(np_bf16(layer.c1)[:R], r["c1"], "MXFP8 FC1 C")
+    _assert_close(np_bf16(layer.d)[:R], r["d"], "MXFP8 FC1 D")
+    report = {}
+    for name, got, ref in [("out", np_bf16(out), r["out"]), ("dh", np_bf16(layer.dh)[:R], r["dh"]),
+                           ("dx", np_bf16(dx), r["dx"]), ("dw1", dw1.cpu().numpy(), r["dw1"]),
+                           ("dw2", dw2.cpu().numpy(), r["dw2"])]:
+        ok, rf, mx, bound = Mx.within_gemm_tolerance(got, ref, REL, ELEM)
+        report[name] = (rf, mx / max(bound / ELEM, 1e-30))
+        assert ok, f"MXFP8 {name}: rel_frob={rf:.3e} max_err/max={mx / (bound / ELEM):.3e}"
+    print("MXFP8 chained errors (rel_frob, max_err/max):", report)
