@@ -301,22 +301,28 @@ def _nvfp4_30b_line(peak_fp4, steps=10):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-also", action="store_true", help="skip the secondary lines")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle sample")
+    ap.add_argument("--case", choices=["headline", "slice"], default="headline",
+                    help="slice: 4096 tokens over 64 experts of the 671B shape (profiling)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
     from microscaled_precision_moe_gb300 import synth
     shape = synth.MOE_671B
+    if args.case == "slice":
+        shape = synth.scaled(shape, T=4096, E=64, name="nvfp4_moe_fwd_T4096_H7168_I2048_E64_k8_zipf1.1")
     peaks = _peaks()
     peak_fp4_sus = peaks["bf16_sus"] * NOMINAL_FP4_OVER_BF16
     peak_fp8_sus = peaks["bf16_sus"] * NOMINAL_FP8_OVER_BF16
     cfg = {"workload": shape.name, "tokens": shape.T, "hidden": shape.H,
            "intermediate": shape.I, "experts": shape.E, "top_k": shape.k,
            "expert_load": "Zipf(1.1) via Gumbel-top-k", "weights": "N(0,0.01), 1e-4 outliers x100",
-           "l2": "no flush: activations 470 MB and FP4 weights 5.6 GB exceed L2"}
+           "l2": "no flush: inputs exceed L2 (activations %d MB, FP4 weights %.1f GB)" % (
+               shape.T * shape.H * 2 // 2 ** 20, shape.E * 3 * shape.H * shape.I * 0.5625 / 1e9)}
 
     if args.impl == "reference":
         rank = int(os.environ.get("RANK", "0"))
@@ -441,7 +447,7 @@ def main():
     del xh, outh, xd, layer, W, x
     torch.cuda.empty_cache()
 
-    if rank == 0:
+    if rank == 0 and not args.no_cpu:
         fl_s, sec_s, desc = _oracle_run(shape, _oracle_prepare(shape, ids, prob, n_experts=3))
         line["cpu_baseline"] = {"value": round(fl_s / sec_s / 1e12, 6), "unit": "TFLOP/s",
                                 "cores": _cores(), "kind": "oracle", "sample": desc}
