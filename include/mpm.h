@@ -158,6 +158,30 @@ mpm_status mpm_nvfp4_quantize_weight(const void* const* parts_dev, const int64_t
                                      uint8_t* q_dev, uint8_t* s_dev, float* tensor_scale_dev,
                                      void* ws_dev, size_t ws_bytes, cudaStream_t stream);
 
+/*
+ * Allocation-free variant of mpm_nvfp4_quantize_weight (the pages have no
+ * counterpart: this is an interface convenience of this library).  For
+ * callers that cannot allocate device memory where they quantise weights --
+ * code whose device memory belongs to a pool it cannot reach there, or a
+ * latency-critical loop where a cudaMalloc, which may synchronise the device,
+ * is not allowed.  Same inputs, outputs, rules and requirements as
+ * mpm_nvfp4_quantize_weight, but no workspace argument: the per-expert amax
+ * scratch lives in a fixed device array declared by the library (16 KiB, room
+ * for E <= 4096 experts; every GPU that loads the library keeps it until the
+ * process exits).  E > 4096 returns MPM_ERR_SHAPE before any launch.
+ * The first call on a device looks up that array's device address (once per
+ * device, with that device current); make that first call before any stream
+ * capture.  The call allocates nothing and clears the slots it uses before
+ * reducing into them.  All calls share the one array: calls whose work can
+ * overlap on the GPU (other streams, other host threads) race on it, so
+ * order them on one stream or synchronise between them.
+ */
+mpm_status mpm_nvfp4_quantize_weight_noalloc(const void* const* parts_dev,
+                                             const int64_t* part_rows, int nparts,
+                                             int64_t K, int64_t E, uint8_t* q_dev,
+                                             uint8_t* s_dev, float* tensor_scale_dev,
+                                             cudaStream_t stream);
+
 /* ------------------------------------------------------------------------ */
 /* Expert segments, permutation, combine                                    */
 /* ------------------------------------------------------------------------ */

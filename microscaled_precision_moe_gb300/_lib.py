@@ -54,6 +54,8 @@ _SIGS = {
     "mpm_nvfp4_weight_workspace_bytes": (_sz, [_i64]),
     "mpm_nvfp4_quantize_weight": (_int, [C.POINTER(_vp), C.POINTER(_i64), _int, _i64, _i64,
                                          _vp, _vp, _vp, _vp, _sz, _vp]),
+    "mpm_nvfp4_quantize_weight_noalloc": (_int, [C.POINTER(_vp), C.POINTER(_i64), _int, _i64,
+                                                 _i64, _vp, _vp, _vp, _vp]),
     "mpm_moe_row_capacity": (_i64, [_i64, _int, _i64]),
     "mpm_moe_segments_workspace_bytes": (_sz, [_i64, _int, _i64]),
     "mpm_moe_build_segments": (_int, [_vp, _vp, _i64, _int, _i64, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
