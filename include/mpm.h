@@ -188,21 +188,22 @@ mpm_status mpm_nvfp4_quantize_weight_noalloc(const void* const* parts_dev,
 
 /*
  * Row capacity of the permuted buffers for T tokens, top-k and E experts with
- * segments padded to 128 rows: pad128(T*k) + 128*E.
+ * segments padded to `pad` rows (128 or 256): pad(T*k) + pad*E.
  */
-int64_t mpm_moe_row_capacity(int64_t T, int k, int64_t E);
+int64_t mpm_moe_row_capacity(int64_t T, int k, int64_t E, int pad);
 size_t mpm_moe_segments_workspace_bytes(int64_t T, int k, int64_t E);
 
 /*
  * Counting sort of the T*k routed (token, slot) pairs by expert into one
- * contiguous buffer, each expert's segment padded to 128 rows.
+ * contiguous buffer, each expert's segment padded to `pad` rows (128: one
+ * MMA tile; 256: one CTA-pair tile, required by the tile_m = 256 GEMM).
  * Source: "miniTE technical report", section 5.2 (contiguous buffer with
  * expert boundaries given by offsets kept on the device; zero-token experts
  * and padding handled in the same path).
  *
  * topk_ids_dev: int32 [T, k] expert ids in [0, E); topk_prob_dev: fp32 [T, k].
  * Outputs (device): seg_offsets int32 [E+1] (seg_offsets[0] = 0, segment e is
- * rows [seg_offsets[e], seg_offsets[e+1]), a multiple of 128 long); perm
+ * rows [seg_offsets[e], seg_offsets[e+1]), a multiple of pad long); perm
  * int32 [capacity] (row -> flat index t*k + j, -1 for padding rows and rows
  * beyond seg_offsets[E]); inv_perm int32 [T*k] (flat index -> row); row_prob
  * fp32 [capacity] (0 for padding).  Rows of one expert are in ascending flat
@@ -210,7 +211,7 @@ size_t mpm_moe_segments_workspace_bytes(int64_t T, int k, int64_t E);
  * the pair is dropped.
  */
 mpm_status mpm_moe_build_segments(const int32_t* topk_ids_dev, const float* topk_prob_dev,
-                                  int64_t T, int k, int64_t E,
+                                  int64_t T, int k, int64_t E, int pad,
                                   int32_t* seg_offsets_dev, int32_t* perm_dev,
                                   int32_t* inv_perm_dev, float* row_prob_dev,
                                   void* ws_dev, size_t ws_bytes, cudaStream_t stream);
@@ -296,12 +297,19 @@ mpm_status mpm_moe_combine(const void* y_perm_dev, const int32_t* inv_perm_dev,
  * of D); "Towards Blackwell-native 8-bit and 4-bit RL", section "Recipe 1 /
  * Training" (dgrad with the column-wise weight copy, wgrad with column-wise
  * activation and gradient copies).
+ * tile_m = 256 runs the tile on a pair of CTAs (tcgen05 cta_group::2): each
+ * SM stages its 128 rows of A and half of B, so B moves through shared
+ * memory once per 256 output rows instead of once per 128.
  * Requirements: K % 256 == 0 (NVFP4) or % 128 == 0 (MXFP8) in GROUP_M;
  * N % 256 == 0 (SwiGLU: N/2 % 128 == 0); GROUP_K: M_out % 128 == 0,
  * segments multiples of 128 rows.
  */
 typedef struct {
   int kind;                    /* MPM_KIND_*                                   */
+  int tile_m;                  /* GROUP_M: 128 (one CTA per 128x256 tile) or 256
+                                  (a CTA pair per 256x256 tile, persistent; the
+                                  expert segments must be multiples of 256
+                                  rows, checked on the device); GROUP_K: 128 */
   int group;                   /* MPM_GROUP_*                                  */
   int epilogue;                /* MPM_EPI_*                                    */
   int64_t E;                   /* experts (groups)                             */

@@ -29,7 +29,7 @@ _vp, _i64, _u32, _int, _sz = C.c_void_p, C.c_int64, C.c_uint, C.c_int, C.c_size_
 class GroupedGemmDesc(C.Structure):
     """Mirror of mpm_grouped_gemm_desc."""
     _fields_ = [
-        ("kind", _int), ("group", _int), ("epilogue", _int),
+        ("kind", _int), ("tile_m", _int), ("group", _int), ("epilogue", _int),
         ("E", _i64), ("a_rows", _i64), ("N", _i64), ("K", _i64),
         ("seg_dev", _vp),
         ("a_dev", _vp), ("lda_bytes", _i64), ("a_total_rows", _i64),
@@ -56,9 +56,10 @@ _SIGS = {
                                          _vp, _vp, _vp, _vp, _sz, _vp]),
     "mpm_nvfp4_quantize_weight_noalloc": (_int, [C.POINTER(_vp), C.POINTER(_i64), _int, _i64,
                                                  _i64, _vp, _vp, _vp, _vp]),
-    "mpm_moe_row_capacity": (_i64, [_i64, _int, _i64]),
+    "mpm_moe_row_capacity": (_i64, [_i64, _int, _i64, _int]),
     "mpm_moe_segments_workspace_bytes": (_sz, [_i64, _int, _i64]),
-    "mpm_moe_build_segments": (_int, [_vp, _vp, _i64, _int, _i64, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
+    "mpm_moe_build_segments": (_int, [_vp, _vp, _i64, _int, _i64, _int, _vp, _vp, _vp, _vp, _vp,
+                                      _sz, _vp]),
     "mpm_moe_gather": (_int, [_int, _vp, _vp, _vp, _i64, _i64, _int, _vp, _vp, _i64, _i64,
                               _vp, _vp, _vp, _vp, _vp]),
     "mpm_moe_combine": (_int, [_vp, _vp, _i64, _int, _i64, _vp, _vp]),

@@ -70,6 +70,21 @@ bool make_tmap(CUtensorMap* m, const void* base, long long pitch, long long rows
   return r == CUDA_SUCCESS;
 }
 
+// 2-D view of a 128x4-tiled scale buffer as [atoms, 128] 32-bit words (one
+// 512-byte tile per row); a box of `atoms_per_box` consecutive tiles.
+bool make_sf_tmap(CUtensorMap* m, const void* base, long long atoms, int atoms_per_box) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {128, (cuuint64_t)atoms};
+  cuuint64_t strides[1] = {512};
+  cuuint32_t box[2] = {128, (cuuint32_t)atoms_per_box};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<void*>(base), dims, strides, box,
+                  estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 }  // namespace
 
 extern "C" {
@@ -154,9 +169,9 @@ mpm_status mpm_nvfp4_quantize_weight(const void* const* parts, const int64_t* pa
                                               static_cast<unsigned*>(ws), stream));
 }
 
-int64_t mpm_moe_row_capacity(int64_t T, int k, int64_t E) {
-  if (T < 1 || k < 1 || E < 1) return 0;
-  return pad_to(T * k, 128) + 128 * E;
+int64_t mpm_moe_row_capacity(int64_t T, int k, int64_t E, int pad) {
+  if (T < 1 || k < 1 || E < 1 || (pad != 128 && pad != 256)) return 0;
+  return pad_to(T * k, pad) + (int64_t)pad * E;
 }
 
 size_t mpm_moe_segments_workspace_bytes(int64_t T, int k, int64_t E) {
@@ -165,17 +180,18 @@ size_t mpm_moe_segments_workspace_bytes(int64_t T, int k, int64_t E) {
 }
 
 mpm_status mpm_moe_build_segments(const int32_t* ids, const float* prob, int64_t T, int k,
-                                  int64_t E, int32_t* seg, int32_t* perm, int32_t* inv,
+                                  int64_t E, int pad, int32_t* seg, int32_t* perm, int32_t* inv,
                                   float* row_prob, void* ws, size_t ws_bytes,
                                   cudaStream_t stream) {
   if (!ids || !prob || !seg || !perm || !inv || !row_prob || !ws) return MPM_ERR_NULL;
   if (T < 1 || k < 1 || k > 64 || E < 1 || E > 1024) return MPM_ERR_SHAPE;
+  if (pad != 128 && pad != 256) return MPM_ERR_SHAPE;
   if (T * k > (1ll << 30)) return MPM_ERR_SHAPE;
   if (ws_bytes < mpm::segments_ws_bytes(T, k, E)) return MPM_ERR_SHAPE;
   if (!aligned(ws, 4)) return MPM_ERR_ALIGN;
-  return cuda_status(mpm::launch_build_segments(ids, prob, T, k, E, seg, perm, inv, row_prob,
-                                                mpm_moe_row_capacity(T, k, E), ws, status_ptr(),
-                                                stream));
+  return cuda_status(mpm::launch_build_segments(ids, prob, T, k, E, pad, seg, perm, inv,
+                                                row_prob, mpm_moe_row_capacity(T, k, E, pad), ws,
+                                                status_ptr(), stream));
 }
 
 mpm_status mpm_moe_gather(int what, const void* src, const uint8_t* src_s, const float* src_ts,
@@ -207,6 +223,9 @@ mpm_status mpm_moe_grouped_gemm(const mpm_grouped_gemm_desc* d, cudaStream_t str
   if (!d) return MPM_ERR_NULL;
   if (d->kind != MPM_KIND_NVFP4 && d->kind != MPM_KIND_MXFP8) return MPM_ERR_UNSUPPORTED;
   if (d->group != MPM_GROUP_M && d->group != MPM_GROUP_K) return MPM_ERR_UNSUPPORTED;
+  const int tile_m = d->tile_m == 0 ? 128 : d->tile_m;
+  if (tile_m != 128 && tile_m != 256) return MPM_ERR_UNSUPPORTED;
+  if (tile_m == 256 && d->group != MPM_GROUP_M) return MPM_ERR_UNSUPPORTED;
   if (d->epilogue < MPM_EPI_F32 || d->epilogue > MPM_EPI_DSWIGLU) return MPM_ERR_UNSUPPORTED;
   if (!d->a_dev || !d->b_dev || !d->sfa_dev || !d->sfb_dev || !d->out_dev) return MPM_ERR_NULL;
   if (d->E < 1 || d->E > 65535 || d->N < 256 || d->N % 256 != 0 || d->a_rows < 1)
@@ -276,6 +295,18 @@ mpm_status mpm_moe_grouped_gemm(const mpm_grouped_gemm_desc* d, cudaStream_t str
   a.amax = d->amax_dev;
   a.status = status_ptr();
 
+  if (tile_m == 256) {
+    const int kind_atoms = d->kind == MPM_KIND_NVFP4 ? 4 : 1;
+    const long long atoms_a = pad_to(d->a_total_rows, 128) * pad_to(d->sfa_cols, 4) / 512;
+    const long long atoms_b = pad_to(d->b_total_rows, 128) * pad_to(d->sfb_cols, 4) / 512;
+    CUtensorMap tsa, tsb;
+    if (!make_sf_tmap(&tsa, d->sfa_dev, atoms_a, kind_atoms)) return MPM_ERR_CUDA;
+    if (!make_sf_tmap(&tsb, d->sfb_dev, atoms_b, kind_atoms)) return MPM_ERR_CUDA;
+    const int n_tiles = (int)(swiglu ? (d->N / 2) / 128 : d->N / 256);
+    const long long n_tasks = (long long)n_tiles * ((d->a_rows + 255) / 256);
+    return cuda_status(mpm::launch_grouped_gemm_pair(d->kind, d->epilogue, ta, tb, tsa, tsb, a,
+                                                     n_tiles, n_tasks, stream));
+  }
   dim3 grid;
   if (d->group == MPM_GROUP_M) {
     grid = dim3((unsigned)(swiglu ? (d->N / 2) / 128 : d->N / 256),

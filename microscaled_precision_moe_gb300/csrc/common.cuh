@@ -127,6 +127,115 @@ MPM_DEV void prefetch_tmap(const void* tmap) {
   asm volatile("prefetch.tensormap [%0];" :: "l"(tmap) : "memory");
 }
 
+// ---------------------------------------------------------------- clusters
+MPM_DEV uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+MPM_DEV uint32_t cluster_id_x() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
+  return r;
+}
+MPM_DEV uint32_t nclusters_x() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
+  return r;
+}
+// shared::cluster address of the same variable in CTA `rank` of the cluster
+MPM_DEV uint32_t map_to_rank(uint32_t saddr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+  return r;
+}
+MPM_DEV void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;"
+               ::: "memory");
+}
+// arrive (release, cluster scope) on an mbarrier given by its shared::cluster address
+MPM_DEV void mbar_arrive_cluster(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];"
+               :: "r"(cluster_addr) : "memory");
+}
+MPM_DEV uint32_t mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
+  return ok;
+}
+// bounded wait with cluster-scope acquire (for barriers other CTAs arrive on)
+MPM_DEV bool mbar_wait_cluster(uint32_t bar, uint32_t parity, int* st) {
+  if (mbar_try_wait_cluster(bar, parity)) return true;
+  long long t0 = clock64();
+  while (true) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    if (clock64() - t0 > kWaitLimitCycles) {
+      set_status(st, MPM_ERR_DEVICE_TIMEOUT);
+      return false;
+    }
+  }
+}
+// TMA load whose completion is signalled on an mbarrier that may live in the
+// peer CTA of the pair (bar is a shared::cluster address)
+MPM_DEV void tma_load_2d_pair(uint32_t dst, const void* tmap, int x, int y, uint32_t bar_cluster) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];"
+      :: "r"(dst), "l"(tmap), "r"(x), "r"(y), "r"(bar_cluster) : "memory");
+}
+// named barrier among a subset of warps
+MPM_DEV void named_sync(uint32_t id, uint32_t nthreads) {
+  asm volatile("bar.sync %0, %1;" :: "r"(id), "r"(nthreads) : "memory");
+}
+
+// ---------------------------------------------------------------- tcgen05 (pair)
+MPM_DEV void tmem_alloc_pair(uint32_t dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;"
+               :: "r"(dst_smem), "r"(ncols) : "memory");
+}
+MPM_DEV void tmem_relinquish_pair() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+MPM_DEV void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;"
+               :: "r"(taddr), "r"(ncols) : "memory");
+}
+// arrive on the mbarrier at this offset in every CTA of cta_mask once all prior
+// tcgen05 async ops of this thread finish
+MPM_DEV void tc_commit_pair(uint32_t bar, uint16_t cta_mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;" :: "r"(bar), "h"(cta_mask) : "memory");
+}
+MPM_DEV void tc_cp_32x128b_x4_pair(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;"
+               :: "r"(taddr), "l"(sdesc) : "memory");
+}
+MPM_DEV void mma_nvf4_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                           uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::mxf4nvf4.block_scale.scale_vec::4X"
+      " [%0], %1, %2, %3, [%5], [%6], p;\n\t}"
+      :: "r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate),
+         "r"(sfa_tmem), "r"(sfb_tmem) : "memory");
+}
+MPM_DEV void mma_mxf8_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                           uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X"
+      " [%0], %1, %2, %3, [%5], [%6], p;\n\t}"
+      :: "r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate),
+         "r"(sfa_tmem), "r"(sfb_tmem) : "memory");
+}
+
 // ---------------------------------------------------------------- tcgen05
 MPM_DEV void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
   asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
@@ -220,17 +329,19 @@ MPM_DEV uint64_t sdesc_sf(uint32_t saddr) {
   return d;
 }
 
-// Instruction descriptor of a block-scaled MMA, M = 128, K-major A and B.
+// Instruction descriptor of a block-scaled MMA with K-major A and B.
 //   fmt: operand format code (E2M1 = 1 for mxf4nvf4, E4M3 = 0 for mxf8f6f4)
 //   ue8m0: scale type (0 = UE4M3, 1 = UE8M0); sf_id: byte of the scale word
+//   m: 128 (one CTA) or 256 (a CTA pair)
 __host__ __device__ constexpr uint32_t idesc_block_scaled(uint32_t fmt, uint32_t n,
-                                                          uint32_t ue8m0, uint32_t sf_id) {
+                                                          uint32_t ue8m0, uint32_t sf_id,
+                                                          uint32_t m = 128) {
   return (sf_id << 4)            // B scale-factor id
        | (fmt << 7)              // A format
        | (fmt << 10)             // B format
        | ((n >> 3) << 17)        // N / 8
        | (ue8m0 << 23)           // scale type
-       | ((128u >> 4) << 24)     // M / 16
+       | ((m >> 4) << 24)        // M / 16
        | (sf_id << 29);          // A scale-factor id
 }
 

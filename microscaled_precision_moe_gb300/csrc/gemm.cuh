@@ -29,4 +29,8 @@ struct GemmArgs {
 
 cudaError_t launch_grouped_gemm(int kind, int epi, const CUtensorMap& ta, const CUtensorMap& tb,
                                 const GemmArgs& a, dim3 grid, cudaStream_t s);
+cudaError_t launch_grouped_gemm_pair(int kind, int epi, const CUtensorMap& ta,
+                                     const CUtensorMap& tb, const CUtensorMap& tsfa,
+                                     const CUtensorMap& tsfb, const GemmArgs& a, int n_tiles,
+                                     long long n_tasks, cudaStream_t s);
 }  // namespace mpm

@@ -1,0 +1,490 @@
+// Block-scaled grouped GEMM on CTA pairs (tcgen05 cta_group::2), persistent.
+//
+// Same contract as the one-CTA kernel in gemm.cu (C_e = A_e * B_e^T, NVFP4 or
+// MXFP8 operands, fp32 accumulation, the same epilogues), for row-segmented
+// GEMMs whose expert segments are multiples of 256 rows.  A cluster of two
+// CTAs computes one 256 x 256 output tile at a time:
+//
+//   * each CTA stages its own 128 rows of A and its own half of B (128 of the
+//     256 B rows) plus the scale tiles of its A rows and of all 256 B rows;
+//     every TMA load, the peer's included, completes on the leader CTA's
+//     barrier (cp.async.bulk.tensor .cta_group::2);
+//   * the leader's MMA thread copies the scale tiles of both CTAs into their
+//     tensor memories and issues tcgen05.mma.cta_group::2 (M = 256, N = 256):
+//     each SM reads only half of B from its shared memory, which halves the
+//     B traffic through shared memory compared with one CTA per 128x256 tile;
+//   * each CTA's four epilogue warps drain its 128 x 256 accumulator; in the
+//     SwiGLU and bf16 epilogues the accumulator is released to the next tile
+//     as soon as it is in registers, so stores overlap the next tile's MMAs;
+//   * clusters loop over tiles (expert-segment M pairs x N tiles) in a fixed
+//     stride, so the shared-memory ring never drains between tiles.
+//
+// Sources: "miniTE technical report", sections 5.2 and 5.4 (grouped GEMM over
+// a contiguous buffer with device offsets; FC1 epilogue); "Towards
+// Blackwell-native 8-bit and 4-bit RL", section "Recipe 1 / Training".
+#include "gemm.cuh"
+
+namespace mpm {
+namespace pairk {
+
+constexpr int BM = 128;              // rows per CTA; 256 per pair
+constexpr int BN = 256;
+constexpr int BKB = 128;             // bytes of K per stage
+constexpr int NTHREADS = 192;        // warp 0 TMA, warp 1 MMA/TMEM, warps 2-5 epilogue
+constexpr int A_STAGE = BM * BKB;    // 16 KB
+constexpr int B_STAGE = 128 * BKB;   // this CTA's half of B: 16 KB
+constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t SF_TMEM_BASE = 256;
+
+template <int KIND> struct Cfg;
+template <> struct Cfg<MPM_KIND_NVFP4> {
+  static constexpr int kElemsPerKB = 256;
+  static constexpr int kAtomsPerKB = 4;
+  static constexpr int kSfaBytes = 4 * 512;
+  static constexpr int kSfbBytes = 2 * 4 * 512;
+  static constexpr int kSfTmemPerStage = 16 + 32;
+  static constexpr int kStages = 5;
+  static constexpr uint32_t kFmt = 1, kUe8m0 = 0;
+};
+template <> struct Cfg<MPM_KIND_MXFP8> {
+  static constexpr int kElemsPerKB = 128;
+  static constexpr int kAtomsPerKB = 1;
+  static constexpr int kSfaBytes = 512;
+  static constexpr int kSfbBytes = 2 * 512;
+  static constexpr int kSfTmemPerStage = 4 + 8;
+  static constexpr int kStages = 6;
+  static constexpr uint32_t kFmt = 0, kUe8m0 = 1;
+};
+
+template <int KIND>
+constexpr int stage_bytes() {
+  return A_STAGE + B_STAGE + Cfg<KIND>::kSfaBytes + Cfg<KIND>::kSfbBytes;
+}
+template <int KIND>
+constexpr int smem_bytes() {
+  return 1024 + Cfg<KIND>::kStages * stage_bytes<KIND>() + (3 * Cfg<KIND>::kStages + 4) * 8 + 32;
+}
+
+MPM_DEV float silu_f(float g) { return g / (1.0f + expf(-g)); }
+MPM_DEV uint32_t pack_bf16(float lo, float hi) {
+  __nv_bfloat162 b = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&b);
+}
+
+struct Task {
+  bool valid;
+  int e;
+  long long row_pair;   // first row of the 256-row pair tile
+  long long n0;         // first output column (D columns for SwiGLU)
+  long long brow[2];    // global B rows of the two 128-row halves
+  int num_kb;
+};
+
+template <int KIND, int EPI>
+MPM_DEV Task task_of(const GemmArgs& p, long long t, int n_tiles, int* bad) {
+  Task k{};
+  const long long mp = t / n_tiles;
+  const int nt = (int)(t - mp * n_tiles);
+  k.row_pair = mp * 2 * BM;
+  long long seg_end = p.a_rows;
+  if (p.seg) seg_end = p.seg[p.E];
+  if (k.row_pair >= seg_end) { k.valid = false; return k; }
+  int e = 0;
+  if (p.seg) {
+    int lo = 0, hi = p.E - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (p.seg[mid] <= k.row_pair) lo = mid; else hi = mid - 1;
+    }
+    e = lo;
+    if ((p.seg[e] & 255) != 0 || (p.seg[e + 1] & 255) != 0) *bad = 1;   // not pair-aligned
+  }
+  k.e = e;
+  const bool swiglu = (EPI == MPM_EPI_SWIGLU || EPI == MPM_EPI_SWIGLU_SAVE);
+  k.n0 = (long long)nt * (swiglu ? BN / 2 : BN);
+  if (swiglu) {
+    k.brow[0] = (long long)e * p.b_rows_per_e + k.n0;
+    k.brow[1] = (long long)e * p.b_rows_per_e + p.N / 2 + k.n0;
+  } else {
+    k.brow[0] = (long long)e * p.b_rows_per_e + k.n0;
+    k.brow[1] = k.brow[0] + 128;
+  }
+  k.num_kb = (int)(p.K / Cfg<KIND>::kElemsPerKB);
+  k.valid = true;
+  return k;
+}
+
+struct PairMaps {
+  CUtensorMap a, b, sfa, sfb;
+};
+
+template <int KIND, int EPI>
+__global__ void __launch_bounds__(NTHREADS, 1)
+grouped_gemm_pair_kernel(const __grid_constant__ PairMaps maps, const GemmArgs p, const int n_tiles,
+                         const long long n_tasks) {
+  using C = Cfg<KIND>;
+  constexpr int S = C::kStages;
+  extern __shared__ uint8_t smem_raw[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();          // 0 = leader of the pair
+  const long long cid = cluster_id_x(), ncl = nclusters_x();
+
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* gbase = smem_raw + (base - raw);
+  const uint32_t sA = base;
+  const uint32_t sB = sA + S * A_STAGE;
+  const uint32_t sSFA = sB + S * B_STAGE;
+  const uint32_t sSFB = sSFA + S * C::kSfaBytes;
+  const uint32_t sBar = sSFB + S * C::kSfbBytes;
+  const uint32_t bar_full = sBar, bar_empty = sBar + 8 * S;
+  const uint32_t bar_accf = sBar + 16 * S, bar_acce = bar_accf + 8;
+  const uint32_t sTmem = bar_acce + 8;
+  const uint32_t sFlag = sTmem + 8;
+  volatile uint32_t* tmem_holder = reinterpret_cast<volatile uint32_t*>(gbase + (sTmem - base));
+  volatile int* fail_flag = reinterpret_cast<volatile int*>(gbase + (sFlag - base));
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(bar_full + 8 * s, 1);
+      mbar_init(bar_empty + 8 * s, 1);
+    }
+    mbar_init(bar_accf, 1);
+    mbar_init(bar_acce, 2);          // one arrive from each CTA's epilogue
+    *fail_flag = 0;
+    fence_mbar_init();
+    fence_proxy_async();
+    prefetch_tmap(&maps.a);
+    prefetch_tmap(&maps.b);
+    prefetch_tmap(&maps.sfa);
+    prefetch_tmap(&maps.sfb);
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(sTmem, TMEM_COLS);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  cluster_sync();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+  const uint32_t acce_leader = map_to_rank(bar_acce, 0);
+  int bad = 0;
+
+  if (warp == 0 && lane == 0) {
+    // ======================================================== TMA producer (both CTAs)
+    uint32_t it = 0;
+    for (long long t = cid; t < n_tasks; t += ncl) {
+      const Task k = task_of<KIND, EPI>(p, t, n_tiles, &bad);
+      if (!k.valid) break;
+      const long long a_row = k.row_pair + rank * BM;
+      const long long sfa_rt = a_row >> 7;
+      bool ok = true;
+      for (int kb = 0; kb < k.num_kb; ++kb, ++it) {
+        const int s = it % S;
+        const uint32_t ph = (it / S) & 1u;
+        if (!mbar_wait_cluster(bar_empty + 8 * s, ph ^ 1u, p.status)) { ok = false; break; }
+        if (rank == 0) mbar_arrive_expect_tx(bar_full + 8 * s, 2 * stage_bytes<KIND>());
+        const uint32_t fb = map_to_rank(bar_full + 8 * s, 0);   // the leader's barrier
+        const long long ka = (long long)kb * C::kElemsPerKB;
+        const long long kbb = (long long)k.e * p.b_k_per_e + ka;
+        const int xa = (int)(KIND == MPM_KIND_NVFP4 ? ka / 2 : ka);
+        const int xb = (int)(KIND == MPM_KIND_NVFP4 ? kbb / 2 : kbb);
+        tma_load_2d_pair(sA + s * A_STAGE, &maps.a, xa, (int)a_row, fb);
+        tma_load_2d_pair(sB + s * B_STAGE, &maps.b, xb, (int)k.brow[rank], fb);
+        const long long atom_a = (KIND == MPM_KIND_NVFP4) ? ka / 64 : ka / 128;
+        const long long atom_b = (KIND == MPM_KIND_NVFP4) ? kbb / 64 : kbb / 128;
+        tma_load_2d_pair(sSFA + s * C::kSfaBytes, &maps.sfa, 0,
+                         (int)(sfa_rt * (p.sfa_cols_pad >> 2) + atom_a), fb);
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+          tma_load_2d_pair(sSFB + s * C::kSfbBytes + h * (C::kSfbBytes / 2), &maps.sfb, 0,
+                           (int)((k.brow[h] >> 7) * (p.sfb_cols_pad >> 2) + atom_b), fb);
+      }
+      if (!ok) break;
+    }
+  } else if (warp == 1 && lane == 0 && rank == 0) {
+    // ======================================================== MMA issuer (leader only)
+    uint32_t it = 0, j = 0;
+    for (long long t = cid; t < n_tasks; t += ncl, ++j) {
+      const Task k = task_of<KIND, EPI>(p, t, n_tiles, &bad);
+      if (!k.valid) break;
+      if (!mbar_wait_cluster(bar_acce, (j & 1u) ^ 1u, p.status)) break;
+      tc_fence_after();
+      bool ok = true;
+      for (int kb = 0; kb < k.num_kb; ++kb, ++it) {
+        const int s = it % S;
+        const uint32_t ph = (it / S) & 1u;
+        if (!mbar_wait_cluster(bar_full + 8 * s, ph, p.status)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t sf_col = tmem + SF_TMEM_BASE + s * C::kSfTmemPerStage;
+        if (KIND == MPM_KIND_NVFP4) {
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks) {
+            tc_cp_32x128b_x4_pair(sf_col + ks * 4, sdesc_sf(sSFA + s * C::kSfaBytes + ks * 512));
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+              tc_cp_32x128b_x4_pair(sf_col + 16 + ks * 8 + h * 4,
+                                    sdesc_sf(sSFB + s * C::kSfbBytes + h * 2048 + ks * 512));
+          }
+        } else {
+          tc_cp_32x128b_x4_pair(sf_col, sdesc_sf(sSFA + s * C::kSfaBytes));
+#pragma unroll
+          for (int h = 0; h < 2; ++h)
+            tc_cp_32x128b_x4_pair(sf_col + 4 + h * 4, sdesc_sf(sSFB + s * C::kSfbBytes + h * 512));
+        }
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks) {
+          const uint64_t adesc = sdesc_sw128(sA + s * A_STAGE + ks * 32);
+          const uint64_t bdesc = sdesc_sw128(sB + s * B_STAGE + ks * 32);
+          const uint32_t acc = (kb > 0 || ks > 0) ? 1u : 0u;
+          if (KIND == MPM_KIND_NVFP4) {
+            const uint32_t idesc = idesc_block_scaled(C::kFmt, BN, C::kUe8m0, 0, 256);
+            mma_nvf4_pair(tmem, adesc, bdesc, idesc, sf_col + ks * 4, sf_col + 16 + ks * 8, acc);
+          } else {
+            const uint32_t idesc = idesc_block_scaled(C::kFmt, BN, C::kUe8m0, (uint32_t)ks, 256);
+            mma_mxf8_pair(tmem, adesc, bdesc, idesc, sf_col, sf_col + 4, acc);
+          }
+        }
+        tc_commit_pair(bar_empty + 8 * s, (uint16_t)3);
+      }
+      tc_commit_pair(bar_accf, (uint16_t)3);
+      if (!ok) break;
+    }
+  } else if (warp >= 2) {
+    // ======================================================== epilogue (both CTAs)
+    const int q = warp & 3;                     // TMEM lane quarter of this warp
+    const int r = q * 32 + lane;                // row within this CTA's 128 rows
+    const uint32_t trow = tmem + ((uint32_t)(q * 32) << 16);
+    uint32_t j = 0;
+    for (long long t = cid; t < n_tasks; t += ncl, ++j) {
+      const Task k = task_of<KIND, EPI>(p, t, n_tiles, &bad);
+      if (!k.valid) break;
+      const bool w_ok = mbar_wait_cluster(bar_accf, j & 1u, p.status);
+      if (!w_ok) *fail_flag = 1;
+      named_sync(1, 128);
+      if (*fail_flag) break;
+      tc_fence_after();
+      const long long grow = k.row_pair + rank * BM + r;
+      const bool row_ok = grow < p.a_rows;
+      float alpha = 1.0f;
+      if (row_ok) {
+        if (p.alpha_a) alpha = p.alpha_a[grow];
+        if (p.alpha_b) alpha = __fmul_rn(alpha, p.alpha_b[k.e]);
+      }
+      uint32_t v[32], u[32];
+      if (EPI == MPM_EPI_SWIGLU || EPI == MPM_EPI_SWIGLU_SAVE) {
+        const float prob = row_ok ? p.row_prob[grow] : 0.0f;
+        uint32_t dw[64];
+        float amax = 0.0f;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          tmem_ld_32x32b_x32(trow + c * 32, v);
+          tmem_ld_32x32b_x32(trow + 128 + c * 32, u);
+          tmem_ld_wait();
+          if (EPI == MPM_EPI_SWIGLU_SAVE && row_ok) {
+            __nv_bfloat16* og = static_cast<__nv_bfloat16*>(p.out) + grow * p.ldo + k.n0 + c * 32;
+            __nv_bfloat16* ou = og + p.N / 2;
+#pragma unroll
+            for (int jj = 0; jj < 32; jj += 8) {
+              uint4 wg, wu;
+              wg.x = pack_bf16(__fmul_rn(__uint_as_float(v[jj]), alpha), __fmul_rn(__uint_as_float(v[jj + 1]), alpha));
+              wg.y = pack_bf16(__fmul_rn(__uint_as_float(v[jj + 2]), alpha), __fmul_rn(__uint_as_float(v[jj + 3]), alpha));
+              wg.z = pack_bf16(__fmul_rn(__uint_as_float(v[jj + 4]), alpha), __fmul_rn(__uint_as_float(v[jj + 5]), alpha));
+              wg.w = pack_bf16(__fmul_rn(__uint_as_float(v[jj + 6]), alpha), __fmul_rn(__uint_as_float(v[jj + 7]), alpha));
+              wu.x = pack_bf16(__fmul_rn(__uint_as_float(u[jj]), alpha), __fmul_rn(__uint_as_float(u[jj + 1]), alpha));
+              wu.y = pack_bf16(__fmul_rn(__uint_as_float(u[jj + 2]), alpha), __fmul_rn(__uint_as_float(u[jj + 3]), alpha));
+              wu.z = pack_bf16(__fmul_rn(__uint_as_float(u[jj + 4]), alpha), __fmul_rn(__uint_as_float(u[jj + 5]), alpha));
+              wu.w = pack_bf16(__fmul_rn(__uint_as_float(u[jj + 6]), alpha), __fmul_rn(__uint_as_float(u[jj + 7]), alpha));
+              *reinterpret_cast<uint4*>(og + jj) = wg;
+              *reinterpret_cast<uint4*>(ou + jj) = wu;
+            }
+          }
+#pragma unroll
+          for (int jj = 0; jj < 32; jj += 2) {
+            const float g0 = __fmul_rn(__uint_as_float(v[jj]), alpha);
+            const float u0 = __fmul_rn(__uint_as_float(u[jj]), alpha);
+            const float g1 = __fmul_rn(__uint_as_float(v[jj + 1]), alpha);
+            const float u1 = __fmul_rn(__uint_as_float(u[jj + 1]), alpha);
+            const uint32_t pk = pack_bf16(__fmul_rn(__fmul_rn(silu_f(g0), u0), prob),
+                                          __fmul_rn(__fmul_rn(silu_f(g1), u1), prob));
+            dw[c * 16 + jj / 2] = pk;
+            amax = fmaxf(amax, fmaxf(fabsf(bf16lo(pk)), fabsf(bf16hi(pk))));
+          }
+        }
+        // accumulator drained: hand it to the next tile, then store
+        tc_fence_before();
+        named_sync(1, 128);
+        if (threadIdx.x == 64) mbar_arrive_cluster(acce_leader);
+        if (row_ok) {
+          __nv_bfloat16* od = static_cast<__nv_bfloat16*>(p.out2) + grow * p.ldo2 + k.n0;
+#pragma unroll
+          for (int jj = 0; jj < 64; jj += 4)
+            *reinterpret_cast<uint4*>(od + 2 * jj) = make_uint4(dw[jj], dw[jj + 1], dw[jj + 2], dw[jj + 3]);
+          if (p.amax && amax > 0.0f)
+            atomicMax(reinterpret_cast<unsigned*>(p.amax) + grow, __float_as_uint(amax));
+        }
+      } else if (EPI == MPM_EPI_BF16) {
+        uint32_t ow[128];
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          tmem_ld_32x32b_x32(trow + c * 32, v);
+          tmem_ld_wait();
+#pragma unroll
+          for (int jj = 0; jj < 32; jj += 2)
+            ow[c * 16 + jj / 2] = pack_bf16(__fmul_rn(__uint_as_float(v[jj]), alpha),
+                                            __fmul_rn(__uint_as_float(v[jj + 1]), alpha));
+        }
+        tc_fence_before();
+        named_sync(1, 128);
+        if (threadIdx.x == 64) mbar_arrive_cluster(acce_leader);
+        if (row_ok) {
+          __nv_bfloat16* o = static_cast<__nv_bfloat16*>(p.out) + grow * p.ldo + k.n0;
+#pragma unroll
+          for (int jj = 0; jj < 128; jj += 4)
+            *reinterpret_cast<uint4*>(o + 2 * jj) = make_uint4(ow[jj], ow[jj + 1], ow[jj + 2], ow[jj + 3]);
+        }
+      } else if (EPI == MPM_EPI_F32) {
+#pragma unroll 1
+        for (int c = 0; c < 8; ++c) {
+          tmem_ld_32x32b_x32(trow + c * 32, v);
+          tmem_ld_wait();
+          if (row_ok) {
+            float* o = static_cast<float*>(p.out) + grow * p.ldo + k.n0 + c * 32;
+#pragma unroll
+            for (int jj = 0; jj < 32; jj += 4)
+              *reinterpret_cast<float4*>(o + jj) = make_float4(
+                  __fmul_rn(__uint_as_float(v[jj]), alpha), __fmul_rn(__uint_as_float(v[jj + 1]), alpha),
+                  __fmul_rn(__uint_as_float(v[jj + 2]), alpha), __fmul_rn(__uint_as_float(v[jj + 3]), alpha));
+          }
+        }
+        tc_fence_before();
+        named_sync(1, 128);
+        if (threadIdx.x == 64) mbar_arrive_cluster(acce_leader);
+      } else {   // MPM_EPI_DSWIGLU
+        const float prob = row_ok ? p.row_prob[grow] : 0.0f;
+        const long long Nh = p.N;
+        const __nv_bfloat16* cg = static_cast<const __nv_bfloat16*>(p.aux) + grow * p.ld_aux;
+        const __nv_bfloat16* cu = cg + Nh;
+        __nv_bfloat16* og = static_cast<__nv_bfloat16*>(p.out) + grow * p.ldo;
+        __nv_bfloat16* ou = og + Nh;
+#pragma unroll 1
+        for (int c = 0; c < 8; ++c) {
+          tmem_ld_32x32b_x32(trow + c * 32, v);
+          tmem_ld_wait();
+          if (!row_ok) continue;
+          const long long col = k.n0 + c * 32;
+#pragma unroll
+          for (int jj = 0; jj < 32; jj += 8) {
+            const uint4 gw = *reinterpret_cast<const uint4*>(cg + col + jj);
+            const uint4 uw = *reinterpret_cast<const uint4*>(cu + col + jj);
+            const uint32_t ga[4] = {gw.x, gw.y, gw.z, gw.w};
+            const uint32_t ua[4] = {uw.x, uw.y, uw.z, uw.w};
+            uint32_t og4[4], ou4[4];
+#pragma unroll
+            for (int qq = 0; qq < 4; ++qq) {
+              float dg2[2], du2[2];
+#pragma unroll
+              for (int h = 0; h < 2; ++h) {
+                const float g = h ? bf16hi(ga[qq]) : bf16lo(ga[qq]);
+                const float uu = h ? bf16hi(ua[qq]) : bf16lo(ua[qq]);
+                const float dd = __fmul_rn(__uint_as_float(v[jj + 2 * qq + h]), alpha);
+                const float sg = 1.0f / (1.0f + expf(-g));
+                const float dp = dd * prob;
+                dg2[h] = dp * uu * (sg * (1.0f + g * (1.0f - sg)));
+                du2[h] = dp * (g * sg);
+              }
+              og4[qq] = pack_bf16(dg2[0], dg2[1]);
+              ou4[qq] = pack_bf16(du2[0], du2[1]);
+            }
+            *reinterpret_cast<uint4*>(og + col + jj) = make_uint4(og4[0], og4[1], og4[2], og4[3]);
+            *reinterpret_cast<uint4*>(ou + col + jj) = make_uint4(ou4[0], ou4[1], ou4[2], ou4[3]);
+          }
+        }
+        tc_fence_before();
+        named_sync(1, 128);
+        if (threadIdx.x == 64) mbar_arrive_cluster(acce_leader);
+      }
+    }
+  }
+  if (bad && threadIdx.x == 0) set_status(p.status, MPM_ERR_DEVICE_BOUNDS);
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem, TMEM_COLS);
+  }
+}
+
+}  // namespace pairk
+
+// ---------------------------------------------------------------- launcher
+template <int KIND, int EPI>
+static cudaError_t launch_pair_one(const pairk::PairMaps& maps, const GemmArgs& a, int n_tiles,
+                                   long long n_tasks, cudaStream_t s) {
+  constexpr int smem = pairk::smem_bytes<KIND>();
+  auto kern = pairk::grouped_gemm_pair_kernel<KIND, EPI>;
+  static int max_clusters[64] = {0};
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.blockDim = dim3(pairk::NTHREADS, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (dev < 64 && max_clusters[dev] == 0) {
+    err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (err != cudaSuccess) return err;
+    int sms = 0;
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    cfg.gridDim = dim3(2 * (sms / 2), 1, 1);
+    int ncl = 0;
+    err = cudaOccupancyMaxActiveClusters(&ncl, kern, &cfg);
+    if (err != cudaSuccess || ncl < 1) ncl = sms / 2;
+    max_clusters[dev] = ncl;
+  }
+  long long ncl = dev < 64 ? max_clusters[dev] : 1;
+  if (ncl > n_tasks) ncl = n_tasks;
+  if (ncl < 1) ncl = 1;
+  cfg.gridDim = dim3((unsigned)(2 * ncl), 1, 1);
+  err = cudaLaunchKernelEx(&cfg, kern, maps, a, n_tiles, n_tasks);
+  if (err != cudaSuccess) return err;
+  return cudaGetLastError();
+}
+
+template <int KIND>
+static cudaError_t pair_dispatch(int epi, const pairk::PairMaps& maps, const GemmArgs& a,
+                                 int n_tiles, long long n_tasks, cudaStream_t s) {
+  switch (epi) {
+    case MPM_EPI_F32: return launch_pair_one<KIND, MPM_EPI_F32>(maps, a, n_tiles, n_tasks, s);
+    case MPM_EPI_BF16: return launch_pair_one<KIND, MPM_EPI_BF16>(maps, a, n_tiles, n_tasks, s);
+    case MPM_EPI_SWIGLU: return launch_pair_one<KIND, MPM_EPI_SWIGLU>(maps, a, n_tiles, n_tasks, s);
+    case MPM_EPI_SWIGLU_SAVE:
+      return launch_pair_one<KIND, MPM_EPI_SWIGLU_SAVE>(maps, a, n_tiles, n_tasks, s);
+    case MPM_EPI_DSWIGLU: return launch_pair_one<KIND, MPM_EPI_DSWIGLU>(maps, a, n_tiles, n_tasks, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+cudaError_t launch_grouped_gemm_pair(int kind, int epi, const CUtensorMap& ta,
+                                     const CUtensorMap& tb, const CUtensorMap& tsfa,
+                                     const CUtensorMap& tsfb, const GemmArgs& a, int n_tiles,
+                                     long long n_tasks, cudaStream_t s) {
+  pairk::PairMaps maps;
+  maps.a = ta;
+  maps.b = tb;
+  maps.sfa = tsfa;
+  maps.sfb = tsfb;
+  if (kind == MPM_KIND_NVFP4) return pair_dispatch<MPM_KIND_NVFP4>(epi, maps, a, n_tiles, n_tasks, s);
+  return pair_dispatch<MPM_KIND_MXFP8>(epi, maps, a, n_tiles, n_tasks, s);
+}
+
+}  // namespace mpm

@@ -3,7 +3,7 @@
 // "miniTE technical report", section 5.2: the routed rows of all experts sit
 // in one contiguous buffer whose expert boundaries are offsets kept on the
 // device; zero-token experts and the padding of each segment (to 128 rows, one
-// MMA tile) are handled in the same path.  Section 5.3: the permute gathers
+// MMA tile, or 256, one CTA-pair tile) are handled in the same path.  Section 5.3: the permute gathers
 // each routed (token, slot) row; the combine sums a token's expert outputs.
 //
 // The counting sort is stable: rows of one expert appear in ascending flat
@@ -36,7 +36,7 @@ __global__ void __launch_bounds__(256) seg_hist_kernel(const int* ids, long long
 // 2) one CTA: per-expert totals, padded segment offsets (exclusive scan), and
 //    each chunk's first row per expert: base[chunk][e]
 __global__ void __launch_bounds__(1024) seg_scan_kernel(const int* hist, int nchunks, int E,
-                                                       int* base, int* seg_offsets) {
+                                                       int pad, int* base, int* seg_offsets) {
   __shared__ int padded[1024];
   __shared__ int total_sh[1024];
   const int e = threadIdx.x;
@@ -49,7 +49,7 @@ __global__ void __launch_bounds__(1024) seg_scan_kernel(const int* hist, int nch
     }
   }
   total_sh[e] = tot;
-  padded[e] = (e < E) ? (tot + 127) / 128 * 128 : 0;
+  padded[e] = (e < E) ? (tot + pad - 1) / pad * pad : 0;
   __syncthreads();
   // Hillis-Steele inclusive scan over padded sizes
   for (int o = 1; o < 1024; o <<= 1) {
@@ -58,7 +58,7 @@ __global__ void __launch_bounds__(1024) seg_scan_kernel(const int* hist, int nch
     padded[e] += v;
     __syncthreads();
   }
-  const int excl = padded[e] - ((e < E) ? (total_sh[e] + 127) / 128 * 128 : 0);
+  const int excl = padded[e] - ((e < E) ? (total_sh[e] + pad - 1) / pad * pad : 0);
   if (e < E) {
     seg_offsets[e] = excl;
     for (int c = 0; c < nchunks; ++c) base[(long long)c * E + e] += excl;
@@ -196,9 +196,9 @@ size_t segments_ws_bytes(long long T, int k, long long E) {
 }
 
 cudaError_t launch_build_segments(const int* ids, const float* prob, long long T, int k,
-                                  long long E, int* seg_offsets, int* perm, int* inv_perm,
-                                  float* row_prob, long long cap, void* ws, int* st,
-                                  cudaStream_t s) {
+                                  long long E, int pad, int* seg_offsets, int* perm,
+                                  int* inv_perm, float* row_prob, long long cap, void* ws,
+                                  int* st, cudaStream_t s) {
   const long long n = T * k;
   const int nchunks = (int)((n + kSegChunk - 1) / kSegChunk);
   int* hist = static_cast<int*>(ws);
@@ -208,7 +208,7 @@ cudaError_t launch_build_segments(const int* ids, const float* prob, long long T
   if ((err = cudaMemsetAsync(row_prob, 0, (size_t)cap * sizeof(float), s)) != cudaSuccess) return err;
   seg_hist_kernel<<<nchunks, 256, (size_t)E * sizeof(int), s>>>(ids, n, (int)E, hist, st);
   if ((err = cudaGetLastError()) != cudaSuccess) return err;
-  seg_scan_kernel<<<1, 1024, 0, s>>>(hist, nchunks, (int)E, base, seg_offsets);
+  seg_scan_kernel<<<1, 1024, 0, s>>>(hist, nchunks, (int)E, pad, base, seg_offsets);
   if ((err = cudaGetLastError()) != cudaSuccess) return err;
   seg_scatter_kernel<<<nchunks, 32, (size_t)E * sizeof(int), s>>>(ids, prob, n, (int)E, base,
                                                                   perm, inv_perm, row_prob);

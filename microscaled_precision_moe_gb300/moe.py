@@ -63,12 +63,15 @@ class NVFP4Weights:
 
 class NVFP4MoE:
     """Buffers and launch sequence of the NVFP4 expert-layer forward for a
-    fixed (T, H, I, E, k)."""
+    fixed (T, H, I, E, k).  tile_m = 256 (default) runs the grouped GEMMs on
+    CTA pairs and pads expert segments to 256 rows; 128 uses one CTA per
+    128-row tile and 128-row segments."""
 
-    def __init__(self, T, H, I, E, k, device="cuda"):
+    def __init__(self, T, H, I, E, k, device="cuda", tile_m=256):
         self.T, self.H, self.I, self.E, self.k = T, H, I, E, k
+        self.tile_m = tile_m
         dev = torch.device(device)
-        cap = ops.moe_row_capacity(T, k, E)
+        cap = ops.moe_row_capacity(T, k, E, tile_m)
         self.cap = cap
         u8, f32, bf = torch.uint8, torch.float32, torch.bfloat16
         e = lambda *s, dtype: torch.empty(*s, dtype=dtype, device=dev)
@@ -95,7 +98,8 @@ class NVFP4MoE:
         ops.nvfp4_quantize_per_token(x, out=self.xq)
         seg, perm, inv, rp = self.seg
         mark(1)
-        ops.moe_build_segments(topk_ids, topk_prob, E, out=self.seg, ws=self.seg_ws)
+        ops.moe_build_segments(topk_ids, topk_prob, E, out=self.seg, ws=self.seg_ws,
+                               pad=self.tile_m)
         mark(2)
         ops.moe_gather_nvfp4(*self.xq, H, perm, seg, E, k, cap, out=self.aq, amax_zero=self.amax)
         aq, as_, ats = self.aq
@@ -103,14 +107,15 @@ class NVFP4MoE:
         ops.moe_grouped_gemm(L.KIND_NVFP4, L.GROUP_M, L.EPI_SWIGLU, E, cap, 2 * I, H, seg,
                              aq, w.w1_q.view(E * 2 * I, H // 2), as_, H // 16, w.w1_s, H // 16,
                              self.d, b_rows_per_expert=2 * I, alpha_a=ats, alpha_b=w.w1_ts,
-                             row_prob=rp, out2=self.d, amax=self.amax)
+                             row_prob=rp, out2=self.d, amax=self.amax, tile_m=self.tile_m)
         mark(4)
         ops.nvfp4_quantize_per_token(self.d, amax_in=self.amax, m_valid=seg[E:], out=self.dq)
         dq, ds, dts = self.dq
         mark(5)
         ops.moe_grouped_gemm(L.KIND_NVFP4, L.GROUP_M, L.EPI_BF16, E, cap, H, I, seg,
                              dq, w.w2_q.view(E * H, I // 2), ds, I // 16, w.w2_s, I // 16,
-                             self.y, b_rows_per_expert=H, alpha_a=dts, alpha_b=w.w2_ts)
+                             self.y, b_rows_per_expert=H, alpha_a=dts, alpha_b=w.w2_ts,
+                             tile_m=self.tile_m)
         mark(6)
         ops.moe_combine(self.y, inv, T, k, out=self.out)
         mark(7)
@@ -133,12 +138,14 @@ class NVFP4MoE:
 
 class MXFP8MoE:
     """Buffers and launch sequence of the MXFP8 expert layer, forward and
-    backward, for a fixed (T, H, I, E, k)."""
+    backward, for a fixed (T, H, I, E, k).  tile_m as for NVFP4MoE (the wgrad
+    GEMMs contract over the segments and always use one CTA per tile)."""
 
-    def __init__(self, T, H, I, E, k, device="cuda"):
+    def __init__(self, T, H, I, E, k, device="cuda", tile_m=256):
         self.T, self.H, self.I, self.E, self.k = T, H, I, E, k
+        self.tile_m = tile_m
         dev = torch.device(device)
-        cap = ops.moe_row_capacity(T, k, E)
+        cap = ops.moe_row_capacity(T, k, E, tile_m)
         self.cap = cap
         u8, f32, bf = torch.uint8, torch.float32, torch.bfloat16
         e = lambda *s, dtype: torch.empty(*s, dtype=dtype, device=dev)
@@ -182,17 +189,19 @@ class MXFP8MoE:
     def forward(self, x, topk_ids, topk_prob):
         T, H, I, E, k, cap = self.T, self.H, self.I, self.E, self.k, self.cap
         seg, perm, inv, rp = self.seg
-        ops.moe_build_segments(topk_ids, topk_prob, E, out=self.seg, ws=self.seg_ws)
+        ops.moe_build_segments(topk_ids, topk_prob, E, out=self.seg, ws=self.seg_ws,
+                               pad=self.tile_m)
         ops.moe_gather_bf16(x, perm, seg, E, k, cap, out=self.xp)
         ops.mxfp8_quantize(self.xp, ldc=cap, m_valid=seg[E:], out=self.xq)
         ops.moe_grouped_gemm(L.KIND_MXFP8, L.GROUP_M, L.EPI_SWIGLU_SAVE, E, cap, 2 * I, H, seg,
                              self.xq["row_q"], self.w1["row_q"], self.xq["row_s"], H // 32,
                              self.w1["row_s"], H // 32, self.c1, b_rows_per_expert=2 * I,
-                             row_prob=rp, out2=self.d)
+                             row_prob=rp, out2=self.d, tile_m=self.tile_m)
         ops.mxfp8_quantize(self.d, ldc=cap, m_valid=seg[E:], out=self.dq)
         ops.moe_grouped_gemm(L.KIND_MXFP8, L.GROUP_M, L.EPI_BF16, E, cap, H, I, seg,
                              self.dq["row_q"], self.w2["row_q"], self.dq["row_s"], I // 32,
-                             self.w2["row_s"], I // 32, self.y, b_rows_per_expert=H)
+                             self.w2["row_s"], I // 32, self.y, b_rows_per_expert=H,
+                             tile_m=self.tile_m)
         ops.moe_combine(self.y, inv, T, k, out=self.out)
         return self.out
 
@@ -205,7 +214,7 @@ class MXFP8MoE:
         ops.moe_grouped_gemm(L.KIND_MXFP8, L.GROUP_M, L.EPI_DSWIGLU, E, cap, I, H, seg,
                              self.dyq["row_q"], self.w2["col_q"], self.dyq["row_s"], H // 32,
                              self.w2["col_s"], (E * H) // 32, self.dh, b_rows_per_expert=0,
-                             b_k_per_expert=H, row_prob=rp, aux=self.c1)
+                             b_k_per_expert=H, row_prob=rp, aux=self.c1, tile_m=self.tile_m)
         # FC2 wgrad: dW2[e] = dY_e^T . D_e
         ops.moe_grouped_gemm(L.KIND_MXFP8, L.GROUP_K, L.EPI_F32, E, H, I, 0, seg,
                              self.dyq["col_q"], self.dq["col_q"], self.dyq["col_s"], cap // 32,
@@ -215,7 +224,7 @@ class MXFP8MoE:
         ops.moe_grouped_gemm(L.KIND_MXFP8, L.GROUP_M, L.EPI_BF16, E, cap, H, 2 * I, seg,
                              self.dhq["row_q"], self.w1["col_q"], self.dhq["row_s"], (2 * I) // 32,
                              self.w1["col_s"], (E * 2 * I) // 32, self.dxp, b_rows_per_expert=0,
-                             b_k_per_expert=2 * I)
+                             b_k_per_expert=2 * I, tile_m=self.tile_m)
         ops.moe_combine(self.dxp, inv, T, k, out=self.dx)
         # FC1 wgrad: dW1[e] = dH_e^T . X_e
         ops.moe_grouped_gemm(L.KIND_MXFP8, L.GROUP_K, L.EPI_F32, E, 2 * I, H, 0, seg,

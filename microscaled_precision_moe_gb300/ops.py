@@ -113,18 +113,19 @@ def nvfp4_quantize_weight(parts, out=None, ws=None):
 
 # ------------------------------------------------------------------ routing
 
-def moe_row_capacity(T: int, k: int, E: int) -> int:
-    return int(L.load().mpm_moe_row_capacity(T, k, E))
+def moe_row_capacity(T: int, k: int, E: int, pad: int = 128) -> int:
+    return int(L.load().mpm_moe_row_capacity(T, k, E, pad))
 
 
-def moe_build_segments(topk_ids, topk_prob, E: int, out=None, ws=None):
-    """(seg_offsets [E+1], perm [cap], inv_perm [T*k], row_prob [cap], cap)."""
+def moe_build_segments(topk_ids, topk_prob, E: int, out=None, ws=None, pad: int = 128):
+    """(seg_offsets [E+1], perm [cap], inv_perm [T*k], row_prob [cap], cap);
+    segments padded to ``pad`` rows (128, or 256 for the CTA-pair GEMM)."""
     lib = L.load()
     _need_cuda(topk_ids, topk_prob)
     assert topk_ids.dtype == torch.int32 and topk_prob.dtype == torch.float32
     T, k = topk_ids.shape
     dev = topk_ids.device
-    cap = moe_row_capacity(T, k, E)
+    cap = moe_row_capacity(T, k, E, pad)
     if out is None:
         out = (torch.empty(E + 1, dtype=torch.int32, device=dev),
                torch.empty(cap, dtype=torch.int32, device=dev),
@@ -135,8 +136,8 @@ def moe_build_segments(topk_ids, topk_prob, E: int, out=None, ws=None):
     if ws is None:
         ws = torch.empty(wsb, dtype=torch.uint8, device=dev)
     st = lib.mpm_moe_build_segments(_ptr(topk_ids.contiguous()), _ptr(topk_prob.contiguous()), T,
-                                    k, E, _ptr(seg), _ptr(perm), _ptr(inv), _ptr(rp), _ptr(ws),
-                                    ws.numel(), _stream(dev))
+                                    k, E, pad, _ptr(seg), _ptr(perm), _ptr(inv), _ptr(rp),
+                                    _ptr(ws), ws.numel(), _stream(dev))
     L.check(st, "mpm_moe_build_segments")
     return seg, perm, inv, rp, cap
 
@@ -184,7 +185,7 @@ def moe_combine(y_perm, inv_perm, T: int, k: int, out=None):
 
 def moe_grouped_gemm(kind, group, epilogue, E, a_rows, N, K, seg, a, b, sfa, sfa_cols, sfb,
                      sfb_cols, out, b_rows_per_expert=0, b_k_per_expert=0, alpha_a=None,
-                     alpha_b=None, row_prob=None, out2=None, aux=None, amax=None):
+                     alpha_b=None, row_prob=None, out2=None, aux=None, amax=None, tile_m=128):
     """One grouped block-scaled GEMM launch (see mpm_grouped_gemm_desc).
 
     a, b: uint8 code matrices [rows, pitch bytes]; out / out2 / aux: row-major
@@ -193,7 +194,7 @@ def moe_grouped_gemm(kind, group, epilogue, E, a_rows, N, K, seg, a, b, sfa, sfa
     lib = L.load()
     _need_cuda(a, b, sfa, sfb, out)
     d = L.GroupedGemmDesc()
-    d.kind, d.group, d.epilogue = kind, group, epilogue
+    d.kind, d.group, d.epilogue, d.tile_m = kind, group, epilogue, tile_m
     d.E, d.a_rows, d.N, d.K = E, a_rows, N, K
     d.seg_dev = None if seg is None else seg.data_ptr()
     d.a_dev, d.lda_bytes, d.a_total_rows = a.data_ptr(), a.stride(0), a.shape[0]

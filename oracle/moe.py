@@ -156,18 +156,19 @@ def fc1_epilogue(acc: np.ndarray, row_prob: np.ndarray, I: int) -> np.ndarray:
     return F.bf16_round(d)
 
 
-def nvfp4_moe_forward(x: np.ndarray, topk_ids, topk_prob, w1, w2, E: int):
+def nvfp4_moe_forward(x: np.ndarray, topk_ids, topk_prob, w1, w2, E: int, pad=ROW_PAD):
     """The full NVFP4 expert-layer forward.
 
     x [T, H] bf16 values; w1 [E, 2I, H]; w2 [E, H, I].  Returns a dict with
-    every intermediate the CUDA path materialises.
+    every intermediate the CUDA path materialises (in the permuted layout with
+    segments padded to ``pad`` rows; the padding changes the layout only).
     """
     T, H = x.shape
     k = np.asarray(topk_ids).shape[1]
     I = w1.shape[1] // 2
     # per-token activation quantisation of X (once per token)
     qx, sx, tsx = Q.nvfp4_quantize_per_token(x)
-    seg, perm, inv, row_prob = build_segments(topk_ids, topk_prob, E)
+    seg, perm, inv, row_prob = build_segments(topk_ids, topk_prob, E, pad)
     xq_deq = Q.nvfp4_dequantize(qx, sx, tsx)                 # [T, H]
     a1 = gather_rows(xq_deq, perm, k)                        # [R_pad, H]
     (w1p, w1s, w1g), (w2p, w2s, w2g) = nvfp4_weights(w1, w2)
@@ -220,7 +221,7 @@ def swiglu_backward(dd: np.ndarray, c1: np.ndarray, row_prob: np.ndarray, I: int
     return np.concatenate([dg, du], axis=1)
 
 
-def mxfp8_moe_fwd_bwd(x, topk_ids, topk_prob, w1, w2, dy, E: int):
+def mxfp8_moe_fwd_bwd(x, topk_ids, topk_prob, w1, w2, dy, E: int, pad=ROW_PAD):
     """End-to-end MXFP8 expert layer, forward and backward.
 
     Every GEMM operand is quantised from bf16: fprop uses row-wise copies,
@@ -230,7 +231,7 @@ def mxfp8_moe_fwd_bwd(x, topk_ids, topk_prob, w1, w2, dy, E: int):
     T, H = x.shape
     k = np.asarray(topk_ids).shape[1]
     I = w1.shape[1] // 2
-    seg, perm, inv, row_prob = build_segments(topk_ids, topk_prob, E)
+    seg, perm, inv, row_prob = build_segments(topk_ids, topk_prob, E, pad)
     xp = gather_rows(np.asarray(x, dtype=np.float64), perm, k)     # bf16 values
     # forward FC1
     b1 = np.stack([mx_rows(w1[e]) for e in range(E)])              # [E, 2I, H]

@@ -37,7 +37,9 @@ def test_pure_host_queries(lib):
     assert lib.mpm_version() == 100
     assert lib.mpm_scale_bytes(8288, 64) == 8320 * 64
     assert lib.mpm_scale_bytes(2048, 259) == 2048 * 260
-    assert lib.mpm_moe_row_capacity(32768, 8, 256) == 262144 + 128 * 256
+    assert lib.mpm_moe_row_capacity(32768, 8, 256, 128) == 262144 + 128 * 256
+    assert lib.mpm_moe_row_capacity(32768, 8, 256, 256) == 262144 + 256 * 256
+    assert lib.mpm_moe_row_capacity(32768, 8, 256, 64) == 0
     assert lib.mpm_status_string(7) == b"MPM_ERR_DEVICE_BOUNDS"
 
 
@@ -58,8 +60,9 @@ def test_host_validation_rejects_before_launch(lib):
     assert lib.mpm_mxfp8_quantize(fake, 4, 40, 40, 1, fake, fake, None, 0, None, None, None) == 2
     assert lib.mpm_mxfp8_quantize(fake, 64, 64, 64, 2, None, None, fake, 32, fake, None, None) == 2
     # segments: E too large, workspace too small
-    assert lib.mpm_moe_build_segments(fake, fake, 4, 2, 2048, fake, fake, fake, fake, fake, 1 << 20, None) == 2
-    assert lib.mpm_moe_build_segments(fake, fake, 4, 2, 8, fake, fake, fake, fake, fake, 0, None) == 2
+    assert lib.mpm_moe_build_segments(fake, fake, 4, 2, 2048, 128, fake, fake, fake, fake, fake, 1 << 20, None) == 2
+    assert lib.mpm_moe_build_segments(fake, fake, 4, 2, 8, 128, fake, fake, fake, fake, fake, 0, None) == 2
+    assert lib.mpm_moe_build_segments(fake, fake, 4, 2, 8, 100, fake, fake, fake, fake, fake, 1 << 20, None) == 2
     # GEMM descriptor: bad N, bad K, wgrad on NVFP4
     d = L.GroupedGemmDesc()
     d.kind, d.group, d.epilogue, d.E, d.a_rows, d.N, d.K = 0, 0, 0, 1, 128, 200, 256
@@ -74,5 +77,7 @@ def test_host_validation_rejects_before_launch(lib):
     assert lib.mpm_moe_grouped_gemm(C.byref(d), None) == 2
     d.K, d.group = 256, 1
     d.seg_dev = 0x10000
+    assert lib.mpm_moe_grouped_gemm(C.byref(d), None) == 4
+    d.group, d.tile_m = 0, 192                      # only 128 or 256
     assert lib.mpm_moe_grouped_gemm(C.byref(d), None) == 4
     assert lib.mpm_moe_grouped_gemm(None, None) == 1

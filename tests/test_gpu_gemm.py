@@ -38,28 +38,30 @@ def _assert_close(got, ref, what):
     assert ok, f"{what}: rel_frob={rf:.3e} max_err={mx:.3e} bound={bound:.3e}"
 
 
-def test_nvfp4_single_expert_gate_up():
+@pytest.mark.parametrize("tile_m", [128, 256])
+def test_nvfp4_single_expert_gate_up(tile_m):
     """128 x 2048 activations (0.1% x50 outliers) against jointly quantised
-    768 x 2048 gate and up weights -> 128 x 1536 fp32."""
+    768 x 2048 gate and up weights -> 128 x 1536 fp32 (one CTA per tile, or a
+    CTA pair whose second half lies past the 128 rows)."""
     ops, L = _ops(), _L()
     x, wg, wu = synth.single_expert_inputs(device="cuda")
     qx, sx, tsx = ops.nvfp4_quantize_per_token(x)
     qw, sw, tsw = ops.nvfp4_quantize_weight([wg[None].contiguous(), wu[None].contiguous()])
     out = torch.empty(128, 1536, dtype=torch.float32, device="cuda")
     ops.moe_grouped_gemm(L.KIND_NVFP4, L.GROUP_M, L.EPI_F32, 1, 128, 1536, 2048, None,
-                         qx, qw[0], sx, 128, sw, 128, out, alpha_a=tsx, alpha_b=tsw)
+                         qx, qw[0], sx, 128, sw, 128, out, alpha_a=tsx, alpha_b=tsw, tile_m=tile_m)
     torch.cuda.synchronize()
     assert ops.get_device_status() == 0
     ref = MO.nvfp4_gemm_single(np_bf16(x), np_bf16(wg), np_bf16(wu))["c"]
     _assert_close(out.cpu().numpy(), ref.astype(np.float32), "single-expert NVFP4")
 
 
-def _grouped_nvfp4_setup(shape, seed=0):
+def _grouped_nvfp4_setup(shape, seed=0, pad=128):
     ops = _ops()
     ids, prob = synth.routing(shape, seed)
     x = synth.moe_activations(shape, seed, device="cuda")
     w1, w2 = synth.moe_weights(shape, seed, device="cuda")
-    seg, perm, inv, rp, cap = ops.moe_build_segments(ids.cuda(), prob.cuda(), shape.E)
+    seg, perm, inv, rp, cap = ops.moe_build_segments(ids.cuda(), prob.cuda(), shape.E, pad=pad)
     return ids, prob, x, w1, w2, seg, perm, inv, rp, cap
 
 
@@ -100,10 +102,11 @@ def _chained_compare(d_gpu, y_gpu, out_gpu, r, k, what):
     assert Mx.rel_frobenius(out_gpu, r["out"]) < 1e-2, f"{what}: layer output"
 
 
-def test_nvfp4_grouped_fc1_swiglu_and_fc2():
+@pytest.mark.parametrize("tile_m", [128, 256])
+def test_nvfp4_grouped_fc1_swiglu_and_fc2(tile_m):
     shape = synth.scaled(synth.MOE_30B, T=300, H=512, I=256, E=6, k=4)
     ops, L = _ops(), _L()
-    ids, prob, x, w1, w2, seg, perm, inv, rp, cap = _grouped_nvfp4_setup(shape)
+    ids, prob, x, w1, w2, seg, perm, inv, rp, cap = _grouped_nvfp4_setup(shape, pad=tile_m)
     E, H, I, k = shape.E, shape.H, shape.I, shape.k
     qx, sx, tsx = ops.nvfp4_quantize_per_token(x)
     amax = torch.full((cap,), 7.0, dtype=torch.float32, device="cuda")    # gather zeroes it
@@ -114,30 +117,31 @@ def test_nvfp4_grouped_fc1_swiglu_and_fc2():
     ops.moe_grouped_gemm(L.KIND_NVFP4, L.GROUP_M, L.EPI_SWIGLU, E, cap, 2 * I, H, seg,
                          aq, q1.view(E * 2 * I, H // 2), as_, H // 16, s1, H // 16, d,
                          b_rows_per_expert=2 * I, alpha_a=ats, alpha_b=t1, row_prob=rp,
-                         out2=d, amax=amax)
+                         out2=d, amax=amax, tile_m=tile_m)
     qd, sd, tsd = ops.nvfp4_quantize_per_token(d, amax_in=amax, m_valid=seg[E:])
     y = torch.empty(cap, H, dtype=torch.bfloat16, device="cuda")
     ops.moe_grouped_gemm(L.KIND_NVFP4, L.GROUP_M, L.EPI_BF16, E, cap, H, I, seg,
                          qd, q2.view(E * H, I // 2), sd, I // 16, s2, I // 16, y,
-                         b_rows_per_expert=H, alpha_a=tsd, alpha_b=t2)
+                         b_rows_per_expert=H, alpha_a=tsd, alpha_b=t2, tile_m=tile_m)
     out = ops.moe_combine(y, inv, shape.T, k)
     torch.cuda.synchronize()
     assert ops.get_device_status() == 0
     with np.errstate(over="ignore"):
         r = MO.nvfp4_moe_forward(np_bf16(x), ids.numpy(), prob.numpy(), np_bf16(w1),
-                                 np_bf16(w2), E)
+                                 np_bf16(w2), E, pad=tile_m)
     R = int(r["seg"][-1])
     amax_ref = np.max(np.abs(np_bf16(d)[:R]), axis=1)
     assert np.array_equal(amax.cpu().numpy()[:R], amax_ref), "amax(D) equals the row max of D"
     _chained_compare(np_bf16(d), np_bf16(y), np_bf16(out), r, k, "NVFP4 layer")
 
 
-def test_nvfp4_fc2_on_identical_operands():
+@pytest.mark.parametrize("tile_m", [128, 256])
+def test_nvfp4_fc2_on_identical_operands(tile_m):
     """FC2 alone: the same seeded bf16 D quantised by both sides (byte-exact),
     then the grouped GEMM against the fp64 GEMM: strict tolerance."""
     shape = synth.scaled(synth.MOE_30B, T=400, H=768, I=512, E=5, k=3)
     ops, L = _ops(), _L()
-    ids, prob, x, w1, w2, seg, perm, inv, rp, cap = _grouped_nvfp4_setup(shape, seed=2)
+    ids, prob, x, w1, w2, seg, perm, inv, rp, cap = _grouped_nvfp4_setup(shape, seed=2, pad=tile_m)
     E, H, I = shape.E, shape.H, shape.I
     dsrc = synth.normal_bf16(2, 77, (cap, I), "cuda", std=0.05, outlier_p=1e-3, outlier_mul=20.0)
     qd, sd, tsd = ops.nvfp4_quantize_per_token(dsrc)
@@ -145,8 +149,9 @@ def test_nvfp4_fc2_on_identical_operands():
     y = torch.empty(cap, H, dtype=torch.bfloat16, device="cuda")
     ops.moe_grouped_gemm(L.KIND_NVFP4, L.GROUP_M, L.EPI_BF16, E, cap, H, I, seg,
                          qd, q2.view(E * H, I // 2), sd, I // 16, s2, I // 16, y,
-                         b_rows_per_expert=H, alpha_a=tsd, alpha_b=t2)
+                         b_rows_per_expert=H, alpha_a=tsd, alpha_b=t2, tile_m=tile_m)
     torch.cuda.synchronize()
+    assert ops.get_device_status() == 0
     segn = seg.cpu().numpy()
     R = int(segn[-1])
     dn = np_bf16(dsrc)[:R]
@@ -158,14 +163,15 @@ def test_nvfp4_fc2_on_identical_operands():
     _assert_close(np_bf16(y)[:R], ref, "NVFP4 FC2 (identical operands)")
 
 
-def test_nvfp4_layer_api():
+@pytest.mark.parametrize("tile_m", [128, 256])
+def test_nvfp4_layer_api(tile_m):
     """The public layer API (NVFP4MoE) on a reduced 30B-A3B-shaped layer."""
     from microscaled_precision_moe_gb300.moe import NVFP4MoE, NVFP4Weights
     shape = synth.scaled(synth.MOE_30B, T=512, H=1024, I=256, E=16)
     ids, prob = synth.routing(shape)
     x = synth.moe_activations(shape, device="cuda")
     w1, w2 = synth.moe_weights(shape, device="cuda")
-    layer = NVFP4MoE(shape.T, shape.H, shape.I, shape.E, shape.k)
+    layer = NVFP4MoE(shape.T, shape.H, shape.I, shape.E, shape.k, tile_m=tile_m)
     w = NVFP4Weights.quantize(w1, w2)
     out = layer.forward(x, ids.cuda(), prob.cuda(), w).clone()
     out2 = layer.forward(x, ids.cuda(), prob.cuda(), w)
@@ -173,14 +179,15 @@ def test_nvfp4_layer_api():
     assert torch.equal(out, out2), "deterministic"
     with np.errstate(over="ignore"):
         r = MO.nvfp4_moe_forward(np_bf16(x), ids.numpy(), prob.numpy(), np_bf16(w1),
-                                 np_bf16(w2), shape.E)
+                                 np_bf16(w2), shape.E, pad=tile_m)
     _chained_compare(np_bf16(layer.d), np_bf16(layer.y), np_bf16(out), r, shape.k, "NVFP4MoE")
 
 
-def test_mxfp8_grouped_fprop_dgrad_wgrad():
+@pytest.mark.parametrize("tile_m", [128, 256])
+def test_mxfp8_grouped_fprop_dgrad_wgrad(tile_m):
     shape = synth.scaled(synth.MOE_30B_BWD, T=256, H=256, I=256, E=4, k=2)
     ops, L = _ops(), _L()
-    ids, prob, x, w1, w2, seg, perm, inv, rp, cap = _grouped_nvfp4_setup(shape)
+    ids, prob, x, w1, w2, seg, perm, inv, rp, cap = _grouped_nvfp4_setup(shape, pad=tile_m)
     E, H, I, k = shape.E, shape.H, shape.I, shape.k
     xp = ops.moe_gather_bf16(x, perm, seg, E, k, cap)
     mx = ops.mxfp8_quantize(xp, m_valid=seg[E:])
@@ -190,14 +197,15 @@ def test_mxfp8_grouped_fprop_dgrad_wgrad():
     y = torch.empty(cap, 256, dtype=torch.bfloat16, device="cuda")
     ops.moe_grouped_gemm(L.KIND_MXFP8, L.GROUP_M, L.EPI_BF16, E, cap, 256, H, seg,
                          mx["row_q"], wq["row_q"], mx["row_s"], H // 32, wq["row_s"], H // 32,
-                         y, b_rows_per_expert=256)
+                         y, b_rows_per_expert=256, tile_m=tile_m)
     # dgrad: dX = G . W_e with the column-wise copy of W ([H, E*256], stored transposed)
     gy = synth.normal_bf16(9, 98, (cap, 256), "cuda", std=1e-3)
     gq = ops.mxfp8_quantize(gy, colwise=False)
     dx = torch.empty(cap, H, dtype=torch.bfloat16, device="cuda")
     ops.moe_grouped_gemm(L.KIND_MXFP8, L.GROUP_M, L.EPI_BF16, E, cap, H, 256, seg,
                          gq["row_q"], wq["col_q"], gq["row_s"], 256 // 32, wq["col_s"],
-                         (E * 256) // 32, dx, b_rows_per_expert=0, b_k_per_expert=256)
+                         (E * 256) // 32, dx, b_rows_per_expert=0, b_k_per_expert=256,
+                         tile_m=tile_m)
     # wgrad: dW_e = gy_e^T . X_e over each expert's rows (column-wise copies)
     gc = ops.mxfp8_quantize(gy, rowwise=False, m_valid=seg[E:])
     dw = torch.empty(E, 256, H, dtype=torch.float32, device="cuda")
@@ -224,7 +232,8 @@ def test_mxfp8_grouped_fprop_dgrad_wgrad():
     _assert_close(dw.cpu().numpy(), ref_dw, "MXFP8 wgrad")
 
 
-def test_mxfp8_layer_fwd_bwd_api():
+@pytest.mark.parametrize("tile_m", [128, 256])
+def test_mxfp8_layer_fwd_bwd_api(tile_m):
     """The MXFP8 layer (forward and backward) through MXFP8MoE against the
     oracle.  FC1's outputs (C = gate|up, D) come from identical operands and
     meet the GEMM tolerance; later stages consume re-quantised tensors, so a
@@ -236,7 +245,7 @@ def test_mxfp8_layer_fwd_bwd_api():
     x = synth.moe_activations(shape, device="cuda")
     w1, w2 = synth.moe_weights(shape, device="cuda")
     dy = synth.moe_grad_out(shape, device="cuda")
-    layer = MXFP8MoE(shape.T, shape.H, shape.I, shape.E, shape.k)
+    layer = MXFP8MoE(shape.T, shape.H, shape.I, shape.E, shape.k, tile_m=tile_m)
     layer.quantize_weights(w1, w2)
     out = layer.forward(x, ids.cuda(), prob.cuda())
     dx, dw1, dw2 = layer.backward(dy)
@@ -245,7 +254,7 @@ def test_mxfp8_layer_fwd_bwd_api():
     assert ops.get_device_status() == 0
     with np.errstate(over="ignore"):
         r = MO.mxfp8_moe_fwd_bwd(np_bf16(x), ids.numpy(), prob.numpy(), np_bf16(w1),
-                                 np_bf16(w2), np_bf16(dy), shape.E)
+                                 np_bf16(w2), np_bf16(dy), shape.E, pad=tile_m)
     R = int(r["seg"][-1])
     _assert_close(np_bf16(layer.c1)[:R], r["c1"], "MXFP8 FC1 C")
     _assert_close(np_bf16(layer.d)[:R], r["d"], "MXFP8 FC1 D")

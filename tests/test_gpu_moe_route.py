@@ -23,11 +23,11 @@ def _ops():
     return ops
 
 
-def _check_segments(ids, prob, E):
+def _check_segments(ids, prob, E, pad=128):
     ops = _ops()
-    seg, perm, inv, rp, cap = ops.moe_build_segments(ids.cuda(), prob.cuda(), E)
+    seg, perm, inv, rp, cap = ops.moe_build_segments(ids.cuda(), prob.cuda(), E, pad=pad)
     torch.cuda.synchronize()
-    rseg, rperm, rinv, rrp = MO.build_segments(ids.numpy(), prob.numpy(), E)
+    rseg, rperm, rinv, rrp = MO.build_segments(ids.numpy(), prob.numpy(), E, pad)
     assert_bytes_equal(seg.cpu().numpy(), rseg, "seg_offsets")
     R = int(rseg[-1])
     assert R <= cap
@@ -39,15 +39,16 @@ def _check_segments(ids, prob, E):
     return seg, perm, inv, rp, cap
 
 
+@pytest.mark.parametrize("pad", [128, 256])
 @pytest.mark.parametrize("shape", [
     synth.scaled(synth.MOE_30B, T=1000, E=16),
     synth.scaled(synth.MOE_671B, T=3000, H=64, I=64),
     synth.MOE_30B,
     synth.MOE_671B,
 ])
-def test_segments_workloads(shape):
+def test_segments_workloads(shape, pad):
     ids, prob = synth.routing(shape)
-    _check_segments(ids, prob, shape.E)
+    _check_segments(ids, prob, shape.E, pad)
 
 
 def test_segments_edge_cases():
@@ -59,6 +60,7 @@ def test_segments_edge_cases():
     # exactly 128 rows per expert (no padding)
     ids = torch.arange(256, dtype=torch.int32).remainder(2).view(128, 2)
     _check_segments(ids, torch.full((128, 2), 0.5), 2)
+    _check_segments(ids, torch.full((128, 2), 0.5), 2, pad=256)
 
 
 def test_segments_bad_id_sets_device_status():

@@ -58,6 +58,9 @@ def test_segments_brute_force():
     ids2 = np.zeros((5, 1), dtype=np.int32) + 2
     seg2, _, _, _ = MO.build_segments(ids2, np.ones((5, 1), np.float32), 4)
     assert list(seg2) == [0, 0, 0, 128, 128]
+    seg3, perm3, _, _ = MO.build_segments(ids, prob, E, pad=256)
+    assert np.all(np.diff(seg3) % 256 == 0)
+    assert np.array_equal(perm3[perm3 >= 0], perm[perm >= 0])   # same order, other padding
 
 
 def test_grouped_gemm_vs_loops():
