@@ -85,6 +85,21 @@ bool make_sf_tmap(CUtensorMap* m, const void* base, long long atoms, int atoms_p
   return r == CUDA_SUCCESS;
 }
 
+// bf16 [rows, cols] output with row pitch `ld` elements: 128-row x 64-column
+// boxes, 128-byte swizzle (the staging layout of the TMA-store epilogues)
+bool make_out_tmap(CUtensorMap* m, const void* base, long long cols, long long rows, long long ld) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)(ld * 2)};
+  cuuint32_t box[2] = {64, 128};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 }  // namespace
 
 extern "C" {
@@ -302,10 +317,17 @@ mpm_status mpm_moe_grouped_gemm(const mpm_grouped_gemm_desc* d, cudaStream_t str
     CUtensorMap tsa, tsb;
     if (!make_sf_tmap(&tsa, d->sfa_dev, atoms_a, kind_atoms)) return MPM_ERR_CUDA;
     if (!make_sf_tmap(&tsb, d->sfb_dev, atoms_b, kind_atoms)) return MPM_ERR_CUDA;
+    CUtensorMap tout;
+    std::memset(&tout, 0, sizeof(tout));
+    if (d->epilogue == MPM_EPI_BF16) {
+      if (!make_out_tmap(&tout, d->out_dev, d->N, d->a_rows, d->ldo)) return MPM_ERR_CUDA;
+    } else if (swiglu) {
+      if (!make_out_tmap(&tout, d->out2_dev, d->N / 2, d->a_rows, d->ldo2)) return MPM_ERR_CUDA;
+    }
     const int n_tiles = (int)(swiglu ? (d->N / 2) / 128 : d->N / 256);
     const long long n_tasks = (long long)n_tiles * ((d->a_rows + 255) / 256);
-    return cuda_status(mpm::launch_grouped_gemm_pair(d->kind, d->epilogue, ta, tb, tsa, tsb, a,
-                                                     n_tiles, n_tasks, stream));
+    return cuda_status(mpm::launch_grouped_gemm_pair(d->kind, d->epilogue, ta, tb, tsa, tsb, tout,
+                                                     a, n_tiles, n_tasks, stream));
   }
   dim3 grid;
   if (d->group == MPM_GROUP_M) {

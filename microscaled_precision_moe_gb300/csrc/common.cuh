@@ -187,6 +187,19 @@ MPM_DEV void tma_load_2d_pair(uint32_t dst, const void* tmap, int x, int y, uint
       " [%0], [%1, {%2, %3}], [%4];"
       :: "r"(dst), "l"(tmap), "r"(x), "r"(y), "r"(bar_cluster) : "memory");
 }
+// TMA tensor store of a shared-memory box to global memory (bulk group)
+MPM_DEV void tma_store_2d(const void* tmap, int x, int y, uint32_t src) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];"
+               :: "l"(tmap), "r"(x), "r"(y), "r"(src) : "memory");
+}
+MPM_DEV void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// wait until this thread's bulk groups no longer read shared memory
+MPM_DEV void bulk_wait_group_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+MPM_DEV void bulk_wait_group0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+MPM_DEV void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" :: "r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
+               : "memory");
+}
 // named barrier among a subset of warps
 MPM_DEV void named_sync(uint32_t id, uint32_t nthreads) {
   asm volatile("bar.sync %0, %1;" :: "r"(id), "r"(nthreads) : "memory");

@@ -16,8 +16,9 @@
 // One CTA computes one 128 x 256 output tile:
 //   warp 0 lane 0  TMA producer: A/B tiles (128-byte swizzle) and the 128x4
 //                  scale tiles (bulk copies) into a 4-stage shared-memory ring
-//   warp 1 lane 0  MMA issuer: scale tiles -> TMEM (tcgen05.cp), then
-//                  tcgen05.mma with block scaling; commits free ring slots
+//   warp 3 lane 0  copies each stage's scale tiles into TMEM (tcgen05.cp)
+//   warp 1 lane 0  MMA issuer: tcgen05.mma with block scaling once a stage's
+//                  scale tiles are in TMEM; commits free ring slots
 //   warp 2         allocates / frees the 512 TMEM columns
 //   warps 0-3      epilogue: tcgen05.ld of the fp32 accumulator (one row per
 //                  thread), outer scales, optional SwiGLU / SwiGLU backward,
@@ -59,7 +60,7 @@ template <int KIND>
 constexpr int smem_bytes() {
   return 1024 /*alignment slack*/ +
          STAGES * (A_STAGE + B_STAGE + KindCfg<KIND>::kSfaBytes + KindCfg<KIND>::kSfbBytes) +
-         (2 * STAGES + 1) * 8 + 16;
+         (3 * STAGES + 1) * 8 + 16;
 }
 
 MPM_DEV float silu_f(float g) { return g / (1.0f + expf(-g)); }
@@ -151,6 +152,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tma_a,
   const uint32_t sBar = sSFB + STAGES * Cfg::kSfbBytes;
   const uint32_t bar_full = sBar, bar_empty = sBar + 8 * STAGES, bar_acc = sBar + 16 * STAGES;
   const uint32_t sTmemHolder = bar_acc + 8;
+  const uint32_t bar_sf = sTmemHolder + 8;     // scale tiles of a stage are in TMEM
   volatile uint32_t* tmem_holder =
       reinterpret_cast<volatile uint32_t*>(gbase + (sTmemHolder - base));
 
@@ -160,6 +162,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tma_a,
       mbar_init(bar_empty + 8 * s, 1);
     }
     mbar_init(bar_acc, 1);
+    for (int s = 0; s < STAGES; ++s) mbar_init(bar_sf + 8 * s, 1);
     fence_mbar_init();
     fence_proxy_async();
     prefetch_tmap(&tma_a);
@@ -206,10 +209,36 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tma_a,
     }
   } else if (warp == 1 && lane == 0) {
     // ======================================================== MMA issuer
+    // Waits until the copy thread (warp 3) has put the stage's scale tiles in
+    // tensor memory; copies and MMAs come from different threads so that the
+    // copies of one stage can run alongside the MMAs of the previous one.
+    bool ok = true;
+    for (int kb = 0; ok && kb < num_kb; ++kb) {
+      const int s = kb % STAGES;
+      if (!mbar_wait(bar_sf + 8 * s, (uint32_t)(kb / STAGES) & 1u, p.status)) break;
+      tc_fence_after();
+      const uint32_t sf_col = tmem + SF_TMEM_BASE + s * Cfg::kSfTmemPerStage;
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks) {
+        const uint64_t adesc = sdesc_sw128(sA + s * A_STAGE + ks * 32);
+        const uint64_t bdesc = sdesc_sw128(sB + s * B_STAGE + ks * 32);
+        const uint32_t acc = (kb > 0 || ks > 0) ? 1u : 0u;
+        if (KIND == MPM_KIND_NVFP4) {
+          const uint32_t idesc = idesc_block_scaled(Cfg::kFmt, BN, Cfg::kUe8m0, 0);
+          mma_nvf4(tmem, adesc, bdesc, idesc, sf_col + ks * 4, sf_col + 16 + ks * 8, acc);
+        } else {
+          const uint32_t idesc = idesc_block_scaled(Cfg::kFmt, BN, Cfg::kUe8m0, (uint32_t)ks);
+          mma_mxf8(tmem, adesc, bdesc, idesc, sf_col, sf_col + 4, acc);
+        }
+      }
+      tc_commit(bar_empty + 8 * s);
+    }
+    tc_commit(bar_acc);
+  } else if (warp == 3 && lane == 0) {
+    // ======================================================== scale-tile copies
     for (int kb = 0; kb < num_kb; ++kb) {
       const int s = kb % STAGES;
-      const uint32_t ph = (uint32_t)(kb / STAGES) & 1u;
-      if (!mbar_wait(bar_full + 8 * s, ph, p.status)) break;
+      if (!mbar_wait(bar_full + 8 * s, (uint32_t)(kb / STAGES) & 1u, p.status)) break;
       tc_fence_after();
       const uint32_t sf_col = tmem + SF_TMEM_BASE + s * Cfg::kSfTmemPerStage;
       if (KIND == MPM_KIND_NVFP4) {
@@ -228,22 +257,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tma_a,
         for (int nt = 0; nt < 2; ++nt)
           tc_cp_32x128b_x4(sf_col + 4 + nt * 4, sdesc_sf(sSFB + s * Cfg::kSfbBytes + nt * 512));
       }
-#pragma unroll
-      for (int ks = 0; ks < 4; ++ks) {
-        const uint64_t adesc = sdesc_sw128(sA + s * A_STAGE + ks * 32);
-        const uint64_t bdesc = sdesc_sw128(sB + s * B_STAGE + ks * 32);
-        const uint32_t acc = (kb > 0 || ks > 0) ? 1u : 0u;
-        if (KIND == MPM_KIND_NVFP4) {
-          const uint32_t idesc = idesc_block_scaled(Cfg::kFmt, BN, Cfg::kUe8m0, 0);
-          mma_nvf4(tmem, adesc, bdesc, idesc, sf_col + ks * 4, sf_col + 16 + ks * 8, acc);
-        } else {
-          const uint32_t idesc = idesc_block_scaled(Cfg::kFmt, BN, Cfg::kUe8m0, (uint32_t)ks);
-          mma_mxf8(tmem, adesc, bdesc, idesc, sf_col, sf_col + 4, acc);
-        }
-      }
-      tc_commit(bar_empty + 8 * s);
+      tc_commit(bar_sf + 8 * s);
     }
-    tc_commit(bar_acc);
   }
   __syncwarp();
 

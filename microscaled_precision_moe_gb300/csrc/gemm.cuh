@@ -31,6 +31,7 @@ cudaError_t launch_grouped_gemm(int kind, int epi, const CUtensorMap& ta, const 
                                 const GemmArgs& a, dim3 grid, cudaStream_t s);
 cudaError_t launch_grouped_gemm_pair(int kind, int epi, const CUtensorMap& ta,
                                      const CUtensorMap& tb, const CUtensorMap& tsfa,
-                                     const CUtensorMap& tsfb, const GemmArgs& a, int n_tiles,
-                                     long long n_tasks, cudaStream_t s);
+                                     const CUtensorMap& tsfb, const CUtensorMap& tout,
+                                     const GemmArgs& a, int n_tiles, long long n_tasks,
+                                     cudaStream_t s);
 }  // namespace mpm

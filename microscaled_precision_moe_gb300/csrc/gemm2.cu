@@ -9,13 +9,19 @@
 //     256 B rows) plus the scale tiles of its A rows and of all 256 B rows;
 //     every TMA load, the peer's included, completes on the leader CTA's
 //     barrier (cp.async.bulk.tensor .cta_group::2);
-//   * the leader's MMA thread copies the scale tiles of both CTAs into their
-//     tensor memories and issues tcgen05.mma.cta_group::2 (M = 256, N = 256):
-//     each SM reads only half of B from its shared memory, which halves the
-//     B traffic through shared memory compared with one CTA per 128x256 tile;
-//   * each CTA's four epilogue warps drain its 128 x 256 accumulator; in the
-//     SwiGLU and bf16 epilogues the accumulator is released to the next tile
-//     as soon as it is in registers, so stores overlap the next tile's MMAs;
+//   * a copy warp of the leader copies the scale tiles of both CTAs into their
+//     tensor memories (tcgen05.cp.cta_group::2) and signals a per-stage
+//     barrier; the leader's MMA thread waits on it and issues
+//     tcgen05.mma.cta_group::2 (M = 256, N = 256).  Issuing the copies from
+//     their own thread lets them run alongside the previous stage's MMAs
+//     instead of in front of the next ones (one thread's tcgen05 operations
+//     execute in issue order); each SM reads only half of B from its shared
+//     memory;
+//   * each CTA's eight epilogue warps (two per TMEM lane quarter, each taking
+//     half of the columns) drain its 128 x 256 accumulator; in the SwiGLU and
+//     bf16 epilogues the accumulator is released to the next tile as soon as
+//     it is in registers, so the activation math and the stores overlap the
+//     next tile's MMAs;
 //   * clusters loop over tiles (expert-segment M pairs x N tiles) in a fixed
 //     stride, so the shared-memory ring never drains between tiles.
 //
@@ -30,7 +36,11 @@ namespace pairk {
 constexpr int BM = 128;              // rows per CTA; 256 per pair
 constexpr int BN = 256;
 constexpr int BKB = 128;             // bytes of K per stage
-constexpr int NTHREADS = 192;        // warp 0 TMA, warp 1 MMA/TMEM, warps 2-5 epilogue
+// warp 0 TMA, warp 1 MMA + TMEM allocation, warp 2 scale-tile copies,
+// warps 3-10 epilogue (two warps per TMEM lane quarter, each half the columns)
+constexpr int NTHREADS = 352;
+constexpr int EPI_WARP0 = 3;
+constexpr int EPI_THREADS = 256;
 constexpr int A_STAGE = BM * BKB;    // 16 KB
 constexpr int B_STAGE = 128 * BKB;   // this CTA's half of B: 16 KB
 constexpr uint32_t TMEM_COLS = 512;
@@ -43,7 +53,7 @@ template <> struct Cfg<MPM_KIND_NVFP4> {
   static constexpr int kSfaBytes = 4 * 512;
   static constexpr int kSfbBytes = 2 * 4 * 512;
   static constexpr int kSfTmemPerStage = 16 + 32;
-  static constexpr int kStages = 5;
+  static constexpr int kStages = 4;
   static constexpr uint32_t kFmt = 1, kUe8m0 = 0;
 };
 template <> struct Cfg<MPM_KIND_MXFP8> {
@@ -52,7 +62,7 @@ template <> struct Cfg<MPM_KIND_MXFP8> {
   static constexpr int kSfaBytes = 512;
   static constexpr int kSfbBytes = 2 * 512;
   static constexpr int kSfTmemPerStage = 4 + 8;
-  static constexpr int kStages = 6;
+  static constexpr int kStages = 4;
   static constexpr uint32_t kFmt = 0, kUe8m0 = 1;
 };
 
@@ -60,12 +70,21 @@ template <int KIND>
 constexpr int stage_bytes() {
   return A_STAGE + B_STAGE + Cfg<KIND>::kSfaBytes + Cfg<KIND>::kSfbBytes;
 }
+// bf16 output staging for the TMA-store epilogues: 128 rows x 256 columns,
+// as four 128-row x 64-column boxes (128 bytes per row, 128-byte swizzle)
+constexpr int OUT_BOX_COLS = 64;
+constexpr int OUT_BOX_BYTES = BM * OUT_BOX_COLS * 2;    // 16 KB
+constexpr int STAGE_OUT_BYTES = 4 * OUT_BOX_BYTES;      // 64 KB
+
 template <int KIND>
 constexpr int smem_bytes() {
-  return 1024 + Cfg<KIND>::kStages * stage_bytes<KIND>() + (3 * Cfg<KIND>::kStages + 4) * 8 + 32;
+  return 1024 + Cfg<KIND>::kStages * stage_bytes<KIND>() + STAGE_OUT_BYTES +
+         (4 * Cfg<KIND>::kStages + 4) * 8 + 32;
 }
 
-MPM_DEV float silu_f(float g) { return g / (1.0f + expf(-g)); }
+// epilogue activation: fast exponential and division (the result is rounded
+// to bf16 right after, far coarser than their error)
+MPM_DEV float silu_f(float g) { return __fdividef(g, 1.0f + __expf(-g)); }
 MPM_DEV uint32_t pack_bf16(float lo, float hi) {
   __nv_bfloat162 b = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&b);
@@ -116,6 +135,7 @@ MPM_DEV Task task_of(const GemmArgs& p, long long t, int n_tiles, int* bad) {
 
 struct PairMaps {
   CUtensorMap a, b, sfa, sfb;
+  CUtensorMap out;    // bf16 output of the BF16 epilogue / D of the SwiGLU epilogues
 };
 
 template <int KIND, int EPI>
@@ -136,9 +156,11 @@ grouped_gemm_pair_kernel(const __grid_constant__ PairMaps maps, const GemmArgs p
   const uint32_t sB = sA + S * A_STAGE;
   const uint32_t sSFA = sB + S * B_STAGE;
   const uint32_t sSFB = sSFA + S * C::kSfaBytes;
-  const uint32_t sBar = sSFB + S * C::kSfbBytes;
+  const uint32_t sOut = sSFB + S * C::kSfbBytes;        // 1024-aligned (stage sizes are)
+  const uint32_t sBar = sOut + STAGE_OUT_BYTES;
   const uint32_t bar_full = sBar, bar_empty = sBar + 8 * S;
   const uint32_t bar_accf = sBar + 16 * S, bar_acce = bar_accf + 8;
+  const uint32_t bar_sf = bar_acce + 8 + 32;   // scale tiles of a stage are in TMEM
   const uint32_t sTmem = bar_acce + 8;
   const uint32_t sFlag = sTmem + 8;
   volatile uint32_t* tmem_holder = reinterpret_cast<volatile uint32_t*>(gbase + (sTmem - base));
@@ -151,6 +173,7 @@ grouped_gemm_pair_kernel(const __grid_constant__ PairMaps maps, const GemmArgs p
     }
     mbar_init(bar_accf, 1);
     mbar_init(bar_acce, 2);          // one arrive from each CTA's epilogue
+    for (int s = 0; s < S; ++s) mbar_init(bar_sf + 8 * s, 1);
     *fail_flag = 0;
     fence_mbar_init();
     fence_proxy_async();
@@ -158,6 +181,8 @@ grouped_gemm_pair_kernel(const __grid_constant__ PairMaps maps, const GemmArgs p
     prefetch_tmap(&maps.b);
     prefetch_tmap(&maps.sfa);
     prefetch_tmap(&maps.sfb);
+    if (EPI == MPM_EPI_BF16 || EPI == MPM_EPI_SWIGLU || EPI == MPM_EPI_SWIGLU_SAVE)
+      prefetch_tmap(&maps.out);
   }
   if (warp == 1) {
     tmem_alloc_pair(sTmem, TMEM_COLS);
@@ -205,16 +230,44 @@ grouped_gemm_pair_kernel(const __grid_constant__ PairMaps maps, const GemmArgs p
   } else if (warp == 1 && lane == 0 && rank == 0) {
     // ======================================================== MMA issuer (leader only)
     uint32_t it = 0, j = 0;
-    for (long long t = cid; t < n_tasks; t += ncl, ++j) {
+    bool ok = true;
+    for (long long t = cid; ok && t < n_tasks; t += ncl, ++j) {
       const Task k = task_of<KIND, EPI>(p, t, n_tiles, &bad);
       if (!k.valid) break;
       if (!mbar_wait_cluster(bar_acce, (j & 1u) ^ 1u, p.status)) break;
       tc_fence_after();
-      bool ok = true;
       for (int kb = 0; kb < k.num_kb; ++kb, ++it) {
         const int s = it % S;
-        const uint32_t ph = (it / S) & 1u;
-        if (!mbar_wait_cluster(bar_full + 8 * s, ph, p.status)) { ok = false; break; }
+        if (!mbar_wait_cluster(bar_sf + 8 * s, (it / S) & 1u, p.status)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t sf_col = tmem + SF_TMEM_BASE + s * C::kSfTmemPerStage;
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks) {
+          const uint64_t adesc = sdesc_sw128(sA + s * A_STAGE + ks * 32);
+          const uint64_t bdesc = sdesc_sw128(sB + s * B_STAGE + ks * 32);
+          const uint32_t acc = (kb > 0 || ks > 0) ? 1u : 0u;
+          if (KIND == MPM_KIND_NVFP4) {
+            const uint32_t idesc = idesc_block_scaled(C::kFmt, BN, C::kUe8m0, 0, 256);
+            mma_nvf4_pair(tmem, adesc, bdesc, idesc, sf_col + ks * 4, sf_col + 16 + ks * 8, acc);
+          } else {
+            const uint32_t idesc = idesc_block_scaled(C::kFmt, BN, C::kUe8m0, (uint32_t)ks, 256);
+            mma_mxf8_pair(tmem, adesc, bdesc, idesc, sf_col, sf_col + 4, acc);
+          }
+        }
+        tc_commit_pair(bar_empty + 8 * s, (uint16_t)3);
+        if (kb + 1 == k.num_kb) tc_commit_pair(bar_accf, (uint16_t)3);
+      }
+    }
+  } else if (warp == 2 && lane == 0 && rank == 0) {
+    // ======================================================== scale-tile copies (leader only)
+    uint32_t it = 0;
+    bool ok = true;
+    for (long long t = cid; ok && t < n_tasks; t += ncl) {
+      const Task k = task_of<KIND, EPI>(p, t, n_tiles, &bad);
+      if (!k.valid) break;
+      for (int kb = 0; kb < k.num_kb; ++kb, ++it) {
+        const int s = it % S;
+        if (!mbar_wait_cluster(bar_full + 8 * s, (it / S) & 1u, p.status)) { ok = false; break; }
         tc_fence_after();
         const uint32_t sf_col = tmem + SF_TMEM_BASE + s * C::kSfTmemPerStage;
         if (KIND == MPM_KIND_NVFP4) {
@@ -232,36 +285,24 @@ grouped_gemm_pair_kernel(const __grid_constant__ PairMaps maps, const GemmArgs p
           for (int h = 0; h < 2; ++h)
             tc_cp_32x128b_x4_pair(sf_col + 4 + h * 4, sdesc_sf(sSFB + s * C::kSfbBytes + h * 512));
         }
-#pragma unroll
-        for (int ks = 0; ks < 4; ++ks) {
-          const uint64_t adesc = sdesc_sw128(sA + s * A_STAGE + ks * 32);
-          const uint64_t bdesc = sdesc_sw128(sB + s * B_STAGE + ks * 32);
-          const uint32_t acc = (kb > 0 || ks > 0) ? 1u : 0u;
-          if (KIND == MPM_KIND_NVFP4) {
-            const uint32_t idesc = idesc_block_scaled(C::kFmt, BN, C::kUe8m0, 0, 256);
-            mma_nvf4_pair(tmem, adesc, bdesc, idesc, sf_col + ks * 4, sf_col + 16 + ks * 8, acc);
-          } else {
-            const uint32_t idesc = idesc_block_scaled(C::kFmt, BN, C::kUe8m0, (uint32_t)ks, 256);
-            mma_mxf8_pair(tmem, adesc, bdesc, idesc, sf_col, sf_col + 4, acc);
-          }
-        }
-        tc_commit_pair(bar_empty + 8 * s, (uint16_t)3);
+        asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];"
+                     :: "r"(bar_sf + 8 * s) : "memory");
       }
-      tc_commit_pair(bar_accf, (uint16_t)3);
-      if (!ok) break;
     }
-  } else if (warp >= 2) {
+  } else if (warp >= EPI_WARP0) {
     // ======================================================== epilogue (both CTAs)
     const int q = warp & 3;                     // TMEM lane quarter of this warp
+    const int half = (warp - EPI_WARP0) >> 2;   // which half of the columns
     const int r = q * 32 + lane;                // row within this CTA's 128 rows
     const uint32_t trow = tmem + ((uint32_t)(q * 32) << 16);
+    const bool leader_thread = (threadIdx.x == EPI_WARP0 * 32);
     uint32_t j = 0;
     for (long long t = cid; t < n_tasks; t += ncl, ++j) {
       const Task k = task_of<KIND, EPI>(p, t, n_tiles, &bad);
       if (!k.valid) break;
       const bool w_ok = mbar_wait_cluster(bar_accf, j & 1u, p.status);
       if (!w_ok) *fail_flag = 1;
-      named_sync(1, 128);
+      named_sync(1, EPI_THREADS);
       if (*fail_flag) break;
       tc_fence_after();
       const long long grow = k.row_pair + rank * BM + r;
@@ -273,79 +314,122 @@ grouped_gemm_pair_kernel(const __grid_constant__ PairMaps maps, const GemmArgs p
       }
       uint32_t v[32], u[32];
       if (EPI == MPM_EPI_SWIGLU || EPI == MPM_EPI_SWIGLU_SAVE) {
+        // this thread: D columns [64*half, 64*half + 64) of the tile
         const float prob = row_ok ? p.row_prob[grow] : 0.0f;
-        uint32_t dw[64];
+        uint32_t dw[32];
         float amax = 0.0f;
+        uint32_t v2[32], u2[32];
+        // the thread's whole share of the accumulator in flight at once, one
+        // wait, then the accumulator goes back to the MMA before any math
+        tmem_ld_32x32b_x32(trow + (half * 2) * 32, v);
+        tmem_ld_32x32b_x32(trow + 128 + (half * 2) * 32, u);
+        tmem_ld_32x32b_x32(trow + (half * 2 + 1) * 32, v2);
+        tmem_ld_32x32b_x32(trow + 128 + (half * 2 + 1) * 32, u2);
+        tmem_ld_wait();
+        tc_fence_before();
+        named_sync(1, EPI_THREADS);
+        if (leader_thread) mbar_arrive_cluster(acce_leader);
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          tmem_ld_32x32b_x32(trow + c * 32, v);
-          tmem_ld_32x32b_x32(trow + 128 + c * 32, u);
-          tmem_ld_wait();
+        for (int cc = 0; cc < 2; ++cc) {
+          const int c = half * 2 + cc;
+          const uint32_t* gv = cc ? v2 : v;
+          const uint32_t* uv = cc ? u2 : u;
           if (EPI == MPM_EPI_SWIGLU_SAVE && row_ok) {
             __nv_bfloat16* og = static_cast<__nv_bfloat16*>(p.out) + grow * p.ldo + k.n0 + c * 32;
             __nv_bfloat16* ou = og + p.N / 2;
 #pragma unroll
             for (int jj = 0; jj < 32; jj += 8) {
               uint4 wg, wu;
-              wg.x = pack_bf16(__fmul_rn(__uint_as_float(v[jj]), alpha), __fmul_rn(__uint_as_float(v[jj + 1]), alpha));
-              wg.y = pack_bf16(__fmul_rn(__uint_as_float(v[jj + 2]), alpha), __fmul_rn(__uint_as_float(v[jj + 3]), alpha));
-              wg.z = pack_bf16(__fmul_rn(__uint_as_float(v[jj + 4]), alpha), __fmul_rn(__uint_as_float(v[jj + 5]), alpha));
-              wg.w = pack_bf16(__fmul_rn(__uint_as_float(v[jj + 6]), alpha), __fmul_rn(__uint_as_float(v[jj + 7]), alpha));
-              wu.x = pack_bf16(__fmul_rn(__uint_as_float(u[jj]), alpha), __fmul_rn(__uint_as_float(u[jj + 1]), alpha));
-              wu.y = pack_bf16(__fmul_rn(__uint_as_float(u[jj + 2]), alpha), __fmul_rn(__uint_as_float(u[jj + 3]), alpha));
-              wu.z = pack_bf16(__fmul_rn(__uint_as_float(u[jj + 4]), alpha), __fmul_rn(__uint_as_float(u[jj + 5]), alpha));
-              wu.w = pack_bf16(__fmul_rn(__uint_as_float(u[jj + 6]), alpha), __fmul_rn(__uint_as_float(u[jj + 7]), alpha));
+              wg.x = pack_bf16(__fmul_rn(__uint_as_float(gv[jj]), alpha), __fmul_rn(__uint_as_float(gv[jj + 1]), alpha));
+              wg.y = pack_bf16(__fmul_rn(__uint_as_float(gv[jj + 2]), alpha), __fmul_rn(__uint_as_float(gv[jj + 3]), alpha));
+              wg.z = pack_bf16(__fmul_rn(__uint_as_float(gv[jj + 4]), alpha), __fmul_rn(__uint_as_float(gv[jj + 5]), alpha));
+              wg.w = pack_bf16(__fmul_rn(__uint_as_float(gv[jj + 6]), alpha), __fmul_rn(__uint_as_float(gv[jj + 7]), alpha));
+              wu.x = pack_bf16(__fmul_rn(__uint_as_float(uv[jj]), alpha), __fmul_rn(__uint_as_float(uv[jj + 1]), alpha));
+              wu.y = pack_bf16(__fmul_rn(__uint_as_float(uv[jj + 2]), alpha), __fmul_rn(__uint_as_float(uv[jj + 3]), alpha));
+              wu.z = pack_bf16(__fmul_rn(__uint_as_float(uv[jj + 4]), alpha), __fmul_rn(__uint_as_float(uv[jj + 5]), alpha));
+              wu.w = pack_bf16(__fmul_rn(__uint_as_float(uv[jj + 6]), alpha), __fmul_rn(__uint_as_float(uv[jj + 7]), alpha));
               *reinterpret_cast<uint4*>(og + jj) = wg;
               *reinterpret_cast<uint4*>(ou + jj) = wu;
             }
           }
 #pragma unroll
           for (int jj = 0; jj < 32; jj += 2) {
-            const float g0 = __fmul_rn(__uint_as_float(v[jj]), alpha);
-            const float u0 = __fmul_rn(__uint_as_float(u[jj]), alpha);
-            const float g1 = __fmul_rn(__uint_as_float(v[jj + 1]), alpha);
-            const float u1 = __fmul_rn(__uint_as_float(u[jj + 1]), alpha);
+            const float g0 = __fmul_rn(__uint_as_float(gv[jj]), alpha);
+            const float u0 = __fmul_rn(__uint_as_float(uv[jj]), alpha);
+            const float g1 = __fmul_rn(__uint_as_float(gv[jj + 1]), alpha);
+            const float u1 = __fmul_rn(__uint_as_float(uv[jj + 1]), alpha);
             const uint32_t pk = pack_bf16(__fmul_rn(__fmul_rn(silu_f(g0), u0), prob),
                                           __fmul_rn(__fmul_rn(silu_f(g1), u1), prob));
-            dw[c * 16 + jj / 2] = pk;
+            dw[cc * 16 + jj / 2] = pk;
             amax = fmaxf(amax, fmaxf(fabsf(bf16lo(pk)), fabsf(bf16hi(pk))));
           }
         }
-        // accumulator drained: hand it to the next tile, then store
-        tc_fence_before();
-        named_sync(1, 128);
-        if (threadIdx.x == 64) mbar_arrive_cluster(acce_leader);
-        if (row_ok) {
-          __nv_bfloat16* od = static_cast<__nv_bfloat16*>(p.out2) + grow * p.ldo2 + k.n0;
+        // D tile (128 rows x 128 columns) -> staging box `half`, then TMA store
+        if (leader_thread) bulk_wait_group_read0();     // previous tile's boxes read
+        named_sync(2, EPI_THREADS);
+        {
+          const uint32_t box = sOut + half * OUT_BOX_BYTES + r * 128;
 #pragma unroll
-          for (int jj = 0; jj < 64; jj += 4)
-            *reinterpret_cast<uint4*>(od + 2 * jj) = make_uint4(dw[jj], dw[jj + 1], dw[jj + 2], dw[jj + 3]);
-          if (p.amax && amax > 0.0f)
-            atomicMax(reinterpret_cast<unsigned*>(p.amax) + grow, __float_as_uint(amax));
+          for (int c16 = 0; c16 < 8; ++c16)
+            st_shared_v4(box + ((c16 ^ (r & 7)) << 4), dw[4 * c16], dw[4 * c16 + 1],
+                         dw[4 * c16 + 2], dw[4 * c16 + 3]);
         }
-      } else if (EPI == MPM_EPI_BF16) {
-        uint32_t ow[128];
+        fence_proxy_async();
+        named_sync(2, EPI_THREADS);
+        if (leader_thread) {
+          const int y = (int)(k.row_pair + rank * BM);
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          tmem_ld_32x32b_x32(trow + c * 32, v);
-          tmem_ld_wait();
+          for (int b = 0; b < 2; ++b)
+            tma_store_2d(&maps.out, (int)k.n0 + b * OUT_BOX_COLS, y, sOut + b * OUT_BOX_BYTES);
+          bulk_commit_group();
+        }
+        if (row_ok && p.amax && amax > 0.0f)
+          atomicMax(reinterpret_cast<unsigned*>(p.amax) + grow, __float_as_uint(amax));
+      } else if (EPI == MPM_EPI_BF16) {
+        // this thread: columns [128*half, 128*half + 128)
+        uint32_t ow[64];
+        uint32_t v2[32], v3[32], v4[32];
+        tmem_ld_32x32b_x32(trow + (half * 4 + 0) * 32, v);
+        tmem_ld_32x32b_x32(trow + (half * 4 + 1) * 32, v2);
+        tmem_ld_32x32b_x32(trow + (half * 4 + 2) * 32, v3);
+        tmem_ld_32x32b_x32(trow + (half * 4 + 3) * 32, v4);
+        tmem_ld_wait();
+        tc_fence_before();
+        named_sync(1, EPI_THREADS);
+        if (leader_thread) mbar_arrive_cluster(acce_leader);
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) {
+          const uint32_t* vv = cc == 0 ? v : (cc == 1 ? v2 : (cc == 2 ? v3 : v4));
 #pragma unroll
           for (int jj = 0; jj < 32; jj += 2)
-            ow[c * 16 + jj / 2] = pack_bf16(__fmul_rn(__uint_as_float(v[jj]), alpha),
-                                            __fmul_rn(__uint_as_float(v[jj + 1]), alpha));
+            ow[cc * 16 + jj / 2] = pack_bf16(__fmul_rn(__uint_as_float(vv[jj]), alpha),
+                                             __fmul_rn(__uint_as_float(vv[jj + 1]), alpha));
         }
-        tc_fence_before();
-        named_sync(1, 128);
-        if (threadIdx.x == 64) mbar_arrive_cluster(acce_leader);
-        if (row_ok) {
-          __nv_bfloat16* o = static_cast<__nv_bfloat16*>(p.out) + grow * p.ldo + k.n0;
+        // this thread's 128 columns -> staging boxes 2*half, 2*half+1, then TMA store
+        if (leader_thread) bulk_wait_group_read0();
+        named_sync(2, EPI_THREADS);
 #pragma unroll
-          for (int jj = 0; jj < 128; jj += 4)
-            *reinterpret_cast<uint4*>(o + 2 * jj) = make_uint4(ow[jj], ow[jj + 1], ow[jj + 2], ow[jj + 3]);
+        for (int bb = 0; bb < 2; ++bb) {
+          const uint32_t box = sOut + (2 * half + bb) * OUT_BOX_BYTES + r * 128;
+#pragma unroll
+          for (int c16 = 0; c16 < 8; ++c16) {
+            const int w = bb * 32 + 4 * c16;
+            st_shared_v4(box + ((c16 ^ (r & 7)) << 4), ow[w], ow[w + 1], ow[w + 2], ow[w + 3]);
+          }
+        }
+        fence_proxy_async();
+        named_sync(2, EPI_THREADS);
+        if (leader_thread) {
+          const int y = (int)(k.row_pair + rank * BM);
+#pragma unroll
+          for (int b = 0; b < 4; ++b)
+            tma_store_2d(&maps.out, (int)k.n0 + b * OUT_BOX_COLS, y, sOut + b * OUT_BOX_BYTES);
+          bulk_commit_group();
         }
       } else if (EPI == MPM_EPI_F32) {
 #pragma unroll 1
-        for (int c = 0; c < 8; ++c) {
+        for (int cc = 0; cc < 4; ++cc) {
+          const int c = half * 4 + cc;
           tmem_ld_32x32b_x32(trow + c * 32, v);
           tmem_ld_wait();
           if (row_ok) {
@@ -358,8 +442,8 @@ grouped_gemm_pair_kernel(const __grid_constant__ PairMaps maps, const GemmArgs p
           }
         }
         tc_fence_before();
-        named_sync(1, 128);
-        if (threadIdx.x == 64) mbar_arrive_cluster(acce_leader);
+        named_sync(1, EPI_THREADS);
+        if (leader_thread) mbar_arrive_cluster(acce_leader);
       } else {   // MPM_EPI_DSWIGLU
         const float prob = row_ok ? p.row_prob[grow] : 0.0f;
         const long long Nh = p.N;
@@ -368,7 +452,8 @@ grouped_gemm_pair_kernel(const __grid_constant__ PairMaps maps, const GemmArgs p
         __nv_bfloat16* og = static_cast<__nv_bfloat16*>(p.out) + grow * p.ldo;
         __nv_bfloat16* ou = og + Nh;
 #pragma unroll 1
-        for (int c = 0; c < 8; ++c) {
+        for (int cc = 0; cc < 4; ++cc) {
+          const int c = half * 4 + cc;
           tmem_ld_32x32b_x32(trow + c * 32, v);
           tmem_ld_wait();
           if (!row_ok) continue;
@@ -388,7 +473,7 @@ grouped_gemm_pair_kernel(const __grid_constant__ PairMaps maps, const GemmArgs p
                 const float g = h ? bf16hi(ga[qq]) : bf16lo(ga[qq]);
                 const float uu = h ? bf16hi(ua[qq]) : bf16lo(ua[qq]);
                 const float dd = __fmul_rn(__uint_as_float(v[jj + 2 * qq + h]), alpha);
-                const float sg = 1.0f / (1.0f + expf(-g));
+                const float sg = __fdividef(1.0f, 1.0f + __expf(-g));
                 const float dp = dd * prob;
                 dg2[h] = dp * uu * (sg * (1.0f + g * (1.0f - sg)));
                 du2[h] = dp * (g * sg);
@@ -401,11 +486,12 @@ grouped_gemm_pair_kernel(const __grid_constant__ PairMaps maps, const GemmArgs p
           }
         }
         tc_fence_before();
-        named_sync(1, 128);
-        if (threadIdx.x == 64) mbar_arrive_cluster(acce_leader);
+        named_sync(1, EPI_THREADS);
+        if (leader_thread) mbar_arrive_cluster(acce_leader);
       }
     }
   }
+  if (threadIdx.x == EPI_WARP0 * 32) bulk_wait_group0();    // output stores complete
   if (bad && threadIdx.x == 0) set_status(p.status, MPM_ERR_DEVICE_BOUNDS);
   __syncwarp();
   tc_fence_before();
@@ -476,13 +562,15 @@ static cudaError_t pair_dispatch(int epi, const pairk::PairMaps& maps, const Gem
 
 cudaError_t launch_grouped_gemm_pair(int kind, int epi, const CUtensorMap& ta,
                                      const CUtensorMap& tb, const CUtensorMap& tsfa,
-                                     const CUtensorMap& tsfb, const GemmArgs& a, int n_tiles,
-                                     long long n_tasks, cudaStream_t s) {
+                                     const CUtensorMap& tsfb, const CUtensorMap& tout,
+                                     const GemmArgs& a, int n_tiles, long long n_tasks,
+                                     cudaStream_t s) {
   pairk::PairMaps maps;
   maps.a = ta;
   maps.b = tb;
   maps.sfa = tsfa;
   maps.sfb = tsfb;
+  maps.out = tout;
   if (kind == MPM_KIND_NVFP4) return pair_dispatch<MPM_KIND_NVFP4>(epi, maps, a, n_tiles, n_tasks, s);
   return pair_dispatch<MPM_KIND_MXFP8>(epi, maps, a, n_tiles, n_tasks, s);
 }
