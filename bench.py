@@ -306,8 +306,9 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-also", action="store_true", help="skip the secondary lines")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle sample")
-    ap.add_argument("--case", choices=["headline", "slice"], default="headline",
-                    help="slice: 4096 tokens over 64 experts of the 671B shape (profiling)")
+    ap.add_argument("--case", choices=["headline", "slice", "mxfp8"], default="headline",
+                    help="slice: 4096 tokens over 64 experts of the 671B shape (profiling); "
+                         "mxfp8: the MXFP8 30B-shaped forward+backward step alone (profiling)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -356,6 +357,15 @@ def main():
     dev = torch.cuda.current_device()
     from microscaled_precision_moe_gb300 import build
     build.build()
+    if args.case == "mxfp8":
+        r = _mxfp8_layer_line(peak_fp8_sus, steps=args.steps)
+        if rank == 0:
+            print(json.dumps({"metric": METRIC, "value": r["TFLOP/s"], "unit": "TFLOP/s",
+                              "n_gpus": world, "steps": args.steps, "warmup": 3,
+                              "ms_per_step": r["ms_per_step"], "higher_is_better": True,
+                              "dtype": "mxfp8", "config": {"workload": r["workload"]},
+                              "note": r["note"]}), flush=True)
+        return 0
     from microscaled_precision_moe_gb300 import ops
     from microscaled_precision_moe_gb300.moe import NVFP4MoE, NVFP4Weights
 

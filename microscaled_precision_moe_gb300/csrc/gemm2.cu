@@ -9,7 +9,7 @@
 //     256 B rows) plus the scale tiles of its A rows and of all 256 B rows;
 //     every TMA load, the peer's included, completes on the leader CTA's
 //     barrier (cp.async.bulk.tensor .cta_group::2);
-//   * a copy warp of the leader copies the scale tiles of both CTAs into their
+//   * copy warps of the leader copy the scale tiles of both CTAs into their
 //     tensor memories (tcgen05.cp.cta_group::2) and signals a per-stage
 //     barrier; the leader's MMA thread waits on it and issues
 //     tcgen05.mma.cta_group::2 (M = 256, N = 256).  Issuing the copies from
@@ -36,9 +36,11 @@ namespace pairk {
 constexpr int BM = 128;              // rows per CTA; 256 per pair
 constexpr int BN = 256;
 constexpr int BKB = 128;             // bytes of K per stage
-// warp 0 TMA, warp 1 MMA + TMEM allocation, warp 2 scale-tile copies,
-// warps 3-10 epilogue (two warps per TMEM lane quarter, each half the columns)
-constexpr int NTHREADS = 352;
+// warp 0 TMA, warp 1 MMA + TMEM allocation, warps 2 and 11 scale-tile copies
+// (six tcgen05.cp each per NVFP4 stage), warps 3-10 epilogue (two warps per
+// TMEM lane quarter, each half the columns)
+constexpr int NTHREADS = 384;
+constexpr int SF_WARP2 = 11;         // second scale-copy warp
 constexpr int EPI_WARP0 = 3;
 constexpr int EPI_THREADS = 256;
 constexpr int A_STAGE = BM * BKB;    // 16 KB
@@ -173,7 +175,7 @@ grouped_gemm_pair_kernel(const __grid_constant__ PairMaps maps, const GemmArgs p
     }
     mbar_init(bar_accf, 1);
     mbar_init(bar_acce, 2);          // one arrive from each CTA's epilogue
-    for (int s = 0; s < S; ++s) mbar_init(bar_sf + 8 * s, 1);
+    for (int s = 0; s < S; ++s) mbar_init(bar_sf + 8 * s, 2);   // both copy warps
     *fail_flag = 0;
     fence_mbar_init();
     fence_proxy_async();
@@ -258,8 +260,12 @@ grouped_gemm_pair_kernel(const __grid_constant__ PairMaps maps, const GemmArgs p
         if (kb + 1 == k.num_kb) tc_commit_pair(bar_accf, (uint16_t)3);
       }
     }
-  } else if (warp == 2 && lane == 0 && rank == 0) {
+  } else if ((warp == 2 || warp == SF_WARP2) && lane == 0 && rank == 0) {
     // ======================================================== scale-tile copies (leader only)
+    // Two threads in two warps each copy half of a stage's scale tiles (one
+    // thread's tcgen05.cp instructions issue one after another) and each
+    // commit to the stage's barrier (count 2).
+    const int part = (warp == 2) ? 0 : 1;
     uint32_t it = 0;
     bool ok = true;
     for (long long t = cid; ok && t < n_tasks; t += ncl) {
@@ -271,25 +277,33 @@ grouped_gemm_pair_kernel(const __grid_constant__ PairMaps maps, const GemmArgs p
         tc_fence_after();
         const uint32_t sf_col = tmem + SF_TMEM_BASE + s * C::kSfTmemPerStage;
         if (KIND == MPM_KIND_NVFP4) {
+          // 12 atoms: SFA ks 0..3, SFB (h, ks); part 0 takes SFA + SFB(h=0, ks<2), part 1 the rest
 #pragma unroll
-          for (int ks = 0; ks < 4; ++ks) {
-            tc_cp_32x128b_x4_pair(sf_col + ks * 4, sdesc_sf(sSFA + s * C::kSfaBytes + ks * 512));
-#pragma unroll
-            for (int h = 0; h < 2; ++h)
+          for (int i = 0; i < 6; ++i) {
+            const int a = part * 6 + i;          // 0..11
+            if (a < 4) {
+              tc_cp_32x128b_x4_pair(sf_col + a * 4, sdesc_sf(sSFA + s * C::kSfaBytes + a * 512));
+            } else {
+              const int bidx = a - 4;            // 0..7 -> (h, ks)
+              const int h = bidx >> 2, ks = bidx & 3;
               tc_cp_32x128b_x4_pair(sf_col + 16 + ks * 8 + h * 4,
                                     sdesc_sf(sSFB + s * C::kSfbBytes + h * 2048 + ks * 512));
+            }
           }
         } else {
-          tc_cp_32x128b_x4_pair(sf_col, sdesc_sf(sSFA + s * C::kSfaBytes));
+          if (part == 0) {
+            tc_cp_32x128b_x4_pair(sf_col, sdesc_sf(sSFA + s * C::kSfaBytes));
+          } else {
 #pragma unroll
-          for (int h = 0; h < 2; ++h)
-            tc_cp_32x128b_x4_pair(sf_col + 4 + h * 4, sdesc_sf(sSFB + s * C::kSfbBytes + h * 512));
+            for (int h = 0; h < 2; ++h)
+              tc_cp_32x128b_x4_pair(sf_col + 4 + h * 4, sdesc_sf(sSFB + s * C::kSfbBytes + h * 512));
+          }
         }
         asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];"
                      :: "r"(bar_sf + 8 * s) : "memory");
       }
     }
-  } else if (warp >= EPI_WARP0) {
+  } else if (warp >= EPI_WARP0 && warp < EPI_WARP0 + 8) {
     // ======================================================== epilogue (both CTAs)
     const int q = warp & 3;                     // TMEM lane quarter of this warp
     const int half = (warp - EPI_WARP0) >> 2;   // which half of the columns

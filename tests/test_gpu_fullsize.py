@@ -1,0 +1,198 @@
+"""Parity at the full workload sizes, in the launch configuration bench.py times
+(CTA-pair GEMMs, 256-row segments).
+
+The layers run whole on the GPU; the oracle recomputes sampled outputs one
+expert at a time (it needs only the weights of the experts it checks):
+
+* per-token codes / scales / token scales of sampled rows: byte-exact;
+* segment offsets, permutation, inverse permutation: bit-exact (whole);
+* FC1 output D on every routed row of the checked experts: GEMM tolerance;
+* FC2 output Y on those rows whose D is bit-identical to the oracle's (so the
+  re-quantised operands are identical): GEMM tolerance; other rows within
+  the NVFP4 re-quantisation noise;
+* combine: the output equals the fp32 slot-order sum of the kernel's own Y
+  rows (a property that holds at any size);
+* MXFP8 forward and backward: C, D, Y, dH rows and the full dW1 / dW2 of the
+  checked experts: GEMM tolerance.
+"""
+import numpy as np
+import pytest
+import torch
+
+from oracle import formats as F
+from oracle import quant as Q
+from oracle import moe as MO
+from oracle import metrics as Mx
+from microscaled_precision_moe_gb300 import synth
+from tests.gpu_util import need_gpu, np_bf16, u8, assert_bytes_equal
+
+pytestmark = pytest.mark.gpu
+
+REL, ELEM = 1e-3, 1e-2
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    need_gpu()
+
+
+def _close(got, ref, what, rel=REL, elem=ELEM):
+    ok, rf, mx, bound = Mx.within_gemm_tolerance(got, ref, rel, elem)
+    assert ok, f"{what}: rel_frob={rf:.3e} max_err={mx:.3e} bound={bound:.3e}"
+
+
+def _pick_experts(seg, n):
+    """The heaviest, the lightest non-empty and a middle expert (n total)."""
+    sizes = np.diff(seg)
+    nz = np.flatnonzero(sizes > 0)
+    order = nz[np.argsort(sizes[nz], kind="stable")]
+    picks = [int(order[-1]), int(order[0])]
+    mid = order[len(order) // 2:]
+    for e in mid:
+        if len(picks) >= n:
+            break
+        if int(e) not in picks:
+            picks.append(int(e))
+    return picks
+
+
+def _slot_sum(y_perm, inv, T, k):
+    """bf16( sum_j y_perm[inv[t*k + j]] ) with fp32 adds in slot order."""
+    idx = torch.from_numpy(np.asarray(inv, dtype=np.int64).reshape(T, k)).cuda()
+    acc = torch.zeros(T, y_perm.shape[1], dtype=torch.float32, device="cuda")
+    for j in range(k):
+        acc += y_perm[idx[:, j]].float()
+    return acc.to(torch.bfloat16)
+
+
+def _nvfp4_expert_reference(xn_rows, w1e, w2e, prob, I):
+    """Oracle NVFP4 path for the rows of one expert: per-token X quantisation,
+    joint gate/up and W2 quantisation, fp64 FC1, SwiGLU x prob -> bf16 D, row
+    amax, re-quantisation, fp64 FC2 -> bf16 Y."""
+    qx, sx, tsx = Q.nvfp4_quantize_per_token(xn_rows)
+    a = Q.nvfp4_dequantize(qx, sx, tsx)
+    b1 = MO.dequant_weights_nvfp4(Q.nvfp4_quantize_joint([w1e[None, :I], w1e[None, I:]], 1))[0]
+    b2 = MO.dequant_weights_nvfp4(Q.nvfp4_quantize_joint([w2e[None]], 1))[0]
+    with np.errstate(over="ignore"):
+        d = MO.fc1_epilogue(a @ b1.T, prob, I)
+    amax = np.max(np.abs(d), axis=1).astype(np.float32)
+    qd, sd, tsd = Q.nvfp4_quantize_per_token(d, amax)
+    y = F.bf16_round(Q.nvfp4_dequantize(qd, sd, tsd) @ b2.T)
+    return d, y
+
+
+def _run_nvfp4_full(shape, n_experts, x_rows_checked):
+    from microscaled_precision_moe_gb300.moe import NVFP4MoE, NVFP4Weights
+    ids, prob = synth.routing(shape)
+    x = synth.moe_activations(shape, device="cuda")
+    w1, w2 = synth.moe_weights(shape, device="cuda")
+    W = NVFP4Weights.quantize(w1, w2)
+    layer = NVFP4MoE(shape.T, shape.H, shape.I, shape.E, shape.k)    # bench launch configuration
+    out = layer.forward(x, ids.cuda(), prob.cuda(), W)
+    torch.cuda.synchronize()
+    from microscaled_precision_moe_gb300 import ops
+    assert ops.get_device_status() == 0
+    T, H, I, E, k = shape.T, shape.H, shape.I, shape.E, shape.k
+    # segments, whole
+    seg_g, perm_g, inv_g, rp_g = [t.cpu().numpy() for t in layer.seg]
+    seg, perm, inv, rp = MO.build_segments(ids.numpy(), prob.numpy(), E, layer.tile_m)
+    assert_bytes_equal(seg_g, seg, "seg_offsets")
+    R = int(seg[-1])
+    assert_bytes_equal(perm_g[:R], perm, "perm")
+    assert_bytes_equal(inv_g, inv, "inv_perm")
+    # per-token quantisation of sampled rows
+    rows = np.random.default_rng(1).choice(T, x_rows_checked, replace=False)
+    xr = np_bf16(x[torch.from_numpy(rows).cuda()])
+    rq, rs, rts = Q.nvfp4_quantize_per_token(xr)
+    qx, sx, tsx = layer.xq
+    assert_bytes_equal(u8(qx)[rows], rq, "X codes (sampled rows)")
+    assert_bytes_equal(Q.unswizzle_scales(u8(sx), T, H // 16)[rows], rs, "X scales (sampled rows)")
+    assert_bytes_equal(tsx.cpu().numpy()[rows].view(np.uint32), rts.view(np.uint32), "X token scales")
+    # combine property on the whole output: fp32 slot-order sum of the
+    # kernel's own Y rows, one rounding (IEEE fp32 adds on the device)
+    assert torch.equal(out, _slot_sum(layer.y, inv_g, T, k)), "combine"
+    # FC1 / FC2 on every routed row of the checked experts
+    d_g = layer.d
+    y_gpu = layer.y
+    for e in _pick_experts(seg, n_experts):
+        r0, r1 = int(seg[e]), int(seg[e + 1])
+        real = perm[r0:r1] >= 0
+        rws = np.arange(r0, r1)[real]
+        toks = perm[rws] // k
+        xe = np_bf16(x[torch.from_numpy(toks).cuda()])
+        w1e = np_bf16(w1[e])
+        w2e = np_bf16(w2[e])
+        d_ref, y_ref = _nvfp4_expert_reference(xe, w1e, w2e, rp[rws], I)
+        d_got = np_bf16(d_g[torch.from_numpy(rws).cuda()])
+        y_got = np_bf16(y_gpu[torch.from_numpy(rws).cuda()])
+        _close(d_got, d_ref, f"expert {e} ({len(rws)} rows): FC1 D")
+        same = (d_got == d_ref).all(axis=1)
+        assert same.mean() > 0.9, f"expert {e}: {same.mean():.3f} of D rows bit-identical"
+        _close(y_got[same], y_ref[same], f"expert {e}: FC2 Y on identical operands")
+        if (~same).any():
+            rel = np.linalg.norm(y_got[~same] - y_ref[~same]) / np.linalg.norm(y_ref[~same])
+            assert rel < 0.1, f"expert {e}: re-quantised rows differ by {rel:.3e}"
+
+
+def test_nvfp4_layer_30b_full_size():
+    """16384 tokens, hidden 2048, 128 experts, intermediate 768, top-8."""
+    _run_nvfp4_full(synth.MOE_30B, n_experts=4, x_rows_checked=512)
+
+
+def test_nvfp4_layer_671b_full_size():
+    """The headline workload: 32768 tokens, hidden 7168, 256 experts,
+    intermediate 2048, top-8 with Zipf(1.1) expert load."""
+    _run_nvfp4_full(synth.MOE_671B, n_experts=3, x_rows_checked=256)
+
+
+def test_mxfp8_layer_30b_fwd_bwd_full_size():
+    """8192 tokens, hidden 2048, 128 experts, intermediate 768, top-8:
+    forward and backward, checked on every row and the full weight gradients
+    of three experts."""
+    from microscaled_precision_moe_gb300.moe import MXFP8MoE
+    shape = synth.MOE_30B_BWD
+    T, H, I, E, k = shape.T, shape.H, shape.I, shape.E, shape.k
+    ids, prob = synth.routing(shape)
+    x = synth.moe_activations(shape, device="cuda")
+    w1, w2 = synth.moe_weights(shape, device="cuda")
+    dy = synth.moe_grad_out(shape, device="cuda")
+    L = MXFP8MoE(T, H, I, E, k)
+    L.quantize_weights(w1, w2)
+    L.forward(x, ids.cuda(), prob.cuda())
+    dx, dw1, dw2 = L.backward(dy)
+    torch.cuda.synchronize()
+    from microscaled_precision_moe_gb300 import ops
+    assert ops.get_device_status() == 0
+    seg, perm, inv, rp = MO.build_segments(ids.numpy(), prob.numpy(), E, L.tile_m)
+    assert_bytes_equal(L.seg[0].cpu().numpy(), seg, "seg_offsets")
+    for e in _pick_experts(seg, 3):
+        r0, r1 = int(seg[e]), int(seg[e + 1])
+        rws = np.arange(r0, r1)
+        real = perm[r0:r1] >= 0
+        toks = np.where(real, perm[r0:r1] // k, 0)
+        # the expert's slice of the permuted operands (padding rows zero)
+        xe = np_bf16(x[torch.from_numpy(toks).cuda()]) * real[:, None]
+        dye = np_bf16(dy[torch.from_numpy(toks).cuda()]) * real[:, None]
+        w1e, w2e = np_bf16(w1[e]), np_bf16(w2[e])
+        p = rp[r0:r1]
+        segl = np.array([0, r1 - r0])
+        with np.errstate(over="ignore"):
+            acc1 = MO.grouped_gemm(MO.mx_rows(xe), MO.mx_rows(w1e)[None], segl)
+            c1 = F.bf16_round(acc1)
+            d = MO.fc1_epilogue(acc1, p, I)
+            y = F.bf16_round(MO.grouped_gemm(MO.mx_rows(d), MO.mx_rows(w2e)[None], segl))
+            dd = MO.grouped_gemm(MO.mx_rows(dye), MO.mx_cols_t(w2e)[None], segl)
+            dh = F.bf16_round(MO.swiglu_backward(dd, c1, p, I))
+            dxp = F.bf16_round(MO.grouped_gemm(MO.mx_rows(dh), MO.mx_cols_t(w1e)[None], segl))
+            dw2e = MO.grouped_wgrad(MO.mx_cols_t(dye), MO.mx_cols_t(d), segl)[0]
+            dw1e = MO.grouped_wgrad(MO.mx_cols_t(dh), MO.mx_cols_t(xe), segl)[0]
+        sel = torch.from_numpy(rws).cuda()
+        _close(np_bf16(L.c1[sel]), c1, f"expert {e}: C = gate|up")
+        _close(np_bf16(L.d[sel]), d, f"expert {e}: D")
+        _close(np_bf16(L.y[sel]), y, f"expert {e}: Y")
+        _close(np_bf16(L.dh[sel]), dh, f"expert {e}: dH")
+        _close(np_bf16(L.dxp[sel]), dxp, f"expert {e}: dX_perm")
+        _close(dw1[e].cpu().numpy(), dw1e, f"expert {e}: dW1")
+        _close(dw2[e].cpu().numpy(), dw2e, f"expert {e}: dW2")
+    # dX combine property, whole
+    assert torch.equal(dx, _slot_sum(L.dxp, L.seg[2].cpu().numpy(), T, k)), "dX combine"
