@@ -185,6 +185,24 @@ def _oracle_run(shape, items):
     return flops, secs, desc
 
 
+def _gemm_traffic():
+    """FC1 DRAM bytes per launch from the committed ncu summary, if the GEMM
+    sources are still the version those counters were taken on (else None)."""
+    import hashlib
+    prof = os.path.join(ROOT, "profiles", "nvfp4_fc1_fc2_T32768_H7168_I2048_E256_dram_traffic.md")
+    csrc = os.path.join(ROOT, "microscaled_precision_moe_gb300", "csrc")
+    try:
+        kv = dict(l.split(": ", 1) for l in open(prof).read().split("\n") if ": " in l
+                  and l.split(": ", 1)[0] in ("fc1_traffic_bytes_per_launch", "gemm_source_sha256"))
+        src = b"".join(open(os.path.join(csrc, f), "rb").read()
+                       for f in ("gemm2.cu", "gemm.cuh", "common.cuh"))
+        if hashlib.sha256(src).hexdigest() == kv["gemm_source_sha256"].strip():
+            return int(kv["fc1_traffic_bytes_per_launch"])
+    except (OSError, KeyError, ValueError):
+        pass
+    return None
+
+
 def _cores():
     try:
         return len(os.sched_getaffinity(0))
@@ -434,9 +452,11 @@ def main():
     # ---- roofline of the dominant kernel (FC1 grouped GEMM, tensor bound)
     fc1_ms = stage_ms["fc1"]
     ach = fl1 / (fc1_ms * 1e-3) / 1e12
-    roof = {"bound": "tensor", "kernel": "grouped_gemm_kernel<NVFP4, SWIGLU> (FC1)",
+    traffic = _gemm_traffic() if args.case == "headline" else None
+    roof = {"bound": "tensor", "kernel": "grouped_gemm_pair_kernel<NVFP4, SWIGLU> (FC1)",
             "achieved": round(ach, 1), "peak": round(peak_fp4_sus, 1), "unit": "TFLOP/s",
-            "frac": round(ach / peak_fp4_sus, 4), "traffic": None,
+            "frac": round(ach / peak_fp4_sus, 4), "traffic": traffic,
+            "traffic_unit": "bytes per launch (DRAM read + write, ncu)",
             "peak_source": f"{peaks['src']} sustained bf16 x {NOMINAL_FP4_OVER_BF16:g} "
                            f"(dense FP4/BF16 nominal ratio)",
             "per_launch_flops": fl1}
