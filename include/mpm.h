@@ -306,10 +306,11 @@ mpm_status mpm_moe_combine(const void* y_perm_dev, const int32_t* inv_perm_dev,
  */
 typedef struct {
   int kind;                    /* MPM_KIND_*                                   */
-  int tile_m;                  /* GROUP_M: 128 (one CTA per 128x256 tile) or 256
-                                  (a CTA pair per 256x256 tile, persistent; the
+  int tile_m;                  /* 128: one CTA per 128x256 tile; 256: a CTA pair
+                                  per 256x256 tile, persistent (GROUP_M: the
                                   expert segments must be multiples of 256
-                                  rows, checked on the device); GROUP_K: 128 */
+                                  rows, checked on the device; GROUP_K: the
+                                  output rows a_rows % 256 == 0)            */
   int group;                   /* MPM_GROUP_*                                  */
   int epilogue;                /* MPM_EPI_*                                    */
   int64_t E;                   /* experts (groups)                             */

@@ -85,18 +85,22 @@ bool make_sf_tmap(CUtensorMap* m, const void* base, long long atoms, int atoms_p
   return r == CUDA_SUCCESS;
 }
 
-// bf16 [rows, cols] output with row pitch `ld` elements: 128-row x 64-column
-// boxes, 128-byte swizzle (the staging layout of the TMA-store epilogues)
-bool make_out_tmap(CUtensorMap* m, const void* base, long long cols, long long rows, long long ld) {
+// [rows, cols] bf16 or fp32 output with row pitch `ld` elements: 128-row boxes
+// of 128 bytes per row (64 bf16 or 32 fp32 columns), 128-byte swizzle (the
+// staging layout of the TMA-store epilogues)
+bool make_out_tmap(CUtensorMap* m, const void* base, long long cols, long long rows, long long ld,
+                   bool f32 = false) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
+  const int esz = f32 ? 4 : 2;
   cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
-  cuuint64_t strides[1] = {(cuuint64_t)(ld * 2)};
-  cuuint32_t box[2] = {64, 128};
+  cuuint64_t strides[1] = {(cuuint64_t)(ld * esz)};
+  cuuint32_t box[2] = {(cuuint32_t)(128 / esz), 128};
   cuuint32_t estr[2] = {1, 1};
-  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
-                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  CUresult r = fn(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                  const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
 
@@ -240,7 +244,7 @@ mpm_status mpm_moe_grouped_gemm(const mpm_grouped_gemm_desc* d, cudaStream_t str
   if (d->group != MPM_GROUP_M && d->group != MPM_GROUP_K) return MPM_ERR_UNSUPPORTED;
   const int tile_m = d->tile_m == 0 ? 128 : d->tile_m;
   if (tile_m != 128 && tile_m != 256) return MPM_ERR_UNSUPPORTED;
-  if (tile_m == 256 && d->group != MPM_GROUP_M) return MPM_ERR_UNSUPPORTED;
+  if (tile_m == 256 && d->group == MPM_GROUP_K && d->a_rows % 256 != 0) return MPM_ERR_SHAPE;
   if (d->epilogue < MPM_EPI_F32 || d->epilogue > MPM_EPI_DSWIGLU) return MPM_ERR_UNSUPPORTED;
   if (!d->a_dev || !d->b_dev || !d->sfa_dev || !d->sfb_dev || !d->out_dev) return MPM_ERR_NULL;
   if (d->E < 1 || d->E > 65535 || d->N < 256 || d->N % 256 != 0 || d->a_rows < 1)
@@ -321,11 +325,15 @@ mpm_status mpm_moe_grouped_gemm(const mpm_grouped_gemm_desc* d, cudaStream_t str
     std::memset(&tout, 0, sizeof(tout));
     if (d->epilogue == MPM_EPI_BF16) {
       if (!make_out_tmap(&tout, d->out_dev, d->N, d->a_rows, d->ldo)) return MPM_ERR_CUDA;
+    } else if (d->epilogue == MPM_EPI_F32) {
+      const long long rows = d->group == MPM_GROUP_K ? d->E * d->a_rows : d->a_rows;
+      if (!make_out_tmap(&tout, d->out_dev, d->N, rows, d->ldo, true)) return MPM_ERR_CUDA;
     } else if (swiglu) {
       if (!make_out_tmap(&tout, d->out2_dev, d->N / 2, d->a_rows, d->ldo2)) return MPM_ERR_CUDA;
     }
     const int n_tiles = (int)(swiglu ? (d->N / 2) / 128 : d->N / 256);
-    const long long n_tasks = (long long)n_tiles * ((d->a_rows + 255) / 256);
+    long long n_tasks = (long long)n_tiles * ((d->a_rows + 255) / 256);
+    if (d->group == MPM_GROUP_K) n_tasks *= d->E;
     return cuda_status(mpm::launch_grouped_gemm_pair(d->kind, d->epilogue, ta, tb, tsa, tsb, tout,
                                                      a, n_tiles, n_tasks, stream));
   }

@@ -95,42 +95,72 @@ MPM_DEV uint32_t pack_bf16(float lo, float hi) {
 struct Task {
   bool valid;
   int e;
-  long long row_pair;   // first row of the 256-row pair tile
+  long long row_pair;   // first row (of A / of the expert's output) of the pair tile
+  long long out_row;    // first output row of this pair tile in the output matrix
   long long n0;         // first output column (D columns for SwiGLU)
   long long brow[2];    // global B rows of the two 128-row halves
+  long long ka0, kb0;   // reduction offsets (elements) of A and B
   int num_kb;
 };
 
+// GROUP_M: tasks = (256-row pair of A rows) x (N tile); the pair's expert is
+// found by binary search over the device offsets.  GROUP_K: tasks = expert x
+// (256-row pair of output rows) x (N tile); the reduction runs over the
+// expert's segment.
 template <int KIND, int EPI>
 MPM_DEV Task task_of(const GemmArgs& p, long long t, int n_tiles, int* bad) {
   Task k{};
-  const long long mp = t / n_tiles;
-  const int nt = (int)(t - mp * n_tiles);
-  k.row_pair = mp * 2 * BM;
-  long long seg_end = p.a_rows;
-  if (p.seg) seg_end = p.seg[p.E];
-  if (k.row_pair >= seg_end) { k.valid = false; return k; }
+  const bool swiglu = (EPI == MPM_EPI_SWIGLU || EPI == MPM_EPI_SWIGLU_SAVE);
   int e = 0;
-  if (p.seg) {
-    int lo = 0, hi = p.E - 1;
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (p.seg[mid] <= k.row_pair) lo = mid; else hi = mid - 1;
+  long long mp, nt;
+  if (p.group == MPM_GROUP_K) {
+    const long long n_mp = p.M_out / (2 * BM);
+    const long long per_e = n_mp * n_tiles;
+    e = (int)(t / per_e);
+    if (e >= p.E) { k.valid = false; return k; }
+    const long long rem = t - (long long)e * per_e;
+    mp = rem / n_tiles;
+    nt = rem - mp * n_tiles;
+    const long long s0 = p.seg[e], s1 = p.seg[e + 1];
+    if (s1 < s0 || ((s1 - s0) % Cfg<KIND>::kElemsPerKB) != 0) *bad = 1;
+    k.num_kb = s1 > s0 ? (int)((s1 - s0) / Cfg<KIND>::kElemsPerKB) : 0;
+    k.row_pair = mp * 2 * BM;
+    k.out_row = (long long)e * p.M_out + k.row_pair;
+    k.ka0 = s0;
+    k.kb0 = s0;
+    k.n0 = nt * BN;
+    k.brow[0] = k.n0;
+    k.brow[1] = k.n0 + 128;
+  } else {
+    mp = t / n_tiles;
+    nt = t - mp * n_tiles;
+    k.row_pair = mp * 2 * BM;
+    long long seg_end = p.a_rows;
+    if (p.seg) seg_end = p.seg[p.E];
+    if (k.row_pair >= seg_end) { k.valid = false; return k; }
+    if (p.seg) {
+      int lo = 0, hi = p.E - 1;
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (p.seg[mid] <= k.row_pair) lo = mid; else hi = mid - 1;
+      }
+      e = lo;
+      if ((p.seg[e] & 255) != 0 || (p.seg[e + 1] & 255) != 0) *bad = 1;   // not pair-aligned
     }
-    e = lo;
-    if ((p.seg[e] & 255) != 0 || (p.seg[e + 1] & 255) != 0) *bad = 1;   // not pair-aligned
+    k.out_row = k.row_pair;
+    k.n0 = nt * (swiglu ? BN / 2 : BN);
+    if (swiglu) {
+      k.brow[0] = (long long)e * p.b_rows_per_e + k.n0;
+      k.brow[1] = (long long)e * p.b_rows_per_e + p.N / 2 + k.n0;
+    } else {
+      k.brow[0] = (long long)e * p.b_rows_per_e + k.n0;
+      k.brow[1] = k.brow[0] + 128;
+    }
+    k.ka0 = 0;
+    k.kb0 = (long long)e * p.b_k_per_e;
+    k.num_kb = (int)(p.K / Cfg<KIND>::kElemsPerKB);
   }
   k.e = e;
-  const bool swiglu = (EPI == MPM_EPI_SWIGLU || EPI == MPM_EPI_SWIGLU_SAVE);
-  k.n0 = (long long)nt * (swiglu ? BN / 2 : BN);
-  if (swiglu) {
-    k.brow[0] = (long long)e * p.b_rows_per_e + k.n0;
-    k.brow[1] = (long long)e * p.b_rows_per_e + p.N / 2 + k.n0;
-  } else {
-    k.brow[0] = (long long)e * p.b_rows_per_e + k.n0;
-    k.brow[1] = k.brow[0] + 128;
-  }
-  k.num_kb = (int)(p.K / Cfg<KIND>::kElemsPerKB);
   k.valid = true;
   return k;
 }
@@ -183,8 +213,7 @@ grouped_gemm_pair_kernel(const __grid_constant__ PairMaps maps, const GemmArgs p
     prefetch_tmap(&maps.b);
     prefetch_tmap(&maps.sfa);
     prefetch_tmap(&maps.sfb);
-    if (EPI == MPM_EPI_BF16 || EPI == MPM_EPI_SWIGLU || EPI == MPM_EPI_SWIGLU_SAVE)
-      prefetch_tmap(&maps.out);
+    if (EPI != MPM_EPI_DSWIGLU) prefetch_tmap(&maps.out);
   }
   if (warp == 1) {
     tmem_alloc_pair(sTmem, TMEM_COLS);
@@ -212,8 +241,8 @@ grouped_gemm_pair_kernel(const __grid_constant__ PairMaps maps, const GemmArgs p
         if (!mbar_wait_cluster(bar_empty + 8 * s, ph ^ 1u, p.status)) { ok = false; break; }
         if (rank == 0) mbar_arrive_expect_tx(bar_full + 8 * s, 2 * stage_bytes<KIND>());
         const uint32_t fb = map_to_rank(bar_full + 8 * s, 0);   // the leader's barrier
-        const long long ka = (long long)kb * C::kElemsPerKB;
-        const long long kbb = (long long)k.e * p.b_k_per_e + ka;
+        const long long ka = k.ka0 + (long long)kb * C::kElemsPerKB;
+        const long long kbb = k.kb0 + (long long)kb * C::kElemsPerKB;
         const int xa = (int)(KIND == MPM_KIND_NVFP4 ? ka / 2 : ka);
         const int xb = (int)(KIND == MPM_KIND_NVFP4 ? kbb / 2 : kbb);
         tma_load_2d_pair(sA + s * A_STAGE, &maps.a, xa, (int)a_row, fb);
@@ -233,10 +262,12 @@ grouped_gemm_pair_kernel(const __grid_constant__ PairMaps maps, const GemmArgs p
     // ======================================================== MMA issuer (leader only)
     uint32_t it = 0, j = 0;
     bool ok = true;
-    for (long long t = cid; ok && t < n_tasks; t += ncl, ++j) {
+    for (long long t = cid; ok && t < n_tasks; t += ncl) {
       const Task k = task_of<KIND, EPI>(p, t, n_tiles, &bad);
       if (!k.valid) break;
+      if (k.num_kb == 0) continue;             // empty reduction: nothing to accumulate
       if (!mbar_wait_cluster(bar_acce, (j & 1u) ^ 1u, p.status)) break;
+      ++j;
       tc_fence_after();
       for (int kb = 0; kb < k.num_kb; ++kb, ++it) {
         const int s = it % S;
@@ -311,18 +342,28 @@ grouped_gemm_pair_kernel(const __grid_constant__ PairMaps maps, const GemmArgs p
     const uint32_t trow = tmem + ((uint32_t)(q * 32) << 16);
     const bool leader_thread = (threadIdx.x == EPI_WARP0 * 32);
     uint32_t j = 0;
-    for (long long t = cid; t < n_tasks; t += ncl, ++j) {
+    for (long long t = cid; t < n_tasks; t += ncl) {
       const Task k = task_of<KIND, EPI>(p, t, n_tiles, &bad);
       if (!k.valid) break;
+      const long long orow = k.out_row + rank * BM;          // this CTA's first output row
+      if (k.num_kb == 0) {
+        // empty reduction (an expert without rows in the wgrad mode): zeros
+        if (EPI == MPM_EPI_F32) {
+          float* o = static_cast<float*>(p.out) + (orow + r) * p.ldo + k.n0 + half * 128;
+          for (int c = 0; c < 128; c += 4) *reinterpret_cast<float4*>(o + c) = make_float4(0, 0, 0, 0);
+        }
+        continue;
+      }
       const bool w_ok = mbar_wait_cluster(bar_accf, j & 1u, p.status);
+      ++j;
       if (!w_ok) *fail_flag = 1;
       named_sync(1, EPI_THREADS);
       if (*fail_flag) break;
       tc_fence_after();
-      const long long grow = k.row_pair + rank * BM + r;
-      const bool row_ok = grow < p.a_rows;
+      const long long grow = k.row_pair + rank * BM + r;     // row of A (GROUP_M)
+      const bool row_ok = (p.group == MPM_GROUP_K) || grow < p.a_rows;
       float alpha = 1.0f;
-      if (row_ok) {
+      if (row_ok && p.group == MPM_GROUP_M) {
         if (p.alpha_a) alpha = p.alpha_a[grow];
         if (p.alpha_b) alpha = __fmul_rn(alpha, p.alpha_b[k.e]);
       }
@@ -391,7 +432,7 @@ grouped_gemm_pair_kernel(const __grid_constant__ PairMaps maps, const GemmArgs p
         fence_proxy_async();
         named_sync(2, EPI_THREADS);
         if (leader_thread) {
-          const int y = (int)(k.row_pair + rank * BM);
+          const int y = (int)orow;
 #pragma unroll
           for (int b = 0; b < 2; ++b)
             tma_store_2d(&maps.out, (int)k.n0 + b * OUT_BOX_COLS, y, sOut + b * OUT_BOX_BYTES);
@@ -434,25 +475,42 @@ grouped_gemm_pair_kernel(const __grid_constant__ PairMaps maps, const GemmArgs p
         fence_proxy_async();
         named_sync(2, EPI_THREADS);
         if (leader_thread) {
-          const int y = (int)(k.row_pair + rank * BM);
+          const int y = (int)orow;
 #pragma unroll
           for (int b = 0; b < 4; ++b)
             tma_store_2d(&maps.out, (int)k.n0 + b * OUT_BOX_COLS, y, sOut + b * OUT_BOX_BYTES);
           bulk_commit_group();
         }
       } else if (EPI == MPM_EPI_F32) {
+        // fp32 boxes of 32 columns (128 bytes) x 128 rows: the staging holds
+        // 128 columns, so the two column halves go out in two rounds
 #pragma unroll 1
-        for (int cc = 0; cc < 4; ++cc) {
-          const int c = half * 4 + cc;
-          tmem_ld_32x32b_x32(trow + c * 32, v);
-          tmem_ld_wait();
-          if (row_ok) {
-            float* o = static_cast<float*>(p.out) + grow * p.ldo + k.n0 + c * 32;
+        for (int round = 0; round < 2; ++round) {
+          if (leader_thread) bulk_wait_group_read0();
+          named_sync(2, EPI_THREADS);
+          if (half == round) {
+#pragma unroll 1
+            for (int cc = 0; cc < 4; ++cc) {
+              tmem_ld_32x32b_x32(trow + (half * 4 + cc) * 32, v);
+              tmem_ld_wait();
+              const uint32_t box = sOut + cc * OUT_BOX_BYTES + r * 128;
 #pragma unroll
-            for (int jj = 0; jj < 32; jj += 4)
-              *reinterpret_cast<float4*>(o + jj) = make_float4(
-                  __fmul_rn(__uint_as_float(v[jj]), alpha), __fmul_rn(__uint_as_float(v[jj + 1]), alpha),
-                  __fmul_rn(__uint_as_float(v[jj + 2]), alpha), __fmul_rn(__uint_as_float(v[jj + 3]), alpha));
+              for (int c16 = 0; c16 < 8; ++c16)
+                st_shared_v4(box + ((c16 ^ (r & 7)) << 4),
+                             __float_as_uint(__fmul_rn(__uint_as_float(v[4 * c16]), alpha)),
+                             __float_as_uint(__fmul_rn(__uint_as_float(v[4 * c16 + 1]), alpha)),
+                             __float_as_uint(__fmul_rn(__uint_as_float(v[4 * c16 + 2]), alpha)),
+                             __float_as_uint(__fmul_rn(__uint_as_float(v[4 * c16 + 3]), alpha)));
+            }
+          }
+          fence_proxy_async();
+          named_sync(2, EPI_THREADS);
+          if (leader_thread) {
+#pragma unroll
+            for (int b = 0; b < 4; ++b)
+              tma_store_2d(&maps.out, (int)(k.n0 + round * 128 + b * 32), (int)orow,
+                           sOut + b * OUT_BOX_BYTES);
+            bulk_commit_group();
           }
         }
         tc_fence_before();

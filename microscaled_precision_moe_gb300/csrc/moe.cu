@@ -13,7 +13,7 @@
 
 namespace mpm {
 
-constexpr int kSegChunk = 4096;   // flat (token, slot) pairs per chunk
+constexpr int kSegChunk = 512;    // flat (token, slot) pairs per chunk (one warp each)
 
 // 1) per-chunk expert histogram: hist[chunk][e]
 __global__ void __launch_bounds__(256) seg_hist_kernel(const int* ids, long long n, int E,
@@ -35,13 +35,15 @@ __global__ void __launch_bounds__(256) seg_hist_kernel(const int* ids, long long
 
 // 2) one CTA: per-expert totals, padded segment offsets (exclusive scan), and
 //    each chunk's first row per expert: base[chunk][e]
-__global__ void __launch_bounds__(1024) seg_scan_kernel(const int* hist, int nchunks, int E,
-                                                       int pad, int* base, int* seg_offsets) {
+__global__ void __launch_bounds__(1024) seg_scan_kernel(const int* __restrict__ hist, int nchunks,
+                                                       int E, int pad, int* __restrict__ base,
+                                                       int* __restrict__ seg_offsets) {
   __shared__ int padded[1024];
   __shared__ int total_sh[1024];
   const int e = threadIdx.x;
   int tot = 0;
   if (e < E) {
+#pragma unroll 8
     for (int c = 0; c < nchunks; ++c) {
       const int v = hist[(long long)c * E + e];
       base[(long long)c * E + e] = tot;        // exclusive within the expert
@@ -61,6 +63,7 @@ __global__ void __launch_bounds__(1024) seg_scan_kernel(const int* hist, int nch
   const int excl = padded[e] - ((e < E) ? (total_sh[e] + pad - 1) / pad * pad : 0);
   if (e < E) {
     seg_offsets[e] = excl;
+#pragma unroll 8
     for (int c = 0; c < nchunks; ++c) base[(long long)c * E + e] += excl;
   }
   if (e == E - 1) seg_offsets[E] = padded[e];
@@ -206,7 +209,7 @@ cudaError_t launch_build_segments(const int* ids, const float* prob, long long T
   cudaError_t err;
   if ((err = cudaMemsetAsync(perm, 0xFF, (size_t)cap * sizeof(int), s)) != cudaSuccess) return err;
   if ((err = cudaMemsetAsync(row_prob, 0, (size_t)cap * sizeof(float), s)) != cudaSuccess) return err;
-  seg_hist_kernel<<<nchunks, 256, (size_t)E * sizeof(int), s>>>(ids, n, (int)E, hist, st);
+  seg_hist_kernel<<<nchunks, 128, (size_t)E * sizeof(int), s>>>(ids, n, (int)E, hist, st);
   if ((err = cudaGetLastError()) != cudaSuccess) return err;
   seg_scan_kernel<<<1, 1024, 0, s>>>(hist, nchunks, (int)E, pad, base, seg_offsets);
   if ((err = cudaGetLastError()) != cudaSuccess) return err;

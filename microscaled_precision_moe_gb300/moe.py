@@ -138,8 +138,9 @@ class NVFP4MoE:
 
 class MXFP8MoE:
     """Buffers and launch sequence of the MXFP8 expert layer, forward and
-    backward, for a fixed (T, H, I, E, k).  tile_m as for NVFP4MoE (the wgrad
-    GEMMs contract over the segments and always use one CTA per tile)."""
+    backward, for a fixed (T, H, I, E, k).  tile_m as for NVFP4MoE; the wgrad
+    GEMMs contract over the expert segments and run on CTA pairs too when the
+    weight's row count is a multiple of 256."""
 
     def __init__(self, T, H, I, E, k, device="cuda", tile_m=256):
         self.T, self.H, self.I, self.E, self.k = T, H, I, E, k
@@ -218,7 +219,7 @@ class MXFP8MoE:
         # FC2 wgrad: dW2[e] = dY_e^T . D_e
         ops.moe_grouped_gemm(L.KIND_MXFP8, L.GROUP_K, L.EPI_F32, E, H, I, 0, seg,
                              self.dyq["col_q"], self.dq["col_q"], self.dyq["col_s"], cap // 32,
-                             self.dq["col_s"], cap // 32, self.dw2)
+                             self.dq["col_s"], cap // 32, self.dw2, tile_m=self._wgrad_tile(H))
         ops.mxfp8_quantize(self.dh, ldc=cap, m_valid=seg[E:], out=self.dhq)
         # FC1 dgrad: dX_perm = dH . W1_e (column-wise W1 copy)
         ops.moe_grouped_gemm(L.KIND_MXFP8, L.GROUP_M, L.EPI_BF16, E, cap, H, 2 * I, seg,
@@ -229,8 +230,11 @@ class MXFP8MoE:
         # FC1 wgrad: dW1[e] = dH_e^T . X_e
         ops.moe_grouped_gemm(L.KIND_MXFP8, L.GROUP_K, L.EPI_F32, E, 2 * I, H, 0, seg,
                              self.dhq["col_q"], self.xq["col_q"], self.dhq["col_s"], cap // 32,
-                             self.xq["col_s"], cap // 32, self.dw1)
+                             self.xq["col_s"], cap // 32, self.dw1, tile_m=self._wgrad_tile(2 * I))
         return self.dx, self.dw1, self.dw2
+
+    def _wgrad_tile(self, m_out):
+        return 256 if (self.tile_m == 256 and m_out % 256 == 0) else 128
 
     def gemm_flops(self):
         R = self.T * self.k

@@ -211,7 +211,7 @@ def test_mxfp8_grouped_fprop_dgrad_wgrad(tile_m):
     dw = torch.empty(E, 256, H, dtype=torch.float32, device="cuda")
     ops.moe_grouped_gemm(L.KIND_MXFP8, L.GROUP_K, L.EPI_F32, E, 256, H, 0, seg,
                          gc["col_q"], mx["col_q"], gc["col_s"], cap // 32, mx["col_s"],
-                         cap // 32, dw)
+                         cap // 32, dw, tile_m=tile_m)
     torch.cuda.synchronize()
     assert ops.get_device_status() == 0
     segn = seg.cpu().numpy()
