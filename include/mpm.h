@@ -250,11 +250,64 @@ mpm_status mpm_moe_combine(const void* y_perm_dev, const int32_t* inv_perm_dev,
                            cudaStream_t stream);
 
 /* ------------------------------------------------------------------------ */
+/* Dequantisation and transpose: operands of the BF16 backward              */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * NVFP4 -> bf16:
+ *   out[r, c] = bf16_rn( e2m1(q[r, c]) * e4m3(s_b[r, c/16]) * s_g[r / rows_per_outer] ),
+ * the product rounded ONCE (to nearest, ties to even) to bf16.
+ * Source: "Towards Blackwell-native 8-bit and 4-bit RL", section
+ * "High-precision and dequantized backward" (the backward GEMMs run in BF16
+ * on the BF16 dequantisation of the exact low-precision forward operands);
+ * "miniTE technical report", section 2.2 (x_hat = q * s_b * s_g).
+ *
+ * q_dev: packed codes u8 [M, K/2] (element 2j in the low nibble); s_dev: E4M3
+ * scales [M, K/16] in 128x4 tiles; outer_dev: fp32 outer scales, one per
+ * rows_per_outer consecutive rows (1 for per-token activations, the rows of
+ * one expert for a weight).  out_dev: bf16 [M, K], leading dimension ldo
+ * elements.  m_valid_dev (nullable): device row count; rows at or beyond it
+ * are not written.  Requirements: K % 64 == 0, rows_per_outer >= 1,
+ * ldo >= K, ldo % 8 == 0, q / s / out 16-byte aligned.
+ */
+mpm_status mpm_nvfp4_dequantize(const uint8_t* q_dev, const uint8_t* s_dev,
+                                const float* outer_dev, int64_t rows_per_outer,
+                                int64_t M, int64_t K, void* out_dev, int64_t ldo,
+                                const int32_t* m_valid_dev, cudaStream_t stream);
+
+/*
+ * MXFP8 (row-wise copy) -> bf16:
+ *   out[r, c] = bf16_rn( e4m3(q[r, c]) * 2^(s[r, c/32] - 127) ).
+ * Source: as above, and "Towards Blackwell-native 8-bit and 4-bit RL",
+ * section "Format background / MXFP8" (blocks of 32 with an E8M0
+ * power-of-two scale).  q_dev u8 [M, K]; s_dev [M, K/32] in 128x4 tiles.
+ * Requirements: K % 32 == 0, ldo >= K, ldo % 8 == 0, pointers 16-byte aligned.
+ */
+mpm_status mpm_mxfp8_dequantize(const uint8_t* q_dev, const uint8_t* s_dev, int64_t M,
+                                int64_t K, void* out_dev, int64_t ldo,
+                                const int32_t* m_valid_dev, cudaStream_t stream);
+
+/*
+ * out[c, r] = in[r, c] for bf16 matrices: the K-major copies that the BF16
+ * weight-gradient and input-gradient GEMMs read.  in [R, C] with leading
+ * dimension ldi; out [C, >= R] with leading dimension ldo >= R.
+ * m_valid_dev (nullable): device row count R' <= R; input rows at or beyond
+ * it are not read and the matching output columns are not written.  Bit
+ * copies, no arithmetic.  Requirements: R, C >= 1, ldi >= C, ldo >= R,
+ * R <= 64 * 65535; in and out do not overlap.
+ */
+mpm_status mpm_transpose_bf16(const void* in_dev, int64_t R, int64_t C, int64_t ldi,
+                              void* out_dev, int64_t ldo, const int32_t* m_valid_dev,
+                              cudaStream_t stream);
+
+/* ------------------------------------------------------------------------ */
 /* Block-scaled grouped GEMM (tcgen05)                                      */
 /* ------------------------------------------------------------------------ */
 
 #define MPM_KIND_NVFP4 0   /* E2M1 x E2M1, E4M3 scales per 16, fp32 accumulate */
 #define MPM_KIND_MXFP8 1   /* E4M3 x E4M3, E8M0 scales per 32, fp32 accumulate */
+#define MPM_KIND_BF16 2    /* bf16 x bf16, fp32 accumulate, no scales (tile_m 256
+                              only): the high-precision / dequantized backward */
 
 #define MPM_GROUP_M 0      /* rows of A split into expert segments (fprop, dgrad) */
 #define MPM_GROUP_K 1      /* reduction split into expert segments (wgrad)        */
@@ -277,7 +330,8 @@ mpm_status mpm_moe_combine(const void* y_perm_dev, const int32_t* inv_perm_dev,
  *   restricted to reduction columns [seg[e], seg[e+1]); output expert e is
  *   [M_out, N] at out + e * M_out * ldo (fp32 only).  Empty experts give 0.
  *
- * a_dev / b_dev: codes (NVFP4: packed, K/2 bytes per row; MXFP8: K bytes),
+ * a_dev / b_dev: codes (NVFP4: packed, K/2 bytes per row; MXFP8: K bytes;
+ * BF16: the bf16 values, 2K bytes per row, sfa_dev / sfb_dev unused),
  * lda_bytes / ldb_bytes their row pitches (multiples of 16).
  * sfa_dev / sfb_dev: their scale matrices in 128x4 tiles, sfa_cols / sfb_cols
  * the UNPADDED scale column counts of the whole A / B matrices
@@ -300,9 +354,13 @@ mpm_status mpm_moe_combine(const void* y_perm_dev, const int32_t* inv_perm_dev,
  * tile_m = 256 runs the tile on a pair of CTAs (tcgen05 cta_group::2): each
  * SM stages its 128 rows of A and half of B, so B moves through shared
  * memory once per 256 output rows instead of once per 128.
- * Requirements: K % 256 == 0 (NVFP4) or % 128 == 0 (MXFP8) in GROUP_M;
- * N % 256 == 0 (SwiGLU: N/2 % 128 == 0); GROUP_K: M_out % 128 == 0,
- * segments multiples of 128 rows.
+ * BF16 (kind::f16 on the tensor cores): "Towards Blackwell-native 8-bit and
+ * 4-bit RL", section "High-precision and dequantized backward" (backward
+ * GEMMs in BF16 on original or dequantised operands).
+ * Requirements: K % 256 == 0 (NVFP4), % 128 == 0 (MXFP8) or % 64 == 0 (BF16)
+ * in GROUP_M; N % 256 == 0 (SwiGLU: N/2 % 128 == 0); GROUP_K (MXFP8 or
+ * BF16, F32 epilogue): M_out % 128 == 0, segments multiples of 128 rows.
+ * BF16 requires tile_m = 256.
  */
 typedef struct {
   int kind;                    /* MPM_KIND_*                                   */

@@ -18,7 +18,7 @@ STATUS_NAMES = {0: "MPM_OK", 1: "MPM_ERR_NULL", 2: "MPM_ERR_SHAPE", 3: "MPM_ERR_
                 7: "MPM_ERR_DEVICE_BOUNDS"}
 
 ROWWISE, COLWISE = 1, 2
-KIND_NVFP4, KIND_MXFP8 = 0, 1
+KIND_NVFP4, KIND_MXFP8, KIND_BF16 = 0, 1, 2
 GROUP_M, GROUP_K = 0, 1
 EPI_F32, EPI_BF16, EPI_SWIGLU, EPI_SWIGLU_SAVE, EPI_DSWIGLU = 0, 1, 2, 3, 4
 GATHER_BF16, GATHER_NVFP4 = 0, 1
@@ -63,6 +63,9 @@ _SIGS = {
     "mpm_moe_gather": (_int, [_int, _vp, _vp, _vp, _i64, _i64, _int, _vp, _vp, _i64, _i64,
                               _vp, _vp, _vp, _vp, _vp]),
     "mpm_moe_combine": (_int, [_vp, _vp, _i64, _int, _i64, _vp, _vp]),
+    "mpm_nvfp4_dequantize": (_int, [_vp, _vp, _vp, _i64, _i64, _i64, _vp, _i64, _vp, _vp]),
+    "mpm_mxfp8_dequantize": (_int, [_vp, _vp, _i64, _i64, _vp, _i64, _vp, _vp]),
+    "mpm_transpose_bf16": (_int, [_vp, _i64, _i64, _i64, _vp, _i64, _vp, _vp]),
     "mpm_moe_grouped_gemm": (_int, [C.POINTER(GroupedGemmDesc), _vp]),
     "mpm_get_device_status": (_int, [C.POINTER(C.c_int32), _vp]),
 }

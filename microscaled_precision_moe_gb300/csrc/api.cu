@@ -9,6 +9,7 @@
 #include "quant.cuh"
 #include "moe.cuh"
 #include "gemm.cuh"
+#include "dequant.cuh"
 
 namespace {
 
@@ -238,27 +239,65 @@ mpm_status mpm_moe_combine(const void* y, const int32_t* inv, int64_t T, int k, 
   return cuda_status(mpm::launch_combine(y, inv, T, k, H, out, stream));
 }
 
+mpm_status mpm_nvfp4_dequantize(const uint8_t* q, const uint8_t* s, const float* outer,
+                                int64_t rows_per_outer, int64_t M, int64_t K, void* out,
+                                int64_t ldo, const int32_t* m_valid, cudaStream_t stream) {
+  if (!q || !s || !outer || !out) return MPM_ERR_NULL;
+  if (M < 1 || K < 64 || K % 64 != 0 || K > (1LL << 30) || rows_per_outer < 1 || ldo < K ||
+      ldo % 8 != 0)
+    return MPM_ERR_SHAPE;
+  if ((M + 3) / 4 > 0x7FFFFFFFLL) return MPM_ERR_SHAPE;
+  if (!aligned(q, 16) || !aligned(s, 16) || !aligned(out, 16) || !aligned(outer, 4))
+    return MPM_ERR_ALIGN;
+  return cuda_status(mpm::launch_nvfp4_dequant(q, s, outer, rows_per_outer, M, (int)K, out, ldo,
+                                               m_valid, stream));
+}
+
+mpm_status mpm_mxfp8_dequantize(const uint8_t* q, const uint8_t* s, int64_t M, int64_t K,
+                                void* out, int64_t ldo, const int32_t* m_valid,
+                                cudaStream_t stream) {
+  if (!q || !s || !out) return MPM_ERR_NULL;
+  if (M < 1 || K < 32 || K % 32 != 0 || K > (1LL << 30) || ldo < K || ldo % 8 != 0)
+    return MPM_ERR_SHAPE;
+  if ((M + 3) / 4 > 0x7FFFFFFFLL) return MPM_ERR_SHAPE;
+  if (!aligned(q, 16) || !aligned(s, 16) || !aligned(out, 16)) return MPM_ERR_ALIGN;
+  return cuda_status(mpm::launch_mxfp8_dequant(q, s, M, (int)K, out, ldo, m_valid, stream));
+}
+
+mpm_status mpm_transpose_bf16(const void* in, int64_t R, int64_t C, int64_t ldi, void* out,
+                              int64_t ldo, const int32_t* m_valid, cudaStream_t stream) {
+  if (!in || !out) return MPM_ERR_NULL;
+  if (R < 1 || C < 1 || ldi < C || ldo < R) return MPM_ERR_SHAPE;
+  if ((C + 63) / 64 > 0x7FFFFFFFLL || (R + 63) / 64 > 65535) return MPM_ERR_SHAPE;
+  if (!aligned(in, 2) || !aligned(out, 2)) return MPM_ERR_ALIGN;
+  return cuda_status(mpm::launch_transpose_bf16(in, R, C, ldi, out, ldo, m_valid, stream));
+}
+
 mpm_status mpm_moe_grouped_gemm(const mpm_grouped_gemm_desc* d, cudaStream_t stream) {
   if (!d) return MPM_ERR_NULL;
-  if (d->kind != MPM_KIND_NVFP4 && d->kind != MPM_KIND_MXFP8) return MPM_ERR_UNSUPPORTED;
+  if (d->kind != MPM_KIND_NVFP4 && d->kind != MPM_KIND_MXFP8 && d->kind != MPM_KIND_BF16)
+    return MPM_ERR_UNSUPPORTED;
+  const bool bf16 = d->kind == MPM_KIND_BF16;
   if (d->group != MPM_GROUP_M && d->group != MPM_GROUP_K) return MPM_ERR_UNSUPPORTED;
   const int tile_m = d->tile_m == 0 ? 128 : d->tile_m;
   if (tile_m != 128 && tile_m != 256) return MPM_ERR_UNSUPPORTED;
   if (tile_m == 256 && d->group == MPM_GROUP_K && d->a_rows % 256 != 0) return MPM_ERR_SHAPE;
+  if (bf16 && tile_m != 256) return MPM_ERR_UNSUPPORTED;
   if (d->epilogue < MPM_EPI_F32 || d->epilogue > MPM_EPI_DSWIGLU) return MPM_ERR_UNSUPPORTED;
-  if (!d->a_dev || !d->b_dev || !d->sfa_dev || !d->sfb_dev || !d->out_dev) return MPM_ERR_NULL;
+  if (!d->a_dev || !d->b_dev || !d->out_dev) return MPM_ERR_NULL;
+  if (!bf16 && (!d->sfa_dev || !d->sfb_dev)) return MPM_ERR_NULL;
   if (d->E < 1 || d->E > 65535 || d->N < 256 || d->N % 256 != 0 || d->a_rows < 1)
     return MPM_ERR_SHAPE;
   const bool swiglu = d->epilogue == MPM_EPI_SWIGLU || d->epilogue == MPM_EPI_SWIGLU_SAVE;
-  const int elems_per_kb = d->kind == MPM_KIND_NVFP4 ? 256 : 128;
+  const int elems_per_kb = d->kind == MPM_KIND_NVFP4 ? 256 : (bf16 ? 64 : 128);
   const int vec = d->kind == MPM_KIND_NVFP4 ? 16 : 32;
   if (d->group == MPM_GROUP_M) {
     if (d->K < elems_per_kb || d->K % elems_per_kb != 0) return MPM_ERR_SHAPE;
     if (!d->seg_dev && d->E != 1) return MPM_ERR_NULL;
-    if (d->b_k_per_expert < 0 || d->b_k_per_expert % (d->kind == MPM_KIND_NVFP4 ? 64 : 128))
+    if (d->b_k_per_expert < 0 || d->b_k_per_expert % (d->kind == MPM_KIND_NVFP4 ? 64 : elems_per_kb))
       return MPM_ERR_SHAPE;
   } else {
-    if (d->kind != MPM_KIND_MXFP8 || d->epilogue != MPM_EPI_F32) return MPM_ERR_UNSUPPORTED;
+    if (d->kind == MPM_KIND_NVFP4 || d->epilogue != MPM_EPI_F32) return MPM_ERR_UNSUPPORTED;
     if (!d->seg_dev) return MPM_ERR_NULL;
     if (d->a_rows % 128 != 0) return MPM_ERR_SHAPE;
   }
@@ -266,14 +305,17 @@ mpm_status mpm_moe_grouped_gemm(const mpm_grouped_gemm_desc* d, cudaStream_t str
   if (d->a_total_rows < 1 || d->b_total_rows < 1) return MPM_ERR_SHAPE;
   if (d->lda_bytes < 128 || d->lda_bytes % 16 || d->ldb_bytes < 128 || d->ldb_bytes % 16)
     return MPM_ERR_ALIGN;
-  if (!aligned(d->a_dev, 16) || !aligned(d->b_dev, 16) || !aligned(d->sfa_dev, 16) ||
-      !aligned(d->sfb_dev, 16) || !aligned(d->out_dev, 16))
+  if (!aligned(d->a_dev, 16) || !aligned(d->b_dev, 16) || !aligned(d->out_dev, 16))
     return MPM_ERR_ALIGN;
-  if (d->sfa_cols < 1 || d->sfb_cols < 1) return MPM_ERR_SHAPE;
+  if (!bf16) {
+    if (!aligned(d->sfa_dev, 16) || !aligned(d->sfb_dev, 16)) return MPM_ERR_ALIGN;
+    if (d->sfa_cols < 1 || d->sfb_cols < 1) return MPM_ERR_SHAPE;
+  }
   if (d->group == MPM_GROUP_M) {
-    const int bytes_per_elem2 = d->kind == MPM_KIND_NVFP4 ? 1 : 2;   // bytes = elems * this / 2
+    // bytes = elems * this / 2
+    const int bytes_per_elem2 = d->kind == MPM_KIND_NVFP4 ? 1 : (bf16 ? 4 : 2);
     if (d->K * bytes_per_elem2 / 2 > d->lda_bytes) return MPM_ERR_SHAPE;
-    if (d->sfa_cols < d->K / vec) return MPM_ERR_SHAPE;
+    if (!bf16 && d->sfa_cols < d->K / vec) return MPM_ERR_SHAPE;
   }
   if (swiglu) {
     if (!d->out2_dev || !d->row_prob_dev) return MPM_ERR_NULL;
@@ -319,8 +361,12 @@ mpm_status mpm_moe_grouped_gemm(const mpm_grouped_gemm_desc* d, cudaStream_t str
     const long long atoms_a = pad_to(d->a_total_rows, 128) * pad_to(d->sfa_cols, 4) / 512;
     const long long atoms_b = pad_to(d->b_total_rows, 128) * pad_to(d->sfb_cols, 4) / 512;
     CUtensorMap tsa, tsb;
-    if (!make_sf_tmap(&tsa, d->sfa_dev, atoms_a, kind_atoms)) return MPM_ERR_CUDA;
-    if (!make_sf_tmap(&tsb, d->sfb_dev, atoms_b, kind_atoms)) return MPM_ERR_CUDA;
+    std::memset(&tsa, 0, sizeof(tsa));
+    std::memset(&tsb, 0, sizeof(tsb));
+    if (!bf16) {
+      if (!make_sf_tmap(&tsa, d->sfa_dev, atoms_a, kind_atoms)) return MPM_ERR_CUDA;
+      if (!make_sf_tmap(&tsb, d->sfb_dev, atoms_b, kind_atoms)) return MPM_ERR_CUDA;
+    }
     CUtensorMap tout;
     std::memset(&tout, 0, sizeof(tout));
     if (d->epilogue == MPM_EPI_BF16) {

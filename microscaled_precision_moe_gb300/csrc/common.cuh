@@ -249,6 +249,16 @@ MPM_DEV void mma_mxf8_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint
          "r"(sfa_tmem), "r"(sfb_tmem) : "memory");
 }
 
+// bf16 x bf16 -> fp32 (kind::f16, no scale factors), M = 256 over the pair
+MPM_DEV void mma_bf16_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                           uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+      :: "r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate) : "memory");
+}
+
 // ---------------------------------------------------------------- tcgen05
 MPM_DEV void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
   asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
@@ -356,6 +366,15 @@ __host__ __device__ constexpr uint32_t idesc_block_scaled(uint32_t fmt, uint32_t
        | (ue8m0 << 23)           // scale type
        | ((m >> 4) << 24)        // M / 16
        | (sf_id << 29);          // A scale-factor id
+}
+
+// instruction descriptor of kind::f16 with bf16 A and B (both K-major), fp32 D
+__host__ __device__ constexpr uint32_t idesc_bf16(uint32_t n, uint32_t m) {
+  return (1u << 4)               // D format fp32
+       | (1u << 7)               // A format bf16
+       | (1u << 10)              // B format bf16
+       | ((n >> 3) << 17)        // N / 8
+       | ((m >> 4) << 24);       // M / 16
 }
 
 }  // namespace mpm

@@ -67,6 +67,17 @@ template <> struct Cfg<MPM_KIND_MXFP8> {
   static constexpr int kStages = 4;
   static constexpr uint32_t kFmt = 0, kUe8m0 = 1;
 };
+// bf16 operands (the high-precision / dequantized backward): 64 elements per
+// 128-byte stage row, no scale tiles, one more stage in the freed space
+template <> struct Cfg<MPM_KIND_BF16> {
+  static constexpr int kElemsPerKB = 64;
+  static constexpr int kAtomsPerKB = 0;
+  static constexpr int kSfaBytes = 0;
+  static constexpr int kSfbBytes = 0;
+  static constexpr int kSfTmemPerStage = 0;
+  static constexpr int kStages = 5;
+  static constexpr uint32_t kFmt = 0, kUe8m0 = 0;
+};
 
 template <int KIND>
 constexpr int stage_bytes() {
@@ -211,8 +222,10 @@ grouped_gemm_pair_kernel(const __grid_constant__ PairMaps maps, const GemmArgs p
     fence_proxy_async();
     prefetch_tmap(&maps.a);
     prefetch_tmap(&maps.b);
-    prefetch_tmap(&maps.sfa);
-    prefetch_tmap(&maps.sfb);
+    if (KIND != MPM_KIND_BF16) {
+      prefetch_tmap(&maps.sfa);
+      prefetch_tmap(&maps.sfb);
+    }
     if (EPI != MPM_EPI_DSWIGLU) prefetch_tmap(&maps.out);
   }
   if (warp == 1) {
@@ -243,10 +256,13 @@ grouped_gemm_pair_kernel(const __grid_constant__ PairMaps maps, const GemmArgs p
         const uint32_t fb = map_to_rank(bar_full + 8 * s, 0);   // the leader's barrier
         const long long ka = k.ka0 + (long long)kb * C::kElemsPerKB;
         const long long kbb = k.kb0 + (long long)kb * C::kElemsPerKB;
-        const int xa = (int)(KIND == MPM_KIND_NVFP4 ? ka / 2 : ka);
-        const int xb = (int)(KIND == MPM_KIND_NVFP4 ? kbb / 2 : kbb);
+        // x coordinates in bytes: 128-byte multiples for every kind
+        const int xa = (int)(KIND == MPM_KIND_NVFP4 ? ka / 2 : (KIND == MPM_KIND_BF16 ? ka * 2 : ka));
+        const int xb =
+            (int)(KIND == MPM_KIND_NVFP4 ? kbb / 2 : (KIND == MPM_KIND_BF16 ? kbb * 2 : kbb));
         tma_load_2d_pair(sA + s * A_STAGE, &maps.a, xa, (int)a_row, fb);
         tma_load_2d_pair(sB + s * B_STAGE, &maps.b, xb, (int)k.brow[rank], fb);
+        if (KIND == MPM_KIND_BF16) continue;
         const long long atom_a = (KIND == MPM_KIND_NVFP4) ? ka / 64 : ka / 128;
         const long long atom_b = (KIND == MPM_KIND_NVFP4) ? kbb / 64 : kbb / 128;
         tma_load_2d_pair(sSFA + s * C::kSfaBytes, &maps.sfa, 0,
@@ -271,7 +287,10 @@ grouped_gemm_pair_kernel(const __grid_constant__ PairMaps maps, const GemmArgs p
       tc_fence_after();
       for (int kb = 0; kb < k.num_kb; ++kb, ++it) {
         const int s = it % S;
-        if (!mbar_wait_cluster(bar_sf + 8 * s, (it / S) & 1u, p.status)) { ok = false; break; }
+        // block-scaled kinds wait for the stage's scale tiles in TMEM (the copy
+        // warps wait for the TMA); bf16 waits for the TMA itself
+        const uint32_t ready = (KIND == MPM_KIND_BF16) ? bar_full + 8 * s : bar_sf + 8 * s;
+        if (!mbar_wait_cluster(ready, (it / S) & 1u, p.status)) { ok = false; break; }
         tc_fence_after();
         const uint32_t sf_col = tmem + SF_TMEM_BASE + s * C::kSfTmemPerStage;
 #pragma unroll
@@ -279,7 +298,9 @@ grouped_gemm_pair_kernel(const __grid_constant__ PairMaps maps, const GemmArgs p
           const uint64_t adesc = sdesc_sw128(sA + s * A_STAGE + ks * 32);
           const uint64_t bdesc = sdesc_sw128(sB + s * B_STAGE + ks * 32);
           const uint32_t acc = (kb > 0 || ks > 0) ? 1u : 0u;
-          if (KIND == MPM_KIND_NVFP4) {
+          if (KIND == MPM_KIND_BF16) {
+            mma_bf16_pair(tmem, adesc, bdesc, idesc_bf16(BN, 256), acc);
+          } else if (KIND == MPM_KIND_NVFP4) {
             const uint32_t idesc = idesc_block_scaled(C::kFmt, BN, C::kUe8m0, 0, 256);
             mma_nvf4_pair(tmem, adesc, bdesc, idesc, sf_col + ks * 4, sf_col + 16 + ks * 8, acc);
           } else {
@@ -291,7 +312,7 @@ grouped_gemm_pair_kernel(const __grid_constant__ PairMaps maps, const GemmArgs p
         if (kb + 1 == k.num_kb) tc_commit_pair(bar_accf, (uint16_t)3);
       }
     }
-  } else if ((warp == 2 || warp == SF_WARP2) && lane == 0 && rank == 0) {
+  } else if ((warp == 2 || warp == SF_WARP2) && lane == 0 && rank == 0 && KIND != MPM_KIND_BF16) {
     // ======================================================== scale-tile copies (leader only)
     // Two threads in two warps each copy half of a stage's scale tiles (one
     // thread's tcgen05.cp instructions issue one after another) and each
@@ -644,6 +665,7 @@ cudaError_t launch_grouped_gemm_pair(int kind, int epi, const CUtensorMap& ta,
   maps.sfb = tsfb;
   maps.out = tout;
   if (kind == MPM_KIND_NVFP4) return pair_dispatch<MPM_KIND_NVFP4>(epi, maps, a, n_tiles, n_tasks, s);
+  if (kind == MPM_KIND_BF16) return pair_dispatch<MPM_KIND_BF16>(epi, maps, a, n_tiles, n_tasks, s);
   return pair_dispatch<MPM_KIND_MXFP8>(epi, maps, a, n_tiles, n_tasks, s);
 }
 

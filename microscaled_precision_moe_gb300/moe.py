@@ -13,6 +13,15 @@ scaling"):
   D --per-token NVFP4 reusing the amax--> A2
   A2 x W2[e]^T --epilogue: alpha--> Y_perm (bf16) --combine--> out (bf16)
 
+BF16 backward of the NVFP4 layer ("Towards Blackwell-native 8-bit and 4-bit
+RL", section "High-precision and dequantized backward"): the four backward
+GEMMs run on the tensor cores in BF16 (fp32 accumulation), either on the
+original BF16 operands ("high_precision") or on the BF16 dequantisation of
+exactly the NVFP4 operands the forward consumed ("dequantized"):
+  dY --gather--> dY_perm;  dY_perm x W2^T-copy --epilogue: SwiGLU backward--> dH
+  dY_perm^T x D per expert --> dW2;  dH x W1^T-copy --> dX_perm --combine--> dX
+  dH^T x X_perm per expert --> dW1
+
 MXFP8 forward + backward ("Towards Blackwell-native 8-bit and 4-bit RL",
 section "Recipe 1 / Training"): every GEMM operand is quantised from bf16;
 fprop uses row-wise copies, dgrad the row-wise gradient and the column-wise
@@ -89,9 +98,12 @@ class NVFP4MoE:
     # each call below is one or more library launches on the current stream
     STAGES = ("quant_x", "segments", "gather", "fc1", "quant_d", "fc2", "combine")
 
-    def forward(self, x, topk_ids, topk_prob, w: NVFP4Weights, mark=None):
+    def forward(self, x, topk_ids, topk_prob, w: NVFP4Weights, mark=None,
+                save_for_backward=False):
         """out [T, H] bf16.  ``mark(i)`` (optional) is called before stage i
-        of STAGES and once more at the end (used to record CUDA events)."""
+        of STAGES and once more at the end (used to record CUDA events).
+        save_for_backward: the FC1 epilogue also stores C = gate|up (bf16,
+        [capacity, 2I]) for the SwiGLU backward."""
         T, H, I, E, k, cap = self.T, self.H, self.I, self.E, self.k, self.cap
         mark = mark or (lambda i: None)
         mark(0)
@@ -104,9 +116,12 @@ class NVFP4MoE:
         ops.moe_gather_nvfp4(*self.xq, H, perm, seg, E, k, cap, out=self.aq, amax_zero=self.amax)
         aq, as_, ats = self.aq
         mark(3)
-        ops.moe_grouped_gemm(L.KIND_NVFP4, L.GROUP_M, L.EPI_SWIGLU, E, cap, 2 * I, H, seg,
+        if save_for_backward:
+            self._alloc_backward()
+        epi, c_out = (L.EPI_SWIGLU_SAVE, self.c1) if save_for_backward else (L.EPI_SWIGLU, self.d)
+        ops.moe_grouped_gemm(L.KIND_NVFP4, L.GROUP_M, epi, E, cap, 2 * I, H, seg,
                              aq, w.w1_q.view(E * 2 * I, H // 2), as_, H // 16, w.w1_s, H // 16,
-                             self.d, b_rows_per_expert=2 * I, alpha_a=ats, alpha_b=w.w1_ts,
+                             c_out, b_rows_per_expert=2 * I, alpha_a=ats, alpha_b=w.w1_ts,
                              row_prob=rp, out2=self.d, amax=self.amax, tile_m=self.tile_m)
         mark(4)
         ops.nvfp4_quantize_per_token(self.d, amax_in=self.amax, m_valid=seg[E:], out=self.dq)
@@ -124,6 +139,121 @@ class NVFP4MoE:
     # kernels launched by one forward: quantiser, 3 segment kernels, gather,
     # FC1, quantiser, FC2, combine
     LAUNCHES_PER_FORWARD = 9
+
+    # ------------------------------------------------------------ BF16 backward
+    BACKWARD_MODES = ("high_precision", "dequantized")
+    BACKWARD_STAGES = ("operands", "gather_dy", "fc2_dgrad", "fc2_wgrad", "fc1_dgrad",
+                       "combine", "fc1_wgrad")
+
+    def _alloc_backward(self):
+        if getattr(self, "c1", None) is not None:
+            return
+        T, H, I, E, cap = self.T, self.H, self.I, self.E, self.cap
+        dev = self.d.device
+        bf, f32 = torch.bfloat16, torch.float32
+        e = lambda *s, dtype=bf: torch.empty(*s, dtype=dtype, device=dev)
+        self.c1 = e(cap, 2 * I)
+        self.xp = e(cap, H)              # X operand of the FC1 wgrad (per mode)
+        self.dop = e(cap, I)             # dequantised D (dequantized mode)
+        self.dyp = e(cap, H)
+        self.dh = e(cap, 2 * I)
+        self.dxp = e(cap, H)
+        self.dx = e(T, H)
+        self.dw1 = e(E, 2 * I, H, dtype=f32)
+        self.dw2 = e(E, H, I, dtype=f32)
+        # K-major copies for the weight-gradient GEMMs (contraction over rows)
+        self.xp_t = e(H, cap)
+        self.dyp_t = e(H, cap)
+        self.d_t = e(I, cap)
+        self.dh_t = e(2 * I, cap)
+        # K-major weight copies for the input-gradient GEMMs
+        self.w1_t = e(H, E * 2 * I)
+        self.w2_t = e(I, E * H)
+        self.w1_op = None
+        self.w2_op = None
+
+    def prepare_backward_weights(self, mode, w1=None, w2=None, w: NVFP4Weights = None):
+        """Transposed BF16 weight copies for the dgrad GEMMs, once per weight
+        update: W2^T [I, E*H] and W1^T [H, E*2I] of the BF16 weights
+        (high_precision, w1 / w2 given) or of the BF16 dequantisation of the
+        NVFP4 weights the forward used (dequantized, w given)."""
+        self._alloc_backward()
+        E, H, I = self.E, self.H, self.I
+        if mode == "high_precision":
+            src1, src2 = w1.reshape(E * 2 * I, H), w2.reshape(E * H, I)
+        elif mode == "dequantized":
+            if self.w1_op is None:
+                self.w1_op = torch.empty(E * 2 * I, H, dtype=torch.bfloat16, device=self.d.device)
+                self.w2_op = torch.empty(E * H, I, dtype=torch.bfloat16, device=self.d.device)
+            src1 = ops.nvfp4_dequantize(w.w1_q.view(E * 2 * I, H // 2), w.w1_s, w.w1_ts, 2 * I, H,
+                                        out=self.w1_op)
+            src2 = ops.nvfp4_dequantize(w.w2_q.view(E * H, I // 2), w.w2_s, w.w2_ts, H, I,
+                                        out=self.w2_op)
+        else:
+            raise ValueError(f"unknown backward mode {mode!r}")
+        ops.transpose_bf16(src1, out=self.w1_t)
+        ops.transpose_bf16(src2, out=self.w2_t)
+
+    def backward(self, dy, mode, x=None, mark=None):
+        """dX [T, H] bf16, dW1 [E, 2I, H] fp32, dW2 [E, H, I] fp32 after a
+        forward with save_for_backward=True and prepare_backward_weights in the
+        same mode.  x: the forward's BF16 input (high_precision only).
+        ``mark(i)`` as in forward, over BACKWARD_STAGES."""
+        if mode not in self.BACKWARD_MODES:
+            raise ValueError(f"unknown backward mode {mode!r}")
+        if getattr(self, "c1", None) is None:
+            raise RuntimeError("backward needs a forward with save_for_backward=True")
+        if self.tile_m != 256:
+            raise ValueError("the BF16 backward runs its GEMMs on CTA pairs: tile_m=256")
+        T, H, I, E, k, cap = self.T, self.H, self.I, self.E, self.k, self.cap
+        seg, perm, inv, rp = self.seg
+        mv = seg[E:]
+        mark = mark or (lambda i: None)
+        bf = L.KIND_BF16
+        mark(0)
+        if mode == "high_precision":
+            ops.moe_gather_bf16(x, perm, seg, E, k, cap, out=self.xp)
+            d_op = self.d
+        else:
+            ops.nvfp4_dequantize(*self.aq, 1, H, m_valid=mv, out=self.xp)
+            ops.nvfp4_dequantize(*self.dq, 1, I, m_valid=mv, out=self.dop)
+            d_op = self.dop
+        mark(1)
+        ops.moe_gather_bf16(dy, perm, seg, E, k, cap, out=self.dyp)
+        mark(2)
+        # FC2 dgrad with the SwiGLU backward fused: dH = [dg | du]
+        ops.moe_grouped_gemm(bf, L.GROUP_M, L.EPI_DSWIGLU, E, cap, I, H, seg, self.dyp, self.w2_t,
+                             None, 0, None, 0, self.dh, b_rows_per_expert=0, b_k_per_expert=H,
+                             row_prob=rp, aux=self.c1, tile_m=256)
+        mark(3)
+        # FC2 wgrad: dW2[e] = dY_e^T . D_e
+        ops.transpose_bf16(self.dyp, m_valid=mv, out=self.dyp_t)
+        ops.transpose_bf16(d_op, m_valid=mv, out=self.d_t)
+        ops.moe_grouped_gemm(bf, L.GROUP_K, L.EPI_F32, E, H, I, 0, seg, self.dyp_t, self.d_t,
+                             None, 0, None, 0, self.dw2, tile_m=256)
+        mark(4)
+        # FC1 dgrad: dX_perm = dH . W1_e
+        ops.moe_grouped_gemm(bf, L.GROUP_M, L.EPI_BF16, E, cap, H, 2 * I, seg, self.dh, self.w1_t,
+                             None, 0, None, 0, self.dxp, b_rows_per_expert=0,
+                             b_k_per_expert=2 * I, tile_m=256)
+        mark(5)
+        ops.moe_combine(self.dxp, inv, T, k, out=self.dx)
+        mark(6)
+        # FC1 wgrad: dW1[e] = dH_e^T . X_e
+        ops.transpose_bf16(self.dh, m_valid=mv, out=self.dh_t)
+        ops.transpose_bf16(self.xp, m_valid=mv, out=self.xp_t)
+        ops.moe_grouped_gemm(bf, L.GROUP_K, L.EPI_F32, E, 2 * I, H, 0, seg, self.dh_t, self.xp_t,
+                             None, 0, None, 0, self.dw1, tile_m=256)
+        mark(7)
+        return self.dx, self.dw1, self.dw2
+
+    # kernels launched by one backward (weights prepared separately)
+    LAUNCHES_PER_BACKWARD = {"high_precision": 11, "dequantized": 12}
+
+    def backward_gemm_flops(self):
+        """Algorithmic FLOPs of the four backward GEMMs over real rows."""
+        R = self.T * self.k
+        return 2 * (2 * R * self.H * 2 * self.I + 2 * R * self.I * self.H)
 
     def gemm_flops(self):
         """Algorithmic FLOPs of the two GEMMs over real (unpadded) rows:

@@ -188,21 +188,28 @@ def moe_grouped_gemm(kind, group, epilogue, E, a_rows, N, K, seg, a, b, sfa, sfa
                      alpha_b=None, row_prob=None, out2=None, aux=None, amax=None, tile_m=128):
     """One grouped block-scaled GEMM launch (see mpm_grouped_gemm_desc).
 
-    a, b: uint8 code matrices [rows, pitch bytes]; out / out2 / aux: row-major
+    a, b: uint8 code matrices [rows, pitch bytes] (bf16 matrices [rows, K]
+    for KIND_BF16, sfa / sfb None); out / out2 / aux: row-major
     tensors whose row strides become ldo / ldo2 / ld_aux.
     """
     lib = L.load()
-    _need_cuda(a, b, sfa, sfb, out)
+    if kind == L.KIND_BF16:
+        _need_cuda(a, b, out)
+        if a.dtype != torch.bfloat16 or b.dtype != torch.bfloat16:
+            raise TypeError("KIND_BF16 takes bf16 operands A and B")
+    else:
+        _need_cuda(a, b, sfa, sfb, out)
     d = L.GroupedGemmDesc()
     d.kind, d.group, d.epilogue, d.tile_m = kind, group, epilogue, tile_m
     d.E, d.a_rows, d.N, d.K = E, a_rows, N, K
     d.seg_dev = None if seg is None else seg.data_ptr()
-    d.a_dev, d.lda_bytes, d.a_total_rows = a.data_ptr(), a.stride(0), a.shape[0]
-    d.b_dev, d.ldb_bytes = b.data_ptr(), b.stride(-2)
+    d.a_dev, d.a_total_rows = a.data_ptr(), a.shape[0]
+    d.lda_bytes = a.stride(0) * a.element_size()
+    d.b_dev, d.ldb_bytes = b.data_ptr(), b.stride(-2) * b.element_size()
     d.b_total_rows = b.numel() // b.stride(-2)
     d.b_rows_per_expert, d.b_k_per_expert = b_rows_per_expert, b_k_per_expert
-    d.sfa_dev, d.sfa_cols = sfa.data_ptr(), sfa_cols
-    d.sfb_dev, d.sfb_cols = sfb.data_ptr(), sfb_cols
+    d.sfa_dev, d.sfa_cols = (None if sfa is None else sfa.data_ptr()), sfa_cols
+    d.sfb_dev, d.sfb_cols = (None if sfb is None else sfb.data_ptr()), sfb_cols
     d.alpha_a_dev = None if alpha_a is None else alpha_a.data_ptr()
     d.alpha_b_dev = None if alpha_b is None else alpha_b.data_ptr()
     d.row_prob_dev = None if row_prob is None else row_prob.data_ptr()
@@ -214,6 +221,50 @@ def moe_grouped_gemm(kind, group, epilogue, E, a_rows, N, K, seg, a, b, sfa, sfa
     d.amax_dev = None if amax is None else amax.data_ptr()
     st = lib.mpm_moe_grouped_gemm(C.byref(d), _stream(a.device))
     L.check(st, "mpm_moe_grouped_gemm")
+    return out
+
+
+# ------------------------------------------------------------ BF16 backward operands
+
+def nvfp4_dequantize(q, s, outer, rows_per_outer: int, K: int, m_valid=None, out=None):
+    """bf16 [M, K] from NVFP4 codes, tiled E4M3 scales and fp32 outer scales
+    (one outer scale per ``rows_per_outer`` rows), each value rounded once."""
+    lib = L.load()
+    _need_cuda(q, s, outer)
+    M = q.shape[0]
+    if out is None:
+        out = torch.empty(M, K, dtype=torch.bfloat16, device=q.device)
+    st = lib.mpm_nvfp4_dequantize(_ptr(q), _ptr(s), _ptr(outer), rows_per_outer, M, K,
+                                  _ptr(out), out.stride(0), _ptr(m_valid), _stream(q.device))
+    L.check(st, "mpm_nvfp4_dequantize")
+    return out
+
+
+def mxfp8_dequantize(q, s, m_valid=None, out=None):
+    """bf16 [M, K] from row-wise MXFP8 codes [M, K] and tiled E8M0 scales."""
+    lib = L.load()
+    _need_cuda(q, s)
+    M, K = q.shape
+    if out is None:
+        out = torch.empty(M, K, dtype=torch.bfloat16, device=q.device)
+    st = lib.mpm_mxfp8_dequantize(_ptr(q), _ptr(s), M, K, _ptr(out), out.stride(0),
+                                  _ptr(m_valid), _stream(q.device))
+    L.check(st, "mpm_mxfp8_dequantize")
+    return out
+
+
+def transpose_bf16(x, m_valid=None, out=None):
+    """out [C, R] = x [R, C]^T for bf16 matrices (bit copies)."""
+    lib = L.load()
+    _need_cuda(x)
+    if x.dtype != torch.bfloat16:
+        raise TypeError("transpose_bf16 takes a bf16 matrix")
+    R, C_ = x.shape
+    if out is None:
+        out = torch.empty(C_, R, dtype=torch.bfloat16, device=x.device)
+    st = lib.mpm_transpose_bf16(_ptr(x), R, C_, x.stride(0), _ptr(out), out.stride(0),
+                                _ptr(m_valid), _stream(x.device))
+    L.check(st, "mpm_transpose_bf16")
     return out
 
 

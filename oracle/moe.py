@@ -11,7 +11,10 @@ by the producer: the permute for FC1, the weighted SwiGLU for FC2), section
 5.4 (FC1 epilogue: ACC x alpha_a[m] (x alpha_b), C = gate | up,
 D = act(gate, up) x prob, amax of D); "Towards Blackwell-native 8-bit and
 4-bit RL", section "Recipe 1 / Training" (dgrad uses the column-wise weight
-copy, wgrad the column-wise activation and gradient copies).
+copy, wgrad the column-wise activation and gradient copies) and section
+"High-precision and dequantized backward" (backward GEMMs in BF16 on the
+original BF16 operands or on the BF16 dequantisation of the forward's
+low-precision operands).
 
 Readings the pages leave open (each one is fixed here):
 * Segment order: rows of expert e are the (token, slot) pairs routed to e in
@@ -254,3 +257,80 @@ def mxfp8_moe_fwd_bwd(x, topk_ids, topk_prob, w1, w2, dy, E: int, pad=ROW_PAD):
     dw1 = grouped_wgrad(mx_cols_t(dh), mx_cols_t(xp), seg)         # [E, 2I, H]
     return dict(seg=seg, perm=perm, inv=inv, row_prob=row_prob, c1=c1, d=d,
                 y=y, out=out, dd=dd, dh=dh, dxp=dxp, dx=dx, dw1=dw1, dw2=dw2)
+
+
+# ------------------------------------------------------------ BF16 backward
+
+BACKWARD_MODES = ("high_precision", "dequantized")
+
+
+def bf16_backward(xp, w1, w2, d, c1, dyp, seg, row_prob, I: int):
+    """Backward of the expert FFN with BF16 GEMMs on the given operands.
+
+    xp [R, H], w1 [E, 2I, H], w2 [E, H, I], d [R, I] (the FC2 input),
+    c1 [R, 2I] (the FC1 output gate|up, where the SwiGLU derivative is
+    taken), dyp [R, H]: the permuted output gradient.  GEMMs in fp64 (one
+    library matmul per expert); dH and dX_perm rounded to bf16 as the kernels
+    store them, dW1 / dW2 left in fp64 (the kernels store fp32).
+
+      dD      = dY_perm W2_e                 [R, I]
+      dH      = SwiGLU'(C1; dD, p)           [R, 2I]
+      dX_perm = dH W1_e                      [R, H]
+      dW2_e   = dY_perm_e^T D_e              [H, I]
+      dW1_e   = dH_e^T X_perm_e              [2I, H]
+    """
+    w2t = np.transpose(np.asarray(w2, dtype=np.float64), (0, 2, 1))     # [E, I, H]
+    w1t = np.transpose(np.asarray(w1, dtype=np.float64), (0, 2, 1))     # [E, H, 2I]
+    dd = grouped_gemm(dyp, w2t, seg)
+    dh = F.bf16_round(swiglu_backward(dd, c1, row_prob, I))
+    dxp = F.bf16_round(grouped_gemm(dh, w1t, seg))
+    dw2 = grouped_wgrad(np.asarray(dyp).T, np.asarray(d).T, seg)
+    dw1 = grouped_wgrad(dh.T, np.asarray(xp).T, seg)
+    return dict(dd=dd, dh=dh, dxp=dxp, dw1=dw1, dw2=dw2)
+
+
+def nvfp4_backward_operands(fwd: dict, x, w1, w2, mode: str):
+    """(X_perm, W1, W2, D) of the BF16 backward after an NVFP4 forward.
+
+    high_precision: the original BF16 operands (X gathered by expert, the
+    BF16 weights, the BF16 D the FC1 epilogue produced before its
+    re-quantisation).  dequantized: the BF16 dequantisation of exactly the
+    NVFP4 operands the forward GEMMs consumed (per-token X codes, the jointly
+    scaled W1 codes, W2 codes, the re-quantised D codes).
+    """
+    k = int(np.asarray(fwd["inv"]).size // np.asarray(x).shape[0])
+    perm = fwd["perm"]
+    if mode == "high_precision":
+        xp = gather_rows(np.asarray(x, dtype=np.float64), perm, k)
+        return xp, np.asarray(w1, np.float64), np.asarray(w2, np.float64), fwd["d"]
+    if mode == "dequantized":
+        xq = Q.nvfp4_dequantize_bf16(fwd["qx"], fwd["sx"], fwd["tsx"])
+        xp = gather_rows(xq, perm, k)
+        (w1p, w1s, w1g), (w2p, w2s, w2g) = fwd["w1"], fwd["w2"]
+        E = w1p.shape[0]
+        b1 = np.stack([Q.nvfp4_dequantize_bf16(w1p[e], w1s[e], w1g[e]) for e in range(E)])
+        b2 = np.stack([Q.nvfp4_dequantize_bf16(w2p[e], w2s[e], w2g[e]) for e in range(E)])
+        dhat = Q.nvfp4_dequantize_bf16(fwd["qd"], fwd["sd"], fwd["tsd"])
+        return xp, b1, b2, dhat
+    raise ValueError(f"unknown backward mode {mode!r}")
+
+
+def nvfp4_moe_backward_bf16(fwd: dict, x, w1, w2, dy, mode: str):
+    """BF16 backward of the NVFP4 expert layer (``fwd`` from nvfp4_moe_forward).
+
+    The SwiGLU derivative is taken at the forward's own FC1 output C1 (the
+    fp64 GEMM of the NVFP4 operands, rounded to bf16 as the forward saves
+    it); routing and probabilities are constants.  Returns the dict of
+    bf16_backward plus dx = bf16(combine(dX_perm)) and the operands used.
+    """
+    T = np.asarray(x).shape[0]
+    inv = np.asarray(fwd["inv"])
+    k = inv.size // T
+    I = np.asarray(w1).shape[1] // 2
+    xp, b1, b2, d = nvfp4_backward_operands(fwd, x, w1, w2, mode)
+    c1 = F.bf16_round(fwd["acc1"])
+    dyp = gather_rows(np.asarray(dy, dtype=np.float64), fwd["perm"], k)
+    r = bf16_backward(xp, b1, b2, d, c1, dyp, fwd["seg"], fwd["row_prob"], I)
+    r["dx"] = F.bf16_round(combine(r["dxp"], inv, T, k))
+    r.update(xp=xp, w1_op=b1, w2_op=b2, d_op=d, c1=c1, dyp=dyp)
+    return r

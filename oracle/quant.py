@@ -233,6 +233,20 @@ def nvfp4_dequantize(packed: np.ndarray, sb: np.ndarray, sg) -> np.ndarray:
     return q * s * sg
 
 
+def nvfp4_dequantize_bf16(packed: np.ndarray, sb: np.ndarray, sg) -> np.ndarray:
+    """The BF16 dequantisation the dequantized backward feeds to its BF16
+    GEMMs ("Towards Blackwell-native 8-bit and 4-bit RL", section
+    "High-precision and dequantized backward"): the exact value q * s_b * s_g
+    rounded once to the nearest bf16 (ties to even).  Returned as fp64."""
+    return F.bf16_round(nvfp4_dequantize(packed, sb, sg))
+
+
+def mxfp8_dequantize_bf16(codes: np.ndarray, scales: np.ndarray) -> np.ndarray:
+    """MXFP8 counterpart (same section): q * 2^e rounded once to bf16 (exact
+    unless the value falls below bf16's normal range)."""
+    return F.bf16_round(mxfp8_dequantize(codes, scales))
+
+
 def nvfp4_encode_exact(x: np.ndarray, sg: np.ndarray):
     """The same encoding with each rounding taken once on the exact real value.
 

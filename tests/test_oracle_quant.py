@@ -272,3 +272,86 @@ def test_storage_sizes_match_memory_tables():
         p, sb, sg = Q.nvfp4_quantize_per_token(np.ascontiguousarray(x.T))
         total += p.nbytes + sb.nbytes
     assert round(total / 2 ** 20, 2) == float(gold["nvfp4_second_copy_mib"])
+
+
+# ------------------------------------------------------------------ dequantisation to bf16
+
+def _bf16_grid_fractions():
+    """Every non-negative finite bf16 value as an exact Fraction, ascending,
+    with its bit pattern (brute-force rounding target)."""
+    from fractions import Fraction
+    bits = np.arange(0, 0x7F80, dtype=np.uint16)            # +0 .. largest finite
+    vals = F.bf16_bits_to_f32(bits).astype(np.float64)
+    return [Fraction(float(v)) for v in vals], bits
+
+
+def _nearest_bf16_brute(v, grid, bits):
+    """Round the exact rational v to the nearest bf16, ties to the even bit
+    pattern, by search over every bf16 value."""
+    import bisect
+    mag = abs(v)
+    i = bisect.bisect_left(grid, mag)
+    if i < len(grid) and grid[i] == mag:
+        j = i
+    elif i == 0:
+        j = 0
+    else:
+        lo, hi = i - 1, min(i, len(grid) - 1)
+        dlo, dhi = mag - grid[lo], grid[hi] - mag
+        j = lo if (dlo < dhi or (dlo == dhi and bits[lo] % 2 == 0)) else hi
+    return float(grid[j]) * (-1.0 if v < 0 else 1.0)
+
+
+def test_nvfp4_dequantize_bf16_brute_force():
+    """q * s_b * s_g rounded once to bf16, against exact rational products and
+    a search over all bf16 values; outer scales chosen to hit exact ties
+    (1 + 2^-8 sits halfway between bf16 neighbours), plain inexact values and
+    the bf16 subnormal range."""
+    from fractions import Fraction
+    grid, bits = _bf16_grid_fractions()
+    rng = np.random.default_rng(5)
+    K = 32
+    sgs = np.array([1.0 + 2.0 ** -8, 1.0 + 3 * 2.0 ** -9, np.float32(1.0 / 3.0), 2.0 ** -130,
+                    np.float32(3.3e-39), np.float32(0.7071)], dtype=np.float32)
+    R = len(sgs)
+    q = rng.integers(0, 16, size=(R, K)).astype(np.uint8)
+    sb = rng.integers(0, 0x7F, size=(R, K // 16)).astype(np.uint8)
+    sb[:, 0] = 0x38                                          # s_b = 1
+    packed = Q.pack_e2m1(q)
+    got = Q.nvfp4_dequantize_bf16(packed, sb, sgs)
+    qv, sv = F.e2m1_decode(q), F.e4m3_decode(sb)
+    for r in range(R):
+        for c in range(K):
+            exact = Fraction(float(qv[r, c])) * Fraction(float(sv[r, c // 16])) * Fraction(float(sgs[r]))
+            assert got[r, c] == _nearest_bf16_brute(exact, grid, bits), (r, c)
+    # the tie row rounds to even: 1 * 1 * (1 + 2^-8) -> 1.0
+    one = Q.pack_e2m1(np.array([[2] + [0] * 15], np.uint8))
+    assert Q.nvfp4_dequantize_bf16(one, np.array([[0x38]], np.uint8),
+                                   np.array([1.0 + 2.0 ** -8], np.float32))[0, 0] == 1.0
+    # double-rounding trap: 1.5 * (1 + 109227 * 2^-23) rounds in fp32 onto a
+    # bf16 tie (and from there down to 1.515625); the single rounding of the
+    # exact product goes up
+    trap = np.float32(1.0 + 109227 * 2.0 ** -23)
+    onefive = Q.pack_e2m1(np.array([[3] + [0] * 15], np.uint8))
+    v = Q.nvfp4_dequantize_bf16(onefive, np.array([[0x38]], np.uint8), np.array([trap]))[0, 0]
+    assert v == 1.5234375
+    assert F.bf16_round(np.array([float(np.float32(1.5 * float(trap)))]))[0] == 1.515625
+
+
+def test_mxfp8_dequantize_bf16_exact_and_extreme():
+    """E4M3 x 2^e is a bf16 value unless it drops below 2^-126 (then one
+    rounding, checked by brute force)."""
+    from fractions import Fraction
+    grid, bits = _bf16_grid_fractions()
+    rng = np.random.default_rng(6)
+    codes = rng.integers(0, 256, size=(3, 64)).astype(np.uint8)
+    codes[(codes & 0x7F) == 0x7F] = 0x10                     # no NaN codes
+    scales = np.array([[127, 140], [0, 3], [120, 1]], dtype=np.uint8)
+    got = Q.mxfp8_dequantize_bf16(codes, scales)
+    ev = F.e4m3_decode(codes)
+    for r in range(3):
+        for c in range(64):
+            exact = Fraction(float(ev[r, c])) * Fraction(2) ** (int(scales[r, c // 32]) - 127)
+            assert got[r, c] == _nearest_bf16_brute(exact, grid, bits), (r, c)
+    normal = scales[:, :, None].repeat(32, axis=2).reshape(3, 64) >= 127
+    assert np.array_equal(got[normal], Q.mxfp8_dequantize(codes, scales)[normal])
