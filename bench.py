@@ -12,7 +12,8 @@ value = algorithmic GEMM FLOPs of the step (real rows, padding excluded) /
 step time, in TFLOP/s.  Inputs are resident in HBM and larger than L2
 (activations 470 MB, FP4 weights 5.6 GB), so no L2 flush is needed.
 Secondary lines (same JSON, key "also"): quantiser GB/s against HBM, the MXFP8
-layer forward+backward on the 30B-shaped layer, the NVFP4 30B-shaped forward.
+layer forward+backward on the 30B-shaped layer, the NVFP4 30B-shaped forward,
+the BF16 (high-precision and dequantized) backward of the NVFP4 layer.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 """
@@ -314,6 +315,54 @@ def _nvfp4_30b_line(peak_fp4, steps=10):
     return r
 
 
+def _nvfp4_bf16_bwd_line(peak_bf16, steps=10):
+    """BF16 backward of the NVFP4 layer (30B-shaped, 8192 tokens), both
+    operand modes: the backward alone is timed (the forward that saves
+    gate|up runs once before); the transposed weight copies are prepared once
+    per weight update and timed separately."""
+    from microscaled_precision_moe_gb300 import synth
+    from microscaled_precision_moe_gb300.moe import NVFP4MoE, NVFP4Weights
+    s = synth.MOE_30B_BWD
+    ids, prob = synth.routing(s)
+    x = synth.moe_activations(s, device="cuda")
+    w1, w2 = synth.moe_weights(s, device="cuda")
+    dy = synth.moe_grad_out(s, device="cuda")
+    W = NVFP4Weights.quantize(w1, w2)
+    L = NVFP4MoE(s.T, s.H, s.I, s.E, s.k)
+    L.forward(x, ids.cuda(), prob.cuda(), W, save_for_backward=True)
+    flops = L.backward_gemm_flops()
+    r = {"workload": s.name, "note": "backward alone / algorithmic FLOPs of its four BF16 GEMMs"}
+    for mode in NVFP4MoE.BACKWARD_MODES:
+        prep = lambda: L.prepare_backward_weights(mode, w1=w1, w2=w2, w=W)
+        for _ in range(2):
+            prep()
+        prep_ms = _time_loop(prep, 3)
+        for _ in range(3):
+            L.backward(dy, mode, x=x)
+        nst = len(NVFP4MoE.BACKWARD_STAGES) + 1
+        ev = [_events(nst) for _ in range(steps)]
+        stream = torch.cuda.current_stream()
+        st, en = _events(2)
+        torch.cuda.synchronize()
+        st.record(stream)
+        for i in range(steps):
+            evi = ev[i]
+            L.backward(dy, mode, x=x, mark=lambda j, evi=evi: evi[j].record(stream))
+        en.record(stream)
+        torch.cuda.synchronize()
+        ms = st.elapsed_time(en) / steps
+        stage = {n: round(float(np.mean([ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(steps)])), 4)
+                 for j, n in enumerate(NVFP4MoE.BACKWARD_STAGES)}
+        tf = flops / (ms * 1e-3) / 1e12
+        r[mode] = {"ms_per_step": round(ms, 3), "TFLOP/s": round(tf, 1),
+                   "frac_bf16_peak": round(tf / peak_bf16, 3), "stage_ms": stage,
+                   "prepare_weights_ms": round(prep_ms, 3),
+                   "gpu_launches_per_step": NVFP4MoE.LAUNCHES_PER_BACKWARD[mode]}
+    del L, W, x, w1, w2, dy
+    torch.cuda.empty_cache()
+    return r
+
+
 # ---------------------------------------------------------------- main
 
 def main():
@@ -324,9 +373,10 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-also", action="store_true", help="skip the secondary lines")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle sample")
-    ap.add_argument("--case", choices=["headline", "slice", "mxfp8"], default="headline",
+    ap.add_argument("--case", choices=["headline", "slice", "mxfp8", "bf16bwd"], default="headline",
                     help="slice: 4096 tokens over 64 experts of the 671B shape (profiling); "
-                         "mxfp8: the MXFP8 30B-shaped forward+backward step alone (profiling)")
+                         "mxfp8: the MXFP8 30B-shaped forward+backward step alone (profiling); "
+                         "bf16bwd: the BF16 backward of the NVFP4 30B-shaped layer alone")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -383,6 +433,15 @@ def main():
                               "ms_per_step": r["ms_per_step"], "higher_is_better": True,
                               "dtype": "mxfp8", "config": {"workload": r["workload"]},
                               "note": r["note"]}), flush=True)
+        return 0
+    if args.case == "bf16bwd":
+        r = _nvfp4_bf16_bwd_line(peaks["bf16_sus"], steps=args.steps)
+        if rank == 0:
+            print(json.dumps({"metric": METRIC, "value": r["dequantized"]["TFLOP/s"],
+                              "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+                              "warmup": 3, "ms_per_step": r["dequantized"]["ms_per_step"],
+                              "higher_is_better": True, "dtype": "bf16",
+                              "config": {"workload": r["workload"]}, "modes": r}), flush=True)
         return 0
     from microscaled_precision_moe_gb300 import ops
     from microscaled_precision_moe_gb300.moe import NVFP4MoE, NVFP4Weights
@@ -485,6 +544,7 @@ def main():
         also = {"quantizers": _quantizer_lines(peaks["hbm"])}
         also["mxfp8_layer_fwd_bwd"] = _mxfp8_layer_line(peak_fp8_sus)
         also["nvfp4_layer_fwd_30b"] = _nvfp4_30b_line(peak_fp4_sus)
+        also["nvfp4_layer_bf16_bwd"] = _nvfp4_bf16_bwd_line(peaks["bf16_sus"])
         also["stage_GBps_or_TFLOPs"] = {
             "quant_x_GB/s": round((shape.T * shape.H * 2.5625 + shape.T * 4) /
                                   (stage_ms["quant_x"] * 1e-3) / 1e9, 1),

@@ -196,3 +196,80 @@ def test_mxfp8_layer_30b_fwd_bwd_full_size():
         _close(dw2[e].cpu().numpy(), dw2e, f"expert {e}: dW2")
     # dX combine property, whole
     assert torch.equal(dx, _slot_sum(L.dxp, L.seg[2].cpu().numpy(), T, k)), "dX combine"
+
+
+def _nvfp4_bf16_bwd_expert_reference(xe, w1e, w2e, dye, p, I, mode):
+    """Oracle for the rows of one expert (padding rows zero): the NVFP4
+    forward (per-token X, joint gate/up W1, W2; C = gate|up in bf16; D; the
+    re-quantised D) and the BF16 backward on the operands of ``mode``."""
+    qx, sx, tsx = Q.nvfp4_quantize_per_token(xe)
+    w1q = Q.nvfp4_quantize_joint([w1e[None, :I], w1e[None, I:]], 1)
+    w2q = Q.nvfp4_quantize_joint([w2e[None]], 1)
+    with np.errstate(over="ignore"):
+        acc1 = Q.nvfp4_dequantize(qx, sx, tsx) @ MO.dequant_weights_nvfp4(w1q)[0].T
+    c1 = F.bf16_round(acc1)
+    d = MO.fc1_epilogue(acc1, p, I)
+    qd, sd, tsd = Q.nvfp4_quantize_per_token(d, np.max(np.abs(d), axis=1).astype(np.float32))
+    if mode == "high_precision":
+        xo, b1, b2, do = xe.astype(np.float64), w1e.astype(np.float64), w2e.astype(np.float64), d
+    else:
+        xo = Q.nvfp4_dequantize_bf16(qx, sx, tsx)
+        b1 = Q.nvfp4_dequantize_bf16(w1q[0][0], w1q[1][0], w1q[2][0])
+        b2 = Q.nvfp4_dequantize_bf16(w2q[0][0], w2q[1][0], w2q[2][0])
+        do = Q.nvfp4_dequantize_bf16(qd, sd, tsd)
+    segl = np.array([0, xe.shape[0]])
+    r = MO.bf16_backward(xo, b1[None], b2[None], do, c1, dye.astype(np.float64), segl, p, I)
+    r.update(c1=c1, d=d, d_op=do)
+    return r
+
+
+def test_nvfp4_layer_30b_bf16_backward_full_size():
+    """8192 tokens, hidden 2048, 128 experts, intermediate 768, top-8: the
+    NVFP4 forward saving gate|up, then the BF16 backward in both operand
+    modes (the bench launch configuration), checked on every row and the
+    full weight gradients of three experts; dX by the combine property."""
+    from microscaled_precision_moe_gb300.moe import NVFP4MoE, NVFP4Weights
+    from microscaled_precision_moe_gb300 import ops
+    shape = synth.MOE_30B_BWD
+    T, H, I, E, k = shape.T, shape.H, shape.I, shape.E, shape.k
+    ids, prob = synth.routing(shape)
+    x = synth.moe_activations(shape, device="cuda")
+    w1, w2 = synth.moe_weights(shape, device="cuda")
+    dy = synth.moe_grad_out(shape, device="cuda")
+    W = NVFP4Weights.quantize(w1, w2)
+    L = NVFP4MoE(T, H, I, E, k)
+    L.forward(x, ids.cuda(), prob.cuda(), W, save_for_backward=True)
+    seg, perm, inv, rp = MO.build_segments(ids.numpy(), prob.numpy(), E, L.tile_m)
+    picks = _pick_experts(seg, 3)
+    for mode in NVFP4MoE.BACKWARD_MODES:
+        L.prepare_backward_weights(mode, w1=w1, w2=w2, w=W)
+        dx, dw1, dw2 = L.backward(dy, mode, x=x)
+        torch.cuda.synchronize()
+        assert ops.get_device_status() == 0
+        for e in picks:
+            r0, r1 = int(seg[e]), int(seg[e + 1])
+            rws = np.arange(r0, r1)
+            real = perm[r0:r1] >= 0
+            toks = np.where(real, perm[r0:r1] // k, 0)
+            sel = torch.from_numpy(toks).cuda()
+            xe = np_bf16(x[sel]) * real[:, None]
+            dye = np_bf16(dy[sel]) * real[:, None]
+            ref = _nvfp4_bf16_bwd_expert_reference(xe, np_bf16(w1[e]), np_bf16(w2[e]), dye,
+                                                   rp[r0:r1], I, mode)
+            gsel = torch.from_numpy(rws).cuda()
+            _close(np_bf16(L.c1[gsel]), ref["c1"], f"{mode} expert {e}: C")
+            _close(np_bf16(L.dh[gsel]), ref["dh"], f"{mode} expert {e}: dH")
+            _close(np_bf16(L.dxp[gsel]), ref["dxp"], f"{mode} expert {e}: dX_perm")
+            _close(dw1[e].cpu().numpy(), ref["dw1"][0], f"{mode} expert {e}: dW1")
+            d_same = (np_bf16(L.d[gsel]) == ref["d"]).all(axis=1)
+            if mode == "high_precision" or d_same.all():
+                _close(dw2[e].cpu().numpy(), ref["dw2"][0], f"{mode} expert {e}: dW2")
+            else:
+                # re-quantised D rows that differ carry another FP4 encoding:
+                # the GEMM against its own operands, then the noise band
+                dop = np_bf16(L.dop[gsel]).astype(np.float64)
+                assert np.array_equal(dop[d_same], ref["d_op"][d_same])
+                _close(dw2[e].cpu().numpy(), dye.astype(np.float64).T @ dop,
+                       f"{mode} expert {e}: dW2 on the kernel's own D_hat")
+                assert Mx.rel_l2(dw2[e].cpu().numpy(), ref["dw2"][0]) < 0.05
+        assert torch.equal(dx, _slot_sum(L.dxp, L.seg[2].cpu().numpy(), T, k)), f"{mode}: dX combine"
