@@ -360,7 +360,13 @@ mpm_status mpm_transpose_bf16(const void* in_dev, int64_t R, int64_t C, int64_t 
  * Requirements: K % 256 == 0 (NVFP4), % 128 == 0 (MXFP8) or % 64 == 0 (BF16)
  * in GROUP_M; N % 256 == 0 (SwiGLU: N/2 % 128 == 0); GROUP_K (MXFP8 or
  * BF16, F32 epilogue): M_out % 128 == 0, segments multiples of 128 rows.
- * BF16 requires tile_m = 256.
+ * BF16 requires tile_m = 256.  MN-major operands (a_mn_major / b_mn_major,
+ * BF16 only) let the backward GEMMs read the row-major activations, gradients
+ * and weights as they are, with no transposed copies: GROUP_M with
+ * b_mn_major (epilogue BF16, F32 or DSWIGLU), GROUP_K with both (F32).
+ * Pitches of MN-major operands: lda_bytes >= 2 * M_out, ldb_bytes >= 2 * N.
+ * Zero-initialise the two fields (memset of the whole descriptor) when they
+ * are not used.
  */
 typedef struct {
   int kind;                    /* MPM_KIND_*                                   */
@@ -391,6 +397,14 @@ typedef struct {
   void* out2_dev; int64_t ldo2;/* SWIGLU(_SAVE): D                             */
   const void* aux_dev; int64_t ld_aux; /* DSWIGLU: C (gate|up)                 */
   float* amax_dev;             /* SWIGLU: fp32 [rows]                          */
+  int a_mn_major;              /* BF16, GROUP_K: 1 = A given as the [rows, M_out]
+                                  matrix (M_out contiguous, rows = the reduction)
+                                  instead of its K-major transpose            */
+  int b_mn_major;              /* BF16: 1 = B given as [K rows, N] (N contiguous):
+                                  GROUP_M: expert e's reduction rows start at
+                                  e * b_k_per_expert and its columns at
+                                  e * b_rows_per_expert; GROUP_K: the [rows, N]
+                                  matrix (with a_mn_major)                    */
 } mpm_grouped_gemm_desc;
 
 mpm_status mpm_moe_grouped_gemm(const mpm_grouped_gemm_desc* desc, cudaStream_t stream);

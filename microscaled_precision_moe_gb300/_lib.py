@@ -42,6 +42,7 @@ class GroupedGemmDesc(C.Structure):
         ("out2_dev", _vp), ("ldo2", _i64),
         ("aux_dev", _vp), ("ld_aux", _i64),
         ("amax_dev", _vp),
+        ("a_mn_major", _int), ("b_mn_major", _int),
     ]
 
 

@@ -58,12 +58,14 @@ EncodeTiledFn encode_fn() {
 
 // 2-D uint8 tensor map over [rows, pitch bytes] with a 128 x 128 box and the
 // 128-byte swizzle (the K-major operand layout of the MMA).
-bool make_tmap(CUtensorMap* m, const void* base, long long pitch, long long rows) {
+// box_rows = 64: the MN-major bf16 staging (128 bytes of M/N x 64 K rows).
+bool make_tmap(CUtensorMap* m, const void* base, long long pitch, long long rows,
+               unsigned box_rows = 128) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[2] = {(cuuint64_t)pitch, (cuuint64_t)rows};
   cuuint64_t strides[1] = {(cuuint64_t)pitch};
-  cuuint32_t box[2] = {128, 128};
+  cuuint32_t box[2] = {128, box_rows};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box,
                   estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -283,6 +285,16 @@ mpm_status mpm_moe_grouped_gemm(const mpm_grouped_gemm_desc* d, cudaStream_t str
   if (tile_m != 128 && tile_m != 256) return MPM_ERR_UNSUPPORTED;
   if (tile_m == 256 && d->group == MPM_GROUP_K && d->a_rows % 256 != 0) return MPM_ERR_SHAPE;
   if (bf16 && tile_m != 256) return MPM_ERR_UNSUPPORTED;
+  const int a_mn = d->a_mn_major ? 1 : 0, b_mn = d->b_mn_major ? 1 : 0;
+  const int maj = a_mn | (b_mn << 1);
+  if (maj != 0) {
+    if (!bf16) return MPM_ERR_UNSUPPORTED;
+    const bool ok_m = d->group == MPM_GROUP_M && maj == 2 &&
+                      (d->epilogue == MPM_EPI_BF16 || d->epilogue == MPM_EPI_F32 ||
+                       d->epilogue == MPM_EPI_DSWIGLU);
+    const bool ok_k = d->group == MPM_GROUP_K && maj == 3 && d->epilogue == MPM_EPI_F32;
+    if (!ok_m && !ok_k) return MPM_ERR_UNSUPPORTED;
+  }
   if (d->epilogue < MPM_EPI_F32 || d->epilogue > MPM_EPI_DSWIGLU) return MPM_ERR_UNSUPPORTED;
   if (!d->a_dev || !d->b_dev || !d->out_dev) return MPM_ERR_NULL;
   if (!bf16 && (!d->sfa_dev || !d->sfb_dev)) return MPM_ERR_NULL;
@@ -315,6 +327,7 @@ mpm_status mpm_moe_grouped_gemm(const mpm_grouped_gemm_desc* d, cudaStream_t str
     // bytes = elems * this / 2
     const int bytes_per_elem2 = d->kind == MPM_KIND_NVFP4 ? 1 : (bf16 ? 4 : 2);
     if (d->K * bytes_per_elem2 / 2 > d->lda_bytes) return MPM_ERR_SHAPE;
+    if (b_mn && 2 * d->N > d->ldb_bytes) return MPM_ERR_SHAPE;
     if (!bf16 && d->sfa_cols < d->K / vec) return MPM_ERR_SHAPE;
   }
   if (swiglu) {
@@ -331,9 +344,15 @@ mpm_status mpm_moe_grouped_gemm(const mpm_grouped_gemm_desc* d, cudaStream_t str
     if (d->ldo % q || d->ldo < d->N) return MPM_ERR_ALIGN;
   }
 
+  if (d->group == MPM_GROUP_K && a_mn &&
+      (2 * d->a_rows > d->lda_bytes || 2 * d->N > d->ldb_bytes))
+    return MPM_ERR_SHAPE;
+
   CUtensorMap ta, tb;
-  if (!make_tmap(&ta, d->a_dev, d->lda_bytes, d->a_total_rows)) return MPM_ERR_CUDA;
-  if (!make_tmap(&tb, d->b_dev, d->ldb_bytes, d->b_total_rows)) return MPM_ERR_CUDA;
+  if (!make_tmap(&ta, d->a_dev, d->lda_bytes, d->a_total_rows, a_mn ? 64 : 128))
+    return MPM_ERR_CUDA;
+  if (!make_tmap(&tb, d->b_dev, d->ldb_bytes, d->b_total_rows, b_mn ? 64 : 128))
+    return MPM_ERR_CUDA;
 
   mpm::GemmArgs a{};
   a.group = d->group;
@@ -380,7 +399,7 @@ mpm_status mpm_moe_grouped_gemm(const mpm_grouped_gemm_desc* d, cudaStream_t str
     const int n_tiles = (int)(swiglu ? (d->N / 2) / 128 : d->N / 256);
     long long n_tasks = (long long)n_tiles * ((d->a_rows + 255) / 256);
     if (d->group == MPM_GROUP_K) n_tasks *= d->E;
-    return cuda_status(mpm::launch_grouped_gemm_pair(d->kind, d->epilogue, ta, tb, tsa, tsb, tout,
+    return cuda_status(mpm::launch_grouped_gemm_pair(d->kind, d->epilogue, maj, ta, tb, tsa, tsb, tout,
                                                      a, n_tiles, n_tasks, stream));
   }
   dim3 grid;

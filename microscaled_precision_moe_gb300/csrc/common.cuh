@@ -341,6 +341,20 @@ MPM_DEV uint64_t sdesc_sw128(uint32_t saddr) {
   d |= (uint64_t)2 << 61;                            // 128-byte swizzle
   return d;
 }
+// Descriptor of an MN-major tile with the 128-byte swizzle: for each k one
+// 128-byte row of the contiguous M (or N) dimension, 8-row groups 1024 bytes
+// apart along K (stride byte offset), blocks of 128 bytes of M/N
+// `mn_block_bytes` apart (leading byte offset).  This is the layout a TMA
+// load with a 128-byte-wide box and the 128-byte swizzle writes.
+MPM_DEV uint64_t sdesc_sw128_mn(uint32_t saddr, uint32_t mn_block_bytes) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)((mn_block_bytes >> 4) & 0x3FFFu) << 16;
+  d |= (uint64_t)(1024 >> 4) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)2 << 61;
+  return d;
+}
 // Descriptor of a 32-row x 16-byte block without swizzle (core matrices of
 // 8 rows x 16 bytes, 128 bytes apart): the source of a scale-factor copy.
 MPM_DEV uint64_t sdesc_sf(uint32_t saddr) {
@@ -368,11 +382,15 @@ __host__ __device__ constexpr uint32_t idesc_block_scaled(uint32_t fmt, uint32_t
        | (sf_id << 29);          // A scale-factor id
 }
 
-// instruction descriptor of kind::f16 with bf16 A and B (both K-major), fp32 D
-__host__ __device__ constexpr uint32_t idesc_bf16(uint32_t n, uint32_t m) {
+// instruction descriptor of kind::f16 with bf16 A and B, fp32 D; a_mn / b_mn
+// mark an operand stored MN-major (M or N contiguous) instead of K-major
+__host__ __device__ constexpr uint32_t idesc_bf16(uint32_t n, uint32_t m, uint32_t a_mn = 0,
+                                                  uint32_t b_mn = 0) {
   return (1u << 4)               // D format fp32
        | (1u << 7)               // A format bf16
        | (1u << 10)              // B format bf16
+       | (a_mn << 15)            // A major-ness
+       | (b_mn << 16)            // B major-ness
        | ((n >> 3) << 17)        // N / 8
        | ((m >> 4) << 24);       // M / 16
 }

@@ -29,7 +29,8 @@ struct GemmArgs {
 
 cudaError_t launch_grouped_gemm(int kind, int epi, const CUtensorMap& ta, const CUtensorMap& tb,
                                 const GemmArgs& a, dim3 grid, cudaStream_t s);
-cudaError_t launch_grouped_gemm_pair(int kind, int epi, const CUtensorMap& ta,
+// maj: bit 0 = A MN-major, bit 1 = B MN-major (bf16 only)
+cudaError_t launch_grouped_gemm_pair(int kind, int epi, int maj, const CUtensorMap& ta,
                                      const CUtensorMap& tb, const CUtensorMap& tsfa,
                                      const CUtensorMap& tsfb, const CUtensorMap& tout,
                                      const GemmArgs& a, int n_tiles, long long n_tasks,

@@ -181,11 +181,17 @@ struct PairMaps {
   CUtensorMap out;    // bf16 output of the BF16 epilogue / D of the SwiGLU epilogues
 };
 
-template <int KIND, int EPI>
+// MAJ (bf16 only): bit 0 = A stored MN-major ([K rows, M] with M contiguous:
+// the weight-gradient A), bit 1 = B stored MN-major ([K rows, N]).  An
+// MN-major operand is staged as two 64-element-wide boxes of 64 K rows each
+// (128 bytes x 64 rows, 128-byte swizzle) per 128 rows of M or N.
+template <int KIND, int EPI, int MAJ>
 __global__ void __launch_bounds__(NTHREADS, 1)
 grouped_gemm_pair_kernel(const __grid_constant__ PairMaps maps, const GemmArgs p, const int n_tiles,
                          const long long n_tasks) {
   using C = Cfg<KIND>;
+  constexpr bool A_MN = (MAJ & 1) != 0, B_MN = (MAJ & 2) != 0;
+  static_assert(MAJ == 0 || KIND == MPM_KIND_BF16, "MN-major operands are bf16 only");
   constexpr int S = C::kStages;
   extern __shared__ uint8_t smem_raw[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -202,10 +208,14 @@ grouped_gemm_pair_kernel(const __grid_constant__ PairMaps maps, const GemmArgs p
   const uint32_t sOut = sSFB + S * C::kSfbBytes;        // 1024-aligned (stage sizes are)
   const uint32_t sBar = sOut + STAGE_OUT_BYTES;
   const uint32_t bar_full = sBar, bar_empty = sBar + 8 * S;
-  const uint32_t bar_accf = sBar + 16 * S, bar_acce = bar_accf + 8;
-  const uint32_t bar_sf = bar_acce + 8 + 32;   // scale tiles of a stage are in TMEM
-  const uint32_t sTmem = bar_acce + 8;
+  // accumulator buffer b: full barrier at bar_acc + 16 b, empty at + 8.  The
+  // bf16 kind keeps two accumulators in TMEM (columns 0-255 and 256-511, no
+  // scale factors there) so a tile's epilogue overlaps the next tile's MMAs.
+  constexpr uint32_t NACC = (KIND == MPM_KIND_BF16) ? 2u : 1u;
+  const uint32_t bar_acc = sBar + 16 * S;
+  const uint32_t sTmem = bar_acc + 32;
   const uint32_t sFlag = sTmem + 8;
+  const uint32_t bar_sf = bar_acc + 48;        // scale tiles of a stage are in TMEM
   volatile uint32_t* tmem_holder = reinterpret_cast<volatile uint32_t*>(gbase + (sTmem - base));
   volatile int* fail_flag = reinterpret_cast<volatile int*>(gbase + (sFlag - base));
 
@@ -214,8 +224,10 @@ grouped_gemm_pair_kernel(const __grid_constant__ PairMaps maps, const GemmArgs p
       mbar_init(bar_full + 8 * s, 1);
       mbar_init(bar_empty + 8 * s, 1);
     }
-    mbar_init(bar_accf, 1);
-    mbar_init(bar_acce, 2);          // one arrive from each CTA's epilogue
+    for (uint32_t b = 0; b < 2; ++b) {
+      mbar_init(bar_acc + 16 * b, 1);
+      mbar_init(bar_acc + 16 * b + 8, 2);   // one arrive from each CTA's epilogue
+    }
     for (int s = 0; s < S; ++s) mbar_init(bar_sf + 8 * s, 2);   // both copy warps
     *fail_flag = 0;
     fence_mbar_init();
@@ -236,7 +248,6 @@ grouped_gemm_pair_kernel(const __grid_constant__ PairMaps maps, const GemmArgs p
   cluster_sync();
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
-  const uint32_t acce_leader = map_to_rank(bar_acce, 0);
   int bad = 0;
 
   if (warp == 0 && lane == 0) {
@@ -260,8 +271,22 @@ grouped_gemm_pair_kernel(const __grid_constant__ PairMaps maps, const GemmArgs p
         const int xa = (int)(KIND == MPM_KIND_NVFP4 ? ka / 2 : (KIND == MPM_KIND_BF16 ? ka * 2 : ka));
         const int xb =
             (int)(KIND == MPM_KIND_NVFP4 ? kbb / 2 : (KIND == MPM_KIND_BF16 ? kbb * 2 : kbb));
-        tma_load_2d_pair(sA + s * A_STAGE, &maps.a, xa, (int)a_row, fb);
-        tma_load_2d_pair(sB + s * B_STAGE, &maps.b, xb, (int)k.brow[rank], fb);
+        if (A_MN) {
+          // A stored [K rows, M]: this CTA's 128 M columns from K row ka
+          tma_load_2d_pair(sA + s * A_STAGE, &maps.a, (int)(a_row * 2), (int)ka, fb);
+          tma_load_2d_pair(sA + s * A_STAGE + A_STAGE / 2, &maps.a, (int)((a_row + 64) * 2),
+                           (int)ka, fb);
+        } else {
+          tma_load_2d_pair(sA + s * A_STAGE, &maps.a, xa, (int)a_row, fb);
+        }
+        if (B_MN) {
+          // B stored [K rows, N]: this CTA's 128 N columns from K row kbb
+          tma_load_2d_pair(sB + s * B_STAGE, &maps.b, (int)(k.brow[rank] * 2), (int)kbb, fb);
+          tma_load_2d_pair(sB + s * B_STAGE + B_STAGE / 2, &maps.b,
+                           (int)((k.brow[rank] + 64) * 2), (int)kbb, fb);
+        } else {
+          tma_load_2d_pair(sB + s * B_STAGE, &maps.b, xb, (int)k.brow[rank], fb);
+        }
         if (KIND == MPM_KIND_BF16) continue;
         const long long atom_a = (KIND == MPM_KIND_NVFP4) ? ka / 64 : ka / 128;
         const long long atom_b = (KIND == MPM_KIND_NVFP4) ? kbb / 64 : kbb / 128;
@@ -282,8 +307,10 @@ grouped_gemm_pair_kernel(const __grid_constant__ PairMaps maps, const GemmArgs p
       const Task k = task_of<KIND, EPI>(p, t, n_tiles, &bad);
       if (!k.valid) break;
       if (k.num_kb == 0) continue;             // empty reduction: nothing to accumulate
-      if (!mbar_wait_cluster(bar_acce, (j & 1u) ^ 1u, p.status)) break;
+      const uint32_t ab = j % NACC, use = j / NACC;
+      if (!mbar_wait_cluster(bar_acc + 16 * ab + 8, (use & 1u) ^ 1u, p.status)) break;
       ++j;
+      const uint32_t dacc = tmem + ab * 256;
       tc_fence_after();
       for (int kb = 0; kb < k.num_kb; ++kb, ++it) {
         const int s = it % S;
@@ -295,21 +322,25 @@ grouped_gemm_pair_kernel(const __grid_constant__ PairMaps maps, const GemmArgs p
         const uint32_t sf_col = tmem + SF_TMEM_BASE + s * C::kSfTmemPerStage;
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks) {
-          const uint64_t adesc = sdesc_sw128(sA + s * A_STAGE + ks * 32);
-          const uint64_t bdesc = sdesc_sw128(sB + s * B_STAGE + ks * 32);
+          // K step of one MMA: 32 bytes along a K-major row, or 16 rows
+          // (2048 bytes) of an MN-major tile
+          const uint64_t adesc = A_MN ? sdesc_sw128_mn(sA + s * A_STAGE + ks * 2048, A_STAGE / 2)
+                                      : sdesc_sw128(sA + s * A_STAGE + ks * 32);
+          const uint64_t bdesc = B_MN ? sdesc_sw128_mn(sB + s * B_STAGE + ks * 2048, B_STAGE / 2)
+                                      : sdesc_sw128(sB + s * B_STAGE + ks * 32);
           const uint32_t acc = (kb > 0 || ks > 0) ? 1u : 0u;
           if (KIND == MPM_KIND_BF16) {
-            mma_bf16_pair(tmem, adesc, bdesc, idesc_bf16(BN, 256), acc);
+            mma_bf16_pair(dacc, adesc, bdesc, idesc_bf16(BN, 256, A_MN ? 1u : 0u, B_MN ? 1u : 0u), acc);
           } else if (KIND == MPM_KIND_NVFP4) {
             const uint32_t idesc = idesc_block_scaled(C::kFmt, BN, C::kUe8m0, 0, 256);
-            mma_nvf4_pair(tmem, adesc, bdesc, idesc, sf_col + ks * 4, sf_col + 16 + ks * 8, acc);
+            mma_nvf4_pair(dacc, adesc, bdesc, idesc, sf_col + ks * 4, sf_col + 16 + ks * 8, acc);
           } else {
             const uint32_t idesc = idesc_block_scaled(C::kFmt, BN, C::kUe8m0, (uint32_t)ks, 256);
-            mma_mxf8_pair(tmem, adesc, bdesc, idesc, sf_col, sf_col + 4, acc);
+            mma_mxf8_pair(dacc, adesc, bdesc, idesc, sf_col, sf_col + 4, acc);
           }
         }
         tc_commit_pair(bar_empty + 8 * s, (uint16_t)3);
-        if (kb + 1 == k.num_kb) tc_commit_pair(bar_accf, (uint16_t)3);
+        if (kb + 1 == k.num_kb) tc_commit_pair(bar_acc + 16 * ab, (uint16_t)3);
       }
     }
   } else if ((warp == 2 || warp == SF_WARP2) && lane == 0 && rank == 0 && KIND != MPM_KIND_BF16) {
@@ -360,7 +391,9 @@ grouped_gemm_pair_kernel(const __grid_constant__ PairMaps maps, const GemmArgs p
     const int q = warp & 3;                     // TMEM lane quarter of this warp
     const int half = (warp - EPI_WARP0) >> 2;   // which half of the columns
     const int r = q * 32 + lane;                // row within this CTA's 128 rows
-    const uint32_t trow = tmem + ((uint32_t)(q * 32) << 16);
+    const uint32_t trow0 = tmem + ((uint32_t)(q * 32) << 16);
+    const uint32_t acce_leader0 = map_to_rank(bar_acc + 8, 0);
+    const uint32_t acce_leader1 = NACC > 1 ? map_to_rank(bar_acc + 16 + 8, 0) : acce_leader0;
     const bool leader_thread = (threadIdx.x == EPI_WARP0 * 32);
     uint32_t j = 0;
     for (long long t = cid; t < n_tasks; t += ncl) {
@@ -375,8 +408,11 @@ grouped_gemm_pair_kernel(const __grid_constant__ PairMaps maps, const GemmArgs p
         }
         continue;
       }
-      const bool w_ok = mbar_wait_cluster(bar_accf, j & 1u, p.status);
+      const uint32_t ab = NACC > 1 ? (j & 1u) : 0u, use = NACC > 1 ? (j >> 1) : j;
+      const bool w_ok = mbar_wait_cluster(bar_acc + 16 * ab, use & 1u, p.status);
       ++j;
+      const uint32_t trow = NACC > 1 ? trow0 + ab * 256 : trow0;
+      const uint32_t acce_leader = (NACC > 1 && ab) ? acce_leader1 : acce_leader0;
       if (!w_ok) *fail_flag = 1;
       named_sync(1, EPI_THREADS);
       if (*fail_flag) break;
@@ -599,11 +635,11 @@ grouped_gemm_pair_kernel(const __grid_constant__ PairMaps maps, const GemmArgs p
 }  // namespace pairk
 
 // ---------------------------------------------------------------- launcher
-template <int KIND, int EPI>
+template <int KIND, int EPI, int MAJ = 0>
 static cudaError_t launch_pair_one(const pairk::PairMaps& maps, const GemmArgs& a, int n_tiles,
                                    long long n_tasks, cudaStream_t s) {
   constexpr int smem = pairk::smem_bytes<KIND>();
-  auto kern = pairk::grouped_gemm_pair_kernel<KIND, EPI>;
+  auto kern = pairk::grouped_gemm_pair_kernel<KIND, EPI, MAJ>;
   static int max_clusters[64] = {0};
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
@@ -653,7 +689,27 @@ static cudaError_t pair_dispatch(int epi, const pairk::PairMaps& maps, const Gem
   }
 }
 
-cudaError_t launch_grouped_gemm_pair(int kind, int epi, const CUtensorMap& ta,
+// bf16 with MN-major operands: B MN-major for the input gradients (bf16 out,
+// or the SwiGLU backward), A and B MN-major for the weight gradients (fp32)
+static cudaError_t pair_dispatch_bf16_mn(int maj, int epi, const pairk::PairMaps& maps,
+                                         const GemmArgs& a, int n_tiles, long long n_tasks,
+                                         cudaStream_t s) {
+  constexpr int K = MPM_KIND_BF16;
+  if (maj == 2) {
+    switch (epi) {
+      case MPM_EPI_F32: return launch_pair_one<K, MPM_EPI_F32, 2>(maps, a, n_tiles, n_tasks, s);
+      case MPM_EPI_BF16: return launch_pair_one<K, MPM_EPI_BF16, 2>(maps, a, n_tiles, n_tasks, s);
+      case MPM_EPI_DSWIGLU:
+        return launch_pair_one<K, MPM_EPI_DSWIGLU, 2>(maps, a, n_tiles, n_tasks, s);
+      default: return cudaErrorInvalidValue;
+    }
+  }
+  if (maj == 3 && epi == MPM_EPI_F32)
+    return launch_pair_one<K, MPM_EPI_F32, 3>(maps, a, n_tiles, n_tasks, s);
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_grouped_gemm_pair(int kind, int epi, int maj, const CUtensorMap& ta,
                                      const CUtensorMap& tb, const CUtensorMap& tsfa,
                                      const CUtensorMap& tsfb, const CUtensorMap& tout,
                                      const GemmArgs& a, int n_tiles, long long n_tasks,
@@ -665,7 +721,10 @@ cudaError_t launch_grouped_gemm_pair(int kind, int epi, const CUtensorMap& ta,
   maps.sfb = tsfb;
   maps.out = tout;
   if (kind == MPM_KIND_NVFP4) return pair_dispatch<MPM_KIND_NVFP4>(epi, maps, a, n_tiles, n_tasks, s);
-  if (kind == MPM_KIND_BF16) return pair_dispatch<MPM_KIND_BF16>(epi, maps, a, n_tiles, n_tasks, s);
+  if (kind == MPM_KIND_BF16) {
+    if (maj != 0) return pair_dispatch_bf16_mn(maj, epi, maps, a, n_tiles, n_tasks, s);
+    return pair_dispatch<MPM_KIND_BF16>(epi, maps, a, n_tiles, n_tasks, s);
+  }
   return pair_dispatch<MPM_KIND_MXFP8>(epi, maps, a, n_tiles, n_tasks, s);
 }
 

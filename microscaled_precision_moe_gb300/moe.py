@@ -161,38 +161,31 @@ class NVFP4MoE:
         self.dx = e(T, H)
         self.dw1 = e(E, 2 * I, H, dtype=f32)
         self.dw2 = e(E, H, I, dtype=f32)
-        # K-major copies for the weight-gradient GEMMs (contraction over rows)
-        self.xp_t = e(H, cap)
-        self.dyp_t = e(H, cap)
-        self.d_t = e(I, cap)
-        self.dh_t = e(2 * I, cap)
-        # K-major weight copies for the input-gradient GEMMs
-        self.w1_t = e(H, E * 2 * I)
-        self.w2_t = e(I, E * H)
-        self.w1_op = None
-        self.w2_op = None
+        self.w1_op = None                # [E*2I, H] bf16 weight operands of the dgrads
+        self.w2_op = None                # [E*H, I]
+        self._wq_op = None
 
     def prepare_backward_weights(self, mode, w1=None, w2=None, w: NVFP4Weights = None):
-        """Transposed BF16 weight copies for the dgrad GEMMs, once per weight
-        update: W2^T [I, E*H] and W1^T [H, E*2I] of the BF16 weights
-        (high_precision, w1 / w2 given) or of the BF16 dequantisation of the
-        NVFP4 weights the forward used (dequantized, w given)."""
+        """Weight operands of the dgrad GEMMs, once per weight update: the BF16
+        weights themselves (high_precision, w1 / w2 given), or the BF16
+        dequantisation of the NVFP4 weights the forward used (dequantized, w
+        given).  The GEMMs read them row-major (MN-major B), no transposes."""
         self._alloc_backward()
         E, H, I = self.E, self.H, self.I
         if mode == "high_precision":
-            src1, src2 = w1.reshape(E * 2 * I, H), w2.reshape(E * H, I)
+            self.w1_op, self.w2_op = w1.reshape(E * 2 * I, H), w2.reshape(E * H, I)
         elif mode == "dequantized":
-            if self.w1_op is None:
-                self.w1_op = torch.empty(E * 2 * I, H, dtype=torch.bfloat16, device=self.d.device)
-                self.w2_op = torch.empty(E * H, I, dtype=torch.bfloat16, device=self.d.device)
-            src1 = ops.nvfp4_dequantize(w.w1_q.view(E * 2 * I, H // 2), w.w1_s, w.w1_ts, 2 * I, H,
-                                        out=self.w1_op)
-            src2 = ops.nvfp4_dequantize(w.w2_q.view(E * H, I // 2), w.w2_s, w.w2_ts, H, I,
-                                        out=self.w2_op)
+            if self._wq_op is None:
+                dev = self.d.device
+                self._wq_op = (torch.empty(E * 2 * I, H, dtype=torch.bfloat16, device=dev),
+                               torch.empty(E * H, I, dtype=torch.bfloat16, device=dev))
+            self.w1_op = ops.nvfp4_dequantize(w.w1_q.view(E * 2 * I, H // 2), w.w1_s, w.w1_ts,
+                                              2 * I, H, out=self._wq_op[0])
+            self.w2_op = ops.nvfp4_dequantize(w.w2_q.view(E * H, I // 2), w.w2_s, w.w2_ts, H, I,
+                                              out=self._wq_op[1])
         else:
             raise ValueError(f"unknown backward mode {mode!r}")
-        ops.transpose_bf16(src1, out=self.w1_t)
-        ops.transpose_bf16(src2, out=self.w2_t)
+        self._w_mode = mode
 
     def backward(self, dy, mode, x=None, mark=None):
         """dX [T, H] bf16, dW1 [E, 2I, H] fp32, dW2 [E, H, I] fp32 after a
@@ -203,11 +196,12 @@ class NVFP4MoE:
             raise ValueError(f"unknown backward mode {mode!r}")
         if getattr(self, "c1", None) is None:
             raise RuntimeError("backward needs a forward with save_for_backward=True")
+        if getattr(self, "_w_mode", None) != mode:
+            raise RuntimeError(f"prepare_backward_weights({mode!r}) first")
         if self.tile_m != 256:
             raise ValueError("the BF16 backward runs its GEMMs on CTA pairs: tile_m=256")
         T, H, I, E, k, cap = self.T, self.H, self.I, self.E, self.k, self.cap
         seg, perm, inv, rp = self.seg
-        mv = seg[E:]
         mark = mark or (lambda i: None)
         bf = L.KIND_BF16
         mark(0)
@@ -215,40 +209,40 @@ class NVFP4MoE:
             ops.moe_gather_bf16(x, perm, seg, E, k, cap, out=self.xp)
             d_op = self.d
         else:
+            mv = seg[E:]
             ops.nvfp4_dequantize(*self.aq, 1, H, m_valid=mv, out=self.xp)
             ops.nvfp4_dequantize(*self.dq, 1, I, m_valid=mv, out=self.dop)
             d_op = self.dop
         mark(1)
         ops.moe_gather_bf16(dy, perm, seg, E, k, cap, out=self.dyp)
         mark(2)
-        # FC2 dgrad with the SwiGLU backward fused: dH = [dg | du]
-        ops.moe_grouped_gemm(bf, L.GROUP_M, L.EPI_DSWIGLU, E, cap, I, H, seg, self.dyp, self.w2_t,
+        # FC2 dgrad with the SwiGLU backward fused: dH = [dg | du];
+        # B = W2 read row-major: expert e's reduction rows e*H .. e*H + H
+        ops.moe_grouped_gemm(bf, L.GROUP_M, L.EPI_DSWIGLU, E, cap, I, H, seg, self.dyp, self.w2_op,
                              None, 0, None, 0, self.dh, b_rows_per_expert=0, b_k_per_expert=H,
-                             row_prob=rp, aux=self.c1, tile_m=256)
+                             row_prob=rp, aux=self.c1, tile_m=256, b_mn_major=True)
         mark(3)
-        # FC2 wgrad: dW2[e] = dY_e^T . D_e
-        ops.transpose_bf16(self.dyp, m_valid=mv, out=self.dyp_t)
-        ops.transpose_bf16(d_op, m_valid=mv, out=self.d_t)
-        ops.moe_grouped_gemm(bf, L.GROUP_K, L.EPI_F32, E, H, I, 0, seg, self.dyp_t, self.d_t,
-                             None, 0, None, 0, self.dw2, tile_m=256)
+        # FC2 wgrad: dW2[e] = dY_e^T . D_e, both read row-major
+        ops.moe_grouped_gemm(bf, L.GROUP_K, L.EPI_F32, E, H, I, 0, seg, self.dyp, d_op,
+                             None, 0, None, 0, self.dw2, tile_m=256, a_mn_major=True,
+                             b_mn_major=True)
         mark(4)
-        # FC1 dgrad: dX_perm = dH . W1_e
-        ops.moe_grouped_gemm(bf, L.GROUP_M, L.EPI_BF16, E, cap, H, 2 * I, seg, self.dh, self.w1_t,
+        # FC1 dgrad: dX_perm = dH . W1_e, W1 read row-major
+        ops.moe_grouped_gemm(bf, L.GROUP_M, L.EPI_BF16, E, cap, H, 2 * I, seg, self.dh, self.w1_op,
                              None, 0, None, 0, self.dxp, b_rows_per_expert=0,
-                             b_k_per_expert=2 * I, tile_m=256)
+                             b_k_per_expert=2 * I, tile_m=256, b_mn_major=True)
         mark(5)
         ops.moe_combine(self.dxp, inv, T, k, out=self.dx)
         mark(6)
         # FC1 wgrad: dW1[e] = dH_e^T . X_e
-        ops.transpose_bf16(self.dh, m_valid=mv, out=self.dh_t)
-        ops.transpose_bf16(self.xp, m_valid=mv, out=self.xp_t)
-        ops.moe_grouped_gemm(bf, L.GROUP_K, L.EPI_F32, E, 2 * I, H, 0, seg, self.dh_t, self.xp_t,
-                             None, 0, None, 0, self.dw1, tile_m=256)
+        ops.moe_grouped_gemm(bf, L.GROUP_K, L.EPI_F32, E, 2 * I, H, 0, seg, self.dh, self.xp,
+                             None, 0, None, 0, self.dw1, tile_m=256, a_mn_major=True,
+                             b_mn_major=True)
         mark(7)
         return self.dx, self.dw1, self.dw2
 
     # kernels launched by one backward (weights prepared separately)
-    LAUNCHES_PER_BACKWARD = {"high_precision": 11, "dequantized": 12}
+    LAUNCHES_PER_BACKWARD = {"high_precision": 7, "dequantized": 8}
 
     def backward_gemm_flops(self):
         """Algorithmic FLOPs of the four backward GEMMs over real rows."""

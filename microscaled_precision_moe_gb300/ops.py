@@ -185,11 +185,13 @@ def moe_combine(y_perm, inv_perm, T: int, k: int, out=None):
 
 def moe_grouped_gemm(kind, group, epilogue, E, a_rows, N, K, seg, a, b, sfa, sfa_cols, sfb,
                      sfb_cols, out, b_rows_per_expert=0, b_k_per_expert=0, alpha_a=None,
-                     alpha_b=None, row_prob=None, out2=None, aux=None, amax=None, tile_m=128):
+                     alpha_b=None, row_prob=None, out2=None, aux=None, amax=None, tile_m=128,
+                     a_mn_major=False, b_mn_major=False):
     """One grouped block-scaled GEMM launch (see mpm_grouped_gemm_desc).
 
     a, b: uint8 code matrices [rows, pitch bytes] (bf16 matrices [rows, K]
-    for KIND_BF16, sfa / sfb None); out / out2 / aux: row-major
+    for KIND_BF16, sfa / sfb None; with a_mn_major / b_mn_major the bf16
+    matrix is [K rows, M or N]); out / out2 / aux: row-major
     tensors whose row strides become ldo / ldo2 / ld_aux.
     """
     lib = L.load()
@@ -219,6 +221,7 @@ def moe_grouped_gemm(kind, group, epilogue, E, a_rows, N, K, seg, a, b, sfa, sfa
     if aux is not None:
         d.aux_dev, d.ld_aux = aux.data_ptr(), aux.stride(-2)
     d.amax_dev = None if amax is None else amax.data_ptr()
+    d.a_mn_major, d.b_mn_major = int(bool(a_mn_major)), int(bool(b_mn_major))
     st = lib.mpm_moe_grouped_gemm(C.byref(d), _stream(a.device))
     L.check(st, "mpm_moe_grouped_gemm")
     return out

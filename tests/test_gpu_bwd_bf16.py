@@ -204,10 +204,22 @@ def test_bf16_grouped_gemm_group_m(epi):
                          out2, b_rows_per_expert=0, b_k_per_expert=K, tile_m=256)
     torch.cuda.synchronize()
     _close(np_bf16(out2[:R]), F.bf16_round(ref), "BF16 GROUP_M, reduction-offset B")
+    # B stored MN-major: [E*K, N], expert e's reduction rows at e*K
+    bmn = torch.cat([b[e * N:(e + 1) * N].t() for e in range(E)], dim=0).contiguous()
+    out3 = torch.empty(cap, N, dtype=out.dtype, device="cuda")
+    ops.moe_grouped_gemm(kind, L.GROUP_M, L.EPI_BF16 if epi == "bf16" else L.EPI_F32, E, cap, N, K,
+                         seg, a, bmn, None, 0, None, 0, out3, b_rows_per_expert=0,
+                         b_k_per_expert=K, tile_m=256, b_mn_major=True)
+    torch.cuda.synchronize()
+    assert ops.get_device_status() == 0
+    got3 = np_bf16(out3[:R]) if epi == "bf16" else out3[:R].cpu().numpy()
+    _close(got3, F.bf16_round(ref) if epi == "bf16" else ref, f"BF16 GROUP_M, MN-major B ({epi})")
 
 
-def test_bf16_grouped_gemm_dswiglu():
-    """dH = SwiGLU backward of dD = dY W2^T-copy, with gate|up read from C."""
+@pytest.mark.parametrize("b_mn", [False, True])
+def test_bf16_grouped_gemm_dswiglu(b_mn):
+    """dH = SwiGLU backward of dD = dY W2 (W2 as a transposed copy, or read
+    row-major as stored), with gate|up read from C."""
     ops, L = _ops(), _L()
     E, I, H = 4, 256, 512
     seg, rp, cap, rseg, rrp = _segments(500, E, 2, 2)
@@ -216,9 +228,10 @@ def test_bf16_grouped_gemm_dswiglu():
     w2t = _bf16_rows(2, 4, I, E * H, std=0.05)           # [I, E*H]
     c1 = _bf16_rows(2, 5, cap, 2 * I, R)
     dh = torch.empty(cap, 2 * I, dtype=torch.bfloat16, device="cuda")
-    ops.moe_grouped_gemm(L.KIND_BF16, L.GROUP_M, L.EPI_DSWIGLU, E, cap, I, H, seg, dy, w2t,
+    bop = w2t.t().contiguous() if b_mn else w2t          # W2 as stored: [E*H, I]
+    ops.moe_grouped_gemm(L.KIND_BF16, L.GROUP_M, L.EPI_DSWIGLU, E, cap, I, H, seg, dy, bop,
                          None, 0, None, 0, dh, b_rows_per_expert=0, b_k_per_expert=H,
-                         row_prob=rp, aux=c1, tile_m=256)
+                         row_prob=rp, aux=c1, tile_m=256, b_mn_major=b_mn)
     torch.cuda.synchronize()
     assert ops.get_device_status() == 0
     w2 = np_bf16(w2t).astype(np.float64).reshape(I, E, H).transpose(1, 0, 2)   # [E, I, H]
@@ -227,9 +240,11 @@ def test_bf16_grouped_gemm_dswiglu():
     _close(np_bf16(dh[:R]), ref, "BF16 dgrad + SwiGLU backward")
 
 
-def test_bf16_grouped_gemm_group_k():
+@pytest.mark.parametrize("mn", [False, True])
+def test_bf16_grouped_gemm_group_k(mn):
     """Weight gradient: contraction over each expert's rows (an empty
-    expert gives zeros), fp32 output per expert."""
+    expert gives zeros), fp32 output per expert; operands as transposed
+    copies, or read row-major as the layer holds them (MN-major)."""
     ops, L = _ops(), _L()
     E, Mo, N = 6, 512, 256
     shape = synth.scaled(synth.MOE_30B, T=400, H=256, I=256, E=E, k=2)
@@ -245,8 +260,9 @@ def test_bf16_grouped_gemm_group_k():
     at[:, R:] = 0
     bt[:, R:] = 0
     out = torch.full((E, Mo, N), 5.0, dtype=torch.float32, device="cuda")
-    ops.moe_grouped_gemm(L.KIND_BF16, L.GROUP_K, L.EPI_F32, E, Mo, N, 0, seg, at, bt,
-                         None, 0, None, 0, out, tile_m=256)
+    aop, bop = (at.t().contiguous(), bt.t().contiguous()) if mn else (at, bt)
+    ops.moe_grouped_gemm(L.KIND_BF16, L.GROUP_K, L.EPI_F32, E, Mo, N, 0, seg, aop, bop,
+                         None, 0, None, 0, out, tile_m=256, a_mn_major=mn, b_mn_major=mn)
     torch.cuda.synchronize()
     assert ops.get_device_status() == 0
     ref = MO.grouped_wgrad(np_bf16(at).astype(np.float64), np_bf16(bt).astype(np.float64), rseg)
