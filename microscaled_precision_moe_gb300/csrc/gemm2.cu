@@ -49,13 +49,16 @@ constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t SF_TMEM_BASE = 256;
 
 template <int KIND> struct Cfg;
+// Stage counts: the ring is latency-bound (TMA issue to data about 2k
+// cycles, data to scale tiles in TMEM about 0.9k more), so it holds as many
+// stages as shared memory allows next to the 32 KB output staging.
 template <> struct Cfg<MPM_KIND_NVFP4> {
   static constexpr int kElemsPerKB = 256;
   static constexpr int kAtomsPerKB = 4;
   static constexpr int kSfaBytes = 4 * 512;
   static constexpr int kSfbBytes = 2 * 4 * 512;
   static constexpr int kSfTmemPerStage = 16 + 32;
-  static constexpr int kStages = 4;
+  static constexpr int kStages = 5;
   static constexpr uint32_t kFmt = 1, kUe8m0 = 0;
 };
 template <> struct Cfg<MPM_KIND_MXFP8> {
@@ -64,7 +67,7 @@ template <> struct Cfg<MPM_KIND_MXFP8> {
   static constexpr int kSfaBytes = 512;
   static constexpr int kSfbBytes = 2 * 512;
   static constexpr int kSfTmemPerStage = 4 + 8;
-  static constexpr int kStages = 4;
+  static constexpr int kStages = 5;
   static constexpr uint32_t kFmt = 0, kUe8m0 = 1;
 };
 // bf16 operands (the high-precision / dequantized backward): 64 elements per
@@ -75,7 +78,7 @@ template <> struct Cfg<MPM_KIND_BF16> {
   static constexpr int kSfaBytes = 0;
   static constexpr int kSfbBytes = 0;
   static constexpr int kSfTmemPerStage = 0;
-  static constexpr int kStages = 5;
+  static constexpr int kStages = 6;
   static constexpr uint32_t kFmt = 0, kUe8m0 = 0;
 };
 
@@ -83,15 +86,16 @@ template <int KIND>
 constexpr int stage_bytes() {
   return A_STAGE + B_STAGE + Cfg<KIND>::kSfaBytes + Cfg<KIND>::kSfbBytes;
 }
-// bf16 output staging for the TMA-store epilogues: 128 rows x 256 columns,
-// as four 128-row x 64-column boxes (128 bytes per row, 128-byte swizzle)
+// output staging for the TMA-store epilogues: two boxes of 128 rows x 128
+// bytes (64 bf16 or 32 fp32 columns, 128-byte swizzle); a CTA's 128 x 256
+// tile goes out in rounds of two boxes
 constexpr int OUT_BOX_COLS = 64;
 constexpr int OUT_BOX_BYTES = BM * OUT_BOX_COLS * 2;    // 16 KB
-constexpr int STAGE_OUT_BYTES = 4 * OUT_BOX_BYTES;      // 64 KB
+constexpr int STAGE_OUT_BYTES = 2 * OUT_BOX_BYTES;      // 32 KB
 
 template <int KIND>
 constexpr int smem_bytes() {
-  return 1024 + Cfg<KIND>::kStages * stage_bytes<KIND>() + STAGE_OUT_BYTES +
+  return 2048 + Cfg<KIND>::kStages * stage_bytes<KIND>() + STAGE_OUT_BYTES +
          (4 * Cfg<KIND>::kStages + 4) * 8 + 32;
 }
 
@@ -205,7 +209,8 @@ grouped_gemm_pair_kernel(const __grid_constant__ PairMaps maps, const GemmArgs p
   const uint32_t sB = sA + S * A_STAGE;
   const uint32_t sSFA = sB + S * B_STAGE;
   const uint32_t sSFB = sSFA + S * C::kSfaBytes;
-  const uint32_t sOut = sSFB + S * C::kSfbBytes;        // 1024-aligned (stage sizes are)
+  // the 128-byte-swizzled staging boxes need a 1024-byte-aligned base
+  const uint32_t sOut = (sSFB + S * C::kSfbBytes + 1023u) & ~1023u;
   const uint32_t sBar = sOut + STAGE_OUT_BYTES;
   const uint32_t bar_full = sBar, bar_empty = sBar + 8 * S;
   // accumulator buffer b: full barrier at bar_acc + 16 b, empty at + 8.  The
@@ -517,62 +522,75 @@ grouped_gemm_pair_kernel(const __grid_constant__ PairMaps maps, const GemmArgs p
             ow[cc * 16 + jj / 2] = pack_bf16(__fmul_rn(__uint_as_float(vv[jj]), alpha),
                                              __fmul_rn(__uint_as_float(vv[jj + 1]), alpha));
         }
-        // this thread's 128 columns -> staging boxes 2*half, 2*half+1, then TMA store
-        if (leader_thread) bulk_wait_group_read0();
-        named_sync(2, EPI_THREADS);
-#pragma unroll
-        for (int bb = 0; bb < 2; ++bb) {
-          const uint32_t box = sOut + (2 * half + bb) * OUT_BOX_BYTES + r * 128;
-#pragma unroll
-          for (int c16 = 0; c16 < 8; ++c16) {
-            const int w = bb * 32 + 4 * c16;
-            st_shared_v4(box + ((c16 ^ (r & 7)) << 4), ow[w], ow[w + 1], ow[w + 2], ow[w + 3]);
-          }
-        }
-        fence_proxy_async();
-        named_sync(2, EPI_THREADS);
-        if (leader_thread) {
-          const int y = (int)orow;
-#pragma unroll
-          for (int b = 0; b < 4; ++b)
-            tma_store_2d(&maps.out, (int)k.n0 + b * OUT_BOX_COLS, y, sOut + b * OUT_BOX_BYTES);
-          bulk_commit_group();
-        }
-      } else if (EPI == MPM_EPI_F32) {
-        // fp32 boxes of 32 columns (128 bytes) x 128 rows: the staging holds
-        // 128 columns, so the two column halves go out in two rounds
+        // two rounds: the warps of column half `round` write their 128
+        // columns into the two staging boxes, then one TMA store each
 #pragma unroll 1
         for (int round = 0; round < 2; ++round) {
           if (leader_thread) bulk_wait_group_read0();
           named_sync(2, EPI_THREADS);
           if (half == round) {
-#pragma unroll 1
-            for (int cc = 0; cc < 4; ++cc) {
-              tmem_ld_32x32b_x32(trow + (half * 4 + cc) * 32, v);
-              tmem_ld_wait();
-              const uint32_t box = sOut + cc * OUT_BOX_BYTES + r * 128;
 #pragma unroll
-              for (int c16 = 0; c16 < 8; ++c16)
-                st_shared_v4(box + ((c16 ^ (r & 7)) << 4),
-                             __float_as_uint(__fmul_rn(__uint_as_float(v[4 * c16]), alpha)),
-                             __float_as_uint(__fmul_rn(__uint_as_float(v[4 * c16 + 1]), alpha)),
-                             __float_as_uint(__fmul_rn(__uint_as_float(v[4 * c16 + 2]), alpha)),
-                             __float_as_uint(__fmul_rn(__uint_as_float(v[4 * c16 + 3]), alpha)));
+            for (int bb = 0; bb < 2; ++bb) {
+              const uint32_t box = sOut + bb * OUT_BOX_BYTES + r * 128;
+#pragma unroll
+              for (int c16 = 0; c16 < 8; ++c16) {
+                const int w = bb * 32 + 4 * c16;
+                st_shared_v4(box + ((c16 ^ (r & 7)) << 4), ow[w], ow[w + 1], ow[w + 2], ow[w + 3]);
+              }
             }
           }
           fence_proxy_async();
           named_sync(2, EPI_THREADS);
           if (leader_thread) {
 #pragma unroll
-            for (int b = 0; b < 4; ++b)
-              tma_store_2d(&maps.out, (int)(k.n0 + round * 128 + b * 32), (int)orow,
+            for (int b = 0; b < 2; ++b)
+              tma_store_2d(&maps.out, (int)k.n0 + round * 128 + b * OUT_BOX_COLS, (int)orow,
                            sOut + b * OUT_BOX_BYTES);
             bulk_commit_group();
           }
         }
+      } else if (EPI == MPM_EPI_F32) {
+        // the thread's 128 fp32 columns are loaded at once and the
+        // accumulator handed back; then fp32 boxes of 32 columns (128 bytes)
+        // x 128 rows go out in four rounds of two boxes
+        uint32_t v2[32], v3[32], v4[32];
+        tmem_ld_32x32b_x32(trow + (half * 4 + 0) * 32, v);
+        tmem_ld_32x32b_x32(trow + (half * 4 + 1) * 32, v2);
+        tmem_ld_32x32b_x32(trow + (half * 4 + 2) * 32, v3);
+        tmem_ld_32x32b_x32(trow + (half * 4 + 3) * 32, v4);
+        tmem_ld_wait();
         tc_fence_before();
         named_sync(1, EPI_THREADS);
         if (leader_thread) mbar_arrive_cluster(acce_leader);
+#pragma unroll
+        for (int round = 0; round < 4; ++round) {
+          if (leader_thread) bulk_wait_group_read0();
+          named_sync(2, EPI_THREADS);
+          if (half == (round >> 1)) {
+#pragma unroll
+            for (int bb = 0; bb < 2; ++bb) {
+              const int cc = (round & 1) * 2 + bb;
+              const uint32_t* vv = cc == 0 ? v : (cc == 1 ? v2 : (cc == 2 ? v3 : v4));
+              const uint32_t box = sOut + bb * OUT_BOX_BYTES + r * 128;
+#pragma unroll
+              for (int c16 = 0; c16 < 8; ++c16)
+                st_shared_v4(box + ((c16 ^ (r & 7)) << 4),
+                             __float_as_uint(__fmul_rn(__uint_as_float(vv[4 * c16]), alpha)),
+                             __float_as_uint(__fmul_rn(__uint_as_float(vv[4 * c16 + 1]), alpha)),
+                             __float_as_uint(__fmul_rn(__uint_as_float(vv[4 * c16 + 2]), alpha)),
+                             __float_as_uint(__fmul_rn(__uint_as_float(vv[4 * c16 + 3]), alpha)));
+            }
+          }
+          fence_proxy_async();
+          named_sync(2, EPI_THREADS);
+          if (leader_thread) {
+#pragma unroll
+            for (int b = 0; b < 2; ++b)
+              tma_store_2d(&maps.out, (int)(k.n0 + (round >> 1) * 128 + ((round & 1) * 2 + b) * 32),
+                           (int)orow, sOut + b * OUT_BOX_BYTES);
+            bulk_commit_group();
+          }
+        }
       } else {   // MPM_EPI_DSWIGLU
         const float prob = row_ok ? p.row_prob[grow] : 0.0f;
         const long long Nh = p.N;
@@ -639,6 +657,7 @@ template <int KIND, int EPI, int MAJ = 0>
 static cudaError_t launch_pair_one(const pairk::PairMaps& maps, const GemmArgs& a, int n_tiles,
                                    long long n_tasks, cudaStream_t s) {
   constexpr int smem = pairk::smem_bytes<KIND>();
+  static_assert(smem <= 227 * 1024, "dynamic shared memory above the per-CTA limit");
   auto kern = pairk::grouped_gemm_pair_kernel<KIND, EPI, MAJ>;
   static int max_clusters[64] = {0};
   int dev = 0;
