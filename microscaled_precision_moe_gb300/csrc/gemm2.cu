@@ -231,7 +231,7 @@ grouped_gemm_pair_kernel(const __grid_constant__ PairMaps maps, const GemmArgs p
     }
     for (uint32_t b = 0; b < 2; ++b) {
       mbar_init(bar_acc + 16 * b, 1);
-      mbar_init(bar_acc + 16 * b + 8, 2);   // one arrive from each CTA's epilogue
+      mbar_init(bar_acc + 16 * b + 8, 16);  // one arrive per epilogue warp of both CTAs
     }
     for (int s = 0; s < S; ++s) mbar_init(bar_sf + 8 * s, 2);   // both copy warps
     *fail_flag = 0;
@@ -444,8 +444,8 @@ grouped_gemm_pair_kernel(const __grid_constant__ PairMaps maps, const GemmArgs p
         tmem_ld_32x32b_x32(trow + 128 + (half * 2 + 1) * 32, u2);
         tmem_ld_wait();
         tc_fence_before();
-        named_sync(1, EPI_THREADS);
-        if (leader_thread) mbar_arrive_cluster(acce_leader);
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(acce_leader);   // this warp's share is read
 #pragma unroll
         for (int cc = 0; cc < 2; ++cc) {
           const int c = half * 2 + cc;
@@ -512,8 +512,8 @@ grouped_gemm_pair_kernel(const __grid_constant__ PairMaps maps, const GemmArgs p
         tmem_ld_32x32b_x32(trow + (half * 4 + 3) * 32, v4);
         tmem_ld_wait();
         tc_fence_before();
-        named_sync(1, EPI_THREADS);
-        if (leader_thread) mbar_arrive_cluster(acce_leader);
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(acce_leader);   // this warp's share is read
 #pragma unroll
         for (int cc = 0; cc < 4; ++cc) {
           const uint32_t* vv = cc == 0 ? v : (cc == 1 ? v2 : (cc == 2 ? v3 : v4));
@@ -560,8 +560,8 @@ grouped_gemm_pair_kernel(const __grid_constant__ PairMaps maps, const GemmArgs p
         tmem_ld_32x32b_x32(trow + (half * 4 + 3) * 32, v4);
         tmem_ld_wait();
         tc_fence_before();
-        named_sync(1, EPI_THREADS);
-        if (leader_thread) mbar_arrive_cluster(acce_leader);
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(acce_leader);   // this warp's share is read
 #pragma unroll
         for (int round = 0; round < 4; ++round) {
           if (leader_thread) bulk_wait_group_read0();
@@ -633,8 +633,8 @@ grouped_gemm_pair_kernel(const __grid_constant__ PairMaps maps, const GemmArgs p
           }
         }
         tc_fence_before();
-        named_sync(1, EPI_THREADS);
-        if (leader_thread) mbar_arrive_cluster(acce_leader);
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(acce_leader);   // this warp's share is read
       }
     }
   }
