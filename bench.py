@@ -13,7 +13,8 @@ step time, in TFLOP/s.  Inputs are resident in HBM and larger than L2
 (activations 470 MB, FP4 weights 5.6 GB), so no L2 flush is needed.
 Secondary lines (same JSON, key "also"): quantiser GB/s against HBM, the MXFP8
 layer forward+backward on the 30B-shaped layer, the NVFP4 30B-shaped forward,
-the BF16 (high-precision and dequantized) backward of the NVFP4 layer.
+the BF16 (high-precision and dequantized) backward of the NVFP4 layer, and
+decode-sized batches of the 671B-shaped layer on the small-M kernel.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 """
@@ -363,6 +364,54 @@ def _nvfp4_bf16_bwd_line(peak_bf16, steps=10):
     return r
 
 
+def _nvfp4_decode_line(peak_hbm, steps=20):
+    """Decode / rollout-sized batches of the 671B-shaped layer (64 and 256
+    tokens, Zipf load over 256 experts): the layer forward on the small-M
+    kernel and, for comparison, on the CTA-pair kernel.  Bound: reading the
+    active experts' FP4 weights (codes + E4M3 scales) once from HBM."""
+    from microscaled_precision_moe_gb300 import synth, _lib as L
+    from microscaled_precision_moe_gb300.moe import NVFP4MoE, NVFP4Weights
+    full = synth.MOE_671B
+    w1, w2 = synth.moe_weights(full, device="cuda")
+    W = NVFP4Weights.quantize(w1, w2)
+    del w1, w2
+    torch.cuda.empty_cache()
+    r = {"workload": "nvfp4_moe_fwd_decode_H7168_I2048_E256_k8_zipf1.1",
+         "note": "layer forward; roofline = active experts' FP4 weight bytes / time vs measured HBM"}
+    for T in (64, 256):
+        s = synth.scaled(full, T=T)
+        ids, prob = synth.routing(s)
+        x = synth.moe_activations(s, device="cuda")
+        idc, prc = ids.cuda(), prob.cuda()
+        active = int(np.unique(ids.numpy()).size)
+        wbytes = active * 3 * s.H * s.I * (0.5 + 1.0 / 16)
+        for name, tm in (("small_m", L.TILE_SMALL_M), ("pair256", 256)):
+            layer = NVFP4MoE(T, s.H, s.I, s.E, s.k, tile_m=tm)
+            nst = len(NVFP4MoE.STAGES) + 1
+            for _ in range(3):
+                layer.forward(x, idc, prc, W)
+            ev = [_events(nst) for _ in range(steps)]
+            torch.cuda.synchronize()
+            for i in range(steps):
+                evi = ev[i]
+                layer.forward(x, idc, prc, W, mark=lambda j, evi=evi: evi[j].record())
+            torch.cuda.synchronize()
+            tot = float(np.median([ev[i][0].elapsed_time(ev[i][nst - 1]) for i in range(steps)]))
+            st = {n: round(float(np.median([ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(steps)])), 4)
+                  for j, n in enumerate(NVFP4MoE.STAGES)}
+            gemm_ms = st["fc1"] + st["fc2"]
+            r[f"T{T}_{name}"] = {"active_experts": active, "ms": round(tot, 4),
+                                 "gemm_ms": round(gemm_ms, 4),
+                                 "weight_GB/s_in_gemms": round(wbytes / (gemm_ms * 1e-3) / 1e9, 1),
+                                 "frac_hbm_gemms": round(wbytes / (gemm_ms * 1e-3) / 1e9 / peak_hbm, 3),
+                                 "stage_ms": st}
+            del layer
+            torch.cuda.empty_cache()
+    del W
+    torch.cuda.empty_cache()
+    return r
+
+
 # ---------------------------------------------------------------- main
 
 def main():
@@ -373,10 +422,12 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-also", action="store_true", help="skip the secondary lines")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle sample")
-    ap.add_argument("--case", choices=["headline", "slice", "mxfp8", "bf16bwd"], default="headline",
+    ap.add_argument("--case", choices=["headline", "slice", "mxfp8", "bf16bwd", "decode"],
+                    default="headline",
                     help="slice: 4096 tokens over 64 experts of the 671B shape (profiling); "
                          "mxfp8: the MXFP8 30B-shaped forward+backward step alone (profiling); "
-                         "bf16bwd: the BF16 backward of the NVFP4 30B-shaped layer alone")
+                         "bf16bwd: the BF16 backward of the NVFP4 30B-shaped layer alone; "
+                         "decode: 64 / 256-token batches of the 671B-shaped layer")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -433,6 +484,14 @@ def main():
                               "ms_per_step": r["ms_per_step"], "higher_is_better": True,
                               "dtype": "mxfp8", "config": {"workload": r["workload"]},
                               "note": r["note"]}), flush=True)
+        return 0
+    if args.case == "decode":
+        r = _nvfp4_decode_line(peaks["hbm"], steps=args.steps)
+        if rank == 0:
+            print(json.dumps({"metric": METRIC, "value": r["T64_small_m"]["ms"], "unit": "ms",
+                              "n_gpus": world, "steps": args.steps, "warmup": 3,
+                              "higher_is_better": False, "dtype": "nvfp4",
+                              "config": {"workload": r["workload"]}, "decode": r}), flush=True)
         return 0
     if args.case == "bf16bwd":
         r = _nvfp4_bf16_bwd_line(peaks["bf16_sus"], steps=args.steps)
@@ -545,6 +604,7 @@ def main():
         also["mxfp8_layer_fwd_bwd"] = _mxfp8_layer_line(peak_fp8_sus)
         also["nvfp4_layer_fwd_30b"] = _nvfp4_30b_line(peak_fp4_sus)
         also["nvfp4_layer_bf16_bwd"] = _nvfp4_bf16_bwd_line(peaks["bf16_sus"])
+        also["nvfp4_layer_decode"] = _nvfp4_decode_line(peaks["hbm"])
         also["stage_GBps_or_TFLOPs"] = {
             "quant_x_GB/s": round((shape.T * shape.H * 2.5625 + shape.T * 4) /
                                   (stage_ms["quant_x"] * 1e-3) / 1e9, 1),

@@ -188,7 +188,8 @@ mpm_status mpm_nvfp4_quantize_weight_noalloc(const void* const* parts_dev,
 
 /*
  * Row capacity of the permuted buffers for T tokens, top-k and E experts with
- * segments padded to `pad` rows (128 or 256): pad(T*k) + pad*E.
+ * segments padded to `pad` rows (16, 32, 64, 128 or 256): pad(T*k) + pad*E;
+ * 0 for an invalid argument.
  */
 int64_t mpm_moe_row_capacity(int64_t T, int k, int64_t E, int pad);
 size_t mpm_moe_segments_workspace_bytes(int64_t T, int k, int64_t E);
@@ -196,7 +197,8 @@ size_t mpm_moe_segments_workspace_bytes(int64_t T, int k, int64_t E);
 /*
  * Counting sort of the T*k routed (token, slot) pairs by expert into one
  * contiguous buffer, each expert's segment padded to `pad` rows (128: one
- * MMA tile; 256: one CTA-pair tile, required by the tile_m = 256 GEMM).
+ * MMA tile; 256: one CTA-pair tile, required by the tile_m = 256 GEMM;
+ * 16 / 32 / 64 for the small-M GEMM, which takes segments of any length).
  * Source: "miniTE technical report", section 5.2 (contiguous buffer with
  * expert boundaries given by offsets kept on the device; zero-token experts
  * and padding handled in the same path).
@@ -309,6 +311,10 @@ mpm_status mpm_transpose_bf16(const void* in_dev, int64_t R, int64_t C, int64_t 
 #define MPM_KIND_BF16 2    /* bf16 x bf16, fp32 accumulate, no scales (tile_m 256
                               only): the high-precision / dequantized backward */
 
+/* tile_m value selecting the small-M (decode / rollout) kernel: one CTA per
+   128 weight rows x 128 routed rows, weights on the MMA's M side */
+#define MPM_TILE_SMALL_M 1
+
 #define MPM_GROUP_M 0      /* rows of A split into expert segments (fprop, dgrad) */
 #define MPM_GROUP_K 1      /* reduction split into expert segments (wgrad)        */
 
@@ -360,7 +366,14 @@ mpm_status mpm_transpose_bf16(const void* in_dev, int64_t R, int64_t C, int64_t 
  * Requirements: K % 256 == 0 (NVFP4), % 128 == 0 (MXFP8) or % 64 == 0 (BF16)
  * in GROUP_M; N % 256 == 0 (SwiGLU: N/2 % 128 == 0); GROUP_K (MXFP8 or
  * BF16, F32 epilogue): M_out % 128 == 0, segments multiples of 128 rows.
- * BF16 requires tile_m = 256.  MN-major operands (a_mn_major / b_mn_major,
+ * BF16 requires tile_m = 256.
+ * tile_m = MPM_TILE_SMALL_M computes the same result with the roles swapped
+ * inside the MMA: 128 weight rows on its M side, a chunk of 128 routed rows
+ * of one segment on its N side, persistent CTAs over (chunk, weight tile),
+ * for batches where each expert receives few rows and the layer is bound by
+ * reading the active experts' weights once ("Towards Blackwell-native 8-bit
+ * and 4-bit RL", the rollout side of section "Per-token activation
+ * scaling").  MN-major operands (a_mn_major / b_mn_major,
  * BF16 only) let the backward GEMMs read the row-major activations, gradients
  * and weights as they are, with no transposed copies: GROUP_M with
  * b_mn_major (epilogue BF16, F32 or DSWIGLU), GROUP_K with both (F32).
@@ -374,7 +387,11 @@ typedef struct {
                                   per 256x256 tile, persistent (GROUP_M: the
                                   expert segments must be multiples of 256
                                   rows, checked on the device; GROUP_K: the
-                                  output rows a_rows % 256 == 0)            */
+                                  output rows a_rows % 256 == 0);
+                                  MPM_TILE_SMALL_M: the small-M kernel
+                                  (GROUP_M, NVFP4 or MXFP8, epilogue F32, BF16
+                                  or SWIGLU, 128-row segments, N (SWIGLU: N/2)
+                                  % 128 == 0)                                */
   int group;                   /* MPM_GROUP_*                                  */
   int epilogue;                /* MPM_EPI_*                                    */
   int64_t E;                   /* experts (groups)                             */

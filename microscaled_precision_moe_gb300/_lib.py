@@ -20,6 +20,7 @@ STATUS_NAMES = {0: "MPM_OK", 1: "MPM_ERR_NULL", 2: "MPM_ERR_SHAPE", 3: "MPM_ERR_
 ROWWISE, COLWISE = 1, 2
 KIND_NVFP4, KIND_MXFP8, KIND_BF16 = 0, 1, 2
 GROUP_M, GROUP_K = 0, 1
+TILE_SMALL_M = 1
 EPI_F32, EPI_BF16, EPI_SWIGLU, EPI_SWIGLU_SAVE, EPI_DSWIGLU = 0, 1, 2, 3, 4
 GATHER_BF16, GATHER_NVFP4 = 0, 1
 

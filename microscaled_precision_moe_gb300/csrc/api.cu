@@ -37,6 +37,10 @@ mpm_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MPM_OK : MPM_E
 
 long long pad_to(long long v, long long m) { return (v + m - 1) / m * m; }
 
+// segment paddings: 256 (CTA-pair tiles), 128 (one-CTA tiles), 16 / 32 / 64
+// (the small-M kernel, which takes segments of any length)
+bool valid_pad(int pad) { return pad == 16 || pad == 32 || pad == 64 || pad == 128 || pad == 256; }
+
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                    const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
                                    const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
@@ -192,7 +196,7 @@ mpm_status mpm_nvfp4_quantize_weight(const void* const* parts, const int64_t* pa
 }
 
 int64_t mpm_moe_row_capacity(int64_t T, int k, int64_t E, int pad) {
-  if (T < 1 || k < 1 || E < 1 || (pad != 128 && pad != 256)) return 0;
+  if (T < 1 || k < 1 || E < 1 || !valid_pad(pad)) return 0;
   return pad_to(T * k, pad) + (int64_t)pad * E;
 }
 
@@ -207,7 +211,7 @@ mpm_status mpm_moe_build_segments(const int32_t* ids, const float* prob, int64_t
                                   cudaStream_t stream) {
   if (!ids || !prob || !seg || !perm || !inv || !row_prob || !ws) return MPM_ERR_NULL;
   if (T < 1 || k < 1 || k > 64 || E < 1 || E > 1024) return MPM_ERR_SHAPE;
-  if (pad != 128 && pad != 256) return MPM_ERR_SHAPE;
+  if (!valid_pad(pad)) return MPM_ERR_SHAPE;
   if (T * k > (1ll << 30)) return MPM_ERR_SHAPE;
   if (ws_bytes < mpm::segments_ws_bytes(T, k, E)) return MPM_ERR_SHAPE;
   if (!aligned(ws, 4)) return MPM_ERR_ALIGN;
@@ -282,7 +286,12 @@ mpm_status mpm_moe_grouped_gemm(const mpm_grouped_gemm_desc* d, cudaStream_t str
   const bool bf16 = d->kind == MPM_KIND_BF16;
   if (d->group != MPM_GROUP_M && d->group != MPM_GROUP_K) return MPM_ERR_UNSUPPORTED;
   const int tile_m = d->tile_m == 0 ? 128 : d->tile_m;
-  if (tile_m != 128 && tile_m != 256) return MPM_ERR_UNSUPPORTED;
+  if (tile_m != 128 && tile_m != 256 && tile_m != MPM_TILE_SMALL_M) return MPM_ERR_UNSUPPORTED;
+  const bool small = tile_m == MPM_TILE_SMALL_M;
+  if (small && (bf16 || d->group != MPM_GROUP_M ||
+                (d->epilogue != MPM_EPI_F32 && d->epilogue != MPM_EPI_BF16 &&
+                 d->epilogue != MPM_EPI_SWIGLU)))
+    return MPM_ERR_UNSUPPORTED;
   if (tile_m == 256 && d->group == MPM_GROUP_K && d->a_rows % 256 != 0) return MPM_ERR_SHAPE;
   if (bf16 && tile_m != 256) return MPM_ERR_UNSUPPORTED;
   const int a_mn = d->a_mn_major ? 1 : 0, b_mn = d->b_mn_major ? 1 : 0;
@@ -375,6 +384,16 @@ mpm_status mpm_moe_grouped_gemm(const mpm_grouped_gemm_desc* d, cudaStream_t str
   a.amax = d->amax_dev;
   a.status = status_ptr();
 
+  if (small) {
+    // weights (B) on the MMA's M side: 128-row weight tiles, 128-row chunks
+    // of the routed rows (A) on its N side
+    const long long n_out = d->epilogue == MPM_EPI_SWIGLU ? d->N / 2 : d->N;
+    if (n_out % 128 != 0) return MPM_ERR_SHAPE;
+    const int n_wt = (int)(n_out / 128);
+    const long long n_tasks = (long long)n_wt * ((d->a_rows + 127) / 128);
+    return cuda_status(mpm::launch_grouped_gemm_small(d->kind, d->epilogue, ta, tb, a, n_wt, n_tasks,
+                                                      stream));
+  }
   if (tile_m == 256) {
     const int kind_atoms = d->kind == MPM_KIND_NVFP4 ? 4 : 1;
     const long long atoms_a = pad_to(d->a_total_rows, 128) * pad_to(d->sfa_cols, 4) / 512;

@@ -35,4 +35,9 @@ cudaError_t launch_grouped_gemm_pair(int kind, int epi, int maj, const CUtensorM
                                      const CUtensorMap& tsfb, const CUtensorMap& tout,
                                      const GemmArgs& a, int n_tiles, long long n_tasks,
                                      cudaStream_t s);
+// small-M kernel (one CTA per 128 weight rows x 128 routed rows): n_wt
+// weight tiles per chunk of 128 rows, tasks = chunks x n_wt
+cudaError_t launch_grouped_gemm_small(int kind, int epi, const CUtensorMap& ta,
+                                      const CUtensorMap& tb, const GemmArgs& a, int n_wt,
+                                      long long n_tasks, cudaStream_t s);
 }  // namespace mpm

@@ -74,13 +74,16 @@ class NVFP4MoE:
     """Buffers and launch sequence of the NVFP4 expert-layer forward for a
     fixed (T, H, I, E, k).  tile_m = 256 (default) runs the grouped GEMMs on
     CTA pairs and pads expert segments to 256 rows; 128 uses one CTA per
-    128-row tile and 128-row segments."""
+    128-row tile and 128-row segments; L.TILE_SMALL_M (1) runs the small-M
+    kernel (weights on the MMA's M side) for decode / rollout batches where
+    each expert receives few rows, with 128-row segments."""
 
     def __init__(self, T, H, I, E, k, device="cuda", tile_m=256):
         self.T, self.H, self.I, self.E, self.k = T, H, I, E, k
         self.tile_m = tile_m
+        self.pad = 128 if tile_m == L.TILE_SMALL_M else tile_m
         dev = torch.device(device)
-        cap = ops.moe_row_capacity(T, k, E, tile_m)
+        cap = ops.moe_row_capacity(T, k, E, self.pad)
         self.cap = cap
         u8, f32, bf = torch.uint8, torch.float32, torch.bfloat16
         e = lambda *s, dtype: torch.empty(*s, dtype=dtype, device=dev)
@@ -111,7 +114,7 @@ class NVFP4MoE:
         seg, perm, inv, rp = self.seg
         mark(1)
         ops.moe_build_segments(topk_ids, topk_prob, E, out=self.seg, ws=self.seg_ws,
-                               pad=self.tile_m)
+                               pad=self.pad)
         mark(2)
         ops.moe_gather_nvfp4(*self.xq, H, perm, seg, E, k, cap, out=self.aq, amax_zero=self.amax)
         aq, as_, ats = self.aq

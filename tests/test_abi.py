@@ -39,7 +39,9 @@ def test_pure_host_queries(lib):
     assert lib.mpm_scale_bytes(2048, 259) == 2048 * 260
     assert lib.mpm_moe_row_capacity(32768, 8, 256, 128) == 262144 + 128 * 256
     assert lib.mpm_moe_row_capacity(32768, 8, 256, 256) == 262144 + 256 * 256
-    assert lib.mpm_moe_row_capacity(32768, 8, 256, 64) == 0
+    assert lib.mpm_moe_row_capacity(32768, 8, 256, 64) == 262144 + 64 * 256
+    assert lib.mpm_moe_row_capacity(64, 8, 256, 16) == 512 + 16 * 256
+    assert lib.mpm_moe_row_capacity(32768, 8, 256, 96) == 0
     assert lib.mpm_status_string(7) == b"MPM_ERR_DEVICE_BOUNDS"
 
 

@@ -81,13 +81,13 @@ def _nvfp4_expert_reference(xn_rows, w1e, w2e, prob, I):
     return d, y
 
 
-def _run_nvfp4_full(shape, n_experts, x_rows_checked):
+def _run_nvfp4_full(shape, n_experts, x_rows_checked, tile_m=256):
     from microscaled_precision_moe_gb300.moe import NVFP4MoE, NVFP4Weights
     ids, prob = synth.routing(shape)
     x = synth.moe_activations(shape, device="cuda")
     w1, w2 = synth.moe_weights(shape, device="cuda")
     W = NVFP4Weights.quantize(w1, w2)
-    layer = NVFP4MoE(shape.T, shape.H, shape.I, shape.E, shape.k)    # bench launch configuration
+    layer = NVFP4MoE(shape.T, shape.H, shape.I, shape.E, shape.k, tile_m=tile_m)
     out = layer.forward(x, ids.cuda(), prob.cuda(), W)
     torch.cuda.synchronize()
     from microscaled_precision_moe_gb300 import ops
@@ -95,7 +95,7 @@ def _run_nvfp4_full(shape, n_experts, x_rows_checked):
     T, H, I, E, k = shape.T, shape.H, shape.I, shape.E, shape.k
     # segments, whole
     seg_g, perm_g, inv_g, rp_g = [t.cpu().numpy() for t in layer.seg]
-    seg, perm, inv, rp = MO.build_segments(ids.numpy(), prob.numpy(), E, layer.tile_m)
+    seg, perm, inv, rp = MO.build_segments(ids.numpy(), prob.numpy(), E, layer.pad)
     assert_bytes_equal(seg_g, seg, "seg_offsets")
     R = int(seg[-1])
     assert_bytes_equal(perm_g[:R], perm, "perm")
@@ -143,6 +143,16 @@ def test_nvfp4_layer_671b_full_size():
     """The headline workload: 32768 tokens, hidden 7168, 256 experts,
     intermediate 2048, top-8 with Zipf(1.1) expert load."""
     _run_nvfp4_full(synth.MOE_671B, n_experts=3, x_rows_checked=256)
+
+
+@pytest.mark.parametrize("T", [64, 256])
+def test_nvfp4_layer_671b_decode_small_m(T):
+    """Decode-sized batches of the 671B-shaped layer (64 and 256 tokens over
+    256 experts, Zipf load) on the small-M kernel, the bench's decode launch
+    configuration: full hidden / intermediate sizes, sampled experts."""
+    from microscaled_precision_moe_gb300 import _lib as L
+    _run_nvfp4_full(synth.scaled(synth.MOE_671B, T=T), n_experts=3, x_rows_checked=min(T, 64),
+                    tile_m=L.TILE_SMALL_M)
 
 
 def test_mxfp8_layer_30b_fwd_bwd_full_size():

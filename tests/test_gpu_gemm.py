@@ -33,12 +33,17 @@ def _L():
     return _lib
 
 
+def _pad(tile_m):
+    """Segment padding a GEMM tile mode needs (the small-M kernel: 128 rows)."""
+    return 128 if tile_m == 1 else tile_m
+
+
 def _assert_close(got, ref, what):
     ok, rf, mx, bound = Mx.within_gemm_tolerance(got, ref, REL, ELEM)
     assert ok, f"{what}: rel_frob={rf:.3e} max_err={mx:.3e} bound={bound:.3e}"
 
 
-@pytest.mark.parametrize("tile_m", [128, 256])
+@pytest.mark.parametrize("tile_m", [128, 256, 1])
 def test_nvfp4_single_expert_gate_up(tile_m):
     """128 x 2048 activations (0.1% x50 outliers) against jointly quantised
     768 x 2048 gate and up weights -> 128 x 1536 fp32 (one CTA per tile, or a
@@ -102,11 +107,11 @@ def _chained_compare(d_gpu, y_gpu, out_gpu, r, k, what):
     assert Mx.rel_frobenius(out_gpu, r["out"]) < 1e-2, f"{what}: layer output"
 
 
-@pytest.mark.parametrize("tile_m", [128, 256])
+@pytest.mark.parametrize("tile_m", [128, 256, 1])
 def test_nvfp4_grouped_fc1_swiglu_and_fc2(tile_m):
     shape = synth.scaled(synth.MOE_30B, T=300, H=512, I=256, E=6, k=4)
     ops, L = _ops(), _L()
-    ids, prob, x, w1, w2, seg, perm, inv, rp, cap = _grouped_nvfp4_setup(shape, pad=tile_m)
+    ids, prob, x, w1, w2, seg, perm, inv, rp, cap = _grouped_nvfp4_setup(shape, pad=_pad(tile_m))
     E, H, I, k = shape.E, shape.H, shape.I, shape.k
     qx, sx, tsx = ops.nvfp4_quantize_per_token(x)
     amax = torch.full((cap,), 7.0, dtype=torch.float32, device="cuda")    # gather zeroes it
@@ -128,20 +133,20 @@ def test_nvfp4_grouped_fc1_swiglu_and_fc2(tile_m):
     assert ops.get_device_status() == 0
     with np.errstate(over="ignore"):
         r = MO.nvfp4_moe_forward(np_bf16(x), ids.numpy(), prob.numpy(), np_bf16(w1),
-                                 np_bf16(w2), E, pad=tile_m)
+                                 np_bf16(w2), E, pad=_pad(tile_m))
     R = int(r["seg"][-1])
     amax_ref = np.max(np.abs(np_bf16(d)[:R]), axis=1)
     assert np.array_equal(amax.cpu().numpy()[:R], amax_ref), "amax(D) equals the row max of D"
     _chained_compare(np_bf16(d), np_bf16(y), np_bf16(out), r, k, "NVFP4 layer")
 
 
-@pytest.mark.parametrize("tile_m", [128, 256])
+@pytest.mark.parametrize("tile_m", [128, 256, 1])
 def test_nvfp4_fc2_on_identical_operands(tile_m):
     """FC2 alone: the same seeded bf16 D quantised by both sides (byte-exact),
     then the grouped GEMM against the fp64 GEMM: strict tolerance."""
     shape = synth.scaled(synth.MOE_30B, T=400, H=768, I=512, E=5, k=3)
     ops, L = _ops(), _L()
-    ids, prob, x, w1, w2, seg, perm, inv, rp, cap = _grouped_nvfp4_setup(shape, seed=2, pad=tile_m)
+    ids, prob, x, w1, w2, seg, perm, inv, rp, cap = _grouped_nvfp4_setup(shape, seed=2, pad=_pad(tile_m))
     E, H, I = shape.E, shape.H, shape.I
     dsrc = synth.normal_bf16(2, 77, (cap, I), "cuda", std=0.05, outlier_p=1e-3, outlier_mul=20.0)
     qd, sd, tsd = ops.nvfp4_quantize_per_token(dsrc)
@@ -163,7 +168,7 @@ def test_nvfp4_fc2_on_identical_operands(tile_m):
     _assert_close(np_bf16(y)[:R], ref, "NVFP4 FC2 (identical operands)")
 
 
-@pytest.mark.parametrize("tile_m", [128, 256])
+@pytest.mark.parametrize("tile_m", [128, 256, 1])
 def test_nvfp4_layer_api(tile_m):
     """The public layer API (NVFP4MoE) on a reduced 30B-A3B-shaped layer."""
     from microscaled_precision_moe_gb300.moe import NVFP4MoE, NVFP4Weights
@@ -179,7 +184,7 @@ def test_nvfp4_layer_api(tile_m):
     assert torch.equal(out, out2), "deterministic"
     with np.errstate(over="ignore"):
         r = MO.nvfp4_moe_forward(np_bf16(x), ids.numpy(), prob.numpy(), np_bf16(w1),
-                                 np_bf16(w2), shape.E, pad=tile_m)
+                                 np_bf16(w2), shape.E, pad=_pad(tile_m))
     _chained_compare(np_bf16(layer.d), np_bf16(layer.y), np_bf16(out), r, shape.k, "NVFP4MoE")
 
 
@@ -266,3 +271,42 @@ def test_mxfp8_layer_fwd_bwd_api(tile_m):
         report[name] = (rf, mx / max(bound / ELEM, 1e-30))
         assert ok, f"MXFP8 {name}: rel_frob={rf:.3e} max_err/max={mx / (bound / ELEM):.3e}"
     print("MXFP8 chained errors (rel_frob, max_err/max):", report)
+
+
+def test_mxfp8_fprop_small_m():
+    """MXFP8 fprop (bf16 and fp32 out) and the SwiGLU epilogue on the small-M
+    kernel: few rows per expert (decode-sized segments)."""
+    shape = synth.scaled(synth.MOE_30B_BWD, T=40, H=512, I=256, E=8, k=2)
+    ops, L = _ops(), _L()
+    ids, prob, x, w1, w2, seg, perm, inv, rp, cap = _grouped_nvfp4_setup(shape, pad=128)
+    E, H, I, k = shape.E, shape.H, shape.I, shape.k
+    xp = ops.moe_gather_bf16(x, perm, seg, E, k, cap)
+    mx = ops.mxfp8_quantize(xp, colwise=False, m_valid=seg[E:])
+    w = synth.normal_bf16(9, 97, (E * 2 * I, H), "cuda", std=0.02)
+    wq = ops.mxfp8_quantize(w, colwise=False)
+    segn = seg.cpu().numpy()
+    R = int(segn[-1])
+    a = MO.mx_rows(np_bf16(xp)[:R])
+    b = np.stack([MO.mx_rows(np_bf16(w).reshape(E, 2 * I, H)[e]) for e in range(E)])
+    ref = MO.grouped_gemm(a, b, segn)
+    for epi, dt in [(L.EPI_BF16, torch.bfloat16), (L.EPI_F32, torch.float32)]:
+        y = torch.empty(cap, 2 * I, dtype=dt, device="cuda")
+        ops.moe_grouped_gemm(L.KIND_MXFP8, L.GROUP_M, epi, E, cap, 2 * I, H, seg,
+                             mx["row_q"], wq["row_q"], mx["row_s"], H // 32, wq["row_s"], H // 32,
+                             y, b_rows_per_expert=2 * I, tile_m=1)
+        torch.cuda.synchronize()
+        assert ops.get_device_status() == 0
+        got = np_bf16(y)[:R] if dt == torch.bfloat16 else y[:R].cpu().numpy()
+        _assert_close(got, F.bf16_round(ref) if dt == torch.bfloat16 else ref,
+                      f"MXFP8 small-M fprop ({epi})")
+    d = torch.empty(cap, I, dtype=torch.bfloat16, device="cuda")
+    amax = torch.zeros(cap, dtype=torch.float32, device="cuda")
+    ops.moe_grouped_gemm(L.KIND_MXFP8, L.GROUP_M, L.EPI_SWIGLU, E, cap, 2 * I, H, seg,
+                         mx["row_q"], wq["row_q"], mx["row_s"], H // 32, wq["row_s"], H // 32,
+                         d, b_rows_per_expert=2 * I, row_prob=rp, out2=d, amax=amax, tile_m=1)
+    torch.cuda.synchronize()
+    assert ops.get_device_status() == 0
+    with np.errstate(over="ignore"):
+        dref = MO.fc1_epilogue(ref, rp.cpu().numpy()[:R], I)
+    _assert_close(np_bf16(d)[:R], dref, "MXFP8 small-M SwiGLU")
+    assert np.array_equal(amax.cpu().numpy()[:R], np.max(np.abs(np_bf16(d)[:R]), axis=1))
