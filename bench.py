@@ -364,21 +364,22 @@ def _nvfp4_bf16_bwd_line(peak_bf16, steps=10):
     return r
 
 
-def _nvfp4_decode_line(peak_hbm, steps=20):
+def _nvfp4_decode_line(peak_hbm, steps=20, experts=None, tokens=(64, 256)):
     """Decode / rollout-sized batches of the 671B-shaped layer (64 and 256
     tokens, Zipf load over 256 experts): the layer forward on the small-M
     kernel and, for comparison, on the CTA-pair kernel.  Bound: reading the
-    active experts' FP4 weights (codes + E4M3 scales) once from HBM."""
+    active experts' FP4 weights (codes + E4M3 scales) once from HBM.
+    experts: fewer experts (a small case for profiling)."""
     from microscaled_precision_moe_gb300 import synth, _lib as L
     from microscaled_precision_moe_gb300.moe import NVFP4MoE, NVFP4Weights
-    full = synth.MOE_671B
+    full = synth.MOE_671B if experts is None else synth.scaled(synth.MOE_671B, E=experts)
     w1, w2 = synth.moe_weights(full, device="cuda")
     W = NVFP4Weights.quantize(w1, w2)
     del w1, w2
     torch.cuda.empty_cache()
-    r = {"workload": "nvfp4_moe_fwd_decode_H7168_I2048_E256_k8_zipf1.1",
+    r = {"workload": f"nvfp4_moe_fwd_decode_H7168_I2048_E{full.E}_k8_zipf1.1",
          "note": "layer forward; roofline = active experts' FP4 weight bytes / time vs measured HBM"}
-    for T in (64, 256):
+    for T in tokens:
         s = synth.scaled(full, T=T)
         ids, prob = synth.routing(s)
         x = synth.moe_activations(s, device="cuda")
@@ -422,12 +423,14 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-also", action="store_true", help="skip the secondary lines")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle sample")
-    ap.add_argument("--case", choices=["headline", "slice", "mxfp8", "bf16bwd", "decode"],
+    ap.add_argument("--case", choices=["headline", "slice", "mxfp8", "bf16bwd", "decode",
+                                       "decode_slice"],
                     default="headline",
                     help="slice: 4096 tokens over 64 experts of the 671B shape (profiling); "
                          "mxfp8: the MXFP8 30B-shaped forward+backward step alone (profiling); "
                          "bf16bwd: the BF16 backward of the NVFP4 30B-shaped layer alone; "
-                         "decode: 64 / 256-token batches of the 671B-shaped layer")
+                         "decode: 64 / 256-token batches of the 671B-shaped layer; "
+                         "decode_slice: 64 tokens over 32 experts of that shape (profiling)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -485,8 +488,9 @@ def main():
                               "dtype": "mxfp8", "config": {"workload": r["workload"]},
                               "note": r["note"]}), flush=True)
         return 0
-    if args.case == "decode":
-        r = _nvfp4_decode_line(peaks["hbm"], steps=args.steps)
+    if args.case in ("decode", "decode_slice"):
+        r = (_nvfp4_decode_line(peaks["hbm"], steps=args.steps) if args.case == "decode" else
+             _nvfp4_decode_line(peaks["hbm"], steps=args.steps, experts=32, tokens=(64,)))
         if rank == 0:
             print(json.dumps({"metric": METRIC, "value": r["T64_small_m"]["ms"], "unit": "ms",
                               "n_gpus": world, "steps": args.steps, "warmup": 3,
