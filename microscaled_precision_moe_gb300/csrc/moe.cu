@@ -3,8 +3,9 @@
 // "miniTE technical report", section 5.2: the routed rows of all experts sit
 // in one contiguous buffer whose expert boundaries are offsets kept on the
 // device; zero-token experts and the padding of each segment (to 128 rows, one
-// MMA tile, or 256, one CTA-pair tile) are handled in the same path.  Section 5.3: the permute gathers
-// each routed (token, slot) row; the combine sums a token's expert outputs.
+// MMA tile, 256, one CTA-pair tile, or 16-64 rows for the small-M kernel) are
+// handled in the same path.  Section 5.3: the permute gathers each routed
+// (token, slot) row; the combine sums a token's expert outputs.
 //
 // The counting sort is stable: rows of one expert appear in ascending flat
 // index t*k + j.  Every step is integer work, so results are bit-identical
@@ -33,25 +34,48 @@ __global__ void __launch_bounds__(256) seg_hist_kernel(const int* ids, long long
   for (int e = threadIdx.x; e < E; e += blockDim.x) hist[(long long)blockIdx.x * E + e] = h[e];
 }
 
-// 2) one CTA: per-expert totals, padded segment offsets (exclusive scan), and
-//    each chunk's first row per expert: base[chunk][e]
-__global__ void __launch_bounds__(1024) seg_scan_kernel(const int* __restrict__ hist, int nchunks,
-                                                       int E, int pad, int* __restrict__ base,
-                                                       int* __restrict__ seg_offsets) {
-  __shared__ int padded[1024];
-  __shared__ int total_sh[1024];
-  const int e = threadIdx.x;
-  int tot = 0;
-  if (e < E) {
-#pragma unroll 8
-    for (int c = 0; c < nchunks; ++c) {
-      const int v = hist[(long long)c * E + e];
-      base[(long long)c * E + e] = tot;        // exclusive within the expert
-      tot += v;
-    }
+// 2a) one CTA per expert: exclusive prefix of the expert's column of the
+//     histogram over the chunks (each thread sums a run of chunks, then a
+//     block scan of the thread sums): base[chunk][e] relative to the
+//     segment start, and the expert's total
+__global__ void __launch_bounds__(256) seg_colscan_kernel(const int* __restrict__ hist, int nchunks,
+                                                         int E, int* __restrict__ base,
+                                                         int* __restrict__ totals) {
+  __shared__ int warp_sum[8];
+  const int e = blockIdx.x;
+  const int per = (nchunks + 255) / 256;
+  const int c0 = threadIdx.x * per;
+  const int c1 = min(c0 + per, nchunks);
+  int local = 0;
+  for (int c = c0; c < c1; ++c) local += hist[(long long)c * E + e];
+  // block exclusive scan of the 256 thread sums
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  int incl = local;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += v;
   }
-  total_sh[e] = tot;
-  padded[e] = (e < E) ? (tot + pad - 1) / pad * pad : 0;
+  if (lane == 31) warp_sum[w] = incl;
+  __syncthreads();
+  int woff = 0;
+  for (int i = 0; i < w; ++i) woff += warp_sum[i];
+  int run = woff + incl - local;                 // exclusive prefix of this thread's run
+  for (int c = c0; c < c1; ++c) {
+    const int v = hist[(long long)c * E + e];
+    base[(long long)c * E + e] = run;
+    run += v;
+  }
+  if (threadIdx.x == 255) totals[e] = woff + incl;
+}
+
+// 2b) one CTA: padded segment offsets from the expert totals (exclusive scan)
+__global__ void __launch_bounds__(1024) seg_offsets_kernel(const int* __restrict__ totals, int E,
+                                                          int pad, int* __restrict__ seg_offsets) {
+  __shared__ int padded[1024];
+  const int e = threadIdx.x;
+  const int mine = (e < E) ? (totals[e] + pad - 1) / pad * pad : 0;
+  padded[e] = mine;
   __syncthreads();
   // Hillis-Steele inclusive scan over padded sizes
   for (int o = 1; o < 1024; o <<= 1) {
@@ -60,23 +84,18 @@ __global__ void __launch_bounds__(1024) seg_scan_kernel(const int* __restrict__ 
     padded[e] += v;
     __syncthreads();
   }
-  const int excl = padded[e] - ((e < E) ? (total_sh[e] + pad - 1) / pad * pad : 0);
-  if (e < E) {
-    seg_offsets[e] = excl;
-#pragma unroll 8
-    for (int c = 0; c < nchunks; ++c) base[(long long)c * E + e] += excl;
-  }
+  if (e < E) seg_offsets[e] = padded[e] - mine;
   if (e == E - 1) seg_offsets[E] = padded[e];
 }
 
 // 3) stable scatter: one warp walks its chunk in order, 32 pairs at a time
 __global__ void __launch_bounds__(32) seg_scatter_kernel(const int* ids, const float* prob,
                                                         long long n, int E, const int* base,
-                                                        int* perm, int* inv_perm,
-                                                        float* row_prob) {
+                                                        const int* seg_offsets, int* perm,
+                                                        int* inv_perm, float* row_prob) {
   extern __shared__ int cnt[];
   const int lane = threadIdx.x;
-  for (int e = lane; e < E; e += 32) cnt[e] = base[(long long)blockIdx.x * E + e];
+  for (int e = lane; e < E; e += 32) cnt[e] = base[(long long)blockIdx.x * E + e] + seg_offsets[e];
   __syncwarp();
   const long long c0 = (long long)blockIdx.x * kSegChunk;
   for (int s = 0; s < kSegChunk; s += 32) {
@@ -128,37 +147,59 @@ __global__ void __launch_bounds__(256) gather_bf16_kernel(const uint4* src, long
 }
 
 // NVFP4 rows: codes (K/2 bytes), 128x4-tiled scales (K/16 columns) and the
-// token scale move together
+// token scale move together.  One CTA per 128 destination rows (one row of
+// scale tiles): each warp copies 16 rows of codes; each 512-byte scale tile of
+// the destination is assembled by 128 threads, one 4-byte word (a row's four
+// scales of the tile) each, and written as one contiguous 512-byte run.
 __global__ void __launch_bounds__(256) gather_nvfp4_kernel(const uint4* src_q, const uint8_t* src_s,
                                                           const float* src_ts, long long K,
                                                           int k, const int* perm,
                                                           const int* seg_end, long long cap,
                                                           uint4* dst_q, uint8_t* dst_s,
                                                           float* dst_ts, float* amax_zero) {
-  const long long row = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
+  __shared__ long long tok[128];                  // source token of each row, -1 for padding
+  const long long rbase = (long long)blockIdx.x * 128;
   long long rend = *seg_end;
   if (rend > cap) rend = cap;
-  if (row >= rend) return;
-  if (amax_zero && lane == 0) amax_zero[row] = 0.0f;
-  const int f = perm[row];
-  const long long q16 = K / 32;          // uint4 chunks of packed codes per row
-  const long long cols = K / 16, cpad = cols;   // K % 64 == 0
-  uint4* dq = dst_q + row * q16;
-  if (f < 0) {
-    for (long long i = lane; i < q16; i += 32) dq[i] = make_uint4(0, 0, 0, 0);
-    for (long long g = lane; g < cols / 4; g += 32)
-      *reinterpret_cast<uint32_t*>(dst_s + sf_offset(row, g * 4, cpad)) = 0u;
-    if (lane == 0) dst_ts[row] = 0.0f;
-    return;
+  if (rbase >= rend) return;
+  const int nrows = (int)min(128LL, rend - rbase);
+  if (threadIdx.x < 128) {
+    const int i = threadIdx.x;
+    long long t = -1;
+    if (i < nrows) {
+      const int f = perm[rbase + i];
+      if (f >= 0) t = f / k;
+      if (amax_zero) amax_zero[rbase + i] = 0.0f;
+      dst_ts[rbase + i] = t >= 0 ? src_ts[t] : 0.0f;
+    }
+    tok[i] = t;
   }
-  const long long t = f / k;
-  const uint4* sq = src_q + t * q16;
-  for (long long i = lane; i < q16; i += 32) dq[i] = __ldg(sq + i);
-  for (long long g = lane; g < cols / 4; g += 32)
-    *reinterpret_cast<uint32_t*>(dst_s + sf_offset(row, g * 4, cpad)) =
-        *reinterpret_cast<const uint32_t*>(src_s + sf_offset(t, g * 4, cpad));
-  if (lane == 0) dst_ts[row] = src_ts[t];
+  __syncthreads();
+  const long long q16 = K / 32;                  // uint4 chunks of packed codes per row
+  const long long cpad = K / 16;                 // scale columns (K % 64 == 0: no padding)
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int i = warp; i < nrows; i += 8) {
+    uint4* d = dst_q + (rbase + i) * q16;
+    const long long t = tok[i];
+    if (t < 0) {
+      for (long long c = lane; c < q16; c += 32) d[c] = make_uint4(0, 0, 0, 0);
+    } else {
+      const uint4* sq = src_q + t * q16;
+      for (long long c = lane; c < q16; c += 32) d[c] = __ldg(sq + c);
+    }
+  }
+  // scale tiles: word w of a tile holds row (w % 4) * 32 + w / 4
+  const long long ntiles = cpad / 4;
+  const long long rt = rbase >> 7;
+  const int w = threadIdx.x & 127;
+  const int r = (w & 3) * 32 + (w >> 2);
+  const long long t = tok[r];
+  for (long long g = threadIdx.x >> 7; g < ntiles; g += 2) {
+    if (r >= nrows) continue;
+    uint32_t v = 0;
+    if (t >= 0) v = *reinterpret_cast<const uint32_t*>(src_s + sf_offset(t, g * 4, cpad));
+    reinterpret_cast<uint32_t*>(dst_s + (rt * ntiles + g) * 512)[w] = v;
+  }
 }
 
 // ---------------------------------------------------------------- combine
@@ -195,7 +236,7 @@ __global__ void __launch_bounds__(128) combine_kernel(const uint4* y, const int*
 size_t segments_ws_bytes(long long T, int k, long long E) {
   const long long n = T * k;
   const long long nchunks = (n + kSegChunk - 1) / kSegChunk;
-  return (size_t)(2 * nchunks * E) * sizeof(int);
+  return (size_t)(2 * nchunks * E + E) * sizeof(int);
 }
 
 cudaError_t launch_build_segments(const int* ids, const float* prob, long long T, int k,
@@ -211,10 +252,14 @@ cudaError_t launch_build_segments(const int* ids, const float* prob, long long T
   if ((err = cudaMemsetAsync(row_prob, 0, (size_t)cap * sizeof(float), s)) != cudaSuccess) return err;
   seg_hist_kernel<<<nchunks, 128, (size_t)E * sizeof(int), s>>>(ids, n, (int)E, hist, st);
   if ((err = cudaGetLastError()) != cudaSuccess) return err;
-  seg_scan_kernel<<<1, 1024, 0, s>>>(hist, nchunks, (int)E, pad, base, seg_offsets);
+  int* totals = base + (long long)nchunks * E;
+  seg_colscan_kernel<<<(unsigned)E, 256, 0, s>>>(hist, nchunks, (int)E, base, totals);
+  if ((err = cudaGetLastError()) != cudaSuccess) return err;
+  seg_offsets_kernel<<<1, 1024, 0, s>>>(totals, (int)E, pad, seg_offsets);
   if ((err = cudaGetLastError()) != cudaSuccess) return err;
   seg_scatter_kernel<<<nchunks, 32, (size_t)E * sizeof(int), s>>>(ids, prob, n, (int)E, base,
-                                                                  perm, inv_perm, row_prob);
+                                                                  seg_offsets, perm, inv_perm,
+                                                                  row_prob);
   return cudaGetLastError();
 }
 
@@ -227,7 +272,8 @@ cudaError_t launch_gather(int what, const void* src, const uint8_t* src_s, const
     gather_bf16_kernel<<<grid, 256, 0, s>>>(static_cast<const uint4*>(src), K / 8, k, perm,
                                             seg_end, cap, static_cast<uint4*>(dst), amax_zero);
   } else {
-    gather_nvfp4_kernel<<<grid, 256, 0, s>>>(static_cast<const uint4*>(src), src_s, src_ts, K,
+    gather_nvfp4_kernel<<<(unsigned)((cap + 127) / 128), 256, 0, s>>>(
+        static_cast<const uint4*>(src), src_s, src_ts, K,
                                              k, perm, seg_end, cap, static_cast<uint4*>(dst),
                                              dst_s, dst_ts, amax_zero);
   }

@@ -139,9 +139,10 @@ class NVFP4MoE:
         mark(7)
         return self.out
 
-    # kernels launched by one forward: quantiser, 3 segment kernels, gather,
-    # FC1, quantiser, FC2, combine
-    LAUNCHES_PER_FORWARD = 9
+    # kernels launched by one forward: quantiser, 4 segment kernels
+    # (histogram, per-expert column scan, offsets, scatter), gather, FC1,
+    # quantiser, FC2, combine
+    LAUNCHES_PER_FORWARD = 10
 
     # ------------------------------------------------------------ BF16 backward
     BACKWARD_MODES = ("high_precision", "dequantized")
