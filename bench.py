@@ -248,11 +248,43 @@ def _quantizer_lines(peak_hbm):
         j = it[0] % 8
         ops.mxfp8_quantize(xs[j], out=outs[j])
         it[0] += 1
-    ms = _time_loop(f, 80)
+    ms_host = _time_loop(f, 80)
+    # device time per launch: the eight launches captured once in a CUDA
+    # graph and replayed, so the host's per-call cost does not pace the GPU
+    torch.cuda.synchronize()
+    side = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(side):
+        for j in range(8):
+            ops.mxfp8_quantize(xs[j], out=outs[j])
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g, stream=side):
+            for j in range(8):
+                ops.mxfp8_quantize(xs[j], out=outs[j])
+    torch.cuda.synchronize()
+    ms = _time_loop(g.replay, 10) / 8
     gbs = byts / (ms * 1e-3) / 1e9
     out["mxfp8_quantize_8288x2048_rowcol"] = {"GB/s": round(gbs, 1), "us": round(ms * 1e3, 2),
-                                              "bytes": byts, "frac_hbm": round(gbs / peak_hbm, 3)}
+                                              "bytes": byts, "frac_hbm": round(gbs / peak_hbm, 3),
+                                              "us_per_call_from_python": round(ms_host * 1e3, 2),
+                                              "timing": "CUDA graph of 8 launches over 8 rotating "
+                                                        "inputs (272 MB > L2), replayed"}
+    del g
     del xs, outs
+    # the same quantiser on a large input (65536 x 2048, 256 MB, the size of
+    # an MXFP8 layer's permuted activations): streaming efficiency without the
+    # fixed per-launch latency of the small case
+    xl = synth.normal_bf16(0, synth.TID_X, (65536, 2048), "cuda")
+    ol = ops.mxfp8_quantize(xl)
+    for _ in range(3):
+        ops.mxfp8_quantize(xl, out=ol)
+    msl = _time_loop(lambda: ops.mxfp8_quantize(xl, out=ol), 20)
+    Ml, Kl = xl.shape
+    bl = Ml * Kl * 4 + ops.scale_bytes(Ml, Kl // 32) + ops.scale_bytes(Kl, (Ml + 31) // 32)
+    gl = bl / (msl * 1e-3) / 1e9
+    out["mxfp8_quantize_65536x2048_rowcol"] = {"GB/s": round(gl, 1), "us": round(msl * 1e3, 2),
+                                               "bytes": bl, "frac_hbm": round(gl / peak_hbm, 3)}
+    del xl, ol
     # NVFP4 per-token activation quantiser, 32768 x 7168 (470 MB > L2)
     x = synth.normal_bf16(0, synth.TID_X, (32768, 7168), "cuda")
     o = ops.nvfp4_quantize_per_token(x)
@@ -424,13 +456,14 @@ def main():
     ap.add_argument("--no-also", action="store_true", help="skip the secondary lines")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle sample")
     ap.add_argument("--case", choices=["headline", "slice", "mxfp8", "bf16bwd", "decode",
-                                       "decode_slice"],
+                                       "decode_slice", "quant"],
                     default="headline",
                     help="slice: 4096 tokens over 64 experts of the 671B shape (profiling); "
                          "mxfp8: the MXFP8 30B-shaped forward+backward step alone (profiling); "
                          "bf16bwd: the BF16 backward of the NVFP4 30B-shaped layer alone; "
                          "decode: 64 / 256-token batches of the 671B-shaped layer; "
-                         "decode_slice: 64 tokens over 32 experts of that shape (profiling)")
+                         "decode_slice: 64 tokens over 32 experts of that shape (profiling); "
+                         "quant: the quantiser lines alone")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -487,6 +520,14 @@ def main():
                               "ms_per_step": r["ms_per_step"], "higher_is_better": True,
                               "dtype": "mxfp8", "config": {"workload": r["workload"]},
                               "note": r["note"]}), flush=True)
+        return 0
+    if args.case == "quant":
+        r = _quantizer_lines(peaks["hbm"])
+        if rank == 0:
+            print(json.dumps({"metric": METRIC, "value": r["mxfp8_quantize_8288x2048_rowcol"]["GB/s"],
+                              "unit": "GB/s", "n_gpus": world, "higher_is_better": True,
+                              "dtype": "mxfp8", "config": {"workload": "mxfp8_quantize_8288x2048_rowcol"},
+                              "quantizers": r}), flush=True)
         return 0
     if args.case in ("decode", "decode_slice"):
         r = (_nvfp4_decode_line(peaks["hbm"], steps=args.steps) if args.case == "decode" else

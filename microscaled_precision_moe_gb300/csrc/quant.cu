@@ -220,12 +220,30 @@ struct Mxfp8Args {
   uint8_t* row_q; uint8_t* row_s; long long row_s_cols_pad;
   uint8_t* col_q; long long ldc; uint8_t* col_s; long long col_s_cols_pad;
   const int* m_valid;
+  int pad_blocks;           // 1: the last row of blocks zeroes the scale padding
 };
 
-constexpr int MX_TM = 128, MX_TK = 64;
+constexpr int MX_TM = 128, MX_TK = 128;
 
+MPM_DEV void zero_scale_padding(uint8_t* s, long long rows, long long cols, long long tid,
+                                long long nthreads);
+
+// One CTA per 128 x 128 tile of x, read once: each thread encodes two 1x32
+// row blocks (row copy) straight from its loads and parks the values in
+// shared memory; then each thread encodes two 32x1 column blocks from there
+// (column copy, stored transposed).
 __global__ void __launch_bounds__(256) mxfp8_quant_kernel(const Mxfp8Args p) {
-  __shared__ __align__(16) uint16_t tile[MX_TM][MX_TK];
+  // +8 elements per row: consecutive rows start 4 banks apart
+  __shared__ __align__(16) uint16_t tile[MX_TM][MX_TK + 8];
+  if (p.pad_blocks && blockIdx.y == gridDim.y - 1) {
+    // the last row of blocks zeroes the padding entries of the scale tiles
+    // (host-sized buffers only; device-sized ones never read their padding)
+    const long long tid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    const long long nth = (long long)gridDim.x * blockDim.x;
+    if (p.flags & MPM_ROWWISE) zero_scale_padding(p.row_s, p.M, p.K / 32, tid, nth);
+    if (p.flags & MPM_COLWISE) zero_scale_padding(p.col_s, p.K, (p.M + 31) / 32, tid, nth);
+    return;
+  }
   const long long m0 = (long long)blockIdx.y * MX_TM;
   const long long k0 = (long long)blockIdx.x * MX_TK;
   long long M_eff = p.M;
@@ -233,94 +251,104 @@ __global__ void __launch_bounds__(256) mxfp8_quant_kernel(const Mxfp8Args p) {
   if (m0 >= M_eff) return;
   const int t = threadIdx.x;
 
-  // ---- load: thread t owns row t/2, columns (t%2)*32 .. +32 (one row block)
+  // ---- load: thread t owns row t/2, columns (t%2)*64 .. +64 (two row blocks)
   {
     const int r = t >> 1, half = t & 1;
     const long long row = m0 + r;
-    const long long col = k0 + half * 32;
-    uint32_t w[16];
-    const bool in = (row < M_eff) && (col < p.K);
-    if (in) {
-      const uint4* src = reinterpret_cast<const uint4*>(p.x + row * p.ldx + col);
+    uint32_t w[2][16];
+    bool in[2];
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        uint4 u = __ldcs(src + j);
-        w[4 * j] = u.x; w[4 * j + 1] = u.y; w[4 * j + 2] = u.z; w[4 * j + 3] = u.w;
+    for (int b = 0; b < 2; ++b) {
+      const long long col = k0 + half * 64 + b * 32;
+      in[b] = (row < M_eff) && (col < p.K);
+      if (in[b]) {
+        const uint4* src = reinterpret_cast<const uint4*>(p.x + row * p.ldx + col);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          uint4 u = __ldcs(src + j);
+          w[b][4 * j] = u.x; w[b][4 * j + 1] = u.y; w[b][4 * j + 2] = u.z; w[b][4 * j + 3] = u.w;
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < 16; ++j) w[b][j] = 0;
       }
-    } else {
-#pragma unroll
-      for (int j = 0; j < 16; ++j) w[j] = 0;
     }
-    if (p.flags & MPM_ROWWISE) {
-      if (in) {
+#pragma unroll
+    for (int b = 0; b < 2; ++b) {
+      const long long col = k0 + half * 64 + b * 32;
+      if ((p.flags & MPM_ROWWISE) && in[b]) {
         uint32_t m = 0;
 #pragma unroll
-        for (int j = 0; j < 16; ++j) m = absmax_bf16x2(m, w[j]);
+        for (int j = 0; j < 16; ++j) m = absmax_bf16x2(m, w[b][j]);
         m = max(m & 0xFFFFu, m >> 16);
         const int e = mx_exponent(m << 16);
         uint32_t o[8];
-        mx_encode32(w, pow2_neg(e), o);
+        mx_encode32(w[b], pow2_neg(e), o);
         uint4* dst = reinterpret_cast<uint4*>(p.row_q + row * p.K + col);
         dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
         dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
         p.row_s[sf_offset(row, col >> 5, p.row_s_cols_pad)] = (uint8_t)(e + 127);
       }
-    }
-    if (p.flags & MPM_COLWISE) {
-      uint4* st = reinterpret_cast<uint4*>(&tile[r][half * 32]);
+      if (p.flags & MPM_COLWISE) {
+        uint4* st = reinterpret_cast<uint4*>(&tile[r][half * 64 + b * 32]);
 #pragma unroll
-      for (int j = 0; j < 4; ++j)
-        st[j] = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+        for (int j = 0; j < 4; ++j)
+          st[j] = make_uint4(w[b][4 * j], w[b][4 * j + 1], w[b][4 * j + 2], w[b][4 * j + 3]);
+      }
     }
   }
   if (!(p.flags & MPM_COLWISE)) return;
   __syncthreads();
 
-  // ---- column blocks: thread t owns column t%64, rows (t/64)*32 .. +32
+  // ---- column blocks: thread t owns column t%128, row groups (t/128)*2 + {0, 1}
   {
-    const int c = t & 63, g = t >> 6;
+    const int c = t & 127;
     const long long col = k0 + c;
-    const long long mb = m0 + g * 32;
-    if (col >= p.K || mb >= M_eff) return;
-    uint32_t w[16];
+    if (col >= p.K) return;
 #pragma unroll
-    for (int j = 0; j < 16; ++j)
-      w[j] = (uint32_t)tile[g * 32 + 2 * j][c] | ((uint32_t)tile[g * 32 + 2 * j + 1][c] << 16);
-    uint32_t m = 0;
+    for (int gg = 0; gg < 2; ++gg) {
+      const int g = (t >> 7) * 2 + gg;
+      const long long mb = m0 + g * 32;
+      if (mb >= M_eff) break;
+      uint32_t w[16];
 #pragma unroll
-    for (int j = 0; j < 16; ++j) m = absmax_bf16x2(m, w[j]);
-    m = max(m & 0xFFFFu, m >> 16);
-    const int e = mx_exponent(m << 16);
-    uint32_t o[8];
-    mx_encode32(w, pow2_neg(e), o);
-    uint8_t* dst = p.col_q + col * p.ldc + mb;
-    const long long nvalid = M_eff - mb;
-    if (nvalid >= 32) {
-      uint4* d4 = reinterpret_cast<uint4*>(dst);
-      d4[0] = make_uint4(o[0], o[1], o[2], o[3]);
-      d4[1] = make_uint4(o[4], o[5], o[6], o[7]);
-    } else {
-      for (int j = 0; j < nvalid; ++j) dst[j] = (uint8_t)(o[j >> 2] >> (8 * (j & 3)));
+      for (int j = 0; j < 16; ++j)
+        w[j] = (uint32_t)tile[g * 32 + 2 * j][c] | ((uint32_t)tile[g * 32 + 2 * j + 1][c] << 16);
+      uint32_t m = 0;
+#pragma unroll
+      for (int j = 0; j < 16; ++j) m = absmax_bf16x2(m, w[j]);
+      m = max(m & 0xFFFFu, m >> 16);
+      const int e = mx_exponent(m << 16);
+      uint32_t o[8];
+      mx_encode32(w, pow2_neg(e), o);
+      uint8_t* dst = p.col_q + col * p.ldc + mb;
+      const long long nvalid = M_eff - mb;
+      if (nvalid >= 32) {
+        uint4* d4 = reinterpret_cast<uint4*>(dst);
+        d4[0] = make_uint4(o[0], o[1], o[2], o[3]);
+        d4[1] = make_uint4(o[4], o[5], o[6], o[7]);
+      } else {
+        for (int j = 0; j < nvalid; ++j) dst[j] = (uint8_t)(o[j >> 2] >> (8 * (j & 3)));
+      }
+      p.col_s[sf_offset(col, mb >> 5, p.col_s_cols_pad)] = (uint8_t)(e + 127);
     }
-    p.col_s[sf_offset(col, mb >> 5, p.col_s_cols_pad)] = (uint8_t)(e + 127);
   }
 }
 
-// Zero the padding entries of a 128x4-tiled scale matrix: columns [cols,
-// cols_pad) of rows [0, rows), and all columns of rows [rows, rows_pad).
-__global__ void zero_scale_padding_kernel(uint8_t* s, long long rows, long long cols) {
+MPM_DEV void zero_scale_padding(uint8_t* s, long long rows, long long cols, long long tid,
+                                long long nthreads) {
   const long long rows_pad = (rows + 127) / 128 * 128, cols_pad = (cols + 3) / 4 * 4;
   const long long ncp = cols_pad - cols;
   const long long nA = rows * ncp;
   const long long nB = (rows_pad - rows) * cols_pad;
-  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < nA + nB;
-       i += (long long)gridDim.x * blockDim.x) {
+  for (long long i = tid; i < nA + nB; i += nthreads) {
     long long r, c;
     if (i < nA) { r = i / ncp; c = cols + i % ncp; }
     else { long long j = i - nA; r = rows + j / cols_pad; c = j % cols_pad; }
     s[sf_offset(r, c, cols_pad)] = 0;
   }
 }
+
 
 // ============================================================================
 // launchers
@@ -417,28 +445,13 @@ cudaError_t launch_mxfp8(const void* x, long long M, long long K, long long ldx,
   p.col_q = col_q; p.ldc = ldc; p.col_s = col_s;
   p.col_s_cols_pad = ((M + 31) / 32 + 3) / 4 * 4;
   p.m_valid = m_valid;
-  const dim3 grid((unsigned)((K + MX_TK - 1) / MX_TK), (unsigned)((M + MX_TM - 1) / MX_TM));
+  // with host-sized buffers one extra row of blocks zeroes the scale padding
+  // (device-sized buffers never read it)
+  p.pad_blocks = m_valid ? 0 : 1;
+  const dim3 grid((unsigned)((K + MX_TK - 1) / MX_TK),
+                  (unsigned)((M + MX_TM - 1) / MX_TM + p.pad_blocks));
   mxfp8_quant_kernel<<<grid, 256, 0, st>>>(p);
-  cudaError_t err = cudaGetLastError();
-  if (err != cudaSuccess) return err;
-  if (m_valid) return cudaSuccess;      // device-sized buffers: padding never read
-  const int zb = 256;
-  if (flags & MPM_ROWWISE) {
-    long long n = ((M + 127) / 128 * 128) * ((K / 32 + 3) / 4 * 4) - M * (K / 32);
-    if (n > 0) {
-      zero_scale_padding_kernel<<<(unsigned)((n + zb - 1) / zb > 1024 ? 1024 : (n + zb - 1) / zb), zb, 0, st>>>(row_s, M, K / 32);
-      if ((err = cudaGetLastError()) != cudaSuccess) return err;
-    }
-  }
-  if (flags & MPM_COLWISE) {
-    const long long cc = (M + 31) / 32;
-    long long n = ((K + 127) / 128 * 128) * ((cc + 3) / 4 * 4) - K * cc;
-    if (n > 0) {
-      zero_scale_padding_kernel<<<(unsigned)((n + zb - 1) / zb > 1024 ? 1024 : (n + zb - 1) / zb), zb, 0, st>>>(col_s, K, cc);
-      if ((err = cudaGetLastError()) != cudaSuccess) return err;
-    }
-  }
-  return cudaSuccess;
+  return cudaGetLastError();
 }
 
 }  // namespace mpm
