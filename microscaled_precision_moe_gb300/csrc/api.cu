@@ -92,6 +92,23 @@ bool make_sf_tmap(CUtensorMap* m, const void* base, long long atoms, int atoms_p
   return r == CUDA_SUCCESS;
 }
 
+// [rows, cols] bf16 input with row pitch `ld` elements, box_cols x box_rows
+// boxes without swizzle (rows land 2 * box_cols bytes apart in shared memory);
+// out-of-range elements read as zero
+bool make_bf16_tmap(CUtensorMap* m, const void* base, long long cols, long long rows, long long ld,
+                    unsigned box_cols, unsigned box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)(ld * 2)};
+  cuuint32_t box[2] = {box_cols, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 // [rows, cols] bf16 or fp32 output with row pitch `ld` elements: 128-row boxes
 // of 128 bytes per row (64 bf16 or 32 fp32 columns), 128-byte swizzle (the
 // staging layout of the TMA-store epilogues)
@@ -153,8 +170,10 @@ mpm_status mpm_mxfp8_quantize(const void* x, int64_t M, int64_t K, int64_t ldx, 
     if (ldc < M) return MPM_ERR_SHAPE;
     if (!aligned(col_q, 16) || ldc % 16 != 0) return MPM_ERR_ALIGN;
   }
-  return cuda_status(mpm::launch_mxfp8(x, M, K, ldx, flags, row_q, row_s, col_q, ldc, col_s,
-                                       m_valid, stream));
+  CUtensorMap tx;
+  if (!make_bf16_tmap(&tx, x, K, M, ldx, 64, 128)) return MPM_ERR_CUDA;
+  return cuda_status(mpm::launch_mxfp8_tma(tx, M, K, ldx, flags, row_q, row_s, col_q, ldc, col_s,
+                                           m_valid, status_ptr(), stream));
 }
 
 mpm_status mpm_nvfp4_quantize_per_token(const void* x, int64_t M, int64_t K, int64_t ldx,

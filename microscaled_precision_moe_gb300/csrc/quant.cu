@@ -220,118 +220,143 @@ struct Mxfp8Args {
   uint8_t* row_q; uint8_t* row_s; long long row_s_cols_pad;
   uint8_t* col_q; long long ldc; uint8_t* col_s; long long col_s_cols_pad;
   const int* m_valid;
-  int pad_blocks;           // 1: the last row of blocks zeroes the scale padding
+  int pad_blocks;           // 1: zero the scale padding (host-sized buffers)
+  int* status;
 };
-
-constexpr int MX_TM = 128, MX_TK = 128;
 
 MPM_DEV void zero_scale_padding(uint8_t* s, long long rows, long long cols, long long tid,
                                 long long nthreads);
 
-// One CTA per 128 x 128 tile of x, read once: each thread encodes two 1x32
-// row blocks (row copy) straight from its loads and parks the values in
-// shared memory; then each thread encodes two 32x1 column blocks from there
-// (column copy, stored transposed).
-__global__ void __launch_bounds__(256) mxfp8_quant_kernel(const Mxfp8Args p) {
-  // +8 elements per row: consecutive rows start 4 banks apart
-  __shared__ __align__(16) uint16_t tile[MX_TM][MX_TK + 8];
-  if (p.pad_blocks && blockIdx.y == gridDim.y - 1) {
-    // the last row of blocks zeroes the padding entries of the scale tiles
-    // (host-sized buffers only; device-sized ones never read their padding)
-    const long long tid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+// max |x| over bf16 pairs with packed bf16 abs / max (finite inputs), as the
+// 16-bit pattern of the larger magnitude in the low half
+template <int N>
+MPM_DEV uint32_t absmax_bf16x2_packed(const uint32_t (&w)[N]) {
+  __nv_bfloat162 acc = __habs2(*reinterpret_cast<const __nv_bfloat162*>(&w[0]));
+#pragma unroll
+  for (int j = 1; j < N; ++j) acc = __hmax2(acc, __habs2(*reinterpret_cast<const __nv_bfloat162*>(&w[j])));
+  const uint32_t m = *reinterpret_cast<uint32_t*>(&acc);
+  return max(m & 0xFFFFu, m >> 16);
+}
+
+// ---------------------------------------------------------------- MXFP8, TMA-staged
+// Persistent CTAs walk 128 x 64 tiles of x; a 3-deep ring of TMA loads keeps
+// the next tiles in flight while a tile is encoded from shared memory.
+// Row pass: four lanes per 32-element row block (16 bytes each), so a warp
+// reads 512 contiguous bytes per step; the block amax is reduced across the
+// four lanes.  Column pass: one 32-row column block per thread.
+constexpr int MQ_TM = 128, MQ_TK = 64, MQ_STAGES = 3;
+constexpr int MQ_TILE_BYTES = MQ_TM * MQ_TK * 2;     // 16 KB
+
+__global__ void __launch_bounds__(256) mxfp8_quant_tma_kernel(const __grid_constant__ CUtensorMap tx,
+                                                             const Mxfp8Args p, int n_kt) {
+  extern __shared__ uint8_t mq_smem[];
+  const uint32_t raw = smem_u32(mq_smem);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  const uint8_t* gbase = mq_smem + (base - raw);
+  const uint32_t bar = base + MQ_STAGES * MQ_TILE_BYTES;
+  const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
+  long long M_eff = p.M;
+  if (p.m_valid) { const long long mv = *p.m_valid; M_eff = mv < M_eff ? mv : M_eff; }
+  const long long n_tiles = (M_eff + MQ_TM - 1) / MQ_TM * n_kt;
+  if (t == 0) {
+    for (int s = 0; s < MQ_STAGES; ++s) mbar_init(bar + 8 * s, 1);
+    fence_mbar_init();
+    prefetch_tmap(&tx);
+    for (int i = 0; i < MQ_STAGES; ++i) {
+      const long long ti = blockIdx.x + (long long)i * gridDim.x;
+      if (ti >= n_tiles) break;
+      mbar_arrive_expect_tx(bar + 8 * i, MQ_TILE_BYTES);
+      tma_load_2d(base + i * MQ_TILE_BYTES, &tx, (int)((ti % n_kt) * MQ_TK), (int)((ti / n_kt) * MQ_TM),
+                  bar + 8 * i);
+    }
+  }
+  __syncthreads();
+  int it = 0;
+  for (long long ti = blockIdx.x; ti < n_tiles; ti += gridDim.x, ++it) {
+    const int s = it % MQ_STAGES;
+    const bool ok = mbar_wait(bar + 8 * s, (uint32_t)(it / MQ_STAGES) & 1u, p.status);
+    if (__syncthreads_or(!ok)) break;
+    const uint8_t* tile = gbase + s * MQ_TILE_BYTES;          // row r at r * 128 bytes
+    const long long m0 = (ti / n_kt) * MQ_TM, k0 = (ti % n_kt) * MQ_TK;
+    if (p.flags & MPM_ROWWISE) {
+#pragma unroll
+      for (int step = 0; step < 4; ++step) {
+        const int rr = (warp * 4 + step) * 4 + (lane >> 3);   // row within the tile
+        const int bl = (lane >> 2) & 1, q = lane & 3;         // row block, quarter
+        const long long row = m0 + rr, col = k0 + bl * 32 + q * 8;
+        const uint4 u = *reinterpret_cast<const uint4*>(tile + rr * 128 + bl * 64 + q * 16);
+        const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
+        uint32_t m = absmax_bf16x2_packed(w4);
+        m = max(m, __shfl_xor_sync(0xffffffffu, m, 1));
+        m = max(m, __shfl_xor_sync(0xffffffffu, m, 2));
+        if (row < M_eff && k0 + bl * 32 < p.K) {
+          const int e = mx_exponent(m << 16);
+          const float sc = pow2_neg(e);
+          const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+          uint32_t o[2];
+#pragma unroll
+          for (int j = 0; j < 2; ++j) {
+            const uint32_t p0 = cvt_e4m3x2(__fmul_rn(bf16lo(w[2 * j]), sc), __fmul_rn(bf16hi(w[2 * j]), sc));
+            const uint32_t p1 = cvt_e4m3x2(__fmul_rn(bf16lo(w[2 * j + 1]), sc),
+                                           __fmul_rn(bf16hi(w[2 * j + 1]), sc));
+            o[j] = p0 | (p1 << 16);
+          }
+          *reinterpret_cast<uint2*>(p.row_q + row * p.K + col) = make_uint2(o[0], o[1]);
+          if (q == 0) p.row_s[sf_offset(row, col >> 5, p.row_s_cols_pad)] = (uint8_t)(e + 127);
+        }
+      }
+    }
+    if (p.flags & MPM_COLWISE) {
+      const int c = t & 63, g = t >> 6;
+      const long long col = k0 + c, mb = m0 + g * 32;
+      if (col < p.K && mb < M_eff) {
+        const long long nvalid = M_eff - mb;
+        uint32_t w[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const int r0 = g * 32 + 2 * j;
+          const uint32_t lo = *reinterpret_cast<const uint16_t*>(tile + r0 * 128 + c * 2);
+          const uint32_t hi = *reinterpret_cast<const uint16_t*>(tile + (r0 + 1) * 128 + c * 2);
+          w[j] = lo | (hi << 16);
+        }
+        if (nvalid < 32) {                                   // rows past the valid count
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            if (2 * j >= nvalid) w[j] &= 0xFFFF0000u;
+            if (2 * j + 1 >= nvalid) w[j] &= 0x0000FFFFu;
+          }
+        }
+        uint32_t m = absmax_bf16x2_packed(w);
+        const int e = mx_exponent(m << 16);
+        uint32_t o[8];
+        mx_encode32(w, pow2_neg(e), o);
+        uint8_t* dst = p.col_q + col * p.ldc + mb;
+        if (nvalid >= 32) {
+          uint4* d4 = reinterpret_cast<uint4*>(dst);
+          d4[0] = make_uint4(o[0], o[1], o[2], o[3]);
+          d4[1] = make_uint4(o[4], o[5], o[6], o[7]);
+        } else {
+          for (int j = 0; j < nvalid; ++j) dst[j] = (uint8_t)(o[j >> 2] >> (8 * (j & 3)));
+        }
+        p.col_s[sf_offset(col, mb >> 5, p.col_s_cols_pad)] = (uint8_t)(e + 127);
+      }
+    }
+    __syncthreads();                                  // stage s fully read
+    if (t == 0) {
+      const long long tn = ti + (long long)MQ_STAGES * gridDim.x;
+      if (tn < n_tiles) {
+        mbar_arrive_expect_tx(bar + 8 * s, MQ_TILE_BYTES);
+        tma_load_2d(base + s * MQ_TILE_BYTES, &tx, (int)((tn % n_kt) * MQ_TK),
+                    (int)((tn / n_kt) * MQ_TM), bar + 8 * s);
+      }
+    }
+  }
+  if (p.pad_blocks) {
+    // host-sized buffers: zero the padding entries of the scale tiles
+    const long long tid = (long long)blockIdx.x * blockDim.x + t;
     const long long nth = (long long)gridDim.x * blockDim.x;
     if (p.flags & MPM_ROWWISE) zero_scale_padding(p.row_s, p.M, p.K / 32, tid, nth);
     if (p.flags & MPM_COLWISE) zero_scale_padding(p.col_s, p.K, (p.M + 31) / 32, tid, nth);
-    return;
-  }
-  const long long m0 = (long long)blockIdx.y * MX_TM;
-  const long long k0 = (long long)blockIdx.x * MX_TK;
-  long long M_eff = p.M;
-  if (p.m_valid) { long long mv = *p.m_valid; M_eff = mv < M_eff ? mv : M_eff; }
-  if (m0 >= M_eff) return;
-  const int t = threadIdx.x;
-
-  // ---- load: thread t owns row t/2, columns (t%2)*64 .. +64 (two row blocks)
-  {
-    const int r = t >> 1, half = t & 1;
-    const long long row = m0 + r;
-    uint32_t w[2][16];
-    bool in[2];
-#pragma unroll
-    for (int b = 0; b < 2; ++b) {
-      const long long col = k0 + half * 64 + b * 32;
-      in[b] = (row < M_eff) && (col < p.K);
-      if (in[b]) {
-        const uint4* src = reinterpret_cast<const uint4*>(p.x + row * p.ldx + col);
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          uint4 u = __ldcs(src + j);
-          w[b][4 * j] = u.x; w[b][4 * j + 1] = u.y; w[b][4 * j + 2] = u.z; w[b][4 * j + 3] = u.w;
-        }
-      } else {
-#pragma unroll
-        for (int j = 0; j < 16; ++j) w[b][j] = 0;
-      }
-    }
-#pragma unroll
-    for (int b = 0; b < 2; ++b) {
-      const long long col = k0 + half * 64 + b * 32;
-      if ((p.flags & MPM_ROWWISE) && in[b]) {
-        uint32_t m = 0;
-#pragma unroll
-        for (int j = 0; j < 16; ++j) m = absmax_bf16x2(m, w[b][j]);
-        m = max(m & 0xFFFFu, m >> 16);
-        const int e = mx_exponent(m << 16);
-        uint32_t o[8];
-        mx_encode32(w[b], pow2_neg(e), o);
-        uint4* dst = reinterpret_cast<uint4*>(p.row_q + row * p.K + col);
-        dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
-        dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
-        p.row_s[sf_offset(row, col >> 5, p.row_s_cols_pad)] = (uint8_t)(e + 127);
-      }
-      if (p.flags & MPM_COLWISE) {
-        uint4* st = reinterpret_cast<uint4*>(&tile[r][half * 64 + b * 32]);
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-          st[j] = make_uint4(w[b][4 * j], w[b][4 * j + 1], w[b][4 * j + 2], w[b][4 * j + 3]);
-      }
-    }
-  }
-  if (!(p.flags & MPM_COLWISE)) return;
-  __syncthreads();
-
-  // ---- column blocks: thread t owns column t%128, row groups (t/128)*2 + {0, 1}
-  {
-    const int c = t & 127;
-    const long long col = k0 + c;
-    if (col >= p.K) return;
-#pragma unroll
-    for (int gg = 0; gg < 2; ++gg) {
-      const int g = (t >> 7) * 2 + gg;
-      const long long mb = m0 + g * 32;
-      if (mb >= M_eff) break;
-      uint32_t w[16];
-#pragma unroll
-      for (int j = 0; j < 16; ++j)
-        w[j] = (uint32_t)tile[g * 32 + 2 * j][c] | ((uint32_t)tile[g * 32 + 2 * j + 1][c] << 16);
-      uint32_t m = 0;
-#pragma unroll
-      for (int j = 0; j < 16; ++j) m = absmax_bf16x2(m, w[j]);
-      m = max(m & 0xFFFFu, m >> 16);
-      const int e = mx_exponent(m << 16);
-      uint32_t o[8];
-      mx_encode32(w, pow2_neg(e), o);
-      uint8_t* dst = p.col_q + col * p.ldc + mb;
-      const long long nvalid = M_eff - mb;
-      if (nvalid >= 32) {
-        uint4* d4 = reinterpret_cast<uint4*>(dst);
-        d4[0] = make_uint4(o[0], o[1], o[2], o[3]);
-        d4[1] = make_uint4(o[4], o[5], o[6], o[7]);
-      } else {
-        for (int j = 0; j < nvalid; ++j) dst[j] = (uint8_t)(o[j >> 2] >> (8 * (j & 3)));
-      }
-      p.col_s[sf_offset(col, mb >> 5, p.col_s_cols_pad)] = (uint8_t)(e + 127);
-    }
   }
 }
 
@@ -435,23 +460,40 @@ cudaError_t launch_nvfp4_weight(const void* const* parts, const long long* part_
   return launch_nvfp4_rows(p, st);
 }
 
-cudaError_t launch_mxfp8(const void* x, long long M, long long K, long long ldx, unsigned flags,
-                         uint8_t* row_q, uint8_t* row_s, uint8_t* col_q, long long ldc,
-                         uint8_t* col_s, const int* m_valid, cudaStream_t st) {
+cudaError_t launch_mxfp8_tma(const CUtensorMap& tx, long long M, long long K, long long ldx,
+                             unsigned flags, uint8_t* row_q, uint8_t* row_s, uint8_t* col_q,
+                             long long ldc, uint8_t* col_s, const int* m_valid, int* status,
+                             cudaStream_t st) {
   Mxfp8Args p{};
-  p.x = static_cast<const __nv_bfloat16*>(x);
   p.M = M; p.K = K; p.ldx = ldx; p.flags = flags;
   p.row_q = row_q; p.row_s = row_s; p.row_s_cols_pad = (K / 32 + 3) / 4 * 4;
   p.col_q = col_q; p.ldc = ldc; p.col_s = col_s;
   p.col_s_cols_pad = ((M + 31) / 32 + 3) / 4 * 4;
   p.m_valid = m_valid;
-  // with host-sized buffers one extra row of blocks zeroes the scale padding
-  // (device-sized buffers never read it)
   p.pad_blocks = m_valid ? 0 : 1;
-  const dim3 grid((unsigned)((K + MX_TK - 1) / MX_TK),
-                  (unsigned)((M + MX_TM - 1) / MX_TM + p.pad_blocks));
-  mxfp8_quant_kernel<<<grid, 256, 0, st>>>(p);
+  p.status = status;
+  const int n_kt = (int)((K + MQ_TK - 1) / MQ_TK);
+  const long long n_tiles = (M + MQ_TM - 1) / MQ_TM * n_kt;
+  constexpr int smem = 1024 + MQ_STAGES * MQ_TILE_BYTES + 64;
+  static int ctas[64] = {0};
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  if (dev < 64 && ctas[dev] == 0) {
+    err = cudaFuncSetAttribute(mxfp8_quant_tma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (err != cudaSuccess) return err;
+    int sms = 0, per = 0;
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, mxfp8_quant_tma_kernel, 256, smem);
+    ctas[dev] = (sms > 0 ? sms : 1) * (per > 0 ? per : 1);
+  }
+  long long grid = dev < 64 ? ctas[dev] : 1;
+  if (grid > n_tiles) grid = n_tiles;
+  if (grid < 1) grid = 1;
+  mxfp8_quant_tma_kernel<<<(unsigned)grid, 256, smem, st>>>(tx, p, n_kt);
   return cudaGetLastError();
 }
+
+
 
 }  // namespace mpm
