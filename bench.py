@@ -311,16 +311,31 @@ def _mxfp8_layer_line(peak_fp8, steps=10):
     L = MXFP8MoE(s.T, s.H, s.I, s.E, s.k)
     idc, prc = ids.cuda(), prob.cuda()
 
-    def step():
+    def step(mark=None):
+        if mark:
+            mark(0)
         L.quantize_weights(w1, w2)
-        L.forward(x, idc, prc)
-        L.backward(dy)
+        L.forward(x, idc, prc, mark=mark)
+        L.backward(dy, mark=mark)
     for _ in range(3):
         step()
     ms = _time_loop(step, steps)
+    # per-stage times from a second, marked pass
+    ns = len(MXFP8MoE.STEP_STAGES) + 1
+    ev = [_events(ns) for _ in range(steps)]
+    torch.cuda.synchronize()
+    for i in range(steps):
+        evi = ev[i]
+        step(mark=lambda j, evi=evi: evi[j].record())
+    torch.cuda.synchronize()
+    stage = {n: round(float(np.mean([ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(steps)])), 4)
+             for j, n in enumerate(MXFP8MoE.STEP_STAGES)}
     tf = L.gemm_flops() / (ms * 1e-3) / 1e12
+    gemm_ms = sum(v for n, v in stage.items() if n.startswith("fc"))
     r = {"workload": s.name, "ms_per_step": round(ms, 3), "TFLOP/s": round(tf, 1),
          "frac_fp8_peak": round(tf / peak_fp8, 3),
+         "gemm_TFLOP/s": round(L.gemm_flops() / (gemm_ms * 1e-3) / 1e12, 1),
+         "stage_ms": stage,
          "note": "whole fwd+bwd step (weight quantisation included) / GEMM algorithmic FLOPs"}
     del L, x, w1, w2, dy
     torch.cuda.empty_cache()
@@ -519,7 +534,8 @@ def main():
                               "n_gpus": world, "steps": args.steps, "warmup": 3,
                               "ms_per_step": r["ms_per_step"], "higher_is_better": True,
                               "dtype": "mxfp8", "config": {"workload": r["workload"]},
-                              "note": r["note"]}), flush=True)
+                              "note": r["note"], "gemm_TFLOP/s": r["gemm_TFLOP/s"],
+                              "stage_ms": r["stage_ms"]}), flush=True)
         return 0
     if args.case == "quant":
         r = _quantizer_lines(peaks["hbm"])
