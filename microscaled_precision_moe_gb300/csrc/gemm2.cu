@@ -413,6 +413,30 @@ grouped_gemm_pair_kernel(const __grid_constant__ PairMaps maps, const GemmArgs p
         }
         continue;
       }
+      // the row's scales come from global memory: load them before waiting
+      // for the accumulator so their latency is not part of the hand-off
+      const long long grow = k.row_pair + rank * BM + r;     // row of A (GROUP_M)
+      const bool row_ok = (p.group == MPM_GROUP_K) || grow < p.a_rows;
+      float alpha_a = 1.0f, alpha_b = 1.0f, prob_r = 0.0f;
+      if (row_ok && p.group == MPM_GROUP_M) {
+        if (p.alpha_a) alpha_a = p.alpha_a[grow];
+        if (p.alpha_b) alpha_b = p.alpha_b[k.e];
+        if ((EPI == MPM_EPI_SWIGLU || EPI == MPM_EPI_SWIGLU_SAVE || EPI == MPM_EPI_DSWIGLU) &&
+            p.row_prob)
+          prob_r = p.row_prob[grow];
+      }
+      // SwiGLU backward: the first 32 columns of this row's gate and up values
+      // (C) are requested before the accumulator wait as well
+      uint4 cgw[4], cuw[4];
+      if (EPI == MPM_EPI_DSWIGLU && row_ok) {
+        const __nv_bfloat16* cg0 = static_cast<const __nv_bfloat16*>(p.aux) + grow * p.ld_aux +
+                                   k.n0 + half * 128;
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+          cgw[q4] = *reinterpret_cast<const uint4*>(cg0 + q4 * 8);
+          cuw[q4] = *reinterpret_cast<const uint4*>(cg0 + p.N + q4 * 8);
+        }
+      }
       const uint32_t ab = NACC > 1 ? (j & 1u) : 0u, use = NACC > 1 ? (j >> 1) : j;
       const bool w_ok = mbar_wait_cluster(bar_acc + 16 * ab, use & 1u, p.status);
       ++j;
@@ -422,17 +446,11 @@ grouped_gemm_pair_kernel(const __grid_constant__ PairMaps maps, const GemmArgs p
       named_sync(1, EPI_THREADS);
       if (*fail_flag) break;
       tc_fence_after();
-      const long long grow = k.row_pair + rank * BM + r;     // row of A (GROUP_M)
-      const bool row_ok = (p.group == MPM_GROUP_K) || grow < p.a_rows;
-      float alpha = 1.0f;
-      if (row_ok && p.group == MPM_GROUP_M) {
-        if (p.alpha_a) alpha = p.alpha_a[grow];
-        if (p.alpha_b) alpha = __fmul_rn(alpha, p.alpha_b[k.e]);
-      }
+      const float alpha = (p.alpha_b && p.group == MPM_GROUP_M) ? __fmul_rn(alpha_a, alpha_b) : alpha_a;
       uint32_t v[32], u[32];
       if (EPI == MPM_EPI_SWIGLU || EPI == MPM_EPI_SWIGLU_SAVE) {
         // this thread: D columns [64*half, 64*half + 64) of the tile
-        const float prob = row_ok ? p.row_prob[grow] : 0.0f;
+        const float prob = prob_r;
         uint32_t dw[32];
         float amax = 0.0f;
         uint32_t v2[32], u2[32];
@@ -592,23 +610,32 @@ grouped_gemm_pair_kernel(const __grid_constant__ PairMaps maps, const GemmArgs p
           }
         }
       } else {   // MPM_EPI_DSWIGLU
-        const float prob = row_ok ? p.row_prob[grow] : 0.0f;
+        const float prob = prob_r;
         const long long Nh = p.N;
         const __nv_bfloat16* cg = static_cast<const __nv_bfloat16*>(p.aux) + grow * p.ld_aux;
         const __nv_bfloat16* cu = cg + Nh;
         __nv_bfloat16* og = static_cast<__nv_bfloat16*>(p.out) + grow * p.ldo;
         __nv_bfloat16* ou = og + Nh;
-#pragma unroll 1
+#pragma unroll
         for (int cc = 0; cc < 4; ++cc) {
           const int c = half * 4 + cc;
           tmem_ld_32x32b_x32(trow + c * 32, v);
+          // next chunk of C in flight while this one is computed
+          uint4 ngw[4], nuw[4];
+          if (row_ok && cc < 3) {
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) {
+              ngw[q4] = *reinterpret_cast<const uint4*>(cg + k.n0 + (c + 1) * 32 + q4 * 8);
+              nuw[q4] = *reinterpret_cast<const uint4*>(cu + k.n0 + (c + 1) * 32 + q4 * 8);
+            }
+          }
           tmem_ld_wait();
-          if (!row_ok) continue;
+          if (row_ok) {
           const long long col = k.n0 + c * 32;
 #pragma unroll
           for (int jj = 0; jj < 32; jj += 8) {
-            const uint4 gw = *reinterpret_cast<const uint4*>(cg + col + jj);
-            const uint4 uw = *reinterpret_cast<const uint4*>(cu + col + jj);
+            const uint4 gw = cgw[jj / 8];
+            const uint4 uw = cuw[jj / 8];
             const uint32_t ga[4] = {gw.x, gw.y, gw.z, gw.w};
             const uint32_t ua[4] = {uw.x, uw.y, uw.z, uw.w};
             uint32_t og4[4], ou4[4];
@@ -630,6 +657,11 @@ grouped_gemm_pair_kernel(const __grid_constant__ PairMaps maps, const GemmArgs p
             }
             *reinterpret_cast<uint4*>(og + col + jj) = make_uint4(og4[0], og4[1], og4[2], og4[3]);
             *reinterpret_cast<uint4*>(ou + col + jj) = make_uint4(ou4[0], ou4[1], ou4[2], ou4[3]);
+          }
+          }
+          if (cc < 3) {
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) { cgw[q4] = ngw[q4]; cuw[q4] = nuw[q4]; }
           }
         }
         tc_fence_before();
