@@ -102,11 +102,12 @@ class NVFP4MoE:
     STAGES = ("quant_x", "segments", "gather", "fc1", "quant_d", "fc2", "combine")
 
     def forward(self, x, topk_ids, topk_prob, w: NVFP4Weights, mark=None,
-                save_for_backward=False):
-        """out [T, H] bf16.  ``mark(i)`` (optional) is called before stage i
-        of STAGES and once more at the end (used to record CUDA events).
-        save_for_backward: the FC1 epilogue also stores C = gate|up (bf16,
-        [capacity, 2I]) for the SwiGLU backward."""
+                save_for_backward=False, out=None):
+        """out [T, H] bf16 (the layer's own buffer, or ``out`` when given).
+        ``mark(i)`` (optional) is called before stage i of STAGES and once
+        more at the end (used to record CUDA events).  save_for_backward: the
+        FC1 epilogue also stores C = gate|up (bf16, [capacity, 2I]) for the
+        SwiGLU backward."""
         T, H, I, E, k, cap = self.T, self.H, self.I, self.E, self.k, self.cap
         mark = mark or (lambda i: None)
         mark(0)
@@ -135,9 +136,10 @@ class NVFP4MoE:
                              self.y, b_rows_per_expert=H, alpha_a=dts, alpha_b=w.w2_ts,
                              tile_m=self.tile_m)
         mark(6)
-        ops.moe_combine(self.y, inv, T, k, out=self.out)
+        dst = self.out if out is None else out
+        ops.moe_combine(self.y, inv, T, k, out=dst)
         mark(7)
-        return self.out
+        return dst
 
     # kernels launched by one forward: quantiser, 4 segment kernels
     # (histogram, per-expert column scan, offsets, scatter), gather, FC1,
