@@ -151,12 +151,15 @@ __global__ void __launch_bounds__(256) gather_bf16_kernel(const uint4* src, long
 // scale tiles): each warp copies 16 rows of codes; each 512-byte scale tile of
 // the destination is assembled by 128 threads, one 4-byte word (a row's four
 // scales of the tile) each, and written as one contiguous 512-byte run.
-__global__ void __launch_bounds__(256) gather_nvfp4_kernel(const uint4* src_q, const uint8_t* src_s,
-                                                          const float* src_ts, long long K,
-                                                          int k, const int* perm,
-                                                          const int* seg_end, long long cap,
-                                                          uint4* dst_q, uint8_t* dst_s,
-                                                          float* dst_ts, float* amax_zero) {
+__global__ void __launch_bounds__(256) gather_nvfp4_kernel(const uint4* __restrict__ src_q,
+                                                          const uint8_t* __restrict__ src_s,
+                                                          const float* __restrict__ src_ts, long long K,
+                                                          int k, const int* __restrict__ perm,
+                                                          const int* __restrict__ seg_end, long long cap,
+                                                          uint4* __restrict__ dst_q,
+                                                          uint8_t* __restrict__ dst_s,
+                                                          float* __restrict__ dst_ts,
+                                                          float* __restrict__ amax_zero) {
   __shared__ long long tok[128];                  // source token of each row, -1 for padding
   const long long rbase = (long long)blockIdx.x * 128;
   long long rend = *seg_end;
@@ -182,9 +185,11 @@ __global__ void __launch_bounds__(256) gather_nvfp4_kernel(const uint4* src_q, c
     uint4* d = dst_q + (rbase + i) * q16;
     const long long t = tok[i];
     if (t < 0) {
+#pragma unroll 4
       for (long long c = lane; c < q16; c += 32) d[c] = make_uint4(0, 0, 0, 0);
     } else {
       const uint4* sq = src_q + t * q16;
+#pragma unroll 4
       for (long long c = lane; c < q16; c += 32) d[c] = __ldg(sq + c);
     }
   }
@@ -194,6 +199,7 @@ __global__ void __launch_bounds__(256) gather_nvfp4_kernel(const uint4* src_q, c
   const int w = threadIdx.x & 127;
   const int r = (w & 3) * 32 + (w >> 2);
   const long long t = tok[r];
+#pragma unroll 4
   for (long long g = threadIdx.x >> 7; g < ntiles; g += 2) {
     if (r >= nrows) continue;
     uint32_t v = 0;
