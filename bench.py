@@ -51,14 +51,19 @@ def _peaks():
 
 # ---------------------------------------------------------------- distributed
 
-def _dist():
+def _dist(backend=None):
+    """(torch.distributed or None, rank, world) from the torchrun environment;
+    one replica per GPU over NCCL, or gloo when no GPU is present."""
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     if ws > 1:
         import torch.distributed as dist
         rank = int(os.environ["RANK"])
         local = int(os.environ.get("LOCAL_RANK", rank))
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl")
+        if backend is None:
+            backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
         return dist, rank, ws
     return None, 0, 1
 
@@ -69,9 +74,11 @@ def _barrier(dist):
 
 
 def _max_over_ranks(dist, v: float) -> float:
+    """The slowest replica's time (every rank gets it)."""
     if dist is None:
         return v
-    t = torch.tensor([v], device="cuda", dtype=torch.float64)
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([v], device=dev, dtype=torch.float64)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
 

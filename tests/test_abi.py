@@ -83,3 +83,68 @@ def test_host_validation_rejects_before_launch(lib):
     d.group, d.tile_m = 0, 192                      # only 128 or 256
     assert lib.mpm_moe_grouped_gemm(C.byref(d), None) == 4
     assert lib.mpm_moe_grouped_gemm(None, None) == 1
+
+
+def _gemm_desc(kind, group, epi, N, K, tile_m):
+    from microscaled_precision_moe_gb300 import _lib as L
+    d = L.GroupedGemmDesc()
+    d.kind, d.group, d.epilogue, d.tile_m = kind, group, epi, tile_m
+    d.E, d.a_rows, d.N, d.K = 1, 256, N, K
+    for f in ("a_dev", "b_dev", "out_dev"):
+        setattr(d, f, 0x10000)
+    d.lda_bytes = d.ldb_bytes = 4096
+    d.a_total_rows = d.b_total_rows = 256
+    d.ldo = 2 * N
+    return d
+
+
+def test_bf16_mn_major_and_small_m_validation(lib):
+    """The BF16 kind, its MN-major operands and the small-M tile mode are
+    checked on the host (CPU only)."""
+    from microscaled_precision_moe_gb300 import _lib as L
+    # BF16 needs the CTA-pair kernel
+    d = _gemm_desc(L.KIND_BF16, L.GROUP_M, L.EPI_BF16, 256, 512, 128)
+    assert lib.mpm_moe_grouped_gemm(C.byref(d), None) == 4
+    # BF16: K % 64
+    d = _gemm_desc(L.KIND_BF16, L.GROUP_M, L.EPI_BF16, 256, 96, 256)
+    assert lib.mpm_moe_grouped_gemm(C.byref(d), None) == 2
+    # MN-major A only in GROUP_K, and only for the bf16 kind
+    d = _gemm_desc(L.KIND_BF16, L.GROUP_M, L.EPI_BF16, 256, 512, 256)
+    d.a_mn_major = 1
+    assert lib.mpm_moe_grouped_gemm(C.byref(d), None) == 4
+    d = _gemm_desc(L.KIND_MXFP8, L.GROUP_M, L.EPI_BF16, 256, 512, 256)
+    d.b_mn_major = 1
+    d.sfa_dev = d.sfb_dev = 0x10000
+    d.sfa_cols = d.sfb_cols = 16
+    assert lib.mpm_moe_grouped_gemm(C.byref(d), None) == 4
+    # GROUP_K with only one operand MN-major is not a supported combination
+    d = _gemm_desc(L.KIND_BF16, L.GROUP_K, L.EPI_F32, 256, 0, 256)
+    d.seg_dev = 0x10000
+    d.a_mn_major = 1
+    assert lib.mpm_moe_grouped_gemm(C.byref(d), None) == 4
+    # small-M kernel: GROUP_M only, no bf16, no SwiGLU-save / DSwiGLU
+    d = _gemm_desc(L.KIND_BF16, L.GROUP_M, L.EPI_BF16, 256, 512, L.TILE_SMALL_M)
+    assert lib.mpm_moe_grouped_gemm(C.byref(d), None) == 4
+    d = _gemm_desc(L.KIND_NVFP4, L.GROUP_M, L.EPI_DSWIGLU, 256, 512, L.TILE_SMALL_M)
+    d.sfa_dev = d.sfb_dev = 0x10000
+    d.sfa_cols = d.sfb_cols = 32
+    assert lib.mpm_moe_grouped_gemm(C.byref(d), None) == 4
+
+
+def test_dequantize_and_transpose_validation(lib):
+    fake = C.c_void_p(0x10000)
+    odd = C.c_void_p(0x10008)
+    # NVFP4 -> bf16: NULL, K % 64, rows_per_outer, ldo, alignment
+    assert lib.mpm_nvfp4_dequantize(None, fake, fake, 1, 4, 64, fake, 64, None, None) == 1
+    assert lib.mpm_nvfp4_dequantize(fake, fake, fake, 1, 4, 48, fake, 64, None, None) == 2
+    assert lib.mpm_nvfp4_dequantize(fake, fake, fake, 0, 4, 64, fake, 64, None, None) == 2
+    assert lib.mpm_nvfp4_dequantize(fake, fake, fake, 1, 4, 64, fake, 60, None, None) == 2
+    assert lib.mpm_nvfp4_dequantize(odd, fake, fake, 1, 4, 64, fake, 64, None, None) == 3
+    # MXFP8 -> bf16: K % 32, ldo % 8
+    assert lib.mpm_mxfp8_dequantize(fake, fake, 4, 48, fake, 48, None, None) == 2
+    assert lib.mpm_mxfp8_dequantize(fake, fake, 4, 64, fake, 68, None, None) == 2
+    # transpose: shapes and leading dimensions
+    assert lib.mpm_transpose_bf16(None, 4, 4, 4, fake, 4, None, None) == 1
+    assert lib.mpm_transpose_bf16(fake, 0, 4, 4, fake, 4, None, None) == 2
+    assert lib.mpm_transpose_bf16(fake, 8, 4, 3, fake, 8, None, None) == 2
+    assert lib.mpm_transpose_bf16(fake, 8, 4, 4, fake, 7, None, None) == 2
