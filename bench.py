@@ -413,7 +413,22 @@ def _nvfp4_bf16_bwd_line(peak_bf16, steps=10):
                    "frac_bf16_peak": round(tf / peak_bf16, 3), "stage_ms": stage,
                    "prepare_weights_ms": round(prep_ms, 3),
                    "gpu_launches_per_step": NVFP4MoE.LAUNCHES_PER_BACKWARD[mode]}
-    del L, W, x, w1, w2, dy
+    del L, W
+    torch.cuda.empty_cache()
+    # the same modes after an MXFP8 forward
+    from microscaled_precision_moe_gb300.moe import MXFP8MoE
+    M8 = MXFP8MoE(s.T, s.H, s.I, s.E, s.k)
+    M8.quantize_weights(w1, w2)
+    M8.forward(x, ids.cuda(), prob.cuda())
+    for mode in MXFP8MoE.BACKWARD_MODES:
+        M8.prepare_backward_weights(mode, w1=w1, w2=w2)
+        for _ in range(3):
+            M8.backward_bf16(dy, mode)
+        ms = _time_loop(lambda: M8.backward_bf16(dy, mode), steps)
+        tf = flops / (ms * 1e-3) / 1e12
+        r["mxfp8_fwd_" + mode] = {"ms_per_step": round(ms, 3), "TFLOP/s": round(tf, 1),
+                                  "frac_bf16_peak": round(tf / peak_bf16, 3)}
+    del M8, x, w1, w2, dy
     torch.cuda.empty_cache()
     return r
 

@@ -41,6 +41,37 @@ def _sb(rows, cols):
     return ops.scale_bytes(rows, cols)
 
 
+def _bf16_backward_gemms(L_, x_op, d_op, w1_op, w2_op, dy, mark, m0):
+    """The BF16 backward of an expert layer on given operands (both layers):
+    gather dY, FC2 dgrad with the SwiGLU backward fused, FC2 wgrad, FC1
+    dgrad, combine, FC1 wgrad — every operand read row-major (MN-major where
+    the GEMM contracts over rows).  Buffers (dyp, dh, dxp, dx, dw1, dw2, c1,
+    seg) belong to the layer ``L_``; ``mark(m0 + i)`` before each stage."""
+    T, H, I, E, k, cap = L_.T, L_.H, L_.I, L_.E, L_.k, L_.cap
+    seg, perm, inv, rp = L_.seg
+    bf = L.KIND_BF16
+    mark(m0)
+    ops.moe_gather_bf16(dy, perm, seg, E, k, cap, out=L_.dyp)
+    mark(m0 + 1)
+    ops.moe_grouped_gemm(bf, L.GROUP_M, L.EPI_DSWIGLU, E, cap, I, H, seg, L_.dyp, w2_op,
+                         None, 0, None, 0, L_.dh, b_rows_per_expert=0, b_k_per_expert=H,
+                         row_prob=rp, aux=L_.c1, tile_m=256, b_mn_major=True)
+    mark(m0 + 2)
+    ops.moe_grouped_gemm(bf, L.GROUP_K, L.EPI_F32, E, H, I, 0, seg, L_.dyp, d_op,
+                         None, 0, None, 0, L_.dw2, tile_m=256, a_mn_major=True, b_mn_major=True)
+    mark(m0 + 3)
+    ops.moe_grouped_gemm(bf, L.GROUP_M, L.EPI_BF16, E, cap, H, 2 * I, seg, L_.dh, w1_op,
+                         None, 0, None, 0, L_.dxp, b_rows_per_expert=0, b_k_per_expert=2 * I,
+                         tile_m=256, b_mn_major=True)
+    mark(m0 + 4)
+    ops.moe_combine(L_.dxp, inv, T, k, out=L_.dx)
+    mark(m0 + 5)
+    ops.moe_grouped_gemm(bf, L.GROUP_K, L.EPI_F32, E, 2 * I, H, 0, seg, L_.dh, x_op,
+                         None, 0, None, 0, L_.dw1, tile_m=256, a_mn_major=True, b_mn_major=True)
+    mark(m0 + 6)
+    return L_.dx, L_.dw1, L_.dw2
+
+
 # ============================================================================
 # NVFP4
 # ============================================================================
@@ -219,33 +250,7 @@ class NVFP4MoE:
             ops.nvfp4_dequantize(*self.aq, 1, H, m_valid=mv, out=self.xp)
             ops.nvfp4_dequantize(*self.dq, 1, I, m_valid=mv, out=self.dop)
             d_op = self.dop
-        mark(1)
-        ops.moe_gather_bf16(dy, perm, seg, E, k, cap, out=self.dyp)
-        mark(2)
-        # FC2 dgrad with the SwiGLU backward fused: dH = [dg | du];
-        # B = W2 read row-major: expert e's reduction rows e*H .. e*H + H
-        ops.moe_grouped_gemm(bf, L.GROUP_M, L.EPI_DSWIGLU, E, cap, I, H, seg, self.dyp, self.w2_op,
-                             None, 0, None, 0, self.dh, b_rows_per_expert=0, b_k_per_expert=H,
-                             row_prob=rp, aux=self.c1, tile_m=256, b_mn_major=True)
-        mark(3)
-        # FC2 wgrad: dW2[e] = dY_e^T . D_e, both read row-major
-        ops.moe_grouped_gemm(bf, L.GROUP_K, L.EPI_F32, E, H, I, 0, seg, self.dyp, d_op,
-                             None, 0, None, 0, self.dw2, tile_m=256, a_mn_major=True,
-                             b_mn_major=True)
-        mark(4)
-        # FC1 dgrad: dX_perm = dH . W1_e, W1 read row-major
-        ops.moe_grouped_gemm(bf, L.GROUP_M, L.EPI_BF16, E, cap, H, 2 * I, seg, self.dh, self.w1_op,
-                             None, 0, None, 0, self.dxp, b_rows_per_expert=0,
-                             b_k_per_expert=2 * I, tile_m=256, b_mn_major=True)
-        mark(5)
-        ops.moe_combine(self.dxp, inv, T, k, out=self.dx)
-        mark(6)
-        # FC1 wgrad: dW1[e] = dH_e^T . X_e
-        ops.moe_grouped_gemm(bf, L.GROUP_K, L.EPI_F32, E, 2 * I, H, 0, seg, self.dh, self.xp,
-                             None, 0, None, 0, self.dw1, tile_m=256, a_mn_major=True,
-                             b_mn_major=True)
-        mark(7)
-        return self.dx, self.dw1, self.dw2
+        return _bf16_backward_gemms(self, self.xp, d_op, self.w1_op, self.w2_op, dy, mark, 1)
 
     # kernels launched by one backward (weights prepared separately)
     LAUNCHES_PER_BACKWARD = {"high_precision": 7, "dequantized": 8}
@@ -388,6 +393,54 @@ class MXFP8MoE:
                              self.xq["col_s"], cap // 32, self.dw1, tile_m=self._wgrad_tile(2 * I))
         mark(16)
         return self.dx, self.dw1, self.dw2
+
+    # ------------------------------------------------------------ BF16 backward
+    # "The same backward mode selection applies to MXFP8": the four backward
+    # GEMMs in BF16 on the original operands or on the BF16 dequantisation of
+    # the row-wise MXFP8 copies the forward consumed.
+    BACKWARD_MODES = ("high_precision", "dequantized")
+    BF16_BACKWARD_STAGES = ("operands", "gather_dy", "fc2_dgrad", "fc2_wgrad", "fc1_dgrad",
+                            "combine", "fc1_wgrad")
+
+    def prepare_backward_weights(self, mode, w1=None, w2=None):
+        """Weight operands of the BF16 dgrads, once per weight update: the
+        BF16 weights (high_precision) or the dequantised row-wise MXFP8 copies
+        made by quantize_weights (dequantized)."""
+        E, H, I = self.E, self.H, self.I
+        if mode == "high_precision":
+            self.w1_op, self.w2_op = w1.reshape(E * 2 * I, H), w2.reshape(E * H, I)
+        elif mode == "dequantized":
+            self.w1_op = ops.mxfp8_dequantize(self.w1["row_q"], self.w1["row_s"])
+            self.w2_op = ops.mxfp8_dequantize(self.w2["row_q"], self.w2["row_s"])
+        else:
+            raise ValueError(f"unknown backward mode {mode!r}")
+        self._w_mode = mode
+
+    def backward_bf16(self, dy, mode, mark=None):
+        """dX, dW1, dW2 with BF16 GEMMs after forward(), in ``mode``
+        (prepare_backward_weights first).  ``mark(i)`` over
+        BF16_BACKWARD_STAGES."""
+        if mode not in self.BACKWARD_MODES:
+            raise ValueError(f"unknown backward mode {mode!r}")
+        if getattr(self, "_w_mode", None) != mode:
+            raise RuntimeError(f"prepare_backward_weights({mode!r}) first")
+        if self.tile_m != 256:
+            raise ValueError("the BF16 backward runs its GEMMs on CTA pairs: tile_m=256")
+        H, I, E, cap = self.H, self.I, self.E, self.cap
+        seg = self.seg[0]
+        mark = mark or (lambda i: None)
+        mark(0)
+        if mode == "high_precision":
+            x_op, d_op = self.xp, self.d
+        else:
+            if getattr(self, "xop", None) is None:
+                self.xop = torch.empty(cap, H, dtype=torch.bfloat16, device=self.xp.device)
+                self.dop = torch.empty(cap, I, dtype=torch.bfloat16, device=self.xp.device)
+            mv = seg[E:]
+            ops.mxfp8_dequantize(self.xq["row_q"], self.xq["row_s"], m_valid=mv, out=self.xop)
+            ops.mxfp8_dequantize(self.dq["row_q"], self.dq["row_s"], m_valid=mv, out=self.dop)
+            x_op, d_op = self.xop, self.dop
+        return _bf16_backward_gemms(self, x_op, d_op, self.w1_op, self.w2_op, dy, mark, 1)
 
     def _wgrad_tile(self, m_out):
         return 256 if (self.tile_m == 256 and m_out % 256 == 0) else 128

@@ -334,3 +334,36 @@ def nvfp4_moe_backward_bf16(fwd: dict, x, w1, w2, dy, mode: str):
     r["dx"] = F.bf16_round(combine(r["dxp"], inv, T, k))
     r.update(xp=xp, w1_op=b1, w2_op=b2, d_op=d, c1=c1, dyp=dyp)
     return r
+
+
+def mxfp8_moe_bf16_backward(x, topk_ids, topk_prob, w1, w2, dy, E: int, mode: str, pad=ROW_PAD):
+    """MXFP8 forward (row-wise copies, as in mxfp8_moe_fwd_bwd) followed by
+    the BF16 backward in one of the two operand modes: high_precision uses
+    the BF16 X_perm, W1, W2 and the FC1 epilogue's BF16 D; dequantized uses
+    the BF16 dequantisation of the row-wise MXFP8 copies the forward GEMMs
+    consumed (X_perm, W1, W2, D).  The SwiGLU derivative is taken at the
+    saved C = gate|up (bf16)."""
+    T, H = np.asarray(x).shape
+    k = np.asarray(topk_ids).shape[1]
+    I = np.asarray(w1).shape[1] // 2
+    seg, perm, inv, row_prob = build_segments(topk_ids, topk_prob, E, pad)
+    xp = gather_rows(np.asarray(x, dtype=np.float64), perm, k)
+    b1 = np.stack([mx_rows(w1[e]) for e in range(E)])
+    acc1 = grouped_gemm(mx_rows(xp), b1, seg)
+    c1 = F.bf16_round(acc1)
+    d = fc1_epilogue(acc1, row_prob, I)
+    if mode == "high_precision":
+        x_op, w1_op, w2_op, d_op = xp, np.asarray(w1, np.float64), np.asarray(w2, np.float64), d
+    elif mode == "dequantized":
+        x_op = F.bf16_round(mx_rows(xp))
+        w1_op = F.bf16_round(b1)
+        w2_op = F.bf16_round(np.stack([mx_rows(w2[e]) for e in range(E)]))
+        d_op = F.bf16_round(mx_rows(d))
+    else:
+        raise ValueError(f"unknown backward mode {mode!r}")
+    dyp = gather_rows(np.asarray(dy, dtype=np.float64), perm, k)
+    r = bf16_backward(x_op, w1_op, w2_op, d_op, c1, dyp, seg, row_prob, I)
+    r["dx"] = F.bf16_round(combine(r["dxp"], inv, T, k))
+    r.update(seg=seg, perm=perm, inv=inv, row_prob=row_prob, c1=c1, d=d, xp=x_op,
+             w1_op=w1_op, w2_op=w2_op, d_op=d_op, dyp=dyp)
+    return r

@@ -330,3 +330,37 @@ def test_nvfp4_layer_bf16_backward(mode):
         _close(dw2.cpu().numpy(), own, f"{mode}: dW2 on the kernel's own D_hat")
         rel = Mx.rel_l2(dw2.cpu().numpy(), r["dw2"])
         assert rel < 0.05, f"{mode}: dW2 differs from the oracle's by {rel:.3e}"
+
+
+@pytest.mark.parametrize("mode", ["high_precision", "dequantized"])
+def test_mxfp8_layer_bf16_backward(mode):
+    """The same backward modes after an MXFP8 forward: BF16 GEMMs on the BF16
+    operands or on the dequantised row-wise MXFP8 copies, against the
+    oracle's MXFP8 forward + BF16 backward (GEMM tolerance whole; the MXFP8
+    re-quantisation of D keeps the chain within it)."""
+    from microscaled_precision_moe_gb300.moe import MXFP8MoE
+    ops = _ops()
+    shape = synth.scaled(synth.MOE_30B_BWD, T=400, H=512, I=256, E=6, k=4)
+    T, H, I, E, k = shape.T, shape.H, shape.I, shape.E, shape.k
+    ids, prob = synth.routing(shape)
+    x = synth.moe_activations(shape, device="cuda")
+    w1, w2 = synth.moe_weights(shape, device="cuda")
+    dy = synth.moe_grad_out(shape, device="cuda")
+    layer = MXFP8MoE(T, H, I, E, k)
+    layer.quantize_weights(w1, w2)
+    layer.forward(x, ids.cuda(), prob.cuda())
+    layer.prepare_backward_weights(mode, w1=w1, w2=w2)
+    dx, dw1, dw2 = layer.backward_bf16(dy, mode)
+    torch.cuda.synchronize()
+    assert ops.get_device_status() == 0
+    with np.errstate(over="ignore"):
+        r = MO.mxfp8_moe_bf16_backward(np_bf16(x).astype(np.float64), ids.numpy(), prob.numpy(),
+                                       np_bf16(w1).astype(np.float64), np_bf16(w2).astype(np.float64),
+                                       np_bf16(dy).astype(np.float64), E, mode, pad=256)
+    R = int(r["seg"][-1])
+    _close(np_bf16(layer.c1[:R]), r["c1"], f"MXFP8 {mode}: C")
+    _close(np_bf16(layer.dh[:R]), r["dh"], f"MXFP8 {mode}: dH")
+    _close(np_bf16(layer.dxp[:R]), r["dxp"], f"MXFP8 {mode}: dX_perm")
+    _close(np_bf16(dx), r["dx"], f"MXFP8 {mode}: dX")
+    _close(dw1.cpu().numpy(), r["dw1"], f"MXFP8 {mode}: dW1")
+    _close(dw2.cpu().numpy(), r["dw2"], f"MXFP8 {mode}: dW2")

@@ -376,3 +376,27 @@ def test_bf16_backward_planted_mistakes_fail(monkeypatch):
         gx, gw1, gw2 = _ste_autograd_backward(x, w1, w2, r["c1"], r["d_op"], ids, prob,
                                               fwd["inv"], dy, shape.I)
         assert Mx.rel_l2(r["dw1"], gw1) > 0.05 or Mx.rel_l2(r["dx"], gx) > 0.05
+
+
+@pytest.mark.parametrize("mode", MO.BACKWARD_MODES)
+def test_mxfp8_bf16_backward_vs_autograd(mode):
+    """The BF16 backward after an MXFP8 forward, both operand modes, against
+    fp64 autograd with the forward's values held by straight-through terms
+    (the same pin as for the NVFP4 forward)."""
+    shape = synth.scaled(synth.MOE_30B_BWD, T=40, H=64, I=32, E=4, k=2)
+    ids, prob = synth.routing(shape)
+    ids, prob = ids.numpy(), prob.numpy()
+    x = synth.moe_activations(shape).double().numpy()
+    w1, w2 = synth.moe_weights(shape)
+    w1, w2 = w1.double().numpy(), w2.double().numpy()
+    dy = synth.moe_grad_out(shape).double().numpy()
+    with np.errstate(over="ignore"):
+        r = MO.mxfp8_moe_bf16_backward(x, ids, prob, w1, w2, dy, shape.E, mode)
+    x_op = x if mode == "high_precision" else F.bf16_round(MO.mx_rows(x))
+    gx, gw1, gw2 = _ste_autograd_backward(x_op, r["w1_op"], r["w2_op"], r["c1"], r["d_op"],
+                                          ids, prob, r["inv"], dy, shape.I)
+    assert Mx.rel_l2(r["dw2"], gw2) < 1e-12
+    assert Mx.rel_l2(r["dw1"], gw1) < 4e-3
+    assert Mx.rel_l2(r["dx"], gx) < 6e-3
+    if mode == "dequantized":
+        assert not np.array_equal(r["w1_op"], w1)
