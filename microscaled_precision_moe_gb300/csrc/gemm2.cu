@@ -118,12 +118,21 @@ struct Task {
   int num_kb;
 };
 
+// Each role of a CTA walks its tasks in increasing order, so it finds a
+// task's expert by moving a cursor forward over the device segment offsets
+// (each offset is read from global memory once per role, not the ~log2(E)
+// dependent reads of a binary search for every task).
+struct SegCursor {
+  int e = -1;               // expert whose [lo, hi) row range is cached
+  long long lo = 0, hi = 0;
+  long long end = -1;       // seg[E] (GROUP_M) once read
+};
+
 // GROUP_M: tasks = (256-row pair of A rows) x (N tile); the pair's expert is
-// found by binary search over the device offsets.  GROUP_K: tasks = expert x
-// (256-row pair of output rows) x (N tile); the reduction runs over the
-// expert's segment.
+// the segment holding its first row.  GROUP_K: tasks = expert x (256-row pair
+// of output rows) x (N tile); the reduction runs over the expert's segment.
 template <int KIND, int EPI>
-MPM_DEV Task task_of(const GemmArgs& p, long long t, int n_tiles, int* bad) {
+MPM_DEV Task task_of(const GemmArgs& p, long long t, int n_tiles, int* bad, SegCursor& cur) {
   Task k{};
   const bool swiglu = (EPI == MPM_EPI_SWIGLU || EPI == MPM_EPI_SWIGLU_SAVE);
   int e = 0;
@@ -136,7 +145,12 @@ MPM_DEV Task task_of(const GemmArgs& p, long long t, int n_tiles, int* bad) {
     const long long rem = t - (long long)e * per_e;
     mp = rem / n_tiles;
     nt = rem - mp * n_tiles;
-    const long long s0 = p.seg[e], s1 = p.seg[e + 1];
+    if (e != cur.e) {
+      cur.e = e;
+      cur.lo = p.seg[e];
+      cur.hi = p.seg[e + 1];
+    }
+    const long long s0 = cur.lo, s1 = cur.hi;
     if (s1 < s0 || ((s1 - s0) % Cfg<KIND>::kElemsPerKB) != 0) *bad = 1;
     k.num_kb = s1 > s0 ? (int)((s1 - s0) / Cfg<KIND>::kElemsPerKB) : 0;
     k.row_pair = mp * 2 * BM;
@@ -150,17 +164,24 @@ MPM_DEV Task task_of(const GemmArgs& p, long long t, int n_tiles, int* bad) {
     mp = t / n_tiles;
     nt = t - mp * n_tiles;
     k.row_pair = mp * 2 * BM;
-    long long seg_end = p.a_rows;
-    if (p.seg) seg_end = p.seg[p.E];
-    if (k.row_pair >= seg_end) { k.valid = false; return k; }
     if (p.seg) {
-      int lo = 0, hi = p.E - 1;
-      while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (p.seg[mid] <= k.row_pair) lo = mid; else hi = mid - 1;
+      if (cur.end < 0) {
+        cur.end = p.seg[p.E];
+        cur.e = 0;
+        cur.lo = p.seg[0];
+        cur.hi = p.seg[1];
       }
-      e = lo;
-      if ((p.seg[e] & 255) != 0 || (p.seg[e + 1] & 255) != 0) *bad = 1;   // not pair-aligned
+      if (k.row_pair >= cur.end) { k.valid = false; return k; }
+      while (cur.e + 1 < p.E && cur.hi <= k.row_pair) {
+        ++cur.e;
+        cur.lo = cur.hi;
+        cur.hi = p.seg[cur.e + 1];
+      }
+      e = cur.e;
+      if ((cur.lo & 255) != 0 || (cur.hi & 255) != 0) *bad = 1;   // not pair-aligned
+    } else if (k.row_pair >= p.a_rows) {
+      k.valid = false;
+      return k;
     }
     k.out_row = k.row_pair;
     k.n0 = nt * (swiglu ? BN / 2 : BN);
@@ -258,8 +279,9 @@ grouped_gemm_pair_kernel(const __grid_constant__ PairMaps maps, const GemmArgs p
   if (warp == 0 && lane == 0) {
     // ======================================================== TMA producer (both CTAs)
     uint32_t it = 0;
+    SegCursor cur;
     for (long long t = cid; t < n_tasks; t += ncl) {
-      const Task k = task_of<KIND, EPI>(p, t, n_tiles, &bad);
+      const Task k = task_of<KIND, EPI>(p, t, n_tiles, &bad, cur);
       if (!k.valid) break;
       const long long a_row = k.row_pair + rank * BM;
       const long long sfa_rt = a_row >> 7;
@@ -308,8 +330,9 @@ grouped_gemm_pair_kernel(const __grid_constant__ PairMaps maps, const GemmArgs p
     // ======================================================== MMA issuer (leader only)
     uint32_t it = 0, j = 0;
     bool ok = true;
+    SegCursor cur;
     for (long long t = cid; ok && t < n_tasks; t += ncl) {
-      const Task k = task_of<KIND, EPI>(p, t, n_tiles, &bad);
+      const Task k = task_of<KIND, EPI>(p, t, n_tiles, &bad, cur);
       if (!k.valid) break;
       if (k.num_kb == 0) continue;             // empty reduction: nothing to accumulate
       const uint32_t ab = j % NACC, use = j / NACC;
@@ -356,8 +379,9 @@ grouped_gemm_pair_kernel(const __grid_constant__ PairMaps maps, const GemmArgs p
     const int part = (warp == 2) ? 0 : 1;
     uint32_t it = 0;
     bool ok = true;
+    SegCursor cur;
     for (long long t = cid; ok && t < n_tasks; t += ncl) {
-      const Task k = task_of<KIND, EPI>(p, t, n_tiles, &bad);
+      const Task k = task_of<KIND, EPI>(p, t, n_tiles, &bad, cur);
       if (!k.valid) break;
       for (int kb = 0; kb < k.num_kb; ++kb, ++it) {
         const int s = it % S;
@@ -401,8 +425,9 @@ grouped_gemm_pair_kernel(const __grid_constant__ PairMaps maps, const GemmArgs p
     const uint32_t acce_leader1 = NACC > 1 ? map_to_rank(bar_acc + 16 + 8, 0) : acce_leader0;
     const bool leader_thread = (threadIdx.x == EPI_WARP0 * 32);
     uint32_t j = 0;
+    SegCursor cur;
     for (long long t = cid; t < n_tasks; t += ncl) {
-      const Task k = task_of<KIND, EPI>(p, t, n_tiles, &bad);
+      const Task k = task_of<KIND, EPI>(p, t, n_tiles, &bad, cur);
       if (!k.valid) break;
       const long long orow = k.out_row + rank * BM;          // this CTA's first output row
       if (k.num_kb == 0) {

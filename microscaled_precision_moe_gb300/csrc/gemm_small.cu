@@ -69,22 +69,39 @@ struct SmallMaps {
   CUtensorMap a, b;   // routed rows (A) and weights (B), 128 x 128-byte boxes
 };
 
+// A role's cached view of the segment offsets: its tasks come in increasing
+// row order, so a cursor moving forward over the offsets finds each task's
+// expert (every offset read once per role, instead of a binary search of
+// dependent global reads per task).
+struct SegCursor {
+  int e = -1;
+  long long lo = 0, hi = 0, end = -1;
+};
+
 // task t -> chunk of 128 routed rows and weight tile; false past the last row
 MPM_DEV bool small_task(const GemmArgs& p, long long t, int n_wt, long long* r0, int* e, int* wt,
-                        int* bad) {
+                        int* bad, SegCursor& cur) {
   const long long ci = t / n_wt;
   *wt = (int)(t - ci * n_wt);
   *r0 = ci * BR;
-  const long long end = p.seg ? p.seg[p.E] : p.a_rows;
-  if (*r0 >= end || *r0 >= p.a_rows) return false;
+  if (cur.end < 0) {
+    cur.end = p.seg ? p.seg[p.E] : p.a_rows;
+    if (p.seg) {
+      cur.e = 0;
+      cur.lo = p.seg[0];
+      cur.hi = p.seg[1];
+    }
+  }
+  if (*r0 >= cur.end || *r0 >= p.a_rows) return false;
   int lo = 0;
   if (p.seg) {
-    int hi = p.E - 1;
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (p.seg[mid] <= *r0) lo = mid; else hi = mid - 1;
+    while (cur.e + 1 < p.E && cur.hi <= *r0) {
+      ++cur.e;
+      cur.lo = cur.hi;
+      cur.hi = p.seg[cur.e + 1];
     }
-    if ((p.seg[lo] & (BR - 1)) != 0 || (p.seg[lo + 1] & (BR - 1)) != 0) *bad = 1;
+    lo = cur.e;
+    if ((cur.lo & (BR - 1)) != 0 || (cur.hi & (BR - 1)) != 0) *bad = 1;
   }
   *e = lo;
   return true;
@@ -142,9 +159,10 @@ grouped_gemm_small_kernel(const __grid_constant__ SmallMaps maps, const GemmArgs
     // ======================================================== TMA producer
     uint32_t it = 0;
     bool ok = true;
+    SegCursor cur;
     for (long long t = blockIdx.x; ok && t < n_tasks; t += gridDim.x) {
       long long r0; int e, wt;
-      if (!small_task(p, t, n_wt, &r0, &e, &wt, &bad)) break;
+      if (!small_task(p, t, n_wt, &r0, &e, &wt, &bad, cur)) break;
       const long long wrow0 = (long long)e * p.b_rows_per_e + (long long)wt * BW;
       const long long wrow1 = wrow0 + p.N / 2;                // up rows (SwiGLU)
       for (int kb = 0; kb < num_kb; ++kb, ++it) {
@@ -181,9 +199,10 @@ grouped_gemm_small_kernel(const __grid_constant__ SmallMaps maps, const GemmArgs
     uint32_t it = 0, j = 0;
     bool ok = true;
     const uint32_t idesc_base = idesc_block_scaled(KC::kFmt, BR, KC::kUe8m0, 0, 128);
+    SegCursor cur;
     for (long long t = blockIdx.x; ok && t < n_tasks; t += gridDim.x) {
       long long r0; int e, wt;
-      if (!small_task(p, t, n_wt, &r0, &e, &wt, &bad)) break;
+      if (!small_task(p, t, n_wt, &r0, &e, &wt, &bad, cur)) break;
       const uint32_t ab = (C::kNacc > 1) ? (j & 1u) : 0u;
       const uint32_t use = (C::kNacc > 1) ? (j >> 1) : j;
       if (!mbar_wait(bar_acc + 16 * ab + 8, (use & 1u) ^ 1u, p.status)) break;
@@ -231,9 +250,10 @@ grouped_gemm_small_kernel(const __grid_constant__ SmallMaps maps, const GemmArgs
     const int q = warp & 3;                       // TMEM lane quarter
     const uint32_t lane_off = (uint32_t)(q * 32) << 16;
     uint32_t j = 0;
+    SegCursor cur;
     for (long long t = blockIdx.x; t < n_tasks; t += gridDim.x) {
       long long r0; int e, wt;
-      if (!small_task(p, t, n_wt, &r0, &e, &wt, &bad)) break;
+      if (!small_task(p, t, n_wt, &r0, &e, &wt, &bad, cur)) break;
       const uint32_t ab = (C::kNacc > 1) ? (j & 1u) : 0u;
       const uint32_t use = (C::kNacc > 1) ? (j >> 1) : j;
       const bool w_ok = mbar_wait(bar_acc + 16 * ab, use & 1u, p.status);
