@@ -8,7 +8,10 @@
 //   * each CTA stages its own 128 rows of A and its own half of B (128 of the
 //     256 B rows) plus the scale tiles of its A rows and of all 256 B rows;
 //     every TMA load, the peer's included, completes on the leader CTA's
-//     barrier (cp.async.bulk.tensor .cta_group::2);
+//     barriers (cp.async.bulk.tensor .cta_group::2).  A stage's scale tiles
+//     are loaded first and complete on a barrier of their own, so their
+//     copies into TMEM overlap the flight of the A and B tiles (the ring is
+//     bound by the latency of one stage's round trip, not by bandwidth);
 //   * copy warps of the leader copy the scale tiles of both CTAs into their
 //     tensor memories (tcgen05.cp.cta_group::2) and signals a per-stage
 //     barrier; the leader's MMA thread waits on it and issues
@@ -36,11 +39,9 @@ namespace pairk {
 constexpr int BM = 128;              // rows per CTA; 256 per pair
 constexpr int BN = 256;
 constexpr int BKB = 128;             // bytes of K per stage
-// warp 0 TMA, warp 1 MMA + TMEM allocation, warps 2 and 11 scale-tile copies
-// (six tcgen05.cp each per NVFP4 stage), warps 3-10 epilogue (two warps per
-// TMEM lane quarter, each half the columns)
-constexpr int NTHREADS = 384;
-constexpr int SF_WARP2 = 11;         // second scale-copy warp
+// warp 0 TMA, warp 1 MMA + TMEM allocation, warp 2 and warps 11, 12, ...
+// scale-tile copies (Cfg::kCopyWarps threads), warps 3-10 epilogue (two warps
+// per TMEM lane quarter, each half the columns)
 constexpr int EPI_WARP0 = 3;
 constexpr int EPI_THREADS = 256;
 constexpr int A_STAGE = BM * BKB;    // 16 KB
@@ -49,9 +50,11 @@ constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t SF_TMEM_BASE = 256;
 
 template <int KIND> struct Cfg;
-// Stage counts: the ring is latency-bound (TMA issue to data about 2k
-// cycles, data to scale tiles in TMEM about 0.9k more), so it holds as many
-// stages as shared memory allows next to the 32 KB output staging.
+// Stage counts: the ring holds as many stages as shared memory allows next to
+// the 32 KB output staging.  Copy warps: the tensor pipe accepts tcgen05.cp
+// instructions from several threads faster than from one, and an NVFP4 stage
+// needs twelve of them (three warps; more would cap every thread at 128
+// registers and spill the wider epilogues); MXFP8 needs three per stage.
 template <> struct Cfg<MPM_KIND_NVFP4> {
   static constexpr int kElemsPerKB = 256;
   static constexpr int kAtomsPerKB = 4;
@@ -59,6 +62,7 @@ template <> struct Cfg<MPM_KIND_NVFP4> {
   static constexpr int kSfbBytes = 2 * 4 * 512;
   static constexpr int kSfTmemPerStage = 16 + 32;
   static constexpr int kStages = 5;
+  static constexpr int kCopyWarps = 3;
   static constexpr uint32_t kFmt = 1, kUe8m0 = 0;
 };
 template <> struct Cfg<MPM_KIND_MXFP8> {
@@ -68,6 +72,7 @@ template <> struct Cfg<MPM_KIND_MXFP8> {
   static constexpr int kSfbBytes = 2 * 512;
   static constexpr int kSfTmemPerStage = 4 + 8;
   static constexpr int kStages = 5;
+  static constexpr int kCopyWarps = 2;
   static constexpr uint32_t kFmt = 0, kUe8m0 = 1;
 };
 // bf16 operands (the high-precision / dequantized backward): 64 elements per
@@ -79,6 +84,7 @@ template <> struct Cfg<MPM_KIND_BF16> {
   static constexpr int kSfbBytes = 0;
   static constexpr int kSfTmemPerStage = 0;
   static constexpr int kStages = 6;
+  static constexpr int kCopyWarps = 2;     // idle: no scale tiles
   static constexpr uint32_t kFmt = 0, kUe8m0 = 0;
 };
 
@@ -210,8 +216,11 @@ struct PairMaps {
 // the weight-gradient A), bit 1 = B stored MN-major ([K rows, N]).  An
 // MN-major operand is staged as two 64-element-wide boxes of 64 K rows each
 // (128 bytes x 64 rows, 128-byte swizzle) per 128 rows of M or N.
+template <int KIND>
+constexpr int nthreads() { return 32 * (10 + Cfg<KIND>::kCopyWarps); }
+
 template <int KIND, int EPI, int MAJ>
-__global__ void __launch_bounds__(NTHREADS, 1)
+__global__ void __launch_bounds__(nthreads<KIND>(), 1)
 grouped_gemm_pair_kernel(const __grid_constant__ PairMaps maps, const GemmArgs p, const int n_tiles,
                          const long long n_tasks) {
   using C = Cfg<KIND>;
@@ -242,6 +251,7 @@ grouped_gemm_pair_kernel(const __grid_constant__ PairMaps maps, const GemmArgs p
   const uint32_t sTmem = bar_acc + 32;
   const uint32_t sFlag = sTmem + 8;
   const uint32_t bar_sf = bar_acc + 48;        // scale tiles of a stage are in TMEM
+  const uint32_t bar_sfull = bar_sf + 8 * S;   // scale tiles of a stage are in shared memory
   volatile uint32_t* tmem_holder = reinterpret_cast<volatile uint32_t*>(gbase + (sTmem - base));
   volatile int* fail_flag = reinterpret_cast<volatile int*>(gbase + (sFlag - base));
 
@@ -254,7 +264,10 @@ grouped_gemm_pair_kernel(const __grid_constant__ PairMaps maps, const GemmArgs p
       mbar_init(bar_acc + 16 * b, 1);
       mbar_init(bar_acc + 16 * b + 8, 16);  // one arrive per epilogue warp of both CTAs
     }
-    for (int s = 0; s < S; ++s) mbar_init(bar_sf + 8 * s, 2);   // both copy warps
+    for (int s = 0; s < S; ++s) {
+      mbar_init(bar_sf + 8 * s, C::kCopyWarps);    // every copy warp
+      mbar_init(bar_sfull + 8 * s, 1);
+    }
     *fail_flag = 0;
     fence_mbar_init();
     fence_proxy_async();
@@ -290,10 +303,27 @@ grouped_gemm_pair_kernel(const __grid_constant__ PairMaps maps, const GemmArgs p
         const int s = it % S;
         const uint32_t ph = (it / S) & 1u;
         if (!mbar_wait_cluster(bar_empty + 8 * s, ph ^ 1u, p.status)) { ok = false; break; }
-        if (rank == 0) mbar_arrive_expect_tx(bar_full + 8 * s, 2 * stage_bytes<KIND>());
-        const uint32_t fb = map_to_rank(bar_full + 8 * s, 0);   // the leader's barrier
+        // the stage's scale tiles go first, on their own barrier: the copy
+        // warps move them into TMEM while A and B are still in flight
+        if (rank == 0) {
+          if (KIND != MPM_KIND_BF16)
+            mbar_arrive_expect_tx(bar_sfull + 8 * s, 2 * (C::kSfaBytes + C::kSfbBytes));
+          mbar_arrive_expect_tx(bar_full + 8 * s, 2 * (A_STAGE + B_STAGE));
+        }
+        const uint32_t fb = map_to_rank(bar_full + 8 * s, 0);   // the leader's barriers
         const long long ka = k.ka0 + (long long)kb * C::kElemsPerKB;
         const long long kbb = k.kb0 + (long long)kb * C::kElemsPerKB;
+        if (KIND != MPM_KIND_BF16) {
+          const uint32_t fsb = map_to_rank(bar_sfull + 8 * s, 0);
+          const long long atom_a = (KIND == MPM_KIND_NVFP4) ? ka / 64 : ka / 128;
+          const long long atom_b = (KIND == MPM_KIND_NVFP4) ? kbb / 64 : kbb / 128;
+          tma_load_2d_pair(sSFA + s * C::kSfaBytes, &maps.sfa, 0,
+                           (int)(sfa_rt * (p.sfa_cols_pad >> 2) + atom_a), fsb);
+#pragma unroll
+          for (int h = 0; h < 2; ++h)
+            tma_load_2d_pair(sSFB + s * C::kSfbBytes + h * (C::kSfbBytes / 2), &maps.sfb, 0,
+                             (int)((k.brow[h] >> 7) * (p.sfb_cols_pad >> 2) + atom_b), fsb);
+        }
         // x coordinates in bytes: 128-byte multiples for every kind
         const int xa = (int)(KIND == MPM_KIND_NVFP4 ? ka / 2 : (KIND == MPM_KIND_BF16 ? ka * 2 : ka));
         const int xb =
@@ -314,15 +344,6 @@ grouped_gemm_pair_kernel(const __grid_constant__ PairMaps maps, const GemmArgs p
         } else {
           tma_load_2d_pair(sB + s * B_STAGE, &maps.b, xb, (int)k.brow[rank], fb);
         }
-        if (KIND == MPM_KIND_BF16) continue;
-        const long long atom_a = (KIND == MPM_KIND_NVFP4) ? ka / 64 : ka / 128;
-        const long long atom_b = (KIND == MPM_KIND_NVFP4) ? kbb / 64 : kbb / 128;
-        tma_load_2d_pair(sSFA + s * C::kSfaBytes, &maps.sfa, 0,
-                         (int)(sfa_rt * (p.sfa_cols_pad >> 2) + atom_a), fb);
-#pragma unroll
-        for (int h = 0; h < 2; ++h)
-          tma_load_2d_pair(sSFB + s * C::kSfbBytes + h * (C::kSfbBytes / 2), &maps.sfb, 0,
-                           (int)((k.brow[h] >> 7) * (p.sfb_cols_pad >> 2) + atom_b), fb);
       }
       if (!ok) break;
     }
@@ -342,10 +363,11 @@ grouped_gemm_pair_kernel(const __grid_constant__ PairMaps maps, const GemmArgs p
       tc_fence_after();
       for (int kb = 0; kb < k.num_kb; ++kb, ++it) {
         const int s = it % S;
-        // block-scaled kinds wait for the stage's scale tiles in TMEM (the copy
-        // warps wait for the TMA); bf16 waits for the TMA itself
-        const uint32_t ready = (KIND == MPM_KIND_BF16) ? bar_full + 8 * s : bar_sf + 8 * s;
-        if (!mbar_wait_cluster(ready, (it / S) & 1u, p.status)) { ok = false; break; }
+        // A and B in shared memory; for the block-scaled kinds also the
+        // stage's scale tiles in TMEM (the copy warps signal it)
+        if (!mbar_wait_cluster(bar_full + 8 * s, (it / S) & 1u, p.status)) { ok = false; break; }
+        if (KIND != MPM_KIND_BF16 &&
+            !mbar_wait_cluster(bar_sf + 8 * s, (it / S) & 1u, p.status)) { ok = false; break; }
         tc_fence_after();
         const uint32_t sf_col = tmem + SF_TMEM_BASE + s * C::kSfTmemPerStage;
 #pragma unroll
@@ -371,12 +393,13 @@ grouped_gemm_pair_kernel(const __grid_constant__ PairMaps maps, const GemmArgs p
         if (kb + 1 == k.num_kb) tc_commit_pair(bar_acc + 16 * ab, (uint16_t)3);
       }
     }
-  } else if ((warp == 2 || warp == SF_WARP2) && lane == 0 && rank == 0 && KIND != MPM_KIND_BF16) {
+  } else if ((warp == 2 || warp >= 11) && lane == 0 && rank == 0 && KIND != MPM_KIND_BF16) {
     // ======================================================== scale-tile copies (leader only)
-    // Two threads in two warps each copy half of a stage's scale tiles (one
-    // thread's tcgen05.cp instructions issue one after another) and each
-    // commit to the stage's barrier (count 2).
-    const int part = (warp == 2) ? 0 : 1;
+    // kCopyWarps threads in as many warps each copy a share of a stage's
+    // scale tiles (one thread's tcgen05.cp instructions issue one after
+    // another) and each commit to the stage's barrier (count kCopyWarps).
+    constexpr int NCP = C::kCopyWarps;
+    const int part = (warp == 2) ? 0 : warp - 10;    // 0 .. NCP-1
     uint32_t it = 0;
     bool ok = true;
     SegCursor cur;
@@ -385,14 +408,15 @@ grouped_gemm_pair_kernel(const __grid_constant__ PairMaps maps, const GemmArgs p
       if (!k.valid) break;
       for (int kb = 0; kb < k.num_kb; ++kb, ++it) {
         const int s = it % S;
-        if (!mbar_wait_cluster(bar_full + 8 * s, (it / S) & 1u, p.status)) { ok = false; break; }
+        if (!mbar_wait_cluster(bar_sfull + 8 * s, (it / S) & 1u, p.status)) { ok = false; break; }
         tc_fence_after();
         const uint32_t sf_col = tmem + SF_TMEM_BASE + s * C::kSfTmemPerStage;
         if (KIND == MPM_KIND_NVFP4) {
-          // 12 atoms: SFA ks 0..3, SFB (h, ks); part 0 takes SFA + SFB(h=0, ks<2), part 1 the rest
+          // 12 atoms: SFA ks 0..3 (a = 0..3), SFB (h, ks) (a = 4..11); part p
+          // takes atoms p, p + NCP, ...
 #pragma unroll
-          for (int i = 0; i < 6; ++i) {
-            const int a = part * 6 + i;          // 0..11
+          for (int i = 0; i < 12 / NCP; ++i) {
+            const int a = part + i * NCP;        // 0..11
             if (a < 4) {
               tc_cp_32x128b_x4_pair(sf_col + a * 4, sdesc_sf(sSFA + s * C::kSfaBytes + a * 512));
             } else {
@@ -403,13 +427,16 @@ grouped_gemm_pair_kernel(const __grid_constant__ PairMaps maps, const GemmArgs p
             }
           }
         } else {
-          if (part == 0) {
-            tc_cp_32x128b_x4_pair(sf_col, sdesc_sf(sSFA + s * C::kSfaBytes));
-          } else {
+          // three atoms: SFA, SFB h = 0, 1
 #pragma unroll
-            for (int h = 0; h < 2; ++h)
-              tc_cp_32x128b_x4_pair(sf_col + 4 + h * 4, sdesc_sf(sSFB + s * C::kSfbBytes + h * 512));
-          }
+          for (int a = 0; a < 3; ++a)
+            if (a % NCP == part) {
+              if (a == 0)
+                tc_cp_32x128b_x4_pair(sf_col, sdesc_sf(sSFA + s * C::kSfaBytes));
+              else
+                tc_cp_32x128b_x4_pair(sf_col + 4 + (a - 1) * 4,
+                                      sdesc_sf(sSFB + s * C::kSfbBytes + (a - 1) * 512));
+            }
         }
         asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];"
                      :: "r"(bar_sf + 8 * s) : "memory");
@@ -726,7 +753,7 @@ static cudaError_t launch_pair_one(const pairk::PairMaps& maps, const GemmArgs& 
   attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
-  cfg.blockDim = dim3(pairk::NTHREADS, 1, 1);
+  cfg.blockDim = dim3(pairk::nthreads<KIND>(), 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cfg.attrs = attr;
