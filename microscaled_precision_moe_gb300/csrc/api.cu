@@ -93,7 +93,8 @@ bool make_sf_tmap(CUtensorMap* m, const void* base, long long atoms, int atoms_p
 }
 
 // [rows, cols] bf16 input with row pitch `ld` elements, box_cols x box_rows
-// boxes without swizzle (rows land 2 * box_cols bytes apart in shared memory);
+// boxes (rows land 2 * box_cols bytes apart in shared memory; a 128-byte wide
+// box with the 128-byte swizzle: 16-byte chunk c of row r at chunk c ^ (r % 8));
 // out-of-range elements read as zero
 bool make_bf16_tmap(CUtensorMap* m, const void* base, long long cols, long long rows, long long ld,
                     unsigned box_cols, unsigned box_rows) {
@@ -104,7 +105,8 @@ bool make_bf16_tmap(CUtensorMap* m, const void* base, long long cols, long long 
   cuuint32_t box[2] = {box_cols, box_rows};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
-                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  box_cols * 2 == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }

@@ -277,9 +277,10 @@ MPM_DEV uint32_t absmax_bf16x2_packed(const uint32_t (&w)[N]) {
 // the next tiles in flight while a tile is encoded from shared memory (two
 // stages, 33 KB per CTA: six CTAs per SM, measured faster than three stages
 // at four CTAs).
-// Row pass: four lanes per 32-element row block (16 bytes each), so a warp
-// reads 512 contiguous bytes per step; the block amax is reduced across the
-// four lanes.  Column pass: one 32-row column block per thread.
+// Row pass: one thread per 32-element row block (its 64 bytes in four
+// 16-byte loads).  Column pass: a pair of adjacent columns x 16 rows per thread
+// (two threads per pair of 32-row column blocks, see below).  The tile is
+// staged with the 128-byte swizzle.
 constexpr int MQ_TM = 128, MQ_TK = 64, MQ_STAGES = 2;
 constexpr int MQ_TILE_BYTES = MQ_TM * MQ_TK * 2;     // 16 KB
 
@@ -315,62 +316,101 @@ __global__ void __launch_bounds__(256) mxfp8_quant_tma_kernel(const __grid_const
     const uint8_t* tile = gbase + s * MQ_TILE_BYTES;          // row r at r * 128 bytes
     const long long m0 = (ti / n_kt) * MQ_TM, k0 = (ti % n_kt) * MQ_TK;
     if (p.flags & MPM_ROWWISE) {
+      // one thread per 32-element row block: warp w takes rows 16 w .. 16 w + 15,
+      // lanes 2 i and 2 i + 1 the two blocks of row 16 w + i; with the swizzle
+      // each of the four 16-byte loads is four conflict-free wavefronts
+      const int rr = warp * 16 + (lane >> 1), bl = lane & 1;
+      const long long row = m0 + rr, col = k0 + bl * 32;
+      uint32_t w[16];
 #pragma unroll
-      for (int step = 0; step < 4; ++step) {
-        const int rr = (warp * 4 + step) * 4 + (lane >> 3);   // row within the tile
-        const int bl = (lane >> 2) & 1, q = lane & 3;         // row block, quarter
-        const long long row = m0 + rr, col = k0 + bl * 32 + q * 8;
-        const uint4 u = *reinterpret_cast<const uint4*>(tile + rr * 128 + bl * 64 + q * 16);
-        const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
-        uint32_t m = absmax_bf16x2_packed(w4);
-        m = max(m, __shfl_xor_sync(0xffffffffu, m, 1));
-        m = max(m, __shfl_xor_sync(0xffffffffu, m, 2));
-        if (row < M_eff && k0 + bl * 32 < p.K) {
-          const int e = mx_exponent(m << 16);
-          const uint64_t sc2 = f32x2_splat(pow2_neg(e));
-          const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-          uint32_t o[2];
-#pragma unroll
-          for (int j = 0; j < 2; ++j)
-            o[j] = e4m3x2_scaled(w[2 * j], sc2) | (e4m3x2_scaled(w[2 * j + 1], sc2) << 16);
-          *reinterpret_cast<uint2*>(p.row_q + row * p.K + col) = make_uint2(o[0], o[1]);
-          if (q == 0) p.row_s[sf_offset(row, col >> 5, p.row_s_cols_pad)] = (uint8_t)(e + 127);
-        }
+      for (int c = 0; c < 4; ++c) {
+        const uint4 u = *reinterpret_cast<const uint4*>(
+            tile + rr * 128 + ((((bl << 2) | c) ^ (rr & 7)) << 4));
+        w[4 * c] = u.x; w[4 * c + 1] = u.y; w[4 * c + 2] = u.z; w[4 * c + 3] = u.w;
+      }
+      if (row < M_eff && col < p.K) {
+        const int e = mx_exponent(absmax_bf16x2_packed(w) << 16);
+        uint32_t o[8];
+        mx_encode32(w, pow2_neg(e), o);
+        uint4* d = reinterpret_cast<uint4*>(p.row_q + row * p.K + col);
+        d[0] = make_uint4(o[0], o[1], o[2], o[3]);
+        d[1] = make_uint4(o[4], o[5], o[6], o[7]);
+        p.row_s[sf_offset(row, col >> 5, p.row_s_cols_pad)] = (uint8_t)(e + 127);
       }
     }
     if (p.flags & MPM_COLWISE) {
-      const int c = t & 63, g = t >> 6;
-      const long long col = k0 + c, mb = m0 + g * 32;
+      // Thread = a pair of adjacent columns x 16 of a 32-row block: warp w
+      // takes row block w / 2 and column pairs 16 (w % 2) .. + 15; the two
+      // lanes of a pair split the block's rows by bit 2 (rows 8a + b and
+      // 8a + 4 + b, b < 4), so at each load the warp's two halves read rows
+      // whose 128-byte swizzle differs by 4 chunks: 32 lanes, 32 banks.
+      const int g = warp >> 1, half = lane & 1;
+      const int cp = (warp & 1) * 16 + (lane >> 1);      // column pair 0..31
+      const long long mb = m0 + g * 32;
+      const long long nvalid = M_eff - mb;
+      const int chunk = cp >> 2, within = (cp & 3) * 4;
+      // row 32 g + 8 a + 4 half + b sits at lane_base + 1024 a + 128 b +
+      // swizzled chunk offset; the four offsets (b = 0..3) are fixed per lane
+      const uint8_t* lane_base = tile + g * 4096 + half * 512 + within;
+      int off[4];
+#pragma unroll
+      for (int b = 0; b < 4; ++b) off[b] = ((chunk ^ (half * 4 + b)) << 4) + b * 128;
+      uint32_t wv[16];                                  // row r: (col 2cp, col 2cp + 1)
+#pragma unroll
+      for (int j = 0; j < 16; ++j)
+        wv[j] = *reinterpret_cast<const uint32_t*>(lane_base + (j >> 2) * 1024 + off[j & 3]);
+      if (nvalid < 32) {                                // rows past the valid count
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+          if ((j >> 2) * 8 + half * 4 + (j & 3) >= nvalid) wv[j] = 0;
+      }
+      uint32_t m = 0;
+      {
+        __nv_bfloat162 acc = __habs2(*reinterpret_cast<const __nv_bfloat162*>(&wv[0]));
+#pragma unroll
+        for (int j = 1; j < 16; ++j)
+          acc = __hmax2(acc, __habs2(*reinterpret_cast<const __nv_bfloat162*>(&wv[j])));
+        m = *reinterpret_cast<uint32_t*>(&acc);
+      }
+      const uint32_t mo = __shfl_xor_sync(0xffffffffu, m, 1);
+      // this lane's column (2cp + half) exponent; the partner's by shuffle
+      const uint32_t mine = half ? max(m >> 16, mo >> 16) : max(m & 0xFFFFu, mo & 0xFFFFu);
+      const int e_own = mx_exponent(mine << 16);
+      const int e_oth = __shfl_xor_sync(0xffffffffu, e_own, 1);
+      const int e0 = half ? e_oth : e_own, e1 = half ? e_own : e_oth;
+      const uint64_t s0 = f32x2_splat(pow2_neg(e0)), s1 = f32x2_splat(pow2_neg(e1));
+      // codes of four consecutive rows per word: column 2cp in p0, 2cp + 1 in p1
+      uint32_t p0[4], p1[4];
+#pragma unroll
+      for (int a = 0; a < 4; ++a) {
+        const uint32_t x0 = wv[4 * a], x1 = wv[4 * a + 1], x2 = wv[4 * a + 2], x3 = wv[4 * a + 3];
+        p0[a] = e4m3x2_scaled(__byte_perm(x0, x1, 0x5410), s0) |
+                (e4m3x2_scaled(__byte_perm(x2, x3, 0x5410), s0) << 16);
+        p1[a] = e4m3x2_scaled(__byte_perm(x0, x1, 0x7632), s1) |
+                (e4m3x2_scaled(__byte_perm(x2, x3, 0x7632), s1) << 16);
+      }
+      // lane 0 of the pair ends with all 32 rows of column 2cp, lane 1 with
+      // column 2cp + 1: each passes the other column's words to its partner
+      uint32_t o[8];
+#pragma unroll
+      for (int a = 0; a < 4; ++a) {
+        const uint32_t got = __shfl_xor_sync(0xffffffffu, half ? p0[a] : p1[a], 1);
+        o[2 * a] = half ? got : p0[a];
+        o[2 * a + 1] = half ? p1[a] : got;
+      }
+      const long long col = k0 + 2 * cp + half;
       if (col < p.K && mb < M_eff) {
-        const long long nvalid = M_eff - mb;
-        uint32_t w[16];
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const int r0 = g * 32 + 2 * j;
-          const uint32_t lo = *reinterpret_cast<const uint16_t*>(tile + r0 * 128 + c * 2);
-          const uint32_t hi = *reinterpret_cast<const uint16_t*>(tile + (r0 + 1) * 128 + c * 2);
-          w[j] = lo | (hi << 16);
-        }
-        if (nvalid < 32) {                                   // rows past the valid count
-#pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            if (2 * j >= nvalid) w[j] &= 0xFFFF0000u;
-            if (2 * j + 1 >= nvalid) w[j] &= 0x0000FFFFu;
-          }
-        }
-        uint32_t m = absmax_bf16x2_packed(w);
-        const int e = mx_exponent(m << 16);
-        uint32_t o[8];
-        mx_encode32(w, pow2_neg(e), o);
         uint8_t* dst = p.col_q + col * p.ldc + mb;
         if (nvalid >= 32) {
           uint4* d4 = reinterpret_cast<uint4*>(dst);
           d4[0] = make_uint4(o[0], o[1], o[2], o[3]);
           d4[1] = make_uint4(o[4], o[5], o[6], o[7]);
         } else {
-          for (int j = 0; j < nvalid; ++j) dst[j] = (uint8_t)(o[j >> 2] >> (8 * (j & 3)));
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (j < nvalid) dst[j] = (uint8_t)(o[j >> 2] >> (8 * (j & 3)));
         }
-        p.col_s[sf_offset(col, mb >> 5, p.col_s_cols_pad)] = (uint8_t)(e + 127);
+        p.col_s[sf_offset(col, mb >> 5, p.col_s_cols_pad)] = (uint8_t)(e_own + 127);
       }
     }
     __syncthreads();                                  // stage s fully read
