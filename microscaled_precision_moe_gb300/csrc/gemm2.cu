@@ -7,19 +7,17 @@
 //
 //   * each CTA stages its own 128 rows of A and its own half of B (128 of the
 //     256 B rows) plus the scale tiles of its A rows and of all 256 B rows;
-//     every TMA load, the peer's included, completes on the leader CTA's
+//     the A and B loads, the peer's included, complete on the leader CTA's
 //     barriers (cp.async.bulk.tensor .cta_group::2).  A stage's scale tiles
-//     are loaded first and complete on a barrier of their own, so their
-//     copies into TMEM overlap the flight of the A and B tiles (the ring is
-//     bound by the latency of one stage's round trip, not by bandwidth);
-//   * copy warps of the leader copy the scale tiles of both CTAs into their
-//     tensor memories (tcgen05.cp.cta_group::2) and signals a per-stage
-//     barrier; the leader's MMA thread waits on it and issues
-//     tcgen05.mma.cta_group::2 (M = 256, N = 256).  Issuing the copies from
-//     their own thread lets them run alongside the previous stage's MMAs
-//     instead of in front of the next ones (one thread's tcgen05 operations
-//     execute in issue order); each SM reads only half of B from its shared
-//     memory;
+//     are loaded first, on a barrier of their own, so they reach TMEM while
+//     the A and B tiles are still in flight (the ring is bound by the latency
+//     of one stage's round trip, not by bandwidth);
+//   * NVFP4: in each CTA four warps, one per TMEM lane quarter, write the
+//     stage's twelve scale tiles into TMEM with tcgen05.st and signal the
+//     leader's per-stage barrier; MXFP8: two warps of the leader move both
+//     CTAs' three tiles with tcgen05.cp.cta_group::2.  The leader's MMA
+//     thread waits for A, B and the scales and issues tcgen05.mma.cta_group::2
+//     (M = 256, N = 256); each SM reads only half of B from its shared memory;
 //   * each CTA's eight epilogue warps (two per TMEM lane quarter, each taking
 //     half of the columns) drain its 128 x 256 accumulator; in the SwiGLU and
 //     bf16 epilogues the accumulator is released to the next tile as soon as
@@ -40,8 +38,8 @@ constexpr int BM = 128;              // rows per CTA; 256 per pair
 constexpr int BN = 256;
 constexpr int BKB = 128;             // bytes of K per stage
 // warp 0 TMA, warp 1 MMA + TMEM allocation, warp 2 and warps 11, 12, ...
-// scale-tile copies (Cfg::kCopyWarps threads), warps 3-10 epilogue (two warps
-// per TMEM lane quarter, each half the columns)
+// the scale tiles (Cfg::kSfWarps warps), warps 3-10 epilogue (two warps per
+// TMEM lane quarter, each half the columns)
 constexpr int EPI_WARP0 = 3;
 constexpr int EPI_THREADS = 256;
 constexpr int A_STAGE = BM * BKB;    // 16 KB
@@ -51,10 +49,13 @@ constexpr uint32_t SF_TMEM_BASE = 256;
 
 template <int KIND> struct Cfg;
 // Stage counts: the ring holds as many stages as shared memory allows next to
-// the 32 KB output staging.  Copy warps: the tensor pipe accepts tcgen05.cp
-// instructions from several threads faster than from one, and an NVFP4 stage
-// needs twelve of them (three warps; more would cap every thread at 128
-// registers and spill the wider epilogues); MXFP8 needs three per stage.
+// the 32 KB output staging.  Scale tiles into TMEM: an NVFP4 stage has twelve
+// 512-byte tiles, each needed replicated in all four TMEM lane quarters.  As
+// tcgen05.cp instructions (about 50 cycles of tensor-pipe issue each) they
+// held the pipe back; instead four warps, one per lane quarter, load them
+// from shared memory and write them with tcgen05.st, which leaves the MMA rate
+// untouched (kSfStore).  MXFP8's three tiles per stage stay tcgen05.cp from
+// two warps (fully hidden behind the MMAs).
 template <> struct Cfg<MPM_KIND_NVFP4> {
   static constexpr int kElemsPerKB = 256;
   static constexpr int kAtomsPerKB = 4;
@@ -62,7 +63,8 @@ template <> struct Cfg<MPM_KIND_NVFP4> {
   static constexpr int kSfbBytes = 2 * 4 * 512;
   static constexpr int kSfTmemPerStage = 16 + 32;
   static constexpr int kStages = 5;
-  static constexpr int kCopyWarps = 3;
+  static constexpr int kSfWarps = 4;       // one per TMEM lane quarter, both CTAs
+  static constexpr bool kSfStore = true;
   static constexpr uint32_t kFmt = 1, kUe8m0 = 0;
 };
 template <> struct Cfg<MPM_KIND_MXFP8> {
@@ -72,7 +74,8 @@ template <> struct Cfg<MPM_KIND_MXFP8> {
   static constexpr int kSfbBytes = 2 * 512;
   static constexpr int kSfTmemPerStage = 4 + 8;
   static constexpr int kStages = 5;
-  static constexpr int kCopyWarps = 2;
+  static constexpr int kSfWarps = 2;       // tcgen05.cp issuers, leader only
+  static constexpr bool kSfStore = false;
   static constexpr uint32_t kFmt = 0, kUe8m0 = 1;
 };
 // bf16 operands (the high-precision / dequantized backward): 64 elements per
@@ -84,7 +87,8 @@ template <> struct Cfg<MPM_KIND_BF16> {
   static constexpr int kSfbBytes = 0;
   static constexpr int kSfTmemPerStage = 0;
   static constexpr int kStages = 6;
-  static constexpr int kCopyWarps = 2;     // idle: no scale tiles
+  static constexpr int kSfWarps = 2;       // idle: no scale tiles
+  static constexpr bool kSfStore = false;
   static constexpr uint32_t kFmt = 0, kUe8m0 = 0;
 };
 
@@ -217,7 +221,26 @@ struct PairMaps {
 // MN-major operand is staged as two 64-element-wide boxes of 64 K rows each
 // (128 bytes x 64 rows, 128-byte swizzle) per 128 rows of M or N.
 template <int KIND>
-constexpr int nthreads() { return 32 * (10 + Cfg<KIND>::kCopyWarps); }
+constexpr int nthreads() { return 32 * (10 + Cfg<KIND>::kSfWarps); }
+
+// one thread's four 32-bit values into four consecutive TMEM columns of its
+// lane (the warp's lane quarter)
+MPM_DEV void tmem_st_32x32b_x4(uint32_t taddr, const uint4& v) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};"
+               :: "r"(taddr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
+}
+MPM_DEV void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+// named barrier over `n` threads that also ORs a predicate across them
+MPM_DEV bool named_sync_or(uint32_t id, uint32_t n, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "barrier.cta.red.or.pred q, %2, %3, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r) : "r"((uint32_t)pred), "r"(id), "r"(n) : "memory");
+  return r != 0;
+}
 
 template <int KIND, int EPI, int MAJ>
 __global__ void __launch_bounds__(nthreads<KIND>(), 1)
@@ -265,7 +288,9 @@ grouped_gemm_pair_kernel(const __grid_constant__ PairMaps maps, const GemmArgs p
       mbar_init(bar_acc + 16 * b + 8, 16);  // one arrive per epilogue warp of both CTAs
     }
     for (int s = 0; s < S; ++s) {
-      mbar_init(bar_sf + 8 * s, C::kCopyWarps);    // every copy warp
+      // NVFP4: one arrive per CTA (its four store warps, after a named
+      // barrier); MXFP8: one commit per copy warp
+      mbar_init(bar_sf + 8 * s, C::kSfStore ? 2 : C::kSfWarps);
       mbar_init(bar_sfull + 8 * s, 1);
     }
     *fail_flag = 0;
@@ -303,10 +328,14 @@ grouped_gemm_pair_kernel(const __grid_constant__ PairMaps maps, const GemmArgs p
         const int s = it % S;
         const uint32_t ph = (it / S) & 1u;
         if (!mbar_wait_cluster(bar_empty + 8 * s, ph ^ 1u, p.status)) { ok = false; break; }
-        // the stage's scale tiles go first, on their own barrier: the copy
-        // warps move them into TMEM while A and B are still in flight
+        // the stage's scale tiles go first, on their own barrier: they move
+        // into TMEM while A and B are still in flight.  NVFP4: each CTA loads
+        // its own tiles on its own barrier (its store warps read them);
+        // MXFP8: the leader's barrier (its copy warps move both CTAs' tiles)
+        if (KIND != MPM_KIND_BF16 && C::kSfStore)
+          mbar_arrive_expect_tx(bar_sfull + 8 * s, C::kSfaBytes + C::kSfbBytes);
         if (rank == 0) {
-          if (KIND != MPM_KIND_BF16)
+          if (KIND != MPM_KIND_BF16 && !C::kSfStore)
             mbar_arrive_expect_tx(bar_sfull + 8 * s, 2 * (C::kSfaBytes + C::kSfbBytes));
           mbar_arrive_expect_tx(bar_full + 8 * s, 2 * (A_STAGE + B_STAGE));
         }
@@ -314,15 +343,23 @@ grouped_gemm_pair_kernel(const __grid_constant__ PairMaps maps, const GemmArgs p
         const long long ka = k.ka0 + (long long)kb * C::kElemsPerKB;
         const long long kbb = k.kb0 + (long long)kb * C::kElemsPerKB;
         if (KIND != MPM_KIND_BF16) {
-          const uint32_t fsb = map_to_rank(bar_sfull + 8 * s, 0);
           const long long atom_a = (KIND == MPM_KIND_NVFP4) ? ka / 64 : ka / 128;
           const long long atom_b = (KIND == MPM_KIND_NVFP4) ? kbb / 64 : kbb / 128;
-          tma_load_2d_pair(sSFA + s * C::kSfaBytes, &maps.sfa, 0,
-                           (int)(sfa_rt * (p.sfa_cols_pad >> 2) + atom_a), fsb);
+          const int ya = (int)(sfa_rt * (p.sfa_cols_pad >> 2) + atom_a);
+          if (C::kSfStore) {
+            tma_load_2d(sSFA + s * C::kSfaBytes, &maps.sfa, 0, ya, bar_sfull + 8 * s);
 #pragma unroll
-          for (int h = 0; h < 2; ++h)
-            tma_load_2d_pair(sSFB + s * C::kSfbBytes + h * (C::kSfbBytes / 2), &maps.sfb, 0,
-                             (int)((k.brow[h] >> 7) * (p.sfb_cols_pad >> 2) + atom_b), fsb);
+            for (int h = 0; h < 2; ++h)
+              tma_load_2d(sSFB + s * C::kSfbBytes + h * (C::kSfbBytes / 2), &maps.sfb, 0,
+                          (int)((k.brow[h] >> 7) * (p.sfb_cols_pad >> 2) + atom_b), bar_sfull + 8 * s);
+          } else {
+            const uint32_t fsb = map_to_rank(bar_sfull + 8 * s, 0);
+            tma_load_2d_pair(sSFA + s * C::kSfaBytes, &maps.sfa, 0, ya, fsb);
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+              tma_load_2d_pair(sSFB + s * C::kSfbBytes + h * (C::kSfbBytes / 2), &maps.sfb, 0,
+                               (int)((k.brow[h] >> 7) * (p.sfb_cols_pad >> 2) + atom_b), fsb);
+          }
         }
         // x coordinates in bytes: 128-byte multiples for every kind
         const int xa = (int)(KIND == MPM_KIND_NVFP4 ? ka / 2 : (KIND == MPM_KIND_BF16 ? ka * 2 : ka));
@@ -393,12 +430,59 @@ grouped_gemm_pair_kernel(const __grid_constant__ PairMaps maps, const GemmArgs p
         if (kb + 1 == k.num_kb) tc_commit_pair(bar_acc + 16 * ab, (uint16_t)3);
       }
     }
+  } else if ((warp == 2 || warp >= 11) && C::kSfStore) {
+    // ======================================================== scale tiles, tcgen05.st (both CTAs)
+    // Warp w writes TMEM lane quarter w % 4 (warps 2, 11, 12, 13: quarters
+    // 2, 3, 0, 1): lane l of each 512-byte tile (its 16-byte row l) goes to
+    // lane 32 q + l, four columns — the replicated layout the block-scaled
+    // MMA reads.  After the stores complete, the four warps meet on a named
+    // barrier and one thread arrives on the leader's stage barrier.  That
+    // arrive (from the peer CTA too) is CTA-scoped: tcgen05.wait::st has
+    // completed the TMEM stores before it executes, so it publishes no memory
+    // operation; a cluster-scoped release there cost about 2k cycles per stage
+    // and held the whole ring back (dense NVFP4 2.4 PFLOP/s instead of 6.2).
+    const int q = warp & 3;
+    const uint32_t tq = tmem + ((uint32_t)(q * 32) << 16);
+    const uint32_t sf_leader = map_to_rank(bar_sf, 0);
+    const bool arriver = (warp == 2 && lane == 0);
+    uint32_t it = 0;
+    bool ok = true;
+    SegCursor cur;
+    for (long long t = cid; ok && t < n_tasks; t += ncl) {
+      const Task k = task_of<KIND, EPI>(p, t, n_tiles, &bad, cur);
+      if (!k.valid) break;
+      for (int kb = 0; kb < k.num_kb; ++kb, ++it) {
+        const int s = it % S;
+        const bool w_ok = mbar_wait_cluster(bar_sfull + 8 * s, (it / S) & 1u, p.status);
+        if (w_ok) {
+          const uint32_t col = tq + SF_TMEM_BASE + s * C::kSfTmemPerStage;
+          const uint8_t* sa = gbase + (sSFA - base) + s * C::kSfaBytes + lane * 16;
+          const uint8_t* sb = gbase + (sSFB - base) + s * C::kSfbBytes + lane * 16;
+#pragma unroll
+          for (int a = 0; a < 4; ++a)
+            tmem_st_32x32b_x4(col + a * 4, *reinterpret_cast<const uint4*>(sa + a * 512));
+#pragma unroll
+          for (int b = 0; b < 8; ++b) {
+            const int h = b >> 2, ks = b & 3;
+            tmem_st_32x32b_x4(col + 16 + ks * 8 + h * 4,
+                              *reinterpret_cast<const uint4*>(sb + h * 2048 + ks * 512));
+          }
+          tmem_st_wait();
+        }
+        tc_fence_before();
+        // every store warp takes part in the barrier, failed wait or not
+        if (named_sync_or(3, 128, !w_ok)) { ok = false; break; }
+        if (arriver) {
+          if (rank == 0) mbar_arrive(bar_sf + 8 * s);
+          else mbar_arrive_cluster(sf_leader + 8 * s);
+        }
+      }
+    }
   } else if ((warp == 2 || warp >= 11) && lane == 0 && rank == 0 && KIND != MPM_KIND_BF16) {
-    // ======================================================== scale-tile copies (leader only)
-    // kCopyWarps threads in as many warps each copy a share of a stage's
-    // scale tiles (one thread's tcgen05.cp instructions issue one after
-    // another) and each commit to the stage's barrier (count kCopyWarps).
-    constexpr int NCP = C::kCopyWarps;
+    // ======================================================== scale-tile copies (MXFP8, leader only)
+    // kSfWarps threads in as many warps each copy a share of a stage's scale
+    // tiles with tcgen05.cp and commit to the stage's barrier.
+    constexpr int NCP = C::kSfWarps;
     const int part = (warp == 2) ? 0 : warp - 10;    // 0 .. NCP-1
     uint32_t it = 0;
     bool ok = true;
@@ -411,33 +495,16 @@ grouped_gemm_pair_kernel(const __grid_constant__ PairMaps maps, const GemmArgs p
         if (!mbar_wait_cluster(bar_sfull + 8 * s, (it / S) & 1u, p.status)) { ok = false; break; }
         tc_fence_after();
         const uint32_t sf_col = tmem + SF_TMEM_BASE + s * C::kSfTmemPerStage;
-        if (KIND == MPM_KIND_NVFP4) {
-          // 12 atoms: SFA ks 0..3 (a = 0..3), SFB (h, ks) (a = 4..11); part p
-          // takes atoms p, p + NCP, ...
+        // three atoms: SFA, SFB h = 0, 1
 #pragma unroll
-          for (int i = 0; i < 12 / NCP; ++i) {
-            const int a = part + i * NCP;        // 0..11
-            if (a < 4) {
-              tc_cp_32x128b_x4_pair(sf_col + a * 4, sdesc_sf(sSFA + s * C::kSfaBytes + a * 512));
-            } else {
-              const int bidx = a - 4;            // 0..7 -> (h, ks)
-              const int h = bidx >> 2, ks = bidx & 3;
-              tc_cp_32x128b_x4_pair(sf_col + 16 + ks * 8 + h * 4,
-                                    sdesc_sf(sSFB + s * C::kSfbBytes + h * 2048 + ks * 512));
-            }
+        for (int a = 0; a < 3; ++a)
+          if (a % NCP == part) {
+            if (a == 0)
+              tc_cp_32x128b_x4_pair(sf_col, sdesc_sf(sSFA + s * C::kSfaBytes));
+            else
+              tc_cp_32x128b_x4_pair(sf_col + 4 + (a - 1) * 4,
+                                    sdesc_sf(sSFB + s * C::kSfbBytes + (a - 1) * 512));
           }
-        } else {
-          // three atoms: SFA, SFB h = 0, 1
-#pragma unroll
-          for (int a = 0; a < 3; ++a)
-            if (a % NCP == part) {
-              if (a == 0)
-                tc_cp_32x128b_x4_pair(sf_col, sdesc_sf(sSFA + s * C::kSfaBytes));
-              else
-                tc_cp_32x128b_x4_pair(sf_col + 4 + (a - 1) * 4,
-                                      sdesc_sf(sSFB + s * C::kSfbBytes + (a - 1) * 512));
-            }
-        }
         asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];"
                      :: "r"(bar_sf + 8 * s) : "memory");
       }
