@@ -310,3 +310,46 @@ def test_mxfp8_fprop_small_m():
         dref = MO.fc1_epilogue(ref, rp.cpu().numpy()[:R], I)
     _assert_close(np_bf16(d)[:R], dref, "MXFP8 small-M SwiGLU")
     assert np.array_equal(amax.cpu().numpy()[:R], np.max(np.abs(np_bf16(d)[:R]), axis=1))
+
+
+@pytest.mark.parametrize("tile_m", [256, 1])
+def test_nvfp4_grouped_with_empty_experts(tile_m):
+    """Experts 0, 3 and 7 of 8 receive no rows (empty segments at the start,
+    in the middle and at the end): the kernels' walk over the segment
+    offsets skips them and the layer still matches the oracle."""
+    base = synth.scaled(synth.MOE_30B, T=260, H=512, I=256, E=5, k=3)
+    ids5, prob = synth.routing(base, 3)
+    remap = torch.tensor([1, 2, 4, 5, 6], dtype=torch.int32)
+    ids = remap[ids5.long()]
+    E = 8
+    shape = synth.scaled(synth.MOE_30B, T=260, H=512, I=256, E=E, k=3)
+    ops, L = _ops(), _L()
+    H, I, k = shape.H, shape.I, shape.k
+    x = synth.moe_activations(shape, 3, device="cuda")
+    w1, w2 = synth.moe_weights(shape, 3, device="cuda")
+    seg, perm, inv, rp, cap = ops.moe_build_segments(ids.cuda(), prob.cuda(), E, pad=_pad(tile_m))
+    segh = seg.cpu().numpy()
+    assert segh[1] == segh[0] and segh[4] == segh[3] and segh[8] == segh[7]
+    qx, sx, tsx = ops.nvfp4_quantize_per_token(x)
+    amax = torch.full((cap,), 7.0, dtype=torch.float32, device="cuda")
+    aq, as_, ats = ops.moe_gather_nvfp4(qx, sx, tsx, H, perm, seg, E, k, cap, amax_zero=amax)
+    q1, s1, t1 = ops.nvfp4_quantize_weight([w1.contiguous()])
+    q2, s2, t2 = ops.nvfp4_quantize_weight([w2])
+    d = torch.empty(cap, I, dtype=torch.bfloat16, device="cuda")
+    ops.moe_grouped_gemm(L.KIND_NVFP4, L.GROUP_M, L.EPI_SWIGLU, E, cap, 2 * I, H, seg,
+                         aq, q1.view(E * 2 * I, H // 2), as_, H // 16, s1, H // 16, d,
+                         b_rows_per_expert=2 * I, alpha_a=ats, alpha_b=t1, row_prob=rp,
+                         out2=d, amax=amax, tile_m=tile_m)
+    qd, sd, tsd = ops.nvfp4_quantize_per_token(d, amax_in=amax, m_valid=seg[E:])
+    y = torch.empty(cap, H, dtype=torch.bfloat16, device="cuda")
+    ops.moe_grouped_gemm(L.KIND_NVFP4, L.GROUP_M, L.EPI_BF16, E, cap, H, I, seg,
+                         qd, q2.view(E * H, I // 2), sd, I // 16, s2, I // 16, y,
+                         b_rows_per_expert=H, alpha_a=tsd, alpha_b=t2, tile_m=tile_m)
+    out = ops.moe_combine(y, inv, shape.T, k)
+    torch.cuda.synchronize()
+    assert ops.get_device_status() == 0
+    with np.errstate(over="ignore"):
+        r = MO.nvfp4_moe_forward(np_bf16(x), ids.numpy(), prob.numpy(), np_bf16(w1),
+                                 np_bf16(w2), E, pad=_pad(tile_m))
+    assert np.array_equal(r["seg"], segh)
+    _chained_compare(np_bf16(d), np_bf16(y), np_bf16(out), r, k, "NVFP4 layer, empty experts")
