@@ -237,16 +237,22 @@ def test_mxfp8_grouped_fprop_dgrad_wgrad(tile_m):
     _assert_close(dw.cpu().numpy(), ref_dw, "MXFP8 wgrad")
 
 
+@pytest.mark.parametrize("empty", [False, True])
 @pytest.mark.parametrize("tile_m", [128, 256])
-def test_mxfp8_layer_fwd_bwd_api(tile_m):
+def test_mxfp8_layer_fwd_bwd_api(tile_m, empty):
     """The MXFP8 layer (forward and backward) through MXFP8MoE against the
     oracle.  FC1's outputs (C = gate|up, D) come from identical operands and
     meet the GEMM tolerance; later stages consume re-quantised tensors, so a
     one-step bf16 difference upstream can move an E4M3 code: their bound is
-    the same GEMM tolerance (measured errors are near 1e-5)."""
+    the same GEMM tolerance (measured errors are near 1e-5).  With ``empty``
+    experts 0, 3 and 7 receive no rows: their weight gradients are zero."""
     from microscaled_precision_moe_gb300.moe import MXFP8MoE
     shape = synth.scaled(synth.MOE_30B_BWD, T=384, H=512, I=256, E=8, k=4)
-    ids, prob = synth.routing(shape)
+    if empty:
+        ids5, prob = synth.routing(synth.scaled(shape, E=5))
+        ids = torch.tensor([1, 2, 4, 5, 6], dtype=torch.int32)[ids5.long()]
+    else:
+        ids, prob = synth.routing(shape)
     x = synth.moe_activations(shape, device="cuda")
     w1, w2 = synth.moe_weights(shape, device="cuda")
     dy = synth.moe_grad_out(shape, device="cuda")
@@ -261,6 +267,10 @@ def test_mxfp8_layer_fwd_bwd_api(tile_m):
         r = MO.mxfp8_moe_fwd_bwd(np_bf16(x), ids.numpy(), prob.numpy(), np_bf16(w1),
                                  np_bf16(w2), np_bf16(dy), shape.E, pad=tile_m)
     R = int(r["seg"][-1])
+    if empty:
+        segh = r["seg"]
+        assert segh[1] == segh[0] and segh[4] == segh[3] and segh[8] == segh[7]
+        assert not dw1[[0, 3, 7]].any() and not dw2[[0, 3, 7]].any()
     _assert_close(np_bf16(layer.c1)[:R], r["c1"], "MXFP8 FC1 C")
     _assert_close(np_bf16(layer.d)[:R], r["d"], "MXFP8 FC1 D")
     report = {}
