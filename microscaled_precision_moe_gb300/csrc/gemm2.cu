@@ -401,10 +401,14 @@ grouped_gemm_pair_kernel(const __grid_constant__ PairMaps maps, const GemmArgs p
       for (int kb = 0; kb < k.num_kb; ++kb, ++it) {
         const int s = it % S;
         // A and B in shared memory; for the block-scaled kinds also the
-        // stage's scale tiles in TMEM (the copy warps signal it)
-        if (!mbar_wait_cluster(bar_full + 8 * s, (it / S) & 1u, p.status)) { ok = false; break; }
+        // stage's scale tiles in TMEM (the scale warps signal it).  The
+        // leader's own barriers, waited with CTA-scoped acquire: the TMA bytes
+        // and the scale stores behind them are complete when they flip, and
+        // tcgen05.fence::after_thread_sync orders the MMAs after the wait
+        // (about 1 % faster than cluster-scoped acquire on the dense GEMM)
+        if (!mbar_wait(bar_full + 8 * s, (it / S) & 1u, p.status)) { ok = false; break; }
         if (KIND != MPM_KIND_BF16 &&
-            !mbar_wait_cluster(bar_sf + 8 * s, (it / S) & 1u, p.status)) { ok = false; break; }
+            !mbar_wait(bar_sf + 8 * s, (it / S) & 1u, p.status)) { ok = false; break; }
         tc_fence_after();
         const uint32_t sf_col = tmem + SF_TMEM_BASE + s * C::kSfTmemPerStage;
 #pragma unroll
