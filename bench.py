@@ -523,7 +523,7 @@ def main():
             return 0
         ids, prob = synth.routing(shape)
         items = _oracle_prepare(shape, ids, prob, n_experts=1)
-        for _ in range(min(args.warmup, 1)):
+        for _ in range(args.warmup):                  # the W untimed steps the line reports
             _oracle_run(shape, items)
         vals, descs = [], []
         t_all = time.perf_counter()
