@@ -386,7 +386,9 @@ grouped_gemm_pair_kernel(const __grid_constant__ PairMaps maps, const GemmArgs p
     }
   } else if (warp == 1 && lane == 0 && rank == 0) {
     // ======================================================== MMA issuer (leader only)
-    uint32_t it = 0, j = 0;
+    uint32_t j = 0;
+    int s = 0;                                 // ring stage and its phase, kept incrementally
+    uint32_t ph = 0;
     bool ok = true;
     SegCursor cur;
     for (long long t = cid; ok && t < n_tasks; t += ncl) {
@@ -398,17 +400,16 @@ grouped_gemm_pair_kernel(const __grid_constant__ PairMaps maps, const GemmArgs p
       ++j;
       const uint32_t dacc = tmem + ab * 256;
       tc_fence_after();
-      for (int kb = 0; kb < k.num_kb; ++kb, ++it) {
-        const int s = it % S;
-        // A and B in shared memory; for the block-scaled kinds also the
-        // stage's scale tiles in TMEM (the scale warps signal it).  The
-        // leader's own barriers, waited with CTA-scoped acquire: the TMA bytes
-        // and the scale stores behind them are complete when they flip, and
-        // tcgen05.fence::after_thread_sync orders the MMAs after the wait
-        // (about 1 % faster than cluster-scoped acquire on the dense GEMM)
-        if (!mbar_wait(bar_full + 8 * s, (it / S) & 1u, p.status)) { ok = false; break; }
-        if (KIND != MPM_KIND_BF16 &&
-            !mbar_wait(bar_sf + 8 * s, (it / S) & 1u, p.status)) { ok = false; break; }
+      for (int kb = 0; kb < k.num_kb; ++kb) {
+        // This thread's instruction stream paces the ring (each tcgen05.mma
+        // takes ~70 cycles to issue), so it waits on one barrier per stage
+        // where it can: NVFP4 — the scale barrier, which the leader's store
+        // warps signal only after the stage's A and B have landed too;
+        // MXFP8 — A/B and the copies' barrier; bf16 — A/B.  CTA-scoped
+        // acquire on the leader's own barriers; tcgen05.fence::after_thread_sync
+        // orders the MMAs after the wait.
+        if (!C::kSfStore && !mbar_wait(bar_full + 8 * s, ph, p.status)) { ok = false; break; }
+        if (KIND != MPM_KIND_BF16 && !mbar_wait(bar_sf + 8 * s, ph, p.status)) { ok = false; break; }
         tc_fence_after();
         const uint32_t sf_col = tmem + SF_TMEM_BASE + s * C::kSfTmemPerStage;
 #pragma unroll
@@ -432,6 +433,7 @@ grouped_gemm_pair_kernel(const __grid_constant__ PairMaps maps, const GemmArgs p
         }
         tc_commit_pair(bar_empty + 8 * s, (uint16_t)3);
         if (kb + 1 == k.num_kb) tc_commit_pair(bar_acc + 16 * ab, (uint16_t)3);
+        if (++s == S) { s = 0; ph ^= 1u; }
       }
     }
   } else if ((warp == 2 || warp >= 11) && C::kSfStore) {
@@ -473,9 +475,13 @@ grouped_gemm_pair_kernel(const __grid_constant__ PairMaps maps, const GemmArgs p
           }
           tmem_st_wait();
         }
+        // the leader's arriver also waits for the stage's A and B, so its
+        // arrive tells the MMA thread that the whole stage is ready
+        bool a_ok = true;
+        if (arriver && rank == 0) a_ok = mbar_wait(bar_full + 8 * s, (it / S) & 1u, p.status);
         tc_fence_before();
         // every store warp takes part in the barrier, failed wait or not
-        if (named_sync_or(3, 128, !w_ok)) { ok = false; break; }
+        if (named_sync_or(3, 128, !(w_ok && a_ok))) { ok = false; break; }
         if (arriver) {
           if (rank == 0) mbar_arrive(bar_sf + 8 * s);
           else mbar_arrive_cluster(sf_leader + 8 * s);
