@@ -26,6 +26,7 @@ Modules:
   quant    - MXFP8 row/column, NVFP4 per-token and joint-weight quantisers,
              the 128x4 scale-tile layout, dequantisation
   moe      - expert segments and permutation, fp64 grouped GEMMs, SwiGLU,
-             combine, the MXFP8 backward
+             combine, the MXFP8 and BF16 backward, the single-pass FC2 with
+             online amax compensation (report section 5.6)
   metrics  - relative L2, SNR, MAE, relative Frobenius error
 """

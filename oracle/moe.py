@@ -9,7 +9,9 @@ contiguous buffer, expert boundaries given by offsets, zero-token experts and
 padding handled in the same grouped path), section 5.3 (row amax accumulated
 by the producer: the permute for FC1, the weighted SwiGLU for FC2), section
 5.4 (FC1 epilogue: ACC x alpha_a[m] (x alpha_b), C = gate | up,
-D = act(gate, up) x prob, amax of D); "Towards Blackwell-native 8-bit and
+D = act(gate, up) x prob, amax of D), section 5.6 (single-pass FC2 fed tile
+by tile with a running row amax and the partial sum rescaled when the outer
+scale grows); "Towards Blackwell-native 8-bit and
 4-bit RL", section "Recipe 1 / Training" (dgrad uses the column-wise weight
 copy, wgrad the column-wise activation and gradient copies) and section
 "High-precision and dequantized backward" (backward GEMMs in BF16 on the
@@ -188,6 +190,90 @@ def nvfp4_moe_forward(x: np.ndarray, topk_ids, topk_prob, w1, w2, E: int, pad=RO
                 row_prob=row_prob, w1=(w1p, w1s, w1g), w2=(w2p, w2s, w2g),
                 acc1=acc1, d=d, amax_d=amax_d, qd=qd, sd=sd, tsd=tsd,
                 y=y_bf16, out=out)
+
+
+def nvfp4_fc2_online_amax(d: np.ndarray, seg_offsets: np.ndarray, w2q, tile_k: int = 256):
+    """FC2 of the single-pass fused FFN with online amax compensation
+    ("miniTE technical report", section 5.6).
+
+    The fused path never holds a whole row of D before FC2 consumes it: FC2
+    walks its K dimension (= I) in tiles P_i of ``tile_k`` columns as FC1 and
+    SwiGLU produce them.  Per row, in tile order:
+
+      gamax <- max(gamax, max|P_i|)      the running row amax
+      gs     = gamax / 2688             the per-token outer-scale rule
+      (s_b, q) = NVFP4 block encoding of P_i against gs (blocks of 16)
+      dO_i   = (q s_b) (q_W s_bW)^T      block scales applied, neither gs nor
+                                         the weight's tensor scale
+      O      = O * (gs_prev / gs) + dO_i,  gs_prev = gs
+
+    A row whose gamax is still 0 skips the tile (its contribution so far is
+    zero); at the end Y = O * gs_prev * s_g(W2_e), and an all-zero row gives 0.
+
+    Readings the section leaves open (each fixed here): P_i is the tile of
+    the weighted SwiGLU output rounded to bf16, i.e. the values the two-pass
+    path writes as D; gs, s_b and q follow the canonical fp32 sequence of the
+    per-token quantiser (with its 2**-116 floor) with gs in place of s_g; the
+    last tile may be shorter than ``tile_k`` (any multiple of 16); O and the
+    ratio gs_prev / gs are carried in fp64 and Y is rounded once to bf16.
+
+    d [R_pad, I] in the permuted layout; w2q = (packed [E, H, I/2], block
+    scales [E, H, I/16], s_g [E]).  Returns y (bf16 values) and y64 (before
+    rounding) [R_pad, H], the per-tile codes [R_pad, I] and block scales
+    [R_pad, I/16] the fused path would feed to FC2 (never materialised
+    there), and gs [R_pad, n_tiles].
+    """
+    d = np.asarray(d, dtype=np.float32)
+    R, I = d.shape
+    w2p, w2s, w2g = w2q
+    E, H, _ = w2p.shape
+    assert tile_k > 0 and tile_k % Q.NV_BLOCK == 0 and I % Q.NV_BLOCK == 0
+    tiles = [(c0, min(c0 + tile_k, I)) for c0 in range(0, I, tile_k)]
+    codes = np.zeros((R, I), dtype=np.uint8)
+    sb = np.zeros((R, I // Q.NV_BLOCK), dtype=np.uint8)
+    gs_tiles = np.zeros((R, len(tiles)), dtype=np.float32)
+    y64 = np.zeros((R, H))
+    for e in range(E):
+        r0, r1 = int(seg_offsets[e]), int(seg_offsets[e + 1])
+        if r1 == r0:
+            continue
+        bw = Q.nvfp4_dequantize(w2p[e], w2s[e], 1.0)         # q_W * s_bW, [H, I]
+        gamax = np.zeros(r1 - r0, dtype=np.float32)
+        gs_prev = np.zeros(r1 - r0, dtype=np.float32)
+        o = np.zeros((r1 - r0, H))
+        for i, (c0, c1) in enumerate(tiles):
+            p = d[r0:r1, c0:c1]
+            gamax = np.maximum(gamax, np.max(np.abs(p), axis=1))
+            live = gamax > 0
+            gs = Q.nvfp4_outer_scale(gamax)
+            q, s = Q.nvfp4_encode_with_outer(p, gs)
+            xs = F.e2m1_decode(q) * np.repeat(F.e4m3_decode(s), Q.NV_BLOCK, axis=1)
+            do = xs @ bw[:, c0:c1].T
+            ratio = np.zeros(r1 - r0)
+            np.divide(gs_prev.astype(np.float64), gs.astype(np.float64), out=ratio, where=live)
+            o = np.where(live[:, None], o * ratio[:, None] + do, o)
+            gs_prev = np.where(live, gs, gs_prev)
+            codes[r0:r1, c0:c1] = q
+            sb[r0:r1, c0 // Q.NV_BLOCK:c1 // Q.NV_BLOCK] = s
+            gs_tiles[r0:r1, i] = gs
+        y64[r0:r1] = o * gs_prev.astype(np.float64)[:, None] * float(w2g[e])
+    return dict(y=F.bf16_round(y64), y64=y64, codes=codes, sb=sb, gs=gs_tiles)
+
+
+def nvfp4_moe_forward_single_pass(x: np.ndarray, topk_ids, topk_prob, w1, w2, E: int,
+                                  tile_k: int = 256, pad=ROW_PAD):
+    """The NVFP4 expert layer with FC2 fed tile by tile (section 5.6 of the
+    miniTE report): the same quantised X, segments, FC1 and SwiGLU as the
+    two-pass forward, then ``nvfp4_fc2_online_amax`` on D instead of the
+    whole-row re-quantisation, then the combine.  Returns the online FC2's
+    outputs, the layer output and the two-pass forward's dict (``two_pass``)."""
+    T = x.shape[0]
+    k = np.asarray(topk_ids).shape[1]
+    r = nvfp4_moe_forward(x, topk_ids, topk_prob, w1, w2, E, pad)
+    s = nvfp4_fc2_online_amax(r["d"], r["seg"], r["w2"], tile_k)
+    s["out"] = F.bf16_round(combine(s["y"], r["inv"], T, k))
+    s["two_pass"] = r
+    return s
 
 
 def nvfp4_gemm_single(x: np.ndarray, w_gate: np.ndarray, w_up: np.ndarray):
