@@ -27,11 +27,17 @@
  *     family block-scaled tensor-core MMA reads its scale factors in.
  *
  * Errors: host-side validation failures return MPM_ERR_NULL / _SHAPE /
- * _ALIGN / _UNSUPPORTED; a failed launch returns MPM_ERR_CUDA.  Problems only
- * visible on the device (an expert offset table that is not monotone or that
- * exceeds the row capacity, a pipeline wait that ran out of time) set a
- * per-device status word and make the kernel skip the affected work (no trap,
- * no hang); read it with mpm_get_device_status().
+ * _ALIGN / _UNSUPPORTED; a failed launch returns MPM_ERR_CUDA.  Sizes must
+ * be at least 1: an empty input (no rows, no tokens, no experts) is a shape
+ * error, not a no-op, so a caller never mistakes unwritten outputs for
+ * results.  Experts that receive no rows are not an empty input: the
+ * segment, gather and GEMM calls handle them inside one call.  When several
+ * requirements are broken at once, which of their statuses is returned is
+ * not specified.  Problems only visible on the device (an expert offset
+ * table that is not monotone or that exceeds the row capacity, a pipeline
+ * wait that ran out of time) set a per-device status word and make the
+ * kernel skip the affected work (no trap, no hang); read it with
+ * mpm_get_device_status().
  */
 #ifndef MPM_H
 #define MPM_H
@@ -124,8 +130,9 @@ mpm_status mpm_mxfp8_quantize(const void* x_dev, int64_t M, int64_t K, int64_t l
  * tiles.  token_scale_dev: fp32 [M] (the s_g above).
  * m_valid_dev (nullable): as for mpm_mxfp8_quantize; rows at or beyond the
  * device row count are left untouched (their scale tiles are not written).
- * Requirements: M >= 1, K % 64 == 0, 64 <= K <= 16384, ldx % 8 == 0,
- * all pointers 16-byte aligned (token_scale_dev and amax_in_dev 4-byte).
+ * Requirements: M >= 1, K % 64 == 0, 64 <= K <= 8192, ldx >= K,
+ * ldx % 8 == 0, all pointers 16-byte aligned (token_scale_dev and
+ * amax_in_dev 4-byte).
  */
 mpm_status mpm_nvfp4_quantize_per_token(const void* x_dev, int64_t M, int64_t K,
                                         int64_t ldx, const float* amax_in_dev,
@@ -149,8 +156,10 @@ mpm_status mpm_nvfp4_quantize_per_token(const void* x_dev, int64_t M, int64_t K,
  * 128x4 tiles, expert e at byte e * mpm_scale_bytes(R, K/16).
  * tensor_scale_dev: fp32 [E] (s_g of each expert).
  * ws_dev: workspace of at least mpm_nvfp4_weight_workspace_bytes(E) bytes.
- * Requirements: nparts in 1..4, E >= 1, K % 64 == 0, 64 <= K <= 16384,
- * each part_rows[p] >= 1, R % 128 == 0.
+ * Requirements: nparts in 1..4, E >= 1, K % 64 == 0, 64 <= K <= 8192,
+ * each part_rows[p] >= 1, R % 128 == 0, ws_bytes at least
+ * mpm_nvfp4_weight_workspace_bytes(E); parts and q_dev 16-byte aligned,
+ * ws_dev and tensor_scale_dev 4-byte.
  */
 size_t mpm_nvfp4_weight_workspace_bytes(int64_t E);
 mpm_status mpm_nvfp4_quantize_weight(const void* const* parts_dev, const int64_t* part_rows,
@@ -210,7 +219,9 @@ size_t mpm_moe_segments_workspace_bytes(int64_t T, int k, int64_t E);
  * beyond seg_offsets[E]); inv_perm int32 [T*k] (flat index -> row); row_prob
  * fp32 [capacity] (0 for padding).  Rows of one expert are in ascending flat
  * index order (stable).  An id outside [0, E) sets MPM_ERR_DEVICE_BOUNDS and
- * the pair is dropped.
+ * the pair is dropped.  Requirements: T >= 1, 1 <= k <= 64, 1 <= E <= 1024,
+ * T * k <= 2^30, pad one of the values above, ws_bytes at least
+ * mpm_moe_segments_workspace_bytes(T, k, E), ws_dev 4-byte aligned.
  */
 mpm_status mpm_moe_build_segments(const int32_t* topk_ids_dev, const float* topk_prob_dev,
                                   int64_t T, int k, int64_t E, int pad,
@@ -229,7 +240,9 @@ mpm_status mpm_moe_build_segments(const int32_t* topk_ids_dev, const float* topk
  * set to 0, ready for the row-amax reduction of the FC1 epilogue.
  * Source: "miniTE technical report", section 5.3 (dispatch/permute before the
  * FC1 quantised GEMM; the padding step handles the activation and its amax
- * together).  Requirements: K % 64 == 0.
+ * together).  Requirements: T, k, E, capacity >= 1, K % 64 == 0, src and
+ * dst 16-byte aligned, the NVFP4 scale pointers 4-byte aligned (amax_zero_dev
+ * too); `what` other than the two kinds is MPM_ERR_UNSUPPORTED.
  */
 #define MPM_GATHER_BF16 0
 #define MPM_GATHER_NVFP4 1
@@ -245,7 +258,8 @@ mpm_status mpm_moe_gather(int what, const void* src_dev, const uint8_t* src_s_de
  * rounded once to bf16.  y_perm bf16 [capacity, H]; out bf16 [T, H].
  * Source: "miniTE technical report", section 5.3 (expert outputs, weighted by
  * the router, summed back per token); the router weight is applied earlier in
- * the FC1 epilogue.  Requirements: H % 8 == 0.
+ * the FC1 epilogue.  Requirements: T, k >= 1, H >= 8, H % 8 == 0, y_perm and
+ * out 16-byte aligned.
  */
 mpm_status mpm_moe_combine(const void* y_perm_dev, const int32_t* inv_perm_dev,
                            int64_t T, int k, int64_t H, void* out_dev,
@@ -269,8 +283,8 @@ mpm_status mpm_moe_combine(const void* y_perm_dev, const int32_t* inv_perm_dev,
  * rows_per_outer consecutive rows (1 for per-token activations, the rows of
  * one expert for a weight).  out_dev: bf16 [M, K], leading dimension ldo
  * elements.  m_valid_dev (nullable): device row count; rows at or beyond it
- * are not written.  Requirements: K % 64 == 0, rows_per_outer >= 1,
- * ldo >= K, ldo % 8 == 0, q / s / out 16-byte aligned.
+ * are not written.  Requirements: M >= 1, K % 64 == 0, rows_per_outer >= 1,
+ * ldo >= K, ldo % 8 == 0, q / s / out 16-byte aligned, outer 4-byte.
  */
 mpm_status mpm_nvfp4_dequantize(const uint8_t* q_dev, const uint8_t* s_dev,
                                 const float* outer_dev, int64_t rows_per_outer,
@@ -283,7 +297,8 @@ mpm_status mpm_nvfp4_dequantize(const uint8_t* q_dev, const uint8_t* s_dev,
  * Source: as above, and "Towards Blackwell-native 8-bit and 4-bit RL",
  * section "Format background / MXFP8" (blocks of 32 with an E8M0
  * power-of-two scale).  q_dev u8 [M, K]; s_dev [M, K/32] in 128x4 tiles.
- * Requirements: K % 32 == 0, ldo >= K, ldo % 8 == 0, pointers 16-byte aligned.
+ * Requirements: M >= 1, K % 32 == 0, ldo >= K, ldo % 8 == 0, pointers 16-byte
+ * aligned.
  */
 mpm_status mpm_mxfp8_dequantize(const uint8_t* q_dev, const uint8_t* s_dev, int64_t M,
                                 int64_t K, void* out_dev, int64_t ldo,

@@ -148,3 +148,65 @@ def test_dequantize_and_transpose_validation(lib):
     assert lib.mpm_transpose_bf16(fake, 0, 4, 4, fake, 4, None, None) == 2
     assert lib.mpm_transpose_bf16(fake, 8, 4, 3, fake, 8, None, None) == 2
     assert lib.mpm_transpose_bf16(fake, 8, 4, 4, fake, 7, None, None) == 2
+
+
+def test_empty_inputs_and_size_limits_are_shape_errors(lib):
+    """An empty input (no rows, tokens or experts) and every documented size
+    limit return MPM_ERR_SHAPE from the host checks, for every entry point
+    that takes sizes (CPU only: none of these calls reaches the GPU)."""
+    from microscaled_precision_moe_gb300 import _lib as L
+    fake = C.c_void_p(0x10000)
+    SHAPE = 2
+    # quantisers: no rows
+    assert lib.mpm_mxfp8_quantize(fake, 0, 64, 64, 3, fake, fake, fake, 16, fake, None, None) == SHAPE
+    assert lib.mpm_nvfp4_quantize_per_token(fake, 0, 64, 64, None, fake, fake, fake, None, None) == SHAPE
+    # NVFP4 rows longer than 8192 elements, and ldx < K
+    assert lib.mpm_nvfp4_quantize_per_token(fake, 4, 8256, 8256, None, fake, fake, fake, None, None) == SHAPE
+    assert lib.mpm_nvfp4_quantize_per_token(fake, 4, 128, 64, None, fake, fake, fake, None, None) == SHAPE
+    # joint weight quantiser: no experts, an empty part, R % 128, K > 8192,
+    # too many parts, a workspace smaller than the query returns
+    parts = (C.c_void_p * 2)(0x10000, 0x20000)
+
+    def wq(rows, nparts=2, K=256, E=4, ws=1 << 16):
+        r = (C.c_int64 * 2)(*rows)
+        return lib.mpm_nvfp4_quantize_weight(parts, r, nparts, K, E, fake, fake, fake, fake, ws, None)
+
+    assert lib.mpm_nvfp4_weight_workspace_bytes(0) == 0
+    assert wq((64, 64), E=0) == SHAPE
+    assert wq((0, 128)) == SHAPE
+    assert wq((64, 32)) == SHAPE
+    assert wq((64, 64), K=8256) == SHAPE
+    assert wq((64, 64), nparts=5) == SHAPE
+    assert wq((64, 64), ws=lib.mpm_nvfp4_weight_workspace_bytes(4) - 1) == SHAPE
+    # segments: no tokens, k out of 1..64, T * k above 2^30
+    ws = 1 << 30
+    assert lib.mpm_moe_segments_workspace_bytes(0, 8, 16) == 0
+    assert lib.mpm_moe_row_capacity(0, 8, 16, 128) == 0
+    assert lib.mpm_moe_build_segments(fake, fake, 0, 8, 16, 128, fake, fake, fake, fake, fake, ws, None) == SHAPE
+    assert lib.mpm_moe_build_segments(fake, fake, 4, 0, 16, 128, fake, fake, fake, fake, fake, ws, None) == SHAPE
+    assert lib.mpm_moe_build_segments(fake, fake, 4, 65, 16, 128, fake, fake, fake, fake, fake, ws, None) == SHAPE
+    assert lib.mpm_moe_build_segments(fake, fake, 1 << 28, 8, 16, 128, fake, fake, fake, fake, fake, ws,
+                                      None) == SHAPE
+    # gather: no tokens, no capacity, K % 64; an unknown kind is unsupported
+    g = lambda what, T, K, cap: lib.mpm_moe_gather(what, fake, fake, fake, T, K, 8, fake, fake, 16, cap,
+                                                   fake, fake, fake, None, None)
+    assert g(L.GATHER_BF16, 0, 256, 1024) == SHAPE
+    assert g(L.GATHER_BF16, 4, 256, 0) == SHAPE
+    assert g(L.GATHER_NVFP4, 4, 96, 1024) == SHAPE
+    assert g(2, 4, 256, 1024) == 4
+    # combine: no tokens, H below 8 or not a multiple of 8
+    assert lib.mpm_moe_combine(fake, fake, 0, 8, 256, fake, None) == SHAPE
+    assert lib.mpm_moe_combine(fake, fake, 4, 8, 4, fake, None) == SHAPE
+    assert lib.mpm_moe_combine(fake, fake, 4, 8, 12, fake, None) == SHAPE
+    # dequantisation and transpose: no rows / no columns
+    assert lib.mpm_nvfp4_dequantize(fake, fake, fake, 1, 0, 64, fake, 64, None, None) == SHAPE
+    assert lib.mpm_mxfp8_dequantize(fake, fake, 0, 64, fake, 64, None, None) == SHAPE
+    assert lib.mpm_transpose_bf16(fake, 4, 0, 4, fake, 4, None, None) == SHAPE
+    # grouped GEMM: no experts, no rows, no operand rows
+    for field, value in (("E", 0), ("a_rows", 0), ("a_total_rows", 0), ("b_total_rows", 0)):
+        d = _gemm_desc(L.KIND_MXFP8, L.GROUP_M, L.EPI_BF16, 256, 512, 256)
+        d.sfa_dev = d.sfb_dev = 0x10000
+        d.sfa_cols = d.sfb_cols = 16
+        d.seg_dev = 0x10000
+        setattr(d, field, value)
+        assert lib.mpm_moe_grouped_gemm(C.byref(d), None) == SHAPE, field
