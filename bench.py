@@ -13,8 +13,10 @@ step time, in TFLOP/s.  Inputs are resident in HBM and larger than L2
 (activations 470 MB, FP4 weights 5.6 GB), so no L2 flush is needed.
 Secondary lines (same JSON, key "also"): quantiser GB/s against HBM, the MXFP8
 layer forward+backward on the 30B-shaped layer, the NVFP4 30B-shaped forward,
-the BF16 (high-precision and dequantized) backward of the NVFP4 layer, and
-decode-sized batches of the 671B-shaped layer on the small-M kernel.
+the BF16 (high-precision and dequantized) backward of the NVFP4 layer,
+decode-sized batches of the 671B-shaped layer on the small-M kernel, and the
+single-expert NVFP4 GEMM (128 x 2048 activations against 1536 x 2048 gate|up
+weights) with its activation quantisation, each timed separately.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 """
@@ -307,6 +309,83 @@ def _quantizer_lines(peak_hbm):
     return out
 
 
+def _single_expert_line(peak_fp4, peak_hbm, reps=3):
+    """The single-expert NVFP4 case: 128 x 2048 activations (0.1 % of entries
+    x50), 768 x 2048 gate and up weights quantised jointly, 128 x 1536 fp32
+    output.  The per-token activation quantisation and the GEMM are timed
+    separately.  Both fit in L2, so each launch reads one of a set of
+    rotating copies whose total exceeds L2.  The launches are queued behind
+    a spin kernel, so the events around them measure back-to-back device time
+    instead of the host's per-call cost.  If the host took longer to queue
+    them than the spin lasted, the line says so ("host_bound")."""
+    from microscaled_precision_moe_gb300 import ops, synth
+    from microscaled_precision_moe_gb300 import _lib as L
+    x, wg, wu = synth.single_expert_inputs(device="cuda")
+    M, K, N = x.shape[0], x.shape[1], 2 * wg.shape[0]
+    n_q, n_g = 256, 96          # 256 x 0.67 MB and 96 x 2.6 MB of rotating data
+    xs = [x.clone() for _ in range(n_q)]
+    qs = [ops.nvfp4_quantize_per_token(xi) for xi in xs]
+    qw, sw, tsw = ops.nvfp4_quantize_weight([wg[None].contiguous(), wu[None].contiguous()])
+    ws = [(qw.clone(), sw.clone(), tsw.clone()) for _ in range(n_g)]
+    outs = [torch.empty(M, N, dtype=torch.float32, device="cuda") for _ in range(n_g)]
+    spin_cycles = int(4e7)      # about 20 ms at the SM clock
+
+    def queued(fn, n):
+        e0, s, e = _events(3)
+        torch.cuda.synchronize()
+        e0.record()
+        torch.cuda._sleep(spin_cycles)
+        s.record()
+        t0 = time.perf_counter()
+        for i in range(n):
+            fn(i)
+        host_ms = (time.perf_counter() - t0) * 1e3
+        e.record()
+        torch.cuda.synchronize()
+        return s.elapsed_time(e) / n, host_ms > e0.elapsed_time(s)
+
+    def quant(i):
+        ops.nvfp4_quantize_per_token(xs[i], out=qs[i])
+
+    def gemm(tile_m):
+        def f(i):
+            qx, sx, tsx = qs[i % n_q]
+            q1, s1, t1 = ws[i]
+            ops.moe_grouped_gemm(L.KIND_NVFP4, L.GROUP_M, L.EPI_F32, 1, M, N, K, None,
+                                 qx, q1[0], sx, K // 16, s1, K // 16, outs[i],
+                                 alpha_a=tsx, alpha_b=t1, tile_m=tile_m)
+        return f
+
+    out = {"workload": f"nvfp4_single_expert_M{M}_N{N}_K{K}",
+           "timing": f"launches over rotating copies ({n_q} activation, {n_g} weight), queued "
+                     "behind a spin kernel; median of the per-launch means of "
+                     f"{reps} runs"}
+    for i in range(3):
+        quant(i)
+    runs = [queued(quant, n_q) for _ in range(reps)]
+    ms = float(np.median([r[0] for r in runs]))
+    byts = M * K * 2 + M * K // 2 + ops.scale_bytes(M, K // 16) + M * 4
+    out["quantize_per_token"] = {"us": round(ms * 1e3, 2), "bytes": byts,
+                                 "GB/s": round(byts / (ms * 1e-3) / 1e9, 1),
+                                 "frac_hbm": round(byts / (ms * 1e-3) / 1e9 / peak_hbm, 3),
+                                 "host_bound": any(r[1] for r in runs)}
+    flops = 2 * M * N * K
+    for tile_m, name in ((128, "gemm_one_cta"), (256, "gemm_cta_pair"), (L.TILE_SMALL_M, "gemm_small_m")):
+        f = gemm(tile_m)
+        for i in range(3):
+            f(i)
+        runs = [queued(f, n_g) for _ in range(reps)]
+        ms = float(np.median([r[0] for r in runs]))
+        tf = flops / (ms * 1e-3) / 1e12
+        out[name] = {"us": round(ms * 1e3, 2), "flops": flops, "TFLOP/s": round(tf, 1),
+                     "frac_fp4": round(tf / peak_fp4, 4), "host_bound": any(r[1] for r in runs)}
+    torch.cuda.synchronize()
+    assert ops.get_device_status() == 0
+    del xs, qs, ws, outs
+    torch.cuda.empty_cache()
+    return out
+
+
 def _mxfp8_layer_line(peak_fp8, steps=10):
     from microscaled_precision_moe_gb300 import synth
     from microscaled_precision_moe_gb300.moe import MXFP8MoE
@@ -493,14 +572,16 @@ def main():
     ap.add_argument("--no-also", action="store_true", help="skip the secondary lines")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle sample")
     ap.add_argument("--case", choices=["headline", "slice", "mxfp8", "bf16bwd", "decode",
-                                       "decode_slice", "quant"],
+                                       "decode_slice", "quant", "single"],
                     default="headline",
                     help="slice: 4096 tokens over 64 experts of the 671B shape (profiling); "
                          "mxfp8: the MXFP8 30B-shaped forward+backward step alone (profiling); "
                          "bf16bwd: the BF16 backward of the NVFP4 30B-shaped layer alone; "
                          "decode: 64 / 256-token batches of the 671B-shaped layer; "
                          "decode_slice: 64 tokens over 32 experts of that shape (profiling); "
-                         "quant: the quantiser lines alone")
+                         "quant: the quantiser lines alone; "
+                         "single: the single-expert 128 x 1536 x 2048 NVFP4 GEMM and its "
+                         "activation quantisation")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -566,6 +647,14 @@ def main():
                               "unit": "GB/s", "n_gpus": world, "higher_is_better": True,
                               "dtype": "mxfp8", "config": {"workload": "mxfp8_quantize_8288x2048_rowcol"},
                               "quantizers": r}), flush=True)
+        return 0
+    if args.case == "single":
+        r = _single_expert_line(peak_fp4_sus, peaks["hbm"])
+        if rank == 0:
+            print(json.dumps({"metric": METRIC, "value": r["gemm_one_cta"]["us"], "unit": "us",
+                              "n_gpus": world, "higher_is_better": False, "dtype": "nvfp4",
+                              "config": {"workload": r["workload"]}, "single_expert": r}),
+                  flush=True)
         return 0
     if args.case in ("decode", "decode_slice"):
         r = (_nvfp4_decode_line(peaks["hbm"], steps=args.steps) if args.case == "decode" else
@@ -727,6 +816,10 @@ def main():
         also["nvfp4_layer_fwd_30b"] = _nvfp4_30b_line(peak_fp4_sus)
         also["nvfp4_layer_bf16_bwd"] = _nvfp4_bf16_bwd_line(peaks["bf16_sus"])
         also["nvfp4_layer_decode"] = _nvfp4_decode_line(peaks["hbm"])
+        try:
+            also["nvfp4_single_expert"] = _single_expert_line(peak_fp4_sus, peaks["hbm"])
+        except Exception as exc:       # a secondary line never costs the main one
+            also["nvfp4_single_expert"] = {"error": f"{type(exc).__name__}: {exc}"}
         also["stage_GBps_or_TFLOPs"] = {
             "quant_x_GB/s": round((shape.T * shape.H * 2.5625 + shape.T * 4) /
                                   (stage_ms["quant_x"] * 1e-3) / 1e9, 1),
