@@ -719,6 +719,16 @@ def main():
     stage_ms = {name: float(np.mean([ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(args.steps)]))
                 for j, name in enumerate(NVFP4MoE.STAGES)}
     value = world * flops / (ms * 1e-3) / 1e12
+    # algorithmic bytes of the HBM-bound stages, for their GB/s (R routed
+    # rows, r_pad rows after per-expert padding; one NVFP4 row of n elements
+    # is n/2 code bytes, n/16 scale bytes and a 4-byte token scale)
+    R = shape.T * shape.k
+    r_pad = int(layer.seg[0][shape.E].item())
+    nv_row = lambda n: n // 2 + n // 16 + 4
+    stage_bytes = {
+        "gather": R * nv_row(shape.H) + r_pad * (nv_row(shape.H) + 4 + 4),
+        "quant_d": r_pad * (shape.I * 2 + 4) + r_pad * nv_row(shape.I),
+        "combine": R * shape.H * 2 + R * 4 + shape.T * shape.H * 2}
 
     # ---- e2e through the public API: every step uploads its inputs from
     # pinned host memory and downloads its output; double-buffered, so step
@@ -825,6 +835,18 @@ def main():
                                   (stage_ms["quant_x"] * 1e-3) / 1e9, 1),
             "fc1_TFLOP/s": round(ach, 1),
             "fc2_TFLOP/s": round(fl2 / (stage_ms["fc2"] * 1e-3) / 1e12, 1)}
+        for name, nb in stage_bytes.items():
+            gbs = nb / (stage_ms[name] * 1e-3) / 1e9
+            also["stage_GBps_or_TFLOPs"][f"{name}_GB/s"] = round(gbs, 1)
+            also["stage_GBps_or_TFLOPs"][f"{name}_frac_hbm"] = round(gbs / peaks["hbm"], 3)
+        also["stage_GBps_or_TFLOPs"]["bytes"] = {
+            **stage_bytes, "rows": R, "padded_rows": r_pad,
+            "counted": "gather: the routed rows' NVFP4 codes, scales and token scales and "
+                       "every padded row's index read, every padded row written with its "
+                       "zeroed amax slot; "
+                       "quant_d: bf16 D and the amax read, NVFP4 D written (padded rows); "
+                       "combine: the routed rows of Y and the inverse map read, the output "
+                       "written"}
         line["also"] = also
     if rank == 0:
         print(json.dumps(line), flush=True)
