@@ -210,3 +210,25 @@ def test_empty_inputs_and_size_limits_are_shape_errors(lib):
         d.seg_dev = 0x10000
         setattr(d, field, value)
         assert lib.mpm_moe_grouped_gemm(C.byref(d), None) == SHAPE, field
+
+
+def test_plain_c_client(lib, tmp_path):
+    """tests/abi_client.c, compiled as C99 with gcc against include/mpm.h and
+    linked with libmpm.so, runs its host-only checks (no GPU, no Python in
+    the client)."""
+    import shutil
+    import subprocess
+    from microscaled_precision_moe_gb300 import _lib
+    gcc = shutil.which("gcc")
+    nvcc = shutil.which("nvcc")
+    if gcc is None or nvcc is None:
+        pytest.skip("gcc and the CUDA toolkit headers are needed")
+    cuda_inc = os.path.join(os.path.dirname(os.path.dirname(os.path.realpath(nvcc))), "include")
+    libdir = os.path.dirname(_lib.LIB_PATH)
+    exe = str(tmp_path / "abi_client")
+    subprocess.run([gcc, "-std=c99", "-Wall", "-Werror", "-I", os.path.join(ROOT, "include"),
+                    "-I", cuda_inc, os.path.join(ROOT, "tests", "abi_client.c"),
+                    "-L", libdir, "-lmpm", f"-Wl,-rpath,{libdir}", "-o", exe], check=True)
+    r = subprocess.run([exe], capture_output=True, text=True, timeout=60)
+    assert r.returncode == 0, r.stderr
+    assert "abi_client: ok" in r.stdout
