@@ -27,6 +27,27 @@ def _need_cuda(*ts):
             raise ValueError("libmpm operates on CUDA tensors only")
 
 
+def _check(t, name, dtype, dim=None, contiguous=False, min_numel=None):
+    """Argument checks the C side cannot make (it sees raw pointers only):
+    element type, rank, dense layout, and that a buffer holds at least the
+    elements the call will touch."""
+    if t.dtype != dtype:
+        raise TypeError(f"{name}: expected {dtype}, got {t.dtype}")
+    if dim is not None and t.dim() != dim:
+        raise ValueError(f"{name}: expected a {dim}-d tensor, got shape {tuple(t.shape)}")
+    if contiguous and not t.is_contiguous():
+        raise ValueError(f"{name}: expected a contiguous tensor")
+    if min_numel is not None and t.numel() < min_numel:
+        raise ValueError(f"{name}: holds {t.numel()} elements, the call needs {min_numel}")
+
+
+def _check_rows(x, name):
+    """A bf16 matrix whose rows are dense (any row pitch)."""
+    _check(x, name, torch.bfloat16, dim=2)
+    if x.stride(1) != 1:
+        raise ValueError(f"{name}: rows must be dense (stride(1) == 1)")
+
+
 def scale_bytes(rows: int, cols: int) -> int:
     return int(L.load().mpm_scale_bytes(rows, cols))
 
@@ -44,8 +65,8 @@ def mxfp8_quantize(x, rowwise=True, colwise=True, ldc=None, m_valid=None, out=No
     (transposed), col_s (tiled [K, ceil(M/32)]).
     """
     lib = L.load()
+    _check_rows(x, "x")
     _need_cuda(x)
-    assert x.dtype == torch.bfloat16 and x.dim() == 2 and x.stride(1) == 1
     M, K = x.shape
     ldc = ldc or pad_to(M, 16)
     dev = x.device
@@ -69,8 +90,8 @@ def nvfp4_quantize_per_token(x, amax_in=None, m_valid=None, out=None):
     """Per-token NVFP4 of bf16 x [M, K]: (q [M, K/2] u8, s tiled [M, K/16] u8,
     token_scale [M] fp32) from one call."""
     lib = L.load()
+    _check_rows(x, "x")
     _need_cuda(x)
-    assert x.dtype == torch.bfloat16 and x.dim() == 2 and x.stride(1) == 1
     M, K = x.shape
     dev = x.device
     if out is None:
@@ -89,10 +110,15 @@ def nvfp4_quantize_weight(parts, out=None, ws=None):
     one FP32 outer scale per expert: (q [E, R, K/2], s [E * tiled(R, K/16)],
     tensor_scale [E])."""
     lib = L.load()
-    _need_cuda(*parts)
+    if not parts:
+        raise ValueError("parts: at least one weight part is needed")
+    for i, p in enumerate(parts):
+        _check(p, f"parts[{i}]", torch.bfloat16, dim=3, contiguous=True)
     E, _, K = parts[0].shape
-    for p in parts:
-        assert p.dtype == torch.bfloat16 and p.is_contiguous() and p.shape[0] == E and p.shape[2] == K
+    for i, p in enumerate(parts):
+        if p.shape[0] != E or p.shape[2] != K:
+            raise ValueError(f"parts[{i}]: shape {tuple(p.shape)} does not match [{E}, rows, {K}]")
+    _need_cuda(*parts)
     R = sum(p.shape[1] for p in parts)
     dev = parts[0].device
     if out is None:
@@ -121,8 +147,12 @@ def moe_build_segments(topk_ids, topk_prob, E: int, out=None, ws=None, pad: int 
     """(seg_offsets [E+1], perm [cap], inv_perm [T*k], row_prob [cap], cap);
     segments padded to ``pad`` rows (128, or 256 for the CTA-pair GEMM)."""
     lib = L.load()
+    _check(topk_ids, "topk_ids", torch.int32, dim=2)
+    _check(topk_prob, "topk_prob", torch.float32, dim=2)
+    if topk_prob.shape != topk_ids.shape:
+        raise ValueError("topk_prob must have the shape of topk_ids")
     _need_cuda(topk_ids, topk_prob)
-    assert topk_ids.dtype == torch.int32 and topk_prob.dtype == torch.float32
+    ids_c, prob_c = topk_ids.contiguous(), topk_prob.contiguous()   # alive until the launch
     T, k = topk_ids.shape
     dev = topk_ids.device
     cap = moe_row_capacity(T, k, E, pad)
@@ -135,18 +165,35 @@ def moe_build_segments(topk_ids, topk_prob, E: int, out=None, ws=None, pad: int 
     wsb = int(lib.mpm_moe_segments_workspace_bytes(T, k, E))
     if ws is None:
         ws = torch.empty(wsb, dtype=torch.uint8, device=dev)
-    st = lib.mpm_moe_build_segments(_ptr(topk_ids.contiguous()), _ptr(topk_prob.contiguous()), T,
+    _check(seg, "seg_offsets", torch.int32, min_numel=E + 1)
+    _check(perm, "perm", torch.int32, min_numel=cap)
+    _check(inv, "inv_perm", torch.int32, min_numel=T * k)
+    _check(rp, "row_prob", torch.float32, min_numel=cap)
+    _check(ws, "ws", torch.uint8, min_numel=wsb)
+    st = lib.mpm_moe_build_segments(_ptr(ids_c), _ptr(prob_c), T,
                                     k, E, pad, _ptr(seg), _ptr(perm), _ptr(inv), _ptr(rp),
                                     _ptr(ws), ws.numel(), _stream(dev))
     L.check(st, "mpm_moe_build_segments")
     return seg, perm, inv, rp, cap
 
 
+def _check_route(perm, seg, E, cap):
+    _check(perm, "perm", torch.int32, min_numel=cap)
+    _check(seg, "seg_offsets", torch.int32, min_numel=E + 1)
+
+
 def moe_gather_bf16(x, perm, seg, E: int, k: int, cap: int, out=None, amax_zero=None):
+    """bf16 rows x [T, K] (dense) -> the permuted layout [cap, K]."""
     lib = L.load()
+    _check(x, "x", torch.bfloat16, dim=2, contiguous=True)
+    _check_route(perm, seg, E, cap)
     T, K = x.shape
     if out is None:
         out = torch.empty(cap, K, dtype=torch.bfloat16, device=x.device)
+    _check(out, "out", torch.bfloat16, contiguous=True, min_numel=cap * K)
+    if amax_zero is not None:
+        _check(amax_zero, "amax_zero", torch.float32, min_numel=cap)
+    _need_cuda(x, perm, seg, out, amax_zero)
     st = lib.mpm_moe_gather(L.GATHER_BF16, _ptr(x), None, None, T, K, k, _ptr(perm), _ptr(seg),
                             E, cap, _ptr(out), None, None, _ptr(amax_zero), _stream(x.device))
     L.check(st, "mpm_moe_gather")
@@ -155,14 +202,28 @@ def moe_gather_bf16(x, perm, seg, E: int, k: int, cap: int, out=None, amax_zero=
 
 def moe_gather_nvfp4(q, s, ts, K: int, perm, seg, E: int, k: int, cap: int, out=None,
                      amax_zero=None):
+    """Per-token NVFP4 rows (codes [T, K/2], tiled scales, token scales [T])
+    -> the same three in the permuted layout of cap rows."""
     lib = L.load()
+    _check(q, "q", torch.uint8, dim=2, contiguous=True)
     T = q.shape[0]
+    if q.shape[1] != K // 2:
+        raise ValueError(f"q: expected [T, {K // 2}] codes, got {tuple(q.shape)}")
+    _check(s, "s", torch.uint8, min_numel=scale_bytes(T, K // 16))
+    _check(ts, "ts", torch.float32, min_numel=T)
+    _check_route(perm, seg, E, cap)
     dev = q.device
     if out is None:
         out = (torch.empty(cap, K // 2, dtype=torch.uint8, device=dev),
                torch.empty(scale_bytes(cap, K // 16), dtype=torch.uint8, device=dev),
                torch.empty(cap, dtype=torch.float32, device=dev))
     dq, ds, dts = out
+    _check(dq, "out codes", torch.uint8, contiguous=True, min_numel=cap * (K // 2))
+    _check(ds, "out scales", torch.uint8, min_numel=scale_bytes(cap, K // 16))
+    _check(dts, "out token scales", torch.float32, min_numel=cap)
+    if amax_zero is not None:
+        _check(amax_zero, "amax_zero", torch.float32, min_numel=cap)
+    _need_cuda(q, s, ts, perm, seg, dq, ds, dts, amax_zero)
     st = lib.mpm_moe_gather(L.GATHER_NVFP4, _ptr(q), _ptr(s), _ptr(ts), T, K, k, _ptr(perm),
                             _ptr(seg), E, cap, _ptr(dq), _ptr(ds), _ptr(dts), _ptr(amax_zero),
                             _stream(dev))
@@ -171,10 +232,15 @@ def moe_gather_nvfp4(q, s, ts, K: int, perm, seg, E: int, k: int, cap: int, out=
 
 
 def moe_combine(y_perm, inv_perm, T: int, k: int, out=None):
+    """out [T, H] bf16: each token's k rows of y_perm summed in slot order."""
     lib = L.load()
+    _check(y_perm, "y_perm", torch.bfloat16, dim=2, contiguous=True)
+    _check(inv_perm, "inv_perm", torch.int32, min_numel=T * k)
     H = y_perm.shape[1]
     if out is None:
         out = torch.empty(T, H, dtype=torch.bfloat16, device=y_perm.device)
+    _check(out, "out", torch.bfloat16, contiguous=True, min_numel=T * H)
+    _need_cuda(y_perm, inv_perm, out)
     st = lib.mpm_moe_combine(_ptr(y_perm), _ptr(inv_perm), T, k, H, _ptr(out),
                              _stream(y_perm.device))
     L.check(st, "mpm_moe_combine")

@@ -232,3 +232,56 @@ def test_plain_c_client(lib, tmp_path):
     r = subprocess.run([exe], capture_output=True, text=True, timeout=60)
     assert r.returncode == 0, r.stderr
     assert "abi_client: ok" in r.stdout
+
+
+def test_binding_checks_arguments_before_the_library(lib):
+    """The Python binding rejects what the C side cannot see (element type,
+    rank, dense rows, buffer sizes) with TypeError / ValueError, and CPU
+    tensors with ValueError; nothing here reaches the library's launches."""
+    import torch
+    from microscaled_precision_moe_gb300 import ops
+    bf, i32, f32, u8 = torch.bfloat16, torch.int32, torch.float32, torch.uint8
+    x = torch.zeros(8, 64, dtype=bf)
+    with pytest.raises(TypeError):
+        ops.nvfp4_quantize_per_token(x.float())
+    with pytest.raises(ValueError, match="dense"):
+        ops.mxfp8_quantize(torch.zeros(64, 8, dtype=bf).t())
+    with pytest.raises(ValueError, match="3-d"):
+        ops.nvfp4_quantize_weight([x])
+    with pytest.raises(ValueError, match="does not match"):
+        ops.nvfp4_quantize_weight([torch.zeros(2, 64, 64, dtype=bf), torch.zeros(3, 64, 64, dtype=bf)])
+    with pytest.raises(ValueError, match="CUDA"):
+        ops.nvfp4_quantize_per_token(x)
+    ids, prob = torch.zeros(4, 2, dtype=i32), torch.zeros(4, 2, dtype=f32)
+    with pytest.raises(TypeError, match="topk_ids"):
+        ops.moe_build_segments(ids.long(), prob, 8)
+    with pytest.raises(ValueError, match="shape of topk_ids"):
+        ops.moe_build_segments(ids, prob[:, :1], 8)
+    with pytest.raises(ValueError, match="CUDA"):
+        ops.moe_build_segments(ids, prob, 8)
+    cap = ops.moe_row_capacity(4, 2, 8, 128)
+    perm, seg = torch.zeros(cap, dtype=i32), torch.zeros(9, dtype=i32)
+    with pytest.raises(ValueError, match="perm"):
+        ops.moe_gather_bf16(x, perm[:10], seg, 8, 2, cap)
+    with pytest.raises(ValueError, match="seg_offsets"):
+        ops.moe_gather_bf16(x, perm, seg[:8], 8, 2, cap)
+    with pytest.raises(ValueError, match="contiguous"):
+        ops.moe_gather_bf16(torch.zeros(64, 8, dtype=bf).t(), perm, seg, 8, 2, cap)
+    with pytest.raises(ValueError, match="CUDA"):
+        ops.moe_gather_bf16(x, perm, seg, 8, 2, cap)
+    q = torch.zeros(8, 32, dtype=u8)
+    s = torch.zeros(ops.scale_bytes(8, 4), dtype=u8)
+    ts = torch.zeros(8, dtype=f32)
+    with pytest.raises(ValueError, match="codes"):
+        ops.moe_gather_nvfp4(q, s, ts, 128, perm, seg, 8, 2, cap)
+    with pytest.raises(ValueError, match="ts"):
+        ops.moe_gather_nvfp4(q, s, ts[:4], 64, perm, seg, 8, 2, cap)
+    with pytest.raises(ValueError, match="CUDA"):
+        ops.moe_gather_nvfp4(q, s, ts, 64, perm, seg, 8, 2, cap)
+    y, inv = torch.zeros(cap, 64, dtype=bf), torch.zeros(8, dtype=i32)
+    with pytest.raises(ValueError, match="inv_perm"):
+        ops.moe_combine(y, inv[:7], 4, 2)
+    with pytest.raises(ValueError, match="out"):
+        ops.moe_combine(y, inv, 4, 2, out=torch.zeros(3, 64, dtype=bf))
+    with pytest.raises(ValueError, match="CUDA"):
+        ops.moe_combine(y, inv, 4, 2)
