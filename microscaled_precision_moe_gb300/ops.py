@@ -41,6 +41,12 @@ def _check(t, name, dtype, dim=None, contiguous=False, min_numel=None):
         raise ValueError(f"{name}: holds {t.numel()} elements, the call needs {min_numel}")
 
 
+def _check_m_valid(m_valid):
+    """The optional device row count: one int32."""
+    if m_valid is not None:
+        _check(m_valid, "m_valid", torch.int32, min_numel=1)
+
+
 def _check_rows(x, name):
     """A bf16 matrix whose rows are dense (any row pitch)."""
     _check(x, name, torch.bfloat16, dim=2)
@@ -66,7 +72,8 @@ def mxfp8_quantize(x, rowwise=True, colwise=True, ldc=None, m_valid=None, out=No
     """
     lib = L.load()
     _check_rows(x, "x")
-    _need_cuda(x)
+    _check_m_valid(m_valid)
+    _need_cuda(x, m_valid)
     M, K = x.shape
     ldc = ldc or pad_to(M, 16)
     dev = x.device
@@ -91,7 +98,10 @@ def nvfp4_quantize_per_token(x, amax_in=None, m_valid=None, out=None):
     token_scale [M] fp32) from one call."""
     lib = L.load()
     _check_rows(x, "x")
-    _need_cuda(x)
+    _check_m_valid(m_valid)
+    if amax_in is not None:
+        _check(amax_in, "amax_in", torch.float32, min_numel=x.shape[0])
+    _need_cuda(x, m_valid, amax_in)
     M, K = x.shape
     dev = x.device
     if out is None:
@@ -262,11 +272,26 @@ def moe_grouped_gemm(kind, group, epilogue, E, a_rows, N, K, seg, a, b, sfa, sfa
     """
     lib = L.load()
     if kind == L.KIND_BF16:
-        _need_cuda(a, b, out)
-        if a.dtype != torch.bfloat16 or b.dtype != torch.bfloat16:
-            raise TypeError("KIND_BF16 takes bf16 operands A and B")
+        _check(a, "a", torch.bfloat16, dim=2)
+        _check(b, "b", torch.bfloat16)
     else:
-        _need_cuda(a, b, sfa, sfb, out)
+        _check(a, "a (codes)", torch.uint8, dim=2)
+        _check(b, "b (codes)", torch.uint8)
+        if sfa is None or sfb is None:
+            raise ValueError("block-scaled kinds need both scale tensors")
+        _check(sfa, "sfa", torch.uint8)
+        _check(sfb, "sfb", torch.uint8)
+    _check(out, "out", torch.float32 if epilogue == L.EPI_F32 else torch.bfloat16)
+    for t, name in ((out2, "out2"), (aux, "aux")):
+        if t is not None:
+            _check(t, name, torch.bfloat16)
+    for t, name in ((alpha_a, "alpha_a"), (alpha_b, "alpha_b"), (row_prob, "row_prob"),
+                    (amax, "amax")):
+        if t is not None:
+            _check(t, name, torch.float32)
+    if seg is not None:
+        _check(seg, "seg_offsets", torch.int32, min_numel=E + 1)
+    _need_cuda(a, b, sfa, sfb, out, out2, aux, alpha_a, alpha_b, row_prob, amax, seg)
     d = L.GroupedGemmDesc()
     d.kind, d.group, d.epilogue, d.tile_m = kind, group, epilogue, tile_m
     d.E, d.a_rows, d.N, d.K = E, a_rows, N, K
@@ -299,10 +324,15 @@ def nvfp4_dequantize(q, s, outer, rows_per_outer: int, K: int, m_valid=None, out
     """bf16 [M, K] from NVFP4 codes, tiled E4M3 scales and fp32 outer scales
     (one outer scale per ``rows_per_outer`` rows), each value rounded once."""
     lib = L.load()
-    _need_cuda(q, s, outer)
+    _check(q, "q", torch.uint8, dim=2)
+    _check(s, "s", torch.uint8)
+    _check(outer, "outer", torch.float32)
+    _check_m_valid(m_valid)
     M = q.shape[0]
     if out is None:
         out = torch.empty(M, K, dtype=torch.bfloat16, device=q.device)
+    _check(out, "out", torch.bfloat16, dim=2)
+    _need_cuda(q, s, outer, m_valid, out)
     st = lib.mpm_nvfp4_dequantize(_ptr(q), _ptr(s), _ptr(outer), rows_per_outer, M, K,
                                   _ptr(out), out.stride(0), _ptr(m_valid), _stream(q.device))
     L.check(st, "mpm_nvfp4_dequantize")
@@ -312,10 +342,14 @@ def nvfp4_dequantize(q, s, outer, rows_per_outer: int, K: int, m_valid=None, out
 def mxfp8_dequantize(q, s, m_valid=None, out=None):
     """bf16 [M, K] from row-wise MXFP8 codes [M, K] and tiled E8M0 scales."""
     lib = L.load()
-    _need_cuda(q, s)
+    _check(q, "q", torch.uint8, dim=2)
+    _check(s, "s", torch.uint8)
+    _check_m_valid(m_valid)
     M, K = q.shape
     if out is None:
         out = torch.empty(M, K, dtype=torch.bfloat16, device=q.device)
+    _check(out, "out", torch.bfloat16, dim=2)
+    _need_cuda(q, s, m_valid, out)
     st = lib.mpm_mxfp8_dequantize(_ptr(q), _ptr(s), M, K, _ptr(out), out.stride(0),
                                   _ptr(m_valid), _stream(q.device))
     L.check(st, "mpm_mxfp8_dequantize")
@@ -325,12 +359,13 @@ def mxfp8_dequantize(q, s, m_valid=None, out=None):
 def transpose_bf16(x, m_valid=None, out=None):
     """out [C, R] = x [R, C]^T for bf16 matrices (bit copies)."""
     lib = L.load()
-    _need_cuda(x)
-    if x.dtype != torch.bfloat16:
-        raise TypeError("transpose_bf16 takes a bf16 matrix")
+    _check(x, "x", torch.bfloat16, dim=2)
+    _check_m_valid(m_valid)
     R, C_ = x.shape
     if out is None:
         out = torch.empty(C_, R, dtype=torch.bfloat16, device=x.device)
+    _check(out, "out", torch.bfloat16, dim=2)
+    _need_cuda(x, m_valid, out)
     st = lib.mpm_transpose_bf16(_ptr(x), R, C_, x.stride(0), _ptr(out), out.stride(0),
                                 _ptr(m_valid), _stream(x.device))
     L.check(st, "mpm_transpose_bf16")

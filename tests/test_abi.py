@@ -285,3 +285,47 @@ def test_binding_checks_arguments_before_the_library(lib):
         ops.moe_combine(y, inv, 4, 2, out=torch.zeros(3, 64, dtype=bf))
     with pytest.raises(ValueError, match="CUDA"):
         ops.moe_combine(y, inv, 4, 2)
+
+
+def test_binding_checks_gemm_and_dequantize_arguments(lib):
+    """The GEMM wrapper checks element types the descriptor cannot carry:
+    codes and scales uint8 (bf16 operands for the BF16 kind), fp32 output
+    only for the fp32 epilogue, fp32 scales / probabilities / amax, int32
+    offsets holding E+1 entries; the dequantisers check codes, scales and
+    the device row count (CPU only)."""
+    import torch
+    from microscaled_precision_moe_gb300 import ops, _lib as L
+    bf, i32, f32, u8 = torch.bfloat16, torch.int32, torch.float32, torch.uint8
+    a, b = torch.zeros(256, 128, dtype=u8), torch.zeros(256, 128, dtype=u8)
+    sf = torch.zeros(256 * 64, dtype=u8)
+    seg = torch.zeros(3, dtype=i32)
+    args = (L.KIND_NVFP4, L.GROUP_M, L.EPI_BF16, 2, 256, 256, 256)
+    with pytest.raises(TypeError, match="a \\(codes\\)"):
+        ops.moe_grouped_gemm(*args, seg, a.to(bf), b, sf, 16, sf, 16, torch.zeros(256, 256, dtype=bf))
+    with pytest.raises(ValueError, match="scale tensors"):
+        ops.moe_grouped_gemm(*args, seg, a, b, None, 16, sf, 16, torch.zeros(256, 256, dtype=bf))
+    with pytest.raises(TypeError, match="out"):
+        ops.moe_grouped_gemm(*args, seg, a, b, sf, 16, sf, 16, torch.zeros(256, 256, dtype=f32))
+    with pytest.raises(TypeError, match="alpha_a"):
+        ops.moe_grouped_gemm(*args, seg, a, b, sf, 16, sf, 16, torch.zeros(256, 256, dtype=bf),
+                             alpha_a=torch.zeros(256, dtype=bf))
+    with pytest.raises(ValueError, match="seg_offsets"):
+        ops.moe_grouped_gemm(*args, seg[:2], a, b, sf, 16, sf, 16, torch.zeros(256, 256, dtype=bf))
+    with pytest.raises(TypeError, match="out"):
+        ops.moe_grouped_gemm(L.KIND_MXFP8, L.GROUP_K, L.EPI_F32, 2, 256, 256, 0, seg, a, b, sf, 16,
+                             sf, 16, torch.zeros(2, 256, 256, dtype=bf))
+    with pytest.raises(TypeError, match="b"):
+        ops.moe_grouped_gemm(L.KIND_BF16, L.GROUP_M, L.EPI_BF16, 2, 256, 256, 256, seg,
+                             torch.zeros(256, 256, dtype=bf), b, None, 0, None, 0,
+                             torch.zeros(256, 256, dtype=bf))
+    with pytest.raises(ValueError, match="CUDA"):
+        ops.moe_grouped_gemm(*args, seg, a, b, sf, 16, sf, 16, torch.zeros(256, 256, dtype=bf))
+    q, s, ts = torch.zeros(8, 32, dtype=u8), torch.zeros(ops.scale_bytes(8, 4), dtype=u8), torch.zeros(8)
+    with pytest.raises(TypeError, match="m_valid"):
+        ops.nvfp4_dequantize(q, s, ts, 1, 64, m_valid=torch.zeros(1, dtype=torch.int64))
+    with pytest.raises(TypeError, match="out"):
+        ops.nvfp4_dequantize(q, s, ts, 1, 64, out=torch.zeros(8, 64, dtype=f32))
+    with pytest.raises(TypeError, match="amax_in"):
+        ops.nvfp4_quantize_per_token(torch.zeros(8, 64, dtype=bf), amax_in=torch.zeros(8, dtype=bf))
+    with pytest.raises(ValueError, match="CUDA"):
+        ops.mxfp8_dequantize(torch.zeros(8, 64, dtype=u8), torch.zeros(ops.scale_bytes(8, 2), dtype=u8))
