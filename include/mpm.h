@@ -178,9 +178,13 @@ mpm_status mpm_nvfp4_quantize_weight(const void* const* parts_dev, const int64_t
  * scratch lives in a fixed device array declared by the library (16 KiB, room
  * for E <= 4096 experts; every GPU that loads the library keeps it until the
  * process exits).  E > 4096 returns MPM_ERR_SHAPE before any launch.
- * The first call on a device looks up that array's device address (once per
- * device, with that device current); make that first call before any stream
- * capture.  The call allocates nothing and clears the slots it uses before
+ * Each call made outside stream capture looks up that array's device address
+ * on the current device (so a device reset, after which the library's device
+ * memory lives elsewhere, is picked up by the next such call); a call made
+ * while the stream is capturing reuses the address the last uncaptured call
+ * on that device found, so make one call on each device (and one after any
+ * device reset) before capturing; a first call under capture returns
+ * MPM_ERR_CUDA.  The call allocates nothing and clears the slots it uses before
  * reducing into them.  All calls share the one array: calls whose work can
  * overlap on the GPU (other streams, other host threads) race on it, so
  * order them on one stream or synchronise between them.
@@ -440,6 +444,25 @@ typedef struct {
 } mpm_grouped_gemm_desc;
 
 mpm_status mpm_moe_grouped_gemm(const mpm_grouped_gemm_desc* desc, cudaStream_t stream);
+
+/*
+ * The weight-gradient grouped GEMM: dW_e = dY_e^T * X_e, the contraction
+ * running over expert e's own rows [seg[e], seg[e+1]) of the permuted
+ * buffers.  Source: "Towards Blackwell-native 8-bit and 4-bit RL", section
+ * "Recipe 1 / Training" (wgrad reads the column-wise 32x1 copies of the
+ * activation and of the output gradient); "miniTE technical report",
+ * section 5.2 (segments given by device offsets, zero-token experts handled
+ * in the same path).
+ * The same descriptor and rules as mpm_moe_grouped_gemm in GROUP_K mode; the
+ * call sets group = MPM_GROUP_K itself (the field is ignored).  a_dev is
+ * the [M_out, R] operand (MXFP8: the column-wise copy of dY, stored
+ * transposed; BF16: with a_mn_major, dY_perm as it is), b_dev the [N, R]
+ * operand (X's column-wise copy; BF16: X_perm with b_mn_major); out_dev
+ * fp32 [E, M_out, N] (ldo elements per row), written whole: an expert with
+ * no rows gets zeros.  Kinds MXFP8 and BF16, epilogue F32 only (anything
+ * else returns MPM_ERR_UNSUPPORTED before any launch).
+ */
+mpm_status mpm_moe_grouped_gemm_wgrad(const mpm_grouped_gemm_desc* desc, cudaStream_t stream);
 
 /* ------------------------------------------------------------------------ */
 /* Device status                                                            */

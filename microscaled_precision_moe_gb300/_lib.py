@@ -69,6 +69,7 @@ _SIGS = {
     "mpm_mxfp8_dequantize": (_int, [_vp, _vp, _i64, _i64, _vp, _i64, _vp, _vp]),
     "mpm_transpose_bf16": (_int, [_vp, _i64, _i64, _i64, _vp, _i64, _vp, _vp]),
     "mpm_moe_grouped_gemm": (_int, [C.POINTER(GroupedGemmDesc), _vp]),
+    "mpm_moe_grouped_gemm_wgrad": (_int, [C.POINTER(GroupedGemmDesc), _vp]),
     "mpm_get_device_status": (_int, [C.POINTER(C.c_int32), _vp]),
 }
 

@@ -453,6 +453,13 @@ mpm_status mpm_moe_grouped_gemm(const mpm_grouped_gemm_desc* d, cudaStream_t str
   return cuda_status(mpm::launch_grouped_gemm(d->kind, d->epilogue, ta, tb, a, grid, stream));
 }
 
+mpm_status mpm_moe_grouped_gemm_wgrad(const mpm_grouped_gemm_desc* d, cudaStream_t stream) {
+  if (!d) return MPM_ERR_NULL;
+  mpm_grouped_gemm_desc w = *d;
+  w.group = MPM_GROUP_K;
+  return mpm_moe_grouped_gemm(&w, stream);
+}
+
 mpm_status mpm_get_device_status(int32_t* host_out, cudaStream_t stream) {
   if (!host_out) return MPM_ERR_NULL;
   int* p = status_ptr();

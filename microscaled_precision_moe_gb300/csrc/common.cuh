@@ -62,6 +62,27 @@ MPM_DEV float e4m3_to_f32(uint32_t code) {
 
 MPM_DEV uint32_t float_bits(float f) { return __float_as_uint(f); }
 
+// ---------------------------------------------------------------- SwiGLU
+// The activation of every FC1 epilogue and its derivative for the SwiGLU
+// backward, defined once so that D (and dH) do not depend on which GEMM
+// kernel produced them: every step is one IEEE binary32 operation (CUDA's
+// expf, correctly rounded division, no contraction into FMAs).
+//   silu(g) = g / (1 + e^-g)
+//   D       = silu(g) * u * p
+MPM_DEV float swiglu_silu(float g) { return __fdiv_rn(g, __fadd_rn(1.0f, expf(-g))); }
+MPM_DEV float swiglu_fwd(float g, float u, float prob) {
+  return __fmul_rn(__fmul_rn(swiglu_silu(g), u), prob);
+}
+// dD -> (dg, du) for D = silu(g) * u * p with p constant:
+//   dg = (dD p) u s (1 + g (1 - s)),  du = (dD p) g s,  s = 1 / (1 + e^-g)
+MPM_DEV void swiglu_bwd(float g, float u, float dd, float prob, float& dg, float& du) {
+  const float s = __fdiv_rn(1.0f, __fadd_rn(1.0f, expf(-g)));
+  const float dp = __fmul_rn(dd, prob);
+  const float dsilu = __fmul_rn(s, __fadd_rn(1.0f, __fmul_rn(g, __fsub_rn(1.0f, s))));
+  dg = __fmul_rn(__fmul_rn(dp, u), dsilu);
+  du = __fmul_rn(dp, __fmul_rn(g, s));
+}
+
 // ---------------------------------------------------------------- 128x4 scale tiles
 // byte offset of scale entry (r, c) in a tiled [rows, cols] scale matrix whose
 // padded column count is cols_pad (multiple of 4)

@@ -63,8 +63,6 @@ constexpr int smem_bytes() {
          (3 * STAGES + 1) * 8 + 16;
 }
 
-MPM_DEV float silu_f(float g) { return g / (1.0f + expf(-g)); }
-
 MPM_DEV uint32_t pack_bf16(float lo, float hi) {
   __nv_bfloat162 b = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&b);
@@ -320,8 +318,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tma_a,
           for (int q = 0; q < 2; ++q) {
             const float g = __fmul_rn(__uint_as_float(v[j + q]), alpha);
             const float uu = __fmul_rn(__uint_as_float(u[j + q]), alpha);
-            const float d = __fmul_rn(__fmul_rn(silu_f(g), uu), prob);
-            d2[q] = d;
+            d2[q] = swiglu_fwd(g, uu, prob);
           }
           const uint32_t pk = pack_bf16(d2[0], d2[1]);
           dw[j / 2] = pk;
@@ -380,12 +377,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tma_a,
               const float g = h ? bf16hi(ga[q]) : bf16lo(ga[q]);
               const float uu = h ? bf16hi(ua[q]) : bf16lo(ua[q]);
               const float dd = __fmul_rn(__uint_as_float(v[j + 2 * q + h]), alpha);
-              const float sg = 1.0f / (1.0f + expf(-g));
-              const float silu = g * sg;
-              const float dsilu = sg * (1.0f + g * (1.0f - sg));
-              const float dp = dd * prob;
-              dg2[h] = dp * uu * dsilu;
-              du2[h] = dp * silu;
+              swiglu_bwd(g, uu, dd, prob, dg2[h], du2[h]);
             }
             og4[q] = pack_bf16(dg2[0], dg2[1]);
             ou4[q] = pack_bf16(du2[0], du2[1]);

@@ -109,9 +109,6 @@ constexpr int smem_bytes() {
          (4 * Cfg<KIND>::kStages + 4) * 8 + 32;
 }
 
-// epilogue activation: fast exponential and division (the result is rounded
-// to bf16 right after, far coarser than their error)
-MPM_DEV float silu_f(float g) { return __fdividef(g, 1.0f + __expf(-g)); }
 MPM_DEV uint32_t pack_bf16(float lo, float hi) {
   __nv_bfloat162 b = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&b);
@@ -622,8 +619,7 @@ grouped_gemm_pair_kernel(const __grid_constant__ PairMaps maps, const GemmArgs p
             const float u0 = __fmul_rn(__uint_as_float(uv[jj]), alpha);
             const float g1 = __fmul_rn(__uint_as_float(gv[jj + 1]), alpha);
             const float u1 = __fmul_rn(__uint_as_float(uv[jj + 1]), alpha);
-            const uint32_t pk = pack_bf16(__fmul_rn(__fmul_rn(silu_f(g0), u0), prob),
-                                          __fmul_rn(__fmul_rn(silu_f(g1), u1), prob));
+            const uint32_t pk = pack_bf16(swiglu_fwd(g0, u0, prob), swiglu_fwd(g1, u1, prob));
             dw[cc * 16 + jj / 2] = pk;
             amax = fmaxf(amax, fmaxf(fabsf(bf16lo(pk)), fabsf(bf16hi(pk))));
           }
@@ -776,10 +772,7 @@ grouped_gemm_pair_kernel(const __grid_constant__ PairMaps maps, const GemmArgs p
                 const float g = h ? bf16hi(ga[qq]) : bf16lo(ga[qq]);
                 const float uu = h ? bf16hi(ua[qq]) : bf16lo(ua[qq]);
                 const float dd = __fmul_rn(__uint_as_float(v[jj + 2 * qq + h]), alpha);
-                const float sg = __fdividef(1.0f, 1.0f + __expf(-g));
-                const float dp = dd * prob;
-                dg2[h] = dp * uu * (sg * (1.0f + g * (1.0f - sg)));
-                du2[h] = dp * (g * sg);
+                swiglu_bwd(g, uu, dd, prob, dg2[h], du2[h]);
               }
               og4[qq] = pack_bf16(dg2[0], dg2[1]);
               ou4[qq] = pack_bf16(du2[0], du2[1]);

@@ -63,8 +63,6 @@ constexpr int smem_bytes() {
   return 1024 + Cfg<KIND, EPI>::kStages * Cfg<KIND, EPI>::kStage + (4 * Cfg<KIND, EPI>::kStages + 8) * 8;
 }
 
-MPM_DEV float silu_f(float g) { return __fdividef(g, 1.0f + __expf(-g)); }
-
 struct SmallMaps {
   CUtensorMap a, b;   // routed rows (A) and weights (B), 128 x 128-byte boxes
 };
@@ -313,7 +311,7 @@ grouped_gemm_small_kernel(const __grid_constant__ SmallMaps maps, const GemmArgs
             const float gv = __fmul_rn(__uint_as_float(g[c]), alpha);
             const float uv = __fmul_rn(__uint_as_float(u[c]), alpha);
             const float prob = __shfl_sync(0xffffffffu, p_lane, c);
-            const __nv_bfloat16 d = __float2bfloat16_rn(__fmul_rn(__fmul_rn(silu_f(gv), uv), prob));
+            const __nv_bfloat16 d = __float2bfloat16_rn(swiglu_fwd(gv, uv, prob));
             static_cast<__nv_bfloat16*>(p.out2)[row * p.ldo2 + f] = d;
             g[c] = __float_as_uint(fabsf(__bfloat162float(d)));
           }

@@ -26,8 +26,12 @@ constexpr int kMaxDevices = 64;
 // Device address of the scratch array for the current device.  In host code
 // the array's name only stands in for the device symbol, so the address must
 // be looked up on each device (with that device current) before a kernel can
-// use it.  The lookup happens once per device, on the first call there.
-unsigned* scratch_on_current_device(cudaError_t* err) {
+// use it.  A call made outside stream capture looks it up again every time,
+// so a device reset or a new context on the device (which reloads the module
+// at another address) is picked up; a call made while `stream` is capturing
+// uses the address the last uncaptured call on that device found (the first
+// call on a device must therefore come before any capture).
+unsigned* scratch_on_current_device(cudaStream_t stream, cudaError_t* err) {
   static unsigned* ptrs[kMaxDevices] = {nullptr};
   static std::mutex mu;
   int dev = 0;
@@ -37,12 +41,18 @@ unsigned* scratch_on_current_device(cudaError_t* err) {
     *err = cudaErrorInvalidDevice;
     return nullptr;
   }
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  *err = cudaStreamIsCapturing(stream, &cap);
+  if (*err != cudaSuccess) return nullptr;
   std::lock_guard<std::mutex> lock(mu);
-  if (!ptrs[dev]) {
+  if (cap == cudaStreamCaptureStatusNone) {
     void* p = nullptr;
     *err = cudaGetSymbolAddress(&p, g_weight_amax_scratch);
     if (*err != cudaSuccess) return nullptr;
     ptrs[dev] = static_cast<unsigned*>(p);
+  } else if (!ptrs[dev]) {
+    *err = cudaErrorStreamCaptureUnsupported;
+    return nullptr;
   }
   return ptrs[dev];
 }
@@ -71,7 +81,7 @@ extern "C" mpm_status mpm_nvfp4_quantize_weight_noalloc(const void* const* parts
   if (R % 128 != 0 || E * R > (1ll << 31) - 256) return MPM_ERR_SHAPE;
   if (!aligned16(q) || (reinterpret_cast<uintptr_t>(ts) % 4) != 0) return MPM_ERR_ALIGN;
   cudaError_t err = cudaSuccess;
-  unsigned* scratch = scratch_on_current_device(&err);
+  unsigned* scratch = scratch_on_current_device(stream, &err);
   if (!scratch) return MPM_ERR_CUDA;
   // The launcher clears the E amax slots it uses (an async memset on
   // `stream`) before the reduction, so the previous call's contents do not

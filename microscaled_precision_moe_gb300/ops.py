@@ -313,8 +313,13 @@ def moe_grouped_gemm(kind, group, epilogue, E, a_rows, N, K, seg, a, b, sfa, sfa
         d.aux_dev, d.ld_aux = aux.data_ptr(), aux.stride(-2)
     d.amax_dev = None if amax is None else amax.data_ptr()
     d.a_mn_major, d.b_mn_major = int(bool(a_mn_major)), int(bool(b_mn_major))
-    st = lib.mpm_moe_grouped_gemm(C.byref(d), _stream(a.device))
-    L.check(st, "mpm_moe_grouped_gemm")
+    if group == L.GROUP_K:
+        # the weight-gradient form has its own entry point
+        st = lib.mpm_moe_grouped_gemm_wgrad(C.byref(d), _stream(a.device))
+        L.check(st, "mpm_moe_grouped_gemm_wgrad")
+    else:
+        st = lib.mpm_moe_grouped_gemm(C.byref(d), _stream(a.device))
+        L.check(st, "mpm_moe_grouped_gemm")
     return out
 
 

@@ -26,7 +26,7 @@ Readings the pages leave open (each one is fixed here):
   u = columns [I, 2I); silu(g) = g / (1 + exp(-g)).
 * D is rounded to bf16 before its row amax and its re-quantisation.
 * The FC2 output Y_perm is rounded to bf16; the combine sums each token's k
-  rows in slot order and rounds once to bf16.
+  rows in binary32, in slot order, and rounds the sum once to bf16.
 * Backward: probabilities and routing are constants (no router gradient);
   dY_perm[row] = dY[token of row].
 """
@@ -129,12 +129,27 @@ def gather_rows(x: np.ndarray, perm: np.ndarray, k: int) -> np.ndarray:
 
 
 def combine(y_perm: np.ndarray, inv_perm: np.ndarray, T: int, k: int) -> np.ndarray:
-    """out[t] = sum over slots j (in order) of y_perm[inv_perm[t*k + j]]."""
+    """out[t] = bf16( y[inv[t*k]] + y[inv[t*k + 1]] + ... + y[inv[t*k + k-1]] ).
+
+    "miniTE technical report", section 5.3: each token's output is the sum of
+    its k expert outputs (the router weight was already applied to D in the
+    FC1 epilogue).  The section gives no accumulation order or precision, so
+    the reading fixed here is: start from +0.0 in binary32, add the token's
+    rows one at a time in slot order j = 0 .. k-1, each addition one IEEE
+    binary32 round-to-nearest-even step (numpy float32 arithmetic), then
+    round the binary32 sum once to bf16 (nearest, ties to even).  The order
+    matters: an fp64 sum, or another slot order, can land on another bf16
+    value.  y_perm holds bf16 values (exact in binary32).  Returns the bf16
+    values as fp64.
+    """
+    y = np.asarray(y_perm)
+    y32 = y.astype(np.float32)
+    assert np.array_equal(y32.astype(y.dtype), y), "combine input must be exact in binary32"
     inv = np.asarray(inv_perm, dtype=np.int64).reshape(T, k)
-    out = np.zeros((T,) + y_perm.shape[1:], dtype=np.float64)
+    acc = np.zeros((T,) + y.shape[1:], dtype=np.float32)
     for j in range(k):
-        out += y_perm[inv[:, j]]
-    return out
+        acc = np.add(acc, y32[inv[:, j]], dtype=np.float32)
+    return F.bf16_bits_to_f32(F.f32_to_bf16_bits(acc)).astype(np.float64)
 
 
 # ------------------------------------------------------------ NVFP4 forward
@@ -185,7 +200,7 @@ def nvfp4_moe_forward(x: np.ndarray, topk_ids, topk_prob, w1, w2, E: int, pad=RO
     b2 = dequant_weights_nvfp4((w2p, w2s, w2g))
     y = grouped_gemm(Q.nvfp4_dequantize(qd, sd, tsd), b2, seg)
     y_bf16 = F.bf16_round(y)
-    out = F.bf16_round(combine(y_bf16, inv, T, k))
+    out = combine(y_bf16, inv, T, k)
     return dict(qx=qx, sx=sx, tsx=tsx, seg=seg, perm=perm, inv=inv,
                 row_prob=row_prob, w1=(w1p, w1s, w1g), w2=(w2p, w2s, w2g),
                 acc1=acc1, d=d, amax_d=amax_d, qd=qd, sd=sd, tsd=tsd,
@@ -271,7 +286,7 @@ def nvfp4_moe_forward_single_pass(x: np.ndarray, topk_ids, topk_prob, w1, w2, E:
     k = np.asarray(topk_ids).shape[1]
     r = nvfp4_moe_forward(x, topk_ids, topk_prob, w1, w2, E, pad)
     s = nvfp4_fc2_online_amax(r["d"], r["seg"], r["w2"], tile_k)
-    s["out"] = F.bf16_round(combine(s["y"], r["inv"], T, k))
+    s["out"] = combine(s["y"], r["inv"], T, k)
     s["two_pass"] = r
     return s
 
@@ -330,7 +345,7 @@ def mxfp8_moe_fwd_bwd(x, topk_ids, topk_prob, w1, w2, dy, E: int, pad=ROW_PAD):
     # forward FC2
     b2 = np.stack([mx_rows(w2[e]) for e in range(E)])              # [E, H, I]
     y = F.bf16_round(grouped_gemm(mx_rows(d), b2, seg))
-    out = F.bf16_round(combine(y, inv, T, k))
+    out = combine(y, inv, T, k)
     # backward
     dyp = gather_rows(np.asarray(dy, dtype=np.float64), perm, k)   # [R_pad, H]
     w2c = np.stack([mx_cols_t(w2[e]) for e in range(E)])           # [E, I, H]
@@ -339,7 +354,7 @@ def mxfp8_moe_fwd_bwd(x, topk_ids, topk_prob, w1, w2, dy, E: int, pad=ROW_PAD):
     dh = F.bf16_round(swiglu_backward(dd, c1, row_prob, I))        # [R_pad, 2I]
     w1c = np.stack([mx_cols_t(w1[e]) for e in range(E)])           # [E, H, 2I]
     dxp = F.bf16_round(grouped_gemm(mx_rows(dh), w1c, seg))        # [R_pad, H]
-    dx = F.bf16_round(combine(dxp, inv, T, k))
+    dx = combine(dxp, inv, T, k)
     dw1 = grouped_wgrad(mx_cols_t(dh), mx_cols_t(xp), seg)         # [E, 2I, H]
     return dict(seg=seg, perm=perm, inv=inv, row_prob=row_prob, c1=c1, d=d,
                 y=y, out=out, dd=dd, dh=dh, dxp=dxp, dx=dx, dw1=dw1, dw2=dw2)
@@ -407,7 +422,7 @@ def nvfp4_moe_backward_bf16(fwd: dict, x, w1, w2, dy, mode: str):
     The SwiGLU derivative is taken at the forward's own FC1 output C1 (the
     fp64 GEMM of the NVFP4 operands, rounded to bf16 as the forward saves
     it); routing and probabilities are constants.  Returns the dict of
-    bf16_backward plus dx = bf16(combine(dX_perm)) and the operands used.
+    bf16_backward plus dx = combine(dX_perm) and the operands used.
     """
     T = np.asarray(x).shape[0]
     inv = np.asarray(fwd["inv"])
@@ -417,7 +432,7 @@ def nvfp4_moe_backward_bf16(fwd: dict, x, w1, w2, dy, mode: str):
     c1 = F.bf16_round(fwd["acc1"])
     dyp = gather_rows(np.asarray(dy, dtype=np.float64), fwd["perm"], k)
     r = bf16_backward(xp, b1, b2, d, c1, dyp, fwd["seg"], fwd["row_prob"], I)
-    r["dx"] = F.bf16_round(combine(r["dxp"], inv, T, k))
+    r["dx"] = combine(r["dxp"], inv, T, k)
     r.update(xp=xp, w1_op=b1, w2_op=b2, d_op=d, c1=c1, dyp=dyp)
     return r
 
@@ -449,7 +464,7 @@ def mxfp8_moe_bf16_backward(x, topk_ids, topk_prob, w1, w2, dy, E: int, mode: st
         raise ValueError(f"unknown backward mode {mode!r}")
     dyp = gather_rows(np.asarray(dy, dtype=np.float64), perm, k)
     r = bf16_backward(x_op, w1_op, w2_op, d_op, c1, dyp, seg, row_prob, I)
-    r["dx"] = F.bf16_round(combine(r["dxp"], inv, T, k))
+    r["dx"] = combine(r["dxp"], inv, T, k)
     r.update(seg=seg, perm=perm, inv=inv, row_prob=row_prob, c1=c1, d=d, xp=x_op,
              w1_op=w1_op, w2_op=w2_op, d_op=d_op, dyp=dyp)
     return r

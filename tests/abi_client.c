@@ -86,6 +86,26 @@ int main(void) {
   d.kind = 7;
   CHECK(mpm_moe_grouped_gemm(&d, 0) == MPM_ERR_UNSUPPORTED);
 
+  /* weight-gradient call: no descriptor; NVFP4 (wgrad is MXFP8 or BF16);
+     no segment offsets; a bf16 epilogue (wgrad writes fp32).  The call sets
+     the group itself, so a descriptor left at GROUP_M is taken as GROUP_K. */
+  CHECK(mpm_moe_grouped_gemm_wgrad(NULL, 0) == MPM_ERR_NULL);
+  d.kind = MPM_KIND_NVFP4;
+  d.group = MPM_GROUP_M;
+  d.N = 256;
+  d.K = 0;
+  d.seg_dev = (const int32_t*)dev;
+  CHECK(mpm_moe_grouped_gemm_wgrad(&d, 0) == MPM_ERR_UNSUPPORTED);
+  d.kind = MPM_KIND_MXFP8;
+  d.seg_dev = NULL;
+  CHECK(mpm_moe_grouped_gemm_wgrad(&d, 0) == MPM_ERR_NULL);
+  d.seg_dev = (const int32_t*)dev;
+  d.epilogue = MPM_EPI_BF16;
+  CHECK(mpm_moe_grouped_gemm_wgrad(&d, 0) == MPM_ERR_UNSUPPORTED);
+  d.epilogue = MPM_EPI_F32;
+  d.a_rows = 200;                                   /* M_out % 128 != 0 */
+  CHECK(mpm_moe_grouped_gemm_wgrad(&d, 0) == MPM_ERR_SHAPE);
+
   printf("abi_client: ok\n");
   return 0;
 }

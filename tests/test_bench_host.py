@@ -41,42 +41,57 @@ def test_clock_summary_without_samples():
 
 
 def test_gemm_traffic_only_while_the_sources_match(tmp_path, monkeypatch):
-    """roofline.traffic comes from the committed counters only while the GEMM
-    sources hash to the value recorded with them; an edited source or a
-    missing summary gives None."""
+    """roofline.traffic comes from the committed counter record (a JSON data
+    file, not the markdown report) only while the GEMM sources hash to the
+    value recorded with it; an edited source, a malformed or a missing record
+    gives None."""
     import hashlib
+    import json
     csrc = tmp_path / "microscaled_precision_moe_gb300" / "csrc"
     csrc.mkdir(parents=True)
     for name, body in (("gemm2.cu", b"pair"), ("gemm.cuh", b"decl"), ("common.cuh", b"util")):
         (csrc / name).write_bytes(body)
     digest = hashlib.sha256(b"pair" + b"decl" + b"util").hexdigest()
-    prof = tmp_path / "profiles"
-    prof.mkdir()
-    (prof / "nvfp4_fc1_fc2_T32768_H7168_I2048_E256_dram_traffic.md").write_text(
-        f"# counters\n\nfc1_traffic_bytes_per_launch: 123456\ngemm_source_sha256: {digest}\n")
+    rec = tmp_path / "traffic.json"
+    rec.write_text(json.dumps({"fc1_bytes_per_launch": 123456, "gemm_source_sha256": digest}))
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
-    assert bench._gemm_traffic() == 123456
+    assert bench.gemm_source_sha256() == digest
+    assert bench._gemm_traffic(str(rec)) == 123456
+    rec.write_text("{not json")
+    assert bench._gemm_traffic(str(rec)) is None
+    rec.write_text(json.dumps({"fc1_bytes_per_launch": 123456, "gemm_source_sha256": digest}))
     (csrc / "gemm2.cu").write_bytes(b"pair, edited")
-    assert bench._gemm_traffic() is None
-    (prof / "nvfp4_fc1_fc2_T32768_H7168_I2048_E256_dram_traffic.md").unlink()
-    assert bench._gemm_traffic() is None
+    assert bench._gemm_traffic(str(rec)) is None
+    rec.unlink()
+    assert bench._gemm_traffic(str(rec)) is None
 
 
 def test_gemm_traffic_of_the_committed_tree_is_consistent():
-    """In this tree the recorded hash predates the current pair kernel, so the
-    bench must report no traffic; if the counters are recaptured and the hash
-    updated, the value read back is the recorded one."""
-    import hashlib
-    csrc = os.path.join(ROOT, "microscaled_precision_moe_gb300", "csrc")
-    src = b"".join(open(os.path.join(csrc, f), "rb").read()
-                   for f in ("gemm2.cu", "gemm.cuh", "common.cuh"))
-    text = open(os.path.join(ROOT, "profiles",
-                             "nvfp4_fc1_fc2_T32768_H7168_I2048_E256_dram_traffic.md")).read()
-    recorded = [l.split(": ", 1)[1].strip() for l in text.split("\n")
-                if l.startswith("gemm_source_sha256: ")]
-    assert len(recorded) == 1
+    """The bench reports the recorded FC1 traffic exactly when the committed
+    record's hash is the current sources' hash, and nothing otherwise."""
+    import json
     t = bench._gemm_traffic()
-    if hashlib.sha256(src).hexdigest() == recorded[0]:
-        assert isinstance(t, int) and t > 0
+    if not os.path.exists(bench.TRAFFIC_FILE):
+        assert t is None
+        return
+    rec = json.load(open(bench.TRAFFIC_FILE))
+    if rec["gemm_source_sha256"] == bench.gemm_source_sha256():
+        assert t == int(rec["fc1_bytes_per_launch"]) and t > 0
     else:
         assert t is None
+
+
+def test_summary_of_a_line():
+    """The compact summary (the line's last key) reads the secondary lines
+    and tolerates missing ones."""
+    peaks = {"bf16": 1900.0, "bf16_sus": 1700.0, "hbm": 6800.0}
+    line = {"roofline": {"frac": 0.5},
+            "also": {"quantizers": {"mxfp8_quantize_8288x2048_rowcol": {"frac_hbm": 0.6}},
+                     "mxfp8_layer_fwd_bwd": {"ms_per_step": 2.5, "gemm_TFLOP/s": 1900.0},
+                     "stage_GBps_or_TFLOPs": {"fc2_TFLOP/s": 5000.0, "gather_frac_hbm": 0.95}}}
+    s = bench._summary(line, peaks)
+    assert s["fc1_frac_fp4"] == 0.5 and s["fc2_TFLOP/s"] == 5000.0
+    assert s["mxfp8_gemm_frac_fp8_burst"] == 0.5
+    assert s["stage_frac_hbm"] == {"gather": 0.95}
+    assert s["nvfp4_30b_ms"] is None and s["nvfp4_30b_frac_fp4_burst"] is None
+    assert bench._summary({"roofline": {"frac": 0.1}}, peaks)["decode_ms"] == {}

@@ -16,6 +16,14 @@ from tests.gpu_util import need_gpu, np_bf16, u8
 pytestmark = pytest.mark.gpu
 
 REL, ELEM = 1e-3, 1e-2
+# Bounds of the chained NVFP4 comparison (FC1 -> re-quantise -> FC2 ->
+# combine); the re-quantisation is discontinuous, so rows of D that the fp32
+# tensor-core accumulation rounds to a neighbouring bf16 value get other FP4
+# operands than the oracle's.
+D_ELEM_DIFF = 1e-3       # fraction of D elements that differ (each by one bf16 step at most)
+D_ROW_DIFF = 0.1         # fraction of D rows with any differing element
+REQUANT_REL = 0.1        # relative error of Y on those rows (NVFP4 re-quantisation noise)
+LAYER_REL = 1e-2         # relative Frobenius error of the layer output
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -91,20 +99,24 @@ def _chained_compare(d_gpu, y_gpu, out_gpu, r, k, what):
     ulp = np.abs(r["d"]) * 2.0 ** -7
     floor = 1e-4 * np.max(np.abs(r["d"]))
     assert np.all(np.abs(d - r["d"]) <= np.maximum(ulp, floor)), f"{what}: D beyond one step"
-    assert diff.mean() < 1e-3, f"{what}: {diff.mean():.2e} of D elements differ"
     same = ~diff.any(axis=1)
-    assert same.mean() > 0.9, f"{what}: only {same.mean():.3f} of D rows bit-identical"
     y = y_gpu[:R]
-    _assert_close(y[same], r["y"][same], f"{what}: FC2 rows with identical operands")
+    rel_re = 0.0
     if (~same).any():
-        rel = np.linalg.norm(y[~same] - r["y"][~same]) / np.linalg.norm(r["y"][~same])
-        assert rel < 0.1, f"{what}: re-quantised rows differ by {rel:.3e}"
+        rel_re = float(np.linalg.norm(y[~same] - r["y"][~same]) / np.linalg.norm(r["y"][~same]))
+    rel_out = Mx.rel_frobenius(out_gpu, r["out"])
+    print(f"PARITY-STATS {what}: D elements differing {diff.mean():.3e}, D rows differing "
+          f"{1.0 - same.mean():.4f}, re-quantised rows rel {rel_re:.3e}, layer rel {rel_out:.3e}")
+    assert diff.mean() < D_ELEM_DIFF, f"{what}: {diff.mean():.2e} of D elements differ"
+    assert 1.0 - same.mean() < D_ROW_DIFF, f"{what}: {1.0 - same.mean():.3f} of D rows differ"
+    _assert_close(y[same], r["y"][same], f"{what}: FC2 rows with identical operands")
+    assert rel_re < REQUANT_REL, f"{what}: re-quantised rows differ by {rel_re:.3e}"
     rows_ok = np.ones(R, dtype=bool)
     rows_ok[~same] = False
     inv = r["inv"].reshape(-1, k)
     tok_ok = rows_ok[inv].all(axis=1)
     _assert_close(out_gpu[tok_ok], r["out"][tok_ok], f"{what}: output of unaffected tokens")
-    assert Mx.rel_frobenius(out_gpu, r["out"]) < 1e-2, f"{what}: layer output"
+    assert rel_out < LAYER_REL, f"{what}: layer output {rel_out:.3e}"
 
 
 @pytest.mark.parametrize("tile_m", [128, 256, 1])
@@ -138,6 +150,47 @@ def test_nvfp4_grouped_fc1_swiglu_and_fc2(tile_m):
     amax_ref = np.max(np.abs(np_bf16(d)[:R]), axis=1)
     assert np.array_equal(amax.cpu().numpy()[:R], amax_ref), "amax(D) equals the row max of D"
     _chained_compare(np_bf16(d), np_bf16(y), np_bf16(out), r, k, "NVFP4 layer")
+
+
+def _fc1_by_flat_row(shape, tile_m):
+    """FC1 (NVFP4, SwiGLU x prob epilogue) with the given GEMM kernel; D and
+    amax(D) returned in routed-row order (token-major, slot-minor), which does
+    not depend on the segment padding the kernel needs."""
+    ops, L = _ops(), _L()
+    ids, prob, x, w1, w2, seg, perm, inv, rp, cap = _grouped_nvfp4_setup(shape, pad=_pad(tile_m))
+    E, H, I, k = shape.E, shape.H, shape.I, shape.k
+    qx, sx, tsx = ops.nvfp4_quantize_per_token(x)
+    amax = torch.empty(cap, dtype=torch.float32, device="cuda")
+    aq, as_, ats = ops.moe_gather_nvfp4(qx, sx, tsx, H, perm, seg, E, k, cap, amax_zero=amax)
+    q1, s1, t1 = ops.nvfp4_quantize_weight([w1.contiguous()])
+    d = torch.empty(cap, I, dtype=torch.bfloat16, device="cuda")
+    ops.moe_grouped_gemm(L.KIND_NVFP4, L.GROUP_M, L.EPI_SWIGLU, E, cap, 2 * I, H, seg,
+                         aq, q1.view(E * 2 * I, H // 2), as_, H // 16, s1, H // 16, d,
+                         b_rows_per_expert=2 * I, alpha_a=ats, alpha_b=t1, row_prob=rp,
+                         out2=d, amax=amax, tile_m=tile_m)
+    torch.cuda.synchronize()
+    assert ops.get_device_status() == 0
+    idx = inv.long()
+    return d[idx].contiguous().view(torch.int16).cpu().numpy(), amax[idx].cpu().numpy()
+
+
+@pytest.mark.parametrize("shape", [
+    synth.scaled(synth.MOE_30B, T=300, H=512, I=256, E=6, k=4),
+    synth.scaled(synth.MOE_30B, T=2048, E=32),
+    synth.scaled(synth.MOE_671B, T=1024, E=16),
+], ids=["small", "30b_H2048_I768", "671b_H7168_I2048"])
+def test_nvfp4_fc1_identical_across_kernels(shape):
+    """The one-CTA (128-row tiles), CTA-pair (256-row tiles) and small-M
+    kernels give byte-identical D and amax(D) for every routed row: one
+    activation definition in every epilogue, so which kernel runs (a choice
+    made from the batch size) never changes the FP4 re-quantisation."""
+    ref_d, ref_a = _fc1_by_flat_row(shape, 128)
+    for tile_m in (256, 1):
+        d, a = _fc1_by_flat_row(shape, tile_m)
+        bad = np.flatnonzero((d != ref_d).any(axis=1))
+        assert bad.size == 0, (f"tile_m {tile_m}: {bad.size} of {d.shape[0]} D rows differ from "
+                               f"the one-CTA kernel's (first routed row {bad[0]})")
+        assert np.array_equal(a.view(np.uint32), ref_a.view(np.uint32)), f"tile_m {tile_m}: amax"
 
 
 @pytest.mark.parametrize("tile_m", [128, 256, 1])

@@ -8,7 +8,7 @@ from oracle import moe as MO
 from oracle import quant as Q
 from oracle import formats as F
 from microscaled_precision_moe_gb300 import synth
-from tests.gpu_util import need_gpu, np_bf16, u8, assert_bytes_equal
+from tests.gpu_util import need_gpu, np_bf16, u8, assert_bytes_equal, bf16_bits
 
 pytestmark = pytest.mark.gpu
 
@@ -95,14 +95,37 @@ def test_gather_bf16_and_nvfp4_and_combine():
     assert_bytes_equal(got_s, MO.gather_rows(rs, rperm, shape.k), "gathered scales")
     assert_bytes_equal(dts.cpu().numpy()[:R].view(np.uint32),
                        MO.gather_rows(rts, rperm, shape.k).view(np.uint32), "gathered ts")
-    # combine: y_perm = gathered bf16 rows scaled per row; out = slot-order fp32 sum
+    # combine: y_perm = gathered bf16 rows scaled per row (padding rows are
+    # never referenced); the output equals the oracle's combine bit for bit
     y = (xp.float() * torch.linspace(0.5, 1.5, cap, device="cuda")[:, None]).to(torch.bfloat16)
     out = ops.moe_combine(y, inv, shape.T, shape.k)
     torch.cuda.synchronize()
-    yn = np_bf16(y).astype(np.float64)
-    inv_n = rinv.reshape(shape.T, shape.k)
-    acc = np.zeros((shape.T, shape.H), dtype=np.float32)
-    for j in range(shape.k):
-        acc = (acc + yn[inv_n[:, j]].astype(np.float32)).astype(np.float32)   # fp32, slot order
-    ref_out = F.bf16_bits_to_f32(F.f32_to_bf16_bits(acc))
-    assert np.array_equal(np_bf16(out), ref_out)
+    ref_out = MO.combine(np_bf16(y)[:R], rinv, shape.T, shape.k)
+    assert_bytes_equal(bf16_bits(out), F.f64_to_bf16_bits(ref_out), "combine")
+
+
+def test_combine_cancellation_and_signed_zero():
+    """Rows chosen so the binary32 running sum rounds, cancels to zero and
+    meets signed zeros: the kernel equals the oracle's combine bit for bit."""
+    ops = _ops()
+    T, k, H = 64, 8, 256
+    rng = np.random.default_rng(7)
+    base = rng.standard_normal((T * k, H)) * 2.0 ** rng.integers(-20, 20, (T * k, 1))
+    y = torch.from_numpy(base).to(torch.bfloat16)
+    yv = y.float().numpy()
+    # token 0: x, -x pairs (exact cancellation to +0); token 1: all -0.0
+    yv[0:8] = np.repeat(yv[0:1], 8, axis=0) * np.array([1, -1] * 4)[:, None]
+    yv[8:16] = -0.0
+    # token 2: 1, 2**-8, 2**-30 ... (binary32 loses the tail, bf16 tie to even)
+    yv[16:24] = 0.0
+    yv[16], yv[17], yv[18] = 1.0, 2.0 ** -8, 2.0 ** -30
+    y = torch.from_numpy(yv).to(torch.bfloat16)
+    perm_rows = rng.permutation(T * k).astype(np.int32)          # any row order
+    y_perm = torch.empty_like(y)
+    y_perm[torch.from_numpy(perm_rows.astype(np.int64))] = y
+    inv = torch.from_numpy(perm_rows).cuda()
+    out = ops.moe_combine(y_perm.cuda(), inv, T, k)
+    torch.cuda.synchronize()
+    ref = MO.combine(y_perm.float().numpy(), perm_rows, T, k)
+    assert_bytes_equal(bf16_bits(out), F.f64_to_bf16_bits(ref), "combine")
+    assert np.all(bf16_bits(out[1]) == 0)                        # +0, not -0

@@ -140,19 +140,73 @@ def test_swiglu_backward_vs_finite_difference():
         assert abs((f(cp) - f(cm)) / (2 * h) - dh[r, c]) < 1e-6
 
 
+def _rne_exact(x, p, emin):
+    """Round the exact rational x to the nearest point of a binary floating
+    grid with p significant bits and smallest normal exponent emin (ties to
+    an even last bit), in exact arithmetic."""
+    from fractions import Fraction
+    if x == 0:
+        return Fraction(0)
+    a = abs(x)
+    e = a.numerator.bit_length() - a.denominator.bit_length()
+    if Fraction(2) ** e > a:
+        e -= 1
+    elif Fraction(2) ** (e + 1) <= a:
+        e += 1
+    ulp = Fraction(2) ** (max(e, emin) - (p - 1))
+    q = a / ulp
+    n = q.numerator // q.denominator
+    rem = q - n
+    if rem > Fraction(1, 2) or (rem == Fraction(1, 2) and n % 2 == 1):
+        n += 1
+    return (n * ulp) if x > 0 else -(n * ulp)
+
+
+def _combine_exact(rows):
+    """Brute force of the combine reading: binary32 running sum from +0 in the
+    given order (each step rounded exactly to 24 bits), then one rounding to
+    bf16 (8 bits)."""
+    from fractions import Fraction
+    acc = Fraction(0)
+    for v in rows:
+        acc = _rne_exact(acc + Fraction(float(v)), 24, -126)
+    return _rne_exact(acc, 8, -126)
+
+
 def test_combine_brute_force():
+    """The combine against an exact-rational brute force of its reading, on
+    random bf16 rows spread over many binades (so additions round)."""
+    from fractions import Fraction
     rng = np.random.default_rng(4)
-    T, k, H = 6, 3, 5
-    ids, prob = _tiny_routing(T, 4, k)
-    seg, perm, inv, _ = MO.build_segments(ids, prob, 4)
-    y = rng.standard_normal((seg[-1], H))
+    T, k, H = 6, 8, 5
+    ids, prob = _tiny_routing(T, 10, k)
+    seg, perm, inv, _ = MO.build_segments(ids, prob, 10)
+    y = _bf16(rng.standard_normal((seg[-1], H)) * 2.0 ** rng.integers(-12, 12, (seg[-1], 1)))
+    y = y.astype(np.float64)
     out = MO.combine(y, inv, T, k)
     for t in range(T):
-        s = np.zeros(H)
-        for j in range(k):
-            r = [r for r in range(seg[-1]) if perm[r] == t * k + j][0]
-            s += y[r]
-        assert np.allclose(out[t], s, rtol=0, atol=1e-12)
+        rows = [[r for r in range(seg[-1]) if perm[r] == t * k + j][0] for j in range(k)]
+        for c in range(H):
+            assert Fraction(float(out[t, c])) == _combine_exact([y[r, c] for r in rows])
+    # a sum of zeros (or of x and -x) is +0
+    z = np.array([[0.0], [-0.0], [1.5], [-1.5]])
+    zo = MO.combine(z, np.array([0, 1, 2, 3]), 2, 2)
+    assert np.all(zo == 0) and not np.any(np.signbit(zo))
+
+
+def test_combine_binary32_order_decides_the_bf16_value():
+    """Cases where the reading decides the result: the fp64 sum of
+    [1, 2**-8, 2**-30] lies just above the bf16 midpoint 1 + 2**-8 and rounds
+    up, while the binary32 running sum loses 2**-30 and lands on the midpoint,
+    which rounds to even (1.0); reordering [1, -1, 2**-30] to [1, 2**-30, -1]
+    changes the binary32 sum from 2**-30 to 0."""
+    y = np.array([[1.0], [2.0 ** -8], [2.0 ** -30]])
+    out = MO.combine(y, np.array([0, 1, 2]), 1, 3)
+    assert out[0, 0] == 1.0 == float(_combine_exact([1.0, 2.0 ** -8, 2.0 ** -30]))
+    assert F.bf16_round(np.array([1.0 + 2.0 ** -8 + 2.0 ** -30]))[0] == 1.0 + 2.0 ** -7
+    y2 = np.array([[1.0], [-1.0], [2.0 ** -30]])
+    assert MO.combine(y2, np.array([0, 1, 2]), 1, 3)[0, 0] == 2.0 ** -30
+    assert MO.combine(y2, np.array([0, 2, 1]), 1, 3)[0, 0] == 0.0
 
 
 def _token_centric_nvfp4(x, ids, prob, w1, w2):
