@@ -142,6 +142,29 @@ mpm_status mpm_nvfp4_quantize_per_token(const void* x_dev, int64_t M, int64_t K,
                                         cudaStream_t stream);
 
 /*
+ * NVFP4 quantisation with a running row amax, tile by tile: the activation
+ * side of the single-pass FC2.  Source: "miniTE technical report", section
+ * 5.6 (a row is consumed in K tiles; the row amax seen so far sets the outer
+ * scale gs = gamax / 2688 each tile is encoded against; the FC2 partial sum
+ * is compensated when gs grows; see MPM_EPI_BF16_ONLINE).
+ *
+ * Per row, tiles t = 0, 1, ... of 256 columns in order:
+ *   gamax_t = max(gamax_{t-1}, max |x| over tile t)   (gamax_{-1} = 0)
+ *   gs_t    = gamax_t / 2688 with the 2^-116 floor; gamax_t = 0 -> gs_t = 0
+ *   the tile's 16-blocks: the steps of mpm_nvfp4_quantize_per_token with
+ *   gs_t in place of s_g.
+ * x_dev: bf16 [M, K] (leading dimension ldx).  q_dev: u8 [M, K/2];
+ * s_dev: scales [M, K/16] in 128x4 tiles; tile_scale_dev: fp32 [M, K/256]
+ * (gs_t of row r at r * K/256 + t).  m_valid_dev (nullable) as for
+ * mpm_nvfp4_quantize_per_token.
+ * Requirements: M >= 1, K % 256 == 0, 256 <= K <= 8192, ldx >= K,
+ * ldx % 8 == 0, pointers 16-byte aligned (tile_scale_dev 4-byte).
+ */
+mpm_status mpm_nvfp4_quantize_online(const void* x_dev, int64_t M, int64_t K, int64_t ldx,
+                                     uint8_t* q_dev, uint8_t* s_dev, float* tile_scale_dev,
+                                     const int32_t* m_valid_dev, cudaStream_t stream);
+
+/*
  * NVFP4 weight quantisation with one FP32 outer scale per expert shared by
  * all given parts (gate and up quantised jointly so that the fused gate|up
  * GEMM sees one weight scale).
@@ -342,6 +365,9 @@ mpm_status mpm_transpose_bf16(const void* in_dev, int64_t R, int64_t C, int64_t 
 #define MPM_EPI_SWIGLU 2         /* out2 = D bf16 [rows, N/2], amax atomically max'd */
 #define MPM_EPI_SWIGLU_SAVE 3    /* SWIGLU and out = C bf16 [rows, N] (gate|up)     */
 #define MPM_EPI_DSWIGLU 4        /* out = dH bf16 [rows, 2N] from aux = C bf16       */
+#define MPM_EPI_BF16_ONLINE 5    /* out bf16 [rows, N] = alpha_b[e] * sum_t aux[row, t] *
+                                    (the product over reduction tile t of 256): the
+                                    FC2 of the single-pass FFN (NVFP4, tile_m 256)   */
 
 /*
  * Descriptor of one grouped GEMM  C_e = A_e * B_e^T  (both operands K-major,
@@ -370,6 +396,14 @@ mpm_status mpm_transpose_bf16(const void* in_dev, int64_t R, int64_t C, int64_t 
  *   max(amax_dev[r], max_j |D[r, j]|) (fp32 bits, caller zeroes it first);
  *   DSWIGLU: dD = acc, with (g, u) read from aux (bf16 C, [rows, 2N]):
  *   dH[r, j] = dD*p*u*silu'(g), dH[r, N+j] = dD*p*silu(g), bf16.
+ *   BF16_ONLINE (NVFP4, tile_m 256, GROUP_M): A quantised tile by tile with
+ *   a running row amax (mpm_nvfp4_quantize_online); aux = its fp32 outer
+ *   scales [rows, ld_aux] (ld_aux >= K/256), alpha_a_dev must be NULL:
+ *   out[r, n] = bf16( alpha_b[e] * sum_t aux[r, t] * P_t[r, n] ), P_t the
+ *   block-scaled product over reduction columns [256 t, 256 t + 256).  This
+ *   is the compensated partial sum of "miniTE technical report", section 5.6
+ *   (O <- O * gs_prev / gs_t + P_t, Y = O * gs_last * s_g(W2)) written as
+ *   its closed form; CTA pairs on 256 x 128 output tiles, N % 128 == 0.
  * Source: "miniTE technical report", section 5.2 (grouped GEMM over a
  * contiguous buffer with device offsets), section 5.4 (FC1 epilogue:
  * ACC x alpha_a[m] (x alpha_b), C = gate|up, D = act(gate, up) x prob, amax

@@ -21,7 +21,7 @@ ROWWISE, COLWISE = 1, 2
 KIND_NVFP4, KIND_MXFP8, KIND_BF16 = 0, 1, 2
 GROUP_M, GROUP_K = 0, 1
 TILE_SMALL_M = 1
-EPI_F32, EPI_BF16, EPI_SWIGLU, EPI_SWIGLU_SAVE, EPI_DSWIGLU = 0, 1, 2, 3, 4
+EPI_F32, EPI_BF16, EPI_SWIGLU, EPI_SWIGLU_SAVE, EPI_DSWIGLU, EPI_BF16_ONLINE = 0, 1, 2, 3, 4, 5
 GATHER_BF16, GATHER_NVFP4 = 0, 1
 
 _vp, _i64, _u32, _int, _sz = C.c_void_p, C.c_int64, C.c_uint, C.c_int, C.c_size_t
@@ -53,6 +53,7 @@ _SIGS = {
     "mpm_scale_bytes": (_sz, [_i64, _i64]),
     "mpm_mxfp8_quantize": (_int, [_vp, _i64, _i64, _i64, _u32, _vp, _vp, _vp, _i64, _vp, _vp, _vp]),
     "mpm_nvfp4_quantize_per_token": (_int, [_vp, _i64, _i64, _i64, _vp, _vp, _vp, _vp, _vp, _vp]),
+    "mpm_nvfp4_quantize_online": (_int, [_vp, _i64, _i64, _i64, _vp, _vp, _vp, _vp, _vp]),
     "mpm_nvfp4_weight_workspace_bytes": (_sz, [_i64]),
     "mpm_nvfp4_quantize_weight": (_int, [C.POINTER(_vp), C.POINTER(_i64), _int, _i64, _i64,
                                          _vp, _vp, _vp, _vp, _sz, _vp]),

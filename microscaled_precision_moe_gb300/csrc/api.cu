@@ -191,6 +191,16 @@ mpm_status mpm_nvfp4_quantize_per_token(const void* x, int64_t M, int64_t K, int
                                                  stream));
 }
 
+mpm_status mpm_nvfp4_quantize_online(const void* x, int64_t M, int64_t K, int64_t ldx, uint8_t* q,
+                                     uint8_t* s, float* gs, const int32_t* m_valid,
+                                     cudaStream_t stream) {
+  if (!x || !q || !s || !gs) return MPM_ERR_NULL;
+  if (M < 1 || K < 256 || K % 256 != 0 || K > 8192 || ldx < K) return MPM_ERR_SHAPE;
+  if (M > (1ll << 31) - 256) return MPM_ERR_SHAPE;
+  if (!aligned(x, 16) || ldx % 8 != 0 || !aligned(q, 16) || !aligned(gs, 4)) return MPM_ERR_ALIGN;
+  return cuda_status(mpm::launch_nvfp4_online(x, M, (int)K, ldx, q, s, gs, m_valid, stream));
+}
+
 size_t mpm_nvfp4_weight_workspace_bytes(int64_t E) {
   return E > 0 ? (size_t)pad_to(E * 4, 256) : 0;
 }
@@ -325,7 +335,16 @@ mpm_status mpm_moe_grouped_gemm(const mpm_grouped_gemm_desc* d, cudaStream_t str
     const bool ok_k = d->group == MPM_GROUP_K && maj == 3 && d->epilogue == MPM_EPI_F32;
     if (!ok_m && !ok_k) return MPM_ERR_UNSUPPORTED;
   }
-  if (d->epilogue < MPM_EPI_F32 || d->epilogue > MPM_EPI_DSWIGLU) return MPM_ERR_UNSUPPORTED;
+  if (d->epilogue < MPM_EPI_F32 || d->epilogue > MPM_EPI_BF16_ONLINE) return MPM_ERR_UNSUPPORTED;
+  if (d->epilogue == MPM_EPI_BF16_ONLINE) {
+    // FC2 of the single-pass FFN: NVFP4, CTA pairs, row segments only
+    if (d->kind != MPM_KIND_NVFP4 || tile_m != 256 || d->group != MPM_GROUP_M || maj != 0)
+      return MPM_ERR_UNSUPPORTED;
+    if (!d->seg_dev || !d->aux_dev) return MPM_ERR_NULL;
+    if (d->alpha_a_dev) return MPM_ERR_UNSUPPORTED;      // the outer scales are per tile, in aux
+    if (d->K % 256 != 0 || d->ld_aux < d->K / 256) return MPM_ERR_SHAPE;
+    if (!aligned(d->aux_dev, 4)) return MPM_ERR_ALIGN;
+  }
   if (!d->a_dev || !d->b_dev || !d->out_dev) return MPM_ERR_NULL;
   if (!bf16 && (!d->sfa_dev || !d->sfb_dev)) return MPM_ERR_NULL;
   if (d->E < 1 || d->E > 65535 || d->N < 256 || d->N % 256 != 0 || d->a_rows < 1)
@@ -411,9 +430,32 @@ mpm_status mpm_moe_grouped_gemm(const mpm_grouped_gemm_desc* d, cudaStream_t str
     const long long n_out = d->epilogue == MPM_EPI_SWIGLU ? d->N / 2 : d->N;
     if (n_out % 128 != 0) return MPM_ERR_SHAPE;
     const int n_wt = (int)(n_out / 128);
+    // one dense group of at most 128 rows (the single-expert GEMM): split K
+    // over a cluster of CTAs per weight tile instead of giving only n_wt
+    // CTAs the whole K chain
+    const int nkb = (int)(d->K / elems_per_kb);
+    if (!d->seg_dev && d->a_rows <= 128 && nkb >= 2 &&
+        (d->epilogue == MPM_EPI_F32 || d->epilogue == MPM_EPI_BF16)) {
+      int ks = 1;
+      for (int c = 8; c >= 2; c >>= 1)
+        if (nkb >= c) { ks = c; break; }
+      return cuda_status(mpm::launch_gemm_splitk(d->kind, d->epilogue, ta, tb, a, n_wt, ks, stream));
+    }
     const long long n_tasks = (long long)n_wt * ((d->a_rows + 127) / 128);
     return cuda_status(mpm::launch_grouped_gemm_small(d->kind, d->epilogue, ta, tb, a, n_wt, n_tasks,
                                                       stream));
+  }
+  if (d->epilogue == MPM_EPI_BF16_ONLINE) {
+    CUtensorMap tb64, tsa, tsb, tout;
+    if (!make_tmap(&tb64, d->b_dev, d->ldb_bytes, d->b_total_rows, 64)) return MPM_ERR_CUDA;
+    const long long atoms_a = pad_to(d->a_total_rows, 128) * pad_to(d->sfa_cols, 4) / 512;
+    const long long atoms_b = pad_to(d->b_total_rows, 128) * pad_to(d->sfb_cols, 4) / 512;
+    if (!make_sf_tmap(&tsa, d->sfa_dev, atoms_a, 4)) return MPM_ERR_CUDA;
+    if (!make_sf_tmap(&tsb, d->sfb_dev, atoms_b, 4)) return MPM_ERR_CUDA;
+    if (!make_out_tmap(&tout, d->out_dev, d->N, d->a_rows, d->ldo)) return MPM_ERR_CUDA;
+    const int n_tiles = (int)(d->N / 128);
+    const long long n_tasks = (long long)n_tiles * ((d->a_rows + 255) / 256);
+    return cuda_status(mpm::launch_fc2_online(ta, tb64, tsa, tsb, tout, a, n_tiles, n_tasks, stream));
   }
   if (tile_m == 256) {
     const int kind_atoms = d->kind == MPM_KIND_NVFP4 ? 4 : 1;
@@ -426,9 +468,13 @@ mpm_status mpm_moe_grouped_gemm(const mpm_grouped_gemm_desc* d, cudaStream_t str
       if (!make_sf_tmap(&tsa, d->sfa_dev, atoms_a, kind_atoms)) return MPM_ERR_CUDA;
       if (!make_sf_tmap(&tsb, d->sfb_dev, atoms_b, kind_atoms)) return MPM_ERR_CUDA;
     }
-    CUtensorMap tout;
+    CUtensorMap tout, taux;
     std::memset(&tout, 0, sizeof(tout));
-    if (d->epilogue == MPM_EPI_BF16) {
+    std::memset(&taux, 0, sizeof(taux));
+    if (d->epilogue == MPM_EPI_DSWIGLU) {
+      if (!make_out_tmap(&tout, d->out_dev, 2 * d->N, d->a_rows, d->ldo)) return MPM_ERR_CUDA;
+      if (!make_out_tmap(&taux, d->aux_dev, 2 * d->N, d->a_rows, d->ld_aux)) return MPM_ERR_CUDA;
+    } else if (d->epilogue == MPM_EPI_BF16) {
       if (!make_out_tmap(&tout, d->out_dev, d->N, d->a_rows, d->ldo)) return MPM_ERR_CUDA;
     } else if (d->epilogue == MPM_EPI_F32) {
       const long long rows = d->group == MPM_GROUP_K ? d->E * d->a_rows : d->a_rows;
@@ -440,7 +486,7 @@ mpm_status mpm_moe_grouped_gemm(const mpm_grouped_gemm_desc* d, cudaStream_t str
     long long n_tasks = (long long)n_tiles * ((d->a_rows + 255) / 256);
     if (d->group == MPM_GROUP_K) n_tasks *= d->E;
     return cuda_status(mpm::launch_grouped_gemm_pair(d->kind, d->epilogue, maj, ta, tb, tsa, tsb, tout,
-                                                     a, n_tiles, n_tasks, stream));
+                                                     taux, a, n_tiles, n_tasks, stream));
   }
   dim3 grid;
   if (d->group == MPM_GROUP_M) {

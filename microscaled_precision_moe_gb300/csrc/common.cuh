@@ -65,18 +65,28 @@ MPM_DEV uint32_t float_bits(float f) { return __float_as_uint(f); }
 // ---------------------------------------------------------------- SwiGLU
 // The activation of every FC1 epilogue and its derivative for the SwiGLU
 // backward, defined once so that D (and dH) do not depend on which GEMM
-// kernel produced them: every step is one IEEE binary32 operation (CUDA's
-// expf, correctly rounded division, no contraction into FMAs).
+// kernel produced them (the three kernels give byte-identical D).
 //   silu(g) = g / (1 + e^-g)
 //   D       = silu(g) * u * p
-MPM_DEV float swiglu_silu(float g) { return __fdiv_rn(g, __fadd_rn(1.0f, expf(-g))); }
+// e^-g is the hardware exponential (__expf: ex2.approx of g * log2 e) and
+// the division the fast one (__fdividef), each a few fp32 ulps from the
+// correctly rounded result; every other step is one IEEE binary32 operation
+// with no contraction into FMAs.  The result is rounded to bf16 (8
+// significant bits) right after, so these ulps move an element of D only
+// when its value lies within a few fp32 ulps of a bf16 rounding midpoint,
+// the same order as the fp32 accumulation error of the GEMM itself.  The
+// correctly rounded forms (expf and IEEE division) cost 15 % of the
+// headline FC1 on GB300 (3.21 against 2.80 ms): the epilogue warps' extra
+// instructions share the SM sub-partitions' issue slots with the warps that
+// feed the tensor cores.
+MPM_DEV float swiglu_silu(float g) { return __fdividef(g, __fadd_rn(1.0f, __expf(-g))); }
 MPM_DEV float swiglu_fwd(float g, float u, float prob) {
   return __fmul_rn(__fmul_rn(swiglu_silu(g), u), prob);
 }
 // dD -> (dg, du) for D = silu(g) * u * p with p constant:
 //   dg = (dD p) u s (1 + g (1 - s)),  du = (dD p) g s,  s = 1 / (1 + e^-g)
 MPM_DEV void swiglu_bwd(float g, float u, float dd, float prob, float& dg, float& du) {
-  const float s = __fdiv_rn(1.0f, __fadd_rn(1.0f, expf(-g)));
+  const float s = __fdividef(1.0f, __fadd_rn(1.0f, __expf(-g)));
   const float dp = __fmul_rn(dd, prob);
   const float dsilu = __fmul_rn(s, __fadd_rn(1.0f, __fmul_rn(g, __fsub_rn(1.0f, s))));
   dg = __fmul_rn(__fmul_rn(dp, u), dsilu);

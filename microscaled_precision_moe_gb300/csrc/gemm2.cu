@@ -103,10 +103,21 @@ constexpr int OUT_BOX_COLS = 64;
 constexpr int OUT_BOX_BYTES = BM * OUT_BOX_COLS * 2;    // 16 KB
 constexpr int STAGE_OUT_BYTES = 2 * OUT_BOX_BYTES;      // 32 KB
 
-template <int KIND>
+// The SwiGLU-backward epilogue streams C in and dH out through two staging
+// buffers of 32 KB (one 64-column chunk of gate and of up each), so its ring
+// has one stage less than the kind's default (the bf16 kind: two less).
+template <int KIND, int EPI>
+constexpr int stages() {
+  return EPI == MPM_EPI_DSWIGLU ? (KIND == MPM_KIND_BF16 ? 5 : 4) : Cfg<KIND>::kStages;
+}
+template <int EPI>
+constexpr int out_staging_bytes() {
+  return EPI == MPM_EPI_DSWIGLU ? 2 * STAGE_OUT_BYTES : STAGE_OUT_BYTES;
+}
+template <int KIND, int EPI>
 constexpr int smem_bytes() {
-  return 2048 + Cfg<KIND>::kStages * stage_bytes<KIND>() + STAGE_OUT_BYTES +
-         (4 * Cfg<KIND>::kStages + 4) * 8 + 32;
+  return 2048 + stages<KIND, EPI>() * stage_bytes<KIND>() + out_staging_bytes<EPI>() +
+         (4 * stages<KIND, EPI>() + 4) * 8 + 32 + 16;
 }
 
 MPM_DEV uint32_t pack_bf16(float lo, float hi) {
@@ -210,7 +221,8 @@ MPM_DEV Task task_of(const GemmArgs& p, long long t, int n_tiles, int* bad, SegC
 
 struct PairMaps {
   CUtensorMap a, b, sfa, sfb;
-  CUtensorMap out;    // bf16 output of the BF16 epilogue / D of the SwiGLU epilogues
+  CUtensorMap out;    // bf16 output of the BF16 epilogue / D of the SwiGLU epilogues / dH
+  CUtensorMap aux;    // C = gate|up read by the SwiGLU-backward epilogue
 };
 
 // MAJ (bf16 only): bit 0 = A stored MN-major ([K rows, M] with M contiguous:
@@ -246,7 +258,7 @@ grouped_gemm_pair_kernel(const __grid_constant__ PairMaps maps, const GemmArgs p
   using C = Cfg<KIND>;
   constexpr bool A_MN = (MAJ & 1) != 0, B_MN = (MAJ & 2) != 0;
   static_assert(MAJ == 0 || KIND == MPM_KIND_BF16, "MN-major operands are bf16 only");
-  constexpr int S = C::kStages;
+  constexpr int S = stages<KIND, EPI>();
   extern __shared__ uint8_t smem_raw[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_ctarank();          // 0 = leader of the pair
@@ -261,7 +273,7 @@ grouped_gemm_pair_kernel(const __grid_constant__ PairMaps maps, const GemmArgs p
   const uint32_t sSFB = sSFA + S * C::kSfaBytes;
   // the 128-byte-swizzled staging boxes need a 1024-byte-aligned base
   const uint32_t sOut = (sSFB + S * C::kSfbBytes + 1023u) & ~1023u;
-  const uint32_t sBar = sOut + STAGE_OUT_BYTES;
+  const uint32_t sBar = sOut + out_staging_bytes<EPI>();
   const uint32_t bar_full = sBar, bar_empty = sBar + 8 * S;
   // accumulator buffer b: full barrier at bar_acc + 16 b, empty at + 8.  The
   // bf16 kind keeps two accumulators in TMEM (columns 0-255 and 256-511, no
@@ -272,6 +284,7 @@ grouped_gemm_pair_kernel(const __grid_constant__ PairMaps maps, const GemmArgs p
   const uint32_t sFlag = sTmem + 8;
   const uint32_t bar_sf = bar_acc + 48;        // scale tiles of a stage are in TMEM
   const uint32_t bar_sfull = bar_sf + 8 * S;   // scale tiles of a stage are in shared memory
+  const uint32_t bar_c = bar_sfull + 8 * S;    // SwiGLU backward: C chunk in staging buffer b (+8 b)
   volatile uint32_t* tmem_holder = reinterpret_cast<volatile uint32_t*>(gbase + (sTmem - base));
   volatile int* fail_flag = reinterpret_cast<volatile int*>(gbase + (sFlag - base));
 
@@ -290,6 +303,10 @@ grouped_gemm_pair_kernel(const __grid_constant__ PairMaps maps, const GemmArgs p
       mbar_init(bar_sf + 8 * s, C::kSfStore ? 2 : C::kSfWarps);
       mbar_init(bar_sfull + 8 * s, 1);
     }
+    if (EPI == MPM_EPI_DSWIGLU) {
+      mbar_init(bar_c, 1);
+      mbar_init(bar_c + 8, 1);
+    }
     *fail_flag = 0;
     fence_mbar_init();
     fence_proxy_async();
@@ -299,7 +316,8 @@ grouped_gemm_pair_kernel(const __grid_constant__ PairMaps maps, const GemmArgs p
       prefetch_tmap(&maps.sfa);
       prefetch_tmap(&maps.sfb);
     }
-    if (EPI != MPM_EPI_DSWIGLU) prefetch_tmap(&maps.out);
+    prefetch_tmap(&maps.out);
+    if (EPI == MPM_EPI_DSWIGLU) prefetch_tmap(&maps.aux);
   }
   if (warp == 1) {
     tmem_alloc_pair(sTmem, TMEM_COLS);
@@ -525,6 +543,9 @@ grouped_gemm_pair_kernel(const __grid_constant__ PairMaps maps, const GemmArgs p
     const uint32_t acce_leader0 = map_to_rank(bar_acc + 8, 0);
     const uint32_t acce_leader1 = NACC > 1 ? map_to_rank(bar_acc + 16 + 8, 0) : acce_leader0;
     const bool leader_thread = (threadIdx.x == EPI_WARP0 * 32);
+    // SwiGLU backward: staging loads not yet waited for, and the phase parity
+    // each one completes
+    uint32_t c_pending = 0, c_parity = 0;
     uint32_t j = 0;
     SegCursor cur;
     for (long long t = cid; t < n_tasks; t += ncl) {
@@ -551,17 +572,21 @@ grouped_gemm_pair_kernel(const __grid_constant__ PairMaps maps, const GemmArgs p
             p.row_prob)
           prob_r = p.row_prob[grow];
       }
-      // SwiGLU backward: the first 32 columns of this row's gate and up values
-      // (C) are requested before the accumulator wait as well
-      uint4 cgw[4], cuw[4];
-      if (EPI == MPM_EPI_DSWIGLU && row_ok) {
-        const __nv_bfloat16* cg0 = static_cast<const __nv_bfloat16*>(p.aux) + grow * p.ld_aux +
-                                   k.n0 + half * 128;
+      // SwiGLU backward: the tile's first two 64-column chunks of C (gate
+      // and up boxes of this CTA's 128 rows) are requested before the
+      // accumulator wait, into the two staging buffers
+      if (EPI == MPM_EPI_DSWIGLU && leader_thread) {
+        bulk_wait_group_read0();                 // the previous tile's dH stores have read them
 #pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
-          cgw[q4] = *reinterpret_cast<const uint4*>(cg0 + q4 * 8);
-          cuw[q4] = *reinterpret_cast<const uint4*>(cg0 + p.N + q4 * 8);
+        for (int b = 0; b < 2; ++b) {
+          const uint32_t buf = sOut + b * STAGE_OUT_BYTES;
+          mbar_arrive_expect_tx(bar_c + 8 * b, STAGE_OUT_BYTES);
+          tma_load_2d(buf, &maps.aux, (int)k.n0 + b * OUT_BOX_COLS, (int)orow, bar_c + 8 * b);
+          tma_load_2d(buf + OUT_BOX_BYTES, &maps.aux, (int)(p.N + k.n0) + b * OUT_BOX_COLS,
+                      (int)orow, bar_c + 8 * b);
         }
+        c_pending = 3u;
+        c_parity = 0u;                          // first load of each buffer in the tile
       }
       const uint32_t ab = NACC > 1 ? (j & 1u) : 0u, use = NACC > 1 ? (j >> 1) : j;
       const bool w_ok = mbar_wait_cluster(bar_acc + 16 * ab, use & 1u, p.status);
@@ -735,34 +760,40 @@ grouped_gemm_pair_kernel(const __grid_constant__ PairMaps maps, const GemmArgs p
           }
         }
       } else {   // MPM_EPI_DSWIGLU
+        // dD = acc * alpha (fp32, not rounded); with (g, u) from C:
+        //   dH[:, j] = dD p u silu'(g),  dH[:, N + j] = dD p silu(g)   (bf16)
+        // The tile goes through in four 64-column chunks.  Chunk cq's gate and
+        // up columns of C arrive by TMA in staging buffer cq % 2 (two 16 KB
+        // boxes, 128-byte swizzle); each thread takes 32 columns of its row
+        // (this warp's half of the chunk), reads dD for them from TMEM,
+        // overwrites the C values in place with dg / du, and the two boxes
+        // go out to dH by TMA stores; the buffer is then refilled with chunk
+        // cq + 2.  The accumulator is handed back once the last chunk's
+        // columns are in registers.
         const float prob = prob_r;
-        const long long Nh = p.N;
-        const __nv_bfloat16* cg = static_cast<const __nv_bfloat16*>(p.aux) + grow * p.ld_aux;
-        const __nv_bfloat16* cu = cg + Nh;
-        __nv_bfloat16* og = static_cast<__nv_bfloat16*>(p.out) + grow * p.ldo;
-        __nv_bfloat16* ou = og + Nh;
-#pragma unroll
-        for (int cc = 0; cc < 4; ++cc) {
-          const int c = half * 4 + cc;
-          tmem_ld_32x32b_x32(trow + c * 32, v);
-          // next chunk of C in flight while this one is computed
-          uint4 ngw[4], nuw[4];
-          if (row_ok && cc < 3) {
-#pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) {
-              ngw[q4] = *reinterpret_cast<const uint4*>(cg + k.n0 + (c + 1) * 32 + q4 * 8);
-              nuw[q4] = *reinterpret_cast<const uint4*>(cu + k.n0 + (c + 1) * 32 + q4 * 8);
-            }
-          }
+#pragma unroll 1
+        for (int cq = 0; cq < 4; ++cq) {
+          tmem_ld_32x32b_x32(trow + cq * 64 + half * 32, v);
           tmem_ld_wait();
-          if (row_ok) {
-          const long long col = k.n0 + c * 32;
+          if (cq == 3) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(acce_leader);   // this warp's share is read
+          }
+          const int b = cq & 1;
+          const uint32_t buf = sOut + b * STAGE_OUT_BYTES;
+          const bool c_ok = mbar_wait(bar_c + 8 * b, (uint32_t)(cq >> 1) & 1u, p.status);
+          if (leader_thread && c_ok) c_pending &= ~(1u << b);
+          if (!c_ok) *fail_flag = 1;
+          const uint32_t rg = buf + r * 128, ru = rg + OUT_BOX_BYTES;
 #pragma unroll
-          for (int jj = 0; jj < 32; jj += 8) {
-            const uint4 gw = cgw[jj / 8];
-            const uint4 uw = cuw[jj / 8];
-            const uint32_t ga[4] = {gw.x, gw.y, gw.z, gw.w};
-            const uint32_t ua[4] = {uw.x, uw.y, uw.z, uw.w};
+          for (int c16 = 0; c16 < 4; ++c16) {
+            const uint32_t off = (uint32_t)(((half * 4 + c16) ^ (r & 7)) << 4);
+            uint32_t ga[4], ua[4];
+            asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                         : "=r"(ga[0]), "=r"(ga[1]), "=r"(ga[2]), "=r"(ga[3]) : "r"(rg + off));
+            asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                         : "=r"(ua[0]), "=r"(ua[1]), "=r"(ua[2]), "=r"(ua[3]) : "r"(ru + off));
             uint32_t og4[4], ou4[4];
 #pragma unroll
             for (int qq = 0; qq < 4; ++qq) {
@@ -771,25 +802,42 @@ grouped_gemm_pair_kernel(const __grid_constant__ PairMaps maps, const GemmArgs p
               for (int h = 0; h < 2; ++h) {
                 const float g = h ? bf16hi(ga[qq]) : bf16lo(ga[qq]);
                 const float uu = h ? bf16hi(ua[qq]) : bf16lo(ua[qq]);
-                const float dd = __fmul_rn(__uint_as_float(v[jj + 2 * qq + h]), alpha);
+                const float dd = __fmul_rn(__uint_as_float(v[c16 * 8 + 2 * qq + h]), alpha);
                 swiglu_bwd(g, uu, dd, prob, dg2[h], du2[h]);
               }
               og4[qq] = pack_bf16(dg2[0], dg2[1]);
               ou4[qq] = pack_bf16(du2[0], du2[1]);
             }
-            *reinterpret_cast<uint4*>(og + col + jj) = make_uint4(og4[0], og4[1], og4[2], og4[3]);
-            *reinterpret_cast<uint4*>(ou + col + jj) = make_uint4(ou4[0], ou4[1], ou4[2], ou4[3]);
+            st_shared_v4(rg + off, og4[0], og4[1], og4[2], og4[3]);
+            st_shared_v4(ru + off, ou4[0], ou4[1], ou4[2], ou4[3]);
           }
-          }
-          if (cc < 3) {
-#pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) { cgw[q4] = ngw[q4]; cuw[q4] = nuw[q4]; }
+          fence_proxy_async();
+          named_sync(2, EPI_THREADS);
+          if (*fail_flag) break;
+          if (leader_thread) {
+            tma_store_2d(&maps.out, (int)k.n0 + cq * OUT_BOX_COLS, (int)orow, buf);
+            tma_store_2d(&maps.out, (int)(p.N + k.n0) + cq * OUT_BOX_COLS, (int)orow,
+                         buf + OUT_BOX_BYTES);
+            bulk_commit_group();
+            if (cq + 2 < 4) {
+              bulk_wait_group_read0();             // the stores have read the buffer
+              mbar_arrive_expect_tx(bar_c + 8 * b, STAGE_OUT_BYTES);
+              tma_load_2d(buf, &maps.aux, (int)k.n0 + (cq + 2) * OUT_BOX_COLS, (int)orow,
+                          bar_c + 8 * b);
+              tma_load_2d(buf + OUT_BOX_BYTES, &maps.aux,
+                          (int)(p.N + k.n0) + (cq + 2) * OUT_BOX_COLS, (int)orow, bar_c + 8 * b);
+              c_pending |= 1u << b;
+              c_parity |= 1u << b;          // the buffer's second load of the tile
+            }
           }
         }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive_cluster(acce_leader);   // this warp's share is read
+        if (*fail_flag) break;
       }
+    }
+    // a failed wait left staging loads in flight: let them land before exit
+    if (EPI == MPM_EPI_DSWIGLU && leader_thread) {
+      for (int b = 0; b < 2; ++b)
+        if (c_pending & (1u << b)) mbar_wait(bar_c + 8 * b, (c_parity >> b) & 1u, p.status);
     }
   }
   if (threadIdx.x == EPI_WARP0 * 32) bulk_wait_group0();    // output stores complete
@@ -810,7 +858,7 @@ grouped_gemm_pair_kernel(const __grid_constant__ PairMaps maps, const GemmArgs p
 template <int KIND, int EPI, int MAJ = 0>
 static cudaError_t launch_pair_one(const pairk::PairMaps& maps, const GemmArgs& a, int n_tiles,
                                    long long n_tasks, cudaStream_t s) {
-  constexpr int smem = pairk::smem_bytes<KIND>();
+  constexpr int smem = pairk::smem_bytes<KIND, EPI>();
   static_assert(smem <= 227 * 1024, "dynamic shared memory above the per-CTA limit");
   auto kern = pairk::grouped_gemm_pair_kernel<KIND, EPI, MAJ>;
   static int max_clusters[64] = {0};
@@ -885,14 +933,15 @@ static cudaError_t pair_dispatch_bf16_mn(int maj, int epi, const pairk::PairMaps
 cudaError_t launch_grouped_gemm_pair(int kind, int epi, int maj, const CUtensorMap& ta,
                                      const CUtensorMap& tb, const CUtensorMap& tsfa,
                                      const CUtensorMap& tsfb, const CUtensorMap& tout,
-                                     const GemmArgs& a, int n_tiles, long long n_tasks,
-                                     cudaStream_t s) {
+                                     const CUtensorMap& taux, const GemmArgs& a, int n_tiles,
+                                     long long n_tasks, cudaStream_t s) {
   pairk::PairMaps maps;
   maps.a = ta;
   maps.b = tb;
   maps.sfa = tsfa;
   maps.sfb = tsfb;
   maps.out = tout;
+  maps.aux = taux;
   if (kind == MPM_KIND_NVFP4) return pair_dispatch<MPM_KIND_NVFP4>(epi, maps, a, n_tiles, n_tasks, s);
   if (kind == MPM_KIND_BF16) {
     if (maj != 0) return pair_dispatch_bf16_mn(maj, epi, maps, a, n_tiles, n_tasks, s);

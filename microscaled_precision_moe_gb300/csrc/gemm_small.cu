@@ -350,6 +350,204 @@ grouped_gemm_small_kernel(const __grid_constant__ SmallMaps maps, const GemmArgs
 
 }  // namespace smallk
 
+// ---------------------------------------------------------------- split K
+// One dense group of at most 128 rows (no segment offsets): the
+// single-expert case.  The kernel above gives it only N / 128 CTAs, each
+// running the whole K chain.  Here a cluster of ks CTAs shares one tile of
+// 128 weight rows: CTA c accumulates k-blocks [c nkb / ks, (c + 1) nkb / ks)
+// in its own TMEM and parks the fp32 partial [128 rows x 128 features] in
+// its shared memory; after a cluster barrier CTA c sums rows
+// [c 128 / ks, (c + 1) 128 / ks) over the ks partials in CTA order 0 .. ks-1
+// (reading its peers' shared memory), applies alpha and writes the output.
+// The order is fixed, so the result is deterministic; it rounds in another
+// order than the unsplit accumulation (both fp32, within the GEMM
+// tolerance).
+namespace splitk {
+using namespace smallk;
+
+constexpr int KS_MAX = 8;              // portable cluster size
+constexpr int S = 4;                   // ring stages
+constexpr uint32_t TMEM_COLS = 256;    // accumulator 128 + scale slots 4 x 32
+
+template <int KIND>
+constexpr int stage_bytes() { return 2 * TILE + 2 * KCfg<KIND>::kAtoms * 512; }
+constexpr int PART_BYTES = BR * BW * 4;        // fp32 [128 rows][128 features]
+template <int KIND>
+constexpr int ring_bytes() {
+  return S * stage_bytes<KIND>() > PART_BYTES ? S * stage_bytes<KIND>() : PART_BYTES;
+}
+template <int KIND>
+constexpr int smem_bytes() { return 1024 + ring_bytes<KIND>() + (2 * S + 2) * 8 + 16; }
+
+template <int KIND, int EPI>
+__global__ void __launch_bounds__(NTHREADS, 1)
+gemm_splitk_kernel(const __grid_constant__ SmallMaps maps, const GemmArgs p, const int ks) {
+  using KC = KCfg<KIND>;
+  constexpr int STB = stage_bytes<KIND>();
+  constexpr int SFC = 2 * 4 * KC::kAtoms;        // TMEM scale columns per stage (weights, rows)
+  extern __shared__ uint8_t smem_raw[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* gbase = smem_raw + (base - raw);
+  const uint32_t sRing = base;                   // the ring; after the MMAs the partial
+  const uint32_t sBar = base + ring_bytes<KIND>();
+  const uint32_t bar_full = sBar, bar_empty = sBar + 8 * S, bar_acc = sBar + 16 * S;
+  const uint32_t sTmem = bar_acc + 16;
+  volatile uint32_t* tmem_holder = reinterpret_cast<volatile uint32_t*>(gbase + (sTmem - base));
+  const int c = (int)cluster_ctarank();          // this CTA's part of K
+  const int wt = (int)(blockIdx.x / ks);         // weight tile
+  const int nkb = (int)(p.K / KC::kElemsPerKB);
+  const int kb0 = c * nkb / ks, kb1 = (c + 1) * nkb / ks;
+  const long long wrow0 = (long long)wt * BW;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(bar_full + 8 * s, 1);
+      mbar_init(bar_empty + 8 * s, 1);
+    }
+    mbar_init(bar_acc, 1);
+    fence_mbar_init();
+    fence_proxy_async();
+    prefetch_tmap(&maps.a);
+    prefetch_tmap(&maps.b);
+  }
+  if (warp == 1) {
+    tmem_alloc(sTmem, TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+  bool ok = true;
+
+  if (warp == 0 && lane == 0) {
+    // ======================================================== TMA producer
+    for (int kb = kb0, it = 0; kb < kb1; ++kb, ++it) {
+      const int s = it % S;
+      if (!mbar_wait(bar_empty + 8 * s, ((it / S) & 1u) ^ 1u, p.status)) break;
+      const uint32_t st = sRing + s * STB;
+      mbar_arrive_expect_tx(bar_full + 8 * s, STB);
+      const long long ke = (long long)kb * KC::kElemsPerKB;
+      const int xb = (int)(KIND == MPM_KIND_NVFP4 ? ke / 2 : ke);
+      tma_load_2d(st, &maps.b, xb, (int)wrow0, bar_full + 8 * s);
+      tma_load_2d(st + TILE, &maps.a, xb, 0, bar_full + 8 * s);
+      const long long atom = (KIND == MPM_KIND_NVFP4) ? ke / 64 : ke / 128;
+      const uint32_t sf0 = st + 2 * TILE;
+      bulk_load(sf0, p.sfb + ((wrow0 >> 7) * (p.sfb_cols_pad >> 2) + atom) * 512,
+                KC::kAtoms * 512, bar_full + 8 * s);
+      bulk_load(sf0 + KC::kAtoms * 512, p.sfa + atom * 512, KC::kAtoms * 512, bar_full + 8 * s);
+    }
+  } else if (warp == 1 && lane == 0) {
+    // ======================================================== scale copies + MMA issue
+    const uint32_t idesc_base = idesc_block_scaled(KC::kFmt, BR, KC::kUe8m0, 0, 128);
+    for (int kb = kb0, it = 0; kb < kb1; ++kb, ++it) {
+      const int s = it % S;
+      if (!mbar_wait(bar_full + 8 * s, (it / S) & 1u, p.status)) { ok = false; break; }
+      tc_fence_after();
+      const uint32_t st = sRing + s * STB;
+      const uint32_t sf0 = st + 2 * TILE;
+      const uint32_t sfcol = tmem + BR + s * SFC;
+#pragma unroll
+      for (int w = 0; w < 2; ++w)
+#pragma unroll
+        for (int a = 0; a < KC::kAtoms; ++a)
+          tc_cp_32x128b_x4(sfcol + (w * KC::kAtoms + a) * 4, sdesc_sf(sf0 + (w * KC::kAtoms + a) * 512));
+      const uint32_t sfrow = sfcol + KC::kAtoms * 4;
+#pragma unroll
+      for (int k4 = 0; k4 < 4; ++k4) {
+        const uint64_t adesc = sdesc_sw128(st + k4 * 32);
+        const uint64_t bdesc = sdesc_sw128(st + TILE + k4 * 32);
+        const uint32_t acc = (it > 0 || k4 > 0) ? 1u : 0u;
+        if (KIND == MPM_KIND_NVFP4) {
+          mma_nvf4(tmem, adesc, bdesc, idesc_base, sfcol + k4 * 4, sfrow + k4 * 4, acc);
+        } else {
+          const uint32_t idesc = idesc_block_scaled(KC::kFmt, BR, KC::kUe8m0, (uint32_t)k4, 128);
+          mma_mxf8(tmem, adesc, bdesc, idesc, sfcol, sfrow, acc);
+        }
+      }
+      tc_commit(bar_empty + 8 * s);
+    }
+    if (ok && kb1 > kb0) tc_commit(bar_acc);
+  } else if (warp >= 2) {
+    // ======================================================== partial -> shared memory
+    const int q = warp & 3;                      // TMEM lane quarter = 32 weight rows
+    const int f = q * 32 + lane;                 // this thread's feature within the tile
+    float* part = reinterpret_cast<float*>(gbase + (sRing - base));
+    bool w_ok = true;
+    if (kb1 > kb0) w_ok = mbar_wait(bar_acc, 0u, p.status);
+    if (kb1 > kb0 && w_ok) {
+      tc_fence_after();
+      const uint32_t tacc = tmem + ((uint32_t)(q * 32) << 16);
+#pragma unroll 1
+      for (int cb = 0; cb < 4; ++cb) {
+        uint32_t v[32];
+        tmem_ld_32x32b_x32(tacc + cb * 32, v);
+        tmem_ld_wait();
+#pragma unroll
+        for (int r = 0; r < 32; ++r) part[(cb * 32 + r) * BW + f] = __uint_as_float(v[r]);
+      }
+    } else {
+      // no k-blocks for this CTA, or a failed wait: a zero partial
+      for (int r = 0; r < BR; ++r) part[r * BW + f] = 0.0f;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();                                // every partial is in place
+  if (warp >= 2) {
+    // ======================================================== fixed-order reduction
+    // a warp takes one row's 128 features (512 contiguous bytes) per step
+    const int t = threadIdx.x - 64;              // 0 .. 127
+    const int rows_per = BR / ks;                // ks divides 128
+    for (int i = 0; i < rows_per / 4; ++i) {
+      const int idx = (i * 128 + t) * 4;         // within this CTA's row slice
+      const int row = c * rows_per + idx / BW;
+      const int feat = idx % BW;
+      const uint32_t off = (uint32_t)((row * BW + feat) * 4);
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int j = 0; j < ks; ++j) {
+        const uint32_t src = map_to_rank(sRing + off, (uint32_t)j);
+        float4 v;
+        asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+                     : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(src));
+        if (j == 0) {
+          acc = v;
+        } else {
+          acc.x = __fadd_rn(acc.x, v.x);
+          acc.y = __fadd_rn(acc.y, v.y);
+          acc.z = __fadd_rn(acc.z, v.z);
+          acc.w = __fadd_rn(acc.w, v.w);
+        }
+      }
+      if (row < p.a_rows) {
+        const float ab = p.alpha_b ? p.alpha_b[0] : 1.0f;
+        const float alpha = p.alpha_a ? __fmul_rn(p.alpha_a[row], ab) : ab;
+        const long long o = (long long)row * p.ldo + wrow0 + feat;
+        const float4 y = make_float4(__fmul_rn(acc.x, alpha), __fmul_rn(acc.y, alpha),
+                                     __fmul_rn(acc.z, alpha), __fmul_rn(acc.w, alpha));
+        if (EPI == MPM_EPI_F32) {
+          *reinterpret_cast<float4*>(static_cast<float*>(p.out) + o) = y;
+        } else {
+          __nv_bfloat162 lo = __floats2bfloat162_rn(y.x, y.y), hi = __floats2bfloat162_rn(y.z, y.w);
+          uint2 w;
+          w.x = *reinterpret_cast<uint32_t*>(&lo);
+          w.y = *reinterpret_cast<uint32_t*>(&hi);
+          *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(p.out) + o) = w;
+        }
+      }
+    }
+  }
+  cluster_sync();                                // the peers are done reading this partial
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, TMEM_COLS);
+  }
+}
+
+}  // namespace splitk
+
 template <int KIND, int EPI>
 static cudaError_t launch_small_one(const smallk::SmallMaps& maps, const GemmArgs& a, int n_wt,
                                     long long n_tasks, cudaStream_t s) {
@@ -373,6 +571,55 @@ static cudaError_t launch_small_one(const smallk::SmallMaps& maps, const GemmArg
   if (grid < 1) grid = 1;
   kern<<<(unsigned)grid, smallk::NTHREADS, smem, s>>>(maps, a, n_wt, n_tasks);
   return cudaGetLastError();
+}
+
+template <int KIND, int EPI>
+static cudaError_t launch_splitk_one(const smallk::SmallMaps& maps, const GemmArgs& a, int n_wt,
+                                     int ks, cudaStream_t s) {
+  constexpr int smem = splitk::smem_bytes<KIND>();
+  static_assert(smem <= 227 * 1024, "dynamic shared memory above the per-CTA limit");
+  static_assert(smem > 114 * 1024, "one CTA per SM (TMEM allocation never waits)");
+  auto kern = splitk::gemm_splitk_kernel<KIND, EPI>;
+  static bool attr_set[64] = {false};
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  if (dev < 64 && !attr_set[dev]) {
+    err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (err != cudaSuccess) return err;
+    attr_set[dev] = true;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)ks;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.gridDim = dim3((unsigned)(n_wt * ks), 1, 1);
+  cfg.blockDim = dim3(smallk::NTHREADS, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  err = cudaLaunchKernelEx(&cfg, kern, maps, a, ks);
+  if (err != cudaSuccess) return err;
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gemm_splitk(int kind, int epi, const CUtensorMap& ta, const CUtensorMap& tb,
+                               const GemmArgs& a, int n_wt, int ks, cudaStream_t s) {
+  smallk::SmallMaps maps;
+  maps.a = ta;
+  maps.b = tb;
+  if (ks < 1 || ks > splitk::KS_MAX || (smallk::BR % ks) != 0) return cudaErrorInvalidValue;
+  if (kind == MPM_KIND_NVFP4) {
+    if (epi == MPM_EPI_F32) return launch_splitk_one<MPM_KIND_NVFP4, MPM_EPI_F32>(maps, a, n_wt, ks, s);
+    if (epi == MPM_EPI_BF16) return launch_splitk_one<MPM_KIND_NVFP4, MPM_EPI_BF16>(maps, a, n_wt, ks, s);
+  } else if (kind == MPM_KIND_MXFP8) {
+    if (epi == MPM_EPI_F32) return launch_splitk_one<MPM_KIND_MXFP8, MPM_EPI_F32>(maps, a, n_wt, ks, s);
+    if (epi == MPM_EPI_BF16) return launch_splitk_one<MPM_KIND_MXFP8, MPM_EPI_BF16>(maps, a, n_wt, ks, s);
+  }
+  return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_grouped_gemm_small(int kind, int epi, const CUtensorMap& ta,

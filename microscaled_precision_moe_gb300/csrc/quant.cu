@@ -185,6 +185,104 @@ __global__ void __launch_bounds__(128) nvfp4_quant_rows_kernel(const Nvfp4Rows p
   }
 }
 
+// ---------------------------------------------------------------- NVFP4, running amax
+// The quantisation of the single-pass FC2 ("miniTE technical report",
+// section 5.6): a row of D is consumed in tiles of 256 columns, in order;
+// tile t is encoded against gs_t = outer(max |x| over tiles 0 .. t), the
+// running row amax, so a tile never waits for the rest of its row.  Same
+// canonical fp32 sequence as the per-token quantiser, with gs_t in place of
+// s_g.  One warp per row: lane l holds blocks i*32 + l (16 elements each),
+// so tile t = 2i + (l >= 16) is the 16 lanes of one half-warp at index i.
+template <int NB>
+__global__ void __launch_bounds__(128) nvfp4_quant_online_kernel(const Nvfp4Rows p, float* gs_out,
+                                                                 int n_tiles) {
+  const int lane = threadIdx.x & 31;
+  const long long row = (long long)blockIdx.x * 4 + (threadIdx.x >> 5);
+  long long rows_eff = p.rows;
+  if (p.m_valid) {
+    long long mv = *p.m_valid;
+    rows_eff = mv < rows_eff ? mv : rows_eff;
+    if (row >= rows_eff) return;
+  }
+  const int nblk = p.K >> 4;
+  const long long cols_pad = nblk;
+  if (row >= rows_eff) {
+    if (row < p.rows_pad) {
+      for (int b = lane; b < nblk; b += 32) p.s[sf_offset(row, b, cols_pad)] = 0;
+    }
+    return;
+  }
+  const __nv_bfloat16* xr = p.part[0] + row * p.ldx;
+  uint4 v[NB][2];
+#pragma unroll
+  for (int i = 0; i < NB; ++i) {
+    const int b = i * 32 + lane;
+    if (b < nblk) {
+      const uint4* src = reinterpret_cast<const uint4*>(xr + (long long)b * 16);
+      v[i][0] = __ldcs(src);
+      v[i][1] = __ldcs(src + 1);
+    } else {
+      v[i][0] = make_uint4(0, 0, 0, 0);
+      v[i][1] = make_uint4(0, 0, 0, 0);
+    }
+  }
+  uint32_t bmax16[NB];
+#pragma unroll
+  for (int i = 0; i < NB; ++i) {
+    uint32_t m = 0;
+    m = absmax_bf16x2(m, v[i][0].x); m = absmax_bf16x2(m, v[i][0].y);
+    m = absmax_bf16x2(m, v[i][0].z); m = absmax_bf16x2(m, v[i][0].w);
+    m = absmax_bf16x2(m, v[i][1].x); m = absmax_bf16x2(m, v[i][1].y);
+    m = absmax_bf16x2(m, v[i][1].z); m = absmax_bf16x2(m, v[i][1].w);
+    bmax16[i] = max(m & 0xFFFFu, m >> 16);
+  }
+  // tile maxima (bf16 patterns of |x| order like unsigned integers), then
+  // the running maximum in tile order: tile 2i, then 2i + 1, then 2i + 2 ...
+  const bool upper = lane >= 16;
+  uint32_t run = 0;
+  float gs_mine[NB];
+#pragma unroll
+  for (int i = 0; i < NB; ++i) {
+    uint32_t t = bmax16[i];
+#pragma unroll
+    for (int o = 8; o > 0; o >>= 1) t = max(t, __shfl_xor_sync(0xFFFFFFFFu, t, o));
+    const uint32_t other = __shfl_xor_sync(0xFFFFFFFFu, t, 16);
+    const uint32_t t_lo = upper ? other : t, t_hi = upper ? t : other;
+    const uint32_t run_lo = max(run, t_lo);
+    run = max(run_lo, t_hi);
+    gs_mine[i] = nvfp4_outer(__uint_as_float((upper ? run : run_lo) << 16));
+    const int tile = 2 * i + (upper ? 1 : 0);
+    if ((lane & 15) == 0 && tile < n_tiles) gs_out[row * n_tiles + tile] = gs_mine[i];
+  }
+  uint8_t* qr = p.q + row * (long long)(p.K >> 1);
+#pragma unroll
+  for (int i = 0; i < NB; ++i) {
+    const int b = i * 32 + lane;
+    if (b >= nblk) continue;
+    const float sg = gs_mine[i];
+    uint32_t sb = 0;
+    if (sg > 0.0f) {
+      const float sbf = __fdiv_rn(__uint_as_float(bmax16[i] << 16), __fmul_rn(6.0f, sg));
+      sb = cvt_e4m3x2(sbf, 0.0f) & 0xFFu;
+    }
+    const float sbv = e4m3_to_f32(sb);
+    uint2 out = make_uint2(0, 0);
+    if (sbv > 0.0f) {
+      const float r = __frcp_rn(__fmul_rn(sbv, sg));
+      const uint32_t w[8] = {v[i][0].x, v[i][0].y, v[i][0].z, v[i][0].w,
+                             v[i][1].x, v[i][1].y, v[i][1].z, v[i][1].w};
+      const uint64_t r2 = f32x2_splat(r);
+      uint32_t bytes[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) bytes[j] = e2m1x2_scaled(w[j], r2);
+      out.x = bytes[0] | (bytes[1] << 8) | (bytes[2] << 16) | (bytes[3] << 24);
+      out.y = bytes[4] | (bytes[5] << 8) | (bytes[6] << 16) | (bytes[7] << 24);
+    }
+    *reinterpret_cast<uint2*>(qr + (long long)b * 8) = out;
+    p.s[sf_offset(row, b, cols_pad)] = (uint8_t)sb;
+  }
+}
+
 // Per-group amax for the joint weight scale: |x| max over a group's rows of
 // all parts, as fp32 bits, reduced with an integer atomicMax (order-free).
 struct GroupAmax {
@@ -530,6 +628,33 @@ cudaError_t launch_nvfp4_weight(const void* const* parts, const long long* part_
   p.q = q; p.s = s; p.ts = ts;
   p.m_valid = nullptr;
   return launch_nvfp4_rows(p, st);
+}
+
+cudaError_t launch_nvfp4_online(const void* x, long long M, int K, long long ldx, uint8_t* q,
+                                uint8_t* s, float* gs, const int* m_valid, cudaStream_t st) {
+  Nvfp4Rows p{};
+  p.part[0] = static_cast<const __nv_bfloat16*>(x);
+  p.part_rows[0] = M;
+  p.nparts = 1;
+  p.R = M;
+  p.ldx = ldx;
+  p.rows = M;
+  p.rows_pad = m_valid ? M : (M + 127) / 128 * 128;
+  p.K = K;
+  p.q = q; p.s = s;
+  p.m_valid = m_valid;
+  const int n_tiles = K / 256;
+  const dim3 grid((unsigned)((p.rows_pad + 3) / 4)), block(128);
+  switch (nb_for(K >> 4)) {
+    case 1: nvfp4_quant_online_kernel<1><<<grid, block, 0, st>>>(p, gs, n_tiles); break;
+    case 2: nvfp4_quant_online_kernel<2><<<grid, block, 0, st>>>(p, gs, n_tiles); break;
+    case 4: nvfp4_quant_online_kernel<4><<<grid, block, 0, st>>>(p, gs, n_tiles); break;
+    case 8: nvfp4_quant_online_kernel<8><<<grid, block, 0, st>>>(p, gs, n_tiles); break;
+    case 14: nvfp4_quant_online_kernel<14><<<grid, block, 0, st>>>(p, gs, n_tiles); break;
+    case 16: nvfp4_quant_online_kernel<16><<<grid, block, 0, st>>>(p, gs, n_tiles); break;
+    default: return cudaErrorInvalidValue;
+  }
+  return cudaGetLastError();
 }
 
 cudaError_t launch_mxfp8_tma(const CUtensorMap& tx, long long M, long long K, long long ldx,

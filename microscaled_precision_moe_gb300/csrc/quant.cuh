@@ -10,6 +10,10 @@ cudaError_t launch_nvfp4_per_token(const void* x, long long M, int K, long long 
 cudaError_t launch_nvfp4_weight(const void* const* parts, const long long* part_rows, int nparts,
                                 int K, long long E, uint8_t* q, uint8_t* s, float* ts,
                                 unsigned* ws, cudaStream_t st);
+// tile-by-tile NVFP4 with the running row amax (256-column tiles; K % 256
+// == 0): codes, tiled block scales and one outer scale per (row, tile)
+cudaError_t launch_nvfp4_online(const void* x, long long M, int K, long long ldx, uint8_t* q,
+                                uint8_t* s, float* gs, const int* m_valid, cudaStream_t st);
 // x is read through a 2-D bf16 tensor map (box 64 columns x 128 rows)
 cudaError_t launch_mxfp8_tma(const CUtensorMap& tx, long long M, long long K, long long ldx,
                              unsigned flags, uint8_t* row_q, uint8_t* row_s, uint8_t* col_q,

@@ -107,10 +107,23 @@ class NVFP4MoE:
     CTA pairs and pads expert segments to 256 rows; 128 uses one CTA per
     128-row tile and 128-row segments; L.TILE_SMALL_M (1) runs the small-M
     kernel (weights on the MMA's M side) for decode / rollout batches where
-    each expert receives few rows, with 128-row segments."""
+    each expert receives few rows, with 128-row segments.
 
-    def __init__(self, T, H, I, E, k, device="cuda", tile_m=256):
+    fc2 = "online" (CTA pairs only) runs FC2 as in the single-pass FFN of the
+    miniTE report, section 5.6: D is quantised tile by tile (256 columns)
+    against a running row amax, and FC2 weighs each tile's product by that
+    tile's outer scale; fc2 = "two_pass" (default) re-quantises whole rows of
+    D against their full amax."""
+
+    FC2_MODES = ("two_pass", "online")
+
+    def __init__(self, T, H, I, E, k, device="cuda", tile_m=256, fc2="two_pass"):
         self.T, self.H, self.I, self.E, self.k = T, H, I, E, k
+        if fc2 not in self.FC2_MODES:
+            raise ValueError(f"fc2 must be one of {self.FC2_MODES}")
+        if fc2 == "online" and (tile_m != 256 or I % 256 != 0):
+            raise ValueError("the online FC2 needs tile_m = 256 and I % 256 == 0")
+        self.fc2 = fc2
         self.tile_m = tile_m
         self.pad = 128 if tile_m == L.TILE_SMALL_M else tile_m
         dev = torch.device(device)
@@ -125,7 +138,9 @@ class NVFP4MoE:
         self.aq = (e(cap, H // 2, dtype=u8), e(_sb(cap, H // 16), dtype=u8), e(cap, dtype=f32))
         self.d = e(cap, I, dtype=bf)
         self.amax = e(cap, dtype=f32)
-        self.dq = (e(cap, I // 2, dtype=u8), e(_sb(cap, I // 16), dtype=u8), e(cap, dtype=f32))
+        # two-pass: one outer scale per row; online: one per (row, 256-column tile)
+        self.dq = (e(cap, I // 2, dtype=u8), e(_sb(cap, I // 16), dtype=u8),
+                   e(cap, dtype=f32) if fc2 == "two_pass" else e(cap, I // 256, dtype=f32))
         self.y = e(cap, H, dtype=bf)
         self.out = e(T, H, dtype=bf)
 
@@ -159,13 +174,22 @@ class NVFP4MoE:
                              c_out, b_rows_per_expert=2 * I, alpha_a=ats, alpha_b=w.w1_ts,
                              row_prob=rp, out2=self.d, amax=self.amax, tile_m=self.tile_m)
         mark(4)
-        ops.nvfp4_quantize_per_token(self.d, amax_in=self.amax, m_valid=seg[E:], out=self.dq)
+        if self.fc2 == "online":
+            ops.nvfp4_quantize_online(self.d, m_valid=seg[E:], out=self.dq)
+        else:
+            ops.nvfp4_quantize_per_token(self.d, amax_in=self.amax, m_valid=seg[E:], out=self.dq)
         dq, ds, dts = self.dq
         mark(5)
-        ops.moe_grouped_gemm(L.KIND_NVFP4, L.GROUP_M, L.EPI_BF16, E, cap, H, I, seg,
-                             dq, w.w2_q.view(E * H, I // 2), ds, I // 16, w.w2_s, I // 16,
-                             self.y, b_rows_per_expert=H, alpha_a=dts, alpha_b=w.w2_ts,
-                             tile_m=self.tile_m)
+        if self.fc2 == "online":
+            ops.moe_grouped_gemm(L.KIND_NVFP4, L.GROUP_M, L.EPI_BF16_ONLINE, E, cap, H, I, seg,
+                                 dq, w.w2_q.view(E * H, I // 2), ds, I // 16, w.w2_s, I // 16,
+                                 self.y, b_rows_per_expert=H, alpha_b=w.w2_ts, aux=dts,
+                                 tile_m=256)
+        else:
+            ops.moe_grouped_gemm(L.KIND_NVFP4, L.GROUP_M, L.EPI_BF16, E, cap, H, I, seg,
+                                 dq, w.w2_q.view(E * H, I // 2), ds, I // 16, w.w2_s, I // 16,
+                                 self.y, b_rows_per_expert=H, alpha_a=dts, alpha_b=w.w2_ts,
+                                 tile_m=self.tile_m)
         mark(6)
         dst = self.out if out is None else out
         ops.moe_combine(self.y, inv, T, k, out=dst)
@@ -237,6 +261,9 @@ class NVFP4MoE:
             raise RuntimeError(f"prepare_backward_weights({mode!r}) first")
         if self.tile_m != 256:
             raise ValueError("the BF16 backward runs its GEMMs on CTA pairs: tile_m=256")
+        if mode == "dequantized" and self.fc2 != "two_pass":
+            raise ValueError("the dequantized backward reads the whole-row re-quantised D: "
+                             "fc2='two_pass'")
         T, H, I, E, k, cap = self.T, self.H, self.I, self.E, self.k, self.cap
         seg, perm, inv, rp = self.seg
         mark = mark or (lambda i: None)

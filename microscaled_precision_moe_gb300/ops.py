@@ -115,6 +115,32 @@ def nvfp4_quantize_per_token(x, amax_in=None, m_valid=None, out=None):
     return q, s, ts
 
 
+def nvfp4_quantize_online(x, m_valid=None, out=None):
+    """Tile-by-tile NVFP4 of bf16 x [M, K] with the running row amax (tiles
+    of 256 columns): (q [M, K/2] u8, s tiled [M, K/16] u8, tile_scale
+    [M, K/256] fp32)."""
+    lib = L.load()
+    _check_rows(x, "x")
+    _check_m_valid(m_valid)
+    _need_cuda(x, m_valid)
+    M, K = x.shape
+    if K % 256 != 0:
+        raise ValueError(f"x: K = {K} is not a multiple of the 256-column tile")
+    dev = x.device
+    if out is None:
+        out = (torch.empty(M, K // 2, dtype=torch.uint8, device=dev),
+               torch.empty(scale_bytes(M, K // 16), dtype=torch.uint8, device=dev),
+               torch.empty(M, K // 256, dtype=torch.float32, device=dev))
+    q, s, gs = out
+    _check(q, "q", torch.uint8, min_numel=M * (K // 2))
+    _check(s, "s", torch.uint8, min_numel=scale_bytes(M, K // 16))
+    _check(gs, "tile_scale", torch.float32, min_numel=M * (K // 256))
+    st = lib.mpm_nvfp4_quantize_online(_ptr(x), M, K, x.stride(0), _ptr(q), _ptr(s), _ptr(gs),
+                                       _ptr(m_valid), _stream(dev))
+    L.check(st, "mpm_nvfp4_quantize_online")
+    return q, s, gs
+
+
 def nvfp4_quantize_weight(parts, out=None, ws=None):
     """Joint NVFP4 quantisation of per-expert parts [E, rows_p, K] (bf16) with
     one FP32 outer scale per expert: (q [E, R, K/2], s [E * tiled(R, K/16)],
@@ -282,9 +308,17 @@ def moe_grouped_gemm(kind, group, epilogue, E, a_rows, N, K, seg, a, b, sfa, sfa
         _check(sfa, "sfa", torch.uint8)
         _check(sfb, "sfb", torch.uint8)
     _check(out, "out", torch.float32 if epilogue == L.EPI_F32 else torch.bfloat16)
-    for t, name in ((out2, "out2"), (aux, "aux")):
-        if t is not None:
-            _check(t, name, torch.bfloat16)
+    if out2 is not None:
+        _check(out2, "out2", torch.bfloat16)
+    if aux is not None:
+        if epilogue == L.EPI_BF16_ONLINE:
+            # the per-(row, 256-column tile) outer scales of the online quantiser
+            _check(aux, "aux (tile scales)", torch.float32, dim=2)
+            if aux.shape[0] < a_rows or aux.shape[1] < K // 256:
+                raise ValueError(f"aux: shape {tuple(aux.shape)}, the call needs "
+                                 f"[{a_rows}, {K // 256}]")
+        else:
+            _check(aux, "aux", torch.bfloat16)
     for t, name in ((alpha_a, "alpha_a"), (alpha_b, "alpha_b"), (row_prob, "row_prob"),
                     (amax, "amax")):
         if t is not None:

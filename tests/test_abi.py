@@ -98,6 +98,35 @@ def _gemm_desc(kind, group, epi, N, K, tile_m):
     return d
 
 
+def test_online_quantiser_and_fc2_validation(lib):
+    """The running-amax quantiser and the online FC2 epilogue reject bad
+    arguments on the host (CPU only)."""
+    from microscaled_precision_moe_gb300 import _lib as L
+    fake = C.c_void_p(0x10000)
+    odd = C.c_void_p(0x10008)
+    assert lib.mpm_nvfp4_quantize_online(None, 4, 256, 256, fake, fake, fake, None, None) == 1
+    assert lib.mpm_nvfp4_quantize_online(fake, 4, 320, 320, fake, fake, fake, None, None) == 2
+    assert lib.mpm_nvfp4_quantize_online(fake, 0, 256, 256, fake, fake, fake, None, None) == 2
+    assert lib.mpm_nvfp4_quantize_online(fake, 4, 256, 128, fake, fake, fake, None, None) == 2
+    assert lib.mpm_nvfp4_quantize_online(odd, 4, 256, 256, fake, fake, fake, None, None) == 3
+    d = _gemm_desc(L.KIND_NVFP4, L.GROUP_M, L.EPI_BF16_ONLINE, 256, 512, 256)
+    d.sfa_dev = d.sfb_dev = 0x10000
+    d.sfa_cols = d.sfb_cols = 32
+    d.seg_dev = 0x10000
+    assert lib.mpm_moe_grouped_gemm(C.byref(d), None) == 1          # no tile scales (aux)
+    d.aux_dev, d.ld_aux = 0x10000, 2
+    d.alpha_a_dev = 0x10000
+    assert lib.mpm_moe_grouped_gemm(C.byref(d), None) == 4          # per-row scale given
+    d.alpha_a_dev = None
+    d.ld_aux = 1
+    assert lib.mpm_moe_grouped_gemm(C.byref(d), None) == 2          # ld_aux < K / 256
+    d.ld_aux = 2
+    d.kind = L.KIND_MXFP8
+    assert lib.mpm_moe_grouped_gemm(C.byref(d), None) == 4          # NVFP4 only
+    d.kind, d.tile_m = L.KIND_NVFP4, 128
+    assert lib.mpm_moe_grouped_gemm(C.byref(d), None) == 4          # CTA pairs only
+
+
 def test_bf16_mn_major_and_small_m_validation(lib):
     """The BF16 kind, its MN-major operands and the small-M tile mode are
     checked on the host (CPU only)."""

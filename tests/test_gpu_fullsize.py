@@ -30,10 +30,13 @@ from tests.gpu_util import need_gpu, np_bf16, u8, assert_bytes_equal, oracle_com
 pytestmark = pytest.mark.gpu
 
 REL, ELEM = 1e-3, 1e-2
-# chained NVFP4 bounds (see tests/test_gpu_gemm.py): fraction of D rows that
-# differ from the oracle's, relative error of Y on those rows
-D_ROW_DIFF = 0.1
-REQUANT_REL = 0.1
+# chained NVFP4 bounds (see tests/test_gpu_gemm.py), per checked expert:
+# fraction of D rows that differ from the oracle's and relative error of Y on
+# those rows.  Measured on GB300 at these sizes: at most 3.8 % of the rows of
+# the heaviest or middle expert differ (7.7 %, 4 of 52 rows, on the smallest
+# decode batch) and their Y is within 1.4e-2.
+D_ROW_DIFF = 0.15
+REQUANT_REL = 0.05
 
 
 @pytest.fixture(scope="module", autouse=True)

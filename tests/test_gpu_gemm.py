@@ -19,11 +19,14 @@ REL, ELEM = 1e-3, 1e-2
 # Bounds of the chained NVFP4 comparison (FC1 -> re-quantise -> FC2 ->
 # combine); the re-quantisation is discontinuous, so rows of D that the fp32
 # tensor-core accumulation rounds to a neighbouring bf16 value get other FP4
-# operands than the oracle's.
-D_ELEM_DIFF = 1e-3       # fraction of D elements that differ (each by one bf16 step at most)
-D_ROW_DIFF = 0.1         # fraction of D rows with any differing element
-REQUANT_REL = 0.1        # relative error of Y on those rows (NVFP4 re-quantisation noise)
-LAYER_REL = 1e-2         # relative Frobenius error of the layer output
+# operands than the oracle's.  Measured on GB300 over the reduced layers of
+# this file (the values each test prints): at most 3.8e-5 of D elements and
+# 0.4 % of D rows differ, those rows' Y is within 2.0e-2 of the oracle's and
+# the layer output within 1.5e-3.  The bounds keep a margin of about 2.5-5x.
+D_ELEM_DIFF = 2e-4       # fraction of D elements that differ (each by one bf16 step at most)
+D_ROW_DIFF = 0.02        # fraction of D rows with any differing element
+REQUANT_REL = 0.05       # relative error of Y on those rows (NVFP4 re-quantisation noise)
+LAYER_REL = 5e-3         # relative Frobenius error of the layer output
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -67,6 +70,52 @@ def test_nvfp4_single_expert_gate_up(tile_m):
     assert ops.get_device_status() == 0
     ref = MO.nvfp4_gemm_single(np_bf16(x), np_bf16(wg), np_bf16(wu))["c"]
     _assert_close(out.cpu().numpy(), ref.astype(np.float32), "single-expert NVFP4")
+
+
+@pytest.mark.parametrize("kind,epi,M,N,K", [
+    ("nvfp4", "bf16", 128, 1536, 2048),     # the single-expert shape, bf16 out
+    ("nvfp4", "f32", 40, 256, 768),         # 3 k-blocks over a 2-CTA cluster (uneven split)
+    ("nvfp4", "f32", 1, 512, 4096),         # one row, 16 k-blocks over 8 CTAs
+    ("mxfp8", "f32", 100, 512, 1024),       # 8 k-blocks of 128
+    ("mxfp8", "bf16", 128, 256, 256),       # 2 k-blocks
+])
+def test_single_group_split_k(kind, epi, M, N, K):
+    """One dense group of at most 128 rows on the small-M path runs split K
+    (a cluster of CTAs per 128 weight rows, fixed-order reduction of their
+    fp32 partials): against the oracle's fp64 GEMM on the dequantised codes,
+    and deterministic from call to call."""
+    ops, L = _ops(), _L()
+    x = synth.normal_bf16(5, 1, (M, K), "cuda", outlier_p=1e-3, outlier_mul=50.0)
+    w = synth.normal_bf16(5, 2, (N, K), "cuda", std=0.02)
+    dt = torch.float32 if epi == "f32" else torch.bfloat16
+    e = L.EPI_F32 if epi == "f32" else L.EPI_BF16
+    out = torch.empty(M, N, dtype=dt, device="cuda")
+    xn, wn = np_bf16(x), np_bf16(w)
+    if kind == "nvfp4":
+        qx, sx, tsx = ops.nvfp4_quantize_per_token(x)
+        qw, sw, tsw = ops.nvfp4_quantize_weight([w[None].contiguous()])
+        run = lambda o: ops.moe_grouped_gemm(L.KIND_NVFP4, L.GROUP_M, e, 1, M, N, K, None, qx, qw[0],
+                                             sx, K // 16, sw, K // 16, o, alpha_a=tsx, alpha_b=tsw,
+                                             tile_m=L.TILE_SMALL_M)
+        rq, rs, rts = Q.nvfp4_quantize_per_token(xn)
+        wp, ws, wg = Q.nvfp4_quantize_joint([wn[None]], 1)
+        ref = Q.nvfp4_dequantize(rq, rs, rts) @ Q.nvfp4_dequantize(wp[0], ws[0], wg[0]).T
+    else:
+        mx = ops.mxfp8_quantize(x, colwise=False)
+        wq = ops.mxfp8_quantize(w, colwise=False)
+        run = lambda o: ops.moe_grouped_gemm(L.KIND_MXFP8, L.GROUP_M, e, 1, M, N, K, None,
+                                             mx["row_q"], wq["row_q"], mx["row_s"], K // 32,
+                                             wq["row_s"], K // 32, o, tile_m=L.TILE_SMALL_M)
+        ref = MO.mx_rows(xn) @ MO.mx_rows(wn).T
+    run(out)
+    out2 = torch.empty_like(out)
+    run(out2)
+    torch.cuda.synchronize()
+    assert ops.get_device_status() == 0
+    assert torch.equal(out, out2), "split-K reduction is deterministic"
+    got = out.cpu().float().numpy()
+    _assert_close(got, ref.astype(np.float32) if epi == "f32" else F.bf16_round(ref),
+                  f"split-K {kind} {M}x{N}x{K}")
 
 
 def _grouped_nvfp4_setup(shape, seed=0, pad=128):
