@@ -456,6 +456,47 @@ def _nvfp4_30b_line(peak_fp4, steps=10):
     return r
 
 
+def _nvfp4_online_line(peak_fp4, steps=10):
+    """The headline layer with the single-pass FC2 of the miniTE report,
+    section 5.6 (D quantised tile by tile against the running row amax, FC2
+    weighing each tile by its outer scale), beside the two-pass layer the
+    headline times; stage times from CUDA events."""
+    from microscaled_precision_moe_gb300 import synth
+    from microscaled_precision_moe_gb300.moe import NVFP4MoE, NVFP4Weights
+    s = synth.MOE_671B
+    ids, prob = synth.routing(s)
+    x = synth.moe_activations(s, device="cuda")
+    w1, w2 = synth.moe_weights(s, device="cuda")
+    W = NVFP4Weights.quantize(w1, w2)
+    del w1, w2
+    torch.cuda.empty_cache()
+    L = NVFP4MoE(s.T, s.H, s.I, s.E, s.k, fc2="online")
+    idc, prc = ids.cuda(), prob.cuda()
+    for _ in range(3):
+        L.forward(x, idc, prc, W)
+    nst = len(NVFP4MoE.STAGES) + 1
+    ev = [_events(nst) for _ in range(steps)]
+    torch.cuda.synchronize()
+    for i in range(steps):
+        evi = ev[i]
+        L.forward(x, idc, prc, W, mark=lambda j, evi=evi: evi[j].record())
+    torch.cuda.synchronize()
+    tot = float(np.mean([ev[i][0].elapsed_time(ev[i][nst - 1]) for i in range(steps)]))
+    st = {n: round(float(np.mean([ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(steps)])), 4)
+          for j, n in enumerate(NVFP4MoE.STAGES)}
+    fl1, fl2 = L.gemm_flops()
+    r = {"workload": s.name + "_fc2_online", "ms_per_step": round(tot, 4),
+         "TFLOP/s": round((fl1 + fl2) / (tot * 1e-3) / 1e12, 1),
+         "fc2_TFLOP/s": round(fl2 / (st["fc2"] * 1e-3) / 1e12, 1),
+         "fc2_frac_fp4": round(fl2 / (st["fc2"] * 1e-3) / 1e12 / peak_fp4, 3),
+         "stage_ms": st,
+         "note": "quant_d = the running-amax tile quantiser; fc2 = CTA pairs on 256 x 128 "
+                 "tiles, each 256-column reduction tile weighed by its own outer scale"}
+    del L, W, x
+    torch.cuda.empty_cache()
+    return r
+
+
 def _nvfp4_bf16_bwd_line(peak_bf16, steps=10):
     """BF16 backward of the NVFP4 layer (30B-shaped, 8192 tokens), both
     operand modes: the backward alone is timed (the forward that saves
@@ -582,6 +623,8 @@ def _summary(line, peaks):
           "mxfp8_gemm_frac_fp8_burst": None,
           "nvfp4_30b_ms": g(a, "nvfp4_layer_fwd_30b", "ms_per_step"),
           "nvfp4_30b_frac_fp4_burst": None,
+          "fc2_online_ms": g(a, "nvfp4_layer_fwd_fc2_online", "stage_ms", "fc2"),
+          "layer_fc2_online_ms": g(a, "nvfp4_layer_fwd_fc2_online", "ms_per_step"),
           "bf16_bwd_ms": {m: g(a, "nvfp4_layer_bf16_bwd", m, "ms_per_step")
                           for m in ("high_precision", "dequantized")},
           "decode_ms": {k: v.get("ms") for k, v in a.get("nvfp4_layer_decode", {}).items()
@@ -619,7 +662,7 @@ def main():
     ap.add_argument("--no-also", action="store_true", help="skip the secondary lines")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle sample")
     ap.add_argument("--case", choices=["headline", "slice", "mxfp8", "bf16bwd", "decode",
-                                       "decode_slice", "quant", "single"],
+                                       "decode_slice", "quant", "single", "online"],
                     default="headline",
                     help="slice: 4096 tokens over 64 experts of the 671B shape (profiling); "
                          "mxfp8: the MXFP8 30B-shaped forward+backward step alone (profiling); "
@@ -628,7 +671,8 @@ def main():
                          "decode_slice: 64 tokens over 32 experts of that shape (profiling); "
                          "quant: the quantiser lines alone; "
                          "single: the single-expert 128 x 1536 x 2048 NVFP4 GEMM and its "
-                         "activation quantisation")
+                         "activation quantisation; "
+                         "online: the headline layer with the single-pass (online amax) FC2")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -695,6 +739,15 @@ def main():
                               "unit": "GB/s", "n_gpus": world, "higher_is_better": True,
                               "dtype": "mxfp8", "config": {"workload": "mxfp8_quantize_8288x2048_rowcol"},
                               "quantizers": r}), flush=True)
+        return 0
+    if args.case == "online":
+        r = _nvfp4_online_line(peaks["bf16"] * NOMINAL_FP4_OVER_BF16, steps=args.steps)
+        if rank == 0:
+            print(json.dumps({"metric": METRIC, "value": r["TFLOP/s"], "unit": "TFLOP/s",
+                              "n_gpus": world, "steps": args.steps, "warmup": 3,
+                              "ms_per_step": r["ms_per_step"], "higher_is_better": True,
+                              "dtype": "nvfp4", "config": {"workload": r["workload"]},
+                              "online": r}), flush=True)
         return 0
     if args.case == "single":
         r = _single_expert_line(peak_fp4_sus, peaks["hbm"])
@@ -876,6 +929,7 @@ def main():
         also = {"quantizers": _quantizer_lines(peaks["hbm"])}
         also["mxfp8_layer_fwd_bwd"] = _mxfp8_layer_line(peak_fp8_sus)
         also["nvfp4_layer_fwd_30b"] = _nvfp4_30b_line(peak_fp4_sus)
+        also["nvfp4_layer_fwd_fc2_online"] = _nvfp4_online_line(peak_fp4)
         also["nvfp4_layer_bf16_bwd"] = _nvfp4_bf16_bwd_line(peaks["bf16_sus"])
         also["nvfp4_layer_decode"] = _nvfp4_decode_line(peaks["hbm"])
         try:

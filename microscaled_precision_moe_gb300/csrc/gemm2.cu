@@ -106,17 +106,25 @@ constexpr int STAGE_OUT_BYTES = 2 * OUT_BOX_BYTES;      // 32 KB
 // The SwiGLU-backward epilogue streams C in and dH out through two staging
 // buffers of 32 KB (one 64-column chunk of gate and of up each), so its ring
 // has one stage less than the kind's default (the bf16 kind: two less).
+// (Staging a whole 128 x 256 bf16 output tile the same way, to store it in
+// one round instead of two, was measured slower for FC2: the ring stage it
+// costs outweighs the second round, 1.86 against 1.70 ms.)
+template <int KIND, int EPI>
+constexpr bool staging64() {
+  return EPI == MPM_EPI_DSWIGLU;
+}
 template <int KIND, int EPI>
 constexpr int stages() {
-  return EPI == MPM_EPI_DSWIGLU ? (KIND == MPM_KIND_BF16 ? 5 : 4) : Cfg<KIND>::kStages;
+  return EPI == MPM_EPI_DSWIGLU ? (KIND == MPM_KIND_BF16 ? 5 : 4)
+                                : (staging64<KIND, EPI>() ? 4 : Cfg<KIND>::kStages);
 }
-template <int EPI>
+template <int KIND, int EPI>
 constexpr int out_staging_bytes() {
-  return EPI == MPM_EPI_DSWIGLU ? 2 * STAGE_OUT_BYTES : STAGE_OUT_BYTES;
+  return staging64<KIND, EPI>() ? 2 * STAGE_OUT_BYTES : STAGE_OUT_BYTES;
 }
 template <int KIND, int EPI>
 constexpr int smem_bytes() {
-  return 2048 + stages<KIND, EPI>() * stage_bytes<KIND>() + out_staging_bytes<EPI>() +
+  return 2048 + stages<KIND, EPI>() * stage_bytes<KIND>() + out_staging_bytes<KIND, EPI>() +
          (4 * stages<KIND, EPI>() + 4) * 8 + 32 + 16;
 }
 
@@ -273,7 +281,7 @@ grouped_gemm_pair_kernel(const __grid_constant__ PairMaps maps, const GemmArgs p
   const uint32_t sSFB = sSFA + S * C::kSfaBytes;
   // the 128-byte-swizzled staging boxes need a 1024-byte-aligned base
   const uint32_t sOut = (sSFB + S * C::kSfbBytes + 1023u) & ~1023u;
-  const uint32_t sBar = sOut + out_staging_bytes<EPI>();
+  const uint32_t sBar = sOut + out_staging_bytes<KIND, EPI>();
   const uint32_t bar_full = sBar, bar_empty = sBar + 8 * S;
   // accumulator buffer b: full barrier at bar_acc + 16 b, empty at + 8.  The
   // bf16 kind keeps two accumulators in TMEM (columns 0-255 and 256-511, no

@@ -94,24 +94,14 @@ MPM_DEV uint32_t e2m1x2_scaled(uint32_t w, uint64_t r2) {
   return out;
 }
 
+// One row of the NVFP4 quantisers, by one warp: the row is read once into
+// registers (NB x 32 lanes x 16 elements), then encoded.  amax_mode 0 takes
+// the row's own max, 1 amax_in[row], 2 the group amax `group_bits` (fp32
+// bits); `evict_first` marks the row's last read.
 template <int NB>
-__global__ void __launch_bounds__(128) nvfp4_quant_rows_kernel(const Nvfp4Rows p) {
-  const int lane = threadIdx.x & 31;
-  const long long row = (long long)blockIdx.x * 4 + (threadIdx.x >> 5);
-  long long rows_eff = p.rows;
-  if (p.m_valid) {
-    long long mv = *p.m_valid;
-    rows_eff = mv < rows_eff ? mv : rows_eff;
-    if (row >= rows_eff) return;
-  }
+MPM_DEV void nvfp4_quant_row(const Nvfp4Rows& p, long long row, int lane, uint32_t group_bits) {
   const int nblk = p.K >> 4;
   const long long cols_pad = nblk;          // K % 64 == 0 -> nblk % 4 == 0
-  if (row >= rows_eff) {
-    if (row < p.rows_pad) {                 // padding rows of the last tile
-      for (int b = lane; b < nblk; b += 32) p.s[sf_offset(row, b, cols_pad)] = 0;
-    }
-    return;
-  }
   const __nv_bfloat16* xr = nvfp4_row_ptr(p, row);
 
   uint4 v[NB][2];
@@ -149,7 +139,7 @@ __global__ void __launch_bounds__(128) nvfp4_quant_rows_kernel(const Nvfp4Rows p
   } else if (p.amax_mode == 1) {
     a = p.amax_in[row];
   } else {
-    a = __uint_as_float(p.group_amax[row / p.R]);
+    a = __uint_as_float(group_bits);
   }
   const float sg = nvfp4_outer(a);
   if (lane == 0) {
@@ -183,6 +173,26 @@ __global__ void __launch_bounds__(128) nvfp4_quant_rows_kernel(const Nvfp4Rows p
     *reinterpret_cast<uint2*>(qr + (long long)b * 8) = out;
     p.s[sf_offset(row, b, cols_pad)] = (uint8_t)sb;
   }
+}
+
+template <int NB>
+__global__ void __launch_bounds__(128) nvfp4_quant_rows_kernel(const Nvfp4Rows p) {
+  const int lane = threadIdx.x & 31;
+  const long long row = (long long)blockIdx.x * 4 + (threadIdx.x >> 5);
+  long long rows_eff = p.rows;
+  if (p.m_valid) {
+    long long mv = *p.m_valid;
+    rows_eff = mv < rows_eff ? mv : rows_eff;
+    if (row >= rows_eff) return;
+  }
+  const int nblk = p.K >> 4;
+  if (row >= rows_eff) {
+    if (row < p.rows_pad) {                 // padding rows of the last tile
+      for (int b = lane; b < nblk; b += 32) p.s[sf_offset(row, b, nblk)] = 0;
+    }
+    return;
+  }
+  nvfp4_quant_row<NB>(p, row, lane, p.amax_mode == 2 ? p.group_amax[row / p.R] : 0u);
 }
 
 // ---------------------------------------------------------------- NVFP4, running amax

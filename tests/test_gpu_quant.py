@@ -128,6 +128,33 @@ def test_nvfp4_weight_experts_with_outliers():
     assert_bytes_equal(ts2.cpu().numpy().view(np.uint32), rts2.view(np.uint32), "W2 s_g")
 
 
+@pytest.mark.parametrize("E,R,K,parts", [
+    (2, 4096, 7168, 1),     # two 671B-shaped W1 experts, the widest rows
+    (40, 128, 64, 2),       # many small experts, the narrowest rows
+    (9, 384, 2048, 3),      # three parts of 128 rows sharing one scale
+])
+def test_nvfp4_weight_shapes(E, R, K, parts):
+    """The joint weight quantiser (per-expert amax pass, then the encode):
+    every code, scale byte and outer scale against the oracle's joint
+    quantisation, from the widest to the narrowest rows and with up to
+    three parts per expert."""
+    ops = _ops()
+    w = synth.normal_bf16(3, 40 + E, (E, R, K), "cuda", std=0.01, outlier_p=1e-4,
+                          outlier_mul=100.0)
+    w[E // 2] *= 1e-3                                  # one expert on another scale
+    rp = R // parts
+    pieces = [w[:, i * rp:(i + 1) * rp].contiguous() for i in range(parts)]
+    q, sc, ts = ops.nvfp4_quantize_weight(pieces)
+    torch.cuda.synchronize()
+    assert ops.get_device_status() == 0
+    rq, rs, rts = Q.nvfp4_quantize_joint([np_bf16(p) for p in pieces], E)
+    assert_bytes_equal(u8(q), rq, "codes")
+    per = Q.scale_bytes(R, K // 16)
+    for e in range(E):
+        assert_bytes_equal(u8(sc)[e * per:(e + 1) * per], Q.swizzle_scales(rs[e]), f"scales e{e}")
+    assert_bytes_equal(ts.cpu().numpy().view(np.uint32), rts.view(np.uint32), "s_g")
+
+
 def _check_mxfp8(x_dev, ldc=None):
     ops = _ops()
     o = ops.mxfp8_quantize(x_dev, ldc=ldc)
