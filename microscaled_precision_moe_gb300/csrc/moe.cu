@@ -124,6 +124,187 @@ __global__ void __launch_bounds__(32) seg_scatter_kernel(const int* ids, const f
   }
 }
 
+// ---------------------------------------------------------------- one cooperative kernel
+// The same four steps (histogram, per-expert column scan, padded offsets,
+// stable scatter) in one persistent launch whose CTAs meet at two grid
+// barriers: at these sizes the separate launches cost more than their work
+// (about 46 us for any T).  The kernel is launched cooperatively, so every
+// CTA is resident; a barrier wait is bounded and, past the limit, records
+// MPM_ERR_DEVICE_TIMEOUT and leaves the kernel.  The results are those of the
+// four kernels above, bit for bit: the same chunks, the same scans, the same
+// per-chunk stable scatter.
+struct SegFused {
+  const int* ids; const float* prob;
+  long long n; int E; int pad; int nchunks;
+  int* hist; int* base; int* totals;
+  int* seg_offsets; int* perm; int* inv_perm; float* row_prob; long long cap;
+  unsigned* bar;            // [2]: arrival count, generation (zeroed by the launcher)
+  int* st;
+};
+
+// grid-wide barrier: the last CTA to arrive resets the count and bumps the
+// generation; the others wait for the generation to move (bounded)
+MPM_DEV bool seg_grid_sync(unsigned* bar, int* st) {
+  __syncthreads();
+  __shared__ int ok;
+  if (threadIdx.x == 0) {
+    ok = 1;
+    volatile unsigned* gen = bar + 1;
+    const unsigned g0 = *gen;
+    __threadfence();
+    if (atomicAdd(bar, 1u) == gridDim.x - 1) {
+      atomicExch(bar, 0u);
+      __threadfence();
+      atomicAdd(bar + 1, 1u);
+    } else {
+      long long n = 0;
+      while (*gen == g0) {
+        if (++n > (1ll << 26)) { set_status(st, MPM_ERR_DEVICE_TIMEOUT); ok = 0; break; }
+        __nanosleep(32);
+      }
+    }
+    __threadfence();
+  }
+  __syncthreads();
+  return ok != 0;
+}
+
+__global__ void __launch_bounds__(256) seg_fused_kernel(const SegFused a) {
+  extern __shared__ int sh[];                  // max(E, 8 E) ints
+  const int E = a.E;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // phase 0: clear the permuted buffers, per-chunk histograms
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < a.cap;
+       i += (long long)gridDim.x * blockDim.x) {
+    a.perm[i] = -1;
+    a.row_prob[i] = 0.0f;
+  }
+  for (int c = blockIdx.x; c < a.nchunks; c += gridDim.x) {
+    for (int e = threadIdx.x; e < E; e += blockDim.x) sh[e] = 0;
+    __syncthreads();
+    const long long base = (long long)c * kSegChunk;
+    for (int i = threadIdx.x; i < kSegChunk; i += blockDim.x) {
+      const long long f = base + i;
+      if (f >= a.n) break;
+      const int e = a.ids[f];
+      if (e >= 0 && e < E) atomicAdd(&sh[e], 1);
+      else set_status(a.st, MPM_ERR_DEVICE_BOUNDS);
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += blockDim.x) a.hist[(long long)c * E + e] = sh[e];
+    __syncthreads();
+  }
+  if (!seg_grid_sync(a.bar, a.st)) return;
+  // phase 1: per-expert exclusive scan over the chunks (as seg_colscan_kernel);
+  // data other CTAs wrote before a barrier is read from L2 (__ldcg)
+  for (int e = blockIdx.x; e < E; e += gridDim.x) {
+    const int per = (a.nchunks + 255) / 256;
+    const int c0 = threadIdx.x * per;
+    const int c1 = min(c0 + per, a.nchunks);
+    int local = 0;
+    for (int c = c0; c < c1; ++c) local += __ldcg(a.hist + (long long)c * E + e);
+    int incl = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    if (lane == 31) sh[warp] = incl;
+    __syncthreads();
+    int woff = 0;
+    for (int i = 0; i < warp; ++i) woff += sh[i];
+    int run = woff + incl - local;
+    for (int c = c0; c < c1; ++c) {
+      const int v = __ldcg(a.hist + (long long)c * E + e);
+      a.base[(long long)c * E + e] = run;
+      run += v;
+    }
+    if (threadIdx.x == 255) a.totals[e] = woff + incl;
+    __syncthreads();
+  }
+  if (!seg_grid_sync(a.bar, a.st)) return;
+  // phase 2: padded offsets, computed by every CTA from the totals (block
+  // scan over E <= 1024 values: 4 per thread), written by CTA 0
+  {
+    int v[4], sum = 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int e = threadIdx.x * 4 + i;
+      v[i] = e < E ? (__ldcg(a.totals + e) + a.pad - 1) / a.pad * a.pad : 0;
+      sum += v[i];
+    }
+    int incl = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int x = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += x;
+    }
+    __syncthreads();
+    if (lane == 31) sh[warp] = incl;
+    __syncthreads();
+    int woff = 0;
+    for (int i = 0; i < warp; ++i) woff += sh[i];
+    int run = woff + incl - sum;
+    __syncthreads();
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int e = threadIdx.x * 4 + i;
+      if (e < E) {
+        sh[e] = run;                             // this CTA's copy of seg_offsets[e]
+        if (blockIdx.x == 0) a.seg_offsets[e] = run;
+      }
+      run += v[i];
+    }
+    if (blockIdx.x == 0 && threadIdx.x == 255) a.seg_offsets[E] = run;
+    __syncthreads();
+  }
+  // phase 3: stable scatter, one warp per chunk (as seg_scatter_kernel), the
+  // warp's counters after the offsets in shared memory
+  int* cnt = sh + E + warp * E;
+  constexpr int kSteps = kSegChunk / 32;
+  for (int c = blockIdx.x * 8 + warp; c < a.nchunks; c += gridDim.x * 8) {
+    const long long c0 = (long long)c * kSegChunk;
+    // the chunk's expert ids and router weights are loaded up front (all
+    // in flight at once), so the ordered walk below waits on no load
+    int ids_r[kSteps];
+    float prob_r[kSteps];
+#pragma unroll
+    for (int s = 0; s < kSteps; ++s) {
+      const long long f = c0 + s * 32 + lane;
+      ids_r[s] = f < a.n ? a.ids[f] : -1;
+      prob_r[s] = f < a.n ? a.prob[f] : 0.0f;
+    }
+    for (int e = lane; e < E; e += 32) cnt[e] = __ldcg(a.base + (long long)c * E + e) + sh[e];
+    __syncwarp();
+#pragma unroll
+    for (int si = 0; si < kSteps; ++si) {
+      const int s = si * 32;
+      const long long f = c0 + s + lane;
+      int e = -1;
+      if (f < a.n) {
+        e = ids_r[si];
+        if (e < 0 || e >= E) e = -1;
+      }
+      const unsigned grp = __match_any_sync(0xFFFFFFFFu, e);
+      const unsigned lt = (1u << lane) - 1u;
+      const int rank = __popc(grp & lt);
+      int row = -1;
+      if (e >= 0) row = cnt[e] + rank;
+      __syncwarp();
+      if (e >= 0 && (grp >> lane) == 1u) cnt[e] += __popc(grp);
+      __syncwarp();
+      if (f < a.n) {
+        a.inv_perm[f] = row;
+        if (row >= 0) {
+          a.perm[row] = (int)f;
+          a.row_prob[row] = prob_r[si];
+        }
+      }
+    }
+    __syncwarp();
+  }
+}
+
 // ---------------------------------------------------------------- gather
 // dst[row] = src[perm[row] / k] (bf16 rows), zeros for padding rows
 __global__ void __launch_bounds__(256) gather_bf16_kernel(const uint4* src, long long K8,
@@ -242,7 +423,38 @@ __global__ void __launch_bounds__(128) combine_kernel(const uint4* y, const int*
 size_t segments_ws_bytes(long long T, int k, long long E) {
   const long long n = T * k;
   const long long nchunks = (n + kSegChunk - 1) / kSegChunk;
-  return (size_t)(2 * nchunks * E + E) * sizeof(int);
+  // histograms, chunk bases, expert totals, the fused kernel's barrier words
+  return (size_t)(2 * nchunks * E + E + 2) * sizeof(int);
+}
+
+// the cooperative form; cudaErrorNotSupported when the device cannot run it
+static cudaError_t launch_segments_fused(const SegFused& a, cudaStream_t s) {
+  static int ctas[64] = {0};
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  if (dev < 0 || dev >= 64) return cudaErrorNotSupported;
+  const size_t smem = (size_t)9 * 1024 * sizeof(int);     // offsets + 8 warps' counters, E <= 1024
+  if (ctas[dev] == 0) {
+    int sms = 0, per = 0, coop = 0;
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev);
+    err = cudaFuncSetAttribute(seg_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)smem);
+    if (err != cudaSuccess) return err;
+    err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, seg_fused_kernel, 256, smem);
+    if (err != cudaSuccess) return err;
+    ctas[dev] = (coop && sms > 0 && per > 0) ? sms * (per < 2 ? per : 2) : -1;
+  }
+  if (ctas[dev] < 0) return cudaErrorNotSupported;
+  // enough CTAs for the widest phase, no more than can be resident
+  long long want = a.nchunks > a.E ? a.nchunks : a.E;
+  if (want < 1) want = 1;
+  const unsigned grid = (unsigned)(want < ctas[dev] ? want : ctas[dev]);
+  SegFused arg = a;
+  void* args[] = {&arg};
+  return cudaLaunchCooperativeKernel((const void*)seg_fused_kernel, dim3(grid), dim3(256), args,
+                                     smem, s);
 }
 
 cudaError_t launch_build_segments(const int* ids, const float* prob, long long T, int k,
@@ -254,6 +466,18 @@ cudaError_t launch_build_segments(const int* ids, const float* prob, long long T
   int* hist = static_cast<int*>(ws);
   int* base = hist + (long long)nchunks * E;
   cudaError_t err;
+  if (E <= 1024) {
+    SegFused a{};
+    a.ids = ids; a.prob = prob; a.n = n; a.E = (int)E; a.pad = pad; a.nchunks = nchunks;
+    a.hist = hist; a.base = base; a.totals = base + (long long)nchunks * E;
+    a.seg_offsets = seg_offsets; a.perm = perm; a.inv_perm = inv_perm; a.row_prob = row_prob;
+    a.cap = cap;
+    a.bar = reinterpret_cast<unsigned*>(a.totals + E);
+    a.st = st;
+    if ((err = cudaMemsetAsync(a.bar, 0, 2 * sizeof(unsigned), s)) != cudaSuccess) return err;
+    err = launch_segments_fused(a, s);
+    if (err != cudaErrorNotSupported) return err;
+  }
   if ((err = cudaMemsetAsync(perm, 0xFF, (size_t)cap * sizeof(int), s)) != cudaSuccess) return err;
   if ((err = cudaMemsetAsync(row_prob, 0, (size_t)cap * sizeof(float), s)) != cudaSuccess) return err;
   seg_hist_kernel<<<nchunks, 128, (size_t)E * sizeof(int), s>>>(ids, n, (int)E, hist, st);
