@@ -196,10 +196,10 @@ class NVFP4MoE:
         mark(7)
         return dst
 
-    # kernels launched by one forward: quantiser, 4 segment kernels
-    # (histogram, per-expert column scan, offsets, scatter), gather, FC1,
-    # quantiser, FC2, combine
-    LAUNCHES_PER_FORWARD = 10
+    # kernels launched by one forward: quantiser, the segment build (one
+    # cooperative kernel, after an 8-byte memset of its barrier words),
+    # gather, FC1, quantiser, FC2, combine
+    LAUNCHES_PER_FORWARD = 7
 
     # ------------------------------------------------------------ BF16 backward
     BACKWARD_MODES = ("high_precision", "dequantized")
