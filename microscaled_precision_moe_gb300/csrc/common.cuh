@@ -83,6 +83,31 @@ MPM_DEV float swiglu_silu(float g) { return __fdividef(g, __fadd_rn(1.0f, __expf
 MPM_DEV float swiglu_fwd(float g, float u, float prob) {
   return __fmul_rn(__fmul_rn(swiglu_silu(g), u), prob);
 }
+// Two elements of D at once: the same operations as swiglu_fwd on each
+// lane, with the multiplications done as packed f32x2 IEEE products (per
+// lane bit-identical to the scalar products): (acc_g, acc_u) pairs scaled by
+// alpha, then silu(g) * u * p.
+MPM_DEV uint64_t f32x2(float lo, float hi) {
+  uint64_t v;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(v) : "f"(lo), "f"(hi));
+  return v;
+}
+MPM_DEV void f32x2_split(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+MPM_DEV uint64_t mul_f32x2(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+MPM_DEV void swiglu_fwd2(uint32_t acc_g0, uint32_t acc_g1, uint32_t acc_u0, uint32_t acc_u1,
+                         uint64_t alpha2, uint64_t prob2, float& d0, float& d1) {
+  float g0, g1;
+  f32x2_split(mul_f32x2(f32x2(__uint_as_float(acc_g0), __uint_as_float(acc_g1)), alpha2), g0, g1);
+  const uint64_t u = mul_f32x2(f32x2(__uint_as_float(acc_u0), __uint_as_float(acc_u1)), alpha2);
+  const uint64_t su = mul_f32x2(f32x2(swiglu_silu(g0), swiglu_silu(g1)), u);
+  f32x2_split(mul_f32x2(su, prob2), d0, d1);
+}
 // dD -> (dg, du) for D = silu(g) * u * p with p constant:
 //   dg = (dD p) u s (1 + g (1 - s)),  du = (dD p) g s,  s = 1 / (1 + e^-g)
 MPM_DEV void swiglu_bwd(float g, float u, float dd, float prob, float& dg, float& du) {

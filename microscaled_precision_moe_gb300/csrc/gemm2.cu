@@ -609,9 +609,9 @@ grouped_gemm_pair_kernel(const __grid_constant__ PairMaps maps, const GemmArgs p
       uint32_t v[32], u[32];
       if (EPI == MPM_EPI_SWIGLU || EPI == MPM_EPI_SWIGLU_SAVE) {
         // this thread: D columns [64*half, 64*half + 64) of the tile
-        const float prob = prob_r;
+        const uint64_t alpha2 = f32x2(alpha, alpha), prob2 = f32x2(prob_r, prob_r);
         uint32_t dw[32];
-        float amax = 0.0f;
+        uint32_t amax2 = 0;
         uint32_t v2[32], u2[32];
         // the thread's whole share of the accumulator in flight at once, one
         // wait, then the accumulator goes back to the MMA before any math
@@ -646,15 +646,16 @@ grouped_gemm_pair_kernel(const __grid_constant__ PairMaps maps, const GemmArgs p
               *reinterpret_cast<uint4*>(ou + jj) = wu;
             }
           }
+          // two elements per step with packed f32x2 products (the same
+          // per-lane results as swiglu_fwd); the row amax over |D| as bf16
+          // bit patterns (non-negative bf16 order like unsigned integers)
 #pragma unroll
           for (int jj = 0; jj < 32; jj += 2) {
-            const float g0 = __fmul_rn(__uint_as_float(gv[jj]), alpha);
-            const float u0 = __fmul_rn(__uint_as_float(uv[jj]), alpha);
-            const float g1 = __fmul_rn(__uint_as_float(gv[jj + 1]), alpha);
-            const float u1 = __fmul_rn(__uint_as_float(uv[jj + 1]), alpha);
-            const uint32_t pk = pack_bf16(swiglu_fwd(g0, u0, prob), swiglu_fwd(g1, u1, prob));
+            float d0, d1;
+            swiglu_fwd2(gv[jj], gv[jj + 1], uv[jj], uv[jj + 1], alpha2, prob2, d0, d1);
+            const uint32_t pk = pack_bf16(d0, d1);
             dw[cc * 16 + jj / 2] = pk;
-            amax = fmaxf(amax, fmaxf(fabsf(bf16lo(pk)), fabsf(bf16hi(pk))));
+            amax2 = absmax_bf16x2(amax2, pk);
           }
         }
         // D tile (128 rows x 128 columns) -> staging box `half`, then TMA store
@@ -676,6 +677,7 @@ grouped_gemm_pair_kernel(const __grid_constant__ PairMaps maps, const GemmArgs p
             tma_store_2d(&maps.out, (int)k.n0 + b * OUT_BOX_COLS, y, sOut + b * OUT_BOX_BYTES);
           bulk_commit_group();
         }
+        const float amax = bf16lo(max(amax2 & 0xFFFFu, amax2 >> 16));
         if (row_ok && p.amax && amax > 0.0f)
           atomicMax(reinterpret_cast<unsigned*>(p.amax) + grow, __float_as_uint(amax));
       } else if (EPI == MPM_EPI_BF16) {

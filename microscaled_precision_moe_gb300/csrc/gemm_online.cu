@@ -16,12 +16,12 @@
 // Layout on GB300: the reduction tile is one ring stage (256 FP4 elements),
 // so every stage produces its own dO_i.  A CTA pair computes a 256-row x
 // 128-column output tile with tcgen05.mma.cta_group::2 (M = 256, N = 128);
-// dO_i goes to one of two 128-column TMEM accumulators (the MMAs of tile
-// i + 1 run while the epilogue drains tile i); the epilogue warps keep O in
+// dO_i goes to one of three 128-column TMEM accumulators (the MMAs of the
+// next two tiles run while the epilogue drains tile i); the epilogue warps keep O in
 // registers (one row per thread, 64 columns), fold each dO_i in with packed
 // f32x2 FMAs, and after the last tile write bf16 Y through a 128-byte-swizzled
-// staging box with TMA stores.  TMEM: two accumulators (256 columns) and the
-// stages' scale tiles (32 columns each).  Expert segments are multiples of
+// staging box with TMA stores.  TMEM: three accumulators (384 columns) and
+// four stages' scale tiles (32 columns each).  Expert segments are multiples of
 // 256 rows (mpm_moe_build_segments with pad = 256), as for the CTA-pair GEMM.
 #include "gemm.cuh"
 
@@ -32,7 +32,7 @@ constexpr int BM = 128;              // rows per CTA; 256 per pair
 constexpr int BN = 128;              // output columns per tile (64 B rows per CTA)
 constexpr int BKB = 128;             // bytes of K per stage (256 FP4 elements)
 constexpr int KT = 256;              // reduction tile of the online quantisation
-constexpr int S = 6;                 // ring stages
+constexpr int S = 4;                 // ring stages (and TMEM scale slots)
 constexpr int A_STAGE = BM * BKB;            // 16 KB
 constexpr int B_STAGE = (BN / 2) * BKB;      // this CTA's 64 rows of B: 8 KB
 constexpr int SFA_BYTES = 4 * 512;           // 4 K-steps x one 128-row tile
@@ -42,14 +42,15 @@ constexpr int OUT_BOX_COLS = 64;
 constexpr int OUT_BOX_BYTES = BM * OUT_BOX_COLS * 2;    // 16 KB
 constexpr int OUT_BYTES = 2 * OUT_BOX_BYTES;            // the 128 x 128 bf16 tile
 constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t SF_TMEM_BASE = 2 * BN;    // after the two accumulators
+constexpr uint32_t NACC = 3;                // accumulators of 128 columns
+constexpr uint32_t SF_TMEM_BASE = NACC * BN;  // after the accumulators
 constexpr uint32_t SF_COLS = 16 + 16;        // SFA 4 tiles + SFB 4 tiles, 4 columns each
 static_assert(SF_TMEM_BASE + S * SF_COLS <= TMEM_COLS, "TMEM budget");
 constexpr int EPI_WARP0 = 3;
 constexpr int EPI_THREADS = 256;
 constexpr int NTHREADS = 14 * 32;    // 0 TMA, 1 MMA, 2 + 11..13 scale stores, 3..10 epilogue
 
-constexpr int smem_bytes() { return 2048 + S * STAGE_BYTES + OUT_BYTES + (4 * S + 4) * 8 + 32; }
+constexpr int smem_bytes() { return 2048 + S * STAGE_BYTES + OUT_BYTES + (4 * S + 2 * NACC) * 8 + 32; }
 
 struct OnlineMaps {
   CUtensorMap a, b, sfa, sfb, out;
@@ -140,9 +141,9 @@ fc2_online_kernel(const __grid_constant__ OnlineMaps maps, const GemmArgs p, con
   const uint32_t sBar = sOut + OUT_BYTES;
   const uint32_t bar_full = sBar, bar_empty = sBar + 8 * S;
   const uint32_t bar_acc = sBar + 16 * S;      // buffer b: full at + 16 b, empty at + 16 b + 8
-  const uint32_t sTmem = bar_acc + 32;
+  const uint32_t sTmem = bar_acc + 16 * NACC;
   const uint32_t sFlag = sTmem + 8;
-  const uint32_t bar_sf = bar_acc + 48;        // scale tiles of a stage in TMEM (leader)
+  const uint32_t bar_sf = sTmem + 16;          // scale tiles of a stage in TMEM (leader)
   const uint32_t bar_sfull = bar_sf + 8 * S;   // scale tiles of a stage in shared memory
   volatile uint32_t* tmem_holder = reinterpret_cast<volatile uint32_t*>(gbase + (sTmem - base));
   volatile int* fail_flag = reinterpret_cast<volatile int*>(gbase + (sFlag - base));
@@ -155,7 +156,7 @@ fc2_online_kernel(const __grid_constant__ OnlineMaps maps, const GemmArgs p, con
       mbar_init(bar_sf + 8 * s, 2);            // one arrive per CTA (after its store warps)
       mbar_init(bar_sfull + 8 * s, 1);
     }
-    for (uint32_t b = 0; b < 2; ++b) {
+    for (uint32_t b = 0; b < NACC; ++b) {
       mbar_init(bar_acc + 16 * b, 1);
       mbar_init(bar_acc + 16 * b + 8, 16);     // one arrive per epilogue warp of both CTAs
     }
@@ -220,7 +221,7 @@ fc2_online_kernel(const __grid_constant__ OnlineMaps maps, const GemmArgs p, con
       const Task k = task_of(p, t, n_tiles, &bad, cur);
       if (!k.valid) break;
       for (int kb = 0; kb < n_kt; ++kb, ++j) {
-        const uint32_t ab = j & 1u, use = j >> 1;
+        const uint32_t ab = j % NACC, use = j / NACC;
         if (!mbar_wait_cluster(bar_acc + 16 * ab + 8, (use & 1u) ^ 1u, p.status)) { ok = false; break; }
         if (!mbar_wait(bar_sf + 8 * s, ph, p.status)) { ok = false; break; }
         tc_fence_after();
@@ -287,8 +288,7 @@ fc2_online_kernel(const __grid_constant__ OnlineMaps maps, const GemmArgs p, con
     const int half = (warp - EPI_WARP0) >> 2;
     const int r = q * 32 + lane;
     const uint32_t trow0 = tmem + ((uint32_t)(q * 32) << 16) + half * 64;
-    const uint32_t acce_leader0 = map_to_rank(bar_acc + 8, 0);
-    const uint32_t acce_leader1 = map_to_rank(bar_acc + 16 + 8, 0);
+    const uint32_t acce_leader0 = map_to_rank(bar_acc + 8, 0);   // buffer b: + 16 b
     const bool leader_thread = (threadIdx.x == EPI_WARP0 * 32);
     const float* gs_rows = static_cast<const float*>(p.aux);    // [rows, n_kt]
     uint32_t j = 0;
@@ -304,7 +304,7 @@ fc2_online_kernel(const __grid_constant__ OnlineMaps maps, const GemmArgs p, con
       float g_next = gsr[0];
       bool failed = false;
       for (int kb = 0; kb < n_kt; ++kb, ++j) {
-        const uint32_t ab = j & 1u, use = j >> 1;
+        const uint32_t ab = j % NACC, use = j / NACC;
         const float g = g_next;
         if (kb + 1 < n_kt) g_next = gsr[kb + 1];
         const bool w_ok = mbar_wait_cluster(bar_acc + 16 * ab, use & 1u, p.status);
@@ -320,7 +320,7 @@ fc2_online_kernel(const __grid_constant__ OnlineMaps maps, const GemmArgs p, con
           if (h == 1) {
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive_cluster(ab ? acce_leader1 : acce_leader0);
+            if (lane == 0) mbar_arrive_cluster(acce_leader0 + 16 * ab);
           }
 #pragma unroll
           for (int c = 0; c < 32; c += 2)
