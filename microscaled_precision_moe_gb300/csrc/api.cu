@@ -481,6 +481,9 @@ mpm_status mpm_moe_grouped_gemm(const mpm_grouped_gemm_desc* d, cudaStream_t str
       if (!make_out_tmap(&tout, d->out_dev, d->N, rows, d->ldo, true)) return MPM_ERR_CUDA;
     } else if (swiglu) {
       if (!make_out_tmap(&tout, d->out2_dev, d->N / 2, d->a_rows, d->ldo2)) return MPM_ERR_CUDA;
+      if (d->epilogue == MPM_EPI_SWIGLU_SAVE &&
+          !make_out_tmap(&taux, d->out_dev, d->N, d->a_rows, d->ldo))
+        return MPM_ERR_CUDA;
     }
     const int n_tiles = (int)(swiglu ? (d->N / 2) / 128 : d->N / 256);
     long long n_tasks = (long long)n_tiles * ((d->a_rows + 255) / 256);

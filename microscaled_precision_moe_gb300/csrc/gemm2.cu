@@ -230,7 +230,7 @@ MPM_DEV Task task_of(const GemmArgs& p, long long t, int n_tiles, int* bad, SegC
 struct PairMaps {
   CUtensorMap a, b, sfa, sfb;
   CUtensorMap out;    // bf16 output of the BF16 epilogue / D of the SwiGLU epilogues / dH
-  CUtensorMap aux;    // C = gate|up read by the SwiGLU-backward epilogue
+  CUtensorMap aux;    // C = gate|up: read by the SwiGLU-backward epilogue, written by SWIGLU_SAVE
 };
 
 // MAJ (bf16 only): bit 0 = A stored MN-major ([K rows, M] with M contiguous:
@@ -325,7 +325,7 @@ grouped_gemm_pair_kernel(const __grid_constant__ PairMaps maps, const GemmArgs p
       prefetch_tmap(&maps.sfb);
     }
     prefetch_tmap(&maps.out);
-    if (EPI == MPM_EPI_DSWIGLU) prefetch_tmap(&maps.aux);
+    if (EPI == MPM_EPI_DSWIGLU || EPI == MPM_EPI_SWIGLU_SAVE) prefetch_tmap(&maps.aux);
   }
   if (warp == 1) {
     tmem_alloc_pair(sTmem, TMEM_COLS);
@@ -611,6 +611,7 @@ grouped_gemm_pair_kernel(const __grid_constant__ PairMaps maps, const GemmArgs p
         // this thread: D columns [64*half, 64*half + 64) of the tile
         const uint64_t alpha2 = f32x2(alpha, alpha), prob2 = f32x2(prob_r, prob_r);
         uint32_t dw[32];
+        uint32_t cgw[EPI == MPM_EPI_SWIGLU_SAVE ? 32 : 1], cuw[EPI == MPM_EPI_SWIGLU_SAVE ? 32 : 1];
         uint32_t amax2 = 0;
         uint32_t v2[32], u2[32];
         // the thread's whole share of the accumulator in flight at once, one
@@ -625,34 +626,28 @@ grouped_gemm_pair_kernel(const __grid_constant__ PairMaps maps, const GemmArgs p
         if (lane == 0) mbar_arrive_cluster(acce_leader);   // this warp's share is read
 #pragma unroll
         for (int cc = 0; cc < 2; ++cc) {
-          const int c = half * 2 + cc;
           const uint32_t* gv = cc ? v2 : v;
           const uint32_t* uv = cc ? u2 : u;
-          if (EPI == MPM_EPI_SWIGLU_SAVE && row_ok) {
-            __nv_bfloat16* og = static_cast<__nv_bfloat16*>(p.out) + grow * p.ldo + k.n0 + c * 32;
-            __nv_bfloat16* ou = og + p.N / 2;
-#pragma unroll
-            for (int jj = 0; jj < 32; jj += 8) {
-              uint4 wg, wu;
-              wg.x = pack_bf16(__fmul_rn(__uint_as_float(gv[jj]), alpha), __fmul_rn(__uint_as_float(gv[jj + 1]), alpha));
-              wg.y = pack_bf16(__fmul_rn(__uint_as_float(gv[jj + 2]), alpha), __fmul_rn(__uint_as_float(gv[jj + 3]), alpha));
-              wg.z = pack_bf16(__fmul_rn(__uint_as_float(gv[jj + 4]), alpha), __fmul_rn(__uint_as_float(gv[jj + 5]), alpha));
-              wg.w = pack_bf16(__fmul_rn(__uint_as_float(gv[jj + 6]), alpha), __fmul_rn(__uint_as_float(gv[jj + 7]), alpha));
-              wu.x = pack_bf16(__fmul_rn(__uint_as_float(uv[jj]), alpha), __fmul_rn(__uint_as_float(uv[jj + 1]), alpha));
-              wu.y = pack_bf16(__fmul_rn(__uint_as_float(uv[jj + 2]), alpha), __fmul_rn(__uint_as_float(uv[jj + 3]), alpha));
-              wu.z = pack_bf16(__fmul_rn(__uint_as_float(uv[jj + 4]), alpha), __fmul_rn(__uint_as_float(uv[jj + 5]), alpha));
-              wu.w = pack_bf16(__fmul_rn(__uint_as_float(uv[jj + 6]), alpha), __fmul_rn(__uint_as_float(uv[jj + 7]), alpha));
-              *reinterpret_cast<uint4*>(og + jj) = wg;
-              *reinterpret_cast<uint4*>(ou + jj) = wu;
-            }
-          }
           // two elements per step with packed f32x2 products (the same
           // per-lane results as swiglu_fwd); the row amax over |D| as bf16
           // bit patterns (non-negative bf16 order like unsigned integers)
 #pragma unroll
           for (int jj = 0; jj < 32; jj += 2) {
-            float d0, d1;
-            swiglu_fwd2(gv[jj], gv[jj + 1], uv[jj], uv[jj + 1], alpha2, prob2, d0, d1);
+            // swiglu_fwd2 written out, so SWIGLU_SAVE keeps the scaled gate
+            // and up values as the bf16 words of C
+            float g0, g1, d0, d1;
+            f32x2_split(mul_f32x2(f32x2(__uint_as_float(gv[jj]), __uint_as_float(gv[jj + 1])), alpha2),
+                        g0, g1);
+            const uint64_t uu = mul_f32x2(f32x2(__uint_as_float(uv[jj]), __uint_as_float(uv[jj + 1])),
+                                          alpha2);
+            if (EPI == MPM_EPI_SWIGLU_SAVE) {
+              float u0, u1;
+              f32x2_split(uu, u0, u1);
+              cgw[cc * 16 + jj / 2] = pack_bf16(g0, g1);
+              cuw[cc * 16 + jj / 2] = pack_bf16(u0, u1);
+            }
+            const uint64_t su = mul_f32x2(f32x2(swiglu_silu(g0), swiglu_silu(g1)), uu);
+            f32x2_split(mul_f32x2(su, prob2), d0, d1);
             const uint32_t pk = pack_bf16(d0, d1);
             dw[cc * 16 + jj / 2] = pk;
             amax2 = absmax_bf16x2(amax2, pk);
@@ -676,6 +671,32 @@ grouped_gemm_pair_kernel(const __grid_constant__ PairMaps maps, const GemmArgs p
           for (int b = 0; b < 2; ++b)
             tma_store_2d(&maps.out, (int)k.n0 + b * OUT_BOX_COLS, y, sOut + b * OUT_BOX_BYTES);
           bulk_commit_group();
+        }
+        if (EPI == MPM_EPI_SWIGLU_SAVE) {
+          // C = gate | up (alpha applied, bf16) for the backward: this
+          // thread's 64 gate columns, then its 64 up columns, each round
+          // through staging box `half` and out by TMA stores (the same bits
+          // as the FC1 output the SwiGLU was computed from)
+#pragma unroll
+          for (int part = 0; part < 2; ++part) {
+            const uint32_t* cw = part ? cuw : cgw;
+            if (leader_thread) bulk_wait_group_read0();   // the previous boxes were read
+            named_sync(2, EPI_THREADS);
+            const uint32_t box = sOut + half * OUT_BOX_BYTES + r * 128;
+#pragma unroll
+            for (int c16 = 0; c16 < 8; ++c16)
+              st_shared_v4(box + ((c16 ^ (r & 7)) << 4), cw[4 * c16], cw[4 * c16 + 1],
+                           cw[4 * c16 + 2], cw[4 * c16 + 3]);
+            fence_proxy_async();
+            named_sync(2, EPI_THREADS);
+            if (leader_thread) {
+              const int x0 = (int)k.n0 + (part ? (int)(p.N / 2) : 0);
+#pragma unroll
+              for (int b = 0; b < 2; ++b)
+                tma_store_2d(&maps.aux, x0 + b * OUT_BOX_COLS, (int)orow, sOut + b * OUT_BOX_BYTES);
+              bulk_commit_group();
+            }
+          }
         }
         const float amax = bf16lo(max(amax2 & 0xFFFFu, amax2 >> 16));
         if (row_ok && p.amax && amax > 0.0f)
