@@ -111,6 +111,24 @@ bool make_bf16_tmap(CUtensorMap* m, const void* base, long long cols, long long 
   return r == CUDA_SUCCESS;
 }
 
+// [rows, cols] uint8 matrix with row pitch `ld` bytes, box_cols x box_rows
+// boxes, optionally with the 128-byte swizzle (box_cols = 128): the code
+// stores of the MXFP8 quantiser
+bool make_u8_tmap(CUtensorMap* m, const void* base, long long cols, long long rows, long long ld,
+                  unsigned box_cols, unsigned box_rows, bool swizzle128) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)ld};
+  cuuint32_t box[2] = {box_cols, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box,
+                  estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 // [rows, cols] bf16 or fp32 output with row pitch `ld` elements: 128-row boxes
 // of 128 bytes per row (64 bf16 or 32 fp32 columns), 128-byte swizzle (the
 // staging layout of the TMA-store epilogues)
@@ -172,10 +190,16 @@ mpm_status mpm_mxfp8_quantize(const void* x, int64_t M, int64_t K, int64_t ldx, 
     if (ldc < M) return MPM_ERR_SHAPE;
     if (!aligned(col_q, 16) || ldc % 16 != 0) return MPM_ERR_ALIGN;
   }
-  CUtensorMap tx;
+  CUtensorMap tx, trow, tcol;
+  std::memset(&trow, 0, sizeof(trow));
+  std::memset(&tcol, 0, sizeof(tcol));
   if (!make_bf16_tmap(&tx, x, K, M, ldx, 64, 128)) return MPM_ERR_CUDA;
-  return cuda_status(mpm::launch_mxfp8_tma(tx, M, K, ldx, flags, row_q, row_s, col_q, ldc, col_s,
-                                           m_valid, status_ptr(), stream));
+  if ((flags & MPM_ROWWISE) && !make_u8_tmap(&trow, row_q, K, M, K, 64, 128, false))
+    return MPM_ERR_CUDA;
+  if ((flags & MPM_COLWISE) && !make_u8_tmap(&tcol, col_q, M, K, ldc, 128, 64, true))
+    return MPM_ERR_CUDA;
+  return cuda_status(mpm::launch_mxfp8_tma(tx, trow, tcol, M, K, ldx, flags, row_q, row_s, col_q,
+                                           ldc, col_s, m_valid, status_ptr(), stream));
 }
 
 mpm_status mpm_nvfp4_quantize_per_token(const void* x, int64_t M, int64_t K, int64_t ldx,

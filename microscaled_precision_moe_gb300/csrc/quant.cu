@@ -392,13 +392,26 @@ MPM_DEV uint32_t absmax_bf16x2_packed(const uint32_t (&w)[N]) {
 constexpr int MQ_TM = 128, MQ_TK = 64, MQ_STAGES = 2;
 constexpr int MQ_TILE_BYTES = MQ_TM * MQ_TK * 2;     // 16 KB
 
+// Codes of a full tile (all 128 rows below the valid row count, all 64
+// columns inside K) leave through shared memory by TMA stores: the
+// row-wise codes as a 128 x 64-byte box, the transposed column-wise codes as
+// a 64 x 128-byte box (128-byte swizzle), double-buffered so a tile's
+// stores drain while the next tile is encoded.  Measured without any code
+// stores the kernel ran in 56 % of its time: the per-thread stores (each
+// warp's column-copy store touching 32 lines) were the bound.  Edge tiles
+// keep the per-thread stores, and the scale bytes always use them.
+constexpr int MQ_OUT_BYTES = MQ_TM * MQ_TK + MQ_TK * MQ_TM;     // 8 KB rows + 8 KB columns
+
 __global__ void __launch_bounds__(256) mxfp8_quant_tma_kernel(const __grid_constant__ CUtensorMap tx,
+                                                             const __grid_constant__ CUtensorMap trow,
+                                                             const __grid_constant__ CUtensorMap tcol,
                                                              const Mxfp8Args p, int n_kt) {
   extern __shared__ uint8_t mq_smem[];
   const uint32_t raw = smem_u32(mq_smem);
   const uint32_t base = (raw + 1023u) & ~1023u;
   const uint8_t* gbase = mq_smem + (base - raw);
-  const uint32_t bar = base + MQ_STAGES * MQ_TILE_BYTES;
+  const uint32_t sOut = base + MQ_STAGES * MQ_TILE_BYTES;        // two output buffers
+  const uint32_t bar = sOut + 2 * MQ_OUT_BYTES;
   const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
   long long M_eff = p.M;
   if (p.m_valid) { const long long mv = *p.m_valid; M_eff = mv < M_eff ? mv : M_eff; }
@@ -407,6 +420,8 @@ __global__ void __launch_bounds__(256) mxfp8_quant_tma_kernel(const __grid_const
     for (int s = 0; s < MQ_STAGES; ++s) mbar_init(bar + 8 * s, 1);
     fence_mbar_init();
     prefetch_tmap(&tx);
+    if (p.flags & MPM_ROWWISE) prefetch_tmap(&trow);
+    if (p.flags & MPM_COLWISE) prefetch_tmap(&tcol);
     for (int i = 0; i < MQ_STAGES; ++i) {
       const long long ti = blockIdx.x + (long long)i * gridDim.x;
       if (ti >= n_tiles) break;
@@ -416,13 +431,23 @@ __global__ void __launch_bounds__(256) mxfp8_quant_tma_kernel(const __grid_const
     }
   }
   __syncthreads();
-  int it = 0;
+  int it = 0, last_buf = -1;                        // last_buf: thread 0's newest store group
   for (long long ti = blockIdx.x; ti < n_tiles; ti += gridDim.x, ++it) {
     const int s = it % MQ_STAGES;
     const bool ok = mbar_wait(bar + 8 * s, (uint32_t)(it / MQ_STAGES) & 1u, p.status);
+    // output buffer it % 2 is free once the store groups that read it have:
+    // all but the newest group, or all of them when the newest used it too
+    // (only full tiles commit a group)
+    if (t == 0) {
+      if (last_buf == (it & 1)) bulk_wait_group_read0();
+      else bulk_wait_group_read1();
+    }
     if (__syncthreads_or(!ok)) break;
     const uint8_t* tile = gbase + s * MQ_TILE_BYTES;          // row r at r * 128 bytes
     const long long m0 = (ti / n_kt) * MQ_TM, k0 = (ti % n_kt) * MQ_TK;
+    const bool full = (m0 + MQ_TM <= M_eff) && (k0 + MQ_TK <= p.K);
+    const uint32_t orow = sOut + (it & 1) * MQ_OUT_BYTES;     // [128 rows][64 B]
+    const uint32_t ocol = orow + MQ_TM * MQ_TK;               // [64 columns][128 B], swizzled
     if (p.flags & MPM_ROWWISE) {
       // one thread per 32-element row block: warp w takes rows 16 w .. 16 w + 15,
       // lanes 2 i and 2 i + 1 the two blocks of row 16 w + i; with the swizzle
@@ -440,9 +465,15 @@ __global__ void __launch_bounds__(256) mxfp8_quant_tma_kernel(const __grid_const
         const int e = mx_exponent(absmax_bf16x2_packed(w) << 16);
         uint32_t o[8];
         mx_encode32(w, pow2_neg(e), o);
-        uint4* d = reinterpret_cast<uint4*>(p.row_q + row * p.K + col);
-        d[0] = make_uint4(o[0], o[1], o[2], o[3]);
-        d[1] = make_uint4(o[4], o[5], o[6], o[7]);
+        if (full) {
+          const uint32_t a = orow + rr * MQ_TK + bl * 32;
+          st_shared_v4(a, o[0], o[1], o[2], o[3]);
+          st_shared_v4(a + 16, o[4], o[5], o[6], o[7]);
+        } else {
+          uint4* d = reinterpret_cast<uint4*>(p.row_q + row * p.K + col);
+          d[0] = make_uint4(o[0], o[1], o[2], o[3]);
+          d[1] = make_uint4(o[4], o[5], o[6], o[7]);
+        }
         p.row_s[sf_offset(row, col >> 5, p.row_s_cols_pad)] = (uint8_t)(e + 127);
       }
     }
@@ -507,7 +538,15 @@ __global__ void __launch_bounds__(256) mxfp8_quant_tma_kernel(const __grid_const
         o[2 * a + 1] = half ? p1[a] : got;
       }
       const long long col = k0 + 2 * cp + half;
-      if (col < p.K && mb < M_eff) {
+      if (full) {
+        // column c of the tile is row c of the staged box; this thread's 32
+        // codes are 16-byte chunks 2g and 2g + 1 of it, 128-byte swizzled
+        const int cr = 2 * cp + half;
+        const uint32_t rowa = ocol + cr * MQ_TM;
+        st_shared_v4(rowa + (((2 * g) ^ (cr & 7)) << 4), o[0], o[1], o[2], o[3]);
+        st_shared_v4(rowa + (((2 * g + 1) ^ (cr & 7)) << 4), o[4], o[5], o[6], o[7]);
+        p.col_s[sf_offset(col, mb >> 5, p.col_s_cols_pad)] = (uint8_t)(e_own + 127);
+      } else if (col < p.K && mb < M_eff) {
         uint8_t* dst = p.col_q + col * p.ldc + mb;
         if (nvalid >= 32) {
           uint4* d4 = reinterpret_cast<uint4*>(dst);
@@ -521,8 +560,15 @@ __global__ void __launch_bounds__(256) mxfp8_quant_tma_kernel(const __grid_const
         p.col_s[sf_offset(col, mb >> 5, p.col_s_cols_pad)] = (uint8_t)(e_own + 127);
       }
     }
+    if (full) fence_proxy_async();                    // staged codes visible to the TMA stores
     __syncthreads();                                  // stage s fully read
     if (t == 0) {
+      if (full) {
+        if (p.flags & MPM_ROWWISE) tma_store_2d(&trow, (int)k0, (int)m0, orow);
+        if (p.flags & MPM_COLWISE) tma_store_2d(&tcol, (int)m0, (int)k0, ocol);
+        bulk_commit_group();
+        last_buf = it & 1;
+      }
       const long long tn = ti + (long long)MQ_STAGES * gridDim.x;
       if (tn < n_tiles) {
         mbar_arrive_expect_tx(bar + 8 * s, MQ_TILE_BYTES);
@@ -531,6 +577,7 @@ __global__ void __launch_bounds__(256) mxfp8_quant_tma_kernel(const __grid_const
       }
     }
   }
+  if (t == 0) bulk_wait_group0();                   // the code stores have completed
   if (p.pad_blocks) {
     // host-sized buffers: zero the padding entries of the scale tiles
     const long long tid = (long long)blockIdx.x * blockDim.x + t;
@@ -667,7 +714,8 @@ cudaError_t launch_nvfp4_online(const void* x, long long M, int K, long long ldx
   return cudaGetLastError();
 }
 
-cudaError_t launch_mxfp8_tma(const CUtensorMap& tx, long long M, long long K, long long ldx,
+cudaError_t launch_mxfp8_tma(const CUtensorMap& tx, const CUtensorMap& trow, const CUtensorMap& tcol,
+                             long long M, long long K, long long ldx,
                              unsigned flags, uint8_t* row_q, uint8_t* row_s, uint8_t* col_q,
                              long long ldc, uint8_t* col_s, const int* m_valid, int* status,
                              cudaStream_t st) {
@@ -681,7 +729,7 @@ cudaError_t launch_mxfp8_tma(const CUtensorMap& tx, long long M, long long K, lo
   p.status = status;
   const int n_kt = (int)((K + MQ_TK - 1) / MQ_TK);
   const long long n_tiles = (M + MQ_TM - 1) / MQ_TM * n_kt;
-  constexpr int smem = 1024 + MQ_STAGES * MQ_TILE_BYTES + 64;
+  constexpr int smem = 1024 + MQ_STAGES * MQ_TILE_BYTES + 2 * MQ_OUT_BYTES + 64;
   static int ctas[64] = {0};
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
@@ -697,7 +745,7 @@ cudaError_t launch_mxfp8_tma(const CUtensorMap& tx, long long M, long long K, lo
   long long grid = dev < 64 ? ctas[dev] : 1;
   if (grid > n_tiles) grid = n_tiles;
   if (grid < 1) grid = 1;
-  mxfp8_quant_tma_kernel<<<(unsigned)grid, 256, smem, st>>>(tx, p, n_kt);
+  mxfp8_quant_tma_kernel<<<(unsigned)grid, 256, smem, st>>>(tx, trow, tcol, p, n_kt);
   return cudaGetLastError();
 }
 

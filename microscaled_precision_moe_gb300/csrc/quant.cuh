@@ -14,8 +14,11 @@ cudaError_t launch_nvfp4_weight(const void* const* parts, const long long* part_
 // == 0): codes, tiled block scales and one outer scale per (row, tile)
 cudaError_t launch_nvfp4_online(const void* x, long long M, int K, long long ldx, uint8_t* q,
                                 uint8_t* s, float* gs, const int* m_valid, cudaStream_t st);
-// x is read through a 2-D bf16 tensor map (box 64 columns x 128 rows)
-cudaError_t launch_mxfp8_tma(const CUtensorMap& tx, long long M, long long K, long long ldx,
+// x is read through a 2-D bf16 tensor map (box 64 columns x 128 rows); the
+// codes of full tiles are stored through trow (row_q, box 64 x 128 bytes)
+// and tcol (col_q, box 128 x 64 bytes, 128-byte swizzle)
+cudaError_t launch_mxfp8_tma(const CUtensorMap& tx, const CUtensorMap& trow, const CUtensorMap& tcol,
+                             long long M, long long K, long long ldx,
                              unsigned flags, uint8_t* row_q, uint8_t* row_s, uint8_t* col_q,
                              long long ldc, uint8_t* col_s, const int* m_valid, int* status,
                              cudaStream_t st);

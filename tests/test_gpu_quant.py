@@ -183,6 +183,49 @@ def test_mxfp8_shapes(M, K):
     _check_mxfp8(x, ldc=((M + 15) // 16) * 16)
 
 
+@pytest.mark.parametrize("rowwise,colwise", [(True, True), (True, False), (False, True)])
+def test_mxfp8_full_and_edge_tiles_mixed(rowwise, colwise):
+    """1000 x 2080: seven full 128 x 64 tiles per column of tiles and a
+    ragged eighth, and a 32-column last tile column, so every CTA meets full
+    tiles (codes staged in shared memory and stored by TMA) and edge tiles
+    (stored per thread) in changing order; then the same input with a
+    device row count of 700 and a padded column pitch: rows at and past it
+    keep the sentinel bytes."""
+    ops = _ops()
+    M, K = 1000, 2080
+    x_dev = synth.normal_bf16(7, 91, (M, K), "cuda", std=2.0, outlier_p=0.01, outlier_mul=1e3)
+    x = np_bf16(x_dev)
+    rq, rs = Q.mxfp8_quantize_rowwise(x)
+    cq, cs = Q.mxfp8_quantize_colwise(x)
+    o = ops.mxfp8_quantize(x_dev, rowwise=rowwise, colwise=colwise)
+    torch.cuda.synchronize()
+    if rowwise:
+        assert_bytes_equal(u8(o["row_q"]), rq, "row codes")
+        assert_bytes_equal(u8(o["row_s"]), Q.swizzle_scales(rs), "row scales")
+    if colwise:
+        assert_bytes_equal(u8(o["col_q"])[:, :M], cq, "col codes")
+        assert_bytes_equal(u8(o["col_s"]), Q.swizzle_scales(cs), "col scales")
+    mv, ldc = 700, 1024
+    out = {}
+    if rowwise:
+        out["row_q"] = torch.full((M, K), 0xA5, dtype=torch.uint8, device="cuda")
+    if colwise:
+        out["col_q"] = torch.full((K, ldc), 0xA5, dtype=torch.uint8, device="cuda")
+    o = ops.mxfp8_quantize(x_dev, rowwise=rowwise, colwise=colwise, ldc=ldc,
+                           m_valid=torch.tensor([mv], dtype=torch.int32, device="cuda"), out=out)
+    torch.cuda.synchronize()
+    xv = x.copy()
+    xv[mv:] = 0
+    if rowwise:
+        got = u8(o["row_q"])
+        assert_bytes_equal(got[:mv], Q.mxfp8_quantize_rowwise(xv[:mv])[0], "row codes, m_valid")
+        assert (got[mv:] == 0xA5).all(), "row codes written past m_valid"
+    if colwise:
+        got = u8(o["col_q"])
+        assert_bytes_equal(got[:, :mv], Q.mxfp8_quantize_colwise(xv)[0][:, :mv], "col codes, m_valid")
+        assert (got[:, mv:] == 0xA5).all(), "col codes written past m_valid"
+
+
 def test_quantizers_deterministic():
     x = synth.normal_bf16(6, 80, (512, 2048), "cuda")
     ops = _ops()
