@@ -393,7 +393,42 @@ def _single_expert_line(peak_fp4, peak_hbm, reps=3):
     return out
 
 
-def _mxfp8_layer_line(peak_fp8, steps=10):
+def _mxfp8_gemm_bounds(T, H, I, E, k, stage_ms, peak_fp8, peak_hbm):
+    """Per GEMM of the MXFP8 step: algorithmic FLOPs (routed rows M = T k),
+    the fewest HBM bytes it can move (each operand read once as stored, E4M3
+    codes plus one E8M0 scale per 32, each output written once: bf16
+    activations, fp32 weight gradients, and for FC1 the saved C = gate|up),
+    the time each floor allows at the given peaks (TFLOP/s, GB/s), and the
+    measured time's fraction of the larger floor."""
+    M = T * k
+    q = lambda n: n * (1 + 1 / 32)                       # MXFP8 operand bytes
+    spec = {
+        "fc1": (2 * M * 2 * I * H, q(M * H) + q(E * 2 * I * H) + 2 * M * I + 2 * M * 2 * I),
+        "fc2": (2 * M * H * I, q(M * I) + q(E * H * I) + 2 * M * H),
+        "fc2_dgrad": (2 * M * I * H, q(M * H) + q(E * I * H) + 2 * M * 2 * I + 2 * M * 2 * I),
+        "fc2_wgrad": (2 * M * H * I, q(H * M) + q(I * M) + 4 * E * H * I),
+        "fc1_dgrad": (2 * M * H * 2 * I, q(M * 2 * I) + q(H * E * 2 * I) + 2 * M * H),
+        "fc1_wgrad": (2 * M * 2 * I * H, q(2 * I * M) + q(H * M) + 4 * E * 2 * I * H),
+    }
+    out, tot_ms, tot_floor = {}, 0.0, 0.0
+    for name, (flops, byts) in spec.items():
+        mma = flops / (peak_fp8 * 1e12) * 1e3
+        hbm = byts / (peak_hbm * 1e9) * 1e3
+        floor = max(mma, hbm)
+        ms = stage_ms.get(name)
+        out[name] = {"ms": ms, "flops": int(flops), "hbm_bytes": int(byts),
+                     "mma_floor_ms": round(mma, 4), "hbm_floor_ms": round(hbm, 4),
+                     "bound": "hbm" if hbm >= mma else "tensor",
+                     "frac_of_bound": round(floor / ms, 3) if ms else None}
+        if ms:
+            tot_ms += ms
+            tot_floor += floor
+    out["all_gemms"] = {"ms": round(tot_ms, 4), "floor_ms": round(tot_floor, 4),
+                        "frac_of_bound": round(tot_floor / tot_ms, 3) if tot_ms else None}
+    return out
+
+
+def _mxfp8_layer_line(peak_fp8, steps=10, peak_hbm=None):
     from microscaled_precision_moe_gb300 import synth
     from microscaled_precision_moe_gb300.moe import MXFP8MoE
     s = synth.MOE_30B_BWD
@@ -429,6 +464,8 @@ def _mxfp8_layer_line(peak_fp8, steps=10):
          "frac_fp8_peak": round(tf / peak_fp8, 3),
          "gemm_TFLOP/s": round(L.gemm_flops() / (gemm_ms * 1e-3) / 1e12, 1),
          "stage_ms": stage,
+         "gemm_bounds": (_mxfp8_gemm_bounds(s.T, s.H, s.I, s.E, s.k, stage, peak_fp8, peak_hbm)
+                         if peak_hbm else None),
          "note": "whole fwd+bwd step (weight quantisation included) / GEMM algorithmic FLOPs"}
     del L, x, w1, w2, dy
     torch.cuda.empty_cache()
@@ -723,14 +760,15 @@ def main():
     from microscaled_precision_moe_gb300 import build
     build.build()
     if args.case == "mxfp8":
-        r = _mxfp8_layer_line(peak_fp8_sus, steps=args.steps)
+        r = _mxfp8_layer_line(peak_fp8_sus, steps=args.steps, peak_hbm=peaks["hbm"])
         if rank == 0:
             print(json.dumps({"metric": METRIC, "value": r["TFLOP/s"], "unit": "TFLOP/s",
                               "n_gpus": world, "steps": args.steps, "warmup": 3,
                               "ms_per_step": r["ms_per_step"], "higher_is_better": True,
                               "dtype": "mxfp8", "config": {"workload": r["workload"]},
                               "note": r["note"], "gemm_TFLOP/s": r["gemm_TFLOP/s"],
-                              "stage_ms": r["stage_ms"]}), flush=True)
+                              "stage_ms": r["stage_ms"], "gemm_bounds": r["gemm_bounds"]}),
+                  flush=True)
         return 0
     if args.case == "quant":
         r = _quantizer_lines(peaks["hbm"])
@@ -927,7 +965,7 @@ def main():
                                 "cores": _cores(), "kind": "oracle", "sample": desc}
     if not args.no_also:
         also = {"quantizers": _quantizer_lines(peaks["hbm"])}
-        also["mxfp8_layer_fwd_bwd"] = _mxfp8_layer_line(peak_fp8_sus)
+        also["mxfp8_layer_fwd_bwd"] = _mxfp8_layer_line(peak_fp8_sus, peak_hbm=peaks["hbm"])
         also["nvfp4_layer_fwd_30b"] = _nvfp4_30b_line(peak_fp4_sus)
         also["nvfp4_layer_fwd_fc2_online"] = _nvfp4_online_line(peak_fp4)
         also["nvfp4_layer_bf16_bwd"] = _nvfp4_bf16_bwd_line(peaks["bf16_sus"])

@@ -118,6 +118,16 @@ constexpr int stages() {
   return EPI == MPM_EPI_DSWIGLU ? (KIND == MPM_KIND_BF16 ? 5 : 4)
                                 : (staging64<KIND, EPI>() ? 4 : Cfg<KIND>::kStages);
 }
+// The SwiGLU-backward epilogue parks the second half of a CTA's dD tile
+// (128 columns) in TMEM columns [DSW_SPARE, 512) when the accumulator and the
+// scale slots leave them free, so it can hand the accumulator back before C
+// streams in (only with one accumulator: the bf16 kind has two).
+constexpr uint32_t DSW_SPARE = 384;
+template <int KIND, int EPI>
+constexpr bool dsw_park() {
+  return EPI == MPM_EPI_DSWIGLU && KIND != MPM_KIND_BF16 &&
+         SF_TMEM_BASE + stages<KIND, EPI>() * Cfg<KIND>::kSfTmemPerStage <= DSW_SPARE;
+}
 template <int KIND, int EPI>
 constexpr int out_staging_bytes() {
   return staging64<KIND, EPI>() ? 2 * STAGE_OUT_BYTES : STAGE_OUT_BYTES;
@@ -799,17 +809,52 @@ grouped_gemm_pair_kernel(const __grid_constant__ PairMaps maps, const GemmArgs p
         // (this warp's half of the chunk), reads dD for them from TMEM,
         // overwrites the C values in place with dg / du, and the two boxes
         // go out to dH by TMA stores; the buffer is then refilled with chunk
-        // cq + 2.  The accumulator is handed back once the last chunk's
-        // columns are in registers.
+        // cq + 2.  Where TMEM has room (dsw_park), the thread's columns of
+        // chunks 2 and 3 are first copied to spare TMEM columns and those of
+        // chunks 0 and 1 loaded into registers, and the accumulator goes back
+        // to the MMA before any C is waited for; otherwise it is handed back
+        // once the last chunk's columns are in registers.
         const float prob = prob_r;
+        constexpr bool kPark = dsw_park<KIND, EPI>();
+        const uint32_t park = trow0 + DSW_SPARE + half * 64;   // this thread's 64 parked columns
+        if (kPark) {
+          tmem_ld_32x32b_x32(trow + 2 * 64 + half * 32, v);
+          tmem_ld_32x32b_x32(trow + 3 * 64 + half * 32, u);
+          tmem_ld_wait();
+          tmem_st_32x32b_x32(park, v);
+          tmem_st_32x32b_x32(park + 32, u);
+          tmem_ld_32x32b_x32(trow + 0 * 64 + half * 32, v);
+          tmem_ld_32x32b_x32(trow + 1 * 64 + half * 32, u);
+          tmem_ld_wait();
+          tmem_st_wait();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive_cluster(acce_leader);     // this warp's share is read
+        }
 #pragma unroll 1
         for (int cq = 0; cq < 4; ++cq) {
-          tmem_ld_32x32b_x32(trow + cq * 64 + half * 32, v);
-          tmem_ld_wait();
-          if (cq == 3) {
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive_cluster(acce_leader);   // this warp's share is read
+          if (kPark) {
+            // v holds the even chunk's columns, u the odd one's: move this
+            // chunk's into v (registers cannot be selected by a runtime index)
+            if (cq == 1) {
+#pragma unroll
+              for (int i = 0; i < 32; ++i) v[i] = u[i];
+            } else if (cq == 2) {
+              tmem_ld_32x32b_x32(park, v);
+              tmem_ld_32x32b_x32(park + 32, u);
+              tmem_ld_wait();
+            } else if (cq == 3) {
+#pragma unroll
+              for (int i = 0; i < 32; ++i) v[i] = u[i];
+            }
+          } else {
+            tmem_ld_32x32b_x32(trow + cq * 64 + half * 32, v);
+            tmem_ld_wait();
+            if (cq == 3) {
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) mbar_arrive_cluster(acce_leader);   // this warp's share is read
+            }
           }
           const int b = cq & 1;
           const uint32_t buf = sOut + b * STAGE_OUT_BYTES;

@@ -95,3 +95,26 @@ def test_summary_of_a_line():
     assert s["stage_frac_hbm"] == {"gather": 0.95}
     assert s["nvfp4_30b_ms"] is None and s["nvfp4_30b_frac_fp4_burst"] is None
     assert bench._summary({"roofline": {"frac": 0.1}}, peaks)["decode_ms"] == {}
+
+
+def test_mxfp8_gemm_bounds_bytes_and_floors():
+    """Hand-counted case: 32 tokens, top-2 (64 routed rows), H 64, I 32,
+    2 experts.  MXFP8 operand = 1 byte per element plus 1/32 byte of scale."""
+    import bench
+    st = {"fc1": 1e-3, "fc2": 1e-3, "fc2_dgrad": 1e-3, "fc2_wgrad": 1e-3, "fc1_dgrad": 1e-3,
+          "fc1_wgrad": 2e-3}
+    r = bench._mxfp8_gemm_bounds(32, 64, 32, 2, 2, st, peak_fp8=1.0, peak_hbm=1.0)
+    # fc2 wgrad: dY column copy 64 x 64, D column copy 32 x 64, dW2 fp32 2 x 64 x 32
+    assert r["fc2_wgrad"]["hbm_bytes"] == 4224 + 2112 + 16384
+    assert r["fc2_wgrad"]["flops"] == 2 * 64 * 64 * 32
+    # fc1: X 64 x 64, W1 2 x 64 x 64 (codes + scales), D 64 x 32 bf16, C 64 x 64 bf16
+    assert r["fc1"]["hbm_bytes"] == 4224 + 8448 + 4096 + 8192
+    # 1 TFLOP/s and 1 GB/s: the floors in ms are flops / 1e9 and bytes / 1e6
+    assert r["fc1"]["mma_floor_ms"] == round(2 * 64 * 64 * 64 / 1e9, 4)
+    assert r["fc1"]["hbm_floor_ms"] == round(24960 / 1e6, 4)
+    assert r["fc1"]["bound"] == "hbm"
+    # fc1 wgrad: dH and X column copies 64 x 64 each, dW1 fp32 2 x 64 x 64
+    assert r["fc1_wgrad"]["hbm_bytes"] == 4224 + 4224 + 32768
+    assert r["fc1_wgrad"]["frac_of_bound"] == round(41216 / 1e6 / 2e-3, 3)
+    tot = sum(st.values())
+    assert abs(r["all_gemms"]["ms"] - tot) < 1e-9

@@ -385,6 +385,32 @@ def test_mxfp8_layer_fwd_bwd_api(tile_m, empty):
     print("MXFP8 chained errors (rel_frob, max_err/max):", report)
 
 
+def test_mxfp8_dswiglu_identical_across_kernels():
+    """The SwiGLU backward fused into the FC2 dgrad gives the same dH bits on
+    the one-CTA kernel (128-row segments) and on the CTA-pair kernel
+    (256-row segments, two columns per packed f32x2 operation): the row-wise
+    operands of each routed row are the same in both layouts, so every routed
+    row's dgrad accumulator and epilogue inputs are too."""
+    from microscaled_precision_moe_gb300.moe import MXFP8MoE
+    shape = synth.scaled(synth.MOE_30B_BWD, T=384, H=512, I=768, E=8, k=4)
+    ids, prob = synth.routing(shape)
+    x = synth.moe_activations(shape, device="cuda")
+    w1, w2 = synth.moe_weights(shape, device="cuda")
+    dy = synth.moe_grad_out(shape, device="cuda")
+    got = {}
+    for tm in (128, 256):
+        layer = MXFP8MoE(shape.T, shape.H, shape.I, shape.E, shape.k, tile_m=tm)
+        layer.quantize_weights(w1, w2)
+        layer.forward(x, ids.cuda(), prob.cuda())
+        layer.backward(dy)
+        torch.cuda.synchronize()
+        inv = layer.seg[2].long()
+        got[tm] = (layer.c1[inv].cpu(), layer.dh[inv].cpu())
+    assert torch.equal(got[128][0], got[256][0]), "C = gate|up differs between kernels"
+    same = (got[128][1] == got[256][1]).all(dim=1)
+    assert bool(same.all()), f"dH differs on {int((~same).sum())} of {same.numel()} routed rows"
+
+
 def test_mxfp8_fprop_small_m():
     """MXFP8 fprop (bf16 and fp32 out) and the SwiGLU epilogue on the small-M
     kernel: few rows per expert (decode-sized segments)."""
