@@ -286,6 +286,27 @@ def _quantizer_lines(peak_hbm):
                                               "timing": "CUDA graph of 8 launches over 8 rotating "
                                                         "inputs (272 MB > L2), replayed"}
     del g
+    # the same bytes moved by a plain device copy (torch's copy kernel), in
+    # the same eight-launch graph: what a launch of this size reaches when it
+    # does nothing but stream, i.e. the share of the gap that is the fixed
+    # cost of a 15 us launch rather than the quantiser
+    n_el = byts // 4                                      # bf16 in + bf16 out = 4 bytes per element
+    srcs = [torch.empty(n_el, dtype=torch.bfloat16, device="cuda").fill_(1) for _ in range(8)]
+    dsts = [torch.empty_like(t) for t in srcs]
+    gc = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(side):
+        for j in range(8):
+            dsts[j].copy_(srcs[j])
+        torch.cuda.synchronize()
+        with torch.cuda.graph(gc, stream=side):
+            for j in range(8):
+                dsts[j].copy_(srcs[j])
+    torch.cuda.synchronize()
+    ms_c = _time_loop(gc.replay, 10) / 8
+    gbs_c = n_el * 4 / (ms_c * 1e-3) / 1e9
+    out["mxfp8_quantize_8288x2048_rowcol"]["copy_same_bytes"] = {
+        "us": round(ms_c * 1e3, 2), "GB/s": round(gbs_c, 1), "frac_hbm": round(gbs_c / peak_hbm, 3)}
+    del gc, srcs, dsts
     del xs, outs
     # the same quantiser on a large input (65536 x 2048, 256 MB, the size of
     # an MXFP8 layer's permuted activations): streaming efficiency without the
@@ -428,6 +449,28 @@ def _mxfp8_gemm_bounds(T, H, I, E, k, stage_ms, peak_fp8, peak_hbm):
     return out
 
 
+def _nvfp4_gemm_bounds(T, H, I, E, k, stage_ms, peak_fp4, peak_hbm):
+    """FC1 and FC2 of the NVFP4 forward: algorithmic FLOPs over the routed
+    rows M = T k, the fewest HBM bytes each can move (NVFP4 operands as
+    stored: half a byte per element plus one E4M3 scale per 16; D and Y
+    written once in bf16), each floor at the given peaks and the measured
+    time's fraction of the larger floor."""
+    M = T * k
+    q = lambda n: n * (0.5 + 1 / 16)
+    spec = {"fc1": (2 * M * 2 * I * H, q(M * H) + q(E * 2 * I * H) + 2 * M * I),
+            "fc2": (2 * M * H * I, q(M * I) + q(E * H * I) + 2 * M * H)}
+    out = {}
+    for name, (flops, byts) in spec.items():
+        mma = flops / (peak_fp4 * 1e12) * 1e3
+        hbm = byts / (peak_hbm * 1e9) * 1e3
+        ms = stage_ms.get(name)
+        out[name] = {"ms": ms, "flops": int(flops), "hbm_bytes": int(byts),
+                     "tensor_floor_ms": round(mma, 4), "hbm_floor_ms": round(hbm, 4),
+                     "bound": "hbm" if hbm >= mma else "tensor",
+                     "frac_of_bound": round(max(mma, hbm) / ms, 3) if ms else None}
+    return out
+
+
 def _mxfp8_layer_line(peak_fp8, steps=10, peak_hbm=None):
     from microscaled_precision_moe_gb300 import synth
     from microscaled_precision_moe_gb300.moe import MXFP8MoE
@@ -472,7 +515,7 @@ def _mxfp8_layer_line(peak_fp8, steps=10, peak_hbm=None):
     return r
 
 
-def _nvfp4_30b_line(peak_fp4, steps=10):
+def _nvfp4_30b_line(peak_fp4, steps=10, peak_hbm=None):
     from microscaled_precision_moe_gb300 import synth
     from microscaled_precision_moe_gb300.moe import NVFP4MoE, NVFP4Weights
     s = synth.MOE_30B
@@ -486,8 +529,20 @@ def _nvfp4_30b_line(peak_fp4, steps=10):
         L.forward(x, idc, prc, W)
     ms = _time_loop(lambda: L.forward(x, idc, prc, W), steps)
     tf = sum(L.gemm_flops()) / (ms * 1e-3) / 1e12
+    # per-stage times from a second, marked pass
+    ns = len(NVFP4MoE.STAGES) + 1
+    ev = [_events(ns) for _ in range(steps)]
+    torch.cuda.synchronize()
+    for i in range(steps):
+        evi = ev[i]
+        L.forward(x, idc, prc, W, mark=lambda j, evi=evi: evi[j].record())
+    torch.cuda.synchronize()
+    stage = {n: round(float(np.mean([ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(steps)])), 4)
+             for j, n in enumerate(NVFP4MoE.STAGES)}
     r = {"workload": s.name, "ms_per_step": round(ms, 3), "TFLOP/s": round(tf, 1),
-         "frac_fp4_peak": round(tf / peak_fp4, 3)}
+         "frac_fp4_peak": round(tf / peak_fp4, 3), "stage_ms": stage}
+    if peak_hbm:
+        r["gemm_bounds"] = _nvfp4_gemm_bounds(s.T, s.H, s.I, s.E, s.k, stage, peak_fp4, peak_hbm)
     del L, W, x, w1, w2
     torch.cuda.empty_cache()
     return r
@@ -948,6 +1003,8 @@ def main():
             "config": cfg, "parallelism": "replicas" if world > 1 else "single",
             "clocks": clk.summary(), "roofline": roof,
             "stage_ms": {k: round(v, 4) for k, v in stage_ms.items()},
+            "gemm_bounds": _nvfp4_gemm_bounds(shape.T, shape.H, shape.I, shape.E, shape.k,
+                                              stage_ms, peak_fp4, peaks["hbm"]),
             "gpu_launches": NVFP4MoE.LAUNCHES_PER_FORWARD * args.steps,
             "e2e": {"value": round(world * flops / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
                     "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
@@ -966,7 +1023,7 @@ def main():
     if not args.no_also:
         also = {"quantizers": _quantizer_lines(peaks["hbm"])}
         also["mxfp8_layer_fwd_bwd"] = _mxfp8_layer_line(peak_fp8_sus, peak_hbm=peaks["hbm"])
-        also["nvfp4_layer_fwd_30b"] = _nvfp4_30b_line(peak_fp4_sus)
+        also["nvfp4_layer_fwd_30b"] = _nvfp4_30b_line(peak_fp4_sus, peak_hbm=peaks["hbm"])
         also["nvfp4_layer_fwd_fc2_online"] = _nvfp4_online_line(peak_fp4)
         also["nvfp4_layer_bf16_bwd"] = _nvfp4_bf16_bwd_line(peaks["bf16_sus"])
         also["nvfp4_layer_decode"] = _nvfp4_decode_line(peaks["hbm"])

@@ -182,6 +182,13 @@ MPM_DEV void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t b
       "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
       :: "r"(dst), "l"(src), "r"(bytes), "r"(bar) : "memory");
 }
+// Programmatic dependent launch: a kernel launched with programmatic stream
+// serialization may start while the previous kernel in the stream finishes;
+// pdl_wait returns once that kernel has completed and its writes are
+// visible (at once when there is none), and pdl_launch_dependents lets the
+// next such kernel start early.
+MPM_DEV void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+MPM_DEV void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 MPM_DEV void prefetch_tmap(const void* tmap) {
   asm volatile("prefetch.tensormap [%0];" :: "l"(tmap) : "memory");
 }

@@ -413,6 +413,11 @@ __global__ void __launch_bounds__(256) mxfp8_quant_tma_kernel(const __grid_const
   const uint32_t sOut = base + MQ_STAGES * MQ_TILE_BYTES;        // two output buffers
   const uint32_t bar = sOut + 2 * MQ_OUT_BYTES;
   const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
+  // launched as a programmatic dependent: no global access before this wait;
+  // the grid is persistent (every CTA resident), so the next launch may
+  // begin its prologue on the SMs this grid's CTAs leave
+  pdl_wait();
+  pdl_launch_dependents();
   long long M_eff = p.M;
   if (p.m_valid) { const long long mv = *p.m_valid; M_eff = mv < M_eff ? mv : M_eff; }
   const long long n_tiles = (M_eff + MQ_TM - 1) / MQ_TM * n_kt;
@@ -745,8 +750,17 @@ cudaError_t launch_mxfp8_tma(const CUtensorMap& tx, const CUtensorMap& trow, con
   long long grid = dev < 64 ? ctas[dev] : 1;
   if (grid > n_tiles) grid = n_tiles;
   if (grid < 1) grid = 1;
-  mxfp8_quant_tma_kernel<<<(unsigned)grid, 256, smem, st>>>(tx, trow, tcol, p, n_kt);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid, 1, 1);
+  cfg.blockDim = dim3(256, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, mxfp8_quant_tma_kernel, tx, trow, tcol, p, n_kt);
 }
 
 

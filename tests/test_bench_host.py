@@ -118,3 +118,17 @@ def test_mxfp8_gemm_bounds_bytes_and_floors():
     assert r["fc1_wgrad"]["frac_of_bound"] == round(41216 / 1e6 / 2e-3, 3)
     tot = sum(st.values())
     assert abs(r["all_gemms"]["ms"] - tot) < 1e-9
+
+
+def test_nvfp4_gemm_bounds_headline_shape():
+    """The headline layer's FC2 writes Y in bf16 and reads every expert's
+    FP4 W2: at the measured peaks its HBM floor exceeds its FP4 floor, while
+    FC1 stays bound by the tensor cores."""
+    import bench
+    r = bench._nvfp4_gemm_bounds(32768, 7168, 2048, 256, 8, {"fc1": 2.8, "fc2": 1.7},
+                                 peak_fp4=11373.0, peak_hbm=6790.0)
+    M = 32768 * 8
+    assert r["fc2"]["hbm_bytes"] == int(M * 2048 * 0.5625 + 256 * 7168 * 2048 * 0.5625
+                                        + 2 * M * 7168)
+    assert r["fc1"]["bound"] == "tensor" and r["fc2"]["bound"] == "hbm"
+    assert 0.4 < r["fc2"]["frac_of_bound"] < 0.7
