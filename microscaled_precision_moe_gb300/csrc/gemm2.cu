@@ -250,13 +250,6 @@ struct PairMaps {
 template <int KIND>
 constexpr int nthreads() { return 32 * (10 + Cfg<KIND>::kSfWarps); }
 
-// one thread's four 32-bit values into four consecutive TMEM columns of its
-// lane (the warp's lane quarter)
-MPM_DEV void tmem_st_32x32b_x4(uint32_t taddr, const uint4& v) {
-  asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};"
-               :: "r"(taddr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
-}
-MPM_DEV void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 // named barrier over `n` threads that also ORs a predicate across them
 MPM_DEV bool named_sync_or(uint32_t id, uint32_t n, bool pred) {
   uint32_t r;

@@ -56,11 +56,6 @@ struct OnlineMaps {
   CUtensorMap a, b, sfa, sfb, out;
 };
 
-MPM_DEV void tmem_st_32x32b_x4(uint32_t taddr, const uint4& v) {
-  asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};"
-               :: "r"(taddr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
-}
-MPM_DEV void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 MPM_DEV bool named_sync_or(uint32_t id, uint32_t n, bool pred) {
   uint32_t r;
   asm volatile(
