@@ -94,21 +94,26 @@ MPM_DEV uint32_t e2m1x2_scaled(uint32_t w, uint64_t r2) {
   return out;
 }
 
-// One row of the NVFP4 quantisers, by one warp: the row is read once into
-// registers (NB x 32 lanes x 16 elements), then encoded.  amax_mode 0 takes
-// the row's own max, 1 amax_in[row], 2 the group amax `group_bits` (fp32
-// bits); `evict_first` marks the row's last read.
-template <int NB>
-MPM_DEV void nvfp4_quant_row(const Nvfp4Rows& p, long long row, int lane, uint32_t group_bits) {
+// One row of the NVFP4 quantisers, by W lanes of a warp (32: one row per
+// warp; 16: one row per half-warp, for rows of at most 64 blocks): the row
+// is read once into registers (NB x W lanes x 16 elements), then encoded.
+// amax_mode 0 takes the row's own max, 1 amax_in[row], 2 the group amax
+// `group_bits` (fp32 bits).  `sub` is the lane within the row's W lanes; a
+// row that is not `live` reads and writes nothing but still takes part in
+// the warp's shuffles.
+template <int NB, int W>
+MPM_DEV void nvfp4_quant_row(const Nvfp4Rows& p, long long row, int sub, bool live,
+                             uint32_t group_bits) {
+  static_assert(W == 32 || W == 16, "a row takes a warp or a half-warp");
   const int nblk = p.K >> 4;
   const long long cols_pad = nblk;          // K % 64 == 0 -> nblk % 4 == 0
-  const __nv_bfloat16* xr = nvfp4_row_ptr(p, row);
+  const __nv_bfloat16* xr = nvfp4_row_ptr(p, live ? row : 0);
 
   uint4 v[NB][2];
 #pragma unroll
   for (int i = 0; i < NB; ++i) {
-    const int b = i * 32 + lane;
-    if (b < nblk) {
+    const int b = i * W + sub;
+    if (live && b < nblk) {
       const uint4* src = reinterpret_cast<const uint4*>(xr + (long long)b * 16);
       v[i][0] = __ldcs(src);
       v[i][1] = __ldcs(src + 1);
@@ -133,16 +138,18 @@ MPM_DEV void nvfp4_quant_row(const Nvfp4Rows& p, long long row, int lane, uint32
   }
   float a;
   if (p.amax_mode == 0) {
+    // xor offsets below W stay within the row's lanes
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) lmax = max(lmax, __shfl_xor_sync(0xFFFFFFFFu, lmax, o));
+    for (int o = W / 2; o > 0; o >>= 1) lmax = max(lmax, __shfl_xor_sync(0xFFFFFFFFu, lmax, o));
     a = __uint_as_float(lmax << 16);
   } else if (p.amax_mode == 1) {
-    a = p.amax_in[row];
+    a = live ? p.amax_in[row] : 0.0f;
   } else {
     a = __uint_as_float(group_bits);
   }
   const float sg = nvfp4_outer(a);
-  if (lane == 0) {
+  if (!live) return;
+  if (sub == 0) {
     if (p.amax_mode != 2) p.ts[row] = sg;
     else if (row % p.R == 0) p.ts[row / p.R] = sg;
   }
@@ -150,7 +157,7 @@ MPM_DEV void nvfp4_quant_row(const Nvfp4Rows& p, long long row, int lane, uint32
   uint8_t* qr = p.q + row * (long long)(p.K >> 1);
 #pragma unroll
   for (int i = 0; i < NB; ++i) {
-    const int b = i * 32 + lane;
+    const int b = i * W + sub;
     if (b >= nblk) continue;
     uint32_t sb = 0;
     if (sg > 0.0f) {
@@ -192,7 +199,30 @@ __global__ void __launch_bounds__(128) nvfp4_quant_rows_kernel(const Nvfp4Rows p
     }
     return;
   }
-  nvfp4_quant_row<NB>(p, row, lane, p.amax_mode == 2 ? p.group_amax[row / p.R] : 0u);
+  nvfp4_quant_row<NB, 32>(p, row, lane, true, p.amax_mode == 2 ? p.group_amax[row / p.R] : 0u);
+}
+
+// Rows of at most 64 blocks (K <= 1024): two rows per warp, one per
+// half-warp, so every lane holds blocks (one warp per row left a quarter of
+// the lanes idle at K = 768 and kept half as many bytes in flight).
+template <int NB>
+__global__ void __launch_bounds__(128) nvfp4_quant_rows_half_kernel(const Nvfp4Rows p) {
+  const int lane = threadIdx.x & 31, sub = lane & 15;
+  const long long row0 = ((long long)blockIdx.x * 4 + (threadIdx.x >> 5)) * 2;   // the warp's rows
+  const long long row = row0 + (lane >> 4);
+  long long rows_eff = p.rows;
+  if (p.m_valid) {
+    const long long mv = *p.m_valid;
+    rows_eff = mv < rows_eff ? mv : rows_eff;
+  }
+  const int nblk = p.K >> 4;
+  const bool live = row < rows_eff;
+  if (row0 < rows_eff)                      // warp-uniform: both halves shuffle together
+    nvfp4_quant_row<NB, 16>(p, row, sub, live,
+                            (p.amax_mode == 2 && live) ? p.group_amax[row / p.R] : 0u);
+  if (!live && !p.m_valid && row < p.rows_pad) {   // padding rows of the last tile
+    for (int b = sub; b < nblk; b += 16) p.s[sf_offset(row, b, nblk)] = 0;
+  }
 }
 
 // ---------------------------------------------------------------- NVFP4, running amax
@@ -619,8 +649,21 @@ static int nb_for(int nblk) {
 }
 
 static cudaError_t launch_nvfp4_rows(const Nvfp4Rows& p, cudaStream_t st) {
-  const int nb = nb_for(p.K >> 4);
-  const long long warps = p.rows_pad > p.rows ? p.rows_pad : p.rows;
+  const int nblk = p.K >> 4;
+  const long long rows = p.rows_pad > p.rows ? p.rows_pad : p.rows;
+  if (nblk <= 64) {                          // two rows per warp, eight per block
+    const dim3 grid((unsigned)((rows + 7) / 8)), block(128);
+    switch ((nblk + 15) / 16) {
+      case 1: nvfp4_quant_rows_half_kernel<1><<<grid, block, 0, st>>>(p); break;
+      case 2: nvfp4_quant_rows_half_kernel<2><<<grid, block, 0, st>>>(p); break;
+      case 3: nvfp4_quant_rows_half_kernel<3><<<grid, block, 0, st>>>(p); break;
+      case 4: nvfp4_quant_rows_half_kernel<4><<<grid, block, 0, st>>>(p); break;
+      default: return cudaErrorInvalidValue;
+    }
+    return cudaGetLastError();
+  }
+  const int nb = nb_for(nblk);
+  const long long warps = rows;
   const dim3 grid((unsigned)((warps + 3) / 4)), block(128);
   switch (nb) {
     case 1: nvfp4_quant_rows_kernel<1><<<grid, block, 0, st>>>(p); break;

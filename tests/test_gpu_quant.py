@@ -226,6 +226,32 @@ def test_mxfp8_full_and_edge_tiles_mixed(rowwise, colwise):
         assert (got[:, mv:] == 0xA5).all(), "col codes written past m_valid"
 
 
+def test_mxfp8_reads_what_the_previous_kernel_wrote():
+    """The MXFP8 quantiser is launched as a programmatic dependent of the
+    kernel before it in the stream.  Here that kernel is a long matmul whose
+    result is the quantiser's input, and the quantiser's output buffers were
+    read by the kernel before that: with no host synchronisation in
+    between, the codes must still be those of the matmul's result."""
+    ops = _ops()
+    M, K = 2048, 4096
+    a = synth.normal_bf16(8, 1, (M, 4096), "cuda")
+    b = synth.normal_bf16(8, 2, (4096, K), "cuda", std=0.02)
+    x = torch.empty(M, K, dtype=torch.bfloat16, device="cuda")
+    o = ops.mxfp8_quantize(torch.zeros(M, K, dtype=torch.bfloat16, device="cuda"))
+    torch.cuda.synchronize()
+    for _ in range(3):
+        probe = o["row_q"].float().sum() + o["col_q"].float().sum()   # reads the outputs
+        torch.matmul(a, b, out=x)                                        # writes the input
+        ops.mxfp8_quantize(x, out=o)
+    torch.cuda.synchronize()
+    assert probe.item() >= 0
+    xn = np_bf16(x)
+    rq, rs = Q.mxfp8_quantize_rowwise(xn)
+    cq, cs = Q.mxfp8_quantize_colwise(xn)
+    assert_bytes_equal(u8(o["row_q"]), rq, "row codes after a producing matmul")
+    assert_bytes_equal(u8(o["col_q"])[:, :M], cq, "col codes after a producing matmul")
+
+
 def test_quantizers_deterministic():
     x = synth.normal_bf16(6, 80, (512, 2048), "cuda")
     ops = _ops()
