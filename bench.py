@@ -88,7 +88,10 @@ def _max_over_ranks(dist, v: float) -> float:
 # ---------------------------------------------------------------- clocks
 
 class ClockSampler:
-    """nvidia-smi samples (200 ms) during the timed region."""
+    """nvidia-smi samples (every 50 ms) during the timed region.  nvidia-smi
+    takes longer to start than a short timed region lasts, so entering waits
+    (at most 3 s) for its first sample, and the summary keeps only the
+    samples that arrived after that (all of them if none did)."""
     Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -97,15 +100,19 @@ class ClockSampler:
         self.gpu = gpu_index
         self.proc = None
         self.lines = []
+        self.first = 0
+        self._ready = threading.Event()
 
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.Q}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self._t = threading.Thread(target=self._read, daemon=True)
             self._t.start()
+            self._ready.wait(timeout=3.0)
+            self.first = len(self.lines)
         except (OSError, FileNotFoundError):
             self.proc = None
         return self
@@ -113,6 +120,7 @@ class ClockSampler:
     def _read(self):
         for line in self.proc.stdout:
             self.lines.append(line.strip())
+            self._ready.set()
 
     def __exit__(self, *a):
         if self.proc is not None:
@@ -125,7 +133,8 @@ class ClockSampler:
     def summary(self):
         sm, mx, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for l in self.lines:
+        inside = self.lines[self.first:] if len(self.lines) > self.first else self.lines
+        for l in inside:
             f = [x.strip() for x in l.split(",")]
             if len(f) < 9:
                 continue

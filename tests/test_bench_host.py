@@ -35,6 +35,20 @@ def test_clock_summary_reports_rejecting_reasons_and_skips_bad_lines():
     assert s["reasons"] == ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown"]
 
 
+def test_clock_summary_keeps_the_samples_of_the_timed_region():
+    """Samples that arrived before the timed region started (the idle clock
+    while nvidia-smi came up) are left out; with none after, all count."""
+    idle = "0, 345, 2070, 120.0, 0x01, Not Active, Not Active, Not Active, Not Active"
+    busy = "0, 2070, 2070, 1100.0, 0x00, Not Active, Not Active, Not Active, Not Active"
+    c = bench.ClockSampler(0)
+    c.lines = [idle, busy, busy]
+    c.first = 1
+    s = c.summary()
+    assert s["samples"] == 2 and s["sm_mhz"] == 2070.0
+    c.lines, c.first = [idle], 1
+    assert c.summary()["samples"] == 1
+
+
 def test_clock_summary_without_samples():
     s = _summary([])
     assert s["samples"] == 0 and s["sm_mhz"] is None and s["reasons"] == ["unsampled"]
