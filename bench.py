@@ -598,7 +598,36 @@ def _nvfp4_online_line(peak_fp4, steps=10):
     return r
 
 
-def _nvfp4_bf16_bwd_line(peak_bf16, steps=10):
+def _bf16_bwd_gemm_bounds(T, H, I, E, k, stage_ms, peak_bf16, peak_hbm):
+    """The four BF16 GEMMs of the backward, as `_mxfp8_gemm_bounds`: bf16
+    operands read once (dY, D or dH, X, the transposed weights), C = gate|up
+    read by the SwiGLU backward, dH and dX written in bf16, dW1 and dW2 in
+    fp32; algorithmic FLOPs over the routed rows."""
+    M = T * k
+    spec = {
+        "fc2_dgrad": (2 * M * I * H, 2 * M * H + 2 * E * H * I + 2 * M * 2 * I + 2 * M * 2 * I),
+        "fc2_wgrad": (2 * M * H * I, 2 * M * H + 2 * M * I + 4 * E * H * I),
+        "fc1_dgrad": (2 * M * 2 * I * H, 2 * M * 2 * I + 2 * E * 2 * I * H + 2 * M * H),
+        "fc1_wgrad": (2 * M * 2 * I * H, 2 * M * 2 * I + 2 * M * H + 4 * E * 2 * I * H),
+    }
+    out, tot_ms, tot_floor = {}, 0.0, 0.0
+    for name, (flops, byts) in spec.items():
+        mma = flops / (peak_bf16 * 1e12) * 1e3
+        hbm = byts / (peak_hbm * 1e9) * 1e3
+        ms = stage_ms.get(name)
+        out[name] = {"ms": ms, "flops": int(flops), "hbm_bytes": int(byts),
+                     "tensor_floor_ms": round(mma, 4), "hbm_floor_ms": round(hbm, 4),
+                     "bound": "hbm" if hbm >= mma else "tensor",
+                     "frac_of_bound": round(max(mma, hbm) / ms, 3) if ms else None}
+        if ms:
+            tot_ms += ms
+            tot_floor += max(mma, hbm)
+    out["all_gemms"] = {"ms": round(tot_ms, 4), "floor_ms": round(tot_floor, 4),
+                        "frac_of_bound": round(tot_floor / tot_ms, 3) if tot_ms else None}
+    return out
+
+
+def _nvfp4_bf16_bwd_line(peak_bf16, steps=10, peak_hbm=None):
     """BF16 backward of the NVFP4 layer (30B-shaped, 8192 tokens), both
     operand modes: the backward alone is timed (the forward that saves
     gate|up runs once before); the transposed weight copies are prepared once
@@ -641,6 +670,9 @@ def _nvfp4_bf16_bwd_line(peak_bf16, steps=10):
                    "frac_bf16_peak": round(tf / peak_bf16, 3), "stage_ms": stage,
                    "prepare_weights_ms": round(prep_ms, 3),
                    "gpu_launches_per_step": NVFP4MoE.LAUNCHES_PER_BACKWARD[mode]}
+        if peak_hbm:
+            r[mode]["gemm_bounds"] = _bf16_bwd_gemm_bounds(s.T, s.H, s.I, s.E, s.k, stage,
+                                                           peak_bf16, peak_hbm)
     del L, W
     torch.cuda.empty_cache()
     # the same modes after an MXFP8 forward
@@ -869,7 +901,7 @@ def main():
                               "config": {"workload": r["workload"]}, "decode": r}), flush=True)
         return 0
     if args.case == "bf16bwd":
-        r = _nvfp4_bf16_bwd_line(peaks["bf16_sus"], steps=args.steps)
+        r = _nvfp4_bf16_bwd_line(peaks["bf16_sus"], steps=args.steps, peak_hbm=peaks["hbm"])
         if rank == 0:
             print(json.dumps({"metric": METRIC, "value": r["dequantized"]["TFLOP/s"],
                               "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
@@ -1034,7 +1066,7 @@ def main():
         also["mxfp8_layer_fwd_bwd"] = _mxfp8_layer_line(peak_fp8_sus, peak_hbm=peaks["hbm"])
         also["nvfp4_layer_fwd_30b"] = _nvfp4_30b_line(peak_fp4_sus, peak_hbm=peaks["hbm"])
         also["nvfp4_layer_fwd_fc2_online"] = _nvfp4_online_line(peak_fp4)
-        also["nvfp4_layer_bf16_bwd"] = _nvfp4_bf16_bwd_line(peaks["bf16_sus"])
+        also["nvfp4_layer_bf16_bwd"] = _nvfp4_bf16_bwd_line(peaks["bf16_sus"], peak_hbm=peaks["hbm"])
         also["nvfp4_layer_decode"] = _nvfp4_decode_line(peaks["hbm"])
         try:
             also["nvfp4_single_expert"] = _single_expert_line(peak_fp4_sus, peaks["hbm"])

@@ -146,3 +146,17 @@ def test_nvfp4_gemm_bounds_headline_shape():
                                         + 2 * M * 7168)
     assert r["fc1"]["bound"] == "tensor" and r["fc2"]["bound"] == "hbm"
     assert 0.4 < r["fc2"]["frac_of_bound"] < 0.7
+
+
+def test_bf16_backward_gemm_bounds_bytes():
+    """Hand-counted case: 64 routed rows, H 64, I 32, 2 experts, bf16
+    operands and outputs, fp32 weight gradients."""
+    import bench
+    st = {"fc2_dgrad": 1e-3, "fc2_wgrad": 1e-3, "fc1_dgrad": 1e-3, "fc1_wgrad": 1e-3}
+    r = bench._bf16_bwd_gemm_bounds(32, 64, 32, 2, 2, st, peak_bf16=1.0, peak_hbm=1.0)
+    # FC2 dgrad: dY 64 x 64, W2 2 x 64 x 32, C 64 x 64 read, dH 64 x 64 written (bf16)
+    assert r["fc2_dgrad"]["hbm_bytes"] == 8192 + 8192 + 8192 + 8192
+    # FC1 wgrad: dH 64 x 64 and X 64 x 64 (bf16), dW1 2 x 64 x 64 fp32
+    assert r["fc1_wgrad"]["hbm_bytes"] == 8192 + 8192 + 32768
+    assert r["fc1_dgrad"]["flops"] == 2 * 64 * 64 * 64
+    assert abs(r["all_gemms"]["ms"] - 4e-3) < 1e-12
