@@ -304,6 +304,25 @@ grouped_gemm_small_kernel(const __grid_constant__ SmallMaps maps, const GemmArgs
           const float a_lane = p.alpha_a ? __fmul_rn(p.alpha_a[rl], ab_e) : ab_e;
           const float p_lane = p.row_prob[rl];
           tmem_ld_wait();
+          // A block whose gate and up accumulators are all +-0 (the padding
+          // rows of a segment, whose operand rows are zero) gives D = +-0
+          // exactly: silu(+-0) = +-0, and the products keep the xor of the
+          // operands' signs.  Those 32 rows are written from the sign bits
+          // alone and add nothing to the row max (decode batches: most of
+          // a 128-row chunk), so the accumulator is held for less time.
+          uint32_t nz = 0;
+#pragma unroll
+          for (int c = 0; c < 32; ++c) nz |= (g[c] | u[c]) & 0x7FFFFFFFu;
+          if (!__any_sync(0xffffffffu, nz != 0)) {
+#pragma unroll
+            for (int c = 0; c < 32; ++c) {
+              const long long row = r0 + cb * 32 + c;
+              const uint32_t sp = __float_as_uint(__shfl_sync(0xffffffffu, p_lane, c));
+              const uint32_t sgn = (g[c] ^ u[c] ^ sp) & 0x80000000u;   // alpha's sign cancels
+              reinterpret_cast<uint16_t*>(p.out2)[row * p.ldo2 + f] = (uint16_t)(sgn >> 16);
+            }
+            continue;
+          }
 #pragma unroll
           for (int c = 0; c < 32; ++c) {
             const long long row = r0 + cb * 32 + c;
