@@ -102,6 +102,10 @@ size_t mpm_scale_bytes(int64_t rows, int64_t cols);
  * used row count is known only on the device).
  * Requirements: M >= 1, K >= 32, K % 32 == 0, ldx >= K, ldx % 8 == 0,
  * x_dev 16-byte aligned, ldc % 16 == 0, all output pointers 16-byte aligned.
+ * The kernel is launched with programmatic stream serialization: it may
+ * start while the previous kernel on the stream finishes, and it touches
+ * global memory only after that kernel has completed (stream order holds
+ * for the caller as for any other launch).
  */
 mpm_status mpm_mxfp8_quantize(const void* x_dev, int64_t M, int64_t K, int64_t ldx,
                               unsigned flags,

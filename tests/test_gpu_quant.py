@@ -46,7 +46,8 @@ def test_nvfp4_single_expert_activation():
     _check_nvfp4(x)
 
 
-@pytest.mark.parametrize("M,K", [(1, 64), (5, 128), (129, 768), (300, 2048), (77, 7168), (64, 8192)])
+@pytest.mark.parametrize("M,K", [(1, 64), (5, 128), (6, 320), (129, 768), (33, 1024), (2, 1088),
+                                 (300, 2048), (77, 7168), (64, 8192)])
 def test_nvfp4_shapes(M, K):
     x = synth.normal_bf16(3, 50 + K, (M, K), "cuda", std=2.0, outlier_p=0.01, outlier_mul=100.0)
     _check_nvfp4(x)
