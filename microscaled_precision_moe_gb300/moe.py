@@ -148,12 +148,17 @@ class NVFP4MoE:
     STAGES = ("quant_x", "segments", "gather", "fc1", "quant_d", "fc2", "combine")
 
     def forward(self, x, topk_ids, topk_prob, w: NVFP4Weights, mark=None,
-                save_for_backward=False, out=None):
+                save_for_backward=False, out=None, out_chunks=1, on_chunk=None):
         """out [T, H] bf16 (the layer's own buffer, or ``out`` when given).
         ``mark(i)`` (optional) is called before stage i of STAGES and once
         more at the end (used to record CUDA events).  save_for_backward: the
         FC1 epilogue also stores C = gate|up (bf16, [capacity, 2I]) for the
-        SwiGLU backward."""
+        SwiGLU backward.  out_chunks > 1 combines the output in that many
+        contiguous token ranges, and ``on_chunk(j, t0, t1)`` (optional) is
+        called right after range j = [t0, t1) is launched on the current
+        stream, so a caller can record an event there and start copying
+        those rows out while the later ranges are combined.  The result is
+        the same bytes: each token's combine is independent of the others."""
         T, H, I, E, k, cap = self.T, self.H, self.I, self.E, self.k, self.cap
         mark = mark or (lambda i: None)
         mark(0)
@@ -192,7 +197,12 @@ class NVFP4MoE:
                                  tile_m=self.tile_m)
         mark(6)
         dst = self.out if out is None else out
-        ops.moe_combine(self.y, inv, T, k, out=dst)
+        n = max(1, min(int(out_chunks), T))
+        for j in range(n):
+            t0, t1 = j * T // n, (j + 1) * T // n
+            ops.moe_combine(self.y, inv[t0 * k:t1 * k], t1 - t0, k, out=dst[t0:t1])
+            if on_chunk is not None:
+                on_chunk(j, t0, t1)
         mark(7)
         return dst
 

@@ -290,6 +290,29 @@ def test_nvfp4_layer_api(tile_m):
     _chained_compare(np_bf16(layer.d), np_bf16(layer.y), np_bf16(out), r, shape.k, "NVFP4MoE")
 
 
+def test_nvfp4_layer_chunked_output():
+    """forward(out_chunks=n, on_chunk=...) combines the output in n token
+    ranges that tile [0, T) in order, each announced right after its launch,
+    and gives the same bytes as one combine (T = 509 does not divide)."""
+    from microscaled_precision_moe_gb300.moe import NVFP4MoE, NVFP4Weights
+    shape = synth.scaled(synth.MOE_30B, T=509, H=1024, I=256, E=16)
+    ids, prob = synth.routing(shape)
+    x = synth.moe_activations(shape, device="cuda")
+    w1, w2 = synth.moe_weights(shape, device="cuda")
+    layer = NVFP4MoE(shape.T, shape.H, shape.I, shape.E, shape.k)
+    w = NVFP4Weights.quantize(w1, w2)
+    ref = layer.forward(x, ids.cuda(), prob.cuda(), w).clone()
+    ranges = []
+    out = torch.full_like(ref, float("nan"))
+    layer.forward(x, ids.cuda(), prob.cuda(), w, out=out, out_chunks=5,
+                  on_chunk=lambda j, t0, t1: ranges.append((j, t0, t1)))
+    torch.cuda.synchronize()
+    assert [r[0] for r in ranges] == list(range(5))
+    assert ranges[0][1] == 0 and ranges[-1][2] == shape.T
+    assert all(ranges[i][2] == ranges[i + 1][1] for i in range(4))
+    assert torch.equal(out.view(torch.int16), ref.view(torch.int16))
+
+
 @pytest.mark.parametrize("tile_m", [128, 256])
 def test_mxfp8_grouped_fprop_dgrad_wgrad(tile_m):
     shape = synth.scaled(synth.MOE_30B_BWD, T=256, H=256, I=256, E=4, k=2)
