@@ -961,7 +961,7 @@ def main():
     r_pad = int(layer.seg[0][shape.E].item())
     nv_row = lambda n: n // 2 + n // 16 + 4
     stage_bytes = {
-        "gather": R * nv_row(shape.H) + r_pad * (nv_row(shape.H) + 4 + 4),
+        "quant_x": shape.T * shape.H * 2 + r_pad * (nv_row(shape.H) + 4) + r_pad * 4 + R * 4,
         "quant_d": r_pad * (shape.I * 2 + 4) + r_pad * nv_row(shape.I),
         "combine": R * shape.H * 2 + R * 4 + shape.T * shape.H * 2}
 
@@ -1086,8 +1086,6 @@ def main():
         except Exception as exc:       # a secondary line never costs the main one
             also["nvfp4_single_expert"] = {"error": f"{type(exc).__name__}: {exc}"}
         also["stage_GBps_or_TFLOPs"] = {
-            "quant_x_GB/s": round((shape.T * shape.H * 2.5625 + shape.T * 4) /
-                                  (stage_ms["quant_x"] * 1e-3) / 1e9, 1),
             "fc1_TFLOP/s": round(ach, 1),
             "fc2_TFLOP/s": round(fl2 / (stage_ms["fc2"] * 1e-3) / 1e12, 1)}
         for name, nb in stage_bytes.items():
@@ -1096,9 +1094,9 @@ def main():
             also["stage_GBps_or_TFLOPs"][f"{name}_frac_hbm"] = round(gbs / peaks["hbm"], 3)
         also["stage_GBps_or_TFLOPs"]["bytes"] = {
             **stage_bytes, "rows": R, "padded_rows": r_pad,
-            "counted": "gather: the routed rows' NVFP4 codes, scales and token scales and "
-                       "every padded row's index read, every padded row written with its "
-                       "zeroed amax slot; "
+            "counted": "quant_x: the bf16 tokens read once, every padded row written "
+                       "(NVFP4 codes, scales, token scale, zeroed amax slot), the row and slot "
+                       "maps read; "
                        "quant_d: bf16 D and the amax read, NVFP4 D written (padded rows); "
                        "combine: the routed rows of Y and the inverse map read, the output "
                        "written"}

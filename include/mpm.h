@@ -285,6 +285,42 @@ mpm_status mpm_moe_gather(int what, const void* src_dev, const uint8_t* src_s_de
                           float* amax_zero_dev, cudaStream_t stream);
 
 /*
+ * Per-token NVFP4 quantisation of x_dev (bf16 [T, K], leading dimension ldx
+ * elements) written straight into the expert-ordered rows: the same bytes as
+ * mpm_nvfp4_quantize_per_token of x followed by mpm_moe_gather
+ * (MPM_GATHER_NVFP4) with the same segments, without the token-ordered copy.
+ * Row r < seg_offsets[E] with perm[r] >= 0 gets the codes, block scales and
+ * outer scale of token perm[r] / k; a padding row (perm[r] < 0) gets zeros;
+ * amax_zero_dev[r] (nullable) is set to 0 for every such row; rows at or
+ * beyond seg_offsets[E] are not written.
+ * Sources: "Towards Blackwell-native 8-bit and 4-bit RL", section
+ * "Per-token activation scaling" (one scale per token, so a token's bytes do
+ * not depend on where its rows go), and "miniTE technical report", section
+ * 5.3 (dispatch/permute ahead of the FC1 quantised GEMM, the activation and
+ * its amax padded together).
+ * Layouts: q_dev u8 [capacity, K/2]; s_dev 128x4 tiles of [capacity, K/16]
+ * (mpm_scale_bytes(capacity, K/16)); ts_dev fp32 [capacity]; inv_perm_dev
+ * int32 [T*k] and perm_dev int32 [capacity] as written by
+ * mpm_moe_build_segments.  A row index outside [0, seg_offsets[E]) in
+ * inv_perm sets MPM_ERR_DEVICE_BOUNDS and that write is dropped.
+ * Two launches: the codes go to the routed rows while each token's block
+ * scales and outer scale go to ws_dev (token order); the second writes the
+ * scale tiles, outer scales, amax slots and padding rows from it.  ws_dev:
+ * caller-owned, at least mpm_nvfp4_quantize_scatter_workspace_bytes(T, K)
+ * bytes, 4-byte aligned; its contents need no initialisation.
+ * Requirements: T >= 1, 64 <= K <= 8192, K % 64 == 0, ldx >= K, ldx % 8 == 0,
+ * 1 <= k <= 64, E >= 1, capacity >= 1; x_dev and q_dev 16-byte aligned,
+ * s_dev, ts_dev and amax_zero_dev 4-byte aligned.
+ */
+size_t mpm_nvfp4_quantize_scatter_workspace_bytes(int64_t T, int64_t K);
+mpm_status mpm_nvfp4_quantize_scatter(const void* x_dev, int64_t T, int64_t K, int64_t ldx,
+                                      const int32_t* inv_perm_dev, int k,
+                                      const int32_t* perm_dev, const int32_t* seg_offsets_dev,
+                                      int64_t E, int64_t capacity, uint8_t* q_dev,
+                                      uint8_t* s_dev, float* ts_dev, float* amax_zero_dev,
+                                      void* ws_dev, size_t ws_bytes, cudaStream_t stream);
+
+/*
  * out[t] = sum over j = 0..k-1 (in that order, fp32) of y_perm[inv_perm[t*k+j]],
  * rounded once to bf16.  y_perm bf16 [capacity, H]; out bf16 [T, H].
  * Source: "miniTE technical report", section 5.3 (expert outputs, weighted by

@@ -66,6 +66,9 @@ _SIGS = {
     "mpm_moe_gather": (_int, [_int, _vp, _vp, _vp, _i64, _i64, _int, _vp, _vp, _i64, _i64,
                               _vp, _vp, _vp, _vp, _vp]),
     "mpm_moe_combine": (_int, [_vp, _vp, _i64, _int, _i64, _vp, _vp]),
+    "mpm_nvfp4_quantize_scatter_workspace_bytes": (C.c_size_t, [_i64, _i64]),
+    "mpm_nvfp4_quantize_scatter": (_int, [_vp, _i64, _i64, _i64, _vp, _int, _vp, _vp, _i64,
+                                          _i64, _vp, _vp, _vp, _vp, _vp, C.c_size_t, _vp]),
     "mpm_nvfp4_dequantize": (_int, [_vp, _vp, _vp, _i64, _i64, _i64, _vp, _i64, _vp, _vp]),
     "mpm_mxfp8_dequantize": (_int, [_vp, _vp, _i64, _i64, _vp, _i64, _vp, _vp]),
     "mpm_transpose_bf16": (_int, [_vp, _i64, _i64, _i64, _vp, _i64, _vp, _vp]),

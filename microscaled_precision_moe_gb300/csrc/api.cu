@@ -292,6 +292,31 @@ mpm_status mpm_moe_gather(int what, const void* src, const uint8_t* src_s, const
                                         dst, dst_s, dst_ts, amax_zero, stream));
 }
 
+size_t mpm_nvfp4_quantize_scatter_workspace_bytes(int64_t T, int64_t K) {
+  if (T < 1 || K < 64 || K % 64 != 0 || K > 8192) return 0;
+  return mpm::nvfp4_scatter_ws_bytes(T, (int)K);
+}
+
+mpm_status mpm_nvfp4_quantize_scatter(const void* x, int64_t T, int64_t K, int64_t ldx,
+                                      const int32_t* inv, int k, const int32_t* perm,
+                                      const int32_t* seg, int64_t E, int64_t capacity,
+                                      uint8_t* q, uint8_t* s, float* ts, float* amax_zero,
+                                      void* ws, size_t ws_bytes, cudaStream_t stream) {
+  if (!x || !inv || !perm || !seg || !q || !s || !ts || !ws) return MPM_ERR_NULL;
+  if (T < 1 || K < 64 || K % 64 != 0 || K > 8192 || ldx < K || k < 1 || k > 64 || E < 1 ||
+      capacity < 1)
+    return MPM_ERR_SHAPE;
+  if (T > (1ll << 31) - 256 || T * k > (1ll << 30)) return MPM_ERR_SHAPE;
+  if (!aligned(x, 16) || ldx % 8 != 0 || !aligned(q, 16) || !aligned(s, 4) || !aligned(ts, 4))
+    return MPM_ERR_ALIGN;
+  if (amax_zero && !aligned(amax_zero, 4)) return MPM_ERR_ALIGN;
+  if (ws_bytes < mpm::nvfp4_scatter_ws_bytes(T, (int)K)) return MPM_ERR_SHAPE;
+  if (!aligned(ws, 4)) return MPM_ERR_ALIGN;
+  return cuda_status(mpm::launch_nvfp4_quantize_scatter(x, T, (int)K, ldx, inv, k, perm, seg + E,
+                                                        capacity, q, s, ts, amax_zero, ws,
+                                                        status_ptr(), stream));
+}
+
 mpm_status mpm_moe_combine(const void* y, const int32_t* inv, int64_t T, int k, int64_t H,
                            void* out, cudaStream_t stream) {
   if (!y || !inv || !out) return MPM_ERR_NULL;

@@ -14,6 +14,15 @@ cudaError_t launch_nvfp4_weight(const void* const* parts, const long long* part_
 // == 0): codes, tiled block scales and one outer scale per (row, tile)
 cudaError_t launch_nvfp4_online(const void* x, long long M, int K, long long ldx, uint8_t* q,
                                 uint8_t* s, float* gs, const int* m_valid, cudaStream_t st);
+// per-token NVFP4 of x [T, K] written into the expert-ordered rows (codes,
+// tiled scales, outer scales; padding rows below *seg_end zeroed); ws holds
+// nvfp4_scatter_ws_bytes(T, K) bytes (4-byte aligned)
+size_t nvfp4_scatter_ws_bytes(long long T, int K);
+cudaError_t launch_nvfp4_quantize_scatter(const void* x, long long T, int K, long long ldx,
+                                          const int* inv, int k, const int* perm,
+                                          const int* seg_end, long long cap, uint8_t* q,
+                                          uint8_t* s, float* ts, float* amax_zero, void* ws,
+                                          int* status, cudaStream_t st);
 // x is read through a 2-D bf16 tensor map (box 64 columns x 128 rows); the
 // codes of full tiles are stored through trow (row_q, box 64 x 128 bytes)
 // and tcol (col_q, box 128 x 64 bytes, 128-byte swizzle)

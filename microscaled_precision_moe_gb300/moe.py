@@ -131,11 +131,11 @@ class NVFP4MoE:
         self.cap = cap
         u8, f32, bf = torch.uint8, torch.float32, torch.bfloat16
         e = lambda *s, dtype: torch.empty(*s, dtype=dtype, device=dev)
-        self.xq = (e(T, H // 2, dtype=u8), e(_sb(T, H // 16), dtype=u8), e(T, dtype=f32))
         self.seg = (e(E + 1, dtype=torch.int32), e(cap, dtype=torch.int32),
                     e(T * k, dtype=torch.int32), e(cap, dtype=f32))
         self.seg_ws = e(int(L.load().mpm_moe_segments_workspace_bytes(T, k, E)), dtype=u8)
         self.aq = (e(cap, H // 2, dtype=u8), e(_sb(cap, H // 16), dtype=u8), e(cap, dtype=f32))
+        self.xq_ws = e(ops.nvfp4_quantize_scatter_workspace_bytes(T, H), dtype=u8)
         self.d = e(cap, I, dtype=bf)
         self.amax = e(cap, dtype=f32)
         # two-pass: one outer scale per row; online: one per (row, 256-column tile)
@@ -145,7 +145,8 @@ class NVFP4MoE:
         self.out = e(T, H, dtype=bf)
 
     # each call below is one or more library launches on the current stream
-    STAGES = ("quant_x", "segments", "gather", "fc1", "quant_d", "fc2", "combine")
+    # (quant_x: each token quantised once, straight into its k routed rows)
+    STAGES = ("segments", "quant_x", "fc1", "quant_d", "fc2", "combine")
 
     def forward(self, x, topk_ids, topk_prob, w: NVFP4Weights, mark=None,
                 save_for_backward=False, out=None, out_chunks=1, on_chunk=None):
@@ -162,15 +163,14 @@ class NVFP4MoE:
         T, H, I, E, k, cap = self.T, self.H, self.I, self.E, self.k, self.cap
         mark = mark or (lambda i: None)
         mark(0)
-        ops.nvfp4_quantize_per_token(x, out=self.xq)
         seg, perm, inv, rp = self.seg
-        mark(1)
         ops.moe_build_segments(topk_ids, topk_prob, E, out=self.seg, ws=self.seg_ws,
                                pad=self.pad)
-        mark(2)
-        ops.moe_gather_nvfp4(*self.xq, H, perm, seg, E, k, cap, out=self.aq, amax_zero=self.amax)
+        mark(1)
+        ops.nvfp4_quantize_scatter(x, inv, perm, seg, E, k, cap, out=self.aq, amax_zero=self.amax,
+                                   ws=self.xq_ws)
         aq, as_, ats = self.aq
-        mark(3)
+        mark(2)
         if save_for_backward:
             self._alloc_backward()
         epi, c_out = (L.EPI_SWIGLU_SAVE, self.c1) if save_for_backward else (L.EPI_SWIGLU, self.d)
@@ -178,13 +178,13 @@ class NVFP4MoE:
                              aq, w.w1_q.view(E * 2 * I, H // 2), as_, H // 16, w.w1_s, H // 16,
                              c_out, b_rows_per_expert=2 * I, alpha_a=ats, alpha_b=w.w1_ts,
                              row_prob=rp, out2=self.d, amax=self.amax, tile_m=self.tile_m)
-        mark(4)
+        mark(3)
         if self.fc2 == "online":
             ops.nvfp4_quantize_online(self.d, m_valid=seg[E:], out=self.dq)
         else:
             ops.nvfp4_quantize_per_token(self.d, amax_in=self.amax, m_valid=seg[E:], out=self.dq)
         dq, ds, dts = self.dq
-        mark(5)
+        mark(4)
         if self.fc2 == "online":
             ops.moe_grouped_gemm(L.KIND_NVFP4, L.GROUP_M, L.EPI_BF16_ONLINE, E, cap, H, I, seg,
                                  dq, w.w2_q.view(E * H, I // 2), ds, I // 16, w.w2_s, I // 16,
@@ -195,7 +195,7 @@ class NVFP4MoE:
                                  dq, w.w2_q.view(E * H, I // 2), ds, I // 16, w.w2_s, I // 16,
                                  self.y, b_rows_per_expert=H, alpha_a=dts, alpha_b=w.w2_ts,
                                  tile_m=self.tile_m)
-        mark(6)
+        mark(5)
         dst = self.out if out is None else out
         n = max(1, min(int(out_chunks), T))
         for j in range(n):
@@ -203,12 +203,12 @@ class NVFP4MoE:
             ops.moe_combine(self.y, inv[t0 * k:t1 * k], t1 - t0, k, out=dst[t0:t1])
             if on_chunk is not None:
                 on_chunk(j, t0, t1)
-        mark(7)
+        mark(6)
         return dst
 
-    # kernels launched by one forward: quantiser, the segment build (one
-    # cooperative kernel, after an 8-byte memset of its barrier words),
-    # gather, FC1, quantiser, FC2, combine
+    # kernels launched by one forward: the segment build (one cooperative
+    # kernel, after an 8-byte memset of its barrier words), the quantiser into
+    # the routed rows (two kernels), FC1, the quantiser of D, FC2, combine
     LAUNCHES_PER_FORWARD = 7
 
     # ------------------------------------------------------------ BF16 backward

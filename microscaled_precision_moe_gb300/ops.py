@@ -236,6 +236,45 @@ def moe_gather_bf16(x, perm, seg, E: int, k: int, cap: int, out=None, amax_zero=
     return out
 
 
+def nvfp4_quantize_scatter_workspace_bytes(T: int, K: int) -> int:
+    return int(L.load().mpm_nvfp4_quantize_scatter_workspace_bytes(T, K))
+
+
+def nvfp4_quantize_scatter(x, inv_perm, perm, seg, E: int, k: int, cap: int, out=None,
+                           amax_zero=None, ws=None):
+    """Per-token NVFP4 of bf16 x [T, K] written straight into the permuted
+    layout of cap rows: (codes [cap, K/2], tiled scales, token scales [cap]),
+    the bytes nvfp4_quantize_per_token followed by moe_gather_nvfp4 give.
+    ws: uint8 workspace of nvfp4_quantize_scatter_workspace_bytes(T, K)."""
+    lib = L.load()
+    _check_rows(x, "x")
+    T, K = x.shape
+    need = nvfp4_quantize_scatter_workspace_bytes(T, K)
+    if ws is None:
+        ws = torch.empty(need, dtype=torch.uint8, device=x.device)
+    _check(ws, "ws", torch.uint8, min_numel=need)
+    _check(inv_perm, "inv_perm", torch.int32, min_numel=T * k)
+    _check_route(perm, seg, E, cap)
+    dev = x.device
+    if out is None:
+        out = (torch.empty(cap, K // 2, dtype=torch.uint8, device=dev),
+               torch.empty(scale_bytes(cap, K // 16), dtype=torch.uint8, device=dev),
+               torch.empty(cap, dtype=torch.float32, device=dev))
+    dq, ds, dts = out
+    _check(dq, "out codes", torch.uint8, contiguous=True, min_numel=cap * (K // 2))
+    _check(ds, "out scales", torch.uint8, min_numel=scale_bytes(cap, K // 16))
+    _check(dts, "out token scales", torch.float32, min_numel=cap)
+    if amax_zero is not None:
+        _check(amax_zero, "amax_zero", torch.float32, min_numel=cap)
+    _need_cuda(x, inv_perm, perm, seg, dq, ds, dts, amax_zero, ws)
+    st = lib.mpm_nvfp4_quantize_scatter(_ptr(x), T, K, x.stride(0), _ptr(inv_perm), k,
+                                        _ptr(perm), _ptr(seg), E, cap, _ptr(dq), _ptr(ds),
+                                        _ptr(dts), _ptr(amax_zero), _ptr(ws), ws.numel(),
+                                        _stream(dev))
+    L.check(st, "mpm_nvfp4_quantize_scatter")
+    return dq, ds, dts
+
+
 def moe_gather_nvfp4(q, s, ts, K: int, perm, seg, E: int, k: int, cap: int, out=None,
                      amax_zero=None):
     """Per-token NVFP4 rows (codes [T, K/2], tiled scales, token scales [T])

@@ -358,3 +358,27 @@ def test_binding_checks_gemm_and_dequantize_arguments(lib):
         ops.nvfp4_quantize_per_token(torch.zeros(8, 64, dtype=bf), amax_in=torch.zeros(8, dtype=bf))
     with pytest.raises(ValueError, match="CUDA"):
         ops.mxfp8_dequantize(torch.zeros(8, 64, dtype=u8), torch.zeros(ops.scale_bytes(8, 2), dtype=u8))
+
+
+def test_quantize_scatter_validation(lib):
+    """mpm_nvfp4_quantize_scatter rejects bad arguments on the host."""
+    fake = C.c_void_p(0x10000)
+    odd = C.c_void_p(0x10008)
+    odd4 = C.c_void_p(0x10002)
+    f = lib.mpm_nvfp4_quantize_scatter
+    assert lib.mpm_nvfp4_quantize_scatter_workspace_bytes(4, 64) == 4 * 4 + 4 * 4 + 16
+    assert lib.mpm_nvfp4_quantize_scatter_workspace_bytes(4, 96) == 0
+    ok = dict(x=fake, T=4, K=64, ldx=64, inv=fake, k=2, perm=fake, seg=fake, E=2, cap=256,
+              q=fake, s=fake, ts=fake, amax=None, ws=fake, wsb=48)
+
+    def call(**kw):
+        a = dict(ok, **kw)
+        return f(a["x"], a["T"], a["K"], a["ldx"], a["inv"], a["k"], a["perm"], a["seg"], a["E"],
+                 a["cap"], a["q"], a["s"], a["ts"], a["amax"], a["ws"], a["wsb"], None)
+    assert call(x=None) == 1 and call(inv=None) == 1 and call(ts=None) == 1 and call(ws=None) == 1
+    assert call(wsb=47) == 2 and call(ws=odd4) == 3
+    assert call(K=96) == 2 and call(K=16384, ldx=16384) == 2 and call(ldx=32) == 2
+    assert call(k=0) == 2 and call(k=65) == 2 and call(T=0) == 2 and call(cap=0) == 2
+    assert call(E=0) == 2
+    assert call(x=odd) == 3 and call(q=odd) == 3 and call(ldx=68) == 3
+    assert call(s=odd4) == 3 and call(amax=odd4) == 3

@@ -102,11 +102,11 @@ def test_summary_of_a_line():
     line = {"roofline": {"frac": 0.5},
             "also": {"quantizers": {"mxfp8_quantize_8288x2048_rowcol": {"frac_hbm": 0.6}},
                      "mxfp8_layer_fwd_bwd": {"ms_per_step": 2.5, "gemm_TFLOP/s": 1900.0},
-                     "stage_GBps_or_TFLOPs": {"fc2_TFLOP/s": 5000.0, "gather_frac_hbm": 0.95}}}
+                     "stage_GBps_or_TFLOPs": {"fc2_TFLOP/s": 5000.0, "quant_x_frac_hbm": 0.95}}}
     s = bench._summary(line, peaks)
     assert s["fc1_frac_fp4"] == 0.5 and s["fc2_TFLOP/s"] == 5000.0
     assert s["mxfp8_gemm_frac_fp8_burst"] == 0.5
-    assert s["stage_frac_hbm"] == {"gather": 0.95}
+    assert s["stage_frac_hbm"] == {"quant_x": 0.95}
     assert s["nvfp4_30b_ms"] is None and s["nvfp4_30b_frac_fp4_burst"] is None
     assert bench._summary({"roofline": {"frac": 0.1}}, peaks)["decode_ms"] == {}
 

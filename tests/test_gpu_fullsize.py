@@ -117,14 +117,17 @@ def _run_nvfp4_full(shape, n_experts, x_rows_checked, tile_m=256):
     R = int(seg[-1])
     assert_bytes_equal(perm_g[:R], perm, "perm")
     assert_bytes_equal(inv_g, inv, "inv_perm")
-    # per-token quantisation of sampled rows
+    # per-token quantisation of sampled tokens, read at each token's first
+    # routed row (the quantiser writes straight into the routed rows)
     rows = np.random.default_rng(1).choice(T, x_rows_checked, replace=False)
     xr = np_bf16(x[torch.from_numpy(rows).cuda()])
     rq, rs, rts = Q.nvfp4_quantize_per_token(xr)
-    qx, sx, tsx = layer.xq
-    assert_bytes_equal(u8(qx)[rows], rq, "X codes (sampled rows)")
-    assert_bytes_equal(Q.unswizzle_scales(u8(sx), T, H // 16)[rows], rs, "X scales (sampled rows)")
-    assert_bytes_equal(tsx.cpu().numpy()[rows].view(np.uint32), rts.view(np.uint32), "X token scales")
+    qx, sx, tsx = layer.aq
+    dst = inv_g[rows * k]
+    cap = qx.shape[0]
+    assert_bytes_equal(u8(qx)[dst], rq, "X codes (sampled tokens)")
+    assert_bytes_equal(Q.unswizzle_scales(u8(sx), cap, H // 16)[dst], rs, "X scales (sampled tokens)")
+    assert_bytes_equal(tsx.cpu().numpy()[dst].view(np.uint32), rts.view(np.uint32), "X token scales")
     # combine on the whole output: the oracle's combine of the kernel's own Y
     # rows, bit for bit
     oracle_combine_check(out, layer.y, inv_g, T, k, "combine")

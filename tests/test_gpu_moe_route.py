@@ -74,6 +74,67 @@ def test_segments_bad_id_sets_device_status():
     assert ops.get_device_status() == 0          # reset by the read
 
 
+@pytest.mark.parametrize("pad", [128, 256])
+@pytest.mark.parametrize("T,H,E,k,strided", [(700, 512, 12, 4, False), (300, 7168, 16, 8, True)])
+def test_nvfp4_quantize_scatter_equals_quantize_then_gather(T, H, E, k, strided, pad):
+    """The fused quantiser writes the routed rows exactly as the per-token
+    quantiser followed by the NVFP4 gather: every byte of the codes, tiled
+    scales, token scales and amax slots, padding rows included, and neither
+    touches rows at or past the segment end (sentinel bytes stay)."""
+    ops = _ops()
+    shape = synth.scaled(synth.MOE_30B, T=T, H=H, E=E, k=k)
+    ids, prob = synth.routing(shape)
+    seg, perm, inv, rp, cap = ops.moe_build_segments(ids.cuda(), prob.cuda(), E, pad=pad)
+    base = synth.normal_bf16(9, 40 + H, (T, H + (64 if strided else 0)), "cuda", std=2.0,
+                             outlier_p=0.01, outlier_mul=50.0)
+    x = base[:, :H] if strided else base
+
+    def bufs():
+        return ((torch.full((cap, H // 2), 0xA5, dtype=torch.uint8, device="cuda"),
+                 torch.full((ops.scale_bytes(cap, H // 16),), 0x5A, dtype=torch.uint8,
+                            device="cuda"),
+                 torch.full((cap,), 3.0, dtype=torch.float32, device="cuda")),
+                torch.full((cap,), 7.0, dtype=torch.float32, device="cuda"))
+    got, got_amax = bufs()
+    ref, ref_amax = bufs()
+    ops.nvfp4_quantize_scatter(x, inv, perm, seg, E, k, cap, out=got, amax_zero=got_amax)
+    q, s, ts = ops.nvfp4_quantize_per_token(x)
+    ops.moe_gather_nvfp4(q, s, ts, H, perm, seg, E, k, cap, out=ref, amax_zero=ref_amax)
+    torch.cuda.synchronize()
+    assert ops.get_device_status() == 0
+    for g, r, what in zip(got + (got_amax,), ref + (ref_amax,),
+                          ("codes", "scales", "token scales", "amax slots")):
+        assert torch.equal(g.view(torch.uint8), r.view(torch.uint8)), what
+    # the routed rows against the oracle's per-token encoding
+    rseg, rperm, rinv, rrp = MO.build_segments(ids.numpy(), prob.numpy(), E, pad)
+    R = int(rseg[-1])
+    rq, rs, rts = Q.nvfp4_quantize_per_token(np_bf16(x))
+    assert_bytes_equal(u8(got[0])[:R], MO.gather_rows(rq, rperm, k), "codes vs oracle")
+    got_s = Q.unswizzle_scales(u8(got[1]), cap, H // 16)[:R]
+    assert_bytes_equal(got_s, MO.gather_rows(rs, rperm, k), "scales vs oracle")
+    assert np.all(u8(got[0])[R:] == 0xA5), "codes written past the segment end"
+
+
+def test_nvfp4_quantize_scatter_bad_row_sets_status():
+    """A routed-row index at or past the segment end is dropped and reported
+    (MPM_ERR_DEVICE_BOUNDS); the other rows are still written."""
+    ops = _ops()
+    shape = synth.scaled(synth.MOE_30B, T=64, H=256, E=4, k=2)
+    ids, prob = synth.routing(shape)
+    seg, perm, inv, rp, cap = ops.moe_build_segments(ids.cuda(), prob.cuda(), shape.E)
+    x = synth.moe_activations(shape, device="cuda")
+    torch.cuda.synchronize()
+    assert ops.get_device_status() == 0
+    bad = inv.clone()
+    bad[5] = int(seg[-1].item())                  # one past the last valid row
+    out = ops.nvfp4_quantize_scatter(x, bad, perm, seg, shape.E, shape.k, cap)
+    torch.cuda.synchronize()
+    assert ops.get_device_status() == 7
+    q, s, ts = ops.nvfp4_quantize_per_token(x)
+    row = int(inv[4].item())                        # token 2, slot 0: still written
+    assert torch.equal(out[0][row], q[2])
+
+
 def test_gather_bf16_and_nvfp4_and_combine():
     shape = synth.scaled(synth.MOE_30B, T=700, H=512, E=12, k=4)
     ids, prob = synth.routing(shape)
