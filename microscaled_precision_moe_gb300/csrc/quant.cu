@@ -361,8 +361,19 @@ __global__ void __launch_bounds__(128) nvfp4_scatter_rows_kernel(const NvScatter
   if (r < nrows) {
     const long long tk = tok[r];
     const uint32_t* src = tk >= 0 ? a.ws_s + tk * ngroups : nullptr;
-    for (long long g = 0; g < ngroups; ++g)
-      reinterpret_cast<uint32_t*>(a.s + (rt * ngroups + g) * 512)[w] = src ? src[g] : 0u;
+    uint32_t* dst = reinterpret_cast<uint32_t*>(a.s + rt * ngroups * 512) + w;
+    long long g = 0;
+    // the token's words four at a time when they are 16-byte aligned
+    if (src && (ngroups & 3) == 0 && (reinterpret_cast<uintptr_t>(a.ws_s) & 15) == 0) {
+      for (; g < ngroups; g += 4) {
+        const uint4 v4 = *reinterpret_cast<const uint4*>(src + g);
+        dst[(g + 0) * 128] = v4.x;
+        dst[(g + 1) * 128] = v4.y;
+        dst[(g + 2) * 128] = v4.z;
+        dst[(g + 3) * 128] = v4.w;
+      }
+    }
+    for (; g < ngroups; ++g) dst[g * 128] = src ? src[g] : 0u;
   }
 }
 
