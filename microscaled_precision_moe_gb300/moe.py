@@ -8,7 +8,9 @@ step: expert offsets stay on the device.
 NVFP4 forward ("miniTE technical report", sections 5.2-5.4; "Towards
 Blackwell-native 8-bit and 4-bit RL", section "Per-token activation
 scaling"):
-  X --per-token NVFP4--> (q, s, ts) --gather by expert--> A
+  X --per-token NVFP4, written straight into the expert-ordered rows--> A
+     (codes, block scales, token scale; the same bytes as quantising then
+     gathering by expert)
   A x W1[e]^T  (gate|up)  --epilogue: alpha, SwiGLU x prob, row amax--> D (bf16)
   D --per-token NVFP4 reusing the amax--> A2
   A2 x W2[e]^T --epilogue: alpha--> Y_perm (bf16) --combine--> out (bf16)
