@@ -321,6 +321,37 @@ mpm_status mpm_nvfp4_quantize_scatter(const void* x_dev, int64_t T, int64_t K, i
                                       void* ws_dev, size_t ws_bytes, cudaStream_t stream);
 
 /*
+ * MXFP8 quantisation of the expert-ordered rows of x_dev (bf16 [T, K],
+ * leading dimension ldx elements) without the gathered bf16 copy: the same
+ * bytes as mpm_moe_gather (MPM_GATHER_BF16) with the same segments followed
+ * by mpm_mxfp8_quantize of the gathered [capacity, K] matrix with
+ * m_valid = seg_offsets + E.  Row r < seg_offsets[E] of the quantised matrix
+ * is token row perm[r] / k of x, a zero row where perm[r] < 0; rows at or
+ * beyond seg_offsets[E] are not written.
+ * Sources: "Towards Blackwell-native 8-bit and 4-bit RL", sections "Format
+ * background / MXFP8" and "Recipe 1 / Training" (row-wise and column-wise
+ * copies of each GEMM operand from one quantisation), and "miniTE technical
+ * report", section 5.3 (dispatch/permute ahead of the quantised expert
+ * GEMMs).
+ * flags, row_q_dev, row_s_dev, col_q_dev, ldc, col_s_dev: as for
+ * mpm_mxfp8_quantize with M = capacity.  perm_dev int32 [capacity] as written
+ * by mpm_moe_build_segments.  A token index perm[r] / k >= T sets
+ * MPM_ERR_DEVICE_BOUNDS and that row reads as zero.
+ * Requirements: T >= 1, capacity >= 1, E >= 1, 1 <= k <= 64, T * k < 2^31,
+ * K >= 32, K % 32 == 0, K <= ldx < 2^31, ldx % 8 == 0, x_dev 16-byte aligned,
+ * ldc >= capacity,
+ * ldc % 16 == 0, output pointers 16-byte aligned.  Launched with programmatic
+ * stream serialization, as mpm_mxfp8_quantize.
+ */
+mpm_status mpm_mxfp8_quantize_gather(const void* x_dev, int64_t T, int64_t K, int64_t ldx,
+                                     const int32_t* perm_dev, int k,
+                                     const int32_t* seg_offsets_dev, int64_t E,
+                                     int64_t capacity, unsigned flags,
+                                     uint8_t* row_q_dev, uint8_t* row_s_dev,
+                                     uint8_t* col_q_dev, int64_t ldc, uint8_t* col_s_dev,
+                                     cudaStream_t stream);
+
+/*
  * out[t] = sum over j = 0..k-1 (in that order, fp32) of y_perm[inv_perm[t*k+j]],
  * rounded once to bf16.  y_perm bf16 [capacity, H]; out bf16 [T, H].
  * Source: "miniTE technical report", section 5.3 (expert outputs, weighted by

@@ -52,6 +52,8 @@ _SIGS = {
     "mpm_version": (_int, []),
     "mpm_scale_bytes": (_sz, [_i64, _i64]),
     "mpm_mxfp8_quantize": (_int, [_vp, _i64, _i64, _i64, _u32, _vp, _vp, _vp, _i64, _vp, _vp, _vp]),
+    "mpm_mxfp8_quantize_gather": (_int, [_vp, _i64, _i64, _i64, _vp, _int, _vp, _i64, _i64, _u32,
+                                         _vp, _vp, _vp, _i64, _vp, _vp]),
     "mpm_nvfp4_quantize_per_token": (_int, [_vp, _i64, _i64, _i64, _vp, _vp, _vp, _vp, _vp, _vp]),
     "mpm_nvfp4_quantize_online": (_int, [_vp, _i64, _i64, _i64, _vp, _vp, _vp, _vp, _vp]),
     "mpm_nvfp4_weight_workspace_bytes": (_sz, [_i64]),

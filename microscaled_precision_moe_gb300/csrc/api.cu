@@ -202,6 +202,40 @@ mpm_status mpm_mxfp8_quantize(const void* x, int64_t M, int64_t K, int64_t ldx, 
                                            ldc, col_s, m_valid, status_ptr(), stream));
 }
 
+mpm_status mpm_mxfp8_quantize_gather(const void* x, int64_t T, int64_t K, int64_t ldx,
+                                     const int32_t* perm, int k, const int32_t* seg, int64_t E,
+                                     int64_t cap, unsigned flags, uint8_t* row_q, uint8_t* row_s,
+                                     uint8_t* col_q, int64_t ldc, uint8_t* col_s,
+                                     cudaStream_t stream) {
+  if (!x || !perm || !seg) return MPM_ERR_NULL;
+  if ((flags & (MPM_ROWWISE | MPM_COLWISE)) == 0 || (flags & ~3u)) return MPM_ERR_SHAPE;
+  if (T < 1 || cap < 1 || E < 1 || k < 1 || k > 64) return MPM_ERR_SHAPE;
+  if (K < 32 || K % 32 != 0 || ldx < K) return MPM_ERR_SHAPE;
+  if (cap > (1ll << 31) - 256 || K > (1ll << 31) - 256 || T * k > (1ll << 31) - 1 ||
+      ldx > (1ll << 31) - 1)
+    return MPM_ERR_SHAPE;
+  if (!aligned(x, 16) || ldx % 8 != 0) return MPM_ERR_ALIGN;
+  if (flags & MPM_ROWWISE) {
+    if (!row_q || !row_s) return MPM_ERR_NULL;
+    if (!aligned(row_q, 16)) return MPM_ERR_ALIGN;
+  }
+  if (flags & MPM_COLWISE) {
+    if (!col_q || !col_s) return MPM_ERR_NULL;
+    if (ldc < cap) return MPM_ERR_SHAPE;
+    if (!aligned(col_q, 16) || ldc % 16 != 0) return MPM_ERR_ALIGN;
+  }
+  CUtensorMap trow, tcol;
+  std::memset(&trow, 0, sizeof(trow));
+  std::memset(&tcol, 0, sizeof(tcol));
+  if ((flags & MPM_ROWWISE) && !make_u8_tmap(&trow, row_q, K, cap, K, 64, 128, false))
+    return MPM_ERR_CUDA;
+  if ((flags & MPM_COLWISE) && !make_u8_tmap(&tcol, col_q, cap, K, ldc, 128, 64, true))
+    return MPM_ERR_CUDA;
+  return cuda_status(mpm::launch_mxfp8_gather(trow, tcol, x, T, K, ldx, perm, k, seg + E, cap,
+                                              flags, row_q, row_s, col_q, ldc, col_s,
+                                              status_ptr(), stream));
+}
+
 mpm_status mpm_nvfp4_quantize_per_token(const void* x, int64_t M, int64_t K, int64_t ldx,
                                         const float* amax_in, uint8_t* q, uint8_t* s,
                                         float* ts, const int32_t* m_valid,

@@ -12,6 +12,7 @@
 // "Format background / MXFP8" and "Recipe 1 / Training").  A CTA reads a
 // 128 x 64 bf16 tile once, writes the row-wise 1x32 copy from registers and the
 // column-wise 32x1 copy, transposed, from a shared-memory copy of the tile.
+#include <cstring>
 #include "quant.cuh"
 
 namespace mpm {
@@ -546,7 +547,31 @@ struct Mxfp8Args {
   const int* m_valid;
   int pad_blocks;           // 1: zero the scale padding (host-sized buffers)
   int* status;
+  // gather form: row r of the quantised matrix is token row perm[r] / kk of
+  // x (T rows, stride ldx); perm[r] < 0 marks a zero padding row.  The
+  // division is a multiply by div_m with shifts div_s1, div_s2 (see
+  // div_magic below); T, ldx < 2^31.
+  const int* perm; int kk; long long T;
+  uint32_t div_m; int div_s1, div_s2;
 };
+
+// Unsigned 32-bit division by an invariant d >= 1 as a multiply and two
+// shifts (Granlund and Montgomery, "Division by invariant integers using
+// multiplication", 1994, the round-up multiplier with the add-and-shift
+// step that keeps it within 32 bits): with l = ceil(log2 d) and
+// m = floor(2^32 (2^l - d) / d) + 1, n / d = (t + ((n - t) >> s1)) >> s2
+// for t = mulhi(m, n), s1 = min(l, 1), s2 = max(l - 1, 0), every n < 2^32.
+static void div_magic(uint32_t d, uint32_t& m, int& s1, int& s2) {
+  int l = 0;
+  while ((1ull << l) < d) ++l;
+  m = (uint32_t)((((1ull << l) - d) << 32) / d + 1);
+  s1 = l < 1 ? l : 1;
+  s2 = l > 1 ? l - 1 : 0;
+}
+MPM_DEV uint32_t div_by_magic(uint32_t n, uint32_t m, int s1, int s2) {
+  const uint32_t t = __umulhi(m, n);
+  return (t + ((n - t) >> s1)) >> s2;
+}
 
 MPM_DEV void zero_scale_padding(uint8_t* s, long long rows, long long cols, long long tid,
                                 long long nthreads);
@@ -584,6 +609,67 @@ constexpr int MQ_TILE_BYTES = MQ_TM * MQ_TK * 2;     // 16 KB
 // keep the per-thread stores, and the scale bytes always use them.
 constexpr int MQ_OUT_BYTES = MQ_TM * MQ_TK + MQ_TK * MQ_TM;     // 8 KB rows + 8 KB columns
 
+// 16-byte global -> shared copy, zero-filled past n bytes (n = 0 or 16)
+MPM_DEV void cp_async_16(uint32_t dst, const void* src, uint32_t n) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(n)
+               : "memory");
+}
+MPM_DEV void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+MPM_DEV void cp_async_wait1() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
+MPM_DEV void cp_async_wait0() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+
+// Tile cursor: tile (mt, kt) of the row-major tile order (kt fastest), moved
+// by the grid stride without a division per step.
+struct MqCursor {
+  int mt, kt;
+  MPM_DEV void init(int ti, int n_kt) { mt = ti / n_kt; kt = ti - mt * n_kt; }
+  MPM_DEV void step(int dq, int dr, int n_kt) {
+    kt += dr; mt += dq;
+    if (kt >= n_kt) { kt -= n_kt; ++mt; }
+  }
+};
+
+// Gather form of the tile load: the 128 routed rows of a tile come from
+// their tokens' rows of x.  Thread t copies 16-byte chunk t % 8 of rows
+// t / 8 + 32 j (j < 4) to the 128-byte-swizzled offset a TMA load of the
+// gathered matrix would have used, so the encode passes read the stage
+// unchanged; rows past the valid count, padding rows and columns past K are
+// zero-filled.  A warp's 16 rows are looked up once each, by lanes 0-15
+// (lane 4 j + q: row 4 w + q + 32 j), one tile before the copies are issued,
+// and handed to the copying lanes by shuffle.
+MPM_DEV int mq_lookup(const Mxfp8Args& p, const MqCursor& c, int n_mt, int M_eff, int warp,
+                      int lane) {
+  if (lane >= 16 || c.mt >= n_mt) return -1;
+  const int row = c.mt * MQ_TM + warp * 4 + (lane & 3) + 32 * (lane >> 2);
+  return row < M_eff ? __ldg(p.perm + row) : -1;
+}
+
+// One copy group per tile (committed even when empty, so the group count
+// stays uniform).  dst_off: this thread's offset for j = 0 (rows j > 0 sit
+// 4096 bytes apart with the same swizzle phase).  A zero-filled copy still
+// names an address inside x (token 0, column 0 of the chunk's tile or 0).
+MPM_DEV void mq_gather_issue(const Mxfp8Args& p, uint32_t dst, const MqCursor& c, int f,
+                             uint32_t dst_off, int lane) {
+  int tok = -1;
+  if (f >= 0) {
+    tok = (int)div_by_magic((uint32_t)f, p.div_m, p.div_s1, p.div_s2);
+    if (tok >= (int)p.T) { set_status(p.status, MPM_ERR_DEVICE_BOUNDS); tok = -1; }
+  }
+  const int col = c.kt * MQ_TK + (lane & 7) * 8;
+  const bool col_ok = col < (int)p.K;
+  const __nv_bfloat16* xc = p.x + (col_ok ? col : 0);
+  const uint32_t ldx = (uint32_t)p.ldx;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int tj = __shfl_sync(0xffffffffu, tok, 4 * j + (lane >> 3));
+    const bool on = col_ok && tj >= 0;
+    const __nv_bfloat16* src = xc + (size_t)((uint32_t)max(tj, 0)) * ldx;
+    cp_async_16(dst + dst_off + 4096u * j, src, on ? 16u : 0u);
+  }
+  cp_async_commit();
+}
+
+template <bool GATHER>
 __global__ void __launch_bounds__(256) mxfp8_quant_tma_kernel(const __grid_constant__ CUtensorMap tx,
                                                              const __grid_constant__ CUtensorMap trow,
                                                              const __grid_constant__ CUtensorMap tcol,
@@ -604,12 +690,14 @@ __global__ void __launch_bounds__(256) mxfp8_quant_tma_kernel(const __grid_const
   if (p.m_valid) { const long long mv = *p.m_valid; M_eff = mv < M_eff ? mv : M_eff; }
   const long long n_tiles = (M_eff + MQ_TM - 1) / MQ_TM * n_kt;
   if (t == 0) {
-    for (int s = 0; s < MQ_STAGES; ++s) mbar_init(bar + 8 * s, 1);
-    fence_mbar_init();
-    prefetch_tmap(&tx);
+    if (!GATHER) {
+      for (int s = 0; s < MQ_STAGES; ++s) mbar_init(bar + 8 * s, 1);
+      fence_mbar_init();
+      prefetch_tmap(&tx);
+    }
     if (p.flags & MPM_ROWWISE) prefetch_tmap(&trow);
     if (p.flags & MPM_COLWISE) prefetch_tmap(&tcol);
-    for (int i = 0; i < MQ_STAGES; ++i) {
+    for (int i = 0; i < MQ_STAGES && !GATHER; ++i) {
       const long long ti = blockIdx.x + (long long)i * gridDim.x;
       if (ti >= n_tiles) break;
       mbar_arrive_expect_tx(bar + 8 * i, MQ_TILE_BYTES);
@@ -617,11 +705,31 @@ __global__ void __launch_bounds__(256) mxfp8_quant_tma_kernel(const __grid_const
                   bar + 8 * i);
     }
   }
+  // gather form: tile cursors (no division per tile); the first MQ_STAGES
+  // tiles in flight, nxt left on tile MQ_STAGES with its row lookup loaded
+  const int n_mt = (int)((M_eff + MQ_TM - 1) / MQ_TM);   // tile counts fit 31 bits (host-checked)
+  const int dq = (int)gridDim.x / n_kt, dr = (int)gridDim.x - dq * n_kt;
+  MqCursor cur, nxt;                                // this tile; the next tile to load
+  int fn = -1;                                      // row lookup of tile nxt
+  const uint32_t dst_off = (uint32_t)((t >> 3) * 128 + (((t & 7) ^ ((t >> 3) & 7)) << 4));
+  if (GATHER) {
+    cur.init((int)blockIdx.x, n_kt);
+    nxt = cur;
+    for (int i = 0; i < MQ_STAGES; ++i) {
+      fn = mq_lookup(p, nxt, n_mt, (int)M_eff, warp, lane);
+      if (nxt.mt < n_mt) mq_gather_issue(p, base + i * MQ_TILE_BYTES, nxt, fn, dst_off, lane);
+      else cp_async_commit();
+      nxt.step(dq, dr, n_kt);
+    }
+    fn = mq_lookup(p, nxt, n_mt, (int)M_eff, warp, lane);
+  }
   __syncthreads();
   int it = 0, last_buf = -1;                        // last_buf: thread 0's newest store group
   for (long long ti = blockIdx.x; ti < n_tiles; ti += gridDim.x, ++it) {
     const int s = it % MQ_STAGES;
-    const bool ok = mbar_wait(bar + 8 * s, (uint32_t)(it / MQ_STAGES) & 1u, p.status);
+    bool ok = true;
+    if (GATHER) cp_async_wait1();                   // this thread's copies of tile it (two groups ring)
+    else ok = mbar_wait(bar + 8 * s, (uint32_t)(it / MQ_STAGES) & 1u, p.status);
     // output buffer it % 2 is free once the store groups that read it have:
     // all but the newest group, or all of them when the newest used it too
     // (only full tiles commit a group)
@@ -631,7 +739,8 @@ __global__ void __launch_bounds__(256) mxfp8_quant_tma_kernel(const __grid_const
     }
     if (__syncthreads_or(!ok)) break;
     const uint8_t* tile = gbase + s * MQ_TILE_BYTES;          // row r at r * 128 bytes
-    const long long m0 = (ti / n_kt) * MQ_TM, k0 = (ti % n_kt) * MQ_TK;
+    const long long m0 = GATHER ? (long long)cur.mt * MQ_TM : (ti / n_kt) * MQ_TM;
+    const long long k0 = GATHER ? (long long)cur.kt * MQ_TK : (ti % n_kt) * MQ_TK;
     const bool full = (m0 + MQ_TM <= M_eff) && (k0 + MQ_TK <= p.K);
     const uint32_t orow = sOut + (it & 1) * MQ_OUT_BYTES;     // [128 rows][64 B]
     const uint32_t ocol = orow + MQ_TM * MQ_TK;               // [64 columns][128 B], swizzled
@@ -757,13 +866,21 @@ __global__ void __launch_bounds__(256) mxfp8_quant_tma_kernel(const __grid_const
         last_buf = it & 1;
       }
       const long long tn = ti + (long long)MQ_STAGES * gridDim.x;
-      if (tn < n_tiles) {
+      if (!GATHER && tn < n_tiles) {
         mbar_arrive_expect_tx(bar + 8 * s, MQ_TILE_BYTES);
         tma_load_2d(base + s * MQ_TILE_BYTES, &tx, (int)((tn % n_kt) * MQ_TK),
                     (int)((tn / n_kt) * MQ_TM), bar + 8 * s);
       }
     }
+    if (GATHER) {
+      if (nxt.mt < n_mt) mq_gather_issue(p, base + s * MQ_TILE_BYTES, nxt, fn, dst_off, lane);
+      else cp_async_commit();
+      nxt.step(dq, dr, n_kt);
+      fn = mq_lookup(p, nxt, n_mt, (int)M_eff, warp, lane);
+      cur.step(dq, dr, n_kt);
+    }
   }
+  if (GATHER) cp_async_wait0();                     // no copy outlives the CTA (loop left early)
   if (t == 0) bulk_wait_group0();                   // the code stores have completed
   if (p.pad_blocks) {
     // host-sized buffers: zero the padding entries of the scale tiles
@@ -945,32 +1062,25 @@ cudaError_t launch_nvfp4_quantize_scatter(const void* x, long long T, int K, lon
   return cudaGetLastError();
 }
 
-cudaError_t launch_mxfp8_tma(const CUtensorMap& tx, const CUtensorMap& trow, const CUtensorMap& tcol,
-                             long long M, long long K, long long ldx,
-                             unsigned flags, uint8_t* row_q, uint8_t* row_s, uint8_t* col_q,
-                             long long ldc, uint8_t* col_s, const int* m_valid, int* status,
-                             cudaStream_t st) {
-  Mxfp8Args p{};
-  p.M = M; p.K = K; p.ldx = ldx; p.flags = flags;
-  p.row_q = row_q; p.row_s = row_s; p.row_s_cols_pad = (K / 32 + 3) / 4 * 4;
-  p.col_q = col_q; p.ldc = ldc; p.col_s = col_s;
-  p.col_s_cols_pad = ((M + 31) / 32 + 3) / 4 * 4;
-  p.m_valid = m_valid;
-  p.pad_blocks = m_valid ? 0 : 1;
-  p.status = status;
-  const int n_kt = (int)((K + MQ_TK - 1) / MQ_TK);
-  const long long n_tiles = (M + MQ_TM - 1) / MQ_TM * n_kt;
+template <bool GATHER>
+static cudaError_t launch_mxfp8_impl(const CUtensorMap& tx, const CUtensorMap& trow,
+                                     const CUtensorMap& tcol, const Mxfp8Args& p,
+                                     cudaStream_t st) {
+  const int n_kt = (int)((p.K + MQ_TK - 1) / MQ_TK);
+  const long long n_tiles = (p.M + MQ_TM - 1) / MQ_TM * n_kt;
+  if (n_tiles > (1ll << 30)) return cudaErrorInvalidValue;   // tile cursors are 32-bit
   constexpr int smem = 1024 + MQ_STAGES * MQ_TILE_BYTES + 2 * MQ_OUT_BYTES + 64;
   static int ctas[64] = {0};
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return err;
   if (dev < 64 && ctas[dev] == 0) {
-    err = cudaFuncSetAttribute(mxfp8_quant_tma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    err = cudaFuncSetAttribute(mxfp8_quant_tma_kernel<GATHER>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (err != cudaSuccess) return err;
     int sms = 0, per = 0;
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, mxfp8_quant_tma_kernel, 256, smem);
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, mxfp8_quant_tma_kernel<GATHER>, 256, smem);
     ctas[dev] = (sms > 0 ? sms : 1) * (per > 0 ? per : 1);
   }
   long long grid = dev < 64 ? ctas[dev] : 1;
@@ -986,9 +1096,44 @@ cudaError_t launch_mxfp8_tma(const CUtensorMap& tx, const CUtensorMap& trow, con
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, mxfp8_quant_tma_kernel, tx, trow, tcol, p, n_kt);
+  return cudaLaunchKernelEx(&cfg, mxfp8_quant_tma_kernel<GATHER>, tx, trow, tcol, p, n_kt);
 }
 
+static Mxfp8Args mxfp8_args(long long M, long long K, long long ldx, unsigned flags,
+                            uint8_t* row_q, uint8_t* row_s, uint8_t* col_q, long long ldc,
+                            uint8_t* col_s, const int* m_valid, int* status) {
+  Mxfp8Args p{};
+  p.M = M; p.K = K; p.ldx = ldx; p.flags = flags;
+  p.row_q = row_q; p.row_s = row_s; p.row_s_cols_pad = (K / 32 + 3) / 4 * 4;
+  p.col_q = col_q; p.ldc = ldc; p.col_s = col_s;
+  p.col_s_cols_pad = ((M + 31) / 32 + 3) / 4 * 4;
+  p.m_valid = m_valid;
+  p.pad_blocks = m_valid ? 0 : 1;
+  p.status = status;
+  return p;
+}
 
+cudaError_t launch_mxfp8_tma(const CUtensorMap& tx, const CUtensorMap& trow, const CUtensorMap& tcol,
+                             long long M, long long K, long long ldx,
+                             unsigned flags, uint8_t* row_q, uint8_t* row_s, uint8_t* col_q,
+                             long long ldc, uint8_t* col_s, const int* m_valid, int* status,
+                             cudaStream_t st) {
+  const Mxfp8Args p = mxfp8_args(M, K, ldx, flags, row_q, row_s, col_q, ldc, col_s, m_valid, status);
+  return launch_mxfp8_impl<false>(tx, trow, tcol, p, st);
+}
+
+cudaError_t launch_mxfp8_gather(const CUtensorMap& trow, const CUtensorMap& tcol, const void* x,
+                                long long T, long long K, long long ldx, const int* perm, int k,
+                                const int* seg_end, long long cap, unsigned flags,
+                                uint8_t* row_q, uint8_t* row_s, uint8_t* col_q, long long ldc,
+                                uint8_t* col_s, int* status, cudaStream_t st) {
+  Mxfp8Args p = mxfp8_args(cap, K, ldx, flags, row_q, row_s, col_q, ldc, col_s, seg_end, status);
+  p.x = static_cast<const __nv_bfloat16*>(x);
+  p.perm = perm; p.kk = k; p.T = T;
+  div_magic((uint32_t)k, p.div_m, p.div_s1, p.div_s2);
+  CUtensorMap none;
+  std::memset(&none, 0, sizeof(none));
+  return launch_mxfp8_impl<true>(none, trow, tcol, p, st);
+}
 
 }  // namespace mpm

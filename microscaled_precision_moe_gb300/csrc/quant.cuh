@@ -31,5 +31,14 @@ cudaError_t launch_mxfp8_tma(const CUtensorMap& tx, const CUtensorMap& trow, con
                              unsigned flags, uint8_t* row_q, uint8_t* row_s, uint8_t* col_q,
                              long long ldc, uint8_t* col_s, const int* m_valid, int* status,
                              cudaStream_t st);
+// the same quantiser over the routed rows of x [T, K]: row r < *seg_end of
+// the quantised matrix (cap rows) is token row perm[r] / k, a zero row where
+// perm[r] < 0; the tiles are gathered by 16-byte copies instead of the
+// tensor-map load
+cudaError_t launch_mxfp8_gather(const CUtensorMap& trow, const CUtensorMap& tcol, const void* x,
+                                long long T, long long K, long long ldx, const int* perm, int k,
+                                const int* seg_end, long long cap, unsigned flags,
+                                uint8_t* row_q, uint8_t* row_s, uint8_t* col_q, long long ldc,
+                                uint8_t* col_s, int* status, cudaStream_t st);
 
 }  // namespace mpm

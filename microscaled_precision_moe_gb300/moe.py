@@ -27,7 +27,10 @@ exactly the NVFP4 operands the forward consumed ("dequantized"):
 MXFP8 forward + backward ("Towards Blackwell-native 8-bit and 4-bit RL",
 section "Recipe 1 / Training"): every GEMM operand is quantised from bf16;
 fprop uses row-wise copies, dgrad the row-wise gradient and the column-wise
-weight copy, wgrad the column-wise gradient and activation copies.
+weight copy, wgrad the column-wise gradient and activation copies.  X and dY
+are quantised straight from their token rows into the expert-ordered row-wise
+and column-wise copies (the same bytes as gathering by expert, then
+quantising), so no permuted bf16 copy is written.
 """
 from __future__ import annotations
 
@@ -357,9 +360,11 @@ class MXFP8MoE:
         self.dw2 = e(E, H, I, dtype=f32)
 
     # stages of one training step, for CUDA-event marks (see forward / backward)
-    STEP_STAGES = ("quant_w", "segments", "gather_x", "quant_x", "fc1", "quant_d", "fc2",
-                   "combine", "gather_dy", "quant_dy", "fc2_dgrad", "fc2_wgrad", "quant_dh",
-                   "fc1_dgrad", "combine_dx", "fc1_wgrad")
+    # (quant_x and quant_dy quantise the routed rows straight from the token
+    # rows: the permute is folded into the quantiser's tile loads)
+    STEP_STAGES = ("quant_w", "segments", "quant_x", "fc1", "quant_d", "fc2", "combine",
+                   "quant_dy", "fc2_dgrad", "fc2_wgrad", "quant_dh", "fc1_dgrad", "combine_dx",
+                   "fc1_wgrad")
 
     def quantize_weights(self, w1, w2):
         E, H, I = self.E, self.H, self.I
@@ -367,70 +372,67 @@ class MXFP8MoE:
         ops.mxfp8_quantize(w2.reshape(E * H, I), ldc=E * H, out=self.w2)
 
     def forward(self, x, topk_ids, topk_prob, mark=None):
-        """``mark(i)`` (optional) before STEP_STAGES[i] for i = 1..7."""
+        """``mark(i)`` (optional) before STEP_STAGES[i] for i = 1..6."""
         T, H, I, E, k, cap = self.T, self.H, self.I, self.E, self.k, self.cap
         mark = mark or (lambda i: None)
         seg, perm, inv, rp = self.seg
         mark(1)
         ops.moe_build_segments(topk_ids, topk_prob, E, out=self.seg, ws=self.seg_ws,
                                pad=self.tile_m)
+        self._x = x                                  # for the high-precision BF16 backward
         mark(2)
-        ops.moe_gather_bf16(x, perm, seg, E, k, cap, out=self.xp)
+        ops.mxfp8_quantize_gather(x, perm, seg, E, k, cap, ldc=cap, out=self.xq)
         mark(3)
-        ops.mxfp8_quantize(self.xp, ldc=cap, m_valid=seg[E:], out=self.xq)
-        mark(4)
         ops.moe_grouped_gemm(L.KIND_MXFP8, L.GROUP_M, L.EPI_SWIGLU_SAVE, E, cap, 2 * I, H, seg,
                              self.xq["row_q"], self.w1["row_q"], self.xq["row_s"], H // 32,
                              self.w1["row_s"], H // 32, self.c1, b_rows_per_expert=2 * I,
                              row_prob=rp, out2=self.d, tile_m=self.tile_m)
-        mark(5)
+        mark(4)
         ops.mxfp8_quantize(self.d, ldc=cap, m_valid=seg[E:], out=self.dq)
-        mark(6)
+        mark(5)
         ops.moe_grouped_gemm(L.KIND_MXFP8, L.GROUP_M, L.EPI_BF16, E, cap, H, I, seg,
                              self.dq["row_q"], self.w2["row_q"], self.dq["row_s"], I // 32,
                              self.w2["row_s"], I // 32, self.y, b_rows_per_expert=H,
                              tile_m=self.tile_m)
-        mark(7)
+        mark(6)
         ops.moe_combine(self.y, inv, T, k, out=self.out)
         return self.out
 
     def backward(self, dy, mark=None):
-        """``mark(i)`` (optional) before STEP_STAGES[i] for i = 8..15 and once
-        more (16) at the end."""
+        """``mark(i)`` (optional) before STEP_STAGES[i] for i = 7..13 and once
+        more (14) at the end."""
         T, H, I, E, k, cap = self.T, self.H, self.I, self.E, self.k, self.cap
         mark = mark or (lambda i: None)
         seg, perm, inv, rp = self.seg
+        mark(7)
+        ops.mxfp8_quantize_gather(dy, perm, seg, E, k, cap, ldc=cap, out=self.dyq)
         mark(8)
-        ops.moe_gather_bf16(dy, perm, seg, E, k, cap, out=self.dyp)
-        mark(9)
-        ops.mxfp8_quantize(self.dyp, ldc=cap, m_valid=seg[E:], out=self.dyq)
-        mark(10)
         # FC2 dgrad with the SwiGLU backward fused: dH = [dg | du]
         ops.moe_grouped_gemm(L.KIND_MXFP8, L.GROUP_M, L.EPI_DSWIGLU, E, cap, I, H, seg,
                              self.dyq["row_q"], self.w2["col_q"], self.dyq["row_s"], H // 32,
                              self.w2["col_s"], (E * H) // 32, self.dh, b_rows_per_expert=0,
                              b_k_per_expert=H, row_prob=rp, aux=self.c1, tile_m=self.tile_m)
-        mark(11)
+        mark(9)
         # FC2 wgrad: dW2[e] = dY_e^T . D_e
         ops.moe_grouped_gemm(L.KIND_MXFP8, L.GROUP_K, L.EPI_F32, E, H, I, 0, seg,
                              self.dyq["col_q"], self.dq["col_q"], self.dyq["col_s"], cap // 32,
                              self.dq["col_s"], cap // 32, self.dw2, tile_m=self._wgrad_tile(H))
-        mark(12)
+        mark(10)
         ops.mxfp8_quantize(self.dh, ldc=cap, m_valid=seg[E:], out=self.dhq)
-        mark(13)
+        mark(11)
         # FC1 dgrad: dX_perm = dH . W1_e (column-wise W1 copy)
         ops.moe_grouped_gemm(L.KIND_MXFP8, L.GROUP_M, L.EPI_BF16, E, cap, H, 2 * I, seg,
                              self.dhq["row_q"], self.w1["col_q"], self.dhq["row_s"], (2 * I) // 32,
                              self.w1["col_s"], (E * 2 * I) // 32, self.dxp, b_rows_per_expert=0,
                              b_k_per_expert=2 * I, tile_m=self.tile_m)
-        mark(14)
+        mark(12)
         ops.moe_combine(self.dxp, inv, T, k, out=self.dx)
-        mark(15)
+        mark(13)
         # FC1 wgrad: dW1[e] = dH_e^T . X_e
         ops.moe_grouped_gemm(L.KIND_MXFP8, L.GROUP_K, L.EPI_F32, E, 2 * I, H, 0, seg,
                              self.dhq["col_q"], self.xq["col_q"], self.dhq["col_s"], cap // 32,
                              self.xq["col_s"], cap // 32, self.dw1, tile_m=self._wgrad_tile(2 * I))
-        mark(16)
+        mark(14)
         return self.dx, self.dw1, self.dw2
 
     # ------------------------------------------------------------ BF16 backward
@@ -470,6 +472,9 @@ class MXFP8MoE:
         mark = mark or (lambda i: None)
         mark(0)
         if mode == "high_precision":
+            # the forward quantised X straight from the token rows: the BF16
+            # wgrad operand is gathered here
+            ops.moe_gather_bf16(self._x, self.seg[1], seg, E, self.k, cap, out=self.xp)
             x_op, d_op = self.xp, self.d
         else:
             if getattr(self, "xop", None) is None:

@@ -93,6 +93,36 @@ def mxfp8_quantize(x, rowwise=True, colwise=True, ldc=None, m_valid=None, out=No
     return o
 
 
+def mxfp8_quantize_gather(x, perm, seg, E: int, k: int, cap: int, rowwise=True, colwise=True,
+                          ldc=None, out=None):
+    """MXFP8 copies of the permuted layout of bf16 x [T, K] (cap rows, row r
+    = token perm[r] // k, zero for padding rows), without the gathered bf16
+    matrix: the bytes moe_gather_bf16 followed by mxfp8_quantize(...,
+    m_valid=seg[E:]) give.  Same output dict as mxfp8_quantize with M = cap."""
+    lib = L.load()
+    _check_rows(x, "x")
+    _check_route(perm, seg, E, cap)
+    _need_cuda(x, perm, seg)
+    T, K = x.shape
+    ldc = ldc or pad_to(cap, 16)
+    dev = x.device
+    o = out or {}
+    flags = (L.ROWWISE if rowwise else 0) | (L.COLWISE if colwise else 0)
+    if rowwise:
+        o.setdefault("row_q", torch.empty(cap, K, dtype=torch.uint8, device=dev))
+        o.setdefault("row_s", torch.empty(scale_bytes(cap, K // 32), dtype=torch.uint8, device=dev))
+    if colwise:
+        o.setdefault("col_q", torch.empty(K, ldc, dtype=torch.uint8, device=dev))
+        o.setdefault("col_s", torch.empty(scale_bytes(K, (cap + 31) // 32), dtype=torch.uint8,
+                                          device=dev))
+    st = lib.mpm_mxfp8_quantize_gather(_ptr(x), T, K, x.stride(0), _ptr(perm), k, _ptr(seg), E,
+                                       cap, flags, _ptr(o.get("row_q")), _ptr(o.get("row_s")),
+                                       _ptr(o.get("col_q")), ldc, _ptr(o.get("col_s")),
+                                       _stream(dev))
+    L.check(st, "mpm_mxfp8_quantize_gather")
+    return o
+
+
 def nvfp4_quantize_per_token(x, amax_in=None, m_valid=None, out=None):
     """Per-token NVFP4 of bf16 x [M, K]: (q [M, K/2] u8, s tiled [M, K/16] u8,
     token_scale [M] fp32) from one call."""

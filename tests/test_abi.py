@@ -360,6 +360,32 @@ def test_binding_checks_gemm_and_dequantize_arguments(lib):
         ops.mxfp8_dequantize(torch.zeros(8, 64, dtype=u8), torch.zeros(ops.scale_bytes(8, 2), dtype=u8))
 
 
+def test_mxfp8_quantize_gather_validation(lib):
+    """mpm_mxfp8_quantize_gather rejects bad arguments on the host."""
+    fake = C.c_void_p(0x10000)
+    odd = C.c_void_p(0x10008)
+    f = lib.mpm_mxfp8_quantize_gather
+    ok = dict(x=fake, T=4, K=64, ldx=64, perm=fake, k=2, seg=fake, E=2, cap=256, flags=3,
+              rq=fake, rs=fake, cq=fake, ldc=256, cs=fake)
+
+    def call(**kw):
+        a = dict(ok, **kw)
+        return f(a["x"], a["T"], a["K"], a["ldx"], a["perm"], a["k"], a["seg"], a["E"], a["cap"],
+                 a["flags"], a["rq"], a["rs"], a["cq"], a["ldc"], a["cs"], None)
+    assert call(x=None) == 1 and call(perm=None) == 1 and call(seg=None) == 1
+    assert call(rq=None) == 1 and call(cs=None) == 1
+    assert call(flags=0) == 2 and call(flags=4) == 2
+    assert call(T=0) == 2 and call(cap=0) == 2 and call(E=0) == 2
+    assert call(k=0) == 2 and call(k=65) == 2
+    assert call(K=16) == 2 and call(K=48) == 2 and call(ldx=32) == 2 and call(ldc=128) == 2
+    assert call(ldx=1 << 31) == 2 and call(T=1 << 30, k=2) == 2
+    assert call(x=odd) == 3 and call(ldx=68) == 3 and call(rq=odd) == 3
+    assert call(cq=odd) == 3 and call(ldc=264) == 3
+    # one copy only: the other copy's pointers are not needed
+    assert call(flags=1, cq=None, cs=None, ldc=0, x=odd) == 3
+    assert call(flags=2, rq=None, rs=None, x=odd) == 3
+
+
 def test_quantize_scatter_validation(lib):
     """mpm_nvfp4_quantize_scatter rejects bad arguments on the host."""
     fake = C.c_void_p(0x10000)

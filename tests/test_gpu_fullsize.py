@@ -13,8 +13,9 @@ expert at a time (it needs only the weights of the experts it checks):
 * combine: the output equals, bit for bit, the oracle's combine of the
   kernel's own Y rows (fetched a chunk of tokens at a time, so it holds at
   any size);
-* MXFP8 forward and backward: C, D, Y, dH rows and the full dW1 / dW2 of the
-  checked experts: GEMM tolerance.
+* MXFP8 forward and backward: X and dY quantised into the checked experts'
+  rows (row-wise and column-wise codes, column scales): byte-exact; C, D, Y,
+  dH rows and the full dW1 / dW2 of the checked experts: GEMM tolerance.
 """
 import numpy as np
 import pytest
@@ -222,6 +223,16 @@ def test_mxfp8_layer_30b_fwd_bwd_full_size():
             dw2e = MO.grouped_wgrad(MO.mx_cols_t(dye), MO.mx_cols_t(d), segl)[0]
             dw1e = MO.grouped_wgrad(MO.mx_cols_t(dh), MO.mx_cols_t(xe), segl)[0]
         sel = torch.from_numpy(rws).cuda()
+        # X and dY quantised from the token rows into this expert's rows
+        # (segments start on 256-row boundaries: whole column blocks), bytes
+        for q, v, what in ((L.xq, xe, "X"), (L.dyq, dye, "dY")):
+            v = np.where(real[:, None], v, 0.0)        # padding rows +0, as gathered
+            rq, rs = Q.mxfp8_quantize_rowwise(v)
+            assert_bytes_equal(u8(q["row_q"][sel]), rq, f"expert {e}: {what} row codes")
+            cq, cs = Q.mxfp8_quantize_colwise(v)
+            assert_bytes_equal(u8(q["col_q"][:, r0:r1]), cq, f"expert {e}: {what} column codes")
+            got_cs = Q.unswizzle_scales(u8(q["col_s"]), H, (L.cap + 31) // 32)
+            assert_bytes_equal(got_cs[:, r0 // 32:r1 // 32], cs, f"expert {e}: {what} column scales")
         _close(np_bf16(L.c1[sel]), c1, f"expert {e}: C = gate|up")
         _close(np_bf16(L.d[sel]), d, f"expert {e}: D")
         _close(np_bf16(L.y[sel]), y, f"expert {e}: Y")

@@ -135,6 +135,84 @@ def test_nvfp4_quantize_scatter_bad_row_sets_status():
     assert torch.equal(out[0][row], q[2])
 
 
+@pytest.mark.parametrize("pad", [128, 256])
+@pytest.mark.parametrize("T,H,E,k,strided", [(700, 512, 12, 4, False), (300, 2080, 16, 8, True),
+                                              (1000, 2048, 128, 8, False), (500, 256, 10, 6, False),
+                                              (200, 64, 3, 1, False)])
+def test_mxfp8_quantize_gather_equals_gather_then_quantize(T, H, E, k, strided, pad):
+    """The MXFP8 quantiser reading the routed rows straight from the token
+    rows writes exactly what the bf16 gather followed by the quantiser (with
+    the device row count) writes: every byte of both code copies and both
+    scale tiles, sentinel bytes past the segment end included.  H = 2080
+    leaves a 32-column last tile; the routed rows against the oracle's
+    gather and MXFP8 encoding."""
+    ops = _ops()
+    shape = synth.scaled(synth.MOE_30B, T=T, H=H, E=E, k=k)
+    ids, prob = synth.routing(shape)
+    seg, perm, inv, rp, cap = ops.moe_build_segments(ids.cuda(), prob.cuda(), E, pad=pad)
+    base = synth.normal_bf16(9, 60 + H, (T, H + (64 if strided else 0)), "cuda", std=2.0,
+                             outlier_p=0.01, outlier_mul=1e3)
+    x = base[:, :H] if strided else base
+    ldc = cap + 16
+
+    def bufs():
+        return {"row_q": torch.full((cap, H), 0xA5, dtype=torch.uint8, device="cuda"),
+                "row_s": torch.full((ops.scale_bytes(cap, H // 32),), 0x5A, dtype=torch.uint8,
+                                    device="cuda"),
+                "col_q": torch.full((H, ldc), 0xA5, dtype=torch.uint8, device="cuda"),
+                "col_s": torch.full((ops.scale_bytes(H, (cap + 31) // 32),), 0x5A,
+                                    dtype=torch.uint8, device="cuda")}
+    got = ops.mxfp8_quantize_gather(x, perm, seg, E, k, cap, ldc=ldc, out=bufs())
+    # the gathered matrix by plain indexing (the library's bf16 gather wants
+    # K % 64 == 0), rows past the segment end left as they are
+    xp = torch.zeros(cap, H, dtype=torch.bfloat16, device="cuda")
+    real = perm >= 0
+    xp[real] = x[(perm[real] // k).long()]
+    ref = ops.mxfp8_quantize(xp, ldc=ldc, m_valid=seg[E:], out=bufs())
+    torch.cuda.synchronize()
+    assert ops.get_device_status() == 0
+    for name in ("row_q", "row_s", "col_q", "col_s"):
+        assert torch.equal(got[name], ref[name]), name
+    rseg, rperm, rinv, rrp = MO.build_segments(ids.numpy(), prob.numpy(), E, pad)
+    R = int(rseg[-1])
+    xg = MO.gather_rows(np_bf16(x), rperm, k)
+    rq, rs = Q.mxfp8_quantize_rowwise(xg)
+    assert_bytes_equal(u8(got["row_q"])[:R], rq, "row codes vs oracle")
+    assert_bytes_equal(Q.unswizzle_scales(u8(got["row_s"]), cap, H // 32)[:R], rs,
+                       "row scales vs oracle")
+    cq, cs = Q.mxfp8_quantize_colwise(xg)
+    assert_bytes_equal(u8(got["col_q"])[:, :R], cq, "column codes vs oracle")
+    assert_bytes_equal(Q.unswizzle_scales(u8(got["col_s"]), H, (cap + 31) // 32)[:, :R // 32],
+                       cs, "column scales vs oracle")
+    assert np.all(u8(got["row_q"])[R:] == 0xA5), "row codes written past the segment end"
+    assert np.all(u8(got["col_q"])[:, R:] == 0xA5), "column codes written past the segment end"
+
+
+def test_mxfp8_quantize_gather_bad_token_sets_status():
+    """A routed row naming a token at or past T reads as zero and is
+    reported (MPM_ERR_DEVICE_BOUNDS); the other rows are still quantised."""
+    ops = _ops()
+    shape = synth.scaled(synth.MOE_30B, T=64, H=256, E=4, k=2)
+    ids, prob = synth.routing(shape)
+    seg, perm, inv, rp, cap = ops.moe_build_segments(ids.cuda(), prob.cuda(), shape.E)
+    x = synth.moe_activations(shape, device="cuda")
+    torch.cuda.synchronize()
+    assert ops.get_device_status() == 0
+    bad = perm.clone()
+    row = int(inv[6].item())                        # token 3, slot 0
+    bad[row] = shape.T * shape.k                    # token T: out of range
+    got = ops.mxfp8_quantize_gather(x, bad, seg, shape.E, shape.k, cap)
+    torch.cuda.synchronize()
+    assert ops.get_device_status() == 7
+    ref = ops.mxfp8_quantize(ops.moe_gather_bf16(x, perm, seg, shape.E, shape.k, cap),
+                             m_valid=seg[shape.E:])
+    torch.cuda.synchronize()
+    assert ops.get_device_status() == 0
+    assert torch.all(got["row_q"][row] == 0)
+    other = int(inv[8].item())                      # token 4, slot 0
+    assert torch.equal(got["row_q"][other], ref["row_q"][other])
+
+
 def test_gather_bf16_and_nvfp4_and_combine():
     shape = synth.scaled(synth.MOE_30B, T=700, H=512, E=12, k=4)
     ids, prob = synth.routing(shape)
