@@ -364,10 +364,24 @@ __global__ void __launch_bounds__(128) nvfp4_scatter_rows_kernel(const NvScatter
     const uint32_t* src = tk >= 0 ? a.ws_s + tk * ngroups : nullptr;
     uint32_t* dst = reinterpret_cast<uint32_t*>(a.s + rt * ngroups * 512) + w;
     long long g = 0;
-    // the token's words four at a time when they are 16-byte aligned
+    // the token's words four at a time when they are 16-byte aligned, eight
+    // such loads in flight before their stores (the rows are L2 hits whose
+    // latency, not bandwidth, paces this launch)
     if (src && (ngroups & 3) == 0 && (reinterpret_cast<uintptr_t>(a.ws_s) & 15) == 0) {
+      for (; g + 32 <= ngroups; g += 32) {
+        uint4 v4[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) v4[u] = __ldg(reinterpret_cast<const uint4*>(src + g) + u);
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          dst[(g + 4 * u + 0) * 128] = v4[u].x;
+          dst[(g + 4 * u + 1) * 128] = v4[u].y;
+          dst[(g + 4 * u + 2) * 128] = v4[u].z;
+          dst[(g + 4 * u + 3) * 128] = v4[u].w;
+        }
+      }
       for (; g < ngroups; g += 4) {
-        const uint4 v4 = *reinterpret_cast<const uint4*>(src + g);
+        const uint4 v4 = __ldg(reinterpret_cast<const uint4*>(src + g));
         dst[(g + 0) * 128] = v4.x;
         dst[(g + 1) * 128] = v4.y;
         dst[(g + 2) * 128] = v4.z;
