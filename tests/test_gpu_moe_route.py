@@ -188,6 +188,43 @@ def test_mxfp8_quantize_gather_equals_gather_then_quantize(T, H, E, k, strided, 
     assert np.all(u8(got["col_q"])[:, R:] == 0xA5), "column codes written past the segment end"
 
 
+@pytest.mark.parametrize("case", ["one_token", "one_expert", "no_padding", "sparse"])
+def test_mxfp8_quantize_gather_degenerate_routings(case):
+    """Degenerate routings through the gather form, byte for byte against
+    the oracle's gather and MXFP8 encoding: a single token (two rows, each
+    its own padded segment), every row on one expert of eight (the other
+    segments empty), segments that need no padding (every tile full), and
+    most experts empty with a single row on the last one."""
+    ops = _ops()
+    if case == "one_token":
+        ids, prob, E, H = torch.tensor([[3, 1]], dtype=torch.int32), torch.tensor([[0.25, 0.75]]), 4, 64
+    elif case == "one_expert":
+        ids, prob, E, H = torch.zeros(300, 1, dtype=torch.int32) + 5, torch.ones(300, 1), 8, 320
+    elif case == "no_padding":
+        ids = torch.arange(512, dtype=torch.int32).remainder(2).view(256, 2)
+        prob, E, H = torch.full((256, 2), 0.5), 2, 256
+    else:
+        ids = torch.zeros(40, 1, dtype=torch.int32)
+        ids[-1, 0] = 63
+        prob, E, H = torch.ones(40, 1), 64, 128
+    T, k = ids.shape
+    seg, perm, inv, rp, cap = ops.moe_build_segments(ids.cuda(), prob.cuda(), E, pad=256)
+    x = synth.normal_bf16(4, 11 + H, (T, H), "cuda", std=3.0, outlier_p=0.05, outlier_mul=1e3)
+    got = ops.mxfp8_quantize_gather(x, perm, seg, E, k, cap, ldc=cap + 32)
+    torch.cuda.synchronize()
+    assert ops.get_device_status() == 0
+    rseg, rperm, rinv, rrp = MO.build_segments(ids.numpy(), prob.numpy(), E, 256)
+    R = int(rseg[-1])
+    xg = MO.gather_rows(np_bf16(x), rperm, k)
+    rq, rs = Q.mxfp8_quantize_rowwise(xg)
+    cq, cs = Q.mxfp8_quantize_colwise(xg)
+    assert_bytes_equal(u8(got["row_q"])[:R], rq, f"{case}: row codes")
+    assert_bytes_equal(Q.unswizzle_scales(u8(got["row_s"]), cap, H // 32)[:R], rs, f"{case}: row scales")
+    assert_bytes_equal(u8(got["col_q"])[:, :R], cq, f"{case}: column codes")
+    assert_bytes_equal(Q.unswizzle_scales(u8(got["col_s"]), H, (cap + 31) // 32)[:, :R // 32], cs,
+                       f"{case}: column scales")
+
+
 def test_mxfp8_quantize_gather_bad_token_sets_status():
     """A routed row naming a token at or past T reads as zero and is
     reported (MPM_ERR_DEVICE_BOUNDS); the other rows are still quantised."""
