@@ -604,8 +604,9 @@ MPM_DEV uint32_t absmax_bf16x2_packed(const uint32_t (&w)[N]) {
 // ---------------------------------------------------------------- MXFP8, TMA-staged
 // Persistent CTAs walk 128 x 64 tiles of x; a 2-deep ring of TMA loads keeps
 // the next tiles in flight while a tile is encoded from shared memory (two
-// stages, 33 KB per CTA: six CTAs per SM, measured faster than three stages
-// at four CTAs).
+// 16 KB input stages and two 16 KB code-staging buffers, 66.6 KB per CTA:
+// three CTAs per SM; deeper rings, and one staging buffer at four CTAs per
+// SM, measured slower).
 // Row pass: one thread per 32-element row block (its 64 bytes in four
 // 16-byte loads).  Column pass: a pair of adjacent columns x 16 rows per thread
 // (two threads per pair of 32-row column blocks, see below).  The tile is
@@ -661,7 +662,8 @@ MPM_DEV int mq_lookup(const Mxfp8Args& p, const MqCursor& c, int n_mt, int M_eff
 // One copy group per tile (committed even when empty, so the group count
 // stays uniform).  dst_off: this thread's offset for j = 0 (rows j > 0 sit
 // 4096 bytes apart with the same swizzle phase).  A zero-filled copy still
-// names an address inside x (token 0, column 0 of the chunk's tile or 0).
+// names an address inside x: token 0 at the chunk's column, or column 0 when
+// the chunk lies past K.
 MPM_DEV void mq_gather_issue(const Mxfp8Args& p, uint32_t dst, const MqCursor& c, int f,
                              uint32_t dst_off, int lane) {
   int tok = -1;
