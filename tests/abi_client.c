@@ -53,6 +53,16 @@ int main(void) {
         MPM_ERR_SHAPE);
   CHECK(mpm_mxfp8_quantize(dev, 4, 64, 64, 0u, dev, dev, dev, 16, dev, NULL, 0) ==
         MPM_ERR_SHAPE);
+  /* the routed-row forms: no routing, a bad top-k, a misaligned input */
+  CHECK(mpm_mxfp8_quantize_gather(dev, 4, 64, 64, NULL, 2, dev, 2, 256, MPM_ROWWISE, dev, dev,
+                                  NULL, 0, NULL, 0) == MPM_ERR_NULL);
+  CHECK(mpm_mxfp8_quantize_gather(dev, 4, 64, 64, dev, 0, dev, 2, 256, MPM_ROWWISE, dev, dev,
+                                  NULL, 0, NULL, 0) == MPM_ERR_SHAPE);
+  CHECK(mpm_mxfp8_quantize_gather(odd, 4, 64, 64, dev, 2, dev, 2, 256, MPM_ROWWISE, dev, dev,
+                                  NULL, 0, NULL, 0) == MPM_ERR_ALIGN);
+  CHECK(mpm_nvfp4_quantize_scatter_workspace_bytes(4, 64) == 4 * 4 + 4 * 4 + 16);
+  CHECK(mpm_nvfp4_quantize_scatter(dev, 4, 64, 64, dev, 65, dev, dev, 2, 256, dev, dev, dev, NULL,
+                                   dev, 48, 0) == MPM_ERR_SHAPE);
 
   /* segments, combine */
   CHECK(mpm_moe_build_segments(dev, dev, 0, 8, 16, 128, dev, dev, dev, dev, dev, 1u << 20, 0) ==
