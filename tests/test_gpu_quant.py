@@ -178,6 +178,35 @@ def test_mxfp8_quantizer_workload():
     _check_mxfp8(x)
 
 
+def test_mxfp8_bench_size_sampled():
+    """The 65536 x 2048 input the benchmark times (about 36 tiles per CTA of
+    the persistent grid): row-wise codes and scales of 1024 sampled rows and
+    the column-wise codes and scales of 32 sampled 32-row blocks, all
+    columns, byte for byte against the oracle."""
+    ops = _ops()
+    M, K = 65536, 2048
+    x_dev = synth.normal_bf16(0, synth.TID_X, (M, K), "cuda")
+    o = ops.mxfp8_quantize(x_dev)
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(3)
+    rows = np.sort(np.concatenate([np.arange(128), rng.choice(M, 768, replace=False),
+                                   np.arange(M - 128, M)]))
+    rows = np.unique(rows)
+    xr = np_bf16(x_dev[torch.from_numpy(rows).cuda()])
+    rq, rs = Q.mxfp8_quantize_rowwise(xr)
+    assert_bytes_equal(u8(o["row_q"])[rows], rq, "row codes (sampled rows)")
+    got_rs = Q.unswizzle_scales(u8(o["row_s"]), M, K // 32)[rows]
+    assert_bytes_equal(got_rs, rs, "row scales (sampled rows)")
+    blocks = np.unique(np.concatenate([[0, M // 32 - 1], rng.choice(M // 32, 30, replace=False)]))
+    got_cq = u8(o["col_q"])
+    got_cs = Q.unswizzle_scales(u8(o["col_s"]), K, M // 32)
+    for b in blocks:
+        xb = np_bf16(x_dev[b * 32:(b + 1) * 32])
+        cq, cs = Q.mxfp8_quantize_colwise(xb)
+        assert_bytes_equal(got_cq[:, b * 32:(b + 1) * 32], cq, f"column codes, block {b}")
+        assert_bytes_equal(got_cs[:, b:b + 1], cs, f"column scales, block {b}")
+
+
 @pytest.mark.parametrize("M,K", [(1, 32), (33, 64), (40, 96), (200, 160), (257, 2048)])
 def test_mxfp8_shapes(M, K):
     x = synth.normal_bf16(5, 70 + K, (M, K), "cuda", std=3.0, outlier_p=0.02, outlier_mul=1e4)
