@@ -454,3 +454,55 @@ def test_mxfp8_bf16_backward_vs_autograd(mode):
     assert Mx.rel_l2(r["dx"], gx) < 6e-3
     if mode == "dequantized":
         assert not np.array_equal(r["w1_op"], w1)
+
+
+def test_gather_rows_invariants():
+    """The permute as properties of any correct gather, not its formula:
+    with one slot per token, gathering and then combining through the
+    inverse permutation returns every token row unchanged; with k slots,
+    every token's row appears in exactly k of the non-padding rows, each
+    routed slot's row is that token's, and padding rows are all zero."""
+    rng = np.random.default_rng(11)
+    T, E, H = 37, 6, 9
+    x = _bf16(rng.standard_normal((T, H)) * 4.0).astype(np.float64)
+    ids1, prob1 = _tiny_routing(T, E, 1, seed=5, skew=True)
+    seg, perm, inv, _ = MO.build_segments(ids1, prob1, E)
+    g = MO.gather_rows(x, perm, 1)
+    assert np.array_equal(MO.combine(g, inv, T, 1), x)
+    k = 4
+    ids, prob = _tiny_routing(T, E, k, seed=6)
+    seg, perm, inv, _ = MO.build_segments(ids, prob, E)
+    g = MO.gather_rows(x, perm, k)
+    pad = perm < 0
+    assert not np.any(g[pad])
+    for t in range(T):
+        hits = [r for r in range(len(perm)) if not pad[r] and np.array_equal(g[r], x[t])]
+        slots = [int(inv[t * k + j]) for j in range(k)]
+        assert sorted(slots) == sorted(r for r in hits if perm[r] // k == t)
+        assert len([r for r in hits if perm[r] // k == t]) == k
+
+
+def _grid_matrix(rng, rows, cols, scale):
+    """Values on the E2M1 grid times `scale`, each 16-element block holding a
+    +-6 (so every block's max, and the row's, is 6 * scale)."""
+    grid = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])
+    m = grid[rng.integers(0, 8, (rows, cols))] * rng.choice([-1.0, 1.0], (rows, cols))
+    m[:, ::16] = 6.0 * rng.choice([-1.0, 1.0], (rows, cols // 16))
+    return m * scale
+
+
+def test_single_expert_gemm_exact_on_representable_inputs():
+    """Inputs NVFP4 represents exactly (E2M1 grid values times 448 * 2^j with
+    a +-6 in every 16-block, so the outer scale is 2^j and every block scale
+    448) quantise without error, so the single-expert GEMM must equal the
+    plain fp64 product of the inputs, C = X [W_gate; W_up]^T, to the last
+    bit; a dropped scale, a transposed operand or a gate/up swap fails."""
+    rng = np.random.default_rng(12)
+    M, N, K = 24, 8, 64
+    x = _grid_matrix(rng, M, K, 448.0 * 2.0 ** -3)
+    wg = _grid_matrix(rng, N, K, 448.0 * 2.0 ** -9)
+    wu = _grid_matrix(rng, N, K, 448.0 * 2.0 ** -9)
+    r = MO.nvfp4_gemm_single(x, wg, wu)
+    assert np.array_equal(r["c"], x @ np.concatenate([wg, wu]).T)
+    assert np.all(r["tsx"] == np.float32(2.0 ** -3))
+    assert np.all(r["wq"][2] == np.float32(2.0 ** -9))
