@@ -76,27 +76,34 @@ struct SegCursor {
   long long lo = 0, hi = 0, end = -1;
 };
 
+// Expert offsets up to this many (E + 1) are copied to shared memory once
+// per CTA: at decode sizes a CTA's next task usually lies several experts
+// (many of them empty) further on, and walking the offsets in global memory
+// put a chain of dependent L2 reads in front of every task's first load.
+constexpr int SEG_SMEM = 1025;
+
 // task t -> chunk of 128 routed rows and weight tile; false past the last row
-MPM_DEV bool small_task(const GemmArgs& p, long long t, int n_wt, long long* r0, int* e, int* wt,
-                        int* bad, SegCursor& cur) {
+// (seg: the expert offsets, in shared or global memory; null for dense A)
+MPM_DEV bool small_task(const GemmArgs& p, const int* seg, long long t, int n_wt, long long* r0,
+                        int* e, int* wt, int* bad, SegCursor& cur) {
   const long long ci = t / n_wt;
   *wt = (int)(t - ci * n_wt);
   *r0 = ci * BR;
   if (cur.end < 0) {
-    cur.end = p.seg ? p.seg[p.E] : p.a_rows;
-    if (p.seg) {
+    cur.end = seg ? seg[p.E] : p.a_rows;
+    if (seg) {
       cur.e = 0;
-      cur.lo = p.seg[0];
-      cur.hi = p.seg[1];
+      cur.lo = seg[0];
+      cur.hi = seg[1];
     }
   }
   if (*r0 >= cur.end || *r0 >= p.a_rows) return false;
   int lo = 0;
-  if (p.seg) {
+  if (seg) {
     while (cur.e + 1 < p.E && cur.hi <= *r0) {
       ++cur.e;
       cur.lo = cur.hi;
-      cur.hi = p.seg[cur.e + 1];
+      cur.hi = seg[cur.e + 1];
     }
     lo = cur.e;
     if ((cur.lo & (BR - 1)) != 0 || (cur.hi & (BR - 1)) != 0) *bad = 1;
@@ -146,6 +153,11 @@ grouped_gemm_small_kernel(const __grid_constant__ SmallMaps maps, const GemmArgs
     tmem_alloc(sTmem, TMEM_COLS);
     tmem_relinquish();
   }
+  __shared__ int s_seg[SEG_SMEM];
+  const bool seg_smem = p.seg && p.E < SEG_SMEM;
+  if (seg_smem)
+    for (int i = threadIdx.x; i <= p.E; i += NTHREADS) s_seg[i] = p.seg[i];
+  const int* seg = seg_smem ? s_seg : p.seg;
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -160,7 +172,7 @@ grouped_gemm_small_kernel(const __grid_constant__ SmallMaps maps, const GemmArgs
     SegCursor cur;
     for (long long t = blockIdx.x; ok && t < n_tasks; t += gridDim.x) {
       long long r0; int e, wt;
-      if (!small_task(p, t, n_wt, &r0, &e, &wt, &bad, cur)) break;
+      if (!small_task(p, seg, t, n_wt, &r0, &e, &wt, &bad, cur)) break;
       const long long wrow0 = (long long)e * p.b_rows_per_e + (long long)wt * BW;
       const long long wrow1 = wrow0 + p.N / 2;                // up rows (SwiGLU)
       for (int kb = 0; kb < num_kb; ++kb, ++it) {
@@ -200,7 +212,7 @@ grouped_gemm_small_kernel(const __grid_constant__ SmallMaps maps, const GemmArgs
     SegCursor cur;
     for (long long t = blockIdx.x; ok && t < n_tasks; t += gridDim.x) {
       long long r0; int e, wt;
-      if (!small_task(p, t, n_wt, &r0, &e, &wt, &bad, cur)) break;
+      if (!small_task(p, seg, t, n_wt, &r0, &e, &wt, &bad, cur)) break;
       const uint32_t ab = (C::kNacc > 1) ? (j & 1u) : 0u;
       const uint32_t use = (C::kNacc > 1) ? (j >> 1) : j;
       if (!mbar_wait(bar_acc + 16 * ab + 8, (use & 1u) ^ 1u, p.status)) break;
@@ -251,7 +263,7 @@ grouped_gemm_small_kernel(const __grid_constant__ SmallMaps maps, const GemmArgs
     SegCursor cur;
     for (long long t = blockIdx.x; t < n_tasks; t += gridDim.x) {
       long long r0; int e, wt;
-      if (!small_task(p, t, n_wt, &r0, &e, &wt, &bad, cur)) break;
+      if (!small_task(p, seg, t, n_wt, &r0, &e, &wt, &bad, cur)) break;
       const uint32_t ab = (C::kNacc > 1) ? (j & 1u) : 0u;
       const uint32_t use = (C::kNacc > 1) ? (j >> 1) : j;
       const bool w_ok = mbar_wait(bar_acc + 16 * ab, use & 1u, p.status);
