@@ -31,7 +31,10 @@ namespace smallk {
 constexpr int BW = 128;               // weight rows per tile (MMA M)
 constexpr int BR = 128;               // routed rows per chunk (MMA N)
 constexpr int BKB = 128;              // bytes of K per stage
-constexpr int NTHREADS = 192;         // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
+constexpr int NTHREADS = 192;         // split K: warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
+// grouped kernel: warp 0 TMA, warp 1 MMA, warps 2-5 epilogue, warps 6-9 the
+// scale tiles into TMEM (one per lane quarter)
+constexpr int NTHREADS_G = 320;
 constexpr int TILE = 128 * BKB;       // 16 KB operand tile
 constexpr uint32_t TMEM_COLS = 512;
 
@@ -113,7 +116,7 @@ MPM_DEV bool small_task(const GemmArgs& p, const int* seg, long long t, int n_wt
 }
 
 template <int KIND, int EPI>
-__global__ void __launch_bounds__(NTHREADS, 1)
+__global__ void __launch_bounds__(NTHREADS_G, 1)
 grouped_gemm_small_kernel(const __grid_constant__ SmallMaps maps, const GemmArgs p, const int n_wt,
                           const long long n_tasks) {
   using C = Cfg<KIND, EPI>;
@@ -131,6 +134,7 @@ grouped_gemm_small_kernel(const __grid_constant__ SmallMaps maps, const GemmArgs
   const uint32_t bar_acc = sBar + 16 * S;                 // full at + 16 b, empty at + 16 b + 8
   const uint32_t sTmem = bar_acc + 32;
   const uint32_t sFlag = sTmem + 8;
+  const uint32_t bar_sf = sFlag + 8;                      // a stage's scale tiles are in TMEM
   volatile uint32_t* tmem_holder = reinterpret_cast<volatile uint32_t*>(gbase + (sTmem - base));
   volatile int* fail_flag = reinterpret_cast<volatile int*>(gbase + (sFlag - base));
 
@@ -138,6 +142,7 @@ grouped_gemm_small_kernel(const __grid_constant__ SmallMaps maps, const GemmArgs
     for (int s = 0; s < S; ++s) {
       mbar_init(bar_full + 8 * s, 1);
       mbar_init(bar_empty + 8 * s, 1);
+      mbar_init(bar_sf + 8 * s, 4);                       // one arrive per scale warp
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(bar_acc + 16 * b, 1);
@@ -156,7 +161,7 @@ grouped_gemm_small_kernel(const __grid_constant__ SmallMaps maps, const GemmArgs
   __shared__ int s_seg[SEG_SMEM];
   const bool seg_smem = p.seg && p.E < SEG_SMEM;
   if (seg_smem)
-    for (int i = threadIdx.x; i <= p.E; i += NTHREADS) s_seg[i] = p.seg[i];
+    for (int i = threadIdx.x; i <= p.E; i += NTHREADS_G) s_seg[i] = p.seg[i];
   const int* seg = seg_smem ? s_seg : p.seg;
   tc_fence_before();
   __syncthreads();
@@ -202,10 +207,11 @@ grouped_gemm_small_kernel(const __grid_constant__ SmallMaps maps, const GemmArgs
       }
     }
   } else if (warp == 1 && lane == 0) {
-    // ======================================================== scale copies + MMA issue
-    // (one thread: its tcgen05.cp and tcgen05.mma execute in issue order, so
-    // a stage's scale copies land before that stage's MMAs read them, and a
-    // TMEM scale slot is rewritten only after the MMAs that read it)
+    // ======================================================== MMA issue
+    // It waits for a stage's scale barrier only: the scale warps arrive on it
+    // after they have seen the stage's TMA loads land and written its scale
+    // tiles into TMEM.  A TMEM scale slot is rewritten only after the stage
+    // was refilled, i.e. after the MMAs that read it completed.
     uint32_t it = 0, j = 0;
     bool ok = true;
     const uint32_t idesc_base = idesc_block_scaled(KC::kFmt, BR, KC::kUe8m0, 0, 128);
@@ -221,19 +227,12 @@ grouped_gemm_small_kernel(const __grid_constant__ SmallMaps maps, const GemmArgs
       const uint32_t dacc = tmem + ab * C::kAccCols;
       for (int kb = 0; kb < num_kb; ++kb, ++it) {
         const int s = it % S;
-        if (!mbar_wait(bar_full + 8 * s, (it / S) & 1u, p.status)) { ok = false; break; }
+        if (!mbar_wait(bar_sf + 8 * s, (it / S) & 1u, p.status)) { ok = false; break; }
         tc_fence_after();
         const uint32_t st = sStage + s * C::kStage;
-        const uint32_t sf0 = st + (C::kWT + 1) * TILE;
-        const uint32_t sfcol = tmem + C::kSfBase + s * C::kSfCols;
         // TMEM scale columns of this stage: weight tile(s) then the row tile,
         // 4 columns per 512-byte scale tile
-#pragma unroll
-        for (int w = 0; w <= C::kWT; ++w)
-#pragma unroll
-          for (int a = 0; a < KC::kAtoms; ++a)
-            tc_cp_32x128b_x4(sfcol + (w * KC::kAtoms + a) * 4,
-                             sdesc_sf(sf0 + w * C::kSfBytes + a * 512));
+        const uint32_t sfcol = tmem + C::kSfBase + s * C::kSfCols;
         const uint32_t sfrow = sfcol + C::kWT * KC::kAtoms * 4;
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks) {
@@ -253,6 +252,38 @@ grouped_gemm_small_kernel(const __grid_constant__ SmallMaps maps, const GemmArgs
         }
         tc_commit(bar_empty + 8 * s);
         if (kb + 1 == num_kb) tc_commit(bar_acc + 16 * ab);
+      }
+    }
+  } else if (warp >= 6) {
+    // ======================================================== scale tiles, tcgen05.st
+    // Warp w writes TMEM lane quarter w % 4 (warps 6-9: quarters 2, 3, 0, 1):
+    // lane l of each 512-byte scale tile (its 16-byte row l) goes to lane
+    // 32 q + l, four columns — the replicated layout the block-scaled MMA
+    // reads, as a 32x128b.warpx4 copy would leave it.  As copies issued by
+    // the MMA thread these ran on the tensor pipe between the MMAs (decode
+    // FC2 0.301 against 0.231 ms with no copies at all).
+    const int q = warp & 3;
+    const uint32_t tq = tmem + ((uint32_t)(q * 32) << 16);
+    constexpr int NT = (C::kWT + 1) * KC::kAtoms;           // scale tiles per stage
+    uint32_t it = 0;
+    bool ok = true;
+    SegCursor cur;
+    for (long long t = blockIdx.x; ok && t < n_tasks; t += gridDim.x) {
+      long long r0; int e, wt;
+      if (!small_task(p, seg, t, n_wt, &r0, &e, &wt, &bad, cur)) break;
+      for (int kb = 0; kb < num_kb; ++kb, ++it) {
+        const int s = it % S;
+        if (!mbar_wait(bar_full + 8 * s, (it / S) & 1u, p.status)) { ok = false; break; }
+        tc_fence_after();
+        const uint8_t* sf = gbase + (sStage - base) + s * C::kStage + (C::kWT + 1) * TILE + lane * 16;
+        const uint32_t col = tq + C::kSfBase + s * C::kSfCols;
+#pragma unroll
+        for (int i = 0; i < NT; ++i)
+          tmem_st_32x32b_x4(col + i * 4, *reinterpret_cast<const uint4*>(sf + i * 512));
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_sf + 8 * s);
       }
     }
   } else if (warp >= 2) {
@@ -600,7 +631,7 @@ static cudaError_t launch_small_one(const smallk::SmallMaps& maps, const GemmArg
   long long grid = dev < 64 ? sms[dev] : 1;
   if (grid > n_tasks) grid = n_tasks;
   if (grid < 1) grid = 1;
-  kern<<<(unsigned)grid, smallk::NTHREADS, smem, s>>>(maps, a, n_wt, n_tasks);
+  kern<<<(unsigned)grid, smallk::NTHREADS_G, smem, s>>>(maps, a, n_wt, n_tasks);
   return cudaGetLastError();
 }
 
