@@ -64,7 +64,7 @@ typedef enum {
 /* Human-readable name of a status code (static string, never NULL). */
 const char* mpm_status_string(int status);
 
-/* Library version, e.g. 100 for 1.0.0. */
+/* Library version, e.g. 101 for 1.0.1 (101: mpm_grouped_gemm_desc.row_perm_dev). */
 int mpm_version(void);
 
 /* Bytes of a 128x4-tiled scale matrix: pad128(rows) * pad4(cols). */
@@ -546,6 +546,13 @@ typedef struct {
                                   e * b_k_per_expert and its columns at
                                   e * b_rows_per_expert; GROUP_K: the [rows, N]
                                   matrix (with a_mn_major)                    */
+  const int32_t* row_perm_dev; /* nullable; GROUP_M: the row map of the segment
+                                  build ([a_rows], -1 for a segment's padding
+                                  rows).  When given, padding rows are not part
+                                  of the result: their output rows may be left
+                                  unwritten (the small-M kernel's F32 / BF16
+                                  epilogues skip them; the combine never reads
+                                  them)                                       */
 } mpm_grouped_gemm_desc;
 
 mpm_status mpm_moe_grouped_gemm(const mpm_grouped_gemm_desc* desc, cudaStream_t stream);

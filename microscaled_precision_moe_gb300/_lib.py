@@ -44,6 +44,7 @@ class GroupedGemmDesc(C.Structure):
         ("aux_dev", _vp), ("ld_aux", _i64),
         ("amax_dev", _vp),
         ("a_mn_major", _int), ("b_mn_major", _int),
+        ("row_perm_dev", _vp),
     ]
 
 

@@ -166,7 +166,7 @@ const char* mpm_status_string(int s) {
   }
 }
 
-int mpm_version(void) { return 100; }
+int mpm_version(void) { return 101; }
 
 size_t mpm_scale_bytes(int64_t rows, int64_t cols) {
   if (rows <= 0 || cols <= 0) return 0;
@@ -505,6 +505,7 @@ mpm_status mpm_moe_grouped_gemm(const mpm_grouped_gemm_desc* d, cudaStream_t str
   a.out2 = d->out2_dev; a.ldo2 = d->ldo2;
   a.aux = d->aux_dev; a.ld_aux = d->ld_aux;
   a.amax = d->amax_dev;
+  a.row_perm = d->row_perm_dev;
   a.status = status_ptr();
 
   if (small) {

@@ -24,6 +24,7 @@ struct GemmArgs {
   void* out2; long long ldo2;
   const void* aux; long long ld_aux;
   float* amax;
+  const int* row_perm;        // nullable: rows with a negative entry are padding (small-M: not stored)
   int* status;
 };
 

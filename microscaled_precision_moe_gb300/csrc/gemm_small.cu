@@ -297,6 +297,21 @@ grouped_gemm_small_kernel(const __grid_constant__ SmallMaps maps, const GemmArgs
       if (!small_task(p, seg, t, n_wt, &r0, &e, &wt, &bad, cur)) break;
       const uint32_t ab = (C::kNacc > 1) ? (j & 1u) : 0u;
       const uint32_t use = (C::kNacc > 1) ? (j >> 1) : j;
+      // F32 / BF16: the 128 rows' scales and row map (lane = row within each
+      // 32-row block) loaded before the accumulator wait, so their latency
+      // is not part of the epilogue
+      float a_pre[4];
+      int m_pre[4];
+      if (!C::kDual) {
+        const float ab_pre = p.alpha_b ? p.alpha_b[e] : 1.0f;
+#pragma unroll
+        for (int cb = 0; cb < 4; ++cb) {
+          const long long rl = r0 + cb * 32 + lane;
+          const bool in = rl < p.a_rows;
+          a_pre[cb] = (p.alpha_a && in) ? __fmul_rn(p.alpha_a[rl], ab_pre) : ab_pre;
+          m_pre[cb] = (p.row_perm && in) ? p.row_perm[rl] : 0;
+        }
+      }
       const bool w_ok = mbar_wait(bar_acc + 16 * ab, use & 1u, p.status);
       ++j;
       if (!w_ok) *fail_flag = 1;
@@ -321,17 +336,32 @@ grouped_gemm_small_kernel(const __grid_constant__ SmallMaps maps, const GemmArgs
 #pragma unroll
         for (int cb = 0; cb < 4; ++cb) {
           const uint32_t* v = cb == 0 ? v0 : (cb == 1 ? v1 : (cb == 2 ? v2 : v3));
-          // the 32 rows' scales, one coalesced load, broadcast by shuffles
-          const float a_lane = p.alpha_a ? __fmul_rn(p.alpha_a[r0 + cb * 32 + lane], ab_e) : ab_e;
+          // the 32 rows' scales, one coalesced load, broadcast by shuffles;
+          // with a row map, a segment's padding rows are not stored (at
+          // decode sizes most rows of a 128-row chunk)
+          const float a_lane = a_pre[cb];
+          const unsigned keep = __ballot_sync(0xffffffffu, m_pre[cb] >= 0);
+          // the arithmetic runs for every row and only the store is
+          // predicated (a branch per row measured slower than storing all)
 #pragma unroll
           for (int c = 0; c < 32; ++c) {
             const long long row = r0 + cb * 32 + c;
             const float alpha = __shfl_sync(0xffffffffu, a_lane, c);
             const float val = __fmul_rn(__uint_as_float(v[c]), alpha);
-            if (EPI == MPM_EPI_F32)
-              static_cast<float*>(p.out)[row * p.ldo + f] = val;
-            else
-              static_cast<__nv_bfloat16*>(p.out)[row * p.ldo + f] = __float2bfloat16_rn(val);
+            const bool st = (keep >> c) & 1u;
+            if (EPI == MPM_EPI_F32) {
+              float* o = static_cast<float*>(p.out) + row * p.ldo + f;
+              asm volatile("{\n\t.reg .pred q;\n\tsetp.ne.u32 q, %2, 0;\n\t"
+                           "@q st.global.f32 [%0], %1;\n\t}"
+                           :: "l"(o), "f"(val), "r"((uint32_t)st) : "memory");
+            } else {
+              __nv_bfloat16* o = static_cast<__nv_bfloat16*>(p.out) + row * p.ldo + f;
+              const __nv_bfloat16 b = __float2bfloat16_rn(val);
+              asm volatile("{\n\t.reg .pred q;\n\tsetp.ne.u32 q, %2, 0;\n\t"
+                           "@q st.global.b16 [%0], %1;\n\t}"
+                           :: "l"(o), "h"(*reinterpret_cast<const uint16_t*>(&b)),
+                              "r"((uint32_t)st) : "memory");
+            }
           }
         }
       } else {

@@ -164,7 +164,9 @@ class NVFP4MoE:
         called right after range j = [t0, t1) is launched on the current
         stream, so a caller can record an event there and start copying
         those rows out while the later ranges are combined.  The result is
-        the same bytes: each token's combine is independent of the others."""
+        the same bytes: each token's combine is independent of the others.
+        self.y holds FC2's output for the routed rows; with the small-M
+        kernel a segment's padding rows of it are left unwritten."""
         T, H, I, E, k, cap = self.T, self.H, self.I, self.E, self.k, self.cap
         mark = mark or (lambda i: None)
         mark(0)
@@ -199,6 +201,7 @@ class NVFP4MoE:
             ops.moe_grouped_gemm(L.KIND_NVFP4, L.GROUP_M, L.EPI_BF16, E, cap, H, I, seg,
                                  dq, w.w2_q.view(E * H, I // 2), ds, I // 16, w.w2_s, I // 16,
                                  self.y, b_rows_per_expert=H, alpha_a=dts, alpha_b=w.w2_ts,
+                                 row_perm=perm,
                                  tile_m=self.tile_m)
         mark(5)
         dst = self.out if out is None else out

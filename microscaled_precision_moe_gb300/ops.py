@@ -357,13 +357,15 @@ def moe_combine(y_perm, inv_perm, T: int, k: int, out=None):
 def moe_grouped_gemm(kind, group, epilogue, E, a_rows, N, K, seg, a, b, sfa, sfa_cols, sfb,
                      sfb_cols, out, b_rows_per_expert=0, b_k_per_expert=0, alpha_a=None,
                      alpha_b=None, row_prob=None, out2=None, aux=None, amax=None, tile_m=128,
-                     a_mn_major=False, b_mn_major=False):
+                     a_mn_major=False, b_mn_major=False, row_perm=None):
     """One grouped block-scaled GEMM launch (see mpm_grouped_gemm_desc).
 
     a, b: uint8 code matrices [rows, pitch bytes] (bf16 matrices [rows, K]
     for KIND_BF16, sfa / sfb None; with a_mn_major / b_mn_major the bf16
     matrix is [K rows, M or N]); out / out2 / aux: row-major
-    tensors whose row strides become ldo / ldo2 / ld_aux.
+    tensors whose row strides become ldo / ldo2 / ld_aux.  row_perm: the
+    segment build's row map; padding rows' outputs may then be left
+    unwritten (small-M kernel).
     """
     lib = L.load()
     if kind == L.KIND_BF16:
@@ -394,7 +396,9 @@ def moe_grouped_gemm(kind, group, epilogue, E, a_rows, N, K, seg, a, b, sfa, sfa
             _check(t, name, torch.float32)
     if seg is not None:
         _check(seg, "seg_offsets", torch.int32, min_numel=E + 1)
-    _need_cuda(a, b, sfa, sfb, out, out2, aux, alpha_a, alpha_b, row_prob, amax, seg)
+    if row_perm is not None:
+        _check(row_perm, "row_perm", torch.int32, min_numel=a_rows)
+    _need_cuda(a, b, sfa, sfb, out, out2, aux, alpha_a, alpha_b, row_prob, amax, seg, row_perm)
     d = L.GroupedGemmDesc()
     d.kind, d.group, d.epilogue, d.tile_m = kind, group, epilogue, tile_m
     d.E, d.a_rows, d.N, d.K = E, a_rows, N, K
@@ -416,6 +420,7 @@ def moe_grouped_gemm(kind, group, epilogue, E, a_rows, N, K, seg, a, b, sfa, sfa
         d.aux_dev, d.ld_aux = aux.data_ptr(), aux.stride(-2)
     d.amax_dev = None if amax is None else amax.data_ptr()
     d.a_mn_major, d.b_mn_major = int(bool(a_mn_major)), int(bool(b_mn_major))
+    d.row_perm_dev = None if row_perm is None else row_perm.data_ptr()
     if group == L.GROUP_K:
         # the weight-gradient form has its own entry point
         st = lib.mpm_moe_grouped_gemm_wgrad(C.byref(d), _stream(a.device))

@@ -28,7 +28,7 @@ int main(void) {
   mpm_grouped_gemm_desc d;
 
   /* queries */
-  CHECK(mpm_version() == 100);
+  CHECK(mpm_version() == 101);
   CHECK(mpm_scale_bytes(8288, 64) == (size_t)8320 * 64);
   CHECK(mpm_scale_bytes(2048, 259) == (size_t)2048 * 260);
   CHECK(mpm_scale_bytes(0, 64) == 0);

@@ -34,7 +34,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_pure_host_queries(lib):
-    assert lib.mpm_version() == 100
+    assert lib.mpm_version() == 101
     assert lib.mpm_scale_bytes(8288, 64) == 8320 * 64
     assert lib.mpm_scale_bytes(2048, 259) == 2048 * 260
     assert lib.mpm_moe_row_capacity(32768, 8, 256, 128) == 262144 + 128 * 256
