@@ -246,6 +246,42 @@ def test_nvfp4_fc1_identical_across_kernels(shape):
         assert np.array_equal(a.view(np.uint32), ref_a.view(np.uint32)), f"tile_m {tile_m}: amax"
 
 
+@pytest.mark.parametrize("epi", ["bf16", "f32"])
+def test_small_m_row_map_leaves_padding_rows(epi):
+    """With the segment build's row map, the small-M kernel writes exactly
+    the routed rows: they are byte-identical to the same GEMM without the
+    map, and every padding row (row map < 0) keeps the sentinel the output
+    buffer held.  Few tokens over many experts, so most rows are padding."""
+    shape = synth.scaled(synth.MOE_30B, T=48, H=512, I=256, E=24, k=4)
+    ops, L = _ops(), _L()
+    ids, prob, x, w1, w2, seg, perm, inv, rp, cap = _grouped_nvfp4_setup(shape, seed=5, pad=128)
+    E, H, I = shape.E, shape.H, shape.I
+    dsrc = synth.normal_bf16(5, 78, (cap, I), "cuda", std=0.05)
+    qd, sd, tsd = ops.nvfp4_quantize_per_token(dsrc)
+    q2, s2, t2 = ops.nvfp4_quantize_weight([w2])
+    dt = torch.bfloat16 if epi == "bf16" else torch.float32
+    code = L.EPI_BF16 if epi == "bf16" else L.EPI_F32
+    outs = []
+    for row_perm in (None, perm):
+        y = torch.full((cap, H), -7.0, dtype=dt, device="cuda")
+        ops.moe_grouped_gemm(L.KIND_NVFP4, L.GROUP_M, code, E, cap, H, I, seg,
+                             qd, q2.view(E * H, I // 2), sd, I // 16, s2, I // 16, y,
+                             b_rows_per_expert=H, alpha_a=tsd, alpha_b=t2,
+                             tile_m=L.TILE_SMALL_M, row_perm=row_perm)
+        outs.append(y)
+    torch.cuda.synchronize()
+    assert ops.get_device_status() == 0
+    R = int(seg[-1].item())
+    real = torch.zeros(cap, dtype=torch.bool, device="cuda")
+    real[:R] = perm[:R] >= 0
+    pad = ~real
+    pad[R:] = False
+    assert int(pad.sum()) > R // 2, "the case should be mostly padding"
+    assert torch.equal(outs[1][real], outs[0][real]), "routed rows"
+    assert bool((outs[1][pad] == -7.0).all()), "padding rows written"
+    assert not bool((outs[0][pad] == -7.0).all()), "without the map every row is written"
+
+
 @pytest.mark.parametrize("tile_m", [128, 256, 1])
 def test_nvfp4_fc2_on_identical_operands(tile_m):
     """FC2 alone: the same seeded bf16 D quantised by both sides (byte-exact),
