@@ -75,7 +75,8 @@ def test_segments_bad_id_sets_device_status():
 
 
 @pytest.mark.parametrize("pad", [128, 256])
-@pytest.mark.parametrize("T,H,E,k,strided", [(700, 512, 12, 4, False), (300, 7168, 16, 8, True)])
+@pytest.mark.parametrize("T,H,E,k,strided", [(700, 512, 12, 4, False), (300, 7168, 16, 8, True),
+                                              (257, 1024, 9, 1, False), (130, 2048, 20, 6, True)])
 def test_nvfp4_quantize_scatter_equals_quantize_then_gather(T, H, E, k, strided, pad):
     """The fused quantiser writes the routed rows exactly as the per-token
     quantiser followed by the NVFP4 gather: every byte of the codes, tiled
