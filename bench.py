@@ -210,11 +210,21 @@ GEMM_SOURCES = ("gemm2.cu", "gemm.cuh", "common.cuh")
 
 
 def gemm_source_sha256() -> str:
-    """Hash of the pair-GEMM sources the DRAM counters belong to."""
+    """Hash of the pair-GEMM sources the DRAM counters belong to: their code
+    with comments and blank lines removed, so a change to a comment keeps the
+    record while any change to the code drops it."""
     import hashlib
+    import re
     csrc = os.path.join(ROOT, "microscaled_precision_moe_gb300", "csrc")
-    return hashlib.sha256(b"".join(open(os.path.join(csrc, f), "rb").read()
-                                   for f in GEMM_SOURCES)).hexdigest()
+    code = []
+    for f in GEMM_SOURCES:
+        text = open(os.path.join(csrc, f), encoding="utf-8").read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        for line in text.splitlines():
+            line = line.split("//", 1)[0].rstrip()
+            if line:
+                code.append(line)
+    return hashlib.sha256("\n".join(code).encode()).hexdigest()
 
 
 def _gemm_traffic(path=TRAFFIC_FILE):

@@ -73,11 +73,16 @@ MPM_DEV uint32_t float_bits(float f) { return __float_as_uint(f); }
 // hardware reciprocal (rcp.approx) of 1 + e^-g times g.  Both are a few fp32
 // ulps from the correctly rounded result; every other step is one IEEE
 // binary32 operation with no contraction into FMAs.  Both use their
-// flush-to-zero forms, which change no result here: the exponent's argument
-// is subnormal only for |g| below about 2^-126 (2^t is 1 either way), its
-// result only for g > 87 (where 1 + e^-g is 1 either way), and the
-// reciprocal's argument is at least 1 (its result flushes to 0 only for
-// g < -87, where the quotient underflows anyway and keeps the sign of g).
+// flush-to-zero forms.  For the exponential that changes no result: its
+// argument is subnormal only for |g| below about 2^-126 (2^t is 1 either
+// way), its result only for g > 87.3 (where 1 + e^-g is 1 either way).  The
+// reciprocal's argument is at least 1; for g < -87.3 (1 + e^-g above 2^126)
+// its result flushes to 0, so silu(g) comes out as a zero with the sign of g
+// where the exact value, |g| e^g, is below 2^-119 (and reaches 0 in fp32
+// only near g = -108): in a row that also holds ordinary gate values, such
+// an element of D lies more than 30 orders of magnitude below the row's
+// amax, and the FP4 re-quantisation codes it 0 either way.  The fast
+// division this replaced returns 0 in the same range.
 // Checked against CUDA's fast intrinsics (__expf, __fdividef), which this
 // replaced: D of the 671B-shaped headline layer byte for byte the same, and
 // that FC1 2.77 -> 2.70 ms (fewer epilogue instructions; see the last

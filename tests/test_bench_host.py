@@ -56,25 +56,29 @@ def test_clock_summary_without_samples():
 
 def test_gemm_traffic_only_while_the_sources_match(tmp_path, monkeypatch):
     """roofline.traffic comes from the committed counter record (a JSON data
-    file, not the markdown report) only while the GEMM sources hash to the
-    value recorded with it; an edited source, a malformed or a missing record
-    gives None."""
+    file, not the markdown report) only while the GEMM sources' code hashes to
+    the value recorded with it: an edited comment keeps the record, edited
+    code, a malformed or a missing record gives None."""
     import hashlib
     import json
     csrc = tmp_path / "microscaled_precision_moe_gb300" / "csrc"
     csrc.mkdir(parents=True)
-    for name, body in (("gemm2.cu", b"pair"), ("gemm.cuh", b"decl"), ("common.cuh", b"util")):
-        (csrc / name).write_bytes(body)
-    digest = hashlib.sha256(b"pair" + b"decl" + b"util").hexdigest()
+    for name, body in (("gemm2.cu", "pair();  // the pair kernel\n\n"),
+                       ("gemm.cuh", "/* declarations\n   of the args */\ndecl;\n"),
+                       ("common.cuh", "util();\n")):
+        (csrc / name).write_text(body)
+    digest = hashlib.sha256(b"pair();\ndecl;\nutil();").hexdigest()
     rec = tmp_path / "traffic.json"
     rec.write_text(json.dumps({"fc1_bytes_per_launch": 123456, "gemm_source_sha256": digest}))
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
     assert bench.gemm_source_sha256() == digest
     assert bench._gemm_traffic(str(rec)) == 123456
+    (csrc / "gemm2.cu").write_text("pair();  // the CTA-pair kernel, reworded\n")
+    assert bench._gemm_traffic(str(rec)) == 123456
     rec.write_text("{not json")
     assert bench._gemm_traffic(str(rec)) is None
     rec.write_text(json.dumps({"fc1_bytes_per_launch": 123456, "gemm_source_sha256": digest}))
-    (csrc / "gemm2.cu").write_bytes(b"pair, edited")
+    (csrc / "gemm2.cu").write_text("pair(1);\n")
     assert bench._gemm_traffic(str(rec)) is None
     rec.unlink()
     assert bench._gemm_traffic(str(rec)) is None

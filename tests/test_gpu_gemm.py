@@ -205,6 +205,63 @@ def test_nvfp4_grouped_fc1_swiglu_and_fc2(tile_m):
     _chained_compare(np_bf16(d), np_bf16(y), np_bf16(out), r, k, "NVFP4 layer")
 
 
+@pytest.mark.parametrize("tile_m", [128, 256, 1])
+def test_nvfp4_fc1_swiglu_extreme_gates(tile_m):
+    """The SwiGLU epilogue where e^-g overflows or underflows fp32 and where
+    g is tiny or exactly zero: tokens scaled by 1e-30, 1e-3, 1, 1e3 and 1e5
+    (gate values from about 1e-35 to 2e5 in magnitude) and all-zero tokens.
+    D stays finite, amax(D) is the row max of D, and D meets the oracle's
+    fp64 SwiGLU within one bf16 step per element (or the row's floor).  Where
+    g < -87.3 the helper's reciprocal of 1 + e^-g (above 2^126) flushes to
+    zero, so D there is a zero, while the exact value is a tiny nonzero
+    number (below 2^-119 |u| p); those elements are checked to be zero and
+    are left out of the count of differing elements."""
+    shape = synth.scaled(synth.MOE_30B, T=300, H=512, I=256, E=6, k=4)
+    ops, L = _ops(), _L()
+    ids, prob, x, w1, w2, seg, perm, inv, rp, cap = _grouped_nvfp4_setup(shape, seed=3,
+                                                                         pad=_pad(tile_m))
+    E, H, I, k = shape.E, shape.H, shape.I, shape.k
+    f = torch.tensor([1e-30, 1e-3, 1.0, 1e3, 1e5, 0.0], dtype=torch.float32)
+    scale = f[torch.arange(shape.T) % f.numel()].cuda()[:, None]
+    x = (x.float() * scale).to(torch.bfloat16).contiguous()
+    qx, sx, tsx = ops.nvfp4_quantize_per_token(x)
+    amax = torch.full((cap,), 7.0, dtype=torch.float32, device="cuda")
+    aq, as_, ats = ops.moe_gather_nvfp4(qx, sx, tsx, H, perm, seg, E, k, cap, amax_zero=amax)
+    q1, s1, t1 = ops.nvfp4_quantize_weight([w1[:, :I].contiguous(), w1[:, I:].contiguous()])
+    d = torch.empty(cap, I, dtype=torch.bfloat16, device="cuda")
+    ops.moe_grouped_gemm(L.KIND_NVFP4, L.GROUP_M, L.EPI_SWIGLU, E, cap, 2 * I, H, seg,
+                         aq, q1.view(E * 2 * I, H // 2), as_, H // 16, s1, H // 16, d,
+                         b_rows_per_expert=2 * I, alpha_a=ats, alpha_b=t1, row_prob=rp,
+                         out2=d, amax=amax, tile_m=tile_m)
+    torch.cuda.synchronize()
+    assert ops.get_device_status() == 0
+    with np.errstate(over="ignore"):
+        r = MO.nvfp4_moe_forward(np_bf16(x), ids.numpy(), prob.numpy(), np_bf16(w1),
+                                 np_bf16(w2), E, pad=_pad(tile_m))
+    R = int(r["seg"][-1])
+    g = r["acc1"][:R, :I]
+    real = np.asarray(r["perm"])[:R] >= 0
+    assert (np.abs(g[real]) > 88).any() and (np.abs(g[real][g[real] != 0]) < 1e-20).any(), \
+        "the inputs reach both ends of the exponential's range"
+    dk = np_bf16(d)[:R]
+    assert np.all(np.isfinite(dk)), "D finite"
+    assert np.array_equal(amax.cpu().numpy()[:R], np.max(np.abs(dk), axis=1)), "amax(D)"
+    ref = r["d"]
+    ulp = np.abs(ref) * 2.0 ** -7
+    # rows of one token share a scale; the floor is relative to that row's largest value
+    floor = 1e-4 * np.max(np.abs(ref), axis=1, keepdims=True)
+    assert np.all(np.abs(dk - ref) <= np.maximum(ulp, floor)), "D beyond one bf16 step"
+    flushed = g < -88.0
+    assert np.all(dk[flushed & real[:, None]] == 0), "D is zero where the reciprocal flushes"
+    assert np.all(np.abs(ref[flushed]) <= 2.0 ** -100 * np.abs(g[flushed]) *
+                  np.abs(r["acc1"][:R, I:][flushed]) + 0.0), "the exact value there is tiny"
+    ordinary = (np.abs(g) <= 87.0) & real[:, None]
+    diff = (dk != ref)[ordinary]
+    print(f"PARITY-STATS extreme gates tile_m {tile_m}: D elements differing {diff.mean():.3e} "
+          f"of {diff.size} with |g| <= 87; {int(flushed.sum())} with g < -88 flushed to zero")
+    assert diff.mean() < D_ELEM_DIFF, f"{diff.mean():.2e} of D elements differ"
+
+
 def _fc1_by_flat_row(shape, tile_m):
     """FC1 (NVFP4, SwiGLU x prob epilogue) with the given GEMM kernel; D and
     amax(D) returned in routed-row order (token-major, slot-minor), which does
