@@ -139,6 +139,9 @@ MPM_DEV void swiglu_fwd2(uint32_t acc_g0, uint32_t acc_g1, uint32_t acc_u0, uint
 }
 // dD -> (dg, du) for D = silu(g) * u * p with p constant:
 //   dg = (dD p) u s (1 + g (1 - s)),  du = (dD p) g s,  s = 1 / (1 + e^-g)
+// s is the forward's sigmoid, so for g < -87.3 it is 0 and dg, du are zeros
+// where their exact values lie below 2^-119 |dD p u| (1 + |g|) and
+// 2^-119 |dD p g|, as D is in the forward.
 MPM_DEV void swiglu_bwd(float g, float u, float dd, float prob, float& dg, float& du) {
   const float s = swiglu_sigmoid(g);
   const float dp = __fmul_rn(dd, prob);
